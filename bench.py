@@ -1,0 +1,511 @@
+#!/usr/bin/env python
+"""MLA verify benchmark: layer-calls/s and us/call at cache 8K, L = 1..16.
+
+Workload (DeepSeek-V3-like geometry): H=128 heads, latent r=512, nope n=128,
+value v=128, RoPE 64, bf16 with fp32 accumulation, one sequence of cache
+length T=8192, verify widths L in {1, 2, 4, 8, 16}, crossover dispatch ("auto",
+which picks the absorbed branch at every one of these widths).  One step is
+one verify call per width (5 layer-calls).  Each call uses its own layer's
+weights and cache; ten layers rotate (about 430 MB, larger than the 129 MB
+L2), so every call streams its operands from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  Under torchrun every rank runs the same
+replica (no data exchange); value is the calls of all ranks over the slowest
+rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WIDTHS = (1, 2, 4, 8, 16)
+CACHE_LEN = 8192
+NUM_LAYERS = 10
+METRIC = "MLA verify layer-calls/s (cache 8K, L=1..16)"
+UNIT = "calls/s"
+WORKLOAD = "dsv3-like B=1 T=8192 L=1,2,4,8,16 auto-dispatch (absorbed)"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work per kernel launch (bytes that must cross HBM, flops that
+# the method must do), for the roofline of the dominant kernel.
+# ---------------------------------------------------------------------------
+
+def _work(kernel: str, L: int, T: int, H=128, r=512, n=128, v=128, rope=64):
+    """(bytes, flops) one launch of `kernel` must move / do for one call at (L, T).
+
+    Bytes count what the kernel's role needs to cross HBM once, with bf16
+    intermediates (q_lat, o_lat) as the minimal hand-off between kernels; the
+    split-KV partials of an implementation are not counted.  Flops count the
+    contraction the kernel performs (2 per multiply-add)."""
+    bf = 2
+    rows = L * H
+    cache = T * (r + rope) * bf
+    fold = (H * n * r * bf + rows * n * bf + rows * r * bf, 2 * rows * n * r)
+    attend = (cache + rows * (r + rope) * bf + rows * r * bf,
+              2 * rows * T * (r + rope) + 2 * rows * T * r)
+    unembed = (H * r * v * bf + rows * r * bf + rows * v * bf, 2 * rows * r * v)
+    table = {
+        "generic_fold": fold,
+        "generic_absorbed_attention": attend,
+        "generic_combine_unembed": unembed,
+    }
+    return table.get(kernel)
+
+
+def _source_sha(names):
+    h = hashlib.sha256()
+    for nm in names:
+        p = os.path.join(ROOT, "mla_attention_speculative_gb300", "csrc", nm)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "generic_absorbed_attention": ["generic_kernels.cu"],
+    "generic_fold": ["generic_kernels.cu"],
+    "generic_combine_unembed": ["generic_kernels.cu"],
+}
+
+
+def _profile_traffic(kernel: str):
+    """dram bytes per launch from a committed ncu summary of this kernel, or None
+    if there is none or the kernel's source changed since it was taken."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    want_sha = _source_sha(KERNEL_SOURCES.get(kernel, []))
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.startswith(kernel + "__"):
+            continue
+        txt = open(os.path.join(pdir, fn)).read()
+        sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+        tb = re.search(r"dram_bytes_per_launch_full_workload:\s*([0-9.eE+]+)", txt)
+        if sha and tb and sha.group(1) == want_sha:
+            return float(tb.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ---------------------------------------------------------------------------
+# Inputs
+# ---------------------------------------------------------------------------
+
+def _layers(dev, num_layers):
+    import torch
+    from mla_attention_speculative_gb300.inputs import DSV3, make_case
+    layers = []
+    for i in range(num_layers):
+        c = make_case(DSV3, max(WIDTHS), [CACHE_LEN], dtype=torch.bfloat16, seed=1000 + i)
+        layers.append(c)
+    return layers
+
+
+def _cpu_oracle_step(case, heads):
+    """One step of the workload on the float64 oracle, restricted to `heads`."""
+    import oracle
+    f = lambda t: t.float().numpy()
+    qn, qr = f(case.q_nope), f(case.q_rope)
+    ckv, kr, wuk, wuv = f(case.c_kv), f(case.k_rope), f(case.W_UK), f(case.W_UV)
+    for L in WIDTHS:
+        oracle.absorbed(qn[:, :L], qr[:, :L], ckv, kr, wuk, wuv, [CACHE_LEN], heads=heads)
+
+
+def cpu_baseline(case, budget_s=12.0, heads_frac=4):
+    """Time the oracle as it stands on this host's cores on a bounded sample."""
+    H = case.geom.H
+    heads = list(range(0, H, heads_frac))
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _cpu_oracle_step(case, heads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 20:
+            break
+    calls = reps * len(WIDTHS) * len(heads) / H
+    return {"value": calls / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{reps} step(s) of 5 calls (L=1,2,4,8,16, T=8192) on {len(heads)} of "
+                      f"{H} heads, float64 numpy; value scaled to all heads ({el:.1f} s)"}
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    import torch
+    from mla_attention_speculative_gb300.inputs import DSV3, make_case
+    case = make_case(DSV3, max(WIDTHS), [CACHE_LEN], dtype=torch.bfloat16, seed=1000)
+    H = DSV3.H
+    heads = list(range(0, H, 16))     # bounded sample: 8 of 128 heads per step
+    for _ in range(args.warmup):
+        _cpu_oracle_step(case, heads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _cpu_oracle_step(case, heads)
+    el = time.perf_counter() - t0
+    calls = args.steps * len(WIDTHS) * len(heads) / H
+    value = calls / el
+    ms_per_step = el * 1e3 / args.steps * H / len(heads)
+    sample = (f"each step = 5 calls (L=1,2,4,8,16, T=8192) on {len(heads)} of {H} heads, "
+              "float64 numpy oracle; value scaled to all heads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "host CPU"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from mla_attention_speculative_gb300 import binding as B
+    from mla_attention_speculative_gb300 import build_lib
+    build_lib.build()
+    B.lib()
+
+    peaks = _peaks()
+    layers = _layers(dev, NUM_LAYERS)
+    geom = layers[0].geom
+    g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope, torch.bfloat16)
+
+    # device-resident inputs for every layer
+    D = []
+    for c in layers:
+        D.append({k: getattr(c, k).to(dev) for k in
+                  ("q_nope", "q_rope", "c_kv", "k_rope", "W_UK", "W_UV")})
+    lens = [CACHE_LEN]
+    lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
+    ws = {L: torch.empty(max(B.mla_workspace_bytes(g, L, lens, "auto"), 256),
+                         dtype=torch.uint8, device=dev) for L in WIDTHS}
+    outs = {L: torch.empty((1, L, geom.H, geom.v), dtype=torch.bfloat16, device=dev)
+            for L in WIDTHS}
+    q = [{L: (d["q_nope"][:, :L].contiguous(), d["q_rope"][:, :L].contiguous())
+          for L in WIDTHS} for d in D]
+    branches = {}
+
+    def call(li, L, stream=None):
+        d = D[li]
+        qn, qr = q[li][L]
+        _, br = B.mla_verify_attention(qn, qr, d["c_kv"], d["k_rope"], d["W_UK"], d["W_UV"],
+                                       lens, mode="auto", out=outs[L], workspace=ws[L],
+                                       cache_lens_dev=lens_dev, stream=stream)
+        branches[L] = br
+
+    # step s uses layers (5*(s%2) + i): two alternating halves of the ten layers
+    def step(s):
+        base = len(WIDTHS) * (s % 2)
+        for i, L in enumerate(WIDTHS):
+            call((base + i) % NUM_LAYERS, L)
+
+    # warm-up (eager), then capture one graph per half
+    for s in range(max(args.warmup, 3)):
+        step(s)
+    torch.cuda.synchronize()
+    graphs = []
+    cap_stream = torch.cuda.Stream(dev)
+    for half in range(2):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap_stream):
+            step(half)
+        graphs.append(gr)
+    for s in range(max(args.warmup, 3)):
+        graphs[s % 2].replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # ---- timed region: K graph-replayed steps --------------------------------
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(args.steps):
+        graphs[s % 2].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    total_calls = world * args.steps * len(WIDTHS)
+    value = total_calls / (ms / 1e3)
+    ms_per_step = ms / args.steps
+
+    # ---- per-kernel device time (events around each launch, eager steps) -----
+    B.mla_kernel_timing_read(reset=True)
+    B.mla_kernel_timing_enable(True)
+    for s in range(args.steps):
+        step(s)
+    torch.cuda.synchronize()
+    B.mla_kernel_timing_enable(False)
+    ktimes = B.mla_kernel_timing_read(reset=True)
+    launches_per_step = sum(n for n, _ in ktimes.values()) / args.steps
+    dominant = max(ktimes, key=lambda k: ktimes[k][1])
+    n_dom, ms_dom = ktimes[dominant]
+    # algorithmic work of the dominant kernel summed over its launches
+    bytes_sum = flops_sum = 0.0
+    for L in WIDTHS:
+        w = _work(dominant, L, CACHE_LEN)
+        if w is None:
+            continue
+        bytes_sum += w[0] * args.steps
+        flops_sum += w[1] * args.steps
+    dur_s = ms_dom / 1e3
+    t_b = bytes_sum / (peaks["hbm_gbs"] * 1e9)
+    t_f = flops_sum / (peaks["bf16_tflops"] * 1e12)
+    if t_b >= t_f:
+        roof = {"bound": "hbm", "achieved": bytes_sum / dur_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops_sum / dur_s / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    tr = _profile_traffic(dominant)
+    roof["traffic"] = tr
+    roof["kernel"] = dominant
+    roof["peak_source"] = f"of {peaks['source']}"
+    roof["avg_launch_us"] = ms_dom * 1e3 / max(n_dom, 1)
+
+    # ---- per-width us/call (graph of one call per layer, rotating) -----------
+    per_L = {}
+    for L in WIDTHS:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap_stream):
+            for li in range(NUM_LAYERS):
+                call(li, L)
+        gr.replay()
+        torch.cuda.synchronize()
+        reps = max(3, args.steps // 5)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        per_L[str(L)] = a.elapsed_time(b) * 1e3 / (reps * NUM_LAYERS)
+        del gr
+
+    # ---- end to end: host inputs -> device -> host result, per step ----------
+    e2e = _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(layers[0])
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD,
+                       "geometry": "H=128 r=512 n=128 v=128 rope=64",
+                       "branch": {str(L): B.BRANCH_NAMES[branches[L]] for L in WIDTHS},
+                       "l2": f"{NUM_LAYERS} rotating layer buffers "
+                             f"({_layer_bytes(geom) * NUM_LAYERS / 1e6:.0f} MB) > L2",
+                       "timing": "CUDA graph per step, CUDA events on the replay stream",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_call": ms_per_step * 1e3 / len(WIDTHS),
+            "per_width_us_per_call": per_L,
+            "roofline": roof,
+            "kernel_ms_per_step": {k: v[1] / args.steps for k, v in ktimes.items()},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _layer_bytes(geom):
+    return (geom.H * geom.n * geom.r + geom.H * geom.r * geom.v
+            + CACHE_LEN * (geom.r + geom.rope)) * 2
+
+
+def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
+    """Same step through the public call, with each step's new inputs (queries
+    and the L new latent rows per call) copied from pinned host memory and the
+    outputs read back to pinned host memory inside the timed region."""
+    import torch
+    host_q = {L: (q[0][L][0].cpu().pin_memory(), q[0][L][1].cpu().pin_memory())
+              for L in WIDTHS}
+    host_new = {L: (D[0]["c_kv"][:, CACHE_LEN - L:].cpu().pin_memory(),
+                    D[0]["k_rope"][:, CACHE_LEN - L:].cpu().pin_memory()) for L in WIDTHS}
+    host_out = {L: torch.empty(outs[L].shape, dtype=outs[L].dtype).pin_memory() for L in WIDTHS}
+    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size()
+              for a, b in list(host_q.values()) + list(host_new.values()))
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    dq = {L: (torch.empty_like(q[0][L][0]), torch.empty_like(q[0][L][1])) for L in WIDTHS}
+
+    def step(s):
+        base = len(WIDTHS) * (s % 2)
+        for i, L in enumerate(WIDTHS):
+            li = (base + i) % len(D)
+            d = D[li]
+            dq[L][0].copy_(host_q[L][0], non_blocking=True)
+            dq[L][1].copy_(host_q[L][1], non_blocking=True)
+            d["c_kv"][:, CACHE_LEN - L:].copy_(host_new[L][0], non_blocking=True)
+            d["k_rope"][:, CACHE_LEN - L:].copy_(host_new[L][1], non_blocking=True)
+            B.mla_verify_attention(dq[L][0], dq[L][1], d["c_kv"], d["k_rope"], d["W_UK"],
+                                   d["W_UV"], lens, mode="auto", out=outs[L], workspace=ws[L],
+                                   cache_lens_dev=lens_dev)
+            host_out[L].copy_(outs[L], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for s in range(3):
+        step(s)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(s)
+    el = time.perf_counter() - t0
+    barrier()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([el], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    return {"value": world * args.steps * len(WIDTHS) / el, "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

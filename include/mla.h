@@ -1,0 +1,184 @@
+/*
+ * mla.h -- C ABI of libmla.so: Multi-head Latent Attention (MLA) for
+ * speculative-decoding verify steps on GB300 (sm_103a).
+ *
+ * What is computed.  A verify call scores L >= 1 new query rows per sequence
+ * against a compressed latent KV cache (c_kv: r = kv_lora_rank values per
+ * cached position, plus a shared RoPE key k_rope of rope_dim values).  The
+ * pages ("One guard, 110x off the verify step", section "The defect") give two
+ * mathematically equivalent ways to do it, both implemented here:
+ *
+ *   absorbed      q_lat = q_nope . W_UK           (fold, n -> r, per head)
+ *                 s_t   = scale*(q_lat . c_kv[t] + q_rope . k_rope[t])
+ *                 o_lat = softmax(s) . c_kv        (accumulated in latent space)
+ *                 out   = o_lat . W_UV             (unembed, r -> v, per head)
+ *
+ *   materialised  K_nope[t] = c_kv[t] . W_UK^T,  V[t] = c_kv[t] . W_UV  (expand)
+ *                 out = softmax(scale*([q_nope||q_rope] . [K_nope[t]||k_rope[t]])) . V
+ *
+ * Row l of sequence b sits at position T_b - L + l and sees cached positions
+ * t <= T_b - L + l (causal among the verify rows); T_b is the cache length
+ * INCLUDING the L new rows.
+ *
+ * Branch choice ("The threshold is not a constant" and "The change" on the same
+ * page; the finite-cache form from the mlx-lm pull request "fix: Speed up
+ * multi-token decode by computing the absorbed MLA threshold", opening section):
+ * absorbed iff L <= floor(r*d*T / (r*d + (2r-d)*T)), d = n + v, evaluated in
+ * exact integer arithmetic, never below 1, and 1 when 2r - d <= 0.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns every buffer.  The library allocates no
+ *    device memory in these calls; scratch comes from the caller's workspace.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *    default stream).  Calls are asynchronous on it; inputs must stay alive
+ *    and unmodified until the stream reaches the call's kernels.
+ *  - Errors: argument errors return before anything is launched; a failed
+ *    launch returns MLA_ERR_CUDA.  mla_last_error() gives a one-line detail
+ *    for the calling thread's last failure.
+ *  - Layouts are row-major, element strides in elements (not bytes).
+ *  - Device pointers must be 16-byte aligned.
+ */
+#ifndef MLA_VERIFY_H_
+#define MLA_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,  /* a pointer, size or geometry is out of range   */
+  MLA_ERR_UNSUPPORTED = -2,  /* valid request this build has no kernel for     */
+  MLA_ERR_WORKSPACE = -3,    /* workspace smaller than mla_workspace_bytes()   */
+  MLA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed              */
+  MLA_ERR_TIMEOUT = -5       /* a bounded device wait ran out (status word)    */
+} mla_status_t;
+
+typedef enum {
+  MLA_MODE_AUTO = 0,          /* crossover threshold decides                   */
+  MLA_MODE_ABSORBED = 1,      /* force the absorbed branch                     */
+  MLA_MODE_MATERIALISED = 2   /* force the materialised branch                 */
+} mla_mode_t;
+
+typedef enum {
+  MLA_BRANCH_ABSORBED = 1,
+  MLA_BRANCH_MATERIALISED = 2
+} mla_branch_t;
+
+typedef enum {
+  MLA_DTYPE_BF16 = 0,   /* bf16 inputs/outputs, fp32 accumulation            */
+  MLA_DTYPE_FP32 = 1    /* fp32 inputs/outputs, fp32 arithmetic (CUDA cores) */
+} mla_dtype_t;
+
+/* Head geometry of one MLA layer.  softmax_scale <= 0 selects
+ * 1/sqrt(qk_nope_dim + rope_dim).  dtype is an mla_dtype_t. */
+typedef struct {
+  int32_t num_heads;      /* H                                   */
+  int32_t kv_lora_rank;   /* r (latent width)                    */
+  int32_t qk_nope_dim;    /* n (no-position query/key width)     */
+  int32_t v_dim;          /* v (value width)                     */
+  int32_t rope_dim;       /* rope (shared RoPE key width)        */
+  float softmax_scale;
+  int32_t dtype;
+} mla_geometry_t;
+
+/* Crossover of the pages' helper.  cache_len <= 0 asks for the long-cache
+ * limit floor(r(n+v)/(2r-n-v)) ("The threshold is not a constant", table:
+ * 170 for 512/128/128, 398 for 512/192/256, 512 for 512/256/256); cache_len
+ * > 0 gives floor(r*d*T / (r*d + (2r-d)*T)) (pull request opening section; 379
+ * for 512/192/256 at T = 8192).  Never below 1; 1 when 2r - d <= 0.  Returns
+ * -1 if r, n or v is not positive.  Pure host code, no CUDA. */
+int64_t mla_max_absorbed_queries(int32_t r, int32_t n, int32_t v, int64_t cache_len);
+
+/* One decision for a batch of sequences: the summed cost model,
+ * floor(r*d*S / (B*r*d + (2r-d)*S)) with S = sum of cache_lens_host[0..batch);
+ * equal to mla_max_absorbed_queries for batch == 1.  Returns -1 on bad
+ * arguments (NULL lengths, batch < 1, a length < 1). */
+int64_t mla_max_absorbed_queries_batch(int32_t r, int32_t n, int32_t v,
+                                       const int32_t* cache_lens_host, int32_t batch);
+
+/* Branch a call would take ("The change": guard L <= max_absorbed); forced
+ * modes override.  Writes an mla_branch_t to *branch.  Host only. */
+mla_status_t mla_select_branch(const mla_geometry_t* geom, int32_t L,
+                               const int32_t* cache_lens_host, int32_t batch,
+                               int32_t mode, int32_t* branch);
+
+/* Bytes of device workspace mla_verify_attention needs for this call
+ * (branch-dependent: split-KV partials for the absorbed branch, the expanded
+ * K_nope/V buffer for the materialised branch).  Host only. */
+mla_status_t mla_workspace_bytes(const mla_geometry_t* geom, int32_t batch, int32_t L,
+                                 const int32_t* cache_lens_host, int32_t mode,
+                                 size_t* bytes);
+
+/* One verify attention call for `batch` sequences of L rows each.
+ *
+ *  q_nope  device [batch, L, H, n]      query, no-position part
+ *  q_rope  device [batch, L, H, rope]   query RoPE part (RoPE already applied)
+ *  c_kv    device latent cache, rows of r values:
+ *            contiguous (page_table == NULL): row (b, t) at
+ *              c_kv + (b*seq_stride_rows + t) * c_kv_row_stride
+ *            paged: row (b, t) at
+ *              c_kv + (page_table[b*max_pages_per_seq + t/page_size]*page_size
+ *                      + t%page_size) * c_kv_row_stride
+ *  k_rope  device RoPE key cache, same addressing with k_rope_row_stride
+ *          (a packed [.., r+rope] cache may pass k_rope = c_kv + r and both
+ *          strides = r + rope)
+ *  W_UK    device [H, n, r]   key up-projection
+ *  W_UV    device [H, r, v]   value up-projection
+ *  cache_lens_dev / cache_lens_host  [batch] int32, T_b with L <= T_b; the
+ *          device copy is read by the kernels, the host copy for dispatch and
+ *          launch sizing (they must agree)
+ *  page_table  device [batch, max_pages_per_seq] int32 page ids in
+ *          [0, num_pages), or NULL for a contiguous cache
+ *  out     device [batch, L, H, v] in the geometry's dtype
+ *  workspace / workspace_bytes  device scratch of at least
+ *          mla_workspace_bytes() bytes (may be NULL when that is 0)
+ *  branch_taken  host, may be NULL; receives the mla_branch_t used
+ */
+mla_status_t mla_verify_attention(
+    const mla_geometry_t* geom,
+    const void* q_nope, const void* q_rope,
+    const void* c_kv, const void* k_rope,
+    int64_t c_kv_row_stride, int64_t k_rope_row_stride, int64_t seq_stride_rows,
+    const void* W_UK, const void* W_UV,
+    const int32_t* cache_lens_dev, const int32_t* cache_lens_host,
+    int32_t batch, int32_t L,
+    const int32_t* page_table, int32_t page_size, int32_t max_pages_per_seq,
+    int32_t num_pages,
+    int32_t mode, void* out, void* workspace, size_t workspace_bytes,
+    void* stream, int32_t* branch_taken);
+
+/* Per-kernel timing, for benchmarks.  While enabled, every kernel launch the
+ * library makes is bracketed by a pair of CUDA events recorded on the call's
+ * stream (events come from a library-owned pool; no device memory).  Do not
+ * enable it while a stream is being captured into a CUDA graph.  Not part of
+ * the method: instrumentation only. */
+mla_status_t mla_kernel_timing_enable(int32_t on);
+
+/* Waits for every recorded event pair, folds them into per-kernel totals and
+ * reports them: names receives the kernel names separated by ';' (truncated
+ * to names_len bytes including the terminator), launches[i] and total_ms[i]
+ * the launch count and summed device milliseconds of kernel i, for up to
+ * max_kernels kernels; *n_kernels receives how many kernels have totals.
+ * With reset != 0 the totals are cleared after reading. */
+mla_status_t mla_kernel_timing_read(char* names, size_t names_len, int32_t* launches,
+                                    double* total_ms, int32_t max_kernels,
+                                    int32_t* n_kernels, int32_t reset);
+
+/* Static name of a status code. */
+const char* mla_status_string(int32_t status);
+
+/* One-line detail of the calling thread's last failed call ("" if none). */
+const char* mla_last_error(void);
+
+/* Library ABI version (major*100 + minor). */
+int32_t mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_VERIFY_H_ */

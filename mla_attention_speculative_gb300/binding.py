@@ -1,0 +1,218 @@
+"""Thin ctypes binding of libmla.so (argument marshalling only).
+
+Every function here has the C entry point's name and forwards to it.  The
+tensors are PyTorch CUDA tensors: PyTorch provides device memory and the
+current stream, nothing else.  Every step of the attention runs in the
+library's kernels; if the library is missing this module raises instead of
+falling back to anything.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla.so")
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARG = -1
+MLA_ERR_UNSUPPORTED = -2
+MLA_ERR_WORKSPACE = -3
+MLA_ERR_CUDA = -4
+MLA_ERR_TIMEOUT = -5
+
+MODES = {"auto": 0, "absorbed": 1, "materialised": 2}
+BRANCH_ABSORBED = 1
+BRANCH_MATERIALISED = 2
+BRANCH_NAMES = {1: "absorbed", 2: "materialised"}
+DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({detail})")
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int32), ("kv_lora_rank", ctypes.c_int32),
+                ("qk_nope_dim", ctypes.c_int32), ("v_dim", ctypes.c_int32),
+                ("rope_dim", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SIGS = {
+    "mla_max_absorbed_queries": (_I64, [_I32, _I32, _I32, _I64]),
+    "mla_max_absorbed_queries_batch": (_I64, [_I32, _I32, _I32, _P, _I32]),
+    "mla_select_branch": (_I32, [_P, _I32, _P, _I32, _I32, _P]),
+    "mla_workspace_bytes": (_I32, [_P, _I32, _I32, _P, _I32, _P]),
+    "mla_verify_attention": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P,
+                                    _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _P,
+                                    ctypes.c_size_t, _P, _P]),
+    "mla_kernel_timing_enable": (_I32, [_I32]),
+    "mla_kernel_timing_read": (_I32, [ctypes.c_char_p, ctypes.c_size_t, _P, _P, _I32, _P,
+                                      _I32]),
+    "mla_status_string": (ctypes.c_char_p, [_I32]),
+    "mla_last_error": (ctypes.c_char_p, []),
+    "mla_version": (_I32, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmla.so (built in-tree by build_lib); raise if it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run "
+                               "`python -m mla_attention_speculative_gb300.build_lib`")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mla_status_string(int(status)).decode()
+
+
+def mla_last_error() -> str:
+    return lib().mla_last_error().decode()
+
+
+def _check(status: int, where: str):
+    if status != MLA_OK:
+        raise MlaError(status, where, mla_last_error())
+
+
+def _lens_array(cache_lens: Sequence[int]):
+    arr = (ctypes.c_int32 * len(cache_lens))(*[int(t) for t in cache_lens])
+    return arr
+
+
+def make_geometry(H, r, n, v, rope, dtype=torch.bfloat16, scale: Optional[float] = None):
+    return Geometry(int(H), int(r), int(n), int(v), int(rope),
+                    float(scale) if scale is not None else 0.0, DTYPES[dtype])
+
+
+def mla_max_absorbed_queries(r: int, n: int, v: int, cache_len: int = 0) -> int:
+    return int(lib().mla_max_absorbed_queries(r, n, v, cache_len))
+
+
+def mla_max_absorbed_queries_batch(r: int, n: int, v: int, cache_lens: Sequence[int]) -> int:
+    arr = _lens_array(cache_lens)
+    return int(lib().mla_max_absorbed_queries_batch(r, n, v, arr, len(cache_lens)))
+
+
+def mla_select_branch(geom: Geometry, L: int, cache_lens: Sequence[int], mode="auto") -> int:
+    arr = _lens_array(cache_lens)
+    out = ctypes.c_int32(0)
+    _check(lib().mla_select_branch(ctypes.byref(geom), L, arr, len(cache_lens),
+                                   MODES.get(mode, mode), ctypes.byref(out)),
+           "mla_select_branch")
+    return out.value
+
+
+def mla_workspace_bytes(geom: Geometry, L: int, cache_lens: Sequence[int], mode="auto") -> int:
+    arr = _lens_array(cache_lens)
+    out = ctypes.c_size_t(0)
+    _check(lib().mla_workspace_bytes(ctypes.byref(geom), len(cache_lens), L, arr,
+                                     MODES.get(mode, mode), ctypes.byref(out)),
+           "mla_workspace_bytes")
+    return out.value
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def cache_strides(c_kv: torch.Tensor, k_rope: torch.Tensor, paged: bool):
+    """(c_kv row stride, k_rope row stride, rows between sequences) in elements."""
+    if c_kv.stride(-1) != 1 or k_rope.stride(-1) != 1:
+        raise ValueError("cache rows must be contiguous in their last dimension")
+    cs, ks = c_kv.stride(1), k_rope.stride(1)
+    if paged:
+        if c_kv.stride(0) != c_kv.shape[1] * cs or k_rope.stride(0) != k_rope.shape[1] * ks:
+            raise ValueError("paged cache pages must be contiguous runs of rows")
+        return cs, ks, 0
+    if c_kv.stride(0) % cs or k_rope.stride(0) % ks or \
+            c_kv.stride(0) // cs != k_rope.stride(0) // ks:
+        raise ValueError("c_kv and k_rope must have the same rows per sequence")
+    return cs, ks, c_kv.stride(0) // cs
+
+
+def mla_verify_attention(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv: torch.Tensor,
+                         k_rope: torch.Tensor, W_UK: torch.Tensor, W_UV: torch.Tensor,
+                         cache_lens: Sequence[int], mode="auto",
+                         out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         page_table: Optional[torch.Tensor] = None,
+                         cache_lens_dev: Optional[torch.Tensor] = None,
+                         scale: Optional[float] = None, stream=None):
+    """One verify call through the C ABI.  Returns (out, branch).
+
+    q_nope [B,L,H,n], q_rope [B,L,H,rope], W_UK [H,n,r], W_UV [H,r,v]; the
+    cache is c_kv [B,Tmax,r] / k_rope [B,Tmax,rope] (contiguous) or
+    [num_pages,page,r] / [num_pages,page,rope] with ``page_table`` [B,max_pages].
+    ``out`` and ``workspace`` are allocated with torch when not given.
+    """
+    B, L, H, n = q_nope.shape
+    rope = q_rope.shape[-1]
+    r = W_UK.shape[-1]
+    v = W_UV.shape[-1]
+    dev = q_nope.device
+    geom = make_geometry(H, r, n, v, rope, q_nope.dtype, scale)
+    lens = [int(t) for t in cache_lens]
+    arr = _lens_array(lens)
+    paged = page_table is not None
+    cs, ks, seq = cache_strides(c_kv, k_rope, paged)
+    if cache_lens_dev is None:
+        cache_lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty((B, L, H, v), dtype=q_nope.dtype, device=dev)
+    m = MODES.get(mode, mode)
+    need = mla_workspace_bytes(geom, L, lens, m)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    page_size = c_kv.shape[1] if paged else 0
+    max_pages = page_table.shape[1] if paged else 0
+    num_pages = c_kv.shape[0] if paged else 0
+    branch = ctypes.c_int32(0)
+    st = lib().mla_verify_attention(
+        ctypes.byref(geom), _ptr(q_nope), _ptr(q_rope), _ptr(c_kv), _ptr(k_rope), cs, ks, seq,
+        _ptr(W_UK), _ptr(W_UV), _ptr(cache_lens_dev), arr, B, L, _ptr(page_table), page_size,
+        max_pages, num_pages, m, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), stream, ctypes.byref(branch))
+    _check(st, "mla_verify_attention")
+    return out, branch.value
+
+
+def mla_kernel_timing_enable(on: bool = True) -> None:
+    """Bracket every library kernel launch with CUDA events (benchmark instrumentation)."""
+    _check(lib().mla_kernel_timing_enable(1 if on else 0), "mla_kernel_timing_enable")
+
+
+def mla_kernel_timing_read(reset: bool = True) -> dict:
+    """{kernel name: (launches, total device ms)} since the last reset (waits for events)."""
+    cap = 64
+    names = ctypes.create_string_buffer(4096)
+    launches = (ctypes.c_int32 * cap)()
+    ms = (ctypes.c_double * cap)()
+    n = ctypes.c_int32(0)
+    _check(lib().mla_kernel_timing_read(names, 4096, launches, ms, cap, ctypes.byref(n),
+                                        1 if reset else 0), "mla_kernel_timing_read")
+    keys = names.value.decode().split(";") if n.value else []
+    return {k: (int(launches[i]), float(ms[i])) for i, k in enumerate(keys[:cap])}

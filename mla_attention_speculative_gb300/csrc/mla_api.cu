@@ -1,0 +1,324 @@
+// C ABI of libmla.so: argument validation, the crossover dispatcher, the
+// workspace plan and the launch of the kernels of the chosen branch.
+//
+// Crossover: "One guard, 110x off the verify step" (sections "The threshold is
+// not a constant" and "The change") and the mlx-lm pull request "fix: Speed up
+// multi-token decode by computing the absorbed MLA threshold" (opening section
+// for the finite-cache form, reviewer comment for exact integer arithmetic).
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+// ---------------------------------------------------------------------------
+// Crossover threshold, exact integer arithmetic
+// ---------------------------------------------------------------------------
+
+// floor(num / den) for num >= 0, den > 0.
+static int64_t floor_div(__int128 num, __int128 den) { return (int64_t)(num / den); }
+
+// Per-head costs ("The threshold is not a constant"): absorbed
+// 2*L*T*r + L*r*d, materialised T*r*d + L*T*d.  Summed over a batch and
+// solved for L: L <= r*d*S / (B*r*d + (2r-d)*S), S = sum of T.  B == 1 is
+// the pull request's finite-cache formula; S -> infinity is the helper's
+// r*d/(2r-d).  The helper's guards: a non-positive 2r-d gives 1, and the
+// answer is never below 1.
+static int64_t threshold_sum(int64_t r, int64_t n, int64_t v, int64_t batch, __int128 sumT,
+                             bool limit) {
+  const int64_t d = n + v;
+  const int64_t denom_lim = 2 * r - d;
+  if (denom_lim <= 0) return 1;
+  int64_t x;
+  if (limit) {
+    x = floor_div((__int128)r * d, denom_lim);
+  } else {
+    const __int128 num = (__int128)r * d * sumT;
+    const __int128 den = (__int128)batch * r * d + (__int128)denom_lim * sumT;
+    x = floor_div(num, den);
+  }
+  return x < 1 ? 1 : x;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int64_t mla_max_absorbed_queries(int32_t r, int32_t n, int32_t v, int64_t cache_len) {
+  if (r <= 0 || n <= 0 || v <= 0) return -1;
+  return threshold_sum(r, n, v, 1, cache_len > 0 ? (__int128)cache_len : 0, cache_len <= 0);
+}
+
+extern "C" int64_t mla_max_absorbed_queries_batch(int32_t r, int32_t n, int32_t v,
+                                                  const int32_t* lens, int32_t batch) {
+  if (r <= 0 || n <= 0 || v <= 0 || lens == nullptr || batch < 1) return -1;
+  __int128 s = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    if (lens[b] < 1) return -1;
+    s += lens[b];
+  }
+  return threshold_sum(r, n, v, batch, s, false);
+}
+
+namespace mla {
+
+// ---------------------------------------------------------------------------
+// Validation and planning
+// ---------------------------------------------------------------------------
+
+static bool geometry_ok(const mla_geometry_t* g) {
+  if (g == nullptr) { set_error("geometry is NULL"); return false; }
+  if (g->num_heads < 1 || g->kv_lora_rank < 1 || g->qk_nope_dim < 1 || g->v_dim < 1 ||
+      g->rope_dim < 0) {
+    set_error("geometry has a non-positive dimension (H=%d r=%d n=%d v=%d rope=%d)",
+              g->num_heads, g->kv_lora_rank, g->qk_nope_dim, g->v_dim, g->rope_dim);
+    return false;
+  }
+  if (g->dtype != MLA_DTYPE_BF16 && g->dtype != MLA_DTYPE_FP32) {
+    set_error("unknown dtype %d", g->dtype);
+    return false;
+  }
+  // every row of every operand is a whole number of 16-byte vectors
+  const int eb = g->dtype == MLA_DTYPE_BF16 ? 2 : 4;
+  const int dims[4] = {g->kv_lora_rank, g->qk_nope_dim, g->v_dim, g->rope_dim};
+  for (int i = 0; i < 4; ++i) {
+    if ((dims[i] * eb) % 16 != 0) {
+      set_error("dimension %d is not a multiple of %d elements", dims[i], 16 / eb);
+      return false;
+    }
+  }
+  if (g->kv_lora_rank > 1024 || g->qk_nope_dim > 512 || g->v_dim > 512 || g->rope_dim > 128) {
+    set_error("geometry beyond supported maxima (r<=1024, n<=512, v<=512, rope<=128)");
+    return false;
+  }
+  return true;
+}
+
+static bool lens_ok(const int32_t* lens, int32_t batch, int32_t L) {
+  if (batch < 1) { set_error("batch %d < 1", batch); return false; }
+  if (L < 1) { set_error("L %d < 1", L); return false; }
+  if (lens == nullptr) { set_error("cache_lens_host is NULL"); return false; }
+  for (int32_t b = 0; b < batch; ++b) {
+    if (lens[b] < L) {
+      set_error("cache_lens[%d] = %d is smaller than L = %d (T includes the new rows)", b,
+                lens[b], L);
+      return false;
+    }
+  }
+  return true;
+}
+
+static constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs
+static constexpr int kGenericRowsPerCTA = 4; // one warp per query row
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static int choose_branch(const mla_geometry_t* g, int32_t L, const int32_t* lens, int32_t batch,
+                         int32_t mode) {
+  if (mode == MLA_MODE_ABSORBED) return MLA_BRANCH_ABSORBED;
+  if (mode == MLA_MODE_MATERIALISED) return MLA_BRANCH_MATERIALISED;
+  const int64_t thr =
+      mla_max_absorbed_queries_batch(g->kv_lora_rank, g->qk_nope_dim, g->v_dim, lens, batch);
+  return L <= thr ? MLA_BRANCH_ABSORBED : MLA_BRANCH_MATERIALISED;
+}
+
+static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
+                              const int32_t* lens, int32_t mode, Plan* p) {
+  if (!geometry_ok(g) || !lens_ok(lens, batch, L)) return MLA_ERR_INVALID_ARG;
+  if (mode != MLA_MODE_AUTO && mode != MLA_MODE_ABSORBED && mode != MLA_MODE_MATERIALISED) {
+    set_error("unknown mode %d", mode);
+    return MLA_ERR_INVALID_ARG;
+  }
+  p->B = batch;
+  p->L = L;
+  p->H = g->num_heads;
+  p->r = g->kv_lora_rank;
+  p->n = g->qk_nope_dim;
+  p->v = g->v_dim;
+  p->rope = g->rope_dim;
+  p->dtype = g->dtype;
+  p->scale = g->softmax_scale > 0.f ? g->softmax_scale
+                                    : (float)(1.0 / std::sqrt((double)(p->n + p->rope)));
+  p->branch = choose_branch(g, L, lens, batch, mode);
+  p->Tmax = 0;
+  p->sumT = 0;
+  for (int b = 0; b < batch; ++b) {
+    p->Tmax = lens[b] > p->Tmax ? lens[b] : p->Tmax;
+    p->sumT += lens[b];
+  }
+  p->fast = false;
+
+  // Split-KV: enough CTAs (one per 4 query rows per piece) to cover the GPU a
+  // few times over, pieces a multiple of 64 rows.
+  const int64_t rows = (int64_t)L * p->H;
+  const int64_t row_ctas = (int64_t)batch * ((rows + kGenericRowsPerCTA - 1) / kGenericRowsPerCTA);
+  const int64_t want = 4 * kNumSMs;
+  int64_t splits = (want + row_ctas - 1) / row_ctas;
+  const int64_t max_splits = (p->Tmax + 63) / 64;
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 1) splits = 1;
+  int64_t chunk = (p->Tmax + splits - 1) / splits;
+  chunk = (chunk + 63) / 64 * 64;
+  p->chunk = (int)chunk;
+  p->splits = (int)((p->Tmax + chunk - 1) / chunk);
+
+  const size_t eb = p->dtype == MLA_DTYPE_BF16 ? 2 : 4;
+  const int dv = p->branch == MLA_BRANCH_ABSORBED ? p->r : p->v;
+  const size_t nrow = (size_t)batch * rows;
+  size_t off = 0;
+  p->off_qlat = p->off_exp = p->off_olat = 0;
+  if (p->branch == MLA_BRANCH_ABSORBED) {
+    p->off_qlat = off;
+    off = align256(off + nrow * p->r * sizeof(float));
+  } else {
+    p->off_exp = off;
+    off = align256(off + (size_t)batch * p->Tmax * p->H * (p->n + p->v) * eb);
+  }
+  p->off_opart = off;
+  off = align256(off + nrow * p->splits * dv * sizeof(float));
+  p->off_ml = off;
+  off = align256(off + nrow * p->splits * 2 * sizeof(float));
+  p->ws_bytes = off;
+  return MLA_OK;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace mla
+
+extern "C" mla_status_t mla_select_branch(const mla_geometry_t* g, int32_t L,
+                                          const int32_t* lens, int32_t batch, int32_t mode,
+                                          int32_t* branch) {
+  if (branch == nullptr) { set_error("branch output is NULL"); return MLA_ERR_INVALID_ARG; }
+  Plan p;
+  const mla_status_t st = make_plan(g, batch, L, lens, mode, &p);
+  if (st != MLA_OK) return st;
+  *branch = p.branch;
+  return MLA_OK;
+}
+
+extern "C" mla_status_t mla_workspace_bytes(const mla_geometry_t* g, int32_t batch, int32_t L,
+                                            const int32_t* lens, int32_t mode, size_t* bytes) {
+  if (bytes == nullptr) { set_error("bytes output is NULL"); return MLA_ERR_INVALID_ARG; }
+  Plan p;
+  const mla_status_t st = make_plan(g, batch, L, lens, mode, &p);
+  if (st != MLA_OK) return st;
+  *bytes = p.ws_bytes;
+  return MLA_OK;
+}
+
+extern "C" mla_status_t mla_verify_attention(
+    const mla_geometry_t* g, const void* q_nope, const void* q_rope, const void* c_kv,
+    const void* k_rope, int64_t c_kv_row_stride, int64_t k_rope_row_stride,
+    int64_t seq_stride_rows, const void* W_UK, const void* W_UV, const int32_t* lens_dev,
+    const int32_t* lens_host, int32_t batch, int32_t L, const int32_t* page_table,
+    int32_t page_size, int32_t max_pages_per_seq, int32_t num_pages, int32_t mode, void* out,
+    void* workspace, size_t workspace_bytes, void* stream, int32_t* branch_taken) {
+  Plan p;
+  mla_status_t st = make_plan(g, batch, L, lens_host, mode, &p);
+  if (st != MLA_OK) return st;
+
+  const void* ptrs[] = {q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, lens_dev, out};
+  const char* names[] = {"q_nope", "q_rope", "c_kv", "k_rope", "W_UK", "W_UV",
+                         "cache_lens_dev", "out"};
+  for (int i = 0; i < 8; ++i) {
+    if (ptrs[i] == nullptr) { set_error("%s is NULL", names[i]); return MLA_ERR_INVALID_ARG; }
+    if (!aligned16(ptrs[i])) {
+      set_error("%s is not 16-byte aligned", names[i]);
+      return MLA_ERR_INVALID_ARG;
+    }
+  }
+  const int64_t eb = p.dtype == MLA_DTYPE_BF16 ? 2 : 4;
+  if (c_kv_row_stride < p.r || k_rope_row_stride < p.rope || (c_kv_row_stride * eb) % 16 ||
+      (k_rope_row_stride * eb) % 16) {
+    set_error("row strides (%lld, %lld) must cover r/rope and be 16-byte multiples",
+              (long long)c_kv_row_stride, (long long)k_rope_row_stride);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (page_table == nullptr) {
+    if (seq_stride_rows < p.Tmax && batch > 1) {
+      set_error("seq_stride_rows %lld < longest cache %d", (long long)seq_stride_rows, p.Tmax);
+      return MLA_ERR_INVALID_ARG;
+    }
+  } else {
+    if (page_size < 1 || max_pages_per_seq < 1 || num_pages < 1) {
+      set_error("paged cache needs page_size, max_pages_per_seq, num_pages >= 1");
+      return MLA_ERR_INVALID_ARG;
+    }
+    if ((int64_t)max_pages_per_seq * page_size < p.Tmax) {
+      set_error("page table of %d pages x %d rows cannot hold %d positions", max_pages_per_seq,
+                page_size, p.Tmax);
+      return MLA_ERR_INVALID_ARG;
+    }
+    if (!aligned16(page_table)) {
+      set_error("page_table is not 16-byte aligned");
+      return MLA_ERR_INVALID_ARG;
+    }
+  }
+  if (workspace_bytes < p.ws_bytes || (p.ws_bytes > 0 && workspace == nullptr)) {
+    set_error("workspace of %zu bytes is smaller than the %zu this call needs",
+              workspace_bytes, p.ws_bytes);
+    return MLA_ERR_WORKSPACE;
+  }
+  if (workspace != nullptr && ((uintptr_t)workspace & 255u)) {
+    set_error("workspace is not 256-byte aligned");
+    return MLA_ERR_INVALID_ARG;
+  }
+
+  Args a;
+  a.q_nope = q_nope;
+  a.q_rope = q_rope;
+  a.cache.c_kv = c_kv;
+  a.cache.k_rope = k_rope;
+  a.cache.ckv_stride = c_kv_row_stride;
+  a.cache.kr_stride = k_rope_row_stride;
+  a.cache.seq_stride = seq_stride_rows;
+  a.cache.page_table = page_table;
+  a.cache.page_size = page_size;
+  a.cache.max_pages = max_pages_per_seq;
+  a.W_UK = W_UK;
+  a.W_UV = W_UV;
+  a.lens = lens_dev;
+  a.out = out;
+  a.ws = (char*)workspace;
+  a.stream = (cudaStream_t)stream;
+
+  cudaError_t e = p.branch == MLA_BRANCH_ABSORBED ? launch_generic_absorbed(p, a)
+                                                  : launch_generic_materialised(p, a);
+  if (e != cudaSuccess) {
+    set_error("CUDA error %d (%s)", (int)e, cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  if (branch_taken) *branch_taken = p.branch;
+  return MLA_OK;
+}
+
+extern "C" const char* mla_status_string(int32_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+extern "C" const char* mla_last_error(void) { return g_err; }
+
+extern "C" int32_t mla_version(void) { return 100; }

@@ -1,0 +1,90 @@
+// Internal interfaces of libmla.so: the per-call plan that the host code builds
+// from the C-ABI arguments, and the kernel launchers that consume it.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Launch plan of one verify call.  Built on the host from the arguments and
+// the host copy of the cache lengths, before anything is launched.
+struct Plan {
+  // geometry
+  int B = 0, L = 0, H = 0, r = 0, n = 0, v = 0, rope = 0;
+  float scale = 0.f;
+  int dtype = MLA_DTYPE_BF16;
+  int branch = MLA_BRANCH_ABSORBED;
+  // cache lengths
+  int Tmax = 0;
+  int64_t sumT = 0;
+  // split-KV: sequence b is cut into ceil(T_b / chunk) pieces of `chunk` rows;
+  // `splits` is the largest such count over the batch
+  int chunk = 0;
+  int splits = 0;
+  // which kernel family runs the call
+  bool fast = false;   // tcgen05/TMA kernels (bf16, r = 512, rope = 64)
+  // workspace carve-up (byte offsets from the workspace base)
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0;
+  size_t ws_bytes = 0;
+};
+
+// Device-side view of the cache addressing shared by all kernels.
+struct CacheView {
+  const void* c_kv;
+  const void* k_rope;
+  int64_t ckv_stride;      // elements between consecutive rows of c_kv
+  int64_t kr_stride;       // elements between consecutive rows of k_rope
+  int64_t seq_stride;      // rows between sequences (contiguous cache)
+  const int32_t* page_table;  // NULL: contiguous
+  int32_t page_size;
+  int32_t max_pages;
+};
+
+// Global row index of cached position t of sequence b.
+__host__ __device__ inline int64_t cache_row(const CacheView& c, int b, int t) {
+  if (c.page_table == nullptr) return (int64_t)b * c.seq_stride + t;
+  const int32_t page = c.page_table[(int64_t)b * c.max_pages + t / c.page_size];
+  return (int64_t)page * c.page_size + (t % c.page_size);
+}
+
+struct Args {
+  const void* q_nope;
+  const void* q_rope;
+  CacheView cache;
+  const void* W_UK;
+  const void* W_UV;
+  const int32_t* lens;      // device
+  void* out;
+  char* ws;                 // device workspace base
+  cudaStream_t stream;
+};
+
+// Generic kernels: CUDA-core arithmetic for any geometry, fp32 or bf16.
+cudaError_t launch_generic_absorbed(const Plan& p, const Args& a);
+cudaError_t launch_generic_materialised(const Plan& p, const Args& a);
+
+// Records a one-line failure description for mla_last_error().
+void set_error(const char* fmt, ...);
+
+// Kernel timing instrumentation (mla_kernel_timing_*): while enabled, a
+// KernelTimer brackets one launch with a pair of CUDA events on its stream.
+bool timing_enabled();
+class KernelTimer {
+ public:
+  KernelTimer(const char* name, cudaStream_t stream);
+  ~KernelTimer();
+  KernelTimer(const KernelTimer&) = delete;
+  KernelTimer& operator=(const KernelTimer&) = delete;
+
+ private:
+  int id_ = -1;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr;
+};
+
+}  // namespace mla

@@ -157,18 +157,19 @@ def _as64(x):
 
 
 def absorbed(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=None,
-             heads=None, head_chunk=16):
+             heads=None, rows=None, head_chunk=16):
     """Absorbed branch ("The defect", first bullet).
 
     Shapes: q_nope [B,L,H,n], q_rope [B,L,H,rope], c_kv [B,Tmax,r],
     k_rope [B,Tmax,rope], W_UK [H,n,r], W_UV [H,r,v], cache_lens [B].
-    Returns out [B,L,len(heads),v] in float64.
+    Returns out [B,len(rows),len(heads),v] in float64 (``heads`` / ``rows``
+    select a subset of heads / verify rows; every output is independent).
 
     Steps: q_lat = q_nope . W_UK (fold, n -> r); scores = scale*(q_lat . c_kv^T
     + q_rope . k_rope^T) with the causal verify mask; softmax; o_lat =
     P . c_kv (accumulated in the latent space); out = o_lat . W_UV (r -> v).
     """
-    q_nope, q_rope, c_kv, k_rope = map(_as64, (q_nope, q_rope, c_kv, k_rope))
+    q_nope, q_rope = _as64(q_nope), _as64(q_rope)
     W_UK, W_UV = _as64(W_UK), _as64(W_UV)
     B, L, H, n = q_nope.shape
     rope = q_rope.shape[-1]
@@ -176,16 +177,17 @@ def absorbed(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=None,
     if scale is None:
         scale = default_scale(n, rope)
     heads = list(range(H)) if heads is None else list(heads)
-    out = np.zeros((B, L, len(heads), v), dtype=np.float64)
+    rows = list(range(L)) if rows is None else list(rows)
+    out = np.zeros((B, len(rows), len(heads), v), dtype=np.float64)
     for b in range(B):
         T = int(cache_lens[b])
-        ckv = c_kv[b, :T]            # [T, r]
-        kr = k_rope[b, :T]           # [T, rope]
-        mask = _causal_mask(T, L)    # [L, T]
+        ckv = _as64(c_kv[b, :T])     # [T, r]   (converted one sequence at a time)
+        kr = _as64(k_rope[b, :T])    # [T, rope]
+        mask = _causal_mask(T, L)[rows]   # [rows, T]
         for c0 in range(0, len(heads), head_chunk):
             hs = heads[c0:c0 + head_chunk]
-            qn = q_nope[b][:, hs]                     # [L, h, n]
-            qr = q_rope[b][:, hs]                     # [L, h, rope]
+            qn = q_nope[b][rows][:, hs]               # [rows, h, n]
+            qr = q_rope[b][rows][:, hs]               # [rows, h, rope]
             q_lat = np.einsum('lhn,hnr->hlr', qn, W_UK[hs])          # fold
             s = (q_lat @ ckv.T + np.einsum('lhp,tp->hlt', qr, kr)) * scale
             s = np.where(mask[None], s, -np.inf)
@@ -197,7 +199,7 @@ def absorbed(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=None,
 
 
 def materialised(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=None,
-                 heads=None, head_chunk=8):
+                 heads=None, rows=None, head_chunk=8):
     """Materialised branch ("The defect", second bullet).
 
     Expand the cached latent to full per-head keys K_nope = c_kv . W_UK^T and
@@ -205,7 +207,7 @@ def materialised(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=Non
     [q_nope || q_rope] against [K_nope || k_rope] (the RoPE key is shared by
     all heads).  Same shapes and return as :func:`absorbed`.
     """
-    q_nope, q_rope, c_kv, k_rope = map(_as64, (q_nope, q_rope, c_kv, k_rope))
+    q_nope, q_rope = _as64(q_nope), _as64(q_rope)
     W_UK, W_UV = _as64(W_UK), _as64(W_UV)
     B, L, H, n = q_nope.shape
     rope = q_rope.shape[-1]
@@ -213,23 +215,24 @@ def materialised(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=Non
     if scale is None:
         scale = default_scale(n, rope)
     heads = list(range(H)) if heads is None else list(heads)
-    out = np.zeros((B, L, len(heads), v), dtype=np.float64)
+    rows = list(range(L)) if rows is None else list(rows)
+    out = np.zeros((B, len(rows), len(heads), v), dtype=np.float64)
     for b in range(B):
         T = int(cache_lens[b])
-        ckv = c_kv[b, :T]
-        kr = k_rope[b, :T]
-        mask = _causal_mask(T, L)
+        ckv = _as64(c_kv[b, :T])
+        kr = _as64(k_rope[b, :T])
+        mask = _causal_mask(T, L)[rows]
         for c0 in range(0, len(heads), head_chunk):
             hs = heads[c0:c0 + head_chunk]
             k_nope = np.einsum('tr,hnr->htn', ckv, W_UK[hs])       # expand keys
             val = np.einsum('tr,hrv->htv', ckv, W_UV[hs])          # expand values
-            qn = np.transpose(q_nope[b][:, hs], (1, 0, 2))         # [h, L, n]
-            qr = q_rope[b][:, hs]
+            qn = np.transpose(q_nope[b][rows][:, hs], (1, 0, 2))   # [h, rows, n]
+            qr = q_rope[b][rows][:, hs]
             s = (qn @ np.transpose(k_nope, (0, 2, 1))
                  + np.einsum('lhp,tp->hlt', qr, kr)) * scale
             s = np.where(mask[None], s, -np.inf)
             p = _softmax_rows(s)
-            o = p @ val                                            # [h, L, v]
+            o = p @ val                                            # [h, rows, v]
             out[b, :, c0:c0 + len(hs)] = np.transpose(o, (1, 0, 2))
     return out
 

@@ -204,6 +204,10 @@ def test_head_subset_matches_full():
     np.testing.assert_array_equal(sub, full[:, :, [9, 2, 5]])
     subm = O.materialised(**c, heads=[1, 7])
     np.testing.assert_allclose(subm, full[:, :, [1, 7]], atol=1e-12)
+    rows = O.absorbed(**c, heads=[3, 4], rows=[3, 0])
+    np.testing.assert_allclose(rows, full[:, [3, 0]][:, :, [3, 4]], atol=1e-14)
+    rowsm = O.materialised(**c, heads=[8], rows=[2])
+    np.testing.assert_allclose(rowsm, full[:, [2]][:, :, [8]], atol=1e-12)
 
 
 def test_closed_form_single_position():

@@ -1,0 +1,205 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Small cases are compared element by element (several KV tiles, ragged tails,
+mixed lengths, paged and packed caches, T == L).  The five measurement
+configurations run at their full sizes and are compared on sampled heads and
+verify rows, which the oracle computes one by one.  Branch choice is checked
+exactly against the oracle's crossover.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_attention_speculative_gb300 import binding as B
+from mla_attention_speculative_gb300 import build_lib
+from mla_attention_speculative_gb300.inputs import (DSV3, GLM47, GLM53, Geometry, TINY,
+                                                    WORKLOADS, make_case, workload_shapes)
+from parity_util import (MODE_TO_ORACLE, compare, device_tensors, oracle_inputs, oracle_out,
+                         run_gpu, sample_indices)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build_lib.build()
+    B.lib()
+    yield
+
+
+def _check_branch(case, mode, branch):
+    g = case.geom
+    want = oracle.select_branch(g.r, g.n, g.v, case.L, case.cache_lens, MODE_TO_ORACLE[mode])
+    assert branch == want, (mode, case.L, case.cache_lens, branch, want)
+
+
+# ---------------------------------------------------------------------------
+# Tiny fp32 layer (H=4, 512/128/128, T=512, L=4), both branches and auto
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", ["absorbed", "materialised", "auto"])
+def test_tiny_fp32_full(mode):
+    w = WORKLOADS["tiny_fp32"]
+    (L, lens), = workload_shapes("tiny_fp32")
+    case = make_case(w["geom"], L, lens, dtype=torch.float32, seed=w["seed"])
+    out, branch = run_gpu(case, mode)
+    _check_branch(case, mode, branch)
+    compare(out, oracle_out(case), torch.float32, f"tiny {mode}")
+
+
+# ---------------------------------------------------------------------------
+# Small element-by-element cases: ragged lengths, several tiles, both branches
+# ---------------------------------------------------------------------------
+
+SMALL = [
+    # geometry, L, lens
+    (Geometry(H=8, n=128, v=128), 1, [1]),
+    (Geometry(H=8, n=128, v=128), 5, [5, 130, 1000]),
+    (Geometry(H=8, n=128, v=128), 16, [16, 77, 700]),
+    (Geometry(H=6, n=192, v=256), 7, [64, 65, 300]),
+    (Geometry(H=4, n=256, v=256), 3, [129, 511]),
+    (Geometry(H=3, n=128, v=128), 2, [2, 33]),
+    (Geometry(H=128, n=128, v=128), 4, [200]),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("mode", ["absorbed", "materialised"])
+@pytest.mark.parametrize("idx", range(len(SMALL)))
+def test_small_full(idx, mode, dtype):
+    geom, L, lens = SMALL[idx]
+    case = make_case(geom, L, lens, dtype=dtype, seed=100 + idx)
+    out, branch = run_gpu(case, mode)
+    _check_branch(case, mode, branch)
+    compare(out, oracle_out(case), dtype, f"small{idx} {mode}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 64, 65, 200])
+def test_cold_cache_T_equals_L(T):
+    case = make_case(Geometry(H=8), T, [T], seed=7 + T)
+    want = oracle_out(case)
+    for mode in ("absorbed", "materialised", "auto"):
+        out, branch = run_gpu(case, mode)
+        _check_branch(case, mode, branch)
+        if mode == "auto":
+            assert branch == (B.BRANCH_ABSORBED if T == 1 else B.BRANCH_MATERIALISED)
+        compare(out, want, torch.bfloat16, f"T=L={T} {mode}")
+
+
+def test_auto_boundary_dsv3_T512():
+    # 512/128/128 at T = 512: r*d*T/(r*d+(2r-d)T) = 128 exactly -> L=128 absorbed, 129 not
+    for L, want in ((128, B.BRANCH_ABSORBED), (129, B.BRANCH_MATERIALISED)):
+        case = make_case(Geometry(H=4), L, [512], seed=L)
+        out, branch = run_gpu(case, "auto")
+        assert branch == want
+        heads = [0, 3]
+        rows = sample_indices(L, 6, L)
+        compare(out[:, rows][:, :, heads], oracle_out(case, heads=heads, rows=rows),
+                torch.bfloat16, f"boundary L={L}")
+
+
+def test_packed_cache_rows():
+    # one [B, T, r + rope] buffer: k_rope is the tail of each row
+    case = make_case(Geometry(H=8), 6, [300, 64], seed=31)
+    packed = torch.cat([case.c_kv, case.k_rope], dim=-1).cuda()
+    d = device_tensors(case)
+    d["c_kv"] = packed[..., :512]
+    d["k_rope"] = packed[..., 512:]
+    want = oracle_out(case)
+    for mode in ("absorbed", "materialised"):
+        out, _ = run_gpu(case, mode, dev_t=d)
+        compare(out, want, torch.bfloat16, f"packed {mode}")
+
+
+@pytest.mark.parametrize("page", [64, 16])
+def test_paged_cache_with_poisoned_tails(page):
+    # rows past each sequence's length and unused pages hold NaN: they must not leak
+    geom = Geometry(H=8)
+    lens = [70, 64, 1, 300]
+    case = make_case(geom, 1, lens, seed=41, page_size=page)
+    want = oracle_out(case)
+    d = device_tensors(case)
+    pt = case.page_table
+    poison_c = d["c_kv"].clone()
+    poison_k = d["k_rope"].clone()
+    used = torch.zeros(poison_c.shape[0], page, dtype=torch.bool)
+    for b, T in enumerate(lens):
+        for t in range(T):
+            used[pt[b, t // page], t % page] = True
+    poison_c[~used.cuda()] = float("nan")
+    poison_k[~used.cuda()] = float("nan")
+    d["c_kv"], d["k_rope"] = poison_c, poison_k
+    for mode in ("absorbed", "materialised"):
+        out, _ = run_gpu(case, mode, dev_t=d)
+        compare(out, want, torch.bfloat16, f"paged{page} {mode}")
+
+
+def test_contiguous_tail_poisoned():
+    # contiguous cache with capacity beyond T: positions >= T hold NaN
+    case = make_case(Geometry(H=8), 4, [100, 37], seed=43, tmax=256)
+    want = oracle_out(case)
+    d = device_tensors(case)
+    for b, T in enumerate(case.cache_lens):
+        d["c_kv"][b, T:] = float("nan")
+        d["k_rope"][b, T:] = float("nan")
+    for mode in ("absorbed", "materialised"):
+        out, _ = run_gpu(case, mode, dev_t=d)
+        compare(out, want, torch.bfloat16, f"tail {mode}")
+
+
+def test_repeat_call_is_deterministic():
+    case = make_case(Geometry(H=16), 8, [1500], seed=5)
+    d = device_tensors(case)
+    for mode in ("absorbed", "materialised"):
+        a, _ = run_gpu(case, mode, dev_t=d)
+        b, _ = run_gpu(case, mode, dev_t=d)
+        assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# The measurement configurations at full size, sampled outputs
+# ---------------------------------------------------------------------------
+
+def _sampled_check(case, modes, what, nheads=6, nrows=6):
+    d = device_tensors(case)
+    inp = oracle_inputs(case)
+    heads = sample_indices(case.geom.H, nheads, case.L)
+    rows = sample_indices(case.L, nrows, case.L + 1)
+    want = oracle.absorbed(**inp, heads=heads, rows=rows)
+    for mode in modes:
+        out, branch = run_gpu(case, mode, dev_t=d)
+        _check_branch(case, mode, branch)
+        compare(out[:, rows][:, :, heads], want, case.dtype, f"{what} {mode}")
+    del d
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("L,lens", workload_shapes("dsv3"))
+def test_dsv3_config(L, lens):
+    w = WORKLOADS["dsv3"]
+    case = make_case(w["geom"], L, lens, seed=w["seed"])
+    modes = ["auto"] + (["materialised"] if L in (1, 16) else [])
+    _sampled_check(case, modes, f"dsv3 T={lens[0]} L={L}")
+
+
+@pytest.mark.parametrize("L,lens", workload_shapes("glm47_sweep"))
+def test_glm47_sweep(L, lens):
+    w = WORKLOADS["glm47_sweep"]
+    case = make_case(w["geom"], L, lens, seed=w["seed"])
+    _sampled_check(case, ["auto", "absorbed", "materialised"], f"glm L={L}")
+
+
+def test_batched_paged_serving():
+    w = WORKLOADS["batched_paged"]
+    (L, lens), = workload_shapes("batched_paged")
+    case = make_case(w["geom"], L, lens, seed=w["seed"], page_size=w["page_size"])
+    _sampled_check(case, ["absorbed", "auto"], "batched paged", nheads=4, nrows=3)
+
+
+@pytest.mark.parametrize("L,lens", workload_shapes("long_context"))
+def test_long_context(L, lens):
+    w = WORKLOADS["long_context"]
+    case = make_case(w["geom"], L, lens, seed=w["seed"])
+    _sampled_check(case, ["auto"], f"long L={L} T={lens[0]}", nheads=4, nrows=4)
