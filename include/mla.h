@@ -151,6 +151,37 @@ mla_status_t mla_verify_attention(
     int32_t mode, void* out, void* workspace, size_t workspace_bytes,
     void* stream, int32_t* branch_taken);
 
+/* The absorbed-branch verify call without a workspace, for callers that cannot
+ * allocate device memory (a plugin host or serving engine that owns every
+ * device allocation and gives its attention back-end no allocator, or a
+ * latency-critical loop that must not call cudaMalloc).  The pages have no
+ * counterpart: it exists for those callers only.
+ *
+ * Arguments are those of mla_verify_attention without mode, workspace and
+ * workspace_bytes; the absorbed branch always runs.  Scratch comes from one
+ * 32 MiB static device array inside the library, which every GPU that loads
+ * the library keeps reserved until the process exits.  A call whose scratch
+ * (mla_workspace_bytes with MLA_MODE_ABSORBED) exceeds 32 MiB returns
+ * MLA_ERR_WORKSPACE before launching anything.  It never calls cudaMalloc,
+ * cudaFree or an allocating library routine.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture starts.  All calls share the array and it keeps
+ * the previous call's contents (nothing in it needs to start at zero): calls
+ * that overlap on the GPU race on it, so issue them one at a time. */
+mla_status_t mla_verify_attention_noalloc(
+    const mla_geometry_t* geom,
+    const void* q_nope, const void* q_rope,
+    const void* c_kv, const void* k_rope,
+    int64_t c_kv_row_stride, int64_t k_rope_row_stride, int64_t seq_stride_rows,
+    const void* W_UK, const void* W_UV,
+    const int32_t* cache_lens_dev, const int32_t* cache_lens_host,
+    int32_t batch, int32_t L,
+    const int32_t* page_table, int32_t page_size, int32_t max_pages_per_seq,
+    int32_t num_pages,
+    void* out, void* stream, int32_t* branch_taken);
+
 /* Per-kernel timing, for benchmarks.  While enabled, every kernel launch the
  * library makes is bracketed by a pair of CUDA events recorded on the call's
  * stream (events come from a library-owned pool; no device memory).  Do not

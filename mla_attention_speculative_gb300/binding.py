@@ -58,6 +58,9 @@ _SIGS = {
     "mla_verify_attention": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P,
                                     _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _P,
                                     ctypes.c_size_t, _P, _P]),
+    "mla_verify_attention_noalloc": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P,
+                                            _P, _P, _I32, _I32, _P, _I32, _I32, _I32, _P,
+                                            _P, _P]),
     "mla_kernel_timing_enable": (_I32, [_I32]),
     "mla_kernel_timing_read": (_I32, [ctypes.c_char_p, ctypes.c_size_t, _P, _P, _I32, _P,
                                       _I32]),
@@ -216,3 +219,41 @@ def mla_kernel_timing_read(reset: bool = True) -> dict:
                                         1 if reset else 0), "mla_kernel_timing_read")
     keys = names.value.decode().split(";") if n.value else []
     return {k: (int(launches[i]), float(ms[i])) for i, k in enumerate(keys[:cap])}
+
+
+def mla_verify_attention_noalloc(q_nope: torch.Tensor, q_rope: torch.Tensor,
+                                 c_kv: torch.Tensor, k_rope: torch.Tensor,
+                                 W_UK: torch.Tensor, W_UV: torch.Tensor,
+                                 cache_lens: Sequence[int], out: Optional[torch.Tensor] = None,
+                                 page_table: Optional[torch.Tensor] = None,
+                                 cache_lens_dev: Optional[torch.Tensor] = None,
+                                 scale: Optional[float] = None, stream=None):
+    """Absorbed-branch verify call that uses the library's static scratch
+    instead of a workspace (for callers that cannot allocate device memory).
+    Same tensors as :func:`mla_verify_attention`; returns (out, branch)."""
+    B, L, H, n = q_nope.shape
+    rope = q_rope.shape[-1]
+    r = W_UK.shape[-1]
+    v = W_UV.shape[-1]
+    dev = q_nope.device
+    geom = make_geometry(H, r, n, v, rope, q_nope.dtype, scale)
+    lens = [int(t) for t in cache_lens]
+    arr = _lens_array(lens)
+    paged = page_table is not None
+    cs, ks, seq = cache_strides(c_kv, k_rope, paged)
+    if cache_lens_dev is None:
+        cache_lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty((B, L, H, v), dtype=q_nope.dtype, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    page_size = c_kv.shape[1] if paged else 0
+    max_pages = page_table.shape[1] if paged else 0
+    num_pages = c_kv.shape[0] if paged else 0
+    branch = ctypes.c_int32(0)
+    st = lib().mla_verify_attention_noalloc(
+        ctypes.byref(geom), _ptr(q_nope), _ptr(q_rope), _ptr(c_kv), _ptr(k_rope), cs, ks, seq,
+        _ptr(W_UK), _ptr(W_UV), _ptr(cache_lens_dev), arr, B, L, _ptr(page_table), page_size,
+        max_pages, num_pages, _ptr(out), stream, ctypes.byref(branch))
+    _check(st, "mla_verify_attention_noalloc")
+    return out, branch.value
