@@ -91,6 +91,9 @@ def _work(kernel: str, L: int, T: int, H=128, r=512, n=128, v=128, rope=64):
         "generic_fold": fold,
         "generic_absorbed_attention": attend,
         "generic_combine_unembed": unembed,
+        "fold_sm103": fold,
+        "absorbed_attn_sm103": attend,
+        "unembed_sm103": unembed,
     }
     return table.get(kernel)
 
@@ -108,6 +111,9 @@ KERNEL_SOURCES = {
     "generic_absorbed_attention": ["generic_kernels.cu"],
     "generic_fold": ["generic_kernels.cu"],
     "generic_combine_unembed": ["generic_kernels.cu"],
+    "fold_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
+    "absorbed_attn_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
+    "unembed_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
 }
 
 

@@ -199,6 +199,14 @@ mla_status_t mla_kernel_timing_read(char* names, size_t names_len, int32_t* laun
                                     double* total_ms, int32_t max_kernels,
                                     int32_t* n_kernels, int32_t reset);
 
+/* Waits for the device to go idle, then reads the kernels' status word:
+ * MLA_OK when no bounded wait inside a kernel ran out since the last clear,
+ * MLA_ERR_TIMEOUT otherwise (*code receives the site that gave up, 0 when
+ * none).  The kernels never hang on a missing signal: each wait gives up
+ * after about a second, records its site here and lets the kernel finish
+ * (its outputs are then undefined).  clear != 0 resets the word. */
+mla_status_t mla_device_status(int32_t* code, int32_t clear);
+
 /* Static name of a status code. */
 const char* mla_status_string(int32_t status);
 

@@ -64,6 +64,7 @@ _SIGS = {
     "mla_kernel_timing_enable": (_I32, [_I32]),
     "mla_kernel_timing_read": (_I32, [ctypes.c_char_p, ctypes.c_size_t, _P, _P, _I32, _P,
                                       _I32]),
+    "mla_device_status": (_I32, [_P, _I32]),
     "mla_status_string": (ctypes.c_char_p, [_I32]),
     "mla_last_error": (ctypes.c_char_p, []),
     "mla_version": (_I32, []),
@@ -140,6 +141,19 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _dense(**tensors):
+    for name, t in tensors.items():
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (row-major)")
+
+
+def mla_device_status(clear: bool = True) -> int:
+    """Wait for the device, then raise MlaError if a kernel's bounded wait ran out."""
+    code = ctypes.c_int32(0)
+    _check(lib().mla_device_status(ctypes.byref(code), 1 if clear else 0), "mla_device_status")
+    return code.value
+
+
 def cache_strides(c_kv: torch.Tensor, k_rope: torch.Tensor, paged: bool):
     """(c_kv row stride, k_rope row stride, rows between sequences) in elements."""
     if c_kv.stride(-1) != 1 or k_rope.stride(-1) != 1:
@@ -175,6 +189,7 @@ def mla_verify_attention(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv: torch
     r = W_UK.shape[-1]
     v = W_UV.shape[-1]
     dev = q_nope.device
+    _dense(q_nope=q_nope, q_rope=q_rope, W_UK=W_UK, W_UV=W_UV, out=out, page_table=page_table)
     geom = make_geometry(H, r, n, v, rope, q_nope.dtype, scale)
     lens = [int(t) for t in cache_lens]
     arr = _lens_array(lens)

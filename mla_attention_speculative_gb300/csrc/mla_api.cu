@@ -160,39 +160,76 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     p->Tmax = lens[b] > p->Tmax ? lens[b] : p->Tmax;
     p->sumT += lens[b];
   }
-  p->fast = false;
 
-  // Split-KV: enough CTAs (one per 4 query rows per piece) to cover the GPU a
-  // few times over, pieces a multiple of 64 rows.
+  // Generic split-KV: enough CTAs (one per 4 query rows per piece) to cover
+  // the GPU a few times over, pieces a multiple of 64 rows.
   const int64_t rows = (int64_t)L * p->H;
-  const int64_t row_ctas = (int64_t)batch * ((rows + kGenericRowsPerCTA - 1) / kGenericRowsPerCTA);
-  const int64_t want = 4 * kNumSMs;
-  int64_t splits = (want + row_ctas - 1) / row_ctas;
-  const int64_t max_splits = (p->Tmax + 63) / 64;
-  if (splits > max_splits) splits = max_splits;
-  if (splits < 1) splits = 1;
-  int64_t chunk = (p->Tmax + splits - 1) / splits;
-  chunk = (chunk + 63) / 64 * 64;
-  p->chunk = (int)chunk;
-  p->splits = (int)((p->Tmax + chunk - 1) / chunk);
-
   const size_t eb = p->dtype == MLA_DTYPE_BF16 ? 2 : 4;
-  const int dv = p->branch == MLA_BRANCH_ABSORBED ? p->r : p->v;
   const size_t nrow = (size_t)batch * rows;
-  size_t off = 0;
-  p->off_qlat = p->off_exp = p->off_olat = 0;
-  if (p->branch == MLA_BRANCH_ABSORBED) {
-    p->off_qlat = off;
-    off = align256(off + nrow * p->r * sizeof(float));
-  } else {
-    p->off_exp = off;
-    off = align256(off + (size_t)batch * p->Tmax * p->H * (p->n + p->v) * eb);
+  {
+    SplitPlan& g = p->generic;
+    const int64_t row_ctas =
+        (int64_t)batch * ((rows + kGenericRowsPerCTA - 1) / kGenericRowsPerCTA);
+    const int64_t want = 4 * kNumSMs;
+    int64_t splits = (want + row_ctas - 1) / row_ctas;
+    const int64_t max_splits = (p->Tmax + 63) / 64;
+    if (splits > max_splits) splits = max_splits;
+    if (splits < 1) splits = 1;
+    int64_t chunk = (p->Tmax + splits - 1) / splits;
+    chunk = (chunk + 63) / 64 * 64;
+    g.chunk = (int)chunk;
+    g.splits = (int)((p->Tmax + chunk - 1) / chunk);
+    const int dv = p->branch == MLA_BRANCH_ABSORBED ? p->r : p->v;
+    size_t off = 0;
+    if (p->branch == MLA_BRANCH_ABSORBED) {
+      g.off_qlat = off;
+      off = align256(off + nrow * p->r * sizeof(float));
+    } else {
+      g.off_exp = off;
+      off = align256(off + (size_t)batch * p->Tmax * p->H * (p->n + p->v) * eb);
+    }
+    g.off_opart = off;
+    off = align256(off + nrow * g.splits * dv * sizeof(float));
+    g.off_ml = off;
+    off = align256(off + nrow * g.splits * 2 * sizeof(float));
+    g.bytes = off;
   }
-  p->off_opart = off;
-  off = align256(off + nrow * p->splits * dv * sizeof(float));
-  p->off_ml = off;
-  off = align256(off + nrow * p->splits * 2 * sizeof(float));
-  p->ws_bytes = off;
+  p->fast_ok = p->branch == MLA_BRANCH_ABSORBED && fast_absorbed_supported(*p);
+  if (p->fast_ok) {
+    // Tensor-core split-KV: clusters of 2 CTAs, one per (128-row tile, piece).
+    // Pick the piece length ct (in 64-row KV tiles) that minimises
+    // waves x (ct + overhead) over the SMs' cluster slots, where the fixed
+    // cost of a cluster (Q load, pipeline fill, writing 128 x 512 fp32
+    // partials that the merge reads back) is worth about kClusterOverhead KV
+    // tiles; ties go to longer pieces (fewer partials).
+    constexpr int64_t kClusterOverhead = 4;
+    SplitPlan& f = p->fast;
+    const int64_t row_tiles = (rows + 127) / 128;
+    const int64_t slots = kNumSMs / 2;
+    const int64_t max_tiles = (p->Tmax + 63) / 64;
+    int64_t best_ct = max_tiles, best_cost = -1;
+    for (int64_t ct = max_tiles; ct >= 1; --ct) {
+      int64_t clusters = 0;
+      for (int b = 0; b < batch; ++b) clusters += row_tiles * (((lens[b] + 63) / 64 + ct - 1) / ct);
+      const int64_t cost = ((clusters + slots - 1) / slots) * (ct + kClusterOverhead);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_ct = ct;
+      }
+    }
+    f.chunk = (int)(best_ct * 64);
+    f.splits = (int)((p->Tmax + f.chunk - 1) / f.chunk);
+    size_t off = 0;
+    f.off_qlat = off;
+    off = align256(off + nrow * p->r * 2);
+    f.off_opart = off;
+    off = align256(off + nrow * f.splits * p->r * sizeof(float));
+    f.off_ml = off;
+    off = align256(off + nrow * f.splits * 2 * sizeof(float));
+    f.bytes = off;
+  }
+  p->ws_bytes = p->fast_ok && p->fast.bytes > p->generic.bytes ? p->fast.bytes : p->generic.bytes;
+  p->use(p->generic);
   return MLA_OK;
 }
 
@@ -290,6 +327,7 @@ extern "C" mla_status_t mla_verify_attention(
   a.cache.page_table = page_table;
   a.cache.page_size = page_size;
   a.cache.max_pages = max_pages_per_seq;
+  a.cache.num_pages = num_pages;
   a.W_UK = W_UK;
   a.W_UV = W_UV;
   a.lens = lens_dev;
@@ -297,8 +335,14 @@ extern "C" mla_status_t mla_verify_attention(
   a.ws = (char*)workspace;
   a.stream = (cudaStream_t)stream;
 
-  cudaError_t e = p.branch == MLA_BRANCH_ABSORBED ? launch_generic_absorbed(p, a)
-                                                  : launch_generic_materialised(p, a);
+  cudaError_t e;
+  if (p.fast_ok && (page_table == nullptr || page_size % 64 == 0)) {
+    p.use(p.fast);
+    e = launch_fast_absorbed(p, a);
+  } else {
+    e = p.branch == MLA_BRANCH_ABSORBED ? launch_generic_absorbed(p, a)
+                                        : launch_generic_materialised(p, a);
+  }
   if (e != cudaSuccess) {
     set_error("CUDA error %d (%s)", (int)e, cudaGetErrorString(e));
     return MLA_ERR_CUDA;
@@ -320,5 +364,19 @@ extern "C" const char* mla_status_string(int32_t s) {
 }
 
 extern "C" const char* mla_last_error(void) { return g_err; }
+
+extern "C" mla_status_t mla_device_status(int32_t* code, int32_t clear) {
+  const int v = absorbed_device_status(clear != 0);
+  if (code) *code = v;
+  if (v < 0) {
+    set_error("could not read the device status word");
+    return MLA_ERR_CUDA;
+  }
+  if (v != 0) {
+    set_error("a bounded device wait ran out (site %d)", v);
+    return MLA_ERR_TIMEOUT;
+  }
+  return MLA_OK;
+}
 
 extern "C" int32_t mla_version(void) { return 100; }

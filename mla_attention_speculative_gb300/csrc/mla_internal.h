@@ -11,6 +11,14 @@
 
 namespace mla {
 
+// Split-KV layout and workspace carve-up of one kernel family.
+struct SplitPlan {
+  int chunk = 0;    // KV rows per piece (multiple of 64)
+  int splits = 0;   // largest number of pieces of any sequence
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0;
+  size_t bytes = 0;
+};
+
 // Launch plan of one verify call.  Built on the host from the arguments and
 // the host copy of the cache lengths, before anything is launched.
 struct Plan {
@@ -26,11 +34,21 @@ struct Plan {
   // `splits` is the largest such count over the batch
   int chunk = 0;
   int splits = 0;
-  // which kernel family runs the call
-  bool fast = false;   // tcgen05/TMA kernels (bf16, r = 512, rope = 64)
-  // workspace carve-up (byte offsets from the workspace base)
-  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0;
+  // the two kernel families' layouts; the workspace covers the larger
+  SplitPlan generic;   // CUDA-core kernels, any geometry and paging
+  SplitPlan fast;      // tcgen05/TMA kernels (bf16, r = 512, rope = 64)
+  bool fast_ok = false;
   size_t ws_bytes = 0;
+  // the layout of the family that runs (copied from generic or fast)
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0;
+  void use(const SplitPlan& sp) {
+    chunk = sp.chunk;
+    splits = sp.splits;
+    off_qlat = sp.off_qlat;
+    off_opart = sp.off_opart;
+    off_ml = sp.off_ml;
+    off_exp = sp.off_exp;
+  }
 };
 
 // Device-side view of the cache addressing shared by all kernels.
@@ -43,6 +61,7 @@ struct CacheView {
   const int32_t* page_table;  // NULL: contiguous
   int32_t page_size;
   int32_t max_pages;
+  int32_t num_pages;
 };
 
 // Global row index of cached position t of sequence b.
@@ -67,6 +86,13 @@ struct Args {
 // Generic kernels: CUDA-core arithmetic for any geometry, fp32 or bf16.
 cudaError_t launch_generic_absorbed(const Plan& p, const Args& a);
 cudaError_t launch_generic_materialised(const Plan& p, const Args& a);
+
+// Tensor-core kernels for the absorbed branch (bf16, r = 512, rope = 64,
+// n a multiple of 64 up to 256, v a multiple of 128 up to 512).
+bool fast_absorbed_supported(const Plan& p);
+cudaError_t launch_fast_absorbed(const Plan& p, const Args& a);
+// Status word of the tensor-core kernels (0 = no wait ran out); synchronises.
+int absorbed_device_status(bool clear);
 
 // Records a one-line failure description for mla_last_error().
 void set_error(const char* fmt, ...);

@@ -52,6 +52,7 @@ def run_gpu(case: Case, mode: str, dev_t=None, **kw):
         case.cache_lens, mode=mode, page_table=d["page_table"],
         cache_lens_dev=d["lens_dev"], **kw)
     torch.cuda.synchronize()
+    B.mla_device_status()   # raises if a kernel's bounded wait ran out
     return out, branch
 
 
