@@ -28,6 +28,7 @@
 // mla_device_status reports MLA_ERR_TIMEOUT).
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cfloat>
 #include <cmath>
@@ -158,19 +159,24 @@ __global__ void __launch_bounds__(128) fold_sm103(const __grid_constant__ CUtens
 // =========================================================================
 constexpr int BM = 128;                 // query rows per tile
 constexpr int BN = 64;                  // cached positions per KV tile
-constexpr int STAGES = 2;
-constexpr int Q_CHUNK = BM * 128;       // one 64-column bf16 chunk of the Q tile
+constexpr int STAGES = 3;
+constexpr int Q_CHUNK = BM * 128;       // one 64-column bf16 chunk of the Q tile (128-B swizzle)
+constexpr int Q_ROPE = BM * 64;         // the 32 RoPE columns of this CTA (64-B swizzle)
 constexpr int KV_CHUNK = BN * 128;      // one 64-column bf16 chunk of a KV tile
-constexpr int MAX_CH = 5;               // 4 latent chunks (+ RoPE on CTA 0)
+constexpr int KV_ROPE = BN * 64;        // 32 RoPE columns of a KV tile
+constexpr int X_BYTES = BM * BN * 2;    // the peer's partial scores, fp16 [128][64]
 constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + MAX_CH * Q_CHUNK;
-constexpr int KV_STAGE = MAX_CH * KV_CHUNK;
-constexpr int OFF_P = OFF_KV + STAGES * KV_STAGE;
-constexpr int OFF_X = OFF_P + BM * 128;          // peer partial scores, fp32 [128][64]
-constexpr int OFF_BAR = OFF_X + BM * BN * 4;
-constexpr int ATTN_SMEM = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
-constexpr uint32_t TM_O = 0;                     // O half: columns [0, 256)
-constexpr uint32_t TM_S = 256;                   // S buffers: 256 + 64*sb
+constexpr int OFF_QR = OFF_Q + 4 * Q_CHUNK;
+constexpr int OFF_KV = OFF_QR + Q_ROPE;
+constexpr int KV_STAGE = 4 * KV_CHUNK + KV_ROPE;
+constexpr int OFF_X = OFF_KV + STAGES * KV_STAGE;
+constexpr int OFF_BAR = OFF_X + X_BYTES;
+constexpr int ATTN_SMEM = OFF_BAR + 256 + 1024;     // + barriers + alignment slack
+constexpr uint32_t TM_O = 0;                        // O half: columns [0, 256)
+constexpr uint32_t TM_S = 256;                      // S / P buffers: 256 + 64*sb
+constexpr int SBUF = 4;                             // S / P buffers (TMEM columns 256..511)
+static_assert(OFF_KV % 1024 == 0 && KV_STAGE % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+static_assert(ATTN_SMEM <= 232448, "shared memory per CTA");
 
 struct AttnParams {
   const int32_t* lens;
@@ -184,10 +190,51 @@ struct AttnParams {
   float* ml;          // [B, splits, R, 2]
 };
 
+// Barrier slots.  Every barrier that is waited on by parity alone has enough
+// copies that it cannot complete twice before its waiter looks: P-full and
+// O-done alternate by tile parity, S buffers by tile % 4.
 enum {
-  B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 3, B_SFULL = 5, B_SFREE = 7, B_PFULL = 9,
-  B_ODONE = 10, B_XFULL = 11, B_XFREE = 12, B_COUNT = 13
+  B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 4, B_SFULL = 7, B_SFREE = 11, B_PFULL = 15,
+  B_ODONE = 17, B_XFULL = 19, B_XFREE = 20, B_COUNT = 21
 };
+
+// This CTA's partial scores of tile j from TMEM, scaled to log2-softmax units.
+__device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t lane_base, int j,
+                                             uint32_t bar_sfull0, uint32_t bar_sfree0,
+                                             float sl2, float (&s)[BN]) {
+  const int sb = j & (SBUF - 1);
+  wait_or_fail(ok, bar_sfull0 + 8 * sb, (j / SBUF) & 1, 20);
+  tc_fence_after();
+  uint32_t v[BN];
+#pragma unroll
+  for (int k = 0; k < BN / 16; ++k)
+    tmem_ld16(tmem + lane_base + TM_S + sb * BN + 16 * k, *(uint32_t(*)[16])(v + 16 * k));
+  tmem_wait_ld();
+#pragma unroll
+  for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(v[e]) * sl2;
+  tc_fence_before();
+  mbar_arrive(bar_sfree0 + 8 * sb);
+}
+
+// Round this row's partial scores to fp16 (both CTAs add the same two rounded
+// partials, so their sums agree bit for bit) and send them into the peer's
+// exchange buffer; each 16-byte store counts itself off the peer's barrier.
+__device__ __forceinline__ void send_partial(uint32_t peer_x, uint32_t peer_xfull, int q,
+                                             float (&s)[BN]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2 v = __floats2half2_rn(s[8 * c + 2 * e], s[8 * c + 2 * e + 1]);
+      h[e] = *reinterpret_cast<const uint32_t*>(&v);
+      const float2 back = __half22float2(v);
+      s[8 * c + 2 * e] = back.x;
+      s[8 * c + 2 * e + 1] = back.y;
+    }
+    st_async_v4(peer_x + q * 128 + ((c ^ (q & 7)) << 4), h[0], h[1], h[2], h[3], peer_xfull);
+  }
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     absorbed_attn_sm103(const __grid_constant__ CUtensorMap tm_ql,
@@ -209,14 +256,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const int kv0 = split * p.chunk;
   const int kv1 = min(min(kv0 + p.chunk, T), vis_end);
   const int ntiles = kv1 > kv0 ? (kv1 - kv0 + BN - 1) / BN : 0;
-  const int nch = rank == 0 ? 5 : 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
-  uint32_t* slot = (uint32_t*)(bars + 16);
+  uint32_t* slot = (uint32_t*)(bars + 24);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t sQ = smem_u32(smem + OFF_Q), sKV = smem_u32(smem + OFF_KV);
-  const uint32_t sP = smem_u32(smem + OFF_P), sX = smem_u32(smem + OFF_X);
+  const uint32_t sQ = smem_u32(smem + OFF_Q), sQR = smem_u32(smem + OFF_QR);
+  const uint32_t sKV = smem_u32(smem + OFF_KV), sX = smem_u32(smem + OFF_X);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
@@ -224,21 +270,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       mbar_init(bar(B_KVFULL + s), 1);
       mbar_init(bar(B_KVEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < SBUF; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
       mbar_init(bar(B_SFREE + s), 128);
     }
-    mbar_init(bar(B_PFULL), 128);
-    mbar_init(bar(B_ODONE), 1);
-    mbar_init(bar(B_XFULL), 128);
-    mbar_init(bar(B_XFREE), 128);
+    for (int s = 0; s < 2; ++s) mbar_init(bar(B_ODONE + s), 1);
+    for (int s = 0; s < 2; ++s) mbar_init(bar(B_PFULL + s), 128);
+    mbar_init(bar(B_XFULL), 1);
+    mbar_init(bar(B_XFREE), 1);
     fence_mbar_init();
+    // arm the exchange barrier for tile 0 (the peer's stores count it down)
+    if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
   }
   if (warp == 1) tmem_alloc(smem_u32(slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers exist before any remote arrive
+  cluster_sync();  // the peer's barriers exist (and are armed) before any remote access
   const uint32_t tmem = *slot;
 
   if (warp == 0) {
@@ -248,10 +296,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       prefetch_tmap(&tm_ql);
       prefetch_tmap(&tm_ckv);
       const int qrow = b * p.R + row0;
-      mbar_arrive_expect_tx(bar(B_QFULL), nch * Q_CHUNK);
+      mbar_arrive_expect_tx(bar(B_QFULL), 4 * Q_CHUNK + Q_ROPE);
       for (int c = 0; c < 4; ++c)
         tma_load_2d(sQ + c * Q_CHUNK, &tm_ql, bar(B_QFULL), (int)(4 * rank + c) * 64, qrow);
-      if (rank == 0) tma_load_2d(sQ + 4 * Q_CHUNK, &tm_qr, bar(B_QFULL), 0, qrow);
+      tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
       for (int i = 0; i < ntiles; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES) wait_or_fail(ok, bar(B_KVEMPTY + s), ((i / STAGES) - 1) & 1, 10);
@@ -262,11 +310,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                                    p.page_size + (t0 % p.page_size)
                          : (long long)b * p.seq_stride + t0;
         const uint32_t st = sKV + s * KV_STAGE;
-        mbar_arrive_expect_tx(bar(B_KVFULL + s), nch * KV_CHUNK);
+        mbar_arrive_expect_tx(bar(B_KVFULL + s), KV_STAGE);
         for (int c = 0; c < 4; ++c)
           tma_load_2d(st + c * KV_CHUNK, &tm_ckv, bar(B_KVFULL + s), (int)(4 * rank + c) * 64,
                       (int)y);
-        if (rank == 0) tma_load_2d(st + 4 * KV_CHUNK, &tm_kr, bar(B_KVFULL + s), 0, (int)y);
+        tma_load_2d(st + 4 * KV_CHUNK, &tm_kr, bar(B_KVFULL + s), (int)rank * 32, (int)y);
       }
     }
   } else if (warp == 1) {
@@ -278,35 +326,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const uint32_t id_o = idesc_bf16(BM, 256, 0, 1);
       for (int i = 0; i <= ntiles && ok; ++i) {
         if (i < ntiles) {
-          const int s = i % STAGES, sb = i & 1;
+          // S(i) = Q . K(i)^T over this CTA's 256 latent + 32 RoPE columns
+          const int s = i % STAGES, sb = i & (SBUF - 1);
           wait_or_fail(ok, bar(B_KVFULL + s), (i / STAGES) & 1, 12);
-          if (i >= 2) wait_or_fail(ok, bar(B_SFREE + sb), ((i - 2) >> 1) & 1, 13);
+          if (i >= SBUF) wait_or_fail(ok, bar(B_SFREE + sb), ((i - SBUF) / SBUF) & 1, 13);
           if (!ok) break;
           tc_fence_after();
           const uint32_t st = sKV + s * KV_STAGE;
-          for (int c = 0; c < nch; ++c)
+          const uint32_t d = tmem + TM_S + sb * BN;
+          for (int c = 0; c < 4; ++c)
             for (int ks = 0; ks < 4; ++ks)
-              mma_bf16(tmem + TM_S + sb * BN, sdesc_sw128(sQ + c * Q_CHUNK + ks * 32, 16, 1024),
+              mma_bf16(d, sdesc_sw128(sQ + c * Q_CHUNK + ks * 32, 16, 1024),
                        sdesc_sw128(st + c * KV_CHUNK + ks * 32, 16, 1024), id_s, (c | ks) != 0);
+          for (int ks = 0; ks < 2; ++ks)
+            mma_bf16(d, sdesc_sw64(sQR + ks * 32, 512), sdesc_sw64(st + 4 * KV_CHUNK + ks * 32, 512),
+                     id_s, 1);
           mma_commit(bar(B_SFULL + sb));
         }
         if (i >= 1) {
-          const int j = i - 1, sj = j % STAGES;
-          wait_or_fail(ok, bar(B_PFULL), j & 1, 14);
+          // O += P(j) . V(j): P from TMEM (bf16 pairs over S buffer j%4), V = this
+          // CTA's 256 latent columns of the KV tile
+          const int j = i - 1, sj = j % STAGES, pb = j & (SBUF - 1);
+          wait_or_fail(ok, bar(B_PFULL + (j & 1)), (j >> 1) & 1, 14);
           if (!ok) break;
           tc_fence_after();
           const uint32_t st = sKV + sj * KV_STAGE;
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + TM_O, sdesc_sw128(sP + ks * 32, 16, 1024),
-                     sdesc_sw128(st + ks * 2048, KV_CHUNK, 1024), id_o, (j > 0 || ks > 0));
-          mma_commit(bar(B_ODONE));
+            mma_bf16_tmem_a(tmem + TM_O, tmem + TM_S + pb * BN + ks * 8,
+                            sdesc_sw128(st + ks * 2048, KV_CHUNK, 1024), id_o, (j > 0 || ks > 0));
+          mma_commit(bar(B_ODONE + (j & 1)));
           mma_commit(bar(B_KVEMPTY + sj));
         }
       }
     }
   } else {
     // ------------------------------------------------- softmax warpgroup
+    // Tile i's scores are finished (own + peer partial) while tile i+1's
+    // partial is already on its way to the peer.  P(i) goes back into the TMEM
+    // columns S(i) came from; S(i+4) reuses them, long after P.V(i) has run.
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const int sm_tid = threadIdx.x - 64;
     const int row = row0 + q;
     const int l = min(row, p.R - 1) / p.H;
     const int last_t = T - p.L + l;
@@ -316,57 +375,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const uint32_t peer_xfree = mapa(bar(B_XFREE), peer);
     bool ok = true;
     float m_run = -INFINITY, l_run = 0.f;
+    float s[BN];
+    if (ntiles > 0) {
+      load_partial(ok, tmem, lane_base, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
+      send_partial(peer_x, peer_xfull, q, s);
+    }
     for (int i = 0; i < ntiles; ++i) {
-      const int sb = i & 1;
-      wait_or_fail(ok, bar(B_SFULL + sb), (i >> 1) & 1, 20);
-      tc_fence_after();
-      float s[BN];
-#pragma unroll
-      for (int k = 0; k < BN / 16; ++k) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_base + TM_S + sb * BN + 16 * k, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) s[16 * k + e] = __uint_as_float(v[e]);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(B_SFREE + sb));
-      // swap partial scores with the peer CTA
-      if (i > 0) wait_cluster_or_fail(ok, bar(B_XFREE), (i - 1) & 1, 21);
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_cluster_v4(peer_x + q * 256 + ((c ^ (q & 15)) << 4), s[4 * c], s[4 * c + 1],
-                      s[4 * c + 2], s[4 * c + 3]);
-      mbar_arrive_remote(peer_xfull);
+      // finish tile i's scores with the peer's partial
       wait_cluster_or_fail(ok, bar(B_XFULL), i & 1, 22);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float4 x;
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
-                     : "r"(sX + q * 256 + ((c ^ (q & 15)) << 4)));
-        s[4 * c] += x.x;
-        s[4 * c + 1] += x.y;
-        s[4 * c + 2] += x.z;
-        s[4 * c + 3] += x.w;
+      for (int c = 0; c < 8; ++c) {
+        uint32_t h[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+                     : "r"(sX + q * 128 + ((c ^ (q & 7)) << 4)));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
+          s[8 * c + 2 * e] += f.x;
+          s[8 * c + 2 * e + 1] += f.y;
+        }
       }
-      mbar_arrive_remote(peer_xfree);
-      // causal verify mask, log2-domain scores, tile maximum
+      named_bar_sync(1, 128);  // every row has read the exchange buffer
+      if (sm_tid == 0) {
+        if (i + 1 < ntiles) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);  // arm tile i+1
+        mbar_arrive_remote(peer_xfree);  // the peer may now send tile i+1
+      }
+      // start tile i+1's exchange
+      float sn[BN];
+      if (i + 1 < ntiles) {
+        load_partial(ok, tmem, lane_base, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn);
+        wait_cluster_or_fail(ok, bar(B_XFREE), i & 1, 21);  // the peer has read my tile i
+        send_partial(peer_x, peer_xfull, q, sn);
+      }
+      // causal verify mask and tile maximum (scores are in log2 units already)
       const int t0 = kv0 + i * BN;
       float mt = -INFINITY;
 #pragma unroll
       for (int j = 0; j < BN; ++j) {
-        s[j] = (t0 + j <= last_t) ? s[j] * p.sl2 : -INFINITY;
+        s[j] = (t0 + j <= last_t) ? s[j] : -INFINITY;
         mt = fmaxf(mt, s[j]);
       }
-      // O (and the P buffer) are free once the previous P.V finished
-      if (i > 0) wait_or_fail(ok, bar(B_ODONE), (i - 1) & 1, 23);
-      tc_fence_after();
-      // lazy rescale: move the running max only when it grows by more than 2^8
+      // lazy rescale: move the running max only when it grows by more than 2^8;
+      // O must then hold every earlier P.V
       const bool need = mt > m_run + 8.f;
       const float m_new = need ? mt : m_run;
-      const float factor = need ? exp2f(m_run - m_new) : 1.f;
+      const float factor = need ? ex2(m_run - m_new) : 1.f;
       if (i > 0 && __any_sync(0xffffffffu, need)) {
+        wait_or_fail(ok, bar(B_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, 23);
+        tc_fence_after();
         for (int c = 0; c < 256; c += 16) {
           uint32_t v[16];
           tmem_ld16(tmem + lane_base + TM_O + c, v);
@@ -379,24 +436,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       }
       l_run *= factor;
       m_run = m_new;
-      // P = 2^(s - m) in bf16, K-major 128-byte-swizzled rows of 64 positions
+      // P = 2^(s - m) as bf16 pairs into the first 32 columns of S buffer i%4
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
       float rs = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
-      for (int j = 0; j < BN; j += 2) {
-        const float a = m_run == -INFINITY ? 0.f : exp2f(s[j] - m_run);
-        const float c = m_run == -INFINITY ? 0.f : exp2f(s[j + 1] - m_run);
-        rs += a + c;
-        pk[j / 2] = pack_bf16(a, c);
+      for (int e = 0; e < BN / 2; ++e) {
+        const float a = ex2(s[2 * e] - m_use);
+        const float d = ex2(s[2 * e + 1] - m_use);
+        rs += a + d;
+        pk[e] = pack_bf16(a, d);
       }
       l_run += rs;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = sP + q * 128 + (((c ^ q) & 7) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c]),
-                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
-      }
+      tmem_st32(tmem + lane_base + TM_S + (i & (SBUF - 1)) * BN, pk);
       // positions at or past T in the last tile: zero their value rows (they may hold
       // anything, and 0 * NaN would poison the accumulator)
       if (t0 + BN > T) {
@@ -409,13 +461,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
                        : "memory");
         }
+        fence_async_shared();
       }
-      fence_async_shared();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
+      mbar_arrive(bar(B_PFULL + (i & 1)));
+#pragma unroll
+      for (int e = 0; e < BN; ++e) s[e] = sn[e];
     }
     // ---------------------------------------------------------------- epilogue
-    if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE), (ntiles - 1) & 1, 24);
+    if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
     tc_fence_after();
     const bool live = row < p.R;
     float* op = p.o_part + (((size_t)b * p.splits + split) * p.R + (live ? row : 0)) * kLat +
@@ -603,15 +658,15 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
 
   CUtensorMap tm_wuk, tm_qn, tm_ql, tm_qr, tm_ckv, tm_kr, tm_wuv;
   const int NB = fast_fold_rows(BL);
-  bool ok = make_tmap_bf16_2d(&tm_wuk, a.W_UK, kLat, (uint64_t)p.H * p.n, kLat * 2, 64, 64, true);
+  bool ok = make_tmap_bf16_2d(&tm_wuk, a.W_UK, kLat, (uint64_t)p.H * p.n, kLat * 2, 64, 64, 128);
   ok = ok && make_tmap_bf16_2d(&tm_qn, a.q_nope, (uint64_t)p.H * p.n, BL, (uint64_t)p.H * p.n * 2,
-                               64, NB, true);
-  ok = ok && make_tmap_bf16_2d(&tm_ql, q_lat, kLat, (uint64_t)p.B * R, kLat * 2, 64, BM, true);
-  ok = ok && make_tmap_bf16_2d(&tm_qr, a.q_rope, 64, (uint64_t)p.B * R, 128, 64, BM, true);
-  ok = ok && make_tmap_bf16_2d(&tm_ckv, c.c_kv, kLat, cache_rows, c.ckv_stride * 2, 64, BN, true);
-  ok = ok && make_tmap_bf16_2d(&tm_kr, c.k_rope, 64, cache_rows, c.kr_stride * 2, 64, BN, true);
+                               64, NB, 128);
+  ok = ok && make_tmap_bf16_2d(&tm_ql, q_lat, kLat, (uint64_t)p.B * R, kLat * 2, 64, BM, 128);
+  ok = ok && make_tmap_bf16_2d(&tm_qr, a.q_rope, 64, (uint64_t)p.B * R, 128, 32, BM, 64);
+  ok = ok && make_tmap_bf16_2d(&tm_ckv, c.c_kv, kLat, cache_rows, c.ckv_stride * 2, 64, BN, 128);
+  ok = ok && make_tmap_bf16_2d(&tm_kr, c.k_rope, 64, cache_rows, c.kr_stride * 2, 32, BN, 64);
   ok = ok && make_tmap_bf16_2d(&tm_wuv, a.W_UV, p.v, (uint64_t)p.H * kLat, (uint64_t)p.v * 2, 64,
-                               128, true);
+                               128, 128);
   if (!ok) return cudaErrorInvalidValue;
 
   static bool attrs = false;

@@ -8,11 +8,12 @@
 namespace mla {
 
 // A [rows, inner] bf16 tensor with `row_stride_bytes` between rows, read in
-// boxes of box_rows x box_inner elements (128-byte swizzle when requested;
-// then box_inner * 2 must be 128).  Elements outside the tensor read as zero.
+// boxes of box_rows x box_inner elements, written to shared memory with the
+// given swizzle (box_inner * 2 must equal the swizzle width: 128 or 64
+// bytes; 0 = no swizzle).  Elements outside the tensor read as zero.
 // Returns false if the encoding fails (bad alignment or sizes).
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
-                       bool swizzle128);
+                       int swizzle_bytes);
 
 }  // namespace mla
