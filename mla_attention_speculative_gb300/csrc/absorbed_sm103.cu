@@ -5,11 +5,12 @@
 // apply the value up-projection.  Three kernels, all bf16 operands with fp32
 // accumulation in tensor memory:
 //
-//  fold_sm103      q_lat[row, h, :] = q_nope[row, h, :] . W_UK[h]  (n -> 512).
-//                  Swap-AB GEMM per head: D[512 x rows] = W_UK[h]^T x q_nope^T,
-//                  so the weight is the 128-row operand read once for all
-//                  B*L rows (the pages' "small-M verify" idea, "Draft caps and
-//                  calibration", section "Small-M verify kernel").
+//  swapab_gemm     fold: q_lat[row, h, :] = q_nope[row, h, :] . W_UK[h] (n -> 512)
+//                  and unembed: out[row, h, :] = o_lat[row, h, :] . W_UV[h]
+//                  (512 -> v).  Swap-AB GEMM per head: D[M x rows] = W[h]^T x
+//                  act^T, so the weight is the 128-row operand read once for
+//                  all B*L rows (the pages' "small-M verify" idea, "Draft caps
+//                  and calibration", section "Small-M verify kernel").
 //  absorbed_attn   split-KV attention of the L*H query rows of a sequence
 //                  against [c_kv || k_rope] (576 wide), online softmax, causal
 //                  verify mask, o_lat = P . c_kv accumulated in the latent space.
@@ -20,8 +21,11 @@
 //                  computes its partial scores over its columns, swaps them
 //                  with the peer through distributed shared memory, and both
 //                  accumulate their half of o_lat (128 x 256 fp32 in TMEM).
-//  unembed_sm103   merges the split-KV pieces (log-sum-exp) and applies W_UV:
-//                  D[v x rows] = W_UV[h]^T x o_lat^T (swap-AB, weight read once).
+//  merge_sm103     log-sum-exp merge of the split-KV pieces into bf16 o_lat.
+//
+// The four kernels are chained with programmatic dependent launch: each one
+// starts the loads that do not depend on its predecessor (weights, the KV
+// cache) before waiting for it.
 //
 // Every wait is bounded; a wait that runs out sets the status word and the
 // kernel finishes without waiting further (results are then undefined and
@@ -32,6 +36,7 @@
 
 #include <cfloat>
 #include <cmath>
+#include <utility>
 
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
@@ -74,32 +79,39 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(int n) {
 }
 
 // =========================================================================
-// fold
+// swap-AB small-M GEMM (fold and unembed)
 // =========================================================================
-struct FoldParams {
-  __nv_bfloat16* q_lat;  // [B*L*H, 512]
-  int BL, H, n, NB;      // NB: rows per CTA (multiple of 16, <= 256)
+// out[row, h, m] = sum_k act[row, h, k] * W[h][k][m] for the B*L rows of a call:
+//   fold:    act = q_nope (K = n),    W = W_UK [H, n, 512], out = q_lat (M = 512)
+//   unembed: act = o_lat  (K = 512),  W = W_UV [H, 512, v], out = out   (M = v)
+// One CTA per (128-wide M tile, head, block of NB rows): D[128 x NB] =
+// W[h][:, tile]^T (MN-major, the 128-row operand) x act^T (K-major).  The
+// weight is read once for all rows.  K arrives in 64-wide chunks, each with
+// its own barrier, and each chunk's MMAs issue as soon as it lands.
+struct GemmParams {
+  __nv_bfloat16* out;  // [rows, H, M]
+  int rows, H, K, M, NB;
 };
 
-__global__ void __launch_bounds__(128) fold_sm103(const __grid_constant__ CUtensorMap tm_wuk,
-                                                  const __grid_constant__ CUtensorMap tm_qn,
-                                                  FoldParams p) {
+constexpr int GEMM_MAX_K = 512;
+
+__global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__ CUtensorMap tm_w,
+                                                         const __grid_constant__ CUtensorMap tm_act,
+                                                         GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int mt = blockIdx.x, h = blockIdx.y, row0 = blockIdx.z * p.NB;
-  const int n = p.n, nk = n / 64, NB = p.NB;
-  uint8_t* sA = smem;                   // W_UK[h][:, mt*128 +: 128], MN-major: 2 atoms x n rows
-  uint8_t* sB = smem + 2 * n * 128;     // q_nope rows, K-major: nk chunks x NB rows
-  uint64_t* bars = (uint64_t*)(sB + nk * NB * 128);
-  uint32_t* slot = (uint32_t*)(bars + 2);
-  volatile int* fail = (volatile int*)(bars + 3);
-  const uint32_t bar_load = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
+  const int K = p.K, nk = K / 64, NB = p.NB;
+  uint8_t* sA = smem;                    // 2 atoms x K rows x 128 B
+  uint8_t* sB = smem + 2 * K * 128;      // nk chunks x NB rows x 128 B
+  uint64_t* bars = (uint64_t*)(sB + nk * NB * 128);   // [0, nk): chunk k landed; nk: MMA done
+  uint32_t* slot = (uint32_t*)(bars + GEMM_MAX_K / 64 + 1);
+  volatile int* fail = (volatile int*)(slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ncols = tmem_cols_for(NB);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_load, 1);
-    mbar_init(bar_mma, 1);
+    for (int k = 0; k <= nk; ++k) mbar_init(smem_u32(&bars[k]), 1);
     *fail = 0;
     fence_mbar_init();
   }
@@ -111,32 +123,39 @@ __global__ void __launch_bounds__(128) fold_sm103(const __grid_constant__ CUtens
 
   if (threadIdx.x == 0) {
     bool ok = true;
-    mbar_arrive_expect_tx(bar_load, 2 * n * 128 + nk * NB * 128);
-    for (int j = 0; j < 2; ++j)
-      for (int kc = 0; kc < nk; ++kc)
-        tma_load_2d(smem_u32(sA + j * n * 128 + kc * 8192), &tm_wuk, bar_load, mt * 128 + 64 * j,
-                    h * n + 64 * kc);
+    // the weights do not depend on the preceding kernel: start them first
+    for (int kc = 0; kc < nk; ++kc) {
+      const uint32_t bk = smem_u32(&bars[kc]);
+      mbar_arrive_expect_tx(bk, 2 * 64 * 128 + NB * 128);
+      for (int j = 0; j < 2; ++j)
+        tma_load_2d(smem_u32(sA + j * K * 128 + kc * 8192), &tm_w, bk, mt * 128 + 64 * j,
+                    h * K + 64 * kc);
+    }
+    pdl_wait();  // the activations may come from the preceding kernel
     for (int kc = 0; kc < nk; ++kc)
-      tma_load_2d(smem_u32(sB + kc * NB * 128), &tm_qn, bar_load, h * n + 64 * kc, row0);
-    wait_or_fail(ok, bar_load, 0, 1);
-    if (ok) {
+      tma_load_2d(smem_u32(sB + kc * NB * 128), &tm_act, smem_u32(&bars[kc]), h * K + 64 * kc,
+                  row0);
+    const uint32_t idesc = idesc_bf16(128, NB, 1, 0);
+    for (int kc = 0; kc < nk && ok; ++kc) {
+      wait_or_fail(ok, smem_u32(&bars[kc]), 0, 1);
+      if (!ok) break;
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, NB, 1, 0);
-      for (int kk = 0; kk < n / 16; ++kk) {
-        const uint64_t a = sdesc_sw128(smem_u32(sA) + kk * 2048, n * 128, 1024);
-        const uint64_t b =
-            sdesc_sw128(smem_u32(sB) + (kk >> 2) * NB * 128 + (kk & 3) * 32, 16, 1024);
-        mma_bf16(tmem, a, b, idesc, kk > 0);
-      }
-      mma_commit(bar_mma);
-      wait_or_fail(ok, bar_mma, 0, 2);
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem, sdesc_sw128(smem_u32(sA) + (kc * 64 + ks * 16) * 128, K * 128, 1024),
+                 sdesc_sw128(smem_u32(sB) + kc * NB * 128 + ks * 32, 16, 1024), idesc,
+                 (kc | ks) != 0);
+    }
+    if (ok) {
+      mma_commit(smem_u32(&bars[nk]));
+      wait_or_fail(ok, smem_u32(&bars[nk]), 0, 2);
     }
     if (!ok) *fail = 1;
   }
   __syncthreads();
+  pdl_launch_dependents();
   tc_fence_after();
   if (!*fail) {
-    const int r = mt * 128 + warp * 32 + lane;
+    const int m = mt * 128 + warp * 32 + lane;
     for (int c0 = 0; c0 < NB; c0 += 16) {
       uint32_t v[16];
       tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
@@ -144,8 +163,8 @@ __global__ void __launch_bounds__(128) fold_sm103(const __grid_constant__ CUtens
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int row = row0 + c0 + i;
-        if (row < p.BL)
-          p.q_lat[((size_t)row * p.H + h) * kLat + r] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        if (row < p.rows)
+          p.out[((size_t)row * p.H + h) * p.M + m] = __float2bfloat16_rn(__uint_as_float(v[i]));
       }
     }
   }
@@ -195,7 +214,7 @@ struct AttnParams {
 // O-done alternate by tile parity, S buffers by tile % 4.
 enum {
   B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 4, B_SFULL = 7, B_SFREE = 11, B_PFULL = 15,
-  B_ODONE = 17, B_XFULL = 19, B_XFREE = 20, B_COUNT = 21
+  B_ODONE = 17, B_XFULL = 19, B_XFREE = 20, B_DRAIN = 21, B_COUNT = 22
 };
 
 // This CTA's partial scores of tile j from TMEM, scaled to log2-softmax units.
@@ -278,6 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     for (int s = 0; s < 2; ++s) mbar_init(bar(B_PFULL + s), 128);
     mbar_init(bar(B_XFULL), 1);
     mbar_init(bar(B_XFREE), 1);
+    mbar_init(bar(B_DRAIN), 1);
     fence_mbar_init();
     // arm the exchange barrier for tile 0 (the peer's stores count it down)
     if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
@@ -296,14 +316,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       prefetch_tmap(&tm_ql);
       prefetch_tmap(&tm_ckv);
       const int qrow = b * p.R + row0;
-      mbar_arrive_expect_tx(bar(B_QFULL), 4 * Q_CHUNK + Q_ROPE);
-      for (int c = 0; c < 4; ++c)
-        tma_load_2d(sQ + c * Q_CHUNK, &tm_ql, bar(B_QFULL), (int)(4 * rank + c) * 64, qrow);
-      tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
-      for (int i = 0; i < ntiles; ++i) {
+      auto load_kv = [&](int i) {
         const int s = i % STAGES;
-        if (i >= STAGES) wait_or_fail(ok, bar(B_KVEMPTY + s), ((i / STAGES) - 1) & 1, 10);
-        if (!ok) break;
         const int t0 = kv0 + i * BN;
         const long long y =
             p.page_table ? (long long)p.page_table[(long long)b * p.max_pages + t0 / p.page_size] *
@@ -315,7 +329,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           tma_load_2d(st + c * KV_CHUNK, &tm_ckv, bar(B_KVFULL + s), (int)(4 * rank + c) * 64,
                       (int)y);
         tma_load_2d(st + 4 * KV_CHUNK, &tm_kr, bar(B_KVFULL + s), (int)rank * 32, (int)y);
+      };
+      // the first stages do not depend on the preceding kernel ...
+      const int pre = min(ntiles, STAGES);
+      for (int i = 0; i < pre; ++i) load_kv(i);
+      // ... q_lat does (the fold writes it)
+      pdl_wait();
+      mbar_arrive_expect_tx(bar(B_QFULL), 4 * Q_CHUNK + Q_ROPE);
+      for (int c = 0; c < 4; ++c)
+        tma_load_2d(sQ + c * Q_CHUNK, &tm_ql, bar(B_QFULL), (int)(4 * rank + c) * 64, qrow);
+      tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
+      int issued = pre;
+      for (int i = STAGES; i < ntiles; ++i) {
+        wait_or_fail(ok, bar(B_KVEMPTY + i % STAGES), ((i / STAGES) - 1) & 1, 10);
+        if (!ok) break;
+        load_kv(i);
+        issued = i + 1;
       }
+      // nothing this thread started may still be landing when the CTA exits
+      mbar_wait(bar(B_QFULL), 0);
+      for (int i = max(issued - STAGES, 0); i < issued; ++i)
+        mbar_wait(bar(B_KVFULL + i % STAGES), (i / STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
@@ -358,6 +392,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           mma_commit(bar(B_KVEMPTY + sj));
         }
       }
+      // every MMA issued here has finished before tensor memory is released
+      mma_commit(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0);
     }
   } else {
     // ------------------------------------------------- softmax warpgroup
@@ -374,15 +411,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
     const uint32_t peer_xfree = mapa(bar(B_XFREE), peer);
     bool ok = true;
+    int armed = ntiles > 0 ? 1 : 0, received = 0;  // exchange phases armed / completed
     float m_run = -INFINITY, l_run = 0.f;
     float s[BN];
     if (ntiles > 0) {
       load_partial(ok, tmem, lane_base, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
-      send_partial(peer_x, peer_xfull, q, s);
+      if (ok) send_partial(peer_x, peer_xfull, q, s);
     }
     for (int i = 0; i < ntiles; ++i) {
       // finish tile i's scores with the peer's partial
       wait_cluster_or_fail(ok, bar(B_XFULL), i & 1, 22);
+      if (ok) received = i + 1;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t h[4];
@@ -397,8 +436,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
       }
       named_bar_sync(1, 128);  // every row has read the exchange buffer
-      if (sm_tid == 0) {
-        if (i + 1 < ntiles) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);  // arm tile i+1
+      if (sm_tid == 0 && ok) {
+        if (i + 1 < ntiles) {
+          mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);  // arm tile i+1
+          ++armed;
+        }
         mbar_arrive_remote(peer_xfree);  // the peer may now send tile i+1
       }
       // start tile i+1's exchange
@@ -406,7 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       if (i + 1 < ntiles) {
         load_partial(ok, tmem, lane_base, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn);
         wait_cluster_or_fail(ok, bar(B_XFREE), i & 1, 21);  // the peer has read my tile i
-        send_partial(peer_x, peer_xfull, q, sn);
+        if (ok) send_partial(peer_x, peer_xfull, q, sn);
       }
       // causal verify mask and tile maximum (scores are in log2 units already)
       const int t0 = kv0 + i * BN;
@@ -469,8 +511,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 #pragma unroll
       for (int e = 0; e < BN; ++e) s[e] = sn[e];
     }
+    // after a failure, let an armed exchange phase finish (or time out) so no
+    // store from the peer is still landing when this CTA exits
+    if (sm_tid == 0 && received < armed) mbar_wait_cluster(bar(B_XFULL), received & 1);
     // ---------------------------------------------------------------- epilogue
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
+    pdl_wait();                // the partials may still be read by an earlier merge
+    pdl_launch_dependents();   // let the merge kernel start its prologue
     tc_fence_after();
     const bool live = row < p.R;
     float* op = p.o_part + (((size_t)b * p.splits + split) * p.R + (live ? row : 0)) * kLat +
@@ -505,127 +552,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 }
 
 // =========================================================================
-// merge + unembed
+// merge of the split-KV pieces
 // =========================================================================
-struct UnembedParams {
-  const float* o_part;
-  const float* ml;
+// o_lat[row] = sum_s 2^(m_s - M) O_s[row] / sum_s 2^(m_s - M) l_s  (bf16).
+// One CTA per query row: 4 groups of 64 threads take every 4th piece, each
+// thread 8 latent columns; the groups' sums are added in shared memory.
+struct MergeParams {
+  const float* o_part;   // [B, splits, R, 512]
+  const float* ml;       // [B, splits, R, 2]
   const int32_t* lens;
-  __nv_bfloat16* out;  // [B, L, H, v]
-  int BL, L, H, v, R, chunk, splits;
+  __nv_bfloat16* o_lat;  // [B*R, 512]
+  int R, chunk, splits;
 };
 
-constexpr int UN_ROWS = 64;
-
-__global__ void __launch_bounds__(128) unembed_sm103(const __grid_constant__ CUtensorMap tm_wuv,
-                                                     UnembedParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  const int vt = blockIdx.x, h = blockIdx.y, rt = blockIdx.z;
-  uint8_t* sW = smem;                     // W_UV[h][:, vt*128 +: 128], MN-major: 2 atoms x 512
-  uint8_t* sO = smem + 2 * 65536;         // merged o_lat rows, K-major: 8 chunks x NRpad rows
-  uint64_t* bars = (uint64_t*)(sO + 8 * UN_ROWS * 128);
-  uint32_t* slot = (uint32_t*)(bars + 2);
-  volatile int* fail = (volatile int*)(bars + 3);
-  const uint32_t bar_w = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const int NR = min(UN_ROWS, p.BL - rt * UN_ROWS);
-  const int NRpad = (NR + 15) & ~15;
-
-  if (tid == 0) {
-    mbar_init(bar_w, 1);
-    mbar_init(bar_mma, 1);
-    *fail = 0;
-    fence_mbar_init();
+__global__ void __launch_bounds__(256) merge_sm103(MergeParams p) {
+  __shared__ float part[4][kLat];
+  __shared__ float den_part[4];
+  pdl_wait();
+  const int rg = blockIdx.x;  // b*R + row
+  const int b = rg / p.R, row = rg - b * p.R;
+  const int g = threadIdx.x >> 6, t = threadIdx.x & 63;
+  const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
+  const size_t base = (size_t)b * p.splits * p.R + row;
+  float M = -FLT_MAX;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.ml[(base + (size_t)s * p.R) * 2]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float den = 0.f;
+#pragma unroll 4
+  for (int s = g; s < nsplit; s += 4) {
+    const float* mls = p.ml + (base + (size_t)s * p.R) * 2;
+    const float ls = mls[1];
+    const float w = ls > 0.f ? ex2(mls[0] - M) : 0.f;
+    den += w * ls;
+    const float* o = p.o_part + (base + (size_t)s * p.R) * kLat + 8 * t;
+    const float4 x0 = *(const float4*)o;
+    const float4 x1 = *(const float4*)(o + 4);
+    acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+    acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
   }
-  if (warp == 0) tmem_alloc(smem_u32(slot), 64);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *slot;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_w, 2 * 65536);
-    for (int j = 0; j < 2; ++j)
-      for (int kb = 0; kb < 4; ++kb)
-        tma_load_2d(smem_u32(sW + j * 65536 + kb * 16384), &tm_wuv, bar_w, vt * 128 + 64 * j,
-                    h * kLat + 128 * kb);
-  }
-  // merge the split-KV pieces of each row (thread owns latent columns 4*tid .. 4*tid+3)
-  for (int nn = 0; nn < NRpad; ++nn) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (nn < NR) {
-      const int bl = rt * UN_ROWS + nn;
-      const int bb = bl / p.L, ll = bl - bb * p.L;
-      const int row = ll * p.H + h;
-      const int nsplit = (p.lens[bb] + p.chunk - 1) / p.chunk;
-      const size_t base = (size_t)bb * p.splits * p.R + row;
-      float M = -FLT_MAX;
-      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.ml[(base + (size_t)s * p.R) * 2]);
-      float den = 0.f;
-      for (int s = 0; s < nsplit; ++s) {
-        const float* mls = p.ml + (base + (size_t)s * p.R) * 2;
-        if (mls[1] > 0.f) {
-          const float w = exp2f(mls[0] - M);
-          den += w * mls[1];
-          const float4 o = *(const float4*)(p.o_part + (base + (size_t)s * p.R) * kLat + 4 * tid);
-          acc.x += w * o.x;
-          acc.y += w * o.y;
-          acc.z += w * o.z;
-          acc.w += w * o.w;
-        }
-      }
-      const float inv = 1.f / den;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
-    }
-    const int k = 4 * tid, c = k >> 6, col = k & 63;
-    const uint32_t addr = smem_u32(sO) + c * NRpad * 128 + sw128_offset(nn, col);
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(pack_bf16(acc.x, acc.y)),
-                 "r"(pack_bf16(acc.z, acc.w))
-                 : "memory");
-  }
-  fence_async_shared();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0) {
-    bool ok = true;
-    wait_or_fail(ok, bar_w, 0, 30);
-    if (ok) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, NRpad, 1, 0);
-      for (int kk = 0; kk < kLat / 16; ++kk)
-        mma_bf16(tmem, sdesc_sw128(smem_u32(sW) + kk * 2048, 65536, 1024),
-                 sdesc_sw128(smem_u32(sO) + (kk >> 2) * NRpad * 128 + (kk & 3) * 32, 16, 1024),
-                 idesc, kk > 0);
-      mma_commit(bar_mma);
-      wait_or_fail(ok, bar_mma, 0, 31);
-    }
-    if (!ok) *fail = 1;
-  }
-  __syncthreads();
-  tc_fence_after();
-  if (!*fail) {
-    const int vcol = vt * 128 + warp * 32 + lane;
-    for (int c0 = 0; c0 < NRpad; c0 += 16) {
-      uint32_t v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-      tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int nn = c0 + i;
-        if (nn < NR) {
-          const int bl = rt * UN_ROWS + nn;
-          p.out[((size_t)bl * p.H + h) * p.v + vcol] = __float2bfloat16_rn(__uint_as_float(v[i]));
-        }
-      }
-    }
-  }
-  tc_fence_before();
+  for (int e = 0; e < 8; ++e) part[g][8 * t + e] = acc[e];
+  if (t == 0) den_part[g] = den;
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 64);
+  pdl_launch_dependents();
+  if (g == 0) {
+    const float inv = 1.f / (den_part[0] + den_part[1] + den_part[2] + den_part[3]);
+    uint32_t pk[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 8 * t + 2 * e;
+      pk[e] = pack_bf16((part[0][c] + part[1][c] + part[2][c] + part[3][c]) * inv,
+                        (part[0][c + 1] + part[1][c + 1] + part[2][c + 1] + part[3][c + 1]) * inv);
+    }
+    *(uint4*)(p.o_lat + (size_t)rg * kLat + 8 * t) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
 }
 
 template <typename K>
@@ -640,10 +620,35 @@ bool fast_absorbed_supported(const Plan& p) {
          p.n >= 64 && p.n <= 256 && p.v % 128 == 0 && p.v <= 512;
 }
 
-int fast_fold_rows(int BL) {
+namespace {
+
+// Rows per CTA of the swap-AB GEMM: the whole batch up to 256 (64 when K is
+// 512, so the weight tile and the activations fit in shared memory).
+int gemm_rows(int BL, int K) {
+  const int cap = K >= 512 ? 64 : 256;
   const int nb = ((BL + 15) / 16) * 16;
-  return nb > 256 ? 256 : nb;
+  return nb > cap ? cap : nb;
 }
+
+int gemm_smem(int K, int NB) { return 2 * K * 128 + (K / 64) * NB * 128 + 1024 + 128; }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace
 
 cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   const int BL = p.B * p.L;
@@ -651,39 +656,47 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   __nv_bfloat16* q_lat = (__nv_bfloat16*)(a.ws + p.off_qlat);
   float* o_part = (float*)(a.ws + p.off_opart);
   float* ml = (float*)(a.ws + p.off_ml);
+  __nv_bfloat16* o_lat = (__nv_bfloat16*)(a.ws + p.off_olat);
   const CacheView& c = a.cache;
   const long long cache_rows =
       c.page_table ? (long long)c.num_pages * c.page_size
                    : (long long)(p.B - 1) * c.seq_stride + p.Tmax;
 
-  CUtensorMap tm_wuk, tm_qn, tm_ql, tm_qr, tm_ckv, tm_kr, tm_wuv;
-  const int NB = fast_fold_rows(BL);
+  CUtensorMap tm_wuk, tm_qn, tm_ql, tm_qr, tm_ckv, tm_kr, tm_wuv, tm_ol;
+  const int NBf = gemm_rows(BL, p.n), NBu = gemm_rows(BL, kLat);
   bool ok = make_tmap_bf16_2d(&tm_wuk, a.W_UK, kLat, (uint64_t)p.H * p.n, kLat * 2, 64, 64, 128);
   ok = ok && make_tmap_bf16_2d(&tm_qn, a.q_nope, (uint64_t)p.H * p.n, BL, (uint64_t)p.H * p.n * 2,
-                               64, NB, 128);
+                               64, NBf, 128);
   ok = ok && make_tmap_bf16_2d(&tm_ql, q_lat, kLat, (uint64_t)p.B * R, kLat * 2, 64, BM, 128);
   ok = ok && make_tmap_bf16_2d(&tm_qr, a.q_rope, 64, (uint64_t)p.B * R, 128, 32, BM, 64);
   ok = ok && make_tmap_bf16_2d(&tm_ckv, c.c_kv, kLat, cache_rows, c.ckv_stride * 2, 64, BN, 128);
   ok = ok && make_tmap_bf16_2d(&tm_kr, c.k_rope, 64, cache_rows, c.kr_stride * 2, 32, BN, 64);
   ok = ok && make_tmap_bf16_2d(&tm_wuv, a.W_UV, p.v, (uint64_t)p.H * kLat, (uint64_t)p.v * 2, 64,
-                               128, 128);
+                               64, 128);
+  ok = ok && make_tmap_bf16_2d(&tm_ol, o_lat, (uint64_t)p.H * kLat, BL, (uint64_t)p.H * kLat * 2,
+                               64, NBu, 128);
   if (!ok) return cudaErrorInvalidValue;
 
-  static bool attrs = false;
-  const int fold_smem = 2 * p.n * 128 + (p.n / 64) * NB * 128 + 1024 + 64;
-  const int un_smem = 2 * 65536 + 8 * UN_ROWS * 128 + 1024 + 64;
-  if (!attrs) {
-    cudaError_t e = set_smem(fold_sm103, 2 * 256 * 128 + 4 * 256 * 128 + 1024 + 64);
-    if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103, ATTN_SMEM);
-    if (e == cudaSuccess) e = set_smem(unembed_sm103, un_smem);
+  static bool attrs[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attrs[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(swapab_gemm_sm103,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         gemm_smem(kLat, 64));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(absorbed_attn_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               ATTN_SMEM);
     if (e != cudaSuccess) return e;
-    attrs = true;
+    attrs[dev] = true;
   }
+  cudaError_t e;
   {
-    FoldParams fp{q_lat, BL, p.H, p.n, NB};
-    dim3 grid(kLat / 128, p.H, (BL + NB - 1) / NB);
+    GemmParams gp{q_lat, BL, p.H, p.n, kLat, NBf};
     KernelTimer kt("fold_sm103", a.stream);
-    fold_sm103<<<grid, 128, fold_smem, a.stream>>>(tm_wuk, tm_qn, fp);
+    e = launch_pdl(swapab_gemm_sm103, dim3(kLat / 128, p.H, (BL + NBf - 1) / NBf), dim3(128),
+                   gemm_smem(p.n, NBf), a.stream, tm_wuk, tm_qn, gp);
+    if (e != cudaSuccess) return e;
   }
   {
     AttnParams ap;
@@ -700,16 +713,23 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.sl2 = p.scale * 1.4426950408889634f;
     ap.o_part = o_part;
     ap.ml = ml;
-    dim3 grid(2 * ((R + BM - 1) / BM), p.splits, p.B);
     KernelTimer kt("absorbed_attn_sm103", a.stream);
-    absorbed_attn_sm103<<<grid, 192, ATTN_SMEM, a.stream>>>(tm_ql, tm_qr, tm_ckv, tm_kr, ap);
+    e = launch_pdl(absorbed_attn_sm103, dim3(2 * ((R + BM - 1) / BM), p.splits, p.B), dim3(192),
+                   ATTN_SMEM, a.stream, tm_ql, tm_qr, tm_ckv, tm_kr, ap);
+    if (e != cudaSuccess) return e;
   }
   {
-    UnembedParams up{o_part, ml, a.lens, (__nv_bfloat16*)a.out, BL, p.L, p.H, p.v, R,
-                     p.chunk, p.splits};
-    dim3 grid(p.v / 128, p.H, (BL + UN_ROWS - 1) / UN_ROWS);
+    MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits};
+    KernelTimer kt("merge_sm103", a.stream);
+    e = launch_pdl(merge_sm103, dim3(p.B * R), dim3(256), 0, a.stream, mp);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    GemmParams gp{(__nv_bfloat16*)a.out, BL, p.H, kLat, p.v, NBu};
     KernelTimer kt("unembed_sm103", a.stream);
-    unembed_sm103<<<grid, 128, un_smem, a.stream>>>(tm_wuv, up);
+    e = launch_pdl(swapab_gemm_sm103, dim3(p.v / 128, p.H, (BL + NBu - 1) / NBu), dim3(128),
+                   gemm_smem(kLat, NBu), a.stream, tm_wuv, tm_ol, gp);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

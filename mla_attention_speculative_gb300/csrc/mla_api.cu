@@ -226,6 +226,8 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     off = align256(off + nrow * f.splits * p->r * sizeof(float));
     f.off_ml = off;
     off = align256(off + nrow * f.splits * 2 * sizeof(float));
+    f.off_olat = off;
+    off = align256(off + nrow * p->r * 2);
     f.bytes = off;
   }
   p->ws_bytes = p->fast_ok && p->fast.bytes > p->generic.bytes ? p->fast.bytes : p->generic.bytes;

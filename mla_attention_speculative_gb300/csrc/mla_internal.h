@@ -15,7 +15,7 @@ namespace mla {
 struct SplitPlan {
   int chunk = 0;    // KV rows per piece (multiple of 64)
   int splits = 0;   // largest number of pieces of any sequence
-  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0;
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0;
   size_t bytes = 0;
 };
 
@@ -40,7 +40,7 @@ struct Plan {
   bool fast_ok = false;
   size_t ws_bytes = 0;
   // the layout of the family that runs (copied from generic or fast)
-  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0;
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0;
   void use(const SplitPlan& sp) {
     chunk = sp.chunk;
     splits = sp.splits;
@@ -48,6 +48,7 @@ struct Plan {
     off_opart = sp.off_opart;
     off_ml = sp.off_ml;
     off_exp = sp.off_exp;
+    off_olat = sp.off_olat;
   }
 };
 

@@ -133,6 +133,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible (a no-op when the kernel was not
+// launched as a dependent), and let the next grid start its prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {

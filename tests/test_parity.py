@@ -149,6 +149,22 @@ def test_contiguous_tail_poisoned():
         compare(out, want, torch.bfloat16, f"tail {mode}")
 
 
+@pytest.mark.parametrize("B,lens", [
+    (32, [192] * 32),                 # pieces of exactly three KV tiles (the pipeline depth)
+    (32, [130] * 32),                 # three tiles, ragged last one
+    (24, [263] * 24),                 # five tiles
+    (32, "mixed"),                    # pieces of 1..7 tiles across a multi-wave grid
+])
+def test_batched_short_pieces(B, lens):
+    if lens == "mixed":
+        rng = np.random.default_rng(5)
+        lens = [int(x) for x in rng.integers(8, 450, size=B)]
+    case = make_case(DSV3, 4, lens, seed=61, page_size=64)
+    out, branch = run_gpu(case, "absorbed")
+    heads = [0, 1, 64, 127]
+    compare(out[:, :, heads], oracle_out(case, heads=heads), torch.bfloat16, f"short B={B}")
+
+
 def test_repeat_call_is_deterministic():
     case = make_case(Geometry(H=16), 8, [1500], seed=5)
     d = device_tensors(case)
