@@ -179,17 +179,22 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
 constexpr int BM = 128;                 // query rows per tile
 constexpr int BN = 64;                  // cached positions per KV tile
 constexpr int STAGES = 3;
+constexpr int SOFTMAX_THREADS = 256;    // two warpgroups, 32 of a row's 64 scores each
+constexpr int ATTN_THREADS = 64 + SOFTMAX_THREADS;
 constexpr int Q_CHUNK = BM * 128;       // one 64-column bf16 chunk of the Q tile (128-B swizzle)
 constexpr int Q_ROPE = BM * 64;         // the 32 RoPE columns of this CTA (64-B swizzle)
 constexpr int KV_CHUNK = BN * 128;      // one 64-column bf16 chunk of a KV tile
 constexpr int KV_ROPE = BN * 64;        // 32 RoPE columns of a KV tile
-constexpr int X_BYTES = BM * BN * 2;    // the peer's partial scores, fp16 [128][64]
+constexpr int X_BYTES = BM * BN * 2;    // partial scores of a tile, fp16 [128][64]
 constexpr int OFF_Q = 0;
 constexpr int OFF_QR = OFF_Q + 4 * Q_CHUNK;
 constexpr int OFF_KV = OFF_QR + Q_ROPE;
 constexpr int KV_STAGE = 4 * KV_CHUNK + KV_ROPE;
-constexpr int OFF_X = OFF_KV + STAGES * KV_STAGE;
-constexpr int OFF_BAR = OFF_X + X_BYTES;
+constexpr int OFF_X = OFF_KV + STAGES * KV_STAGE;   // the peer's partial scores land here
+constexpr int OFF_STG = OFF_X + X_BYTES;            // this CTA's partial scores, outgoing
+constexpr int OFF_RED = OFF_STG + X_BYTES;          // row maxima of the two warpgroups
+constexpr int OFF_LS = OFF_RED + 2 * BM * 4;        // row sums, second warpgroup
+constexpr int OFF_BAR = OFF_LS + BM * 4;
 constexpr int ATTN_SMEM = OFF_BAR + 256 + 1024;     // + barriers + alignment slack
 constexpr uint32_t TM_O = 0;                        // O half: columns [0, 256)
 constexpr uint32_t TM_S = 256;                      // S / P buffers: 256 + 64*sb
@@ -217,45 +222,44 @@ enum {
   B_ODONE = 17, B_XFULL = 19, B_XFREE = 20, B_DRAIN = 21, B_COUNT = 22
 };
 
-// This CTA's partial scores of tile j from TMEM, scaled to log2-softmax units.
-__device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t lane_base, int j,
-                                             uint32_t bar_sfull0, uint32_t bar_sfree0,
-                                             float sl2, float (&s)[BN]) {
+// This thread's 32 partial scores of tile j (columns c0..c0+31 of this CTA's
+// share) from TMEM, scaled to log2-softmax units and rounded through fp16:
+// both CTAs add the same two rounded partials, so their sums agree bit for bit.
+__device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t lane_base, int c0,
+                                             int j, uint32_t bar_sfull0, uint32_t bar_sfree0,
+                                             float sl2, float (&s)[32]) {
   const int sb = j & (SBUF - 1);
   wait_or_fail(ok, bar_sfull0 + 8 * sb, (j / SBUF) & 1, 20);
   tc_fence_after();
-  uint32_t v[BN];
-#pragma unroll
-  for (int k = 0; k < BN / 16; ++k)
-    tmem_ld16(tmem + lane_base + TM_S + sb * BN + 16 * k, *(uint32_t(*)[16])(v + 16 * k));
+  uint32_t v[32];
+  tmem_ld16(tmem + lane_base + TM_S + sb * BN + c0, *(uint32_t(*)[16])(v));
+  tmem_ld16(tmem + lane_base + TM_S + sb * BN + c0 + 16, *(uint32_t(*)[16])(v + 16));
   tmem_wait_ld();
 #pragma unroll
-  for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(v[e]) * sl2;
+  for (int e = 0; e < 32; ++e) s[e] = __half2float(__float2half_rn(__uint_as_float(v[e]) * sl2));
   tc_fence_before();
   mbar_arrive(bar_sfree0 + 8 * sb);
 }
 
-// Round this row's partial scores to fp16 (both CTAs add the same two rounded
-// partials, so their sums agree bit for bit) and send them into the peer's
-// exchange buffer; each 16-byte store counts itself off the peer's barrier.
-__device__ __forceinline__ void send_partial(uint32_t peer_x, uint32_t peer_xfull, int q,
-                                             float (&s)[BN]) {
+// Row q, columns c0..c0+31 as fp16 into a [128][64] exchange tile (16-byte
+// chunks XOR-swizzled by row so the 32 rows of a warp hit distinct banks).
+__device__ __forceinline__ void put_partial(uint32_t tile, int q, int c0, const float (&s)[32]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int k = 0; k < 4; ++k) {
     uint32_t h[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const __half2 v = __floats2half2_rn(s[8 * c + 2 * e], s[8 * c + 2 * e + 1]);
+      const __half2 v = __floats2half2_rn(s[8 * k + 2 * e], s[8 * k + 2 * e + 1]);
       h[e] = *reinterpret_cast<const uint32_t*>(&v);
-      const float2 back = __half22float2(v);
-      s[8 * c + 2 * e] = back.x;
-      s[8 * c + 2 * e + 1] = back.y;
     }
-    st_async_v4(peer_x + q * 128 + ((c ^ (q & 7)) << 4), h[0], h[1], h[2], h[3], peer_xfull);
+    const int c = (c0 >> 3) + k;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + q * 128 + ((c ^ (q & 7)) << 4)),
+                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                 : "memory");
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     absorbed_attn_sm103(const __grid_constant__ CUtensorMap tm_ql,
                         const __grid_constant__ CUtensorMap tm_qr,
                         const __grid_constant__ CUtensorMap tm_ckv,
@@ -282,6 +286,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t sQ = smem_u32(smem + OFF_Q), sQR = smem_u32(smem + OFF_QR);
   const uint32_t sKV = smem_u32(smem + OFF_KV), sX = smem_u32(smem + OFF_X);
+  const uint32_t sStg = smem_u32(smem + OFF_STG);
+  float* red = (float*)(smem + OFF_RED);
+  float* lsum = (float*)(smem + OFF_LS);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
@@ -291,15 +298,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     }
     for (int s = 0; s < SBUF; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SFREE + s), 128);
+      mbar_init(bar(B_SFREE + s), SOFTMAX_THREADS);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(bar(B_ODONE + s), 1);
-    for (int s = 0; s < 2; ++s) mbar_init(bar(B_PFULL + s), 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_PFULL + s), SOFTMAX_THREADS);
+      mbar_init(bar(B_ODONE + s), 1);
+    }
     mbar_init(bar(B_XFULL), 1);
     mbar_init(bar(B_XFREE), 1);
     mbar_init(bar(B_DRAIN), 1);
     fence_mbar_init();
-    // arm the exchange barrier for tile 0 (the peer's stores count it down)
+    // arm the exchange barrier for tile 0 (the peer's bulk copy counts it down)
     if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
   }
   if (warp == 1) tmem_alloc(smem_u32(slot), 512);
@@ -355,9 +364,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
-      wait_or_fail(ok, bar(B_QFULL), 0, 11);
+      // descriptors are built once; a byte offset o adds o >> 4 to the start field
+      const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dqr = sdesc_sw64(sQR, 512);
+      const uint64_t dk = sdesc_sw128(sKV, 16, 1024);
+      const uint64_t dkr = sdesc_sw64(sKV + 4 * KV_CHUNK, 512);
+      const uint64_t dv = sdesc_sw128(sKV, KV_CHUNK, 1024);
       const uint32_t id_s = idesc_bf16(BM, BN, 0, 0);
       const uint32_t id_o = idesc_bf16(BM, 256, 0, 1);
+      wait_or_fail(ok, bar(B_QFULL), 0, 11);
       for (int i = 0; i <= ntiles && ok; ++i) {
         if (i < ntiles) {
           // S(i) = Q . K(i)^T over this CTA's 256 latent + 32 RoPE columns
@@ -366,15 +381,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           if (i >= SBUF) wait_or_fail(ok, bar(B_SFREE + sb), ((i - SBUF) / SBUF) & 1, 13);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t st = sKV + s * KV_STAGE;
+          const uint64_t soff = (uint64_t)(s * (KV_STAGE >> 4));
           const uint32_t d = tmem + TM_S + sb * BN;
+#pragma unroll
           for (int c = 0; c < 4; ++c)
+#pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              mma_bf16(d, sdesc_sw128(sQ + c * Q_CHUNK + ks * 32, 16, 1024),
-                       sdesc_sw128(st + c * KV_CHUNK + ks * 32, 16, 1024), id_s, (c | ks) != 0);
-          for (int ks = 0; ks < 2; ++ks)
-            mma_bf16(d, sdesc_sw64(sQR + ks * 32, 512), sdesc_sw64(st + 4 * KV_CHUNK + ks * 32, 512),
-                     id_s, 1);
+              mma_bf16(d, dq + ((c * Q_CHUNK + ks * 32) >> 4),
+                       dk + soff + ((c * KV_CHUNK + ks * 32) >> 4), id_s, (c | ks) != 0);
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) mma_bf16(d, dqr + 2 * ks, dkr + soff + 2 * ks, id_s, 1);
           mma_commit(bar(B_SFULL + sb));
         }
         if (i >= 1) {
@@ -384,10 +400,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           wait_or_fail(ok, bar(B_PFULL + (j & 1)), (j >> 1) & 1, 14);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t st = sKV + sj * KV_STAGE;
+          const uint64_t soff = (uint64_t)(sj * (KV_STAGE >> 4));
+#pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_tmem_a(tmem + TM_O, tmem + TM_S + pb * BN + ks * 8,
-                            sdesc_sw128(st + ks * 2048, KV_CHUNK, 1024), id_o, (j > 0 || ks > 0));
+            mma_bf16_tmem_a(tmem + TM_O, tmem + TM_S + pb * BN + ks * 8, dv + soff + ks * 128, id_o,
+                            (j > 0 || ks > 0));
           mma_commit(bar(B_ODONE + (j & 1)));
           mma_commit(bar(B_KVEMPTY + sj));
         }
@@ -397,11 +414,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       mbar_wait(bar(B_DRAIN), 0);
     }
   } else {
-    // ------------------------------------------------- softmax warpgroup
-    // Tile i's scores are finished (own + peer partial) while tile i+1's
-    // partial is already on its way to the peer.  P(i) goes back into the TMEM
-    // columns S(i) came from; S(i+4) reuses them, long after P.V(i) has run.
+    // ------------------------------------------------- softmax warpgroups
+    // Two warpgroups: thread (wg, q) owns row q, score columns 32wg..32wg+31 and
+    // O columns 128wg..128wg+127.  Tile i's scores are finished (own + peer
+    // partial) while tile i+1's partial is already on its way to the peer (one
+    // bulk copy of the staged tile).  P(i) goes back into the TMEM columns S(i)
+    // came from; S(i+4) reuses them, long after P.V(i) has run.
+    const int wg = (warp - 2) >> 2;
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const int c0 = 32 * wg;
     const int sm_tid = threadIdx.x - 64;
     const int row = row0 + q;
     const int l = min(row, p.R - 1) / p.H;
@@ -412,30 +433,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const uint32_t peer_xfree = mapa(bar(B_XFREE), peer);
     bool ok = true;
     int armed = ntiles > 0 ? 1 : 0, received = 0;  // exchange phases armed / completed
-    float m_run = -INFINITY, l_run = 0.f;
-    float s[BN];
+    float m_run = -INFINITY, l_part = 0.f;
+    float s[32];
     if (ntiles > 0) {
-      load_partial(ok, tmem, lane_base, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
-      if (ok) send_partial(peer_x, peer_xfull, q, s);
+      load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
+      put_partial(sStg, q, c0, s);
+      fence_async_shared();
+      named_bar_sync(1, SOFTMAX_THREADS);
+      if (sm_tid == 0 && ok) bulk_copy_to_peer(peer_x, sStg, X_BYTES, peer_xfull);
     }
     for (int i = 0; i < ntiles; ++i) {
-      // finish tile i's scores with the peer's partial
+      const int t0 = kv0 + i * BN;
+      // finish tile i's scores with the peer's partial; causal verify mask
       wait_cluster_or_fail(ok, bar(B_XFULL), i & 1, 22);
       if (ok) received = i + 1;
+      float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int k = 0; k < 4; ++k) {
         uint32_t h[4];
+        const int c = (c0 >> 3) + k;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
                      : "r"(sX + q * 128 + ((c ^ (q & 7)) << 4)));
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
-          s[8 * c + 2 * e] += f.x;
-          s[8 * c + 2 * e + 1] += f.y;
+          const int j = 8 * k + 2 * e;
+          s[j] = (t0 + c0 + j <= last_t) ? s[j] + f.x : -INFINITY;
+          s[j + 1] = (t0 + c0 + j + 1 <= last_t) ? s[j + 1] + f.y : -INFINITY;
+          mt = fmaxf(mt, fmaxf(s[j], s[j + 1]));
         }
       }
-      named_bar_sync(1, 128);  // every row has read the exchange buffer
+      red[wg * BM + q] = mt;
+      named_bar_sync(1, SOFTMAX_THREADS);  // exchange tile read by all; row maxima visible
+      mt = fmaxf(mt, red[(1 - wg) * BM + q]);
       if (sm_tid == 0 && ok) {
         if (i + 1 < ntiles) {
           mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);  // arm tile i+1
@@ -444,19 +475,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         mbar_arrive_remote(peer_xfree);  // the peer may now send tile i+1
       }
       // start tile i+1's exchange
-      float sn[BN];
+      float sn[32];
       if (i + 1 < ntiles) {
-        load_partial(ok, tmem, lane_base, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn);
-        wait_cluster_or_fail(ok, bar(B_XFREE), i & 1, 21);  // the peer has read my tile i
-        if (ok) send_partial(peer_x, peer_xfull, q, sn);
-      }
-      // causal verify mask and tile maximum (scores are in log2 units already)
-      const int t0 = kv0 + i * BN;
-      float mt = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < BN; ++j) {
-        s[j] = (t0 + j <= last_t) ? s[j] : -INFINITY;
-        mt = fmaxf(mt, s[j]);
+        load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn);
+        if (sm_tid == 0) {
+          wait_cluster_or_fail(ok, bar(B_XFREE), i & 1, 21);  // the peer has read my tile i
+          bulk_wait_read();                                  // my staging tile is free
+        }
+        named_bar_sync(1, SOFTMAX_THREADS);
+        put_partial(sStg, q, c0, sn);
+        fence_async_shared();
+        named_bar_sync(1, SOFTMAX_THREADS);
+        if (sm_tid == 0 && ok) bulk_copy_to_peer(peer_x, sStg, X_BYTES, peer_xfull);
       }
       // lazy rescale: move the running max only when it grows by more than 2^8;
       // O must then hold every earlier P.V
@@ -466,38 +496,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       if (i > 0 && __any_sync(0xffffffffu, need)) {
         wait_or_fail(ok, bar(B_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, 23);
         tc_fence_after();
-        for (int c = 0; c < 256; c += 16) {
+        for (int c = 0; c < 128; c += 16) {
           uint32_t v[16];
-          tmem_ld16(tmem + lane_base + TM_O + c, v);
+          tmem_ld16(tmem + lane_base + TM_O + 128 * wg + c, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * factor);
-          tmem_st16(tmem + lane_base + TM_O + c, v);
+          tmem_st16(tmem + lane_base + TM_O + 128 * wg + c, v);
         }
         tmem_wait_st();
       }
-      l_run *= factor;
+      l_part *= factor;
       m_run = m_new;
-      // P = 2^(s - m) as bf16 pairs into the first 32 columns of S buffer i%4
+      // P = 2^(s - m) as bf16 pairs into columns 16wg..16wg+15 of S buffer i%4
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       float rs = 0.f;
-      uint32_t pk[BN / 2];
+      uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < BN / 2; ++e) {
+      for (int e = 0; e < 16; ++e) {
         const float a = ex2(s[2 * e] - m_use);
         const float d = ex2(s[2 * e + 1] - m_use);
         rs += a + d;
         pk[e] = pack_bf16(a, d);
       }
-      l_run += rs;
-      tmem_st32(tmem + lane_base + TM_S + (i & (SBUF - 1)) * BN, pk);
+      l_part += rs;
+      tmem_st16b(tmem + lane_base + TM_S + (i & (SBUF - 1)) * BN + 16 * wg, pk);
       // positions at or past T in the last tile: zero their value rows (they may hold
       // anything, and 0 * NaN would poison the accumulator)
       if (t0 + BN > T) {
         const int z0 = max(T - t0, 0);
         const uint32_t st = sKV + (i % STAGES) * KV_STAGE;
         const int units = (BN - z0) * 8;  // 16-byte units per 128-byte row
-        for (int u = q; u < 4 * units; u += 128) {
+        for (int u = sm_tid; u < 4 * units; u += SOFTMAX_THREADS) {
           const int c = u / units, w = u - c * units;
           const uint32_t addr = st + c * KV_CHUNK + (z0 + w / 8) * 128 + (w & 7) * 16;
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
@@ -509,11 +539,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + (i & 1)));
 #pragma unroll
-      for (int e = 0; e < BN; ++e) s[e] = sn[e];
+      for (int e = 0; e < 32; ++e) s[e] = sn[e];
     }
     // after a failure, let an armed exchange phase finish (or time out) so no
-    // store from the peer is still landing when this CTA exits
+    // copy from the peer is still landing when this CTA exits
     if (sm_tid == 0 && received < armed) mbar_wait_cluster(bar(B_XFULL), received & 1);
+    if (sm_tid == 0) bulk_wait_read();
     // ---------------------------------------------------------------- epilogue
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
     pdl_wait();                // the partials may still be read by an earlier merge
@@ -521,11 +552,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     tc_fence_after();
     const bool live = row < p.R;
     float* op = p.o_part + (((size_t)b * p.splits + split) * p.R + (live ? row : 0)) * kLat +
-                rank * 256;
-    for (int c = 0; c < 256; c += 16) {
+                rank * 256 + 128 * wg;
+    for (int c = 0; c < 128; c += 16) {
       uint32_t v[16];
       if (ntiles > 0) {
-        tmem_ld16(tmem + lane_base + TM_O + c, v);
+        tmem_ld16(tmem + lane_base + TM_O + 128 * wg + c, v);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -539,10 +570,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                           __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
       }
     }
-    if (live && rank == 0) {
+    if (wg == 1) lsum[q] = l_part;
+    named_bar_sync(1, SOFTMAX_THREADS);
+    if (live && rank == 0 && wg == 0) {
       float* mlp = p.ml + (((size_t)b * p.splits + split) * p.R + row) * 2;
       mlp[0] = m_run == -INFINITY ? -FLT_MAX : m_run;
-      mlp[1] = l_run;
+      mlp[1] = l_part + lsum[q];
     }
   }
   tc_fence_before();
@@ -714,7 +747,8 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.o_part = o_part;
     ap.ml = ml;
     KernelTimer kt("absorbed_attn_sm103", a.stream);
-    e = launch_pdl(absorbed_attn_sm103, dim3(2 * ((R + BM - 1) / BM), p.splits, p.B), dim3(192),
+    e = launch_pdl(absorbed_attn_sm103, dim3(2 * ((R + BM - 1) / BM), p.splits, p.B),
+                   dim3(ATTN_THREADS),
                    ATTN_SMEM, a.stream, tm_ql, tm_qr, tm_ckv, tm_kr, ap);
     if (e != cudaSuccess) return e;
   }
