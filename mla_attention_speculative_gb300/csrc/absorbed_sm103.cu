@@ -178,36 +178,43 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
 // =========================================================================
 constexpr int BM = 128;                 // query rows per tile
 constexpr int BN = 64;                  // cached positions per KV tile
-constexpr int STAGES = 3;
+constexpr int STAGES = 4;
 constexpr int SOFTMAX_THREADS = 256;    // two warpgroups, 32 of a row's 64 scores each
 constexpr int ATTN_THREADS = 64 + SOFTMAX_THREADS;
-constexpr int Q_CHUNK = BM * 128;       // one 64-column bf16 chunk of the Q tile (128-B swizzle)
-constexpr int Q_ROPE = BM * 64;         // the 32 RoPE columns of this CTA (64-B swizzle)
+constexpr int Q_ROPE = BM * 64;         // the 32 RoPE columns of this CTA's Q rows (64-B swizzle)
 constexpr int KV_CHUNK = BN * 128;      // one 64-column bf16 chunk of a KV tile
 constexpr int KV_ROPE = BN * 64;        // 32 RoPE columns of a KV tile
+constexpr int P_TILE = BM * 128;        // one bf16 P tile (128 rows x 64 positions)
 constexpr int X_BYTES = BM * BN * 2;    // partial scores of a tile, fp16 [128][64]
-constexpr int OFF_Q = 0;
-constexpr int OFF_QR = OFF_Q + 4 * Q_CHUNK;
+constexpr int OFF_QR = 0;
 constexpr int OFF_KV = OFF_QR + Q_ROPE;
 constexpr int KV_STAGE = 4 * KV_CHUNK + KV_ROPE;
-constexpr int OFF_X = OFF_KV + STAGES * KV_STAGE;   // the peer's partial scores land here
+constexpr int OFF_P = OFF_KV + STAGES * KV_STAGE;   // two P buffers
+constexpr int OFF_X = OFF_P + 2 * P_TILE;           // the peer's partial scores land here
 constexpr int OFF_STG = OFF_X + X_BYTES;            // this CTA's partial scores, outgoing
 constexpr int OFF_RED = OFF_STG + X_BYTES;          // row maxima of the two warpgroups
 constexpr int OFF_LS = OFF_RED + 2 * BM * 4;        // row sums, second warpgroup
 constexpr int OFF_BAR = OFF_LS + BM * 4;
 constexpr int ATTN_SMEM = OFF_BAR + 256 + 1024;     // + barriers + alignment slack
-constexpr uint32_t TM_O = 0;                        // O half: columns [0, 256)
-constexpr uint32_t TM_S = 256;                      // S / P buffers: 256 + 64*sb
-constexpr int SBUF = 4;                             // S / P buffers (TMEM columns 256..511)
-static_assert(OFF_KV % 1024 == 0 && KV_STAGE % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+// Tensor memory: O half [0,256) fp32; this CTA's 256 latent query columns as
+// bf16 pairs [256,384) (the A operand of the score MMAs); S buffers [384,512).
+constexpr uint32_t TM_O = 0;
+constexpr uint32_t TM_QL = 256;
+constexpr uint32_t TM_S = 384;
+constexpr int SBUF = 2;
+constexpr int S_AHEAD = 3;                          // scores run this many tiles ahead of P.V
+static_assert(OFF_KV % 1024 == 0 && KV_STAGE % 1024 == 0 && OFF_P % 1024 == 0,
+              "swizzle atoms need 1 KiB alignment");
 static_assert(ATTN_SMEM <= 232448, "shared memory per CTA");
 
 struct AttnParams {
   const int32_t* lens;
   const int32_t* page_table;
+  const __nv_bfloat16* q_lat;  // [B*R, 512]
   int page_size, max_pages;
   long long seq_stride;
   int L, H, R;        // R = L*H query rows per sequence
+  int B;
   int chunk, splits;  // KV rows per split (multiple of 64), splits per sequence (max)
   float sl2;          // softmax scale * log2(e)
   float* o_part;      // [B, splits, R, 512]
@@ -215,19 +222,20 @@ struct AttnParams {
 };
 
 // Barrier slots.  Every barrier that is waited on by parity alone has enough
-// copies that it cannot complete twice before its waiter looks: P-full and
-// O-done alternate by tile parity, S buffers by tile % 4.
+// copies that it cannot complete twice before its waiter looks.
 enum {
-  B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 4, B_SFULL = 7, B_SFREE = 11, B_PFULL = 15,
-  B_ODONE = 17, B_XFULL = 19, B_XFREE = 20, B_DRAIN = 21, B_COUNT = 22
+  B_QFULL = 0, B_QTMEM = 1, B_KVFULL = 2, B_KVEMPTY = 6, B_SFULL = 10, B_SFREE = 12,
+  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 19, B_DRAIN = 20, B_COUNT = 21
 };
 
 // This thread's 32 partial scores of tile j (columns c0..c0+31 of this CTA's
-// share) from TMEM, scaled to log2-softmax units and rounded through fp16:
-// both CTAs add the same two rounded partials, so their sums agree bit for bit.
+// share) from TMEM, scaled to log2-softmax units and rounded to fp16 pairs:
+// `h` is what goes to the peer, `s` the same rounded values in fp32.  Both
+// CTAs add the same two rounded partials, so their sums agree bit for bit.
+// (Packed conversions: the scalar ones would crowd the pipe the exponentials need.)
 __device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t lane_base, int c0,
                                              int j, uint32_t bar_sfull0, uint32_t bar_sfree0,
-                                             float sl2, float (&s)[32]) {
+                                             float sl2, float (&s)[32], uint32_t (&h)[16]) {
   const int sb = j & (SBUF - 1);
   wait_or_fail(ok, bar_sfull0 + 8 * sb, (j / SBUF) & 1, 20);
   tc_fence_after();
@@ -236,32 +244,32 @@ __device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t l
   tmem_ld16(tmem + lane_base + TM_S + sb * BN + c0 + 16, *(uint32_t(*)[16])(v + 16));
   tmem_wait_ld();
 #pragma unroll
-  for (int e = 0; e < 32; ++e) s[e] = __half2float(__float2half_rn(__uint_as_float(v[e]) * sl2));
+  for (int e = 0; e < 16; ++e) {
+    const __half2 x = __floats2half2_rn(__uint_as_float(v[2 * e]) * sl2,
+                                        __uint_as_float(v[2 * e + 1]) * sl2);
+    h[e] = *reinterpret_cast<const uint32_t*>(&x);
+    const float2 f = __half22float2(x);
+    s[2 * e] = f.x;
+    s[2 * e + 1] = f.y;
+  }
   tc_fence_before();
   mbar_arrive(bar_sfree0 + 8 * sb);
 }
 
-// Row q, columns c0..c0+31 as fp16 into a [128][64] exchange tile (16-byte
-// chunks XOR-swizzled by row so the 32 rows of a warp hit distinct banks).
-__device__ __forceinline__ void put_partial(uint32_t tile, int q, int c0, const float (&s)[32]) {
+// Row q's 16 fp16 pairs (columns c0..c0+31) into a [128][64] exchange tile
+// (16-byte chunks XOR-swizzled by row so the 32 rows of a warp hit distinct banks).
+__device__ __forceinline__ void put_partial(uint32_t tile, int q, int c0, const uint32_t (&h)[16]) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint32_t h[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __half2 v = __floats2half2_rn(s[8 * k + 2 * e], s[8 * k + 2 * e + 1]);
-      h[e] = *reinterpret_cast<const uint32_t*>(&v);
-    }
     const int c = (c0 >> 3) + k;
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + q * 128 + ((c ^ (q & 7)) << 4)),
-                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                 "r"(h[4 * k]), "r"(h[4 * k + 1]), "r"(h[4 * k + 2]), "r"(h[4 * k + 3])
                  : "memory");
   }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
-    absorbed_attn_sm103(const __grid_constant__ CUtensorMap tm_ql,
-                        const __grid_constant__ CUtensorMap tm_qr,
+    absorbed_attn_sm103(const __grid_constant__ CUtensorMap tm_qr,
                         const __grid_constant__ CUtensorMap tm_ckv,
                         const __grid_constant__ CUtensorMap tm_kr, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -284,23 +292,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
   uint32_t* slot = (uint32_t*)(bars + 24);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t sQ = smem_u32(smem + OFF_Q), sQR = smem_u32(smem + OFF_QR);
-  const uint32_t sKV = smem_u32(smem + OFF_KV), sX = smem_u32(smem + OFF_X);
+  const uint32_t sQR = smem_u32(smem + OFF_QR), sKV = smem_u32(smem + OFF_KV);
+  const uint32_t sP = smem_u32(smem + OFF_P), sX = smem_u32(smem + OFF_X);
   const uint32_t sStg = smem_u32(smem + OFF_STG);
   float* red = (float*)(smem + OFF_RED);
   float* lsum = (float*)(smem + OFF_LS);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QTMEM), SOFTMAX_THREADS);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(B_KVFULL + s), 1);
       mbar_init(bar(B_KVEMPTY + s), 1);
     }
-    for (int s = 0; s < SBUF; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
       mbar_init(bar(B_SFREE + s), SOFTMAX_THREADS);
-    }
-    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_PFULL + s), SOFTMAX_THREADS);
       mbar_init(bar(B_ODONE + s), 1);
     }
@@ -322,7 +329,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
-      prefetch_tmap(&tm_ql);
       prefetch_tmap(&tm_ckv);
       const int qrow = b * p.R + row0;
       auto load_kv = [&](int i) {
@@ -339,14 +345,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
                       (int)y);
         tma_load_2d(st + 4 * KV_CHUNK, &tm_kr, bar(B_KVFULL + s), (int)rank * 32, (int)y);
       };
-      // the first stages do not depend on the preceding kernel ...
+      // the cache does not depend on the preceding kernel: start every stage now
       const int pre = min(ntiles, STAGES);
       for (int i = 0; i < pre; ++i) load_kv(i);
-      // ... q_lat does (the fold writes it)
+      // q_rope is a call input; it still waits so no read overtakes the predecessor
       pdl_wait();
-      mbar_arrive_expect_tx(bar(B_QFULL), 4 * Q_CHUNK + Q_ROPE);
-      for (int c = 0; c < 4; ++c)
-        tma_load_2d(sQ + c * Q_CHUNK, &tm_ql, bar(B_QFULL), (int)(4 * rank + c) * 64, qrow);
+      mbar_arrive_expect_tx(bar(B_QFULL), Q_ROPE);
       tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
       int issued = pre;
       for (int i = STAGES; i < ntiles; ++i) {
@@ -362,52 +366,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
+    // Order: S(0), S(1), S(2), then for each j: P.V(j), S(j+3).  Scores run
+    // three tiles ahead of P.V, so the softmax never waits on the tensor pipe
+    // for them; S(j+3) reuses the buffer of S(j+1), read during softmax(j).
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
-      // descriptors are built once; a byte offset o adds o >> 4 to the start field
-      const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dqr = sdesc_sw64(sQR, 512);
       const uint64_t dk = sdesc_sw128(sKV, 16, 1024);
       const uint64_t dkr = sdesc_sw64(sKV + 4 * KV_CHUNK, 512);
       const uint64_t dv = sdesc_sw128(sKV, KV_CHUNK, 1024);
+      const uint64_t dp = sdesc_sw128(sP, 16, 1024);
       const uint32_t id_s = idesc_bf16(BM, BN, 0, 0);
       const uint32_t id_o = idesc_bf16(BM, 256, 0, 1);
       wait_or_fail(ok, bar(B_QFULL), 0, 11);
-      for (int i = 0; i <= ntiles && ok; ++i) {
-        if (i < ntiles) {
-          // S(i) = Q . K(i)^T over this CTA's 256 latent + 32 RoPE columns
-          const int s = i % STAGES, sb = i & (SBUF - 1);
-          wait_or_fail(ok, bar(B_KVFULL + s), (i / STAGES) & 1, 12);
-          if (i >= SBUF) wait_or_fail(ok, bar(B_SFREE + sb), ((i - SBUF) / SBUF) & 1, 13);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t soff = (uint64_t)(s * (KV_STAGE >> 4));
-          const uint32_t d = tmem + TM_S + sb * BN;
+      wait_or_fail(ok, bar(B_QTMEM), 0, 15);
+      auto issue_s = [&](int i) {
+        // S(i) = Q . K(i)^T over this CTA's 256 latent (Q from TMEM) + 32 RoPE columns
+        const int s = i % STAGES, sb = i & (SBUF - 1);
+        wait_or_fail(ok, bar(B_KVFULL + s), (i / STAGES) & 1, 12);
+        if (i >= SBUF) wait_or_fail(ok, bar(B_SFREE + sb), ((i - SBUF) / SBUF) & 1, 13);
+        if (!ok) return;
+        tc_fence_after();
+        const uint64_t soff = (uint64_t)(s * (KV_STAGE >> 4));
+        const uint32_t d = tmem + TM_S + sb * BN;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+        for (int kk = 0; kk < 16; ++kk)
+          mma_bf16_tmem_a(d, tmem + TM_QL + 8 * kk,
+                          dk + soff + (((kk >> 2) * KV_CHUNK + (kk & 3) * 32) >> 4), id_s, kk != 0);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_bf16(d, dq + ((c * Q_CHUNK + ks * 32) >> 4),
-                       dk + soff + ((c * KV_CHUNK + ks * 32) >> 4), id_s, (c | ks) != 0);
+        for (int ks = 0; ks < 2; ++ks) mma_bf16(d, dqr + 2 * ks, dkr + soff + 2 * ks, id_s, 1);
+        mma_commit(bar(B_SFULL + sb));
+      };
+      for (int i = 0; i < min(ntiles, S_AHEAD) && ok; ++i) issue_s(i);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        // O += P(j) . V(j) over this CTA's 256 latent columns of the KV tile
+        const int sj = j % STAGES, pb = j & 1;
+        wait_or_fail(ok, bar(B_PFULL + pb), (j >> 1) & 1, 14);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t soff = (uint64_t)(sj * (KV_STAGE >> 4));
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) mma_bf16(d, dqr + 2 * ks, dkr + soff + 2 * ks, id_s, 1);
-          mma_commit(bar(B_SFULL + sb));
-        }
-        if (i >= 1) {
-          // O += P(j) . V(j): P from TMEM (bf16 pairs over S buffer j%4), V = this
-          // CTA's 256 latent columns of the KV tile
-          const int j = i - 1, sj = j % STAGES, pb = j & (SBUF - 1);
-          wait_or_fail(ok, bar(B_PFULL + (j & 1)), (j >> 1) & 1, 14);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t soff = (uint64_t)(sj * (KV_STAGE >> 4));
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_tmem_a(tmem + TM_O, tmem + TM_S + pb * BN + ks * 8, dv + soff + ks * 128, id_o,
-                            (j > 0 || ks > 0));
-          mma_commit(bar(B_ODONE + (j & 1)));
-          mma_commit(bar(B_KVEMPTY + sj));
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + TM_O, dp + pb * (P_TILE >> 4) + 2 * ks, dv + soff + ks * 128, id_o,
+                   (j > 0 || ks > 0));
+        mma_commit(bar(B_ODONE + pb));
+        mma_commit(bar(B_KVEMPTY + sj));
+        if (j + S_AHEAD < ntiles) issue_s(j + S_AHEAD);
       }
       // every MMA issued here has finished before tensor memory is released
       mma_commit(bar(B_DRAIN));
@@ -418,8 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // Two warpgroups: thread (wg, q) owns row q, score columns 32wg..32wg+31 and
     // O columns 128wg..128wg+127.  Tile i's scores are finished (own + peer
     // partial) while tile i+1's partial is already on its way to the peer (one
-    // bulk copy of the staged tile).  P(i) goes back into the TMEM columns S(i)
-    // came from; S(i+4) reuses them, long after P.V(i) has run.
+    // bulk copy of the staged tile).
     const int wg = (warp - 2) >> 2;
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
     const int c0 = 32 * wg;
@@ -436,15 +439,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     float m_run = -INFINITY, l_part = 0.f;
     float s[32];
     if (ntiles > 0) {
-      load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
-      put_partial(sStg, q, c0, s);
+      // this CTA's latent query columns into TMEM as bf16 pairs (the fold wrote them)
+      pdl_wait();
+      const long long grow = (long long)b * p.R + row;
+      const bool have = grow < (long long)p.B * p.R;
+      const uint4* src = (const uint4*)(p.q_lat + (have ? grow : 0) * kLat + 256 * rank + 128 * wg);
+      uint32_t v[64];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint4 x = have ? src[k] : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * k] = x.x;
+        v[4 * k + 1] = x.y;
+        v[4 * k + 2] = x.z;
+        v[4 * k + 3] = x.w;
+      }
+      tmem_st32(tmem + lane_base + TM_QL + 64 * wg, *(const uint32_t(*)[32])(v));
+      tmem_st32(tmem + lane_base + TM_QL + 64 * wg + 32, *(const uint32_t(*)[32])(v + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_QTMEM));
+      uint32_t h0[16];
+      load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s, h0);
+      put_partial(sStg, q, c0, h0);
       fence_async_shared();
       named_bar_sync(1, SOFTMAX_THREADS);
       if (sm_tid == 0 && ok) bulk_copy_to_peer(peer_x, sStg, X_BYTES, peer_xfull);
     }
-    for (int i = 0; i < ntiles; ++i) {
+    // One tile of the softmax; `s` holds tile i's own (rounded) partial on entry
+    // and `sn` receives tile i+1's.  Called with the two arrays alternating so
+    // the registers swap roles instead of being copied.
+    auto softmax_tile = [&](int i, float (&s)[32], float (&sn)[32]) {
       const int t0 = kv0 + i * BN;
-      // finish tile i's scores with the peer's partial; causal verify mask
+      // finish tile i's scores with the peer's partial; the causal verify mask
+      // only matters on tiles that reach past the first row's last position
+      const bool edge = t0 + BN - 1 > T - p.L;
       wait_cluster_or_fail(ok, bar(B_XFULL), i & 1, 22);
       if (ok) received = i + 1;
       float mt = -INFINITY;
@@ -459,11 +487,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
           const int j = 8 * k + 2 * e;
-          s[j] = (t0 + c0 + j <= last_t) ? s[j] + f.x : -INFINITY;
-          s[j + 1] = (t0 + c0 + j + 1 <= last_t) ? s[j + 1] + f.y : -INFINITY;
-          mt = fmaxf(mt, fmaxf(s[j], s[j + 1]));
+          s[j] += f.x;
+          s[j + 1] += f.y;
         }
       }
+      if (edge) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[j] = (t0 + c0 + j <= last_t) ? s[j] : -INFINITY;
+      }
+      float m2[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+      for (int j = 4; j < 32; ++j) m2[j & 3] = fmaxf(m2[j & 3], s[j]);
+      mt = fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3]));
       red[wg * BM + q] = mt;
       named_bar_sync(1, SOFTMAX_THREADS);  // exchange tile read by all; row maxima visible
       mt = fmaxf(mt, red[(1 - wg) * BM + q]);
@@ -472,18 +507,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
           mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);  // arm tile i+1
           ++armed;
         }
-        mbar_arrive_remote(peer_xfree);  // the peer may now send tile i+1
+        // the peer may now send tile i+1: every read of the exchange tile has
+        // returned (its values were used before the bar.sync), so no fence
+        mbar_arrive_remote_relaxed(peer_xfree);
       }
       // start tile i+1's exchange
-      float sn[32];
       if (i + 1 < ntiles) {
-        load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn);
+        uint32_t hn[16];
+        load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn, hn);
         if (sm_tid == 0) {
           wait_cluster_or_fail(ok, bar(B_XFREE), i & 1, 21);  // the peer has read my tile i
           bulk_wait_read();                                  // my staging tile is free
         }
         named_bar_sync(1, SOFTMAX_THREADS);
-        put_partial(sStg, q, c0, sn);
+        put_partial(sStg, q, c0, hn);
         fence_async_shared();
         named_bar_sync(1, SOFTMAX_THREADS);
         if (sm_tid == 0 && ok) bulk_copy_to_peer(peer_x, sStg, X_BYTES, peer_xfull);
@@ -508,19 +545,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       }
       l_part *= factor;
       m_run = m_new;
-      // P = 2^(s - m) as bf16 pairs into columns 16wg..16wg+15 of S buffer i%4
+      // P = 2^(s - m) in bf16 into P buffer i&1 (K-major, 128-byte swizzled rows),
+      // which P.V(i-2) has finished reading
+      if (i >= 2) wait_or_fail(ok, bar(B_ODONE + (i & 1)), ((i - 2) >> 1) & 1, 24);
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      float rs = 0.f;
-      uint32_t pk[16];
+      float rs[2] = {0.f, 0.f};
+      const uint32_t prow = sP + (i & 1) * P_TILE + q * 128;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float a = ex2(s[2 * e] - m_use);
-        const float d = ex2(s[2 * e + 1] - m_use);
-        rs += a + d;
-        pk[e] = pack_bf16(a, d);
+      for (int k = 0; k < 4; ++k) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = ex2(s[8 * k + 2 * e] - m_use);
+          const float d = ex2(s[8 * k + 2 * e + 1] - m_use);
+          rs[0] += a;
+          rs[1] += d;
+          pk[e] = pack_bf16(a, d);
+        }
+        const int c = (c0 >> 3) + k;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + (((c ^ q) & 7) << 4)),
+                     "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                     : "memory");
       }
-      l_part += rs;
-      tmem_st16b(tmem + lane_base + TM_S + (i & (SBUF - 1)) * BN + 16 * wg, pk);
+      l_part += rs[0] + rs[1];
       // positions at or past T in the last tile: zero their value rows (they may hold
       // anything, and 0 * NaN would poison the accumulator)
       if (t0 + BN > T) {
@@ -533,13 +580,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
                        : "memory");
         }
-        fence_async_shared();
       }
-      tmem_wait_st();
+      fence_async_shared();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + (i & 1)));
-#pragma unroll
-      for (int e = 0; e < 32; ++e) s[e] = sn[e];
+    };
+    float s2[32];
+    for (int i = 0; i < ntiles; i += 2) {
+      softmax_tile(i, s, s2);
+      if (i + 1 < ntiles) softmax_tile(i + 1, s2, s);
     }
     // after a failure, let an armed exchange phase finish (or time out) so no
     // copy from the peer is still landing when this CTA exits
@@ -695,12 +744,11 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
       c.page_table ? (long long)c.num_pages * c.page_size
                    : (long long)(p.B - 1) * c.seq_stride + p.Tmax;
 
-  CUtensorMap tm_wuk, tm_qn, tm_ql, tm_qr, tm_ckv, tm_kr, tm_wuv, tm_ol;
+  CUtensorMap tm_wuk, tm_qn, tm_qr, tm_ckv, tm_kr, tm_wuv, tm_ol;
   const int NBf = gemm_rows(BL, p.n), NBu = gemm_rows(BL, kLat);
   bool ok = make_tmap_bf16_2d(&tm_wuk, a.W_UK, kLat, (uint64_t)p.H * p.n, kLat * 2, 64, 64, 128);
   ok = ok && make_tmap_bf16_2d(&tm_qn, a.q_nope, (uint64_t)p.H * p.n, BL, (uint64_t)p.H * p.n * 2,
                                64, NBf, 128);
-  ok = ok && make_tmap_bf16_2d(&tm_ql, q_lat, kLat, (uint64_t)p.B * R, kLat * 2, 64, BM, 128);
   ok = ok && make_tmap_bf16_2d(&tm_qr, a.q_rope, 64, (uint64_t)p.B * R, 128, 32, BM, 64);
   ok = ok && make_tmap_bf16_2d(&tm_ckv, c.c_kv, kLat, cache_rows, c.ckv_stride * 2, 64, BN, 128);
   ok = ok && make_tmap_bf16_2d(&tm_kr, c.k_rope, 64, cache_rows, c.kr_stride * 2, 32, BN, 64);
@@ -735,6 +783,8 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     AttnParams ap;
     ap.lens = a.lens;
     ap.page_table = c.page_table;
+    ap.q_lat = q_lat;
+    ap.B = p.B;
     ap.page_size = c.page_size;
     ap.max_pages = c.max_pages;
     ap.seq_stride = c.seq_stride;
@@ -749,7 +799,7 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     KernelTimer kt("absorbed_attn_sm103", a.stream);
     e = launch_pdl(absorbed_attn_sm103, dim3(2 * ((R + BM - 1) / BM), p.splits, p.B),
                    dim3(ATTN_THREADS),
-                   ATTN_SMEM, a.stream, tm_ql, tm_qr, tm_ckv, tm_kr, ap);
+                   ATTN_SMEM, a.stream, tm_qr, tm_ckv, tm_kr, ap);
     if (e != cudaSuccess) return e;
   }
   {

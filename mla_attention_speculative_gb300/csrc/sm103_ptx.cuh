@@ -52,23 +52,32 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
+// Relaxed remote arrive: no fence.  For signals whose protected accesses are
+// already complete (loads whose values have been consumed before a bar.sync).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+// try_wait suspends the thread in hardware until the phase completes or about
+// kSuspendNs pass, so a waiting thread does not spin on issue slots.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
       "selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3; "
       "selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -283,6 +292,16 @@ __device__ __forceinline__ void tmem_wait_st() {
 // is XORed with row % 8.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
   return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + ((col & 7u) << 1);
+}
+
+// fp16 pair -> two fp32 with integer operations (exact for normal numbers and
+// zero; fp16 subnormals, below 6.1e-5 in magnitude, come out within 2^-14 of
+// their value).  Keeps the conversion pipe free for the exponentials.
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t h) {
+  const uint32_t lo = h & 0xFFFFu, hi = h >> 16;
+  const uint32_t flo = ((lo & 0x8000u) << 16) | ((lo & 0x7FFFu) ? ((lo & 0x7FFFu) << 13) + 0x38000000u : 0u);
+  const uint32_t fhi = ((hi & 0x8000u) << 16) | ((hi & 0x7FFFu) ? ((hi & 0x7FFFu) << 13) + 0x38000000u : 0u);
+  return make_float2(__uint_as_float(flo), __uint_as_float(fhi));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
