@@ -46,6 +46,8 @@ def _args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-materialised", action="store_true",
+                    help="skip the materialised-branch shapes")
     return ap.parse_args()
 
 
@@ -96,6 +98,103 @@ def _work(kernel: str, L: int, T: int, H=128, r=512, n=128, v=128, rope=64):
         "unembed_sm103": unembed,
     }
     return table.get(kernel)
+
+
+def _mat_work(kernel: str, geom, L: int, lens):
+    """(bytes, flops) of one materialised-branch launch: the expansion GEMM
+    (sum(T) x H*(n+v) x r) and causal attention over the expanded cache (row l
+    of a sequence sees T - L + l + 1 positions; masked work is not counted)."""
+    bf = 2
+    H, r, n, v, rope = geom.H, geom.r, geom.n, geom.v, geom.rope
+    d = n + v
+    sT = sum(lens)
+    if kernel in ("expand_sm103", "generic_expand"):
+        return (sT * r * bf + H * r * d * bf + sT * H * d * bf, 2 * sT * r * H * d)
+    if kernel in ("mat_attn_sm103", "generic_materialised_attention"):
+        vis = sum(L * (T - L) + L * (L + 1) // 2 for T in lens)
+        byts = sT * H * d * bf + sT * rope * bf + len(lens) * L * H * (n + rope + v) * bf
+        return (byts, 2 * H * (n + rope + v) * vis)
+    return None
+
+
+# The materialised branch's measurement shapes: the GLM-4.7-Flash-like
+# crossover sweep past its threshold, the long-context cold prefill (T = L),
+# and the DeepSeek-V3-like width-16 call forced onto this branch.
+MAT_SHAPES = (
+    ("glm47-like T=8192 L=512", "GLM47", 512, [8192], "auto"),
+    ("glm47-like T=8192 L=2048", "GLM47", 2048, [8192], "auto"),
+    ("512/256/256 H=64 B=4 T=L=2048 cold prefill", "GLM53", 2048, [2048] * 4, "auto"),
+    ("dsv3-like T=8192 L=16 forced", "DSV3", 16, [8192], "materialised"),
+)
+
+
+def _bench_materialised(B, dev, peaks, reps):
+    """Per shape: us per call (graph replay, CUDA events) and each kernel's
+    achieved rate against its roofline (events around each launch)."""
+    import torch
+    from mla_attention_speculative_gb300 import inputs as I
+    res = []
+    for name, gname, L, lens, mode in MAT_SHAPES:
+        geom = getattr(I, gname)
+        c = I.make_case(geom, L, lens, dtype=torch.bfloat16, seed=2000 + L)
+        d = {k: getattr(c, k).to(dev) for k in
+             ("q_nope", "q_rope", "c_kv", "k_rope", "W_UK", "W_UV")}
+        del c
+        lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
+        g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope, torch.bfloat16)
+        ws = torch.empty(B.mla_workspace_bytes(g, L, lens, mode), dtype=torch.uint8, device=dev)
+        out = torch.empty((len(lens), L, geom.H, geom.v), dtype=torch.bfloat16, device=dev)
+        br = {}
+
+        def call():
+            _, br["b"] = B.mla_verify_attention(d["q_nope"], d["q_rope"], d["c_kv"], d["k_rope"],
+                                                d["W_UK"], d["W_UV"], lens, mode=mode, out=out,
+                                                workspace=ws, cache_lens_dev=lens_dev)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        st = torch.cuda.Stream(dev)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=st):
+            call()
+        gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us_call = a.elapsed_time(b) * 1e3 / reps
+        B.mla_kernel_timing_read(reset=True)
+        B.mla_kernel_timing_enable(True)
+        for _ in range(reps):
+            call()
+        torch.cuda.synchronize()
+        B.mla_kernel_timing_enable(False)
+        kt = B.mla_kernel_timing_read(reset=True)
+        kern = {}
+        for k, (nl, ms) in kt.items():
+            w = _mat_work(k, geom, L, lens)
+            us = ms * 1e3 / max(nl, 1)
+            ent = {"us": us}
+            if w is not None:
+                tb, tf = w[0] / (peaks["hbm_gbs"] * 1e9), w[1] / (peaks["bf16_tflops"] * 1e12)
+                if tf >= tb:
+                    ach = w[1] / (us * 1e-6) / 1e12
+                    ent.update(bound="tensor", achieved=ach, unit="TFLOP/s",
+                               frac=ach / peaks["bf16_tflops"])
+                else:
+                    ach = w[0] / (us * 1e-6) / 1e9
+                    ent.update(bound="hbm", achieved=ach, unit="GB/s", frac=ach / peaks["hbm_gbs"])
+            kern[k] = ent
+        res.append({"workload": name, "branch": B.BRANCH_NAMES[br["b"]],
+                    "us_per_call": us_call, "kernels": kern})
+        del d, ws, out, gr
+        torch.cuda.empty_cache()
+    return {"shapes": res, "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
+            "peak_source": f"of {peaks['source']}",
+            "note": "workspace (the expanded cache) is larger than L2 and is rewritten each call"}
 
 
 def _source_sha(names):
@@ -421,6 +520,10 @@ def run_ours(args):
     # ---- end to end: host inputs -> device -> host result, per step ----------
     e2e = _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world)
 
+    mat = None
+    if not args.no_materialised:
+        mat = _bench_materialised(B, dev, peaks, reps=max(3, min(args.steps, 20)))
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(layers[0])
@@ -442,6 +545,7 @@ def run_ours(args):
             "per_width_us_per_call": per_L,
             "roofline": roof,
             "kernel_ms_per_step": {k: v[1] / args.steps for k, v in ktimes.items()},
+            "materialised": mat,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": e2e,

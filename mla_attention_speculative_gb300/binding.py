@@ -224,7 +224,8 @@ def mla_kernel_timing_enable(on: bool = True) -> None:
 
 
 def mla_kernel_timing_read(reset: bool = True) -> dict:
-    """{kernel name: (launches, total device ms)} since the last reset (waits for events)."""
+    """{kernel name: (launches, total device ms)} of the kernels launched since
+    the last reset (waits for their events)."""
     cap = 64
     names = ctypes.create_string_buffer(4096)
     launches = (ctypes.c_int32 * cap)()
@@ -233,7 +234,8 @@ def mla_kernel_timing_read(reset: bool = True) -> dict:
     _check(lib().mla_kernel_timing_read(names, 4096, launches, ms, cap, ctypes.byref(n),
                                         1 if reset else 0), "mla_kernel_timing_read")
     keys = names.value.decode().split(";") if n.value else []
-    return {k: (int(launches[i]), float(ms[i])) for i, k in enumerate(keys[:cap])}
+    return {k: (int(launches[i]), float(ms[i])) for i, k in enumerate(keys[:cap])
+            if launches[i] > 0}
 
 
 def mla_verify_attention_noalloc(q_nope: torch.Tensor, q_rope: torch.Tensor,

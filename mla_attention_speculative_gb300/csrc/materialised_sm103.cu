@@ -1,0 +1,620 @@
+// Materialised-branch MLA verify on GB300 tensor cores (tcgen05 + TMEM + TMA).
+//
+// "One guard, 110x off the verify step", section "The defect": expand the
+// whole cached latent back into full keys and values, then attend normally.
+// Two kernels, bf16 operands with fp32 accumulation in tensor memory, chained
+// with programmatic dependent launch:
+//
+//  expand_sm103    K_nope[b,h,t,:] = c_kv[b,t] . W_UK[h]^T   (512 -> n)
+//                  V[b,h,t,:]      = c_kv[b,t] . W_UV[h]     (512 -> v)
+//                  into one [B*H, Tmax, n+v] bf16 buffer (each head's keys and
+//                  values contiguous).  One CTA per (128 cached positions,
+//                  head): each 64-wide latent chunk of the cache tile feeds
+//                  both GEMMs (two TMEM accumulators); the chunks stream
+//                  through a TMA ring; the bf16 tile leaves through shared
+//                  memory with TMA stores clipped at Tmax.
+//  mat_attn_sm103  causal attention of the L verify rows of one head against
+//                  keys [K_nope || k_rope] (the RoPE key is shared by all heads)
+//                  and values V: S = Q K^T on the tensor cores, an online
+//                  softmax in registers (one thread per query row, the running
+//                  max moved only when it grows by more than 2^8), P written
+//                  back to tensor memory as the A operand of O += P V.  One CTA
+//                  per (128-row query tile, head, sequence).
+//
+// Every wait is bounded; a wait that runs out sets the status word and the
+// kernel finishes without waiting further (results are then undefined and
+// mla_device_status reports MLA_ERR_TIMEOUT).
+
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <cmath>
+#include <utility>
+
+#include "mla_internal.h"
+#include "sm103_ptx.cuh"
+#include "tma_host.h"
+
+namespace mla {
+using namespace sm103;
+
+static __device__ int g_materialised_status;
+
+namespace {
+
+constexpr int kLat = 512;
+constexpr int kSmemPerBlock = 232448;   // opt-in maximum per CTA
+constexpr int kSmemPerSM = 233472;
+constexpr int kSmemReserved = 1024;     // per CTA, taken by the runtime
+constexpr int kSmemExtra = 1024 + 256;  // 1024-byte realignment + barriers
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+__device__ __forceinline__ void report_timeout(int code) {
+  atomicCAS(&g_materialised_status, 0, code);
+}
+__device__ __forceinline__ void wait_or_fail(bool& ok, uint32_t bar, uint32_t parity, int code) {
+  if (!ok) return;
+  if (!mbar_wait(bar, parity)) {
+    ok = false;
+    report_timeout(code);
+  }
+}
+
+// Row of cached position t of sequence b in the 2-D cache tensors.
+__device__ __forceinline__ int cache_y(const int32_t* page_table, int page_size, int max_pages,
+                                       long long seq_stride, int b, int t) {
+  return page_table ? (int)((long long)page_table[(long long)b * max_pages + t / page_size] *
+                                page_size +
+                            (t % page_size))
+                    : (int)((long long)b * seq_stride + t);
+}
+
+// =========================================================================
+// expansion GEMM
+// =========================================================================
+struct ExpandParams {
+  const int32_t* lens;
+  const int32_t* page_table;
+  int page_size, max_pages;
+  long long seq_stride;
+  int H, n, v, stages;
+  uint32_t tmem_cols, v_col;  // TMEM allocation; V accumulator's first column
+};
+
+constexpr int EX_BM = 128;
+
+__host__ __device__ constexpr int expand_stage_bytes(int n, int v) {
+  return EX_BM * 128 + (n + v) * 128;
+}
+
+__global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ CUtensorMap tm_ckv,
+                                                       const __grid_constant__ CUtensorMap tm_wuk,
+                                                       const __grid_constant__ CUtensorMap tm_wuv,
+                                                       const __grid_constant__ CUtensorMap tm_out,
+                                                       ExpandParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int mt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  pdl_wait();  // the cache and its lengths may come from the preceding kernel
+  const int T = p.lens[b];
+  const int t0 = mt * EX_BM;
+  if (t0 >= T) return;
+  const int n = p.n, v = p.v, S = p.stages;
+  const int SB = expand_stage_bytes(n, v);
+  uint64_t* bars = (uint64_t*)(smem + S * SB);  // [0,S) full, [S,2S) empty, 2S done
+  uint32_t* slot = (uint32_t*)(bars + 2 * S + 1);
+  volatile int* fail = (volatile int*)(slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[S + s]); };
+  const uint32_t done = smem_u32(&bars[2 * S]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(done, 1);
+    *fail = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(slot), p.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  constexpr int kChunks = kLat / 64;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    // The 128-row cache tile is two 64-row boxes; with paging each box lies
+    // in one page (page sizes are multiples of 64).  Rows at or past T are
+    // loaded but never read back.
+    bool ok = true;
+    const int y0 = cache_y(p.page_table, p.page_size, p.max_pages, p.seq_stride, b, t0);
+    const int y1 = t0 + 64 < T
+                       ? cache_y(p.page_table, p.page_size, p.max_pages, p.seq_stride, b, t0 + 64)
+                       : y0 + 64;
+    int issued = 0;
+    for (int kc = 0; kc < kChunks; ++kc) {
+      const int s = kc % S;
+      if (kc >= S) wait_or_fail(ok, empty(s), ((kc / S) - 1) & 1, 40);
+      if (!ok) break;
+      const uint32_t st = sbase + s * SB;
+      mbar_arrive_expect_tx(full(s), SB);
+      tma_load_2d(st, &tm_ckv, full(s), 64 * kc, y0);
+      tma_load_2d(st + 8192, &tm_ckv, full(s), 64 * kc, y1);
+      const uint32_t bn = st + EX_BM * 128;
+      for (int r = 0; r < n / 64; ++r)
+        tma_load_2d(bn + r * 8192, &tm_wuk, full(s), 64 * kc, h * n + 64 * r);
+      const uint32_t bv = bn + n * 128;
+      for (int j = 0; j < v / 64; ++j)
+        tma_load_2d(bv + j * 8192, &tm_wuv, full(s), 64 * j, h * kLat + 64 * kc);
+      issued = kc + 1;
+    }
+    // no load may still be landing when the ring is reused for the output
+    for (int kc = max(issued - S, 0); kc < issued; ++kc) mbar_wait(full(kc % S), (kc / S) & 1);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------- MMA
+    bool ok = true;
+    const uint32_t id_n = idesc_bf16(128, n, 0, 0);
+    const uint32_t id_v = idesc_bf16(128, v, 0, 1);
+    for (int kc = 0; kc < kChunks; ++kc) {
+      const int s = kc % S;
+      wait_or_fail(ok, full(s), (kc / S) & 1, 41);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t st = sbase + s * SB;
+      const uint64_t da = sdesc_sw128(st, 16, 1024);
+      const uint64_t dn = sdesc_sw128(st + EX_BM * 128, 16, 1024);
+      const uint64_t dv = sdesc_sw128(st + EX_BM * 128 + n * 128, 8192, 1024);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_bf16(tmem, da + 2 * ks, dn + 2 * ks, id_n, (kc | ks) != 0);
+        mma_bf16(tmem + p.v_col, da + 2 * ks, dv + 128 * ks, id_v, (kc | ks) != 0);
+      }
+      mma_commit(empty(s));
+    }
+    if (!ok) *fail = 1;
+    mma_commit(done);
+    if (!mbar_wait(done, 0)) {
+      *fail = 1;
+      report_timeout(42);
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  pdl_launch_dependents();
+  const bool ok = !*fail;
+  if (ok) {
+    // TMEM -> bf16 -> shared memory in the 128-byte-swizzled layout of the
+    // store boxes (64 columns x 128 rows, 16 KB each), then TMA stores.
+    const int q = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    auto emit = [&](uint32_t col0, int width, int out_col0) {
+      for (int c = 0; c < width; c += 32) {
+        uint32_t r[32];
+        tmem_ld16(tmem + lane_base + col0 + c, *(uint32_t(*)[16])(r));
+        tmem_ld16(tmem + lane_base + col0 + c + 16, *(uint32_t(*)[16])(r + 16));
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          const int col = out_col0 + c + e;
+          const uint32_t addr = sbase + (col >> 6) * (EX_BM * 128) + q * 128 +
+                                ((((col & 63) >> 3) ^ (q & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "r"(pack_bf16(__uint_as_float(r[e]), __uint_as_float(r[e + 1]))),
+                       "r"(pack_bf16(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]))),
+                       "r"(pack_bf16(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]))),
+                       "r"(pack_bf16(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7])))
+                       : "memory");
+        }
+      }
+    };
+    emit(0, n, 0);
+    emit(p.v_col, v, n);
+    fence_async_shared();
+  }
+  __syncthreads();
+  if (ok && threadIdx.x == 0) {
+    const int plane = b * p.H + h;
+    for (int c = 0; c < (n + v) / 64; ++c)
+      tma_store_3d(&tm_out, sbase + c * (EX_BM * 128), 64 * c, t0, plane);
+    bulk_commit();
+    bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// =========================================================================
+// flash attention over the expanded cache
+// =========================================================================
+struct MatAttnParams {
+  const int32_t* lens;
+  const int32_t* page_table;
+  int page_size, max_pages;
+  long long seq_stride;
+  __nv_bfloat16* out;  // [B, L, H, v]
+  int L, H, n, v, stages;
+  float sl2;           // softmax scale x log2(e)
+};
+
+constexpr int MA_BM = 128;
+constexpr int MA_BN = 64;
+constexpr uint32_t MA_TM_S = 256;  // S / P buffers at 256 + 64*sb; O at [0, v)
+
+__host__ __device__ constexpr int mat_q_bytes(int n) { return (n / 64 + 1) * MA_BM * 128; }
+__host__ __device__ constexpr int mat_stage_bytes(int n, int v) {
+  return (n / 64 + 1 + v / 64) * MA_BN * 128;
+}
+
+enum { M_QFULL = 0, M_SFULL = 1, M_PFULL = 3, M_ODONE = 5, M_DRAIN = 7, M_KV = 8 };
+
+__global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__ CUtensorMap tm_qn,
+                                                         const __grid_constant__ CUtensorMap tm_qr,
+                                                         const __grid_constant__ CUtensorMap tm_kx,
+                                                         const __grid_constant__ CUtensorMap tm_kr,
+                                                         MatAttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int T = p.lens[b];
+  const int n = p.n, v = p.v, S = p.stages, L = p.L;
+  const int l0 = qt * MA_BM;
+  const int l_last = min(L - 1, l0 + MA_BM - 1);
+  const int kv_end = T - L + l_last + 1;  // no row of the tile sees t >= kv_end
+  const int ntiles = (kv_end + MA_BN - 1) / MA_BN;
+  const int nq = n / 64 + 1;  // Q / K chunks of 64 columns: n/64 nope + 1 RoPE
+  const int QB = mat_q_bytes(n), SB = mat_stage_bytes(n, v);
+  const uint32_t sQ = smem_u32(smem), sKV = sQ + QB;
+  uint64_t* bars = (uint64_t*)(smem + QB + S * SB);
+  uint32_t* slot = (uint32_t*)(bars + M_KV + 2 * S);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto kv_full = [&](int s) { return bar(M_KV + s); };
+  auto kv_empty = [&](int s) { return bar(M_KV + S + s); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(M_QFULL), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(M_SFULL + i), 1);
+      mbar_init(bar(M_PFULL + i), 128);
+      mbar_init(bar(M_ODONE + i), 1);
+    }
+    mbar_init(bar(M_DRAIN), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  const int plane = b * p.H + h;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      bool ok = true;
+      pdl_wait();  // the expanded cache comes from the expansion kernel
+      const int qrow = b * L + l0;
+      mbar_arrive_expect_tx(bar(M_QFULL), QB);
+      for (int c = 0; c < n / 64; ++c)
+        tma_load_2d(sQ + c * MA_BM * 128, &tm_qn, bar(M_QFULL), h * n + 64 * c, qrow);
+      tma_load_2d(sQ + (n / 64) * MA_BM * 128, &tm_qr, bar(M_QFULL), h * 64, qrow);
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % S;
+        if (i >= S) wait_or_fail(ok, kv_empty(s), ((i / S) - 1) & 1, 50);
+        if (!ok) break;
+        const int t0 = i * MA_BN;
+        const int y = cache_y(p.page_table, p.page_size, p.max_pages, p.seq_stride, b, t0);
+        const uint32_t st = sKV + s * SB;
+        mbar_arrive_expect_tx(kv_full(s), SB);
+        for (int c = 0; c < n / 64; ++c)
+          tma_load_3d(st + c * 8192, &tm_kx, kv_full(s), 64 * c, t0, plane);
+        tma_load_2d(st + (n / 64) * 8192, &tm_kr, kv_full(s), 0, y);
+        for (int j = 0; j < v / 64; ++j)
+          tma_load_3d(st + (nq + j) * 8192, &tm_kx, kv_full(s), n + 64 * j, t0, plane);
+        issued = i + 1;
+      }
+      // drain: nothing may still be landing when the CTA exits
+      mbar_wait(bar(M_QFULL), 0);
+      for (int i = max(issued - S, 0); i < issued; ++i) mbar_wait(kv_full(i % S), (i / S) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    // Order: S(0), then for each j: S(j+1), O += P(j) V(j).  P(j) sits in S
+    // buffer j&1, which S(j+2) overwrites only after P(j) V(j) in issue order.
+    if (lane == 0) {
+      bool ok = true;
+      const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dk = sdesc_sw128(sKV, 16, 1024);
+      const uint64_t dv = sdesc_sw128(sKV + nq * 8192, 8192, 1024);
+      const uint32_t id_s = idesc_bf16(MA_BM, MA_BN, 0, 0);
+      const uint32_t id_o = idesc_bf16(MA_BM, v, 0, 1);
+      wait_or_fail(ok, bar(M_QFULL), 0, 51);
+      auto issue_s = [&](int i) {
+        const int s = i % S, sb = i & 1;
+        wait_or_fail(ok, kv_full(s), (i / S) & 1, 52);
+        if (!ok) return;
+        tc_fence_after();
+        const uint64_t soff = (uint64_t)(s * (SB >> 4));
+        for (int c = 0; c < nq; ++c)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + MA_TM_S + sb * MA_BN, dq + ((c * MA_BM * 128 + ks * 32) >> 4),
+                     dk + soff + ((c * 8192 + ks * 32) >> 4), id_s, (c | ks) != 0);
+        mma_commit(bar(M_SFULL + sb));
+      };
+      issue_s(0);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        if (j + 1 < ntiles) issue_s(j + 1);
+        if (!ok) break;
+        const int sj = j % S, pb = j & 1;
+        wait_or_fail(ok, bar(M_PFULL + pb), (j >> 1) & 1, 53);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t soff = (uint64_t)(sj * (SB >> 4));
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16_tmem_a(tmem, tmem + MA_TM_S + pb * MA_BN + ks * 8, dv + soff + ks * 128, id_o,
+                          (j > 0 || ks > 0));
+        mma_commit(bar(M_ODONE + pb));
+        mma_commit(kv_empty(sj));
+      }
+      mma_commit(bar(M_DRAIN));
+      mbar_wait(bar(M_DRAIN), 0);
+    }
+  } else {
+    // ------------------------------------------------- softmax warpgroup
+    const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const int l = min(l0 + q, L - 1);
+    const int last_t = T - L + l;          // the last position row l may see
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int i = 0; i < ntiles; ++i) {
+      const int sb = i & 1;
+      const int t0 = i * MA_BN;
+      wait_or_fail(ok, bar(M_SFULL + sb), (i >> 1) & 1, 54);
+      tc_fence_after();
+      uint32_t u[MA_BN];
+#pragma unroll
+      for (int k = 0; k < MA_BN / 16; ++k)
+        tmem_ld16(tmem + lane_base + MA_TM_S + sb * MA_BN + 16 * k,
+                  *(uint32_t(*)[16])(u + 16 * k));
+      tmem_wait_ld();
+      // Masked columns: past the row's causal limit (this also covers
+      // positions at or past T, whose keys may hold anything).
+      float s[MA_BN];
+      const bool edge = t0 + MA_BN - 1 > T - L;
+#pragma unroll
+      for (int j = 0; j < MA_BN; ++j) {
+        const float x = __uint_as_float(u[j]) * p.sl2;
+        s[j] = (!edge || t0 + j <= last_t) ? x : -INFINITY;
+      }
+      float m4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+      for (int j = 4; j < MA_BN; ++j) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      const bool need = mt > m_run + 8.f;
+      const float m_new = need ? mt : m_run;
+      const float factor = need ? ex2(m_run - m_new) : 1.f;
+      if (i > 0 && __any_sync(0xffffffffu, need)) {
+        // O must hold P(i-1) V(i-1) before it is rescaled
+        wait_or_fail(ok, bar(M_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, 55);
+        tc_fence_after();
+        for (int c = 0; c < v; c += 16) {
+          uint32_t w[16];
+          tmem_ld16(tmem + lane_base + c, w);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * factor);
+          tmem_st16(tmem + lane_base + c, w);
+        }
+      }
+      l_run *= factor;
+      m_run = m_new;
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pk[MA_BN / 2];
+#pragma unroll
+      for (int e = 0; e < MA_BN / 2; ++e) {
+        const float a = ex2(s[2 * e] - m_use);
+        const float d = ex2(s[2 * e + 1] - m_use);
+        rs0 += a;
+        rs1 += d;
+        pk[e] = pack_bf16(a, d);
+      }
+      l_run += rs0 + rs1;
+      tmem_st32(tmem + lane_base + MA_TM_S + sb * MA_BN, pk);
+      // Value rows at or past T in the last tile may hold anything (0 x NaN
+      // would poison O): zero them in shared memory before P V reads them.
+      if (ok && t0 + MA_BN > T) {
+        const int z0 = max(T - t0, 0);
+        const uint32_t st = sKV + (i % S) * SB + nq * 8192;
+        const int units = (MA_BN - z0) * 8;  // 16-byte units per 64-column chunk
+        for (int w = q; w < (v / 64) * units; w += 128) {
+          const int c = w / units, r = w - c * units;
+          const uint32_t addr = st + c * 8192 + (z0 + r / 8) * 128 + (r & 7) * 16;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
+                       : "memory");
+        }
+        fence_async_shared();
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(M_PFULL + sb));
+    }
+    // ---------------------------------------------------------------- epilogue
+    wait_or_fail(ok, bar(M_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 56);
+    tc_fence_after();
+    pdl_launch_dependents();
+    const bool live = l0 + q < L;
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    __nv_bfloat16* dst = p.out + (((size_t)b * L + (live ? l0 + q : 0)) * p.H + h) * (size_t)v;
+    for (int c = 0; c < v; c += 32) {
+      uint32_t r[32];
+      tmem_ld16(tmem + lane_base + c, *(uint32_t(*)[16])(r));
+      tmem_ld16(tmem + lane_base + c + 16, *(uint32_t(*)[16])(r + 16));
+      tmem_wait_ld();
+      if (live) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv);
+          w.y = pack_bf16(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+          w.z = pack_bf16(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv);
+          w.w = pack_bf16(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv);
+          *(uint4*)(dst + c + e) = w;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Expansion layout: accumulators need n + v TMEM columns.  When they fit in
+// 256, two CTAs share an SM (one's epilogue overlaps the other's GEMM), so the
+// ring gets half the shared memory.
+struct ExpandShape {
+  uint32_t tmem_cols, v_col;
+  int stages, smem;
+};
+ExpandShape expand_shape(int n, int v) {
+  ExpandShape e;
+  const bool pair = n + v <= 256;
+  e.tmem_cols = pair ? 256u : 512u;
+  e.v_col = pair ? (uint32_t)n : 256u;
+  const int budget = pair ? kSmemPerSM / 2 - kSmemReserved : kSmemPerBlock;
+  const int sb = expand_stage_bytes(n, v);
+  int s = (budget - kSmemExtra) / sb;
+  e.stages = s > 4 ? 4 : s;
+  e.smem = e.stages * sb + kSmemExtra;
+  return e;
+}
+int mat_stages(int n, int v) {
+  const int s = (kSmemPerBlock - kSmemExtra - mat_q_bytes(n)) / mat_stage_bytes(n, v);
+  return s > 4 ? 4 : s;
+}
+
+}  // namespace
+
+bool fast_materialised_supported(const Plan& p) {
+  if (!(p.dtype == MLA_DTYPE_BF16 && p.r == kLat && p.rope == 64 && p.n % 64 == 0 && p.n >= 64 &&
+        p.n <= 256 && p.v % 64 == 0 && p.v >= 64 && p.v <= 256))
+    return false;
+  const ExpandShape e = expand_shape(p.n, p.v);
+  // the output tile (128 x (n+v) bf16) is staged in the drained ring
+  return e.stages >= 2 && e.stages * expand_stage_bytes(p.n, p.v) >= EX_BM * (p.n + p.v) * 2 &&
+         mat_stages(p.n, p.v) >= 2;
+}
+
+size_t fast_materialised_workspace(const Plan& p) {
+  return (size_t)p.B * p.H * p.Tmax * (p.n + p.v) * 2;
+}
+
+cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
+  const CacheView& c = a.cache;
+  const long long cache_rows = c.page_table ? (long long)c.num_pages * c.page_size
+                                            : (long long)(p.B - 1) * c.seq_stride + p.Tmax;
+  __nv_bfloat16* kexp = (__nv_bfloat16*)(a.ws + p.off_exp);
+  const int d = p.n + p.v;
+  const uint64_t planes = (uint64_t)p.B * p.H;
+  CUtensorMap tm_ckv, tm_wuk, tm_wuv, tm_store, tm_qn, tm_qr, tm_kx, tm_kr;
+  bool ok = make_tmap_bf16_2d(&tm_ckv, c.c_kv, kLat, cache_rows, c.ckv_stride * 2, 64, 64, 128);
+  ok = ok && make_tmap_bf16_2d(&tm_wuk, a.W_UK, kLat, (uint64_t)p.H * p.n, kLat * 2, 64, 64, 128);
+  ok = ok && make_tmap_bf16_2d(&tm_wuv, a.W_UV, p.v, (uint64_t)p.H * kLat, (uint64_t)p.v * 2, 64,
+                               64, 128);
+  ok = ok && make_tmap_bf16_3d(&tm_store, kexp, d, p.Tmax, planes, (uint64_t)d * 2,
+                               (uint64_t)p.Tmax * d * 2, 64, EX_BM);
+  ok = ok && make_tmap_bf16_2d(&tm_qn, a.q_nope, (uint64_t)p.H * p.n, (uint64_t)p.B * p.L,
+                               (uint64_t)p.H * p.n * 2, 64, MA_BM, 128);
+  ok = ok && make_tmap_bf16_2d(&tm_qr, a.q_rope, (uint64_t)p.H * 64, (uint64_t)p.B * p.L,
+                               (uint64_t)p.H * 64 * 2, 64, MA_BM, 128);
+  ok = ok && make_tmap_bf16_3d(&tm_kx, kexp, d, p.Tmax, planes, (uint64_t)d * 2,
+                               (uint64_t)p.Tmax * d * 2, 64, MA_BN);
+  ok = ok && make_tmap_bf16_2d(&tm_kr, c.k_rope, 64, cache_rows, c.kr_stride * 2, 64, MA_BN, 128);
+  if (!ok) return cudaErrorInvalidValue;
+
+  const ExpandShape es = expand_shape(p.n, p.v);
+  const int ms = mat_stages(p.n, p.v);
+  const int ma_smem = mat_q_bytes(p.n) + ms * mat_stage_bytes(p.n, p.v) + kSmemExtra;
+  static bool attrs[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attrs[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(expand_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemPerBlock);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mat_attn_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemPerBlock);
+    if (e != cudaSuccess) return e;
+    attrs[dev] = true;
+  }
+  cudaError_t e;
+  {
+    ExpandParams ep{a.lens, c.page_table, c.page_size, c.max_pages, c.seq_stride,
+                    p.H,    p.n,          p.v,         es.stages,   es.tmem_cols,
+                    es.v_col};
+    KernelTimer kt("expand_sm103", a.stream);
+    e = launch_pdl(expand_sm103, dim3((p.Tmax + EX_BM - 1) / EX_BM, p.H, p.B), dim3(128), es.smem,
+                   a.stream, tm_ckv, tm_wuk, tm_wuv, tm_store, ep);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    MatAttnParams mp{a.lens, c.page_table, c.page_size, c.max_pages, c.seq_stride,
+                     (__nv_bfloat16*)a.out, p.L, p.H, p.n, p.v, ms,
+                     p.scale * 1.4426950408889634f};
+    KernelTimer kt("mat_attn_sm103", a.stream);
+    e = launch_pdl(mat_attn_sm103, dim3((p.L + MA_BM - 1) / MA_BM, p.H, p.B), dim3(192), ma_smem,
+                   a.stream, tm_qn, tm_qr, tm_kx, tm_kr, mp);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
+int materialised_device_status(bool clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_materialised_status, sizeof(int)) != cudaSuccess) return -1;
+  if (clear && v != 0) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_materialised_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
+}
+
+}  // namespace mla

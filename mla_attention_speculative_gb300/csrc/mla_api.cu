@@ -194,8 +194,17 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     off = align256(off + nrow * g.splits * 2 * sizeof(float));
     g.bytes = off;
   }
-  p->fast_ok = p->branch == MLA_BRANCH_ABSORBED && fast_absorbed_supported(*p);
-  if (p->fast_ok) {
+  p->fast_ok = p->branch == MLA_BRANCH_ABSORBED ? fast_absorbed_supported(*p)
+                                                : fast_materialised_supported(*p);
+  if (p->fast_ok && p->branch == MLA_BRANCH_MATERIALISED) {
+    // no split-KV: one CTA per (128-row query tile, head, sequence) walks the
+    // whole visible cache
+    SplitPlan& f = p->fast;
+    f.chunk = p->Tmax;
+    f.splits = 1;
+    f.off_exp = 0;
+    f.bytes = align256(fast_materialised_workspace(*p));
+  } else if (p->fast_ok) {
     // Tensor-core split-KV: clusters of 2 CTAs, one per (128-row tile, piece).
     // Pick the piece length ct (in 64-row KV tiles) that minimises
     // waves x (ct + overhead) over the SMs' cluster slots, where the fixed
@@ -337,10 +346,17 @@ extern "C" mla_status_t mla_verify_attention(
   a.ws = (char*)workspace;
   a.stream = (cudaStream_t)stream;
 
+  // The tensor-core kernels address the cache with 32-bit TMA row
+  // coordinates and read 64-row boxes that must not straddle pages.
+  const int64_t cache_rows = page_table ? (int64_t)num_pages * page_size
+                                        : (int64_t)(batch - 1) * seq_stride_rows + p.Tmax;
+  const bool fast = p.fast_ok && (page_table == nullptr || page_size % 64 == 0) &&
+                    cache_rows < ((int64_t)1 << 31);
   cudaError_t e;
-  if (p.fast_ok && (page_table == nullptr || page_size % 64 == 0)) {
+  if (fast) {
     p.use(p.fast);
-    e = launch_fast_absorbed(p, a);
+    e = p.branch == MLA_BRANCH_ABSORBED ? launch_fast_absorbed(p, a)
+                                        : launch_fast_materialised(p, a);
   } else {
     e = p.branch == MLA_BRANCH_ABSORBED ? launch_generic_absorbed(p, a)
                                         : launch_generic_materialised(p, a);
@@ -368,7 +384,9 @@ extern "C" const char* mla_status_string(int32_t s) {
 extern "C" const char* mla_last_error(void) { return g_err; }
 
 extern "C" mla_status_t mla_device_status(int32_t* code, int32_t clear) {
-  const int v = absorbed_device_status(clear != 0);
+  const int va = absorbed_device_status(clear != 0);
+  const int vm = materialised_device_status(clear != 0);
+  const int v = va < 0 || vm < 0 ? -1 : va != 0 ? va : vm;
   if (code) *code = v;
   if (v < 0) {
     set_error("could not read the device status word");

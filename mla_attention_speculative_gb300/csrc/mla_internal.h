@@ -36,7 +36,7 @@ struct Plan {
   int splits = 0;
   // the two kernel families' layouts; the workspace covers the larger
   SplitPlan generic;   // CUDA-core kernels, any geometry and paging
-  SplitPlan fast;      // tcgen05/TMA kernels (bf16, r = 512, rope = 64)
+  SplitPlan fast;      // tcgen05/TMA kernels of the chosen branch
   bool fast_ok = false;
   size_t ws_bytes = 0;
   // the layout of the family that runs (copied from generic or fast)
@@ -94,6 +94,14 @@ bool fast_absorbed_supported(const Plan& p);
 cudaError_t launch_fast_absorbed(const Plan& p, const Args& a);
 // Status word of the tensor-core kernels (0 = no wait ran out); synchronises.
 int absorbed_device_status(bool clear);
+
+// Tensor-core kernels for the materialised branch (bf16, r = 512, rope = 64,
+// n and v multiples of 64 up to 256): a tcgen05 expansion GEMM into a
+// [B*H, Tmax, n+v] workspace, then flash attention over it.
+bool fast_materialised_supported(const Plan& p);
+size_t fast_materialised_workspace(const Plan& p);
+cudaError_t launch_fast_materialised(const Plan& p, const Args& a);
+int materialised_device_status(bool clear);
 
 // Records a one-line failure description for mla_last_error().
 void set_error(const char* fmt, ...);

@@ -1,4 +1,4 @@
-// Host-side TMA tensor-map encoding for 2-D bf16 tensors.
+// Host-side TMA tensor-map encoding for 2-D and 3-D bf16 tensors.
 #pragma once
 
 #include <cuda.h>
@@ -15,5 +15,12 @@ namespace mla {
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                        int swizzle_bytes);
+
+// A [planes, rows, inner] bf16 tensor, boxes of 1 x box_rows x box_inner with
+// 128-byte swizzle (box_inner = 64).  Loads outside the tensor read zero;
+// stores are clipped to it.
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t planes, uint64_t row_stride_bytes, uint64_t plane_stride_bytes,
+                       uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace mla

@@ -219,3 +219,35 @@ def test_long_context(L, lens):
     w = WORKLOADS["long_context"]
     case = make_case(w["geom"], L, lens, seed=w["seed"])
     _sampled_check(case, ["auto"], f"long L={L} T={lens[0]}", nheads=4, nrows=4)
+
+
+# ---------------------------------------------------------------------------
+# Which kernels run: the tensor-core path for bf16 at the supported
+# geometries (contiguous and 64-row pages), the CUDA-core kernels otherwise
+# ---------------------------------------------------------------------------
+
+TC_ABSORBED = {"fold_sm103", "absorbed_attn_sm103", "merge_sm103", "unembed_sm103"}
+TC_MATERIALISED = {"expand_sm103", "mat_attn_sm103"}
+
+
+@pytest.mark.parametrize("mode,dtype,page,want", [
+    ("absorbed", torch.bfloat16, 0, TC_ABSORBED),
+    ("materialised", torch.bfloat16, 0, TC_MATERIALISED),
+    ("absorbed", torch.bfloat16, 64, TC_ABSORBED),
+    ("materialised", torch.bfloat16, 64, TC_MATERIALISED),
+    ("materialised", torch.bfloat16, 16, {"generic_expand", "generic_materialised_attention",
+                                          "generic_combine"}),
+    ("materialised", torch.float32, 0, {"generic_expand", "generic_materialised_attention",
+                                        "generic_combine"}),
+])
+def test_kernel_routing(mode, dtype, page, want):
+    case = make_case(Geometry(H=8), 4, [300, 129], dtype=dtype, seed=71, page_size=page)
+    B.mla_kernel_timing_enable(True)
+    try:
+        B.mla_kernel_timing_read(reset=True)
+        out, _ = run_gpu(case, mode)
+        ran = set(B.mla_kernel_timing_read(reset=True))
+    finally:
+        B.mla_kernel_timing_enable(False)
+    assert ran == want, ran
+    compare(out, oracle_out(case), dtype, f"routing {mode} page={page}")
