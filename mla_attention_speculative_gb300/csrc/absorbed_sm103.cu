@@ -89,8 +89,13 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(int n) {
 // weight is read once for all rows.  K arrives in 64-wide chunks, each with
 // its own barrier, and each chunk's MMAs issue as soon as it lands.
 struct GemmParams {
-  __nv_bfloat16* out;  // [rows, H, M]
+  __nv_bfloat16* out;  // [rows, H, M], or the attention's Q tiles (see below)
   int rows, H, K, M, NB;
+  // L > 0: write q_lat as the attention reads it.  Query row r = l*H + h of
+  // sequence b belongs to tile r/128 (row r%128 in it); a tile is 64 chunks of
+  // 8 latent columns, each chunk 128 rows x 16 B, so a warp that loads one
+  // chunk for its 32 rows reads 512 contiguous bytes.
+  int L, ntile;
 };
 
 constexpr int GEMM_MAX_K = 512;
@@ -163,8 +168,15 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int row = row0 + c0 + i;
-        if (row < p.rows)
-          p.out[((size_t)row * p.H + h) * p.M + m] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        if (row >= p.rows) continue;
+        size_t idx;
+        if (p.L > 0) {
+          const int b = row / p.L, r = (row - b * p.L) * p.H + h;
+          idx = ((((size_t)b * p.ntile + (r >> 7)) * 64 + (m >> 3)) * 128 + (r & 127)) * 8 + (m & 7);
+        } else {
+          idx = ((size_t)row * p.H + h) * p.M + m;
+        }
+        p.out[idx] = __float2bfloat16_rn(__uint_as_float(v[i]));
       }
     }
   }
@@ -210,15 +222,18 @@ static_assert(ATTN_SMEM <= 232448, "shared memory per CTA");
 struct AttnParams {
   const int32_t* lens;
   const int32_t* page_table;
-  const __nv_bfloat16* q_lat;  // [B*R, 512]
+  const __nv_bfloat16* q_lat;  // Q tiles [B, rtiles, 64 chunks, 128 rows, 8] bf16
   int page_size, max_pages;
   long long seq_stride;
   int L, H, R;        // R = L*H query rows per sequence
+  int rtiles;         // ceil(R / 128)
   int B;
   int chunk, splits;  // KV rows per split (multiple of 64), splits per sequence (max)
   float sl2;          // softmax scale * log2(e)
   float* o_part;      // [B, splits, R, 512]
   float* ml;          // [B, splits, R, 2]
+  const char* pf;     // W_UV, pulled into L2 while the attention runs
+  size_t pf_bytes;
 };
 
 // Barrier slots.  Every barrier that is waited on by parity alone has enough
@@ -271,12 +286,22 @@ __device__ __forceinline__ void put_partial(uint32_t tile, int q, int c0, const 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     absorbed_attn_sm103(const __grid_constant__ CUtensorMap tm_qr,
                         const __grid_constant__ CUtensorMap tm_ckv,
-                        const __grid_constant__ CUtensorMap tm_kr, AttnParams p) {
+                        const __grid_constant__ CUtensorMap tm_kr,
+                        const __grid_constant__ CUtensorMap tm_op, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int tile = blockIdx.x >> 1, split = blockIdx.y, b = blockIdx.z;
+  // The unembedding weights are read right after this kernel; at verify widths
+  // the attention leaves HBM mostly idle, so each CTA pulls a slice into L2.
+  if (threadIdx.x == 32 && p.pf != nullptr) {
+    const size_t nct = (size_t)gridDim.x * gridDim.y * gridDim.z;
+    const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    const size_t slice = ((p.pf_bytes + nct - 1) / nct + 4095) & ~(size_t)4095;
+    for (size_t o = id * slice; o < min(p.pf_bytes, (id + 1) * slice); o += 32768)
+      prefetch_l2(p.pf + o, (uint32_t)min((size_t)32768, p.pf_bytes - o));
+  }
   const int T = p.lens[b];
   const int nsplit = (T + p.chunk - 1) / p.chunk;
   if (split >= nsplit) return;  // both CTAs of the cluster leave together
@@ -441,13 +466,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     if (ntiles > 0) {
       // this CTA's latent query columns into TMEM as bf16 pairs (the fold wrote them)
       pdl_wait();
-      const long long grow = (long long)b * p.R + row;
-      const bool have = grow < (long long)p.B * p.R;
-      const uint4* src = (const uint4*)(p.q_lat + (have ? grow : 0) * kLat + 256 * rank + 128 * wg);
+      // chunk k of this thread's 128 columns: 16 B of row q (rows past R hold
+      // whatever the workspace held; they only feed their own, unused, rows)
+      const uint4* src = (const uint4*)(p.q_lat) +
+                         (((size_t)b * p.rtiles + tile) * 64 + 32 * rank + 16 * wg) * 128 + q;
       uint32_t v[64];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const uint4 x = have ? src[k] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 x = src[(size_t)k * 128];
         v[4 * k] = x.x;
         v[4 * k + 1] = x.y;
         v[4 * k + 2] = x.z;
@@ -600,8 +626,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     pdl_launch_dependents();   // let the merge kernel start its prologue
     tc_fence_after();
     const bool live = row < p.R;
-    float* op = p.o_part + (((size_t)b * p.splits + split) * p.R + (live ? row : 0)) * kLat +
-                rank * 256 + 128 * wg;
+    // This CTA's O half (128 rows x 256 fp32) goes through the drained KV
+    // stages as eight 128-byte-swizzled boxes of 32 columns, then out with TMA
+    // stores (rows past R are clipped), so no thread writes a strided row.
     for (int c = 0; c < 128; c += 16) {
       uint32_t v[16];
       if (ntiles > 0) {
@@ -611,16 +638,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = 0u;
       }
-      if (live) {
 #pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *(float4*)(op + c + e) =
-              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                          __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+      for (int u = 0; u < 4; ++u) {
+        const int col = 128 * wg + c + 4 * u;
+        const uint32_t addr = sKV + (col >> 5) * (BM * 128) + q * 128 +
+                              ((((col & 31) >> 2) ^ (q & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[4 * u]),
+                     "r"(v[4 * u + 1]), "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
+                     : "memory");
       }
     }
+    fence_async_shared();
     if (wg == 1) lsum[q] = l_part;
     named_bar_sync(1, SOFTMAX_THREADS);
+    if (sm_tid == 0) {
+      for (int bx = 0; bx < 8; ++bx)
+        tma_store_3d(&tm_op, sKV + bx * (BM * 128), (int)rank * 256 + 32 * bx, row0,
+                     b * p.splits + split);
+      bulk_commit();
+      bulk_wait_all();
+    }
     if (live && rank == 0 && wg == 0) {
       float* mlp = p.ml + (((size_t)b * p.splits + split) * p.R + row) * 2;
       mlp[0] = m_run == -INFINITY ? -FLT_MAX : m_run;
@@ -637,8 +674,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
 // merge of the split-KV pieces
 // =========================================================================
 // o_lat[row] = sum_s 2^(m_s - M) O_s[row] / sum_s 2^(m_s - M) l_s  (bf16).
-// One CTA per query row: 4 groups of 64 threads take every 4th piece, each
-// thread 8 latent columns; the groups' sums are added in shared memory.
+// One CTA per (query row, 32*4*CPL-column slice): warp w takes every 4th
+// piece, each lane CPL float4 columns, with its own running maximum (rescaled
+// when a piece's maximum is larger, so there is no separate max pass and the
+// loads of several pieces are in flight at once); the four warps' sums are
+// combined in shared memory.  CPL = 1 when pieces are many (more CTAs, fewer
+// loads each), 4 when they are few.
 struct MergeParams {
   const float* o_part;   // [B, splits, R, 512]
   const float* ml;       // [B, splits, R, 2]
@@ -647,46 +688,88 @@ struct MergeParams {
   int R, chunk, splits;
 };
 
-__global__ void __launch_bounds__(256) merge_sm103(MergeParams p) {
-  __shared__ float part[4][kLat];
-  __shared__ float den_part[4];
+template <int CPL>
+__global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
+  constexpr int NBATCH = 16 / CPL;  // pieces whose loads are in flight together
+  __shared__ float4 part[4][32 * CPL];
+  __shared__ float mden[4][2];
+  // the unembedding may start loading its weights now; it waits for this grid
+  // before reading o_lat
+  pdl_launch_dependents();
   pdl_wait();
   const int rg = blockIdx.x;  // b*R + row
+  const int col0 = blockIdx.y * 128 * CPL;
   const int b = rg / p.R, row = rg - b * p.R;
-  const int g = threadIdx.x >> 6, t = threadIdx.x & 63;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
   const size_t base = (size_t)b * p.splits * p.R + row;
-  float M = -FLT_MAX;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.ml[(base + (size_t)s * p.R) * 2]);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float den = 0.f;
-#pragma unroll 4
-  for (int s = g; s < nsplit; s += 4) {
-    const float* mls = p.ml + (base + (size_t)s * p.R) * 2;
-    const float ls = mls[1];
-    const float w = ls > 0.f ? ex2(mls[0] - M) : 0.f;
-    den += w * ls;
-    const float* o = p.o_part + (base + (size_t)s * p.R) * kLat + 8 * t;
-    const float4 x0 = *(const float4*)o;
-    const float4 x1 = *(const float4*)(o + 4);
-    acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-    acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+  const size_t stride = (size_t)p.R;
+  float M = -FLT_MAX, den = 0.f;
+  float4 acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = w; s0 < nsplit; s0 += 4 * NBATCH) {
+    float2 mls[NBATCH];
+    float4 x[NBATCH][CPL];
+#pragma unroll
+    for (int k = 0; k < NBATCH; ++k) {
+      const int s = s0 + 4 * k;
+      const size_t e = base + (size_t)min(s, nsplit - 1) * stride;
+      mls[k] = *(const float2*)(p.ml + e * 2);
+      const float* o = p.o_part + e * kLat + col0 + 4 * lane;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) x[k][c] = *(const float4*)(o + 128 * c);
+      if (s >= nsplit) mls[k].y = 0.f;  // past the last piece: weight 0
+    }
+#pragma unroll
+    for (int k = 0; k < NBATCH; ++k) {
+      if (mls[k].y > 0.f) {
+        if (mls[k].x > M) {  // warp-uniform: every lane reads the same (m, l)
+          const float f = ex2(M - mls[k].x);
+          M = mls[k].x;
+          den *= f;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            acc[c].x *= f; acc[c].y *= f; acc[c].z *= f; acc[c].w *= f;
+          }
+        }
+        const float wt = ex2(mls[k].x - M);
+        den += wt * mls[k].y;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          acc[c].x += wt * x[k][c].x; acc[c].y += wt * x[k][c].y;
+          acc[c].z += wt * x[k][c].z; acc[c].w += wt * x[k][c].w;
+        }
+      }
+    }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) part[g][8 * t + e] = acc[e];
-  if (t == 0) den_part[g] = den;
+  for (int c = 0; c < CPL; ++c) part[w][32 * c + lane] = acc[c];
+  if (lane == 0) {
+    mden[w][0] = M;
+    mden[w][1] = den;
+  }
   __syncthreads();
-  pdl_launch_dependents();
-  if (g == 0) {
-    const float inv = 1.f / (den_part[0] + den_part[1] + den_part[2] + den_part[3]);
-    uint32_t pk[4];
+  if (w == 0) {
+    const float Mall = fmaxf(fmaxf(mden[0][0], mden[1][0]), fmaxf(mden[2][0], mden[3][0]));
+    float f[4], dsum = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int c = 8 * t + 2 * e;
-      pk[e] = pack_bf16((part[0][c] + part[1][c] + part[2][c] + part[3][c]) * inv,
-                        (part[0][c + 1] + part[1][c + 1] + part[2][c + 1] + part[3][c + 1]) * inv);
+    for (int g = 0; g < 4; ++g) {
+      f[g] = mden[g][1] > 0.f ? ex2(mden[g][0] - Mall) : 0.f;
+      dsum += f[g] * mden[g][1];
     }
-    *(uint4*)(p.o_lat + (size_t)rg * kLat + 8 * t) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const float4 z = part[g][32 * c + lane];
+        y.x += f[g] * z.x; y.y += f[g] * z.y; y.z += f[g] * z.z; y.w += f[g] * z.w;
+      }
+      *(uint2*)(p.o_lat + (size_t)rg * kLat + col0 + 128 * c + 4 * lane) =
+          make_uint2(pack_bf16(y.x * inv, y.y * inv), pack_bf16(y.z * inv, y.w * inv));
+    }
   }
 }
 
@@ -744,7 +827,7 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
       c.page_table ? (long long)c.num_pages * c.page_size
                    : (long long)(p.B - 1) * c.seq_stride + p.Tmax;
 
-  CUtensorMap tm_wuk, tm_qn, tm_qr, tm_ckv, tm_kr, tm_wuv, tm_ol;
+  CUtensorMap tm_wuk, tm_qn, tm_qr, tm_ckv, tm_kr, tm_wuv, tm_ol, tm_op;
   const int NBf = gemm_rows(BL, p.n), NBu = gemm_rows(BL, kLat);
   bool ok = make_tmap_bf16_2d(&tm_wuk, a.W_UK, kLat, (uint64_t)p.H * p.n, kLat * 2, 64, 64, 128);
   ok = ok && make_tmap_bf16_2d(&tm_qn, a.q_nope, (uint64_t)p.H * p.n, BL, (uint64_t)p.H * p.n * 2,
@@ -756,6 +839,8 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
                                64, 128);
   ok = ok && make_tmap_bf16_2d(&tm_ol, o_lat, (uint64_t)p.H * kLat, BL, (uint64_t)p.H * kLat * 2,
                                64, NBu, 128);
+  ok = ok && make_tmap_f32_3d(&tm_op, o_part, kLat, R, (uint64_t)p.B * p.splits, kLat * 4,
+                              (uint64_t)R * kLat * 4, 32, BM);
   if (!ok) return cudaErrorInvalidValue;
 
   static bool attrs[64] = {};
@@ -773,7 +858,7 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   }
   cudaError_t e;
   {
-    GemmParams gp{q_lat, BL, p.H, p.n, kLat, NBf};
+    GemmParams gp{q_lat, BL, p.H, p.n, kLat, NBf, p.L, (R + BM - 1) / BM};
     KernelTimer kt("fold_sm103", a.stream);
     e = launch_pdl(swapab_gemm_sm103, dim3(kLat / 128, p.H, (BL + NBf - 1) / NBf), dim3(128),
                    gemm_smem(p.n, NBf), a.stream, tm_wuk, tm_qn, gp);
@@ -791,25 +876,31 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.L = p.L;
     ap.H = p.H;
     ap.R = R;
+    ap.rtiles = (R + BM - 1) / BM;
     ap.chunk = p.chunk;
     ap.splits = p.splits;
     ap.sl2 = p.scale * 1.4426950408889634f;
     ap.o_part = o_part;
     ap.ml = ml;
+    ap.pf = (const char*)a.W_UV;
+    ap.pf_bytes = (size_t)p.H * kLat * p.v * 2;
     KernelTimer kt("absorbed_attn_sm103", a.stream);
     e = launch_pdl(absorbed_attn_sm103, dim3(2 * ((R + BM - 1) / BM), p.splits, p.B),
                    dim3(ATTN_THREADS),
-                   ATTN_SMEM, a.stream, tm_qr, tm_ckv, tm_kr, ap);
+                   ATTN_SMEM, a.stream, tm_qr, tm_ckv, tm_kr, tm_op, ap);
     if (e != cudaSuccess) return e;
   }
   {
     MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits};
     KernelTimer kt("merge_sm103", a.stream);
-    e = launch_pdl(merge_sm103, dim3(p.B * R), dim3(256), 0, a.stream, mp);
+    if (p.splits >= 16)
+      e = launch_pdl(merge_sm103<1>, dim3(p.B * R, 4), dim3(128), 0, a.stream, mp);
+    else
+      e = launch_pdl(merge_sm103<4>, dim3(p.B * R, 1), dim3(128), 0, a.stream, mp);
     if (e != cudaSuccess) return e;
   }
   {
-    GemmParams gp{(__nv_bfloat16*)a.out, BL, p.H, kLat, p.v, NBu};
+    GemmParams gp{(__nv_bfloat16*)a.out, BL, p.H, kLat, p.v, NBu, 0, 0};
     KernelTimer kt("unembed_sm103", a.stream);
     e = launch_pdl(swapab_gemm_sm103, dim3(p.v / 128, p.H, (BL + NBu - 1) / NBu), dim3(128),
                    gemm_smem(kLat, NBu), a.stream, tm_wuv, tm_ol, gp);

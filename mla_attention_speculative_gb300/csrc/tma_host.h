@@ -22,5 +22,9 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t planes, uint64_t row_stride_bytes, uint64_t plane_stride_bytes,
                        uint32_t box_inner, uint32_t box_rows);
+// The same for fp32 elements (box_inner = 32).
+bool make_tmap_f32_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                      uint64_t planes, uint64_t row_stride_bytes, uint64_t plane_stride_bytes,
+                      uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace mla
