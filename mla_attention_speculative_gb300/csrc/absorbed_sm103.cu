@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
+  // The next kernel may launch now and start its own independent loads; it
+  // waits for this grid before reading what it writes.
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     bool ok = true;
@@ -157,7 +160,6 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
     if (!ok) *fail = 1;
   }
   __syncthreads();
-  pdl_launch_dependents();
   tc_fence_after();
   if (!*fail) {
     const int m = mt * 128 + warp * 32 + lane;
@@ -205,8 +207,8 @@ constexpr int OFF_P = OFF_KV + STAGES * KV_STAGE;   // two P buffers
 constexpr int OFF_X = OFF_P + 2 * P_TILE;           // the peer's partial scores land here
 constexpr int OFF_STG = OFF_X + X_BYTES;            // this CTA's partial scores, outgoing
 constexpr int OFF_RED = OFF_STG + X_BYTES;          // row maxima of the two warpgroups
-constexpr int OFF_LS = OFF_RED + 2 * BM * 4;        // row sums, second warpgroup
-constexpr int OFF_BAR = OFF_LS + BM * 4;
+constexpr int OFF_LS = OFF_RED + 2 * BM * 4;        // row sums of the two warpgroups
+constexpr int OFF_BAR = OFF_LS + 2 * BM * 4;
 constexpr int ATTN_SMEM = OFF_BAR + 256 + 1024;     // + barriers + alignment slack
 // Tensor memory: O half [0,256) fp32; this CTA's 256 latent query columns as
 // bf16 pairs [256,384) (the A operand of the score MMAs); S buffers [384,512).
@@ -230,8 +232,8 @@ struct AttnParams {
   int B;
   int chunk, splits;  // KV rows per split (multiple of 64), splits per sequence (max)
   float sl2;          // softmax scale * log2(e)
-  float* o_part;      // [B, splits, R, 512]
-  float* ml;          // [B, splits, R, 2]
+  __nv_bfloat16* o_part;  // [B, splits, R, 512]: O / l of each piece
+  float* ml;              // [B, splits, R, 2]: (m, l) of each piece
   const char* pf;     // W_UV, pulled into L2 while the attention runs
   size_t pf_bytes;
 };
@@ -349,6 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist (and are armed) before any remote access
   const uint32_t tmem = *slot;
+  pdl_launch_dependents();  // the merge may launch; it waits for this grid
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -622,13 +625,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     if (sm_tid == 0) bulk_wait_read();
     // ---------------------------------------------------------------- epilogue
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
-    pdl_wait();                // the partials may still be read by an earlier merge
-    pdl_launch_dependents();   // let the merge kernel start its prologue
+    pdl_wait();  // the partials may still be read by the previous call's merge
     tc_fence_after();
     const bool live = row < p.R;
-    // This CTA's O half (128 rows x 256 fp32) goes through the drained KV
-    // stages as eight 128-byte-swizzled boxes of 32 columns, then out with TMA
-    // stores (rows past R are clipped), so no thread writes a strided row.
+    // The row's total l: the sum of the two warpgroups' shares (both CTAs of the
+    // pair hold the same P, so their totals agree).
+    lsum[wg * BM + q] = l_part;
+    named_bar_sync(1, SOFTMAX_THREADS);
+    const float l_tot = lsum[q] + lsum[BM + q];
+    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+    // This CTA's half of O / l (128 rows x 256 columns, bf16) goes through the
+    // drained KV stages as four 128-byte-swizzled boxes of 64 columns, then
+    // out with TMA stores (rows past R are clipped).
     for (int c = 0; c < 128; c += 16) {
       uint32_t v[16];
       if (ntiles > 0) {
@@ -639,21 +647,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         for (int e = 0; e < 16; ++e) v[e] = 0u;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int col = 128 * wg + c + 4 * u;
-        const uint32_t addr = sKV + (col >> 5) * (BM * 128) + q * 128 +
-                              ((((col & 31) >> 2) ^ (q & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[4 * u]),
-                     "r"(v[4 * u + 1]), "r"(v[4 * u + 2]), "r"(v[4 * u + 3])
+      for (int u = 0; u < 2; ++u) {
+        const int col = 128 * wg + c + 8 * u;
+        const uint32_t addr = sKV + (col >> 6) * (BM * 128) + q * 128 +
+                              ((((col & 63) >> 3) ^ (q & 7)) << 4);
+        const uint32_t* w = v + 8 * u;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                     "r"(pack_bf16(__uint_as_float(w[0]) * inv, __uint_as_float(w[1]) * inv)),
+                     "r"(pack_bf16(__uint_as_float(w[2]) * inv, __uint_as_float(w[3]) * inv)),
+                     "r"(pack_bf16(__uint_as_float(w[4]) * inv, __uint_as_float(w[5]) * inv)),
+                     "r"(pack_bf16(__uint_as_float(w[6]) * inv, __uint_as_float(w[7]) * inv))
                      : "memory");
       }
     }
     fence_async_shared();
-    if (wg == 1) lsum[q] = l_part;
     named_bar_sync(1, SOFTMAX_THREADS);
     if (sm_tid == 0) {
-      for (int bx = 0; bx < 8; ++bx)
-        tma_store_3d(&tm_op, sKV + bx * (BM * 128), (int)rank * 256 + 32 * bx, row0,
+      for (int bx = 0; bx < 4; ++bx)
+        tma_store_3d(&tm_op, sKV + bx * (BM * 128), (int)rank * 256 + 64 * bx, row0,
                      b * p.splits + split);
       bulk_commit();
       bulk_wait_all();
@@ -661,7 +672,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     if (live && rank == 0 && wg == 0) {
       float* mlp = p.ml + (((size_t)b * p.splits + split) * p.R + row) * 2;
       mlp[0] = m_run == -INFINITY ? -FLT_MAX : m_run;
-      mlp[1] = l_part + lsum[q];
+      mlp[1] = l_tot;
     }
   }
   tc_fence_before();
@@ -673,52 +684,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
 // =========================================================================
 // merge of the split-KV pieces
 // =========================================================================
-// o_lat[row] = sum_s 2^(m_s - M) O_s[row] / sum_s 2^(m_s - M) l_s  (bf16).
-// One CTA per (query row, 32*4*CPL-column slice): warp w takes every 4th
-// piece, each lane CPL float4 columns, with its own running maximum (rescaled
-// when a piece's maximum is larger, so there is no separate max pass and the
-// loads of several pieces are in flight at once); the four warps' sums are
-// combined in shared memory.  CPL = 1 when pieces are many (more CTAs, fewer
-// loads each), 4 when they are few.
+// o_lat[row] = sum_s w_s (O_s / l_s)[row] / sum_s w_s with w_s = 2^(m_s - M) l_s
+// (bf16 out).  One CTA per (query row, 256*CPL-column slice): warp w takes every
+// 4th piece, each lane CPL groups of 8 columns, with its own running maximum
+// (raised, and the sums rescaled, when a piece's maximum is larger), so there
+// is no separate max pass and the loads of many pieces are in flight at once;
+// the four warps' sums are combined in shared memory.  CPL = 1 when pieces are
+// many (more CTAs, fewer loads each), 2 when they are few.
 struct MergeParams {
-  const float* o_part;   // [B, splits, R, 512]
-  const float* ml;       // [B, splits, R, 2]
+  const __nv_bfloat16* o_part;  // [B, splits, R, 512]
+  const float* ml;              // [B, splits, R, 2]
   const int32_t* lens;
-  __nv_bfloat16* o_lat;  // [B*R, 512]
+  __nv_bfloat16* o_lat;         // [B*R, 512]
   int R, chunk, splits;
 };
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
 
 template <int CPL>
 __global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
   constexpr int NBATCH = 16 / CPL;  // pieces whose loads are in flight together
-  __shared__ float4 part[4][32 * CPL];
+  __shared__ float part[4][CPL * 8][32];
   __shared__ float mden[4][2];
   // the unembedding may start loading its weights now; it waits for this grid
   // before reading o_lat
   pdl_launch_dependents();
   pdl_wait();
   const int rg = blockIdx.x;  // b*R + row
-  const int col0 = blockIdx.y * 128 * CPL;
+  const int col0 = blockIdx.y * 256 * CPL;
   const int b = rg / p.R, row = rg - b * p.R;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
   const size_t base = (size_t)b * p.splits * p.R + row;
   const size_t stride = (size_t)p.R;
   float M = -FLT_MAX, den = 0.f;
-  float4 acc[CPL];
+  float acc[CPL][8];
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < CPL; ++c)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[c][e] = 0.f;
   for (int s0 = w; s0 < nsplit; s0 += 4 * NBATCH) {
     float2 mls[NBATCH];
-    float4 x[NBATCH][CPL];
+    uint4 x[NBATCH][CPL];
 #pragma unroll
     for (int k = 0; k < NBATCH; ++k) {
       const int s = s0 + 4 * k;
       const size_t e = base + (size_t)min(s, nsplit - 1) * stride;
       mls[k] = *(const float2*)(p.ml + e * 2);
-      const float* o = p.o_part + e * kLat + col0 + 4 * lane;
+      const __nv_bfloat16* o = p.o_part + e * kLat + col0 + 8 * lane;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) x[k][c] = *(const float4*)(o + 128 * c);
+      for (int c = 0; c < CPL; ++c) x[k][c] = *(const uint4*)(o + 256 * c);
       if (s >= nsplit) mls[k].y = 0.f;  // past the last piece: weight 0
     }
 #pragma unroll
@@ -729,22 +751,26 @@ __global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
           M = mls[k].x;
           den *= f;
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            acc[c].x *= f; acc[c].y *= f; acc[c].z *= f; acc[c].w *= f;
-          }
+          for (int c = 0; c < CPL; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[c][e] *= f;
         }
-        const float wt = ex2(mls[k].x - M);
-        den += wt * mls[k].y;
+        const float wt = ex2(mls[k].x - M) * mls[k].y;
+        den += wt;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-          acc[c].x += wt * x[k][c].x; acc[c].y += wt * x[k][c].y;
-          acc[c].z += wt * x[k][c].z; acc[c].w += wt * x[k][c].w;
+          float f[8];
+          bf16x8_to_f32(x[k][c], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[c][e] += wt * f[e];
         }
       }
     }
   }
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) part[w][32 * c + lane] = acc[c];
+  for (int c = 0; c < CPL; ++c)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[w][8 * c + e][lane] = acc[c][e];
   if (lane == 0) {
     mden[w][0] = M;
     mden[w][1] = den;
@@ -761,14 +787,14 @@ __global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
     const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
-      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+      float y[8];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const float4 z = part[g][32 * c + lane];
-        y.x += f[g] * z.x; y.y += f[g] * z.y; y.z += f[g] * z.z; y.w += f[g] * z.w;
-      }
-      *(uint2*)(p.o_lat + (size_t)rg * kLat + col0 + 128 * c + 4 * lane) =
-          make_uint2(pack_bf16(y.x * inv, y.y * inv), pack_bf16(y.z * inv, y.w * inv));
+      for (int e = 0; e < 8; ++e)
+        y[e] = (f[0] * part[0][8 * c + e][lane] + f[1] * part[1][8 * c + e][lane] +
+                f[2] * part[2][8 * c + e][lane] + f[3] * part[3][8 * c + e][lane]) * inv;
+      *(uint4*)(p.o_lat + (size_t)rg * kLat + col0 + 256 * c + 8 * lane) =
+          make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                     pack_bf16(y[6], y[7]));
     }
   }
 }
@@ -819,7 +845,7 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   const int BL = p.B * p.L;
   const int R = p.L * p.H;
   __nv_bfloat16* q_lat = (__nv_bfloat16*)(a.ws + p.off_qlat);
-  float* o_part = (float*)(a.ws + p.off_opart);
+  __nv_bfloat16* o_part = (__nv_bfloat16*)(a.ws + p.off_opart);
   float* ml = (float*)(a.ws + p.off_ml);
   __nv_bfloat16* o_lat = (__nv_bfloat16*)(a.ws + p.off_olat);
   const CacheView& c = a.cache;
@@ -839,8 +865,8 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
                                64, 128);
   ok = ok && make_tmap_bf16_2d(&tm_ol, o_lat, (uint64_t)p.H * kLat, BL, (uint64_t)p.H * kLat * 2,
                                64, NBu, 128);
-  ok = ok && make_tmap_f32_3d(&tm_op, o_part, kLat, R, (uint64_t)p.B * p.splits, kLat * 4,
-                              (uint64_t)R * kLat * 4, 32, BM);
+  ok = ok && make_tmap_bf16_3d(&tm_op, o_part, kLat, R, (uint64_t)p.B * p.splits, kLat * 2,
+                               (uint64_t)R * kLat * 2, 64, BM);
   if (!ok) return cudaErrorInvalidValue;
 
   static bool attrs[64] = {};
@@ -894,9 +920,9 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits};
     KernelTimer kt("merge_sm103", a.stream);
     if (p.splits >= 16)
-      e = launch_pdl(merge_sm103<1>, dim3(p.B * R, 4), dim3(128), 0, a.stream, mp);
+      e = launch_pdl(merge_sm103<1>, dim3(p.B * R, 2), dim3(128), 0, a.stream, mp);
     else
-      e = launch_pdl(merge_sm103<4>, dim3(p.B * R, 1), dim3(128), 0, a.stream, mp);
+      e = launch_pdl(merge_sm103<2>, dim3(p.B * R, 1), dim3(128), 0, a.stream, mp);
     if (e != cudaSuccess) return e;
   }
   {

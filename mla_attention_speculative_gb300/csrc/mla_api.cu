@@ -231,8 +231,8 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     size_t off = 0;
     f.off_qlat = off;  // Q tiles: every sequence's rows padded to 128-row tiles
     off = align256(off + (size_t)batch * row_tiles * 128 * p->r * 2);
-    f.off_opart = off;
-    off = align256(off + nrow * f.splits * p->r * sizeof(float));
+    f.off_opart = off;  // bf16 O / l of every piece
+    off = align256(off + nrow * f.splits * p->r * 2);
     f.off_ml = off;
     off = align256(off + nrow * f.splits * 2 * sizeof(float));
     f.off_olat = off;
