@@ -273,16 +273,12 @@ __device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t l
   mbar_arrive(bar_sfree0 + 8 * sb);
 }
 
-// Row q's 16 fp16 pairs (columns c0..c0+31) into a [128][64] exchange tile
-// (16-byte chunks XOR-swizzled by row so the 32 rows of a warp hit distinct banks).
-__device__ __forceinline__ void put_partial(uint32_t tile, int q, int c0, const uint32_t (&h)[16]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int c = (c0 >> 3) + k;
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + q * 128 + ((c ^ (q & 7)) << 4)),
-                 "r"(h[4 * k]), "r"(h[4 * k + 1]), "r"(h[4 * k + 2]), "r"(h[4 * k + 3])
-                 : "memory");
-  }
+// Exchange tile layout: [warpgroup][128 rows][64 B] (the row's 32 fp16
+// partial scores of that warpgroup's columns), 16-byte chunks XOR-swizzled by
+// row so a warp's stores hit distinct banks.  The 32 rows of one warp are one
+// contiguous 2 KB block, which that warp ships to the peer on its own.
+__device__ __forceinline__ uint32_t xchg_offset(int wg, int q, int c) {
+  return (uint32_t)(wg * (BM * 64) + q * 64 + ((c ^ ((q >> 1) & 3)) << 4));
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
@@ -449,8 +445,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // ------------------------------------------------- softmax warpgroups
     // Two warpgroups: thread (wg, q) owns row q, score columns 32wg..32wg+31 and
     // O columns 128wg..128wg+127.  Tile i's scores are finished (own + peer
-    // partial) while tile i+1's partial is already on its way to the peer (one
-    // bulk copy of the staged tile).
+    // partial) while tile i+1's partial is already on its way: each warp stages
+    // its 32 rows (2 KB) and ships them to the peer with one bulk copy, so the
+    // exchange needs no block-wide barrier.
     const int wg = (warp - 2) >> 2;
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
     const int c0 = 32 * wg;
@@ -459,6 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     const int l = min(row, p.R - 1) / p.H;
     const int last_t = T - p.L + l;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t wblock = (uint32_t)(wg * (BM * 64) + (warp & 3) * 32 * 64);  // this warp's 2 KB
     const uint32_t peer_x = mapa(sX, peer);
     const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
     const uint32_t peer_xfree = mapa(bar(B_XFREE), peer);
@@ -466,6 +464,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     int armed = ntiles > 0 ? 1 : 0, received = 0;  // exchange phases armed / completed
     float m_run = -INFINITY, l_part = 0.f;
     float s[32];
+    // tile j's own partial of row q to the peer (this warp's block of it)
+    auto send = [&](int j, const uint32_t (&h)[16]) {
+      if (lane == 0) {
+        bulk_wait_read();  // this warp's previous copy has left the staging block
+        // the peer has read tile j-1 out of its exchange tile
+        if (j >= 1) wait_cluster_or_fail(ok, bar(B_XFREE), (j - 1) & 1, 21);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sStg + xchg_offset(wg, q, k)),
+                     "r"(h[4 * k]), "r"(h[4 * k + 1]), "r"(h[4 * k + 2]), "r"(h[4 * k + 3])
+                     : "memory");
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0 && ok) bulk_copy_to_peer(peer_x + wblock, sStg + wblock, 32 * 64, peer_xfull);
+    };
     if (ntiles > 0) {
       // this CTA's latent query columns into TMEM as bf16 pairs (the fold wrote them)
       pdl_wait();
@@ -489,10 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_arrive(bar(B_QTMEM));
       uint32_t h0[16];
       load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s, h0);
-      put_partial(sStg, q, c0, h0);
-      fence_async_shared();
-      named_bar_sync(1, SOFTMAX_THREADS);
-      if (sm_tid == 0 && ok) bulk_copy_to_peer(peer_x, sStg, X_BYTES, peer_xfull);
+      send(0, h0);
     }
     // One tile of the softmax; `s` holds tile i's own (rounded) partial on entry
     // and `sn` receives tile i+1's.  Called with the two arrays alternating so
@@ -508,10 +520,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t h[4];
-        const int c = (c0 >> 3) + k;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-                     : "r"(sX + q * 128 + ((c ^ (q & 7)) << 4)));
+                     : "r"(sX + xchg_offset(wg, q, k)));
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
@@ -540,21 +551,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         // returned (its values were used before the bar.sync), so no fence
         mbar_arrive_remote_relaxed(peer_xfree);
       }
-      // start tile i+1's exchange
+      // tile i+1's partial to the peer
       if (i + 1 < ntiles) {
         uint32_t hn[16];
         load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn, hn);
-        if (sm_tid == 0) {
-          wait_cluster_or_fail(ok, bar(B_XFREE), i & 1, 21);  // the peer has read my tile i
-          bulk_wait_read();                                  // my staging tile is free
-        }
-        named_bar_sync(1, SOFTMAX_THREADS);
-        put_partial(sStg, q, c0, hn);
-        fence_async_shared();
-        named_bar_sync(1, SOFTMAX_THREADS);
-        if (sm_tid == 0 && ok) bulk_copy_to_peer(peer_x, sStg, X_BYTES, peer_xfull);
+        send(i + 1, hn);
       }
-      // lazy rescale: move the running max only when it grows by more than 2^8;
+    // lazy rescale: move the running max only when it grows by more than 2^8;
       // O must then hold every earlier P.V
       const bool need = mt > m_run + 8.f;
       const float m_new = need ? mt : m_run;
@@ -622,7 +625,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // after a failure, let an armed exchange phase finish (or time out) so no
     // copy from the peer is still landing when this CTA exits
     if (sm_tid == 0 && received < armed) mbar_wait_cluster(bar(B_XFULL), received & 1);
-    if (sm_tid == 0) bulk_wait_read();
+    if (lane == 0) bulk_wait_read();
     // ---------------------------------------------------------------- epilogue
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
     pdl_wait();  // the partials may still be read by the previous call's merge
