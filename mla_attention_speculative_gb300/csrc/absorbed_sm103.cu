@@ -193,7 +193,10 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
 constexpr int BM = 128;                 // query rows per tile
 constexpr int BN = 64;                  // cached positions per KV tile
 constexpr int STAGES = 4;
-constexpr int SOFTMAX_THREADS = 256;    // two warpgroups, 32 of a row's 64 scores each
+constexpr int NWG = 2;                  // softmax warpgroups; each takes 1/NWG of a row
+constexpr int CPT = 64 / NWG;           // score columns per softmax thread
+constexpr int OPT = 256 / NWG;          // O (and latent Q) columns per softmax thread
+constexpr int SOFTMAX_THREADS = 128 * NWG;
 constexpr int ATTN_THREADS = 64 + SOFTMAX_THREADS;
 constexpr int Q_ROPE = BM * 64;         // the 32 RoPE columns of this CTA's Q rows (64-B swizzle)
 constexpr int KV_CHUNK = BN * 128;      // one 64-column bf16 chunk of a KV tile
@@ -203,12 +206,12 @@ constexpr int X_BYTES = BM * BN * 2;    // partial scores of a tile, fp16 [128][
 constexpr int OFF_QR = 0;
 constexpr int OFF_KV = OFF_QR + Q_ROPE;
 constexpr int KV_STAGE = 4 * KV_CHUNK + KV_ROPE;
-constexpr int OFF_P = OFF_KV + STAGES * KV_STAGE;   // two P buffers
-constexpr int OFF_X = OFF_P + 2 * P_TILE;           // the peer's partial scores land here
-constexpr int OFF_STG = OFF_X + X_BYTES;            // this CTA's partial scores, outgoing
-constexpr int OFF_RED = OFF_STG + X_BYTES;          // row maxima of the two warpgroups
-constexpr int OFF_LS = OFF_RED + 2 * BM * 4;        // row sums of the two warpgroups
-constexpr int OFF_BAR = OFF_LS + 2 * BM * 4;
+constexpr int OFF_P = OFF_KV + STAGES * KV_STAGE;   // the P tile
+constexpr int OFF_X = OFF_P + P_TILE;               // the peer's partial scores land here (x2)
+constexpr int OFF_STG = OFF_X + 2 * X_BYTES;        // this CTA's partial scores, outgoing
+constexpr int OFF_RED = OFF_STG + X_BYTES;          // row maxima of the warpgroups
+constexpr int OFF_LS = OFF_RED + NWG * BM * 4;      // row sums of the warpgroups
+constexpr int OFF_BAR = OFF_LS + NWG * BM * 4;
 constexpr int ATTN_SMEM = OFF_BAR + 256 + 1024;     // + barriers + alignment slack
 // Tensor memory: O half [0,256) fp32; this CTA's 256 latent query columns as
 // bf16 pairs [256,384) (the A operand of the score MMAs); S buffers [384,512).
@@ -242,26 +245,27 @@ struct AttnParams {
 // copies that it cannot complete twice before its waiter looks.
 enum {
   B_QFULL = 0, B_QTMEM = 1, B_KVFULL = 2, B_KVEMPTY = 6, B_SFULL = 10, B_SFREE = 12,
-  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 19, B_DRAIN = 20, B_COUNT = 21
+  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22, B_COUNT = 23
 };
 
-// This thread's 32 partial scores of tile j (columns c0..c0+31 of this CTA's
-// share) from TMEM, scaled to log2-softmax units and rounded to fp16 pairs:
-// `h` is what goes to the peer, `s` the same rounded values in fp32.  Both
-// CTAs add the same two rounded partials, so their sums agree bit for bit.
+// This thread's CPT partial scores of tile j (columns c0..c0+CPT-1 of this
+// CTA's share) from TMEM, scaled to log2-softmax units and rounded to fp16
+// pairs: `h` is what goes to the peer, `s` the same rounded values in fp32.
+// Both CTAs add the same two rounded partials, so their sums agree bit for bit.
 // (Packed conversions: the scalar ones would crowd the pipe the exponentials need.)
 __device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t lane_base, int c0,
                                              int j, uint32_t bar_sfull0, uint32_t bar_sfree0,
-                                             float sl2, float (&s)[32], uint32_t (&h)[16]) {
+                                             float sl2, float (&s)[CPT], uint32_t (&h)[CPT / 2]) {
   const int sb = j & (SBUF - 1);
   wait_or_fail(ok, bar_sfull0 + 8 * sb, (j / SBUF) & 1, 20);
   tc_fence_after();
-  uint32_t v[32];
-  tmem_ld16(tmem + lane_base + TM_S + sb * BN + c0, *(uint32_t(*)[16])(v));
-  tmem_ld16(tmem + lane_base + TM_S + sb * BN + c0 + 16, *(uint32_t(*)[16])(v + 16));
+  uint32_t v[CPT];
+#pragma unroll
+  for (int k = 0; k < CPT / 16; ++k)
+    tmem_ld16(tmem + lane_base + TM_S + sb * BN + c0 + 16 * k, *(uint32_t(*)[16])(v + 16 * k));
   tmem_wait_ld();
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
+  for (int e = 0; e < CPT / 2; ++e) {
     const __half2 x = __floats2half2_rn(__uint_as_float(v[2 * e]) * sl2,
                                         __uint_as_float(v[2 * e + 1]) * sl2);
     h[e] = *reinterpret_cast<const uint32_t*>(&x);
@@ -273,12 +277,15 @@ __device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t l
   mbar_arrive(bar_sfree0 + 8 * sb);
 }
 
-// Exchange tile layout: [warpgroup][128 rows][64 B] (the row's 32 fp16
+// Exchange tile layout: [warpgroup][128 rows][2*CPT B] (the row's CPT fp16
 // partial scores of that warpgroup's columns), 16-byte chunks XOR-swizzled by
 // row so a warp's stores hit distinct banks.  The 32 rows of one warp are one
-// contiguous 2 KB block, which that warp ships to the peer on its own.
+// contiguous block, which that warp ships to the peer on its own.
+constexpr int XROW = 2 * CPT;                   // bytes per row and warpgroup
+constexpr int XCH = XROW / 16;                  // 16-byte chunks per row and warpgroup
 __device__ __forceinline__ uint32_t xchg_offset(int wg, int q, int c) {
-  return (uint32_t)(wg * (BM * 64) + q * 64 + ((c ^ ((q >> 1) & 3)) << 4));
+  const int sw = XCH == 4 ? ((q >> 1) & 3) : XCH == 2 ? ((q >> 2) & 1) : 0;
+  return (uint32_t)(wg * (BM * XROW) + q * XROW + ((c ^ sw) << 4));
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
@@ -334,12 +341,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_init(bar(B_PFULL + s), SOFTMAX_THREADS);
       mbar_init(bar(B_ODONE + s), 1);
     }
-    mbar_init(bar(B_XFULL), 1);
-    mbar_init(bar(B_XFREE), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(B_XFULL + k), 1);
+      mbar_init(bar(B_XFREE + k), 1);
+    }
     mbar_init(bar(B_DRAIN), 1);
     fence_mbar_init();
     // arm the exchange barrier for tile 0 (the peer's bulk copy counts it down)
     if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
+    if (ntiles > 1) mbar_arrive_expect_tx(bar(B_XFULL + 1), X_BYTES);
   }
   if (warp == 1) tmem_alloc(smem_u32(slot), 512);
   tc_fence_before();
@@ -431,7 +441,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         const uint64_t soff = (uint64_t)(sj * (KV_STAGE >> 4));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + TM_O, dp + pb * (P_TILE >> 4) + 2 * ks, dv + soff + ks * 128, id_o,
+          mma_bf16(tmem + TM_O, dp + 2 * ks, dv + soff + ks * 128, id_o,
                    (j > 0 || ks > 0));
         mma_commit(bar(B_ODONE + pb));
         mma_commit(bar(B_KVEMPTY + sj));
@@ -443,43 +453,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     }
   } else {
     // ------------------------------------------------- softmax warpgroups
-    // Two warpgroups: thread (wg, q) owns row q, score columns 32wg..32wg+31 and
-    // O columns 128wg..128wg+127.  Tile i's scores are finished (own + peer
-    // partial) while tile i+1's partial is already on its way: each warp stages
-    // its 32 rows (2 KB) and ships them to the peer with one bulk copy, so the
-    // exchange needs no block-wide barrier.
+    // NWG warpgroups: thread (wg, q) owns row q, score columns CPT*wg.. and O
+    // (and latent Q) columns OPT*wg.. of this CTA's share.  Tile i's scores
+    // are finished (own + peer partial) while tile i+1's partial is already on
+    // its way: each warp stages its 32 rows and ships them to the peer with one
+    // bulk copy, so the exchange needs no block-wide barrier.
     const int wg = (warp - 2) >> 2;
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
-    const int c0 = 32 * wg;
+    const int c0 = CPT * wg;
     const int sm_tid = threadIdx.x - 64;
     const int row = row0 + q;
     const int l = min(row, p.R - 1) / p.H;
     const int last_t = T - p.L + l;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t wblock = (uint32_t)(wg * (BM * 64) + (warp & 3) * 32 * 64);  // this warp's 2 KB
+    const uint32_t wblock = (uint32_t)(wg * (BM * XROW) + (warp & 3) * 32 * XROW);  // this warp's rows
     const uint32_t peer_x = mapa(sX, peer);
     const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
     const uint32_t peer_xfree = mapa(bar(B_XFREE), peer);
     bool ok = true;
-    int armed = ntiles > 0 ? 1 : 0, received = 0;  // exchange phases armed / completed
+    int armed = min(ntiles, 2), received = 0;  // exchange phases armed / completed
     float m_run = -INFINITY, l_part = 0.f;
-    float s[32];
+    float s[CPT];
     // tile j's own partial of row q to the peer (this warp's block of it)
-    auto send = [&](int j, const uint32_t (&h)[16]) {
+    auto send = [&](int j, const uint32_t (&h)[CPT / 2]) {
       if (lane == 0) {
         bulk_wait_read();  // this warp's previous copy has left the staging block
-        // the peer has read tile j-1 out of its exchange tile
-        if (j >= 1) wait_cluster_or_fail(ok, bar(B_XFREE), (j - 1) & 1, 21);
+        // the peer has read tile j-2 out of exchange buffer j&1
+        if (j >= 2) wait_cluster_or_fail(ok, bar(B_XFREE + (j & 1)), ((j - 2) >> 1) & 1, 21);
       }
       __syncwarp();
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
+      for (int k = 0; k < XCH; ++k)
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sStg + xchg_offset(wg, q, k)),
                      "r"(h[4 * k]), "r"(h[4 * k + 1]), "r"(h[4 * k + 2]), "r"(h[4 * k + 3])
                      : "memory");
       fence_async_shared();
       __syncwarp();
-      if (lane == 0 && ok) bulk_copy_to_peer(peer_x + wblock, sStg + wblock, 32 * 64, peer_xfull);
+      if (lane == 0 && ok)
+        bulk_copy_to_peer(peer_x + (j & 1) * X_BYTES + wblock, sStg + wblock, 32 * XROW,
+                          peer_xfull + 8 * (j & 1));
     };
     if (ntiles > 0) {
       // this CTA's latent query columns into TMEM as bf16 pairs (the fold wrote them)
@@ -487,42 +499,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       // chunk k of this thread's 128 columns: 16 B of row q (rows past R hold
       // whatever the workspace held; they only feed their own, unused, rows)
       const uint4* src = (const uint4*)(p.q_lat) +
-                         (((size_t)b * p.rtiles + tile) * 64 + 32 * rank + 16 * wg) * 128 + q;
-      uint32_t v[64];
+                         (((size_t)b * p.rtiles + tile) * 64 + 32 * rank + (OPT / 8) * wg) * 128 +
+                         q;
+      uint32_t v[OPT / 2];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < OPT / 8; ++k) {
         const uint4 x = src[(size_t)k * 128];
         v[4 * k] = x.x;
         v[4 * k + 1] = x.y;
         v[4 * k + 2] = x.z;
         v[4 * k + 3] = x.w;
       }
-      tmem_st32(tmem + lane_base + TM_QL + 64 * wg, *(const uint32_t(*)[32])(v));
-      tmem_st32(tmem + lane_base + TM_QL + 64 * wg + 32, *(const uint32_t(*)[32])(v + 32));
+#pragma unroll
+      for (int k = 0; k < OPT / 64; ++k)
+        tmem_st32(tmem + lane_base + TM_QL + (OPT / 2) * wg + 32 * k,
+                  *(const uint32_t(*)[32])(v + 32 * k));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_QTMEM));
-      uint32_t h0[16];
+      uint32_t h0[CPT / 2];
       load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s, h0);
       send(0, h0);
     }
     // One tile of the softmax; `s` holds tile i's own (rounded) partial on entry
     // and `sn` receives tile i+1's.  Called with the two arrays alternating so
     // the registers swap roles instead of being copied.
-    auto softmax_tile = [&](int i, float (&s)[32], float (&sn)[32]) {
+    auto softmax_tile = [&](int i, float (&s)[CPT], float (&sn)[CPT]) {
       const int t0 = kv0 + i * BN;
       // finish tile i's scores with the peer's partial; the causal verify mask
       // only matters on tiles that reach past the first row's last position
       const bool edge = t0 + BN - 1 > T - p.L;
-      wait_cluster_or_fail(ok, bar(B_XFULL), i & 1, 22);
+      const int xb = i & 1;  // exchange buffer of tile i
+      wait_cluster_or_fail(ok, bar(B_XFULL + xb), (i >> 1) & 1, 22);
       if (ok) received = i + 1;
       float mt = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < XCH; ++k) {
         uint32_t h[4];
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-                     : "r"(sX + xchg_offset(wg, q, k)));
+                     : "r"(sX + xb * X_BYTES + xchg_offset(wg, q, k)));
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
@@ -533,27 +549,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       }
       if (edge) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) s[j] = (t0 + c0 + j <= last_t) ? s[j] : -INFINITY;
+        for (int j = 0; j < CPT; ++j) s[j] = (t0 + c0 + j <= last_t) ? s[j] : -INFINITY;
       }
       float m2[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int j = 4; j < 32; ++j) m2[j & 3] = fmaxf(m2[j & 3], s[j]);
+      for (int j = 4; j < CPT; ++j) m2[j & 3] = fmaxf(m2[j & 3], s[j]);
       mt = fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3]));
       red[wg * BM + q] = mt;
       named_bar_sync(1, SOFTMAX_THREADS);  // exchange tile read by all; row maxima visible
-      mt = fmaxf(mt, red[(1 - wg) * BM + q]);
+#pragma unroll
+      for (int g = 0; g < NWG; ++g) mt = fmaxf(mt, red[g * BM + q]);
       if (sm_tid == 0 && ok) {
-        if (i + 1 < ntiles) {
-          mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);  // arm tile i+1
+        if (i + 2 < ntiles) {
+          mbar_arrive_expect_tx(bar(B_XFULL + xb), X_BYTES);  // arm buffer xb for tile i+2
           ++armed;
         }
-        // the peer may now send tile i+1: every read of the exchange tile has
+        // the peer may now send tile i+2 into buffer xb: every read of it has
         // returned (its values were used before the bar.sync), so no fence
-        mbar_arrive_remote_relaxed(peer_xfree);
+        mbar_arrive_remote_relaxed(peer_xfree + 8 * xb);
       }
       // tile i+1's partial to the peer
       if (i + 1 < ntiles) {
-        uint32_t hn[16];
+        uint32_t hn[CPT / 2];
         load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn, hn);
         send(i + 1, hn);
       }
@@ -565,26 +582,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       if (i > 0 && __any_sync(0xffffffffu, need)) {
         wait_or_fail(ok, bar(B_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, 23);
         tc_fence_after();
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = 0; c < OPT; c += 16) {
           uint32_t v[16];
-          tmem_ld16(tmem + lane_base + TM_O + 128 * wg + c, v);
+          tmem_ld16(tmem + lane_base + TM_O + OPT * wg + c, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * factor);
-          tmem_st16(tmem + lane_base + TM_O + 128 * wg + c, v);
+          tmem_st16(tmem + lane_base + TM_O + OPT * wg + c, v);
         }
         tmem_wait_st();
       }
       l_part *= factor;
       m_run = m_new;
-      // P = 2^(s - m) in bf16 into P buffer i&1 (K-major, 128-byte swizzled rows),
-      // which P.V(i-2) has finished reading
-      if (i >= 2) wait_or_fail(ok, bar(B_ODONE + (i & 1)), ((i - 2) >> 1) & 1, 24);
+      // P = 2^(s - m) in bf16 into the P tile (K-major, 128-byte swizzled rows),
+      // which P.V(i-1) has finished reading
+      if (i >= 1) wait_or_fail(ok, bar(B_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, 24);
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       float rs[2] = {0.f, 0.f};
-      const uint32_t prow = sP + (i & 1) * P_TILE + q * 128;
+      const uint32_t prow = sP + q * 128;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < CPT / 8; ++k) {
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -617,14 +634,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + (i & 1)));
     };
-    float s2[32];
+    float s2[CPT];
     for (int i = 0; i < ntiles; i += 2) {
       softmax_tile(i, s, s2);
       if (i + 1 < ntiles) softmax_tile(i + 1, s2, s);
     }
     // after a failure, let an armed exchange phase finish (or time out) so no
     // copy from the peer is still landing when this CTA exits
-    if (sm_tid == 0 && received < armed) mbar_wait_cluster(bar(B_XFULL), received & 1);
+    if (sm_tid == 0)
+      for (int j = received; j < armed; ++j)
+        mbar_wait_cluster(bar(B_XFULL + (j & 1)), (j >> 1) & 1);
     if (lane == 0) bulk_wait_read();
     // ---------------------------------------------------------------- epilogue
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
@@ -635,15 +654,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // pair hold the same P, so their totals agree).
     lsum[wg * BM + q] = l_part;
     named_bar_sync(1, SOFTMAX_THREADS);
-    const float l_tot = lsum[q] + lsum[BM + q];
+    float l_tot = 0.f;
+#pragma unroll
+    for (int g = 0; g < NWG; ++g) l_tot += lsum[g * BM + q];
     const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
     // This CTA's half of O / l (128 rows x 256 columns, bf16) goes through the
     // drained KV stages as four 128-byte-swizzled boxes of 64 columns, then
     // out with TMA stores (rows past R are clipped).
-    for (int c = 0; c < 128; c += 16) {
+    for (int c = 0; c < OPT; c += 16) {
       uint32_t v[16];
       if (ntiles > 0) {
-        tmem_ld16(tmem + lane_base + TM_O + 128 * wg + c, v);
+        tmem_ld16(tmem + lane_base + TM_O + OPT * wg + c, v);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -651,7 +672,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int col = 128 * wg + c + 8 * u;
+        const int col = OPT * wg + c + 8 * u;
         const uint32_t addr = sKV + (col >> 6) * (BM * 128) + q * 128 +
                               ((((col & 63) >> 3) ^ (q & 7)) << 4);
         const uint32_t* w = v + 8 * u;
