@@ -100,6 +100,37 @@ def _work(kernel: str, L: int, T: int, H=128, r=512, n=128, v=128, rope=64):
     return table.get(kernel)
 
 
+def call_work(branch: str, geom, L: int, lens):
+    """Algorithmic (bytes, flops, cache_bytes) of one verify call, as the
+    method must do it (causal triangle and softmax ignored):
+      absorbed:     flops = sum_b 2 H L (n r + T_b (r + rope) + T_b r + r v)
+                    bytes = sum_b T_b (r + rope) 2 + H (n r + r v) 2 + B L H (n + rope + v) 2
+      materialised: flops = sum_b 2 H (T_b r d + L T_b (n + rope) + L T_b v)
+                    bytes = the absorbed bytes + 2 sum_b T_b H d 2 (the expanded
+                    keys and values written once and read once)."""
+    H, r, n, v, rope = geom.H, geom.r, geom.n, geom.v, geom.rope
+    d = n + v
+    B = len(lens)
+    cache = sum(T * (r + rope) * 2 for T in lens)
+    byts = cache + H * (n * r + r * v) * 2 + B * L * H * (n + rope + v) * 2
+    if branch == "absorbed":
+        flops = sum(2 * H * L * (n * r + T * (r + rope) + T * r + r * v) for T in lens)
+    else:
+        flops = sum(2 * H * (T * r * d + L * T * (n + rope) + L * T * v) for T in lens)
+        byts += 2 * sum(T * H * d * 2 for T in lens)
+    return byts, flops, cache
+
+
+def call_roofline(branch: str, geom, L: int, lens, us: float, peaks) -> dict:
+    """Fraction of the call roofline max(bytes / BW, flops / peak) reached in `us`."""
+    byts, flops, cache = call_work(branch, geom, L, lens)
+    t_b = byts / (peaks["hbm_gbs"] * 1e3)      # us
+    t_f = flops / (peaks["bf16_tflops"] * 1e6)  # us
+    t_c = cache / (peaks["hbm_gbs"] * 1e3)
+    return {"us": us, "roofline_us": max(t_b, t_f), "bound": "hbm" if t_b >= t_f else "tensor",
+            "frac": max(t_b, t_f) / us, "cache_only_frac": max(t_c, t_f) / us}
+
+
 def _mat_work(kernel: str, geom, L: int, lens):
     """(bytes, flops) of one materialised-branch launch: the expansion GEMM
     (sum(T) x H*(n+v) x r) and causal attention over the expanded cache (row l
@@ -189,7 +220,10 @@ def _bench_materialised(B, dev, peaks, reps):
                     ent.update(bound="hbm", achieved=ach, unit="GB/s", frac=ach / peaks["hbm_gbs"])
             kern[k] = ent
         res.append({"workload": name, "branch": B.BRANCH_NAMES[br["b"]],
-                    "us_per_call": us_call, "kernels": kern})
+                    "us_per_call": us_call,
+                    "call_roofline": call_roofline(B.BRANCH_NAMES[br["b"]], geom, L, lens,
+                                                   us_call, peaks),
+                    "kernels": kern})
         del d, ws, out, gr
         torch.cuda.empty_cache()
     return {"shapes": res, "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
@@ -212,7 +246,10 @@ KERNEL_SOURCES = {
     "generic_combine_unembed": ["generic_kernels.cu"],
     "fold_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "absorbed_attn_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
+    "merge_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "unembed_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
+    "expand_sm103": ["materialised_sm103.cu", "sm103_ptx.cuh"],
+    "mat_attn_sm103": ["materialised_sm103.cu", "sm103_ptx.cuh"],
 }
 
 
@@ -543,6 +580,9 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_call": ms_per_step * 1e3 / len(WIDTHS),
             "per_width_us_per_call": per_L,
+            "per_width_call_roofline": {
+                L: call_roofline(B.BRANCH_NAMES[branches[int(L)]], geom, int(L), [CACHE_LEN],
+                                 us, peaks) for L, us in per_L.items()},
             "roofline": roof,
             "kernel_ms_per_step": {k: v[1] / args.steps for k, v in ktimes.items()},
             "materialised": mat,
