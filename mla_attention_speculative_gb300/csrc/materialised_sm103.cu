@@ -16,10 +16,11 @@
 //  mat_attn_sm103  causal attention of the L verify rows of one head against
 //                  keys [K_nope || k_rope] (the RoPE key is shared by all heads)
 //                  and values V: S = Q K^T on the tensor cores, an online
-//                  softmax in registers (one thread per query row, the running
-//                  max moved only when it grows by more than 2^8), P written
-//                  back to tensor memory as the A operand of O += P V.  One CTA
-//                  per (128-row query tile, head, sequence).
+//                  softmax in registers (two threads per query row, each half
+//                  of the tile's positions; the running max moved only when it
+//                  grows by more than 2^8), P written back to tensor memory as
+//                  the A operand of O += P V.  One CTA per (128-row query tile,
+//                  head, sequence).
 //
 // Every wait is bounded; a wait that runs out sets the status word and the
 // kernel finishes without waiting further (results are then undefined and
@@ -47,6 +48,7 @@ constexpr int kSmemPerBlock = 232448;   // opt-in maximum per CTA
 constexpr int kSmemPerSM = 233472;
 constexpr int kSmemReserved = 1024;     // per CTA, taken by the runtime
 constexpr int kSmemExtra = 1024 + 256;  // 1024-byte realignment + barriers
+constexpr int kMatRowBytes = 2 * 128 * 4;  // per (warpgroup, row) floats of mat_attn
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
@@ -243,22 +245,29 @@ struct MatAttnParams {
   int page_size, max_pages;
   long long seq_stride;
   __nv_bfloat16* out;  // [B, L, H, v]
-  int L, H, n, v, stages;
+  int L, H, n, v;
+  int ks, vs;          // K ring and V ring depths
   float sl2;           // softmax scale x log2(e)
 };
 
 constexpr int MA_BM = 128;
 constexpr int MA_BN = 64;
+constexpr int MA_NWG = 2;                       // softmax warpgroups; each takes half a row
+constexpr int MA_CPT = MA_BN / MA_NWG;          // score columns per softmax thread
+constexpr int MA_SOFTMAX = 128 * MA_NWG;
+constexpr int MA_THREADS = 96 + MA_SOFTMAX;      // key producer, MMA, value producer, softmax
 constexpr uint32_t MA_TM_S = 256;  // S / P buffers at 256 + 64*sb; O at [0, v)
 
 __host__ __device__ constexpr int mat_q_bytes(int n) { return (n / 64 + 1) * MA_BM * 128; }
-__host__ __device__ constexpr int mat_stage_bytes(int n, int v) {
-  return (n / 64 + 1 + v / 64) * MA_BN * 128;
-}
+// A key tile [K_nope || k_rope] (64 positions) and a value tile, in 64-column chunks.
+__host__ __device__ constexpr int mat_k_bytes(int n) { return (n / 64 + 1) * MA_BN * 128; }
+__host__ __device__ constexpr int mat_v_bytes(int v) { return (v / 64) * MA_BN * 128; }
 
-enum { M_QFULL = 0, M_SFULL = 1, M_PFULL = 3, M_ODONE = 5, M_DRAIN = 7, M_KV = 8 };
+// barriers: Q, S full x2, P full x2, O done x2, drain, then the K ring (full,
+// empty) and the V ring (full, empty)
+enum { M_QFULL = 0, M_SFULL = 1, M_PFULL = 3, M_ODONE = 5, M_DRAIN = 7, M_RINGS = 8 };
 
-__global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__ CUtensorMap tm_qn,
+__global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_constant__ CUtensorMap tm_qn,
                                                          const __grid_constant__ CUtensorMap tm_qr,
                                                          const __grid_constant__ CUtensorMap tm_kx,
                                                          const __grid_constant__ CUtensorMap tm_kr,
@@ -267,32 +276,42 @@ __global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__
   uint8_t* smem = align1024(smem_raw);
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int T = p.lens[b];
-  const int n = p.n, v = p.v, S = p.stages, L = p.L;
+  const int n = p.n, v = p.v, L = p.L;
   const int l0 = qt * MA_BM;
   const int l_last = min(L - 1, l0 + MA_BM - 1);
   const int kv_end = T - L + l_last + 1;  // no row of the tile sees t >= kv_end
   const int ntiles = (kv_end + MA_BN - 1) / MA_BN;
   const int nq = n / 64 + 1;  // Q / K chunks of 64 columns: n/64 nope + 1 RoPE
-  const int QB = mat_q_bytes(n), SB = mat_stage_bytes(n, v);
-  const uint32_t sQ = smem_u32(smem), sKV = sQ + QB;
-  uint64_t* bars = (uint64_t*)(smem + QB + S * SB);
-  uint32_t* slot = (uint32_t*)(bars + M_KV + 2 * S);
+  const int KS = p.ks, VS = p.vs;
+  const int QB = mat_q_bytes(n), KB = mat_k_bytes(n), VB = mat_v_bytes(v);
+  const uint32_t sQ = smem_u32(smem), sK = sQ + QB, sV = sK + KS * KB;
+  uint8_t* tail = smem + QB + KS * KB + VS * VB;
+  uint64_t* bars = (uint64_t*)tail;
+  uint32_t* slot = (uint32_t*)(bars + M_RINGS + 2 * KS + 2 * VS);
+  // per (warpgroup, row): the tile maxima, and at the end the row sums
+  float* xrow = (float*)(tail + 256);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  auto kv_full = [&](int s) { return bar(M_KV + s); };
-  auto kv_empty = [&](int s) { return bar(M_KV + S + s); };
+  auto k_full = [&](int s) { return bar(M_RINGS + s); };
+  auto k_empty = [&](int s) { return bar(M_RINGS + KS + s); };
+  auto v_full = [&](int s) { return bar(M_RINGS + 2 * KS + s); };
+  auto v_empty = [&](int s) { return bar(M_RINGS + 2 * KS + VS + s); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(M_QFULL), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(M_SFULL + i), 1);
-      mbar_init(bar(M_PFULL + i), 128);
+      mbar_init(bar(M_PFULL + i), MA_SOFTMAX);
       mbar_init(bar(M_ODONE + i), 1);
     }
     mbar_init(bar(M_DRAIN), 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
     }
     fence_mbar_init();
   }
@@ -304,7 +323,10 @@ __global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__
   const int plane = b * p.H + h;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producers
+    // Warp 0 loads Q and the key ring, warp 2 the value ring (each in its own
+    // warp, so neither waits behind the other): a key tile is free once S has
+    // read it, a value tile once P.V has.
     if (lane == 0) {
       bool ok = true;
       pdl_wait();  // the expanded cache comes from the expansion kernel
@@ -315,23 +337,38 @@ __global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__
       tma_load_2d(sQ + (n / 64) * MA_BM * 128, &tm_qr, bar(M_QFULL), h * 64, qrow);
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
-        const int s = i % S;
-        if (i >= S) wait_or_fail(ok, kv_empty(s), ((i / S) - 1) & 1, 50);
+        const int s = i % KS;
+        if (i >= KS) wait_or_fail(ok, k_empty(s), ((i / KS) - 1) & 1, 50);
         if (!ok) break;
         const int t0 = i * MA_BN;
         const int y = cache_y(p.page_table, p.page_size, p.max_pages, p.seq_stride, b, t0);
-        const uint32_t st = sKV + s * SB;
-        mbar_arrive_expect_tx(kv_full(s), SB);
+        const uint32_t st = sK + s * KB;
+        mbar_arrive_expect_tx(k_full(s), KB);
         for (int c = 0; c < n / 64; ++c)
-          tma_load_3d(st + c * 8192, &tm_kx, kv_full(s), 64 * c, t0, plane);
-        tma_load_2d(st + (n / 64) * 8192, &tm_kr, kv_full(s), 0, y);
-        for (int j = 0; j < v / 64; ++j)
-          tma_load_3d(st + (nq + j) * 8192, &tm_kx, kv_full(s), n + 64 * j, t0, plane);
+          tma_load_3d(st + c * 8192, &tm_kx, k_full(s), 64 * c, t0, plane);
+        tma_load_2d(st + (n / 64) * 8192, &tm_kr, k_full(s), 0, y);
         issued = i + 1;
       }
       // drain: nothing may still be landing when the CTA exits
       mbar_wait(bar(M_QFULL), 0);
-      for (int i = max(issued - S, 0); i < issued; ++i) mbar_wait(kv_full(i % S), (i / S) & 1);
+      for (int i = max(issued - KS, 0); i < issued; ++i) mbar_wait(k_full(i % KS), (i / KS) & 1);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      bool ok = true;
+      pdl_wait();
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % VS;
+        if (i >= VS) wait_or_fail(ok, v_empty(s), ((i / VS) - 1) & 1, 57);
+        if (!ok) break;
+        const uint32_t st = sV + s * VB;
+        mbar_arrive_expect_tx(v_full(s), VB);
+        for (int j = 0; j < v / 64; ++j)
+          tma_load_3d(st + j * 8192, &tm_kx, v_full(s), n + 64 * j, i * MA_BN, plane);
+        issued = i + 1;
+      }
+      for (int i = max(issued - VS, 0); i < issued; ++i) mbar_wait(v_full(i % VS), (i / VS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
@@ -340,46 +377,55 @@ __global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__
     if (lane == 0) {
       bool ok = true;
       const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
-      const uint64_t dk = sdesc_sw128(sKV, 16, 1024);
-      const uint64_t dv = sdesc_sw128(sKV + nq * 8192, 8192, 1024);
+      const uint64_t dk = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dv = sdesc_sw128(sV, 8192, 1024);
       const uint32_t id_s = idesc_bf16(MA_BM, MA_BN, 0, 0);
       const uint32_t id_o = idesc_bf16(MA_BM, v, 0, 1);
       wait_or_fail(ok, bar(M_QFULL), 0, 51);
       auto issue_s = [&](int i) {
-        const int s = i % S, sb = i & 1;
-        wait_or_fail(ok, kv_full(s), (i / S) & 1, 52);
+        const int s = i % KS, sb = i & 1;
+        wait_or_fail(ok, k_full(s), (i / KS) & 1, 52);
         if (!ok) return;
         tc_fence_after();
-        const uint64_t soff = (uint64_t)(s * (SB >> 4));
+        const uint64_t soff = (uint64_t)(s * (KB >> 4));
         for (int c = 0; c < nq; ++c)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_bf16(tmem + MA_TM_S + sb * MA_BN, dq + ((c * MA_BM * 128 + ks * 32) >> 4),
                      dk + soff + ((c * 8192 + ks * 32) >> 4), id_s, (c | ks) != 0);
         mma_commit(bar(M_SFULL + sb));
+        mma_commit(k_empty(s));
       };
       issue_s(0);
       for (int j = 0; j < ntiles && ok; ++j) {
         if (j + 1 < ntiles) issue_s(j + 1);
         if (!ok) break;
-        const int sj = j % S, pb = j & 1;
+        const int vj = j % VS, pb = j & 1;
         wait_or_fail(ok, bar(M_PFULL + pb), (j >> 1) & 1, 53);
+        wait_or_fail(ok, v_full(vj), (j / VS) & 1, 58);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t soff = (uint64_t)(sj * (SB >> 4));
+        const uint64_t voff = (uint64_t)(vj * (VB >> 4));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16_tmem_a(tmem, tmem + MA_TM_S + pb * MA_BN + ks * 8, dv + soff + ks * 128, id_o,
+          mma_bf16_tmem_a(tmem, tmem + MA_TM_S + pb * MA_BN + ks * 8, dv + voff + ks * 128, id_o,
                           (j > 0 || ks > 0));
         mma_commit(bar(M_ODONE + pb));
-        mma_commit(kv_empty(sj));
+        mma_commit(v_empty(vj));
       }
       mma_commit(bar(M_DRAIN));
       mbar_wait(bar(M_DRAIN), 0);
     }
   } else {
-    // ------------------------------------------------- softmax warpgroup
+    // ------------------------------------------------- softmax warpgroups
+    // Thread (wg, q) owns row q, score columns MA_CPT*wg.. of each tile and O
+    // columns (v/MA_NWG)*wg..; the warpgroups combine their row maxima (and at
+    // the end their row sums) through shared memory.
+    const int wg = (warp - 3) >> 2;
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
+    const int c0 = MA_CPT * wg;
+    const int opt = v / MA_NWG;            // O columns per thread
+    const int sm_tid = threadIdx.x - 96;
     const int l = min(l0 + q, L - 1);
     const int last_t = T - L + l;          // the last position row l may see
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -390,25 +436,31 @@ __global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__
       const int t0 = i * MA_BN;
       wait_or_fail(ok, bar(M_SFULL + sb), (i >> 1) & 1, 54);
       tc_fence_after();
-      uint32_t u[MA_BN];
+      uint32_t u[MA_CPT];
 #pragma unroll
-      for (int k = 0; k < MA_BN / 16; ++k)
-        tmem_ld16(tmem + lane_base + MA_TM_S + sb * MA_BN + 16 * k,
+      for (int k = 0; k < MA_CPT / 16; ++k)
+        tmem_ld16(tmem + lane_base + MA_TM_S + sb * MA_BN + c0 + 16 * k,
                   *(uint32_t(*)[16])(u + 16 * k));
       tmem_wait_ld();
       // Masked columns: past the row's causal limit (this also covers
       // positions at or past T, whose keys may hold anything).
-      float s[MA_BN];
+      float s[MA_CPT];
       const bool edge = t0 + MA_BN - 1 > T - L;
 #pragma unroll
-      for (int j = 0; j < MA_BN; ++j) {
+      for (int j = 0; j < MA_CPT; ++j) {
         const float x = __uint_as_float(u[j]) * p.sl2;
-        s[j] = (!edge || t0 + j <= last_t) ? x : -INFINITY;
+        s[j] = (!edge || t0 + c0 + j <= last_t) ? x : -INFINITY;
       }
       float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int j = 4; j < MA_BN; ++j) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
-      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      for (int j = 4; j < MA_CPT; ++j) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      xrow[wg * MA_BM + q] = mt;
+      named_bar_sync(1, MA_SOFTMAX);
+#pragma unroll
+      for (int g = 0; g < MA_NWG; ++g) mt = fmaxf(mt, xrow[g * MA_BM + q]);
+      // every warpgroup has read this tile's maxima before any writes the next
+      named_bar_sync(2, MA_SOFTMAX);
       const bool need = mt > m_run + 8.f;
       const float m_new = need ? mt : m_run;
       const float factor = need ? ex2(m_run - m_new) : 1.f;
@@ -416,22 +468,22 @@ __global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__
         // O must hold P(i-1) V(i-1) before it is rescaled
         wait_or_fail(ok, bar(M_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, 55);
         tc_fence_after();
-        for (int c = 0; c < v; c += 16) {
+        for (int c = 0; c < opt; c += 16) {
           uint32_t w[16];
-          tmem_ld16(tmem + lane_base + c, w);
+          tmem_ld16(tmem + lane_base + opt * wg + c, w);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * factor);
-          tmem_st16(tmem + lane_base + c, w);
+          tmem_st16(tmem + lane_base + opt * wg + c, w);
         }
       }
       l_run *= factor;
       m_run = m_new;
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[MA_BN / 2];
+      uint32_t pk[MA_CPT / 2];
 #pragma unroll
-      for (int e = 0; e < MA_BN / 2; ++e) {
+      for (int e = 0; e < MA_CPT / 2; ++e) {
         const float a = ex2(s[2 * e] - m_use);
         const float d = ex2(s[2 * e + 1] - m_use);
         rs0 += a;
@@ -439,14 +491,20 @@ __global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__
         pk[e] = pack_bf16(a, d);
       }
       l_run += rs0 + rs1;
-      tmem_st32(tmem + lane_base + MA_TM_S + sb * MA_BN, pk);
+      // P(i) as bf16 pairs over S buffer sb: this thread's positions are the
+      // pair columns c0/2 ..
+#pragma unroll
+      for (int k = 0; k < MA_CPT / 32; ++k)
+        tmem_st16(tmem + lane_base + MA_TM_S + sb * MA_BN + c0 / 2 + 16 * k,
+                  *(const uint32_t(*)[16])(pk + 16 * k));
       // Value rows at or past T in the last tile may hold anything (0 x NaN
       // would poison O): zero them in shared memory before P V reads them.
       if (ok && t0 + MA_BN > T) {
         const int z0 = max(T - t0, 0);
-        const uint32_t st = sKV + (i % S) * SB + nq * 8192;
+        wait_or_fail(ok, v_full(i % VS), (i / VS) & 1, 59);  // the value tile has landed
+        const uint32_t st = sV + (i % VS) * VB;
         const int units = (MA_BN - z0) * 8;  // 16-byte units per 64-column chunk
-        for (int w = q; w < (v / 64) * units; w += 128) {
+        for (int w = sm_tid; w < (v / 64) * units; w += MA_SOFTMAX) {
           const int c = w / units, r = w - c * units;
           const uint32_t addr = st + c * 8192 + (z0 + r / 8) * 128 + (r & 7) * 16;
           asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
@@ -462,13 +520,19 @@ __global__ void __launch_bounds__(192, 1) mat_attn_sm103(const __grid_constant__
     wait_or_fail(ok, bar(M_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 56);
     tc_fence_after();
     pdl_launch_dependents();
+    xrow[wg * MA_BM + q] = l_run;
+    named_bar_sync(1, MA_SOFTMAX);
+    float l_tot = 0.f;
+#pragma unroll
+    for (int g = 0; g < MA_NWG; ++g) l_tot += xrow[g * MA_BM + q];
     const bool live = l0 + q < L;
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    __nv_bfloat16* dst = p.out + (((size_t)b * L + (live ? l0 + q : 0)) * p.H + h) * (size_t)v;
-    for (int c = 0; c < v; c += 32) {
+    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+    __nv_bfloat16* dst =
+        p.out + (((size_t)b * L + (live ? l0 + q : 0)) * p.H + h) * (size_t)v + opt * wg;
+    for (int c = 0; c < opt; c += 32) {
       uint32_t r[32];
-      tmem_ld16(tmem + lane_base + c, *(uint32_t(*)[16])(r));
-      tmem_ld16(tmem + lane_base + c + 16, *(uint32_t(*)[16])(r + 16));
+      tmem_ld16(tmem + lane_base + opt * wg + c, *(uint32_t(*)[16])(r));
+      tmem_ld16(tmem + lane_base + opt * wg + c + 16, *(uint32_t(*)[16])(r + 16));
       tmem_wait_ld();
       if (live) {
 #pragma unroll
@@ -526,9 +590,21 @@ ExpandShape expand_shape(int n, int v) {
   e.smem = e.stages * sb + kSmemExtra;
   return e;
 }
-int mat_stages(int n, int v) {
-  const int s = (kSmemPerBlock - kSmemExtra - mat_q_bytes(n)) / mat_stage_bytes(n, v);
-  return s > 4 ? 4 : s;
+// Key and value ring depths that fit next to Q, or {0, 0} if not even two of
+// each fit.  Values come first: a key tile is freed as soon as S has read it,
+// a value tile only after P.V, so the value ring is the one that runs dry.
+struct MatRings {
+  int ks, vs, smem;
+};
+MatRings mat_rings(int n, int v) {
+  const int budget = kSmemPerBlock - kSmemExtra - kMatRowBytes - mat_q_bytes(n);
+  const int cand[][2] = {{4, 4}, {3, 4}, {4, 3}, {3, 3}, {2, 4}, {2, 3}, {3, 2}, {2, 2}};
+  for (const auto& c : cand) {
+    const int bytes = c[0] * mat_k_bytes(n) + c[1] * mat_v_bytes(v);
+    if (bytes <= budget)
+      return {c[0], c[1], mat_q_bytes(n) + bytes + kSmemExtra + kMatRowBytes};
+  }
+  return {0, 0, 0};
 }
 
 }  // namespace
@@ -540,7 +616,7 @@ bool fast_materialised_supported(const Plan& p) {
   const ExpandShape e = expand_shape(p.n, p.v);
   // the output tile (128 x (n+v) bf16) is staged in the drained ring
   return e.stages >= 2 && e.stages * expand_stage_bytes(p.n, p.v) >= EX_BM * (p.n + p.v) * 2 &&
-         mat_stages(p.n, p.v) >= 2;
+         mat_rings(p.n, p.v).ks >= 2;
 }
 
 size_t fast_materialised_workspace(const Plan& p) {
@@ -571,8 +647,8 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
   if (!ok) return cudaErrorInvalidValue;
 
   const ExpandShape es = expand_shape(p.n, p.v);
-  const int ms = mat_stages(p.n, p.v);
-  const int ma_smem = mat_q_bytes(p.n) + ms * mat_stage_bytes(p.n, p.v) + kSmemExtra;
+  const MatRings mr = mat_rings(p.n, p.v);
+  const int ma_smem = mr.smem;
   static bool attrs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -597,10 +673,11 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
   }
   {
     MatAttnParams mp{a.lens, c.page_table, c.page_size, c.max_pages, c.seq_stride,
-                     (__nv_bfloat16*)a.out, p.L, p.H, p.n, p.v, ms,
+                     (__nv_bfloat16*)a.out, p.L, p.H, p.n, p.v, mr.ks, mr.vs,
                      p.scale * 1.4426950408889634f};
     KernelTimer kt("mat_attn_sm103", a.stream);
-    e = launch_pdl(mat_attn_sm103, dim3((p.L + MA_BM - 1) / MA_BM, p.H, p.B), dim3(192), ma_smem,
+    e = launch_pdl(mat_attn_sm103, dim3((p.L + MA_BM - 1) / MA_BM, p.H, p.B), dim3(MA_THREADS),
+                   ma_smem,
                    a.stream, tm_qn, tm_qr, tm_kx, tm_kr, mp);
     if (e != cudaSuccess) return e;
   }
