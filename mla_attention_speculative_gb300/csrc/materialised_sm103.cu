@@ -9,8 +9,9 @@
 //                  V[b,h,t,:]      = c_kv[b,t] . W_UV[h]     (512 -> v)
 //                  into one [B*H, Tmax, n+v] bf16 buffer (each head's keys and
 //                  values contiguous).  One CTA per (128 cached positions,
-//                  head): each 64-wide latent chunk of the cache tile feeds
-//                  both GEMMs (two TMEM accumulators); the chunks stream
+//                  head) computes both products (n+v <= 256: two TMEM
+//                  accumulators fed by each 64-wide latent chunk) or one of
+//                  them (wider heads), two CTAs per SM; the chunks stream
 //                  through a TMA ring; the bf16 tile leaves through shared
 //                  memory with TMA stores clipped at Tmax.
 //  mat_attn_sm103  causal attention of the L verify rows of one head against
@@ -83,6 +84,7 @@ struct ExpandParams {
   long long seq_stride;
   int H, n, v, stages;
   uint32_t tmem_cols, v_col;  // TMEM allocation; V accumulator's first column
+  int split;                  // 1: K_nope and V in separate CTAs (blockIdx.x & 1)
 };
 
 constexpr int EX_BM = 128;
@@ -98,13 +100,19 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
                                                        ExpandParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  const int mt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int mt = p.split ? blockIdx.x >> 1 : blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // which products this CTA computes: both, or (split) K_nope or V alone
+  const bool has_k = !p.split || (blockIdx.x & 1) == 0;
+  const bool has_v = !p.split || (blockIdx.x & 1) == 1;
   pdl_wait();  // the cache and its lengths may come from the preceding kernel
   const int T = p.lens[b];
   const int t0 = mt * EX_BM;
   if (t0 >= T) return;
   const int n = p.n, v = p.v, S = p.stages;
-  const int SB = expand_stage_bytes(n, v);
+  const int nk = has_k ? n : 0, nv = has_v ? v : 0;   // B columns of each product
+  const uint32_t vcol = has_k ? p.v_col : 0u;         // V accumulator's TMEM column
+  const int out0 = has_k ? 0 : n;                     // first output column
+  const int SB = EX_BM * 128 + (nk + nv) * 128;
   uint64_t* bars = (uint64_t*)(smem + S * SB);  // [0,S) full, [S,2S) empty, 2S done
   uint32_t* slot = (uint32_t*)(bars + 2 * S + 1);
   volatile int* fail = (volatile int*)(slot + 1);
@@ -150,10 +158,10 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
       tma_load_2d(st, &tm_ckv, full(s), 64 * kc, y0);
       tma_load_2d(st + 8192, &tm_ckv, full(s), 64 * kc, y1);
       const uint32_t bn = st + EX_BM * 128;
-      for (int r = 0; r < n / 64; ++r)
+      for (int r = 0; r < nk / 64; ++r)
         tma_load_2d(bn + r * 8192, &tm_wuk, full(s), 64 * kc, h * n + 64 * r);
-      const uint32_t bv = bn + n * 128;
-      for (int j = 0; j < v / 64; ++j)
+      const uint32_t bv = bn + nk * 128;
+      for (int j = 0; j < nv / 64; ++j)
         tma_load_2d(bv + j * 8192, &tm_wuv, full(s), 64 * j, h * kLat + 64 * kc);
       issued = kc + 1;
     }
@@ -172,11 +180,11 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
       const uint32_t st = sbase + s * SB;
       const uint64_t da = sdesc_sw128(st, 16, 1024);
       const uint64_t dn = sdesc_sw128(st + EX_BM * 128, 16, 1024);
-      const uint64_t dv = sdesc_sw128(st + EX_BM * 128 + n * 128, 8192, 1024);
+      const uint64_t dv = sdesc_sw128(st + EX_BM * 128 + nk * 128, 8192, 1024);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tmem, da + 2 * ks, dn + 2 * ks, id_n, (kc | ks) != 0);
-        mma_bf16(tmem + p.v_col, da + 2 * ks, dv + 128 * ks, id_v, (kc | ks) != 0);
+        if (has_k) mma_bf16(tmem, da + 2 * ks, dn + 2 * ks, id_n, (kc | ks) != 0);
+        if (has_v) mma_bf16(tmem + vcol, da + 2 * ks, dv + 128 * ks, id_v, (kc | ks) != 0);
       }
       mma_commit(empty(s));
     }
@@ -193,7 +201,8 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
   const bool ok = !*fail;
   if (ok) {
     // TMEM -> bf16 -> shared memory in the 128-byte-swizzled layout of the
-    // store boxes (64 columns x 128 rows, 16 KB each), then TMA stores.
+    // store boxes (64 columns x 128 rows, 16 KB each, box 0 = output column
+    // out0), then TMA stores.
     const int q = warp * 32 + lane;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     auto emit = [&](uint32_t col0, int width, int out_col0) {
@@ -204,7 +213,7 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
-          const int col = out_col0 + c + e;
+          const int col = out_col0 - out0 + c + e;
           const uint32_t addr = sbase + (col >> 6) * (EX_BM * 128) + q * 128 +
                                 ((((col & 63) >> 3) ^ (q & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
@@ -216,15 +225,15 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
         }
       }
     };
-    emit(0, n, 0);
-    emit(p.v_col, v, n);
+    if (has_k) emit(0, n, 0);
+    if (has_v) emit(vcol, v, n);
     fence_async_shared();
   }
   __syncthreads();
   if (ok && threadIdx.x == 0) {
     const int plane = b * p.H + h;
-    for (int c = 0; c < (n + v) / 64; ++c)
-      tma_store_3d(&tm_out, sbase + c * (EX_BM * 128), 64 * c, t0, plane);
+    for (int c = 0; c < (nk + nv) / 64; ++c)
+      tma_store_3d(&tm_out, sbase + c * (EX_BM * 128), out0 + 64 * c, t0, plane);
     bulk_commit();
     bulk_wait_all();
   }
@@ -571,20 +580,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Expansion layout: accumulators need n + v TMEM columns.  When they fit in
-// 256, two CTAs share an SM (one's epilogue overlaps the other's GEMM), so the
-// ring gets half the shared memory.
+// Expansion layout.  When n + v <= 256 one CTA computes both products (two
+// accumulators in 256 TMEM columns) and two CTAs share an SM.  Otherwise
+// K_nope and V get separate CTAs (each <= 256 columns, the latent tile read
+// once per product), again two per SM, so one CTA's epilogue overlaps the
+// other's GEMM.  The ring gets half the SM's shared memory either way.
 struct ExpandShape {
   uint32_t tmem_cols, v_col;
-  int stages, smem;
+  int stages, smem, split;
 };
 ExpandShape expand_shape(int n, int v) {
   ExpandShape e;
-  const bool pair = n + v <= 256;
-  e.tmem_cols = pair ? 256u : 512u;
-  e.v_col = pair ? (uint32_t)n : 256u;
-  const int budget = pair ? kSmemPerSM / 2 - kSmemReserved : kSmemPerBlock;
-  const int sb = expand_stage_bytes(n, v);
+  e.split = n + v > 256 ? 1 : 0;
+  e.tmem_cols = 256u;
+  e.v_col = e.split ? 0u : (uint32_t)n;
+  const int budget = kSmemPerSM / 2 - kSmemReserved;
+  const int sb = e.split ? EX_BM * 128 + (n > v ? n : v) * 128 : expand_stage_bytes(n, v);
   int s = (budget - kSmemExtra) / sb;
   e.stages = s > 4 ? 4 : s;
   e.smem = e.stages * sb + kSmemExtra;
@@ -614,9 +625,9 @@ bool fast_materialised_supported(const Plan& p) {
         p.n <= 256 && p.v % 64 == 0 && p.v >= 64 && p.v <= 256))
     return false;
   const ExpandShape e = expand_shape(p.n, p.v);
-  // the output tile (128 x (n+v) bf16) is staged in the drained ring
-  return e.stages >= 2 && e.stages * expand_stage_bytes(p.n, p.v) >= EX_BM * (p.n + p.v) * 2 &&
-         mat_rings(p.n, p.v).ks >= 2;
+  // the output tile (128 rows x the CTA's columns, bf16) is staged in the drained ring
+  const int cols = e.split ? (p.n > p.v ? p.n : p.v) : p.n + p.v;
+  return e.stages >= 2 && e.smem - kSmemExtra >= EX_BM * cols * 2 && mat_rings(p.n, p.v).ks >= 2;
 }
 
 size_t fast_materialised_workspace(const Plan& p) {
@@ -665,9 +676,10 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
   {
     ExpandParams ep{a.lens, c.page_table, c.page_size, c.max_pages, c.seq_stride,
                     p.H,    p.n,          p.v,         es.stages,   es.tmem_cols,
-                    es.v_col};
+                    es.v_col, es.split};
     KernelTimer kt("expand_sm103", a.stream);
-    e = launch_pdl(expand_sm103, dim3((p.Tmax + EX_BM - 1) / EX_BM, p.H, p.B), dim3(128), es.smem,
+    const int mtiles = (p.Tmax + EX_BM - 1) / EX_BM;
+    e = launch_pdl(expand_sm103, dim3(mtiles * (es.split ? 2 : 1), p.H, p.B), dim3(128), es.smem,
                    a.stream, tm_ckv, tm_wuk, tm_wuv, tm_store, ep);
     if (e != cudaSuccess) return e;
   }
