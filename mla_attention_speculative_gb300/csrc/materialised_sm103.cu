@@ -276,6 +276,10 @@ __host__ __device__ constexpr int mat_v_bytes(int v) { return (v / 64) * MA_BN *
 // empty) and the V ring (full, empty)
 enum { M_QFULL = 0, M_SFULL = 1, M_PFULL = 3, M_ODONE = 5, M_DRAIN = 7, M_RINGS = 8 };
 
+// NQ = n/64 + 1 (the 64-column chunks of [q_nope || q_rope]) is a template
+// parameter so the score MMAs unroll with constant descriptor offsets: tcgen05
+// MMA issue is nearly synchronous, so arithmetic between MMAs idles the pipe.
+template <int NQ>
 __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_constant__ CUtensorMap tm_qn,
                                                          const __grid_constant__ CUtensorMap tm_qr,
                                                          const __grid_constant__ CUtensorMap tm_kx,
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
   const int l_last = min(L - 1, l0 + MA_BM - 1);
   const int kv_end = T - L + l_last + 1;  // no row of the tile sees t >= kv_end
   const int ntiles = (kv_end + MA_BN - 1) / MA_BN;
-  const int nq = n / 64 + 1;  // Q / K chunks of 64 columns: n/64 nope + 1 RoPE
+  constexpr int nq = NQ;  // Q / K chunks of 64 columns: n/64 nope + 1 RoPE
   const int KS = p.ks, VS = p.vs;
   const int QB = mat_q_bytes(n), KB = mat_k_bytes(n), VB = mat_v_bytes(v);
   const uint32_t sQ = smem_u32(smem), sK = sQ + QB, sV = sK + KS * KB;
@@ -396,12 +400,14 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
         wait_or_fail(ok, k_full(s), (i / KS) & 1, 52);
         if (!ok) return;
         tc_fence_after();
-        const uint64_t soff = (uint64_t)(s * (KB >> 4));
-        for (int c = 0; c < nq; ++c)
+        const uint64_t dks = dk + (uint64_t)(s * (KB >> 4));
+        const uint32_t dst = tmem + MA_TM_S + sb * MA_BN;
+#pragma unroll
+        for (int c = 0; c < NQ; ++c)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + MA_TM_S + sb * MA_BN, dq + ((c * MA_BM * 128 + ks * 32) >> 4),
-                     dk + soff + ((c * 8192 + ks * 32) >> 4), id_s, (c | ks) != 0);
+            mma_bf16(dst, dq + ((c * MA_BM * 128 + ks * 32) >> 4),
+                     dks + ((c * 8192 + ks * 32) >> 4), id_s, (c | ks) != 0);
         mma_commit(bar(M_SFULL + sb));
         mma_commit(k_empty(s));
       };
@@ -666,8 +672,10 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
   if (dev >= 0 && dev < 64 && !attrs[dev]) {
     cudaError_t e = cudaFuncSetAttribute(expand_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemPerBlock);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mat_attn_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const void* attn[] = {(const void*)mat_attn_sm103<2>, (const void*)mat_attn_sm103<3>,
+                          (const void*)mat_attn_sm103<4>, (const void*)mat_attn_sm103<5>};
+    for (int k = 0; k < 4 && e == cudaSuccess; ++k)
+      e = cudaFuncSetAttribute(attn[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemPerBlock);
     if (e != cudaSuccess) return e;
     attrs[dev] = true;
@@ -688,9 +696,17 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
                      (__nv_bfloat16*)a.out, p.L, p.H, p.n, p.v, mr.ks, mr.vs,
                      p.scale * 1.4426950408889634f};
     KernelTimer kt("mat_attn_sm103", a.stream);
-    e = launch_pdl(mat_attn_sm103, dim3((p.L + MA_BM - 1) / MA_BM, p.H, p.B), dim3(MA_THREADS),
-                   ma_smem,
-                   a.stream, tm_qn, tm_qr, tm_kx, tm_kr, mp);
+    const dim3 grid((p.L + MA_BM - 1) / MA_BM, p.H, p.B);
+    auto go = [&](auto kernel) {
+      return launch_pdl(kernel, grid, dim3(MA_THREADS), ma_smem, a.stream, tm_qn, tm_qr, tm_kx,
+                        tm_kr, mp);
+    };
+    switch (p.n / 64 + 1) {  // n is a multiple of 64 in [64, 256]
+      case 2: e = go(mat_attn_sm103<2>); break;
+      case 3: e = go(mat_attn_sm103<3>); break;
+      case 4: e = go(mat_attn_sm103<4>); break;
+      default: e = go(mat_attn_sm103<5>); break;
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
