@@ -264,7 +264,8 @@ constexpr int MA_BN = 64;
 constexpr int MA_NWG = 2;                       // softmax warpgroups; each takes half a row
 constexpr int MA_CPT = MA_BN / MA_NWG;          // score columns per softmax thread
 constexpr int MA_SOFTMAX = 128 * MA_NWG;
-constexpr int MA_THREADS = 96 + MA_SOFTMAX;      // key producer, MMA, value producer, softmax
+// warps: key producer, score-MMA issuer, value producer, P.V issuer, softmax
+constexpr int MA_THREADS = 128 + MA_SOFTMAX;
 constexpr uint32_t MA_TM_S = 256;  // S / P buffers at 256 + 64*sb; O at [0, v)
 
 __host__ __device__ constexpr int mat_q_bytes(int n) { return (n / 64 + 1) * MA_BM * 128; }
@@ -272,9 +273,9 @@ __host__ __device__ constexpr int mat_q_bytes(int n) { return (n / 64 + 1) * MA_
 __host__ __device__ constexpr int mat_k_bytes(int n) { return (n / 64 + 1) * MA_BN * 128; }
 __host__ __device__ constexpr int mat_v_bytes(int v) { return (v / 64) * MA_BN * 128; }
 
-// barriers: Q, S full x2, P full x2, O done x2, drain, then the K ring (full,
-// empty) and the V ring (full, empty)
-enum { M_QFULL = 0, M_SFULL = 1, M_PFULL = 3, M_ODONE = 5, M_DRAIN = 7, M_RINGS = 8 };
+// barriers: Q, S full x2, P full x2, O done x2, drain x2 (one per MMA issuer),
+// then the K ring (full, empty) and the V ring (full, empty)
+enum { M_QFULL = 0, M_SFULL = 1, M_PFULL = 3, M_ODONE = 5, M_DRAIN = 7, M_RINGS = 9 };
 
 // NQ = n/64 + 1 (the 64-column chunks of [q_nope || q_rope]) is a template
 // parameter so the score MMAs unroll with constant descriptor offsets: tcgen05
@@ -318,6 +319,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
       mbar_init(bar(M_ODONE + i), 1);
     }
     mbar_init(bar(M_DRAIN), 1);
+    mbar_init(bar(M_DRAIN + 1), 1);
     for (int s = 0; s < KS; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
@@ -384,21 +386,21 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
       for (int i = max(issued - VS, 0); i < issued; ++i) mbar_wait(v_full(i % VS), (i / VS) & 1);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
-    // Order: S(0), then for each j: S(j+1), O += P(j) V(j).  P(j) sits in S
-    // buffer j&1, which S(j+2) overwrites only after P(j) V(j) in issue order.
+    // ------------------------------------------------------- score-MMA issuer
+    // S(i) goes to S buffer i&1, which holds P(i-2) until P(i-2) V(i-2) is done.
+    // MMA issue is nearly synchronous, so the scores and P.V come from two
+    // warps: a wait in one leaves the tensor pipe to the other.
     if (lane == 0) {
       bool ok = true;
       const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk = sdesc_sw128(sK, 16, 1024);
-      const uint64_t dv = sdesc_sw128(sV, 8192, 1024);
       const uint32_t id_s = idesc_bf16(MA_BM, MA_BN, 0, 0);
-      const uint32_t id_o = idesc_bf16(MA_BM, v, 0, 1);
       wait_or_fail(ok, bar(M_QFULL), 0, 51);
-      auto issue_s = [&](int i) {
+      for (int i = 0; i < ntiles && ok; ++i) {
         const int s = i % KS, sb = i & 1;
         wait_or_fail(ok, k_full(s), (i / KS) & 1, 52);
-        if (!ok) return;
+        if (i >= 2) wait_or_fail(ok, bar(M_ODONE + sb), ((i - 2) >> 1) & 1, 60);
+        if (!ok) break;
         tc_fence_after();
         const uint64_t dks = dk + (uint64_t)(s * (KB >> 4));
         const uint32_t dst = tmem + MA_TM_S + sb * MA_BN;
@@ -410,11 +412,17 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
                      dks + ((c * 8192 + ks * 32) >> 4), id_s, (c | ks) != 0);
         mma_commit(bar(M_SFULL + sb));
         mma_commit(k_empty(s));
-      };
-      issue_s(0);
+      }
+      mma_commit(bar(M_DRAIN));
+      mbar_wait(bar(M_DRAIN), 0);
+    }
+  } else if (warp == 3) {
+    // --------------------------------------------------------- P.V issuer
+    if (lane == 0) {
+      bool ok = true;
+      const uint64_t dv = sdesc_sw128(sV, 8192, 1024);
+      const uint32_t id_o = idesc_bf16(MA_BM, v, 0, 1);
       for (int j = 0; j < ntiles && ok; ++j) {
-        if (j + 1 < ntiles) issue_s(j + 1);
-        if (!ok) break;
         const int vj = j % VS, pb = j & 1;
         wait_or_fail(ok, bar(M_PFULL + pb), (j >> 1) & 1, 53);
         wait_or_fail(ok, v_full(vj), (j / VS) & 1, 58);
@@ -428,19 +436,19 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
         mma_commit(bar(M_ODONE + pb));
         mma_commit(v_empty(vj));
       }
-      mma_commit(bar(M_DRAIN));
-      mbar_wait(bar(M_DRAIN), 0);
+      mma_commit(bar(M_DRAIN + 1));
+      mbar_wait(bar(M_DRAIN + 1), 0);
     }
   } else {
     // ------------------------------------------------- softmax warpgroups
     // Thread (wg, q) owns row q, score columns MA_CPT*wg.. of each tile and O
     // columns (v/MA_NWG)*wg..; the warpgroups combine their row maxima (and at
     // the end their row sums) through shared memory.
-    const int wg = (warp - 3) >> 2;
+    const int wg = (warp - 4) >> 2;
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
     const int c0 = MA_CPT * wg;
     const int opt = v / MA_NWG;            // O columns per thread
-    const int sm_tid = threadIdx.x - 96;
+    const int sm_tid = threadIdx.x - 128;
     const int l = min(l0 + q, L - 1);
     const int last_t = T - L + l;          // the last position row l may see
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
