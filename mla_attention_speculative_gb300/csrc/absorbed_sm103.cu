@@ -197,7 +197,7 @@ constexpr int NWG = 2;                  // softmax warpgroups; each takes 1/NWG 
 constexpr int CPT = 64 / NWG;           // score columns per softmax thread
 constexpr int OPT = 256 / NWG;          // O (and latent Q) columns per softmax thread
 constexpr int SOFTMAX_THREADS = 128 * NWG;
-constexpr int ATTN_THREADS = 64 + SOFTMAX_THREADS;
+constexpr int ATTN_THREADS = 96 + SOFTMAX_THREADS;  // producer, S issuer, P.V issuer, softmax
 constexpr int Q_ROPE = BM * 64;         // the 32 RoPE columns of this CTA's Q rows (64-B swizzle)
 constexpr int KV_CHUNK = BN * 128;      // one 64-column bf16 chunk of a KV tile
 constexpr int KV_ROPE = BN * 64;        // 32 RoPE columns of a KV tile
@@ -219,7 +219,6 @@ constexpr uint32_t TM_O = 0;
 constexpr uint32_t TM_QL = 256;
 constexpr uint32_t TM_S = 384;
 constexpr int SBUF = 2;
-constexpr int S_AHEAD = 3;                          // scores run this many tiles ahead of P.V
 static_assert(OFF_KV % 1024 == 0 && KV_STAGE % 1024 == 0 && OFF_P % 1024 == 0,
               "swizzle atoms need 1 KiB alignment");
 static_assert(ATTN_SMEM <= 232448, "shared memory per CTA");
@@ -245,7 +244,7 @@ struct AttnParams {
 // copies that it cannot complete twice before its waiter looks.
 enum {
   B_QFULL = 0, B_QTMEM = 1, B_KVFULL = 2, B_KVEMPTY = 6, B_SFULL = 10, B_SFREE = 12,
-  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22, B_COUNT = 23
+  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22, B_COUNT = 24
 };
 
 // This thread's CPT partial scores of tile j (columns c0..c0+CPT-1 of this
@@ -320,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
-  uint32_t* slot = (uint32_t*)(bars + 24);
+  uint32_t* slot = (uint32_t*)(bars + B_COUNT + 4);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t sQR = smem_u32(smem + OFF_QR), sKV = smem_u32(smem + OFF_KV);
   const uint32_t sP = smem_u32(smem + OFF_P), sX = smem_u32(smem + OFF_X);
@@ -346,6 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_init(bar(B_XFREE + k), 1);
     }
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN + 1), 1);
     fence_mbar_init();
     // arm the exchange barrier for tile 0 (the peer's bulk copy counts it down)
     if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
@@ -399,27 +399,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         mbar_wait(bar(B_KVFULL + i % STAGES), (i / STAGES) & 1);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
-    // Order: S(0), S(1), S(2), then for each j: P.V(j), S(j+3).  Scores run
-    // three tiles ahead of P.V, so the softmax never waits on the tensor pipe
-    // for them; S(j+3) reuses the buffer of S(j+1), read during softmax(j).
+    // ------------------------------------------------------- score-MMA issuer
+    // S(i) = Q . K(i)^T over this CTA's 256 latent (Q from TMEM) + 32 RoPE
+    // columns, into S buffer i&1 once the softmax has read S(i-2) from it.
+    // The scores run ahead of the softmax on their own; P.V comes from another
+    // warp (MMA issue is nearly synchronous, so a wait in one issuer leaves
+    // the tensor pipe to the other).
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
       const uint64_t dqr = sdesc_sw64(sQR, 512);
       const uint64_t dk = sdesc_sw128(sKV, 16, 1024);
       const uint64_t dkr = sdesc_sw64(sKV + 4 * KV_CHUNK, 512);
-      const uint64_t dv = sdesc_sw128(sKV, KV_CHUNK, 1024);
-      const uint64_t dp = sdesc_sw128(sP, 16, 1024);
       const uint32_t id_s = idesc_bf16(BM, BN, 0, 0);
-      const uint32_t id_o = idesc_bf16(BM, 256, 0, 1);
       wait_or_fail(ok, bar(B_QFULL), 0, 11);
       wait_or_fail(ok, bar(B_QTMEM), 0, 15);
-      auto issue_s = [&](int i) {
-        // S(i) = Q . K(i)^T over this CTA's 256 latent (Q from TMEM) + 32 RoPE columns
+      for (int i = 0; i < ntiles && ok; ++i) {
         const int s = i % STAGES, sb = i & (SBUF - 1);
         wait_or_fail(ok, bar(B_KVFULL + s), (i / STAGES) & 1, 12);
         if (i >= SBUF) wait_or_fail(ok, bar(B_SFREE + sb), ((i - SBUF) / SBUF) & 1, 13);
-        if (!ok) return;
+        if (!ok) break;
         tc_fence_after();
         const uint64_t soff = (uint64_t)(s * (KV_STAGE >> 4));
         const uint32_t d = tmem + TM_S + sb * BN;
@@ -430,10 +428,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) mma_bf16(d, dqr + 2 * ks, dkr + soff + 2 * ks, id_s, 1);
         mma_commit(bar(B_SFULL + sb));
-      };
-      for (int i = 0; i < min(ntiles, S_AHEAD) && ok; ++i) issue_s(i);
+      }
+      // every MMA issued here has finished before tensor memory is released
+      mma_commit(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0);
+    }
+  } else if (warp == 2) {
+    // --------------------------------------------------------- P.V issuer
+    // O += P(j) . V(j) over this CTA's 256 latent columns of the KV tile; the
+    // stage is free afterwards (S(j) finished before the softmax made P(j)).
+    if (lane == 0 && ntiles > 0) {
+      bool ok = true;
+      const uint64_t dv = sdesc_sw128(sKV, KV_CHUNK, 1024);
+      const uint64_t dp = sdesc_sw128(sP, 16, 1024);
+      const uint32_t id_o = idesc_bf16(BM, 256, 0, 1);
       for (int j = 0; j < ntiles && ok; ++j) {
-        // O += P(j) . V(j) over this CTA's 256 latent columns of the KV tile
         const int sj = j % STAGES, pb = j & 1;
         wait_or_fail(ok, bar(B_PFULL + pb), (j >> 1) & 1, 14);
         if (!ok) break;
@@ -441,15 +450,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         const uint64_t soff = (uint64_t)(sj * (KV_STAGE >> 4));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + TM_O, dp + 2 * ks, dv + soff + ks * 128, id_o,
-                   (j > 0 || ks > 0));
+          mma_bf16(tmem + TM_O, dp + 2 * ks, dv + soff + ks * 128, id_o, (j > 0 || ks > 0));
         mma_commit(bar(B_ODONE + pb));
         mma_commit(bar(B_KVEMPTY + sj));
-        if (j + S_AHEAD < ntiles) issue_s(j + S_AHEAD);
       }
-      // every MMA issued here has finished before tensor memory is released
-      mma_commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0);
+      mma_commit(bar(B_DRAIN + 1));
+      mbar_wait(bar(B_DRAIN + 1), 0);
     }
   } else {
     // ------------------------------------------------- softmax warpgroups
@@ -458,10 +464,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // are finished (own + peer partial) while tile i+1's partial is already on
     // its way: each warp stages its 32 rows and ships them to the peer with one
     // bulk copy, so the exchange needs no block-wide barrier.
-    const int wg = (warp - 2) >> 2;
+    const int wg = (warp - 3) >> 2;
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
     const int c0 = CPT * wg;
-    const int sm_tid = threadIdx.x - 64;
+    const int sm_tid = threadIdx.x - 96;
     const int row = row0 + q;
     const int l = min(row, p.R - 1) / p.H;
     const int last_t = T - p.L + l;
