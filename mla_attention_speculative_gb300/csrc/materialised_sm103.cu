@@ -267,15 +267,24 @@ constexpr int MA_SOFTMAX = 128 * MA_NWG;
 // warps: key producer, score-MMA issuer, value producer, P.V issuer, softmax
 constexpr int MA_THREADS = 128 + MA_SOFTMAX;
 constexpr uint32_t MA_TM_S = 256;  // S / P buffers at 256 + 64*sb; O at [0, v)
+constexpr int MA_SBUF = 4;         // S / P buffers (TMEM columns 256..511)
 
 __host__ __device__ constexpr int mat_q_bytes(int n) { return (n / 64 + 1) * MA_BM * 128; }
 // A key tile [K_nope || k_rope] (64 positions) and a value tile, in 64-column chunks.
 __host__ __device__ constexpr int mat_k_bytes(int n) { return (n / 64 + 1) * MA_BN * 128; }
 __host__ __device__ constexpr int mat_v_bytes(int v) { return (v / 64) * MA_BN * 128; }
 
-// barriers: Q, S full x2, P full x2, O done x2, drain x2 (one per MMA issuer),
-// then the K ring (full, empty) and the V ring (full, empty)
-enum { M_QFULL = 0, M_SFULL = 1, M_PFULL = 3, M_ODONE = 5, M_DRAIN = 7, M_RINGS = 9 };
+// barriers: Q, then one S full, P full and O done per S buffer (tile i uses
+// copy i % MA_SBUF, phase i / MA_SBUF), drain x2 (one per MMA issuer), then the
+// K ring (full, empty) and the V ring (full, empty)
+enum {
+  M_QFULL = 0,
+  M_SFULL = 1,
+  M_PFULL = M_SFULL + MA_SBUF,
+  M_ODONE = M_PFULL + MA_SBUF,
+  M_DRAIN = M_ODONE + MA_SBUF,
+  M_RINGS = M_DRAIN + 2
+};
 
 // NQ = n/64 + 1 (the 64-column chunks of [q_nope || q_rope]) is a template
 // parameter so the score MMAs unroll with constant descriptor offsets: tcgen05
@@ -313,7 +322,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
 
   if (threadIdx.x == 0) {
     mbar_init(bar(M_QFULL), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < MA_SBUF; ++i) {
       mbar_init(bar(M_SFULL + i), 1);
       mbar_init(bar(M_PFULL + i), MA_SOFTMAX);
       mbar_init(bar(M_ODONE + i), 1);
@@ -387,7 +396,8 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- score-MMA issuer
-    // S(i) goes to S buffer i&1, which holds P(i-2) until P(i-2) V(i-2) is done.
+    // S(i) goes to S buffer i % MA_SBUF, which holds P(i - MA_SBUF) until its
+    // P.V is done.
     // MMA issue is nearly synchronous, so the scores and P.V come from two
     // warps: a wait in one leaves the tensor pipe to the other.
     if (lane == 0) {
@@ -397,9 +407,10 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
       const uint32_t id_s = idesc_bf16(MA_BM, MA_BN, 0, 0);
       wait_or_fail(ok, bar(M_QFULL), 0, 51);
       for (int i = 0; i < ntiles && ok; ++i) {
-        const int s = i % KS, sb = i & 1;
+        const int s = i % KS, sb = i % MA_SBUF;
         wait_or_fail(ok, k_full(s), (i / KS) & 1, 52);
-        if (i >= 2) wait_or_fail(ok, bar(M_ODONE + sb), ((i - 2) >> 1) & 1, 60);
+        // S buffer sb held P(i - MA_SBUF): its P.V must be done
+        if (i >= MA_SBUF) wait_or_fail(ok, bar(M_ODONE + sb), ((i / MA_SBUF) - 1) & 1, 60);
         if (!ok) break;
         tc_fence_after();
         const uint64_t dks = dk + (uint64_t)(s * (KB >> 4));
@@ -423,8 +434,8 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
       const uint64_t dv = sdesc_sw128(sV, 8192, 1024);
       const uint32_t id_o = idesc_bf16(MA_BM, v, 0, 1);
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int vj = j % VS, pb = j & 1;
-        wait_or_fail(ok, bar(M_PFULL + pb), (j >> 1) & 1, 53);
+        const int vj = j % VS, pb = j % MA_SBUF;
+        wait_or_fail(ok, bar(M_PFULL + pb), (j / MA_SBUF) & 1, 53);
         wait_or_fail(ok, v_full(vj), (j / VS) & 1, 58);
         if (!ok) break;
         tc_fence_after();
@@ -455,9 +466,9 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
     bool ok = true;
     float m_run = -INFINITY, l_run = 0.f;
     for (int i = 0; i < ntiles; ++i) {
-      const int sb = i & 1;
+      const int sb = i % MA_SBUF;
       const int t0 = i * MA_BN;
-      wait_or_fail(ok, bar(M_SFULL + sb), (i >> 1) & 1, 54);
+      wait_or_fail(ok, bar(M_SFULL + sb), (i / MA_SBUF) & 1, 54);
       tc_fence_after();
       uint32_t u[MA_CPT];
 #pragma unroll
@@ -489,7 +500,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
       const float factor = need ? ex2(m_run - m_new) : 1.f;
       if (i > 0 && __any_sync(0xffffffffu, need)) {
         // O must hold P(i-1) V(i-1) before it is rescaled
-        wait_or_fail(ok, bar(M_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, 55);
+        wait_or_fail(ok, bar(M_ODONE + (i - 1) % MA_SBUF), ((i - 1) / MA_SBUF) & 1, 55);
         tc_fence_after();
         for (int c = 0; c < opt; c += 16) {
           uint32_t w[16];
@@ -540,7 +551,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
       mbar_arrive(bar(M_PFULL + sb));
     }
     // ---------------------------------------------------------------- epilogue
-    wait_or_fail(ok, bar(M_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 56);
+    wait_or_fail(ok, bar(M_ODONE + (ntiles - 1) % MA_SBUF), ((ntiles - 1) / MA_SBUF) & 1, 56);
     tc_fence_after();
     pdl_launch_dependents();
     xrow[wg * MA_BM + q] = l_run;
@@ -623,7 +634,7 @@ struct MatRings {
 };
 MatRings mat_rings(int n, int v) {
   const int budget = kSmemPerBlock - kSmemExtra - kMatRowBytes - mat_q_bytes(n);
-  const int cand[][2] = {{4, 4}, {3, 4}, {4, 3}, {3, 3}, {2, 4}, {2, 3}, {3, 2}, {2, 2}};
+  const int cand[][2] = {{4, 4}, {4, 3}, {3, 4}, {3, 3}, {4, 2}, {3, 2}, {2, 4}, {2, 3}, {2, 2}};
   for (const auto& c : cand) {
     const int bytes = c[0] * mat_k_bytes(n) + c[1] * mat_v_bytes(v);
     if (bytes <= budget)
