@@ -3,11 +3,12 @@
 
 Workload (DeepSeek-V3-like geometry): H=128 heads, latent r=512, nope n=128,
 value v=128, RoPE 64, bf16 with fp32 accumulation, one sequence of cache
-length T=8192, verify widths L in {1, 2, 4, 8, 16}, crossover dispatch ("auto",
-which picks the absorbed branch at every one of these widths).  One step is
-one verify call per width (5 layer-calls).  Each call uses its own layer's
-weights and cache; ten layers rotate (about 430 MB, larger than the 129 MB
-L2), so every call streams its operands from HBM.
+length T=8192 (each layer's c_kv and k_rope packed as [T, 576] rows),
+verify widths L in {1, 2, 4, 8, 16}, crossover dispatch ("auto", which picks
+the absorbed branch at every one of these widths).  One step is one verify
+call per width (5 layer-calls).  Each call uses its own layer's weights and
+cache; ten layers rotate (about 430 MB, larger than the 129 MB L2), so every
+call streams its operands from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -428,10 +429,17 @@ def run_ours(args):
     g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope, torch.bfloat16)
 
     # device-resident inputs for every layer
+    # Each layer's latent cache is one packed [1, T, r + rope] buffer (c_kv and
+    # k_rope are views with a row stride of r + rope elements), so the L new
+    # rows of a call are one contiguous region.
     D = []
     for c in layers:
-        D.append({k: getattr(c, k).to(dev) for k in
-                  ("q_nope", "q_rope", "c_kv", "k_rope", "W_UK", "W_UV")})
+        d = {k: getattr(c, k).to(dev) for k in ("q_nope", "q_rope", "W_UK", "W_UV")}
+        packed = torch.cat([c.c_kv, c.k_rope], dim=-1).to(dev)
+        d["packed"] = packed
+        d["c_kv"] = packed[..., :c.geom.r]
+        d["k_rope"] = packed[..., c.geom.r:]
+        D.append(d)
     lens = [CACHE_LEN]
     lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
     ws = {L: torch.empty(max(B.mla_workspace_bytes(g, L, lens, "auto"), 256),
@@ -602,33 +610,49 @@ def _layer_bytes(geom):
 
 
 def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
-    """Same step through the public call, with each step's new inputs (queries
-    and the L new latent rows per call) copied from pinned host memory and the
-    outputs read back to pinned host memory inside the timed region."""
+    """Same step through the public call, with each step's new inputs (the
+    queries of all widths and the L new latent rows per call) copied from
+    pinned host memory and the outputs read back to pinned host memory inside
+    the timed region.  The queries of a step travel in one copy (each call gets
+    views of the staged buffer), each call's new rows in one copy into its
+    layer's packed cache, and the outputs in one copy back."""
     import torch
-    host_q = {L: (q[0][L][0].cpu().pin_memory(), q[0][L][1].cpu().pin_memory())
-              for L in WIDTHS}
-    host_new = {L: (D[0]["c_kv"][:, CACHE_LEN - L:].cpu().pin_memory(),
-                    D[0]["k_rope"][:, CACHE_LEN - L:].cpu().pin_memory()) for L in WIDTHS}
-    host_out = {L: torch.empty(outs[L].shape, dtype=outs[L].dtype).pin_memory() for L in WIDTHS}
-    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size()
-              for a, b in list(host_q.values()) + list(host_new.values()))
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    dq = {L: (torch.empty_like(q[0][L][0]), torch.empty_like(q[0][L][1])) for L in WIDTHS}
+    H, n, v, rope, r = geom.H, geom.n, geom.v, geom.rope, geom.r
+    qn_el = {L: L * H * n for L in WIDTHS}
+    qr_el = {L: L * H * rope for L in WIDTHS}
+    q_total = sum(qn_el[L] + qr_el[L] for L in WIDTHS)
+    host_q = torch.empty(q_total, dtype=torch.bfloat16).pin_memory()
+    dev_q = torch.empty(q_total, dtype=torch.bfloat16, device=dev)
+    views, off = {}, 0
+    for L in WIDTHS:
+        qn = dev_q[off:off + qn_el[L]].view(1, L, H, n)
+        host_q[off:off + qn_el[L]].copy_(q[0][L][0].reshape(-1).cpu())
+        off += qn_el[L]
+        qr = dev_q[off:off + qr_el[L]].view(1, L, H, rope)
+        host_q[off:off + qr_el[L]].copy_(q[0][L][1].reshape(-1).cpu())
+        off += qr_el[L]
+        views[L] = (qn, qr)
+    host_new = {L: D[0]["packed"][:, CACHE_LEN - L:].cpu().pin_memory() for L in WIDTHS}
+    out_el = {L: L * H * v for L in WIDTHS}
+    dev_out = torch.empty(sum(out_el.values()), dtype=torch.bfloat16, device=dev)
+    host_out = torch.empty(dev_out.numel(), dtype=torch.bfloat16).pin_memory()
+    ovs, off = {}, 0
+    for L in WIDTHS:
+        ovs[L] = dev_out[off:off + out_el[L]].view(1, L, H, v)
+        off += out_el[L]
+    h2d = host_q.numel() * 2 + sum(t.numel() * 2 for t in host_new.values())
+    d2h = host_out.numel() * 2
 
     def step(s):
         base = len(WIDTHS) * (s % 2)
+        dev_q.copy_(host_q, non_blocking=True)
         for i, L in enumerate(WIDTHS):
-            li = (base + i) % len(D)
-            d = D[li]
-            dq[L][0].copy_(host_q[L][0], non_blocking=True)
-            dq[L][1].copy_(host_q[L][1], non_blocking=True)
-            d["c_kv"][:, CACHE_LEN - L:].copy_(host_new[L][0], non_blocking=True)
-            d["k_rope"][:, CACHE_LEN - L:].copy_(host_new[L][1], non_blocking=True)
-            B.mla_verify_attention(dq[L][0], dq[L][1], d["c_kv"], d["k_rope"], d["W_UK"],
-                                   d["W_UV"], lens, mode="auto", out=outs[L], workspace=ws[L],
+            d = D[(base + i) % len(D)]
+            d["packed"][:, CACHE_LEN - L:].copy_(host_new[L], non_blocking=True)
+            B.mla_verify_attention(views[L][0], views[L][1], d["c_kv"], d["k_rope"], d["W_UK"],
+                                   d["W_UV"], lens, mode="auto", out=ovs[L], workspace=ws[L],
                                    cache_lens_dev=lens_dev)
-            host_out[L].copy_(outs[L], non_blocking=True)
+        host_out.copy_(dev_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for s in range(3):

@@ -110,6 +110,29 @@ def make_geometry(H, r, n, v, rope, dtype=torch.bfloat16, scale: Optional[float]
                     float(scale) if scale is not None else 0.0, DTYPES[dtype])
 
 
+_GEOMS = {}
+
+
+def _geometry(H, r, n, v, rope, dtype, scale):
+    """A Geometry per distinct shape, built once (the call only reads it)."""
+    key = (H, r, n, v, rope, dtype, scale)
+    g = _GEOMS.get(key)
+    if g is None:
+        g = _GEOMS[key] = make_geometry(H, r, n, v, rope, dtype, scale)
+    return g
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _current_stream(dev: torch.device) -> int:
+    """The raw handle of the current CUDA stream of `dev` (PyTorch's fast accessor
+    when present, else the public one)."""
+    if _raw_stream is not None:
+        return _raw_stream(dev.index if dev.index is not None else torch.cuda.current_device())
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
 def mla_max_absorbed_queries(r: int, n: int, v: int, cache_len: int = 0) -> int:
     return int(lib().mla_max_absorbed_queries(r, n, v, cache_len))
 
@@ -190,7 +213,7 @@ def mla_verify_attention(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv: torch
     v = W_UV.shape[-1]
     dev = q_nope.device
     _dense(q_nope=q_nope, q_rope=q_rope, W_UK=W_UK, W_UV=W_UV, out=out, page_table=page_table)
-    geom = make_geometry(H, r, n, v, rope, q_nope.dtype, scale)
+    geom = _geometry(H, r, n, v, rope, q_nope.dtype, scale)
     lens = [int(t) for t in cache_lens]
     arr = _lens_array(lens)
     paged = page_table is not None
@@ -200,11 +223,11 @@ def mla_verify_attention(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv: torch
     if out is None:
         out = torch.empty((B, L, H, v), dtype=q_nope.dtype, device=dev)
     m = MODES.get(mode, mode)
-    need = mla_workspace_bytes(geom, L, lens, m)
-    if workspace is None:
+    if workspace is None:  # (a given workspace that is too small is rejected by the call)
+        need = mla_workspace_bytes(geom, L, lens, m)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     if stream is None:
-        stream = torch.cuda.current_stream(dev).cuda_stream
+        stream = _current_stream(dev)
     page_size = c_kv.shape[1] if paged else 0
     max_pages = page_table.shape[1] if paged else 0
     num_pages = c_kv.shape[0] if paged else 0
@@ -253,7 +276,7 @@ def mla_verify_attention_noalloc(q_nope: torch.Tensor, q_rope: torch.Tensor,
     r = W_UK.shape[-1]
     v = W_UV.shape[-1]
     dev = q_nope.device
-    geom = make_geometry(H, r, n, v, rope, q_nope.dtype, scale)
+    geom = _geometry(H, r, n, v, rope, q_nope.dtype, scale)
     lens = [int(t) for t in cache_lens]
     arr = _lens_array(lens)
     paged = page_table is not None
@@ -263,7 +286,7 @@ def mla_verify_attention_noalloc(q_nope: torch.Tensor, q_rope: torch.Tensor,
     if out is None:
         out = torch.empty((B, L, H, v), dtype=q_nope.dtype, device=dev)
     if stream is None:
-        stream = torch.cuda.current_stream(dev).cuda_stream
+        stream = _current_stream(dev)
     page_size = c_kv.shape[1] if paged else 0
     max_pages = page_table.shape[1] if paged else 0
     num_pages = c_kv.shape[0] if paged else 0
