@@ -197,7 +197,9 @@ constexpr int NWG = 2;                  // softmax warpgroups; each takes 1/NWG 
 constexpr int CPT = 64 / NWG;           // score columns per softmax thread
 constexpr int OPT = 256 / NWG;          // O (and latent Q) columns per softmax thread
 constexpr int SOFTMAX_THREADS = 128 * NWG;
-constexpr int ATTN_THREADS = 96 + SOFTMAX_THREADS;  // producer, S issuer, P.V issuer, softmax
+constexpr int XCHG_WARP0 = 3 + SOFTMAX_THREADS / 32;  // first of the four score-exchange warps
+// producer, S issuer, P.V issuer, softmax, score exchange
+constexpr int ATTN_THREADS = 96 + SOFTMAX_THREADS + 128;
 constexpr int Q_ROPE = BM * 64;         // the 32 RoPE columns of this CTA's Q rows (64-B swizzle)
 constexpr int KV_CHUNK = BN * 128;      // one 64-column bf16 chunk of a KV tile
 constexpr int KV_ROPE = BN * 64;        // 32 RoPE columns of a KV tile
@@ -247,14 +249,20 @@ enum {
   B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22, B_COUNT = 24
 };
 
+// One partial score of this CTA in log2-softmax units, rounded to fp16: the
+// exchange warps send exactly this to the peer and the softmax adds exactly
+// this to the peer's, so both CTAs of a pair sum the same two rounded values
+// and their scores agree bit for bit.  (Packed conversions: the scalar ones
+// would crowd the pipe the exponentials need.)
+__device__ __forceinline__ __half2 round_partial(uint32_t a, uint32_t b, float sl2) {
+  return __floats2half2_rn(__uint_as_float(a) * sl2, __uint_as_float(b) * sl2);
+}
+
 // This thread's CPT partial scores of tile j (columns c0..c0+CPT-1 of this
-// CTA's share) from TMEM, scaled to log2-softmax units and rounded to fp16
-// pairs: `h` is what goes to the peer, `s` the same rounded values in fp32.
-// Both CTAs add the same two rounded partials, so their sums agree bit for bit.
-// (Packed conversions: the scalar ones would crowd the pipe the exponentials need.)
+// CTA's share) from TMEM, rounded as they are sent, in fp32.
 __device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t lane_base, int c0,
                                              int j, uint32_t bar_sfull0, uint32_t bar_sfree0,
-                                             float sl2, float (&s)[CPT], uint32_t (&h)[CPT / 2]) {
+                                             float sl2, float (&s)[CPT]) {
   const int sb = j & (SBUF - 1);
   wait_or_fail(ok, bar_sfull0 + 8 * sb, (j / SBUF) & 1, 20);
   tc_fence_after();
@@ -265,10 +273,7 @@ __device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t l
   tmem_wait_ld();
 #pragma unroll
   for (int e = 0; e < CPT / 2; ++e) {
-    const __half2 x = __floats2half2_rn(__uint_as_float(v[2 * e]) * sl2,
-                                        __uint_as_float(v[2 * e + 1]) * sl2);
-    h[e] = *reinterpret_cast<const uint32_t*>(&x);
-    const float2 f = __half22float2(x);
+    const float2 f = __half22float2(round_partial(v[2 * e], v[2 * e + 1], sl2));
     s[2 * e] = f.x;
     s[2 * e + 1] = f.y;
   }
@@ -276,15 +281,17 @@ __device__ __forceinline__ void load_partial(bool& ok, uint32_t tmem, uint32_t l
   mbar_arrive(bar_sfree0 + 8 * sb);
 }
 
-// Exchange tile layout: [warpgroup][128 rows][2*CPT B] (the row's CPT fp16
-// partial scores of that warpgroup's columns), 16-byte chunks XOR-swizzled by
-// row so a warp's stores hit distinct banks.  The 32 rows of one warp are one
-// contiguous block, which that warp ships to the peer on its own.
+// Exchange tile layout: [lane quarter][warpgroup][32 rows][2*CPT B] (a row's
+// CPT fp16 partial scores of that warpgroup's columns), 16-byte chunks
+// XOR-swizzled by row so a warp's accesses hit distinct banks.  The 32 rows of
+// one TMEM lane quarter are one contiguous block, which one exchange warp
+// ships to the peer with a single bulk copy.
 constexpr int XROW = 2 * CPT;                   // bytes per row and warpgroup
 constexpr int XCH = XROW / 16;                  // 16-byte chunks per row and warpgroup
+constexpr int XQUARTER = 32 * XROW * NWG;       // bytes per lane quarter
 __device__ __forceinline__ uint32_t xchg_offset(int wg, int q, int c) {
   const int sw = XCH == 4 ? ((q >> 1) & 3) : XCH == 2 ? ((q >> 2) & 1) : 0;
-  return (uint32_t)(wg * (BM * XROW) + q * XROW + ((c ^ sw) << 4));
+  return (uint32_t)((q >> 5) * XQUARTER + wg * (32 * XROW) + (q & 31) * XROW + ((c ^ sw) << 4));
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
@@ -336,7 +343,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SFREE + s), SOFTMAX_THREADS);
+      mbar_init(bar(B_SFREE + s), SOFTMAX_THREADS + 4);  // + one per exchange warp
       mbar_init(bar(B_PFULL + s), SOFTMAX_THREADS);
       mbar_init(bar(B_ODONE + s), 1);
     }
@@ -457,13 +464,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mma_commit(bar(B_DRAIN + 1));
       mbar_wait(bar(B_DRAIN + 1), 0);
     }
+  } else if (warp >= XCHG_WARP0) {
+    // ------------------------------------------------------- score exchange
+    // One warp per TMEM lane quarter ships this CTA's partial scores of each
+    // tile to the peer as soon as the score MMAs finish, up to two tiles ahead
+    // of the softmax, so the softmax's own steps never wait on a copy.
+    if (ntiles > 0) {
+      bool ok = true;
+      const int quarter = warp & 3;
+      const int q = quarter * 32 + lane;
+      const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+      const uint32_t block = (uint32_t)(quarter * XQUARTER);
+      const uint32_t peer_x = mapa(sX, peer);
+      const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
+      for (int j = 0; j < ntiles; ++j) {
+        const int sb = j & (SBUF - 1);
+        wait_or_fail(ok, bar(B_SFULL + sb), (j / SBUF) & 1, 26);
+        tc_fence_after();
+        uint32_t h[BN / 2];  // the row's partials, rounded, as fp16 pairs
+#pragma unroll
+        for (int g = 0; g < BN / 32; ++g) {
+          uint32_t v[32];
+          tmem_ld16(tmem + lane_base + TM_S + sb * BN + 32 * g, *(uint32_t(*)[16])(v));
+          tmem_ld16(tmem + lane_base + TM_S + sb * BN + 32 * g + 16, *(uint32_t(*)[16])(v + 16));
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const __half2 x = round_partial(v[2 * e], v[2 * e + 1], p.sl2);
+            h[16 * g + e] = *reinterpret_cast<const uint32_t*>(&x);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SFREE + sb));
+        if (lane == 0) {
+          bulk_wait_read();  // this warp's previous copy has left the staging block
+          // the peer has read tile j-2 out of exchange buffer j&1
+          if (j >= 2) wait_cluster_or_fail(ok, bar(B_XFREE + (j & 1)), ((j - 2) >> 1) & 1, 21);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < NWG; ++g)
+#pragma unroll
+          for (int k = 0; k < XCH; ++k) {
+            const uint32_t* w = h + g * (CPT / 2) + 4 * k;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             sStg + xchg_offset(g, q, k)),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                         : "memory");
+          }
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0 && ok)
+          bulk_copy_to_peer(peer_x + (j & 1) * X_BYTES + block, sStg + block, XQUARTER,
+                            peer_xfull + 8 * (j & 1));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      if (lane == 0) bulk_wait_read();
+    }
   } else {
     // ------------------------------------------------- softmax warpgroups
     // NWG warpgroups: thread (wg, q) owns row q, score columns CPT*wg.. and O
     // (and latent Q) columns OPT*wg.. of this CTA's share.  Tile i's scores
-    // are finished (own + peer partial) while tile i+1's partial is already on
-    // its way: each warp stages its 32 rows and ships them to the peer with one
-    // bulk copy, so the exchange needs no block-wide barrier.
+    // are this CTA's partial (read again from TMEM, rounded as it was sent)
+    // plus the peer's, which the exchange warps have usually delivered by then.
     const int wg = (warp - 3) >> 2;
     const int q = (warp & 3) * 32 + lane;  // tile row == TMEM lane
     const int c0 = CPT * wg;
@@ -472,33 +537,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     const int l = min(row, p.R - 1) / p.H;
     const int last_t = T - p.L + l;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t wblock = (uint32_t)(wg * (BM * XROW) + (warp & 3) * 32 * XROW);  // this warp's rows
-    const uint32_t peer_x = mapa(sX, peer);
-    const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
     const uint32_t peer_xfree = mapa(bar(B_XFREE), peer);
     bool ok = true;
     int armed = min(ntiles, 2), received = 0;  // exchange phases armed / completed
     float m_run = -INFINITY, l_part = 0.f;
     float s[CPT];
-    // tile j's own partial of row q to the peer (this warp's block of it)
-    auto send = [&](int j, const uint32_t (&h)[CPT / 2]) {
-      if (lane == 0) {
-        bulk_wait_read();  // this warp's previous copy has left the staging block
-        // the peer has read tile j-2 out of exchange buffer j&1
-        if (j >= 2) wait_cluster_or_fail(ok, bar(B_XFREE + (j & 1)), ((j - 2) >> 1) & 1, 21);
-      }
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < XCH; ++k)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sStg + xchg_offset(wg, q, k)),
-                     "r"(h[4 * k]), "r"(h[4 * k + 1]), "r"(h[4 * k + 2]), "r"(h[4 * k + 3])
-                     : "memory");
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0 && ok)
-        bulk_copy_to_peer(peer_x + (j & 1) * X_BYTES + wblock, sStg + wblock, 32 * XROW,
-                          peer_xfull + 8 * (j & 1));
-    };
     if (ntiles > 0) {
       // this CTA's latent query columns into TMEM as bf16 pairs (the fold wrote them)
       pdl_wait();
@@ -507,25 +550,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       const uint4* src = (const uint4*)(p.q_lat) +
                          (((size_t)b * p.rtiles + tile) * 64 + 32 * rank + (OPT / 8) * wg) * 128 +
                          q;
-      uint32_t v[OPT / 2];
 #pragma unroll
-      for (int k = 0; k < OPT / 8; ++k) {
-        const uint4 x = src[(size_t)k * 128];
-        v[4 * k] = x.x;
-        v[4 * k + 1] = x.y;
-        v[4 * k + 2] = x.z;
-        v[4 * k + 3] = x.w;
+      for (int k = 0; k < OPT / 64; ++k) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = src[(size_t)(8 * k + u) * 128];
+          v[4 * u] = x.x;
+          v[4 * u + 1] = x.y;
+          v[4 * u + 2] = x.z;
+          v[4 * u + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_base + TM_QL + (OPT / 2) * wg + 32 * k, v);
       }
-#pragma unroll
-      for (int k = 0; k < OPT / 64; ++k)
-        tmem_st32(tmem + lane_base + TM_QL + (OPT / 2) * wg + 32 * k,
-                  *(const uint32_t(*)[32])(v + 32 * k));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_QTMEM));
-      uint32_t h0[CPT / 2];
-      load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s, h0);
-      send(0, h0);
+      load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
     }
     // One tile of the softmax; `s` holds tile i's own (rounded) partial on entry
     // and `sn` receives tile i+1's.  Called with the two arrays alternating so
@@ -574,12 +615,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         // returned (its values were used before the bar.sync), so no fence
         mbar_arrive_remote_relaxed(peer_xfree + 8 * xb);
       }
-      // tile i+1's partial to the peer
-      if (i + 1 < ntiles) {
-        uint32_t hn[CPT / 2];
-        load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn, hn);
-        send(i + 1, hn);
-      }
+      // this CTA's partial of tile i+1
+      if (i + 1 < ntiles)
+        load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn);
     // lazy rescale: move the running max only when it grows by more than 2^8;
       // O must then hold every earlier P.V
       const bool need = mt > m_run + 8.f;
@@ -650,7 +688,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     if (sm_tid == 0)
       for (int j = received; j < armed; ++j)
         mbar_wait_cluster(bar(B_XFULL + (j & 1)), (j >> 1) & 1);
-    if (lane == 0) bulk_wait_read();
     // ---------------------------------------------------------------- epilogue
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
     pdl_wait();  // the partials may still be read by the previous call's merge
