@@ -568,10 +568,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_arrive(bar(B_QTMEM));
       load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
     }
-    // One tile of the softmax; `s` holds tile i's own (rounded) partial on entry
-    // and `sn` receives tile i+1's.  Called with the two arrays alternating so
-    // the registers swap roles instead of being copied.
-    auto softmax_tile = [&](int i, float (&s)[CPT], float (&sn)[CPT]) {
+    // One tile of the softmax; `s` holds tile i's own (rounded) partial on
+    // entry and tile i+1's on exit (read once P(i) is out, so only one tile's
+    // scores are ever live in registers).
+    for (int i = 0; i < ntiles; ++i) {
       const int t0 = kv0 + i * BN;
       // finish tile i's scores with the peer's partial; the causal verify mask
       // only matters on tiles that reach past the first row's last position
@@ -615,9 +615,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         // returned (its values were used before the bar.sync), so no fence
         mbar_arrive_remote_relaxed(peer_xfree + 8 * xb);
       }
-      // this CTA's partial of tile i+1
-      if (i + 1 < ntiles)
-        load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, sn);
     // lazy rescale: move the running max only when it grows by more than 2^8;
       // O must then hold every earlier P.V
       const bool need = mt > m_run + 8.f;
@@ -677,11 +674,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       fence_async_shared();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + (i & 1)));
-    };
-    float s2[CPT];
-    for (int i = 0; i < ntiles; i += 2) {
-      softmax_tile(i, s, s2);
-      if (i + 1 < ntiles) softmax_tile(i + 1, s2, s);
+      // this CTA's partial of tile i+1
+      if (i + 1 < ntiles)
+        load_partial(ok, tmem, lane_base, c0, i + 1, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
     }
     // after a failure, let an armed exchange phase finish (or time out) so no
     // copy from the peer is still landing when this CTA exits
