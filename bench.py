@@ -615,7 +615,9 @@ def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
     pinned host memory and the outputs read back to pinned host memory inside
     the timed region.  The queries of a step travel in one copy (each call gets
     views of the staged buffer), each call's new rows in one copy into its
-    layer's packed cache, and the outputs in one copy back."""
+    layer's packed cache, all before the step's first call (so the calls'
+    kernels follow one another with no copy between them), and the outputs in
+    one copy back."""
     import torch
     H, n, v, rope, r = geom.H, geom.n, geom.v, geom.rope, geom.r
     qn_el = {L: L * H * n for L in WIDTHS}
@@ -647,8 +649,10 @@ def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
         base = len(WIDTHS) * (s % 2)
         dev_q.copy_(host_q, non_blocking=True)
         for i, L in enumerate(WIDTHS):
+            D[(base + i) % len(D)]["packed"][:, CACHE_LEN - L:].copy_(host_new[L],
+                                                                      non_blocking=True)
+        for i, L in enumerate(WIDTHS):
             d = D[(base + i) % len(D)]
-            d["packed"][:, CACHE_LEN - L:].copy_(host_new[L], non_blocking=True)
             B.mla_verify_attention(views[L][0], views[L][1], d["c_kv"], d["k_rope"], d["W_UK"],
                                    d["W_UV"], lens, mode="auto", out=ovs[L], workspace=ws[L],
                                    cache_lens_dev=lens_dev)
