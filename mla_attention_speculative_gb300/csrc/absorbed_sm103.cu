@@ -778,12 +778,14 @@ __global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
   // the unembedding may start loading its weights now; it waits for this grid
   // before reading o_lat
   pdl_launch_dependents();
-  pdl_wait();
   const int rg = blockIdx.x;  // b*R + row
   const int col0 = blockIdx.y * 256 * CPL;
   const int b = rg / p.R, row = rg - b * p.R;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the length is a call input: read it while the attention finishes, so the
+  // pieces' loads are the only round trip after the wait
   const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
+  pdl_wait();
   const size_t base = (size_t)b * p.splits * p.R + row;
   const size_t stride = (size_t)p.R;
   float M = -FLT_MAX, den = 0.f;
