@@ -49,6 +49,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-materialised", action="store_true",
                     help="skip the materialised-branch shapes")
+    ap.add_argument("--widths", default=None,
+                    help="comma-separated verify widths instead of 1,2,4,8,16 (for profiling "
+                         "one width; the line then describes that workload, not the headline)")
     return ap.parse_args()
 
 
@@ -678,7 +681,11 @@ def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
 
 
 def main():
+    global WIDTHS, WORKLOAD
     args = _args()
+    if args.widths:
+        WIDTHS = tuple(int(x) for x in args.widths.split(","))
+        WORKLOAD = WORKLOAD.replace("L=1,2,4,8,16", "L=" + ",".join(map(str, WIDTHS)))
     if args.impl == "reference":
         run_reference(args)
     else:
