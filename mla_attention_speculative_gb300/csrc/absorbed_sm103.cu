@@ -304,15 +304,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int tile = blockIdx.x >> 1, split = blockIdx.y, b = blockIdx.z;
-  // The unembedding weights are read right after this kernel; at verify widths
-  // the attention leaves HBM mostly idle, so each CTA pulls a slice into L2.
-  if (threadIdx.x == 32 && p.pf != nullptr) {
-    const size_t nct = (size_t)gridDim.x * gridDim.y * gridDim.z;
-    const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-    const size_t slice = ((p.pf_bytes + nct - 1) / nct + 4095) & ~(size_t)4095;
-    for (size_t o = id * slice; o < min(p.pf_bytes, (id + 1) * slice); o += 32768)
-      prefetch_l2(p.pf + o, (uint32_t)min((size_t)32768, p.pf_bytes - o));
-  }
   const int T = p.lens[b];
   const int nsplit = (T + p.chunk - 1) / p.chunk;
   if (split >= nsplit) return;  // both CTAs of the cluster leave together
@@ -393,6 +384,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       pdl_wait();
       mbar_arrive_expect_tx(bar(B_QFULL), Q_ROPE);
       tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
+      // The unembedding weights are read right after this kernel; at verify
+      // widths the attention leaves HBM mostly idle, so each CTA pulls a slice
+      // into L2 -- once its own first KV tiles are requested, which it needs
+      // first.
+      if (p.pf != nullptr) {
+        const size_t nct = (size_t)gridDim.x * gridDim.y * gridDim.z;
+        const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const size_t slice = ((p.pf_bytes + nct - 1) / nct + 4095) & ~(size_t)4095;
+        for (size_t o = id * slice; o < min(p.pf_bytes, (id + 1) * slice); o += 32768)
+          prefetch_l2(p.pf + o, (uint32_t)min((size_t)32768, p.pf_bytes - o));
+      }
       int issued = pre;
       for (int i = STAGES; i < ntiles; ++i) {
         wait_or_fail(ok, bar(B_KVEMPTY + i % STAGES), ((i / STAGES) - 1) & 1, 10);
