@@ -386,9 +386,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
       // The unembedding weights are read right after this kernel; at verify
       // widths the attention leaves HBM mostly idle, so each CTA pulls a slice
-      // into L2 -- once its own first KV tiles are requested, which it needs
-      // first.
+      // into L2 -- once its own first KV tiles have landed, so that the two do
+      // not share the HBM bandwidth the first tiles wait for.
       if (p.pf != nullptr) {
+        mbar_wait(bar(B_KVFULL + (pre - 1) % STAGES), 0);
         const size_t nct = (size_t)gridDim.x * gridDim.y * gridDim.z;
         const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
         const size_t slice = ((p.pf_bytes + nct - 1) / nct + 4095) & ~(size_t)4095;
