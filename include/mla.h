@@ -207,6 +207,14 @@ mla_status_t mla_kernel_timing_read(char* names, size_t names_len, int32_t* laun
  * (its outputs are then undefined).  clear != 0 resets the word. */
 mla_status_t mla_device_status(int32_t* code, int32_t clear);
 
+/* Failure-path self-test: launches one CTA on `stream` (cudaStream_t, NULL =
+ * default stream) whose bounded wait on a barrier that nothing signals runs
+ * out after about a second and records site 99 in the status word, as a
+ * kernel whose signal never arrived would.  It touches no caller buffer and
+ * leaves the context usable; mla_device_status then returns MLA_ERR_TIMEOUT
+ * with *code == 99.  Returns MLA_ERR_CUDA if the launch fails. */
+mla_status_t mla_selftest_bounded_wait(void* stream);
+
 /* Static name of a status code. */
 const char* mla_status_string(int32_t status);
 

@@ -65,6 +65,7 @@ _SIGS = {
     "mla_kernel_timing_read": (_I32, [ctypes.c_char_p, ctypes.c_size_t, _P, _P, _I32, _P,
                                       _I32]),
     "mla_device_status": (_I32, [_P, _I32]),
+    "mla_selftest_bounded_wait": (_I32, [_P]),
     "mla_status_string": (ctypes.c_char_p, [_I32]),
     "mla_last_error": (ctypes.c_char_p, []),
     "mla_version": (_I32, []),
@@ -175,6 +176,14 @@ def mla_device_status(clear: bool = True) -> int:
     code = ctypes.c_int32(0)
     _check(lib().mla_device_status(ctypes.byref(code), 1 if clear else 0), "mla_device_status")
     return code.value
+
+
+def mla_selftest_bounded_wait(stream=None) -> None:
+    """Launch the library's failure-path self-test (a bounded wait that runs out
+    after about a second); mla_device_status then raises MLA_ERR_TIMEOUT."""
+    if stream is None:
+        stream = _current_stream(torch.device("cuda", torch.cuda.current_device()))
+    _check(lib().mla_selftest_bounded_wait(stream), "mla_selftest_bounded_wait")
 
 
 def cache_strides(c_kv: torch.Tensor, k_rope: torch.Tensor, paged: bool):

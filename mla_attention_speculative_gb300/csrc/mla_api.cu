@@ -399,4 +399,13 @@ extern "C" mla_status_t mla_device_status(int32_t* code, int32_t clear) {
   return MLA_OK;
 }
 
+extern "C" mla_status_t mla_selftest_bounded_wait(void* stream) {
+  const cudaError_t e = launch_wait_selftest((cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    set_error("CUDA error %d (%s)", (int)e, cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
 extern "C" int32_t mla_version(void) { return 100; }

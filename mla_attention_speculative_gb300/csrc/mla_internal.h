@@ -94,6 +94,11 @@ bool fast_absorbed_supported(const Plan& p);
 cudaError_t launch_fast_absorbed(const Plan& p, const Args& a);
 // Status word of the tensor-core kernels (0 = no wait ran out); synchronises.
 int absorbed_device_status(bool clear);
+// The status-word site the bounded-wait self-test records.
+constexpr int kSelftestSite = 99;
+// One CTA whose bounded wait runs out on purpose (no fault, no hang: the wait
+// gives up after its limit and records kSelftestSite).
+cudaError_t launch_wait_selftest(cudaStream_t stream);
 
 // Tensor-core kernels for the materialised branch (bf16, r = 512, rope = 64,
 // n and v multiples of 64 up to 256): a tcgen05 expansion GEMM into a

@@ -251,3 +251,22 @@ def test_kernel_routing(mode, dtype, page, want):
         B.mla_kernel_timing_enable(False)
     assert ran == want, ran
     compare(out, oracle_out(case), dtype, f"routing {mode} page={page}")
+
+
+# ---------------------------------------------------------------------------
+# Failure path: a bounded device wait that runs out is reported, not hung on
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_runs_out_and_context_stays_usable():
+    import ctypes
+    code = ctypes.c_int32(0)
+    assert B.lib().mla_device_status(ctypes.byref(code), 1) == B.MLA_OK  # start clean
+    B.mla_selftest_bounded_wait()  # a barrier nothing signals: gives up after ~1 s
+    assert B.lib().mla_device_status(ctypes.byref(code), 1) == B.MLA_ERR_TIMEOUT
+    assert code.value == 99
+    assert B.lib().mla_device_status(ctypes.byref(code), 1) == B.MLA_OK  # cleared
+    assert code.value == 0
+    # the context still runs a call, and that call reports no timeout
+    case = make_case(Geometry(H=8), 4, [300], seed=91)
+    out, _ = run_gpu(case, "absorbed")
+    compare(out, oracle_out(case), torch.bfloat16, "after the self-test")
