@@ -1002,26 +1002,6 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   return cudaGetLastError();
 }
 
-namespace {
-// One thread waits on a shared-memory barrier that nothing ever signals: the
-// bounded wait gives up after its limit and records kSelftestSite, exactly as
-// a kernel whose signal never came would.
-__global__ void __launch_bounds__(32) wait_selftest_sm103() {
-  __shared__ uint64_t bar;
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar), 1);
-    fence_mbar_init();
-    bool ok = true;
-    wait_or_fail(ok, smem_u32(&bar), 0, kSelftestSite);
-  }
-}
-}  // namespace
-
-cudaError_t launch_wait_selftest(cudaStream_t stream) {
-  wait_selftest_sm103<<<1, 32, 0, stream>>>();
-  return cudaGetLastError();
-}
-
 int absorbed_device_status(bool clear) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_absorbed_status, sizeof(int)) != cudaSuccess) return -1;

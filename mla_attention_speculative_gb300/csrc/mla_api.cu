@@ -386,7 +386,8 @@ extern "C" const char* mla_last_error(void) { return g_err; }
 extern "C" mla_status_t mla_device_status(int32_t* code, int32_t clear) {
   const int va = absorbed_device_status(clear != 0);
   const int vm = materialised_device_status(clear != 0);
-  const int v = va < 0 || vm < 0 ? -1 : va != 0 ? va : vm;
+  const int vs = selftest_device_status(clear != 0);
+  const int v = va < 0 || vm < 0 || vs < 0 ? -1 : va != 0 ? va : vm != 0 ? vm : vs;
   if (code) *code = v;
   if (v < 0) {
     set_error("could not read the device status word");

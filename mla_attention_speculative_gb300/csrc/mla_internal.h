@@ -99,6 +99,7 @@ constexpr int kSelftestSite = 99;
 // One CTA whose bounded wait runs out on purpose (no fault, no hang: the wait
 // gives up after its limit and records kSelftestSite).
 cudaError_t launch_wait_selftest(cudaStream_t stream);
+int selftest_device_status(bool clear);
 
 // Tensor-core kernels for the materialised branch (bf16, r = 512, rope = 64,
 // n and v multiples of 64 up to 256): a tcgen05 expansion GEMM into a
