@@ -612,6 +612,24 @@ def _layer_bytes(geom):
             + CACHE_LEN * (geom.r + geom.rope)) * 2
 
 
+def _cudart():
+    """The CUDA runtime the process already uses (for plain async copies: a
+    cudaMemcpyAsync costs the host about a microsecond, a tensor copy_ call
+    several)."""
+    import ctypes
+    for name in ("libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so.13",
+                 "/usr/local/cuda/lib64/libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+        except OSError:
+            continue
+        rt.cudaMemcpyAsync.restype = ctypes.c_int
+        rt.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                       ctypes.c_int, ctypes.c_void_p]
+        return rt
+    raise RuntimeError("no CUDA runtime library found for the end-to-end copies")
+
+
 def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
     """Same step through the public call, with each step's new inputs (the
     queries of all widths and the L new latent rows per call) copied from
@@ -620,7 +638,8 @@ def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
     views of the staged buffer), each call's new rows in one copy into its
     layer's packed cache, all before the step's first call (so the calls'
     kernels follow one another with no copy between them), and the outputs in
-    one copy back."""
+    one copy back.  The copies are plain cudaMemcpyAsync calls on the current
+    stream."""
     import torch
     H, n, v, rope, r = geom.H, geom.n, geom.v, geom.rope, geom.r
     qn_el = {L: L * H * n for L in WIDTHS}
@@ -647,19 +666,34 @@ def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
         off += out_el[L]
     h2d = host_q.numel() * 2 + sum(t.numel() * 2 for t in host_new.values())
     d2h = host_out.numel() * 2
+    rt = _cudart()
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    H2D, D2H = 1, 2
+    # (destination, source, bytes) of every input copy of a step, per half of the layers
+    ins = []
+    for half in range(2):
+        cp = [(dev_q.data_ptr(), host_q.data_ptr(), host_q.numel() * 2)]
+        for i, L in enumerate(WIDTHS):
+            dst = D[(len(WIDTHS) * half + i) % len(D)]["packed"][:, CACHE_LEN - L:]
+            assert dst.is_contiguous()
+            cp.append((dst.data_ptr(), host_new[L].data_ptr(), host_new[L].numel() * 2))
+        ins.append(cp)
+    outcp = (host_out.data_ptr(), dev_out.data_ptr(), host_out.numel() * 2)
+
+    def copy(dst, src, nbytes, kind):
+        if rt.cudaMemcpyAsync(dst, src, nbytes, kind, stream) != 0:
+            raise RuntimeError("cudaMemcpyAsync failed")
 
     def step(s):
         base = len(WIDTHS) * (s % 2)
-        dev_q.copy_(host_q, non_blocking=True)
-        for i, L in enumerate(WIDTHS):
-            D[(base + i) % len(D)]["packed"][:, CACHE_LEN - L:].copy_(host_new[L],
-                                                                      non_blocking=True)
+        for dst, src, nbytes in ins[s % 2]:
+            copy(dst, src, nbytes, H2D)
         for i, L in enumerate(WIDTHS):
             d = D[(base + i) % len(D)]
             B.mla_verify_attention(views[L][0], views[L][1], d["c_kv"], d["k_rope"], d["W_UK"],
                                    d["W_UV"], lens, mode="auto", out=ovs[L], workspace=ws[L],
                                    cache_lens_dev=lens_dev)
-        host_out.copy_(dev_out, non_blocking=True)
+        copy(*outcp, D2H)
         torch.cuda.current_stream().synchronize()
 
     for s in range(3):
