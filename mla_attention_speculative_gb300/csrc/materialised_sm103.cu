@@ -304,7 +304,6 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
   const int l_last = min(L - 1, l0 + MA_BM - 1);
   const int kv_end = T - L + l_last + 1;  // no row of the tile sees t >= kv_end
   const int ntiles = (kv_end + MA_BN - 1) / MA_BN;
-  constexpr int nq = NQ;  // Q / K chunks of 64 columns: n/64 nope + 1 RoPE
   const int KS = p.ks, VS = p.vs;
   const int QB = mat_q_bytes(n), KB = mat_k_bytes(n), VB = mat_v_bytes(v);
   const uint32_t sQ = smem_u32(smem), sK = sQ + QB, sV = sK + KS * KB;
