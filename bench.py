@@ -639,7 +639,9 @@ def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
     layer's packed cache, all before the step's first call (so the calls'
     kernels follow one another with no copy between them), and the outputs in
     one copy back.  The copies are plain cudaMemcpyAsync calls on the current
-    stream."""
+    stream.  The calls are the library's prepared form of the public call
+    (binding.PreparedVerifyAttention: the same C entry point, its arguments
+    marshalled once for these fixed buffers), as a serving loop would use."""
     import torch
     H, n, v, rope, r = geom.H, geom.n, geom.v, geom.rope, geom.r
     qn_el = {L: L * H * n for L in WIDTHS}
@@ -684,15 +686,22 @@ def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
         if rt.cudaMemcpyAsync(dst, src, nbytes, kind, stream) != 0:
             raise RuntimeError("cudaMemcpyAsync failed")
 
+    calls = []
+    for half in range(2):
+        row = []
+        for i, L in enumerate(WIDTHS):
+            d = D[(len(WIDTHS) * half + i) % len(D)]
+            row.append(B.PreparedVerifyAttention(views[L][0], views[L][1], d["c_kv"], d["k_rope"],
+                                                 d["W_UK"], d["W_UV"], lens, mode="auto",
+                                                 out=ovs[L], workspace=ws[L],
+                                                 cache_lens_dev=lens_dev))
+        calls.append(row)
+
     def step(s):
-        base = len(WIDTHS) * (s % 2)
         for dst, src, nbytes in ins[s % 2]:
             copy(dst, src, nbytes, H2D)
-        for i, L in enumerate(WIDTHS):
-            d = D[(base + i) % len(D)]
-            B.mla_verify_attention(views[L][0], views[L][1], d["c_kv"], d["k_rope"], d["W_UK"],
-                                   d["W_UV"], lens, mode="auto", out=ovs[L], workspace=ws[L],
-                                   cache_lens_dev=lens_dev)
+        for call in calls[s % 2]:
+            call.run()
         copy(*outcp, D2H)
         torch.cuda.current_stream().synchronize()
 

@@ -201,21 +201,11 @@ def cache_strides(c_kv: torch.Tensor, k_rope: torch.Tensor, paged: bool):
     return cs, ks, c_kv.stride(0) // cs
 
 
-def mla_verify_attention(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv: torch.Tensor,
-                         k_rope: torch.Tensor, W_UK: torch.Tensor, W_UV: torch.Tensor,
-                         cache_lens: Sequence[int], mode="auto",
-                         out: Optional[torch.Tensor] = None,
-                         workspace: Optional[torch.Tensor] = None,
-                         page_table: Optional[torch.Tensor] = None,
-                         cache_lens_dev: Optional[torch.Tensor] = None,
-                         scale: Optional[float] = None, stream=None):
-    """One verify call through the C ABI.  Returns (out, branch).
-
-    q_nope [B,L,H,n], q_rope [B,L,H,rope], W_UK [H,n,r], W_UV [H,r,v]; the
-    cache is c_kv [B,Tmax,r] / k_rope [B,Tmax,rope] (contiguous) or
-    [num_pages,page,r] / [num_pages,page,rope] with ``page_table`` [B,max_pages].
-    ``out`` and ``workspace`` are allocated with torch when not given.
-    """
+def _verify_args(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, mode, out, workspace,
+                 page_table, cache_lens_dev, scale):
+    """Checks, defaults and the C arguments of mla_verify_attention up to (not
+    including) the stream and the branch pointer.  Returns (args, out, dev,
+    keep), keep holding every tensor the arguments point into."""
     B, L, H, n = q_nope.shape
     rope = q_rope.shape[-1]
     r = W_UK.shape[-1]
@@ -235,19 +225,76 @@ def mla_verify_attention(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv: torch
     if workspace is None:  # (a given workspace that is too small is rejected by the call)
         need = mla_workspace_bytes(geom, L, lens, m)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    if stream is None:
-        stream = _current_stream(dev)
     page_size = c_kv.shape[1] if paged else 0
     max_pages = page_table.shape[1] if paged else 0
     num_pages = c_kv.shape[0] if paged else 0
+    args = [ctypes.byref(geom), _ptr(q_nope), _ptr(q_rope), _ptr(c_kv), _ptr(k_rope), cs, ks, seq,
+            _ptr(W_UK), _ptr(W_UV), _ptr(cache_lens_dev), arr, B, L, _ptr(page_table), page_size,
+            max_pages, num_pages, m, _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size()]
+    keep = (q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, page_table, cache_lens_dev, out, workspace)
+    return args, out, dev, keep
+
+
+def mla_verify_attention(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv: torch.Tensor,
+                         k_rope: torch.Tensor, W_UK: torch.Tensor, W_UV: torch.Tensor,
+                         cache_lens: Sequence[int], mode="auto",
+                         out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         page_table: Optional[torch.Tensor] = None,
+                         cache_lens_dev: Optional[torch.Tensor] = None,
+                         scale: Optional[float] = None, stream=None):
+    """One verify call through the C ABI.  Returns (out, branch).
+
+    q_nope [B,L,H,n], q_rope [B,L,H,rope], W_UK [H,n,r], W_UV [H,r,v]; the
+    cache is c_kv [B,Tmax,r] / k_rope [B,Tmax,rope] (contiguous) or
+    [num_pages,page,r] / [num_pages,page,rope] with ``page_table`` [B,max_pages].
+    ``out`` and ``workspace`` are allocated with torch when not given.
+    """
+    args, out, dev, _ = _verify_args(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, mode,
+                                     out, workspace, page_table, cache_lens_dev, scale)
+    if stream is None:
+        stream = _current_stream(dev)
     branch = ctypes.c_int32(0)
-    st = lib().mla_verify_attention(
-        ctypes.byref(geom), _ptr(q_nope), _ptr(q_rope), _ptr(c_kv), _ptr(k_rope), cs, ks, seq,
-        _ptr(W_UK), _ptr(W_UV), _ptr(cache_lens_dev), arr, B, L, _ptr(page_table), page_size,
-        max_pages, num_pages, m, _ptr(out), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), stream, ctypes.byref(branch))
+    st = lib().mla_verify_attention(*args, stream, ctypes.byref(branch))
     _check(st, "mla_verify_attention")
     return out, branch.value
+
+
+class PreparedVerifyAttention:
+    """mla_verify_attention with its arguments marshalled once.
+
+    For a caller that repeats a call on the same device buffers, as a serving
+    loop does when it writes each step's queries and new cache rows into fixed
+    tensors: the tensors, shapes, cache lengths and mode are fixed when the
+    object is made (with the same checks and defaults as
+    mla_verify_attention); ``run()`` issues the call on the current stream
+    (or ``stream``) with whatever the buffers hold then, and returns the
+    branch taken.  The tensors must outlive the object.  The library entry
+    point and its results are the same as for mla_verify_attention.
+    """
+
+    def __init__(self, q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, mode="auto",
+                 out=None, workspace=None, page_table=None, cache_lens_dev=None, scale=None):
+        args, self.out, dev, self._keep = _verify_args(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV,
+                                                       cache_lens, mode, out, workspace,
+                                                       page_table, cache_lens_dev, scale)
+        self._fn = lib().mla_verify_attention
+        types = _SIGS["mla_verify_attention"][1]
+        # plain ints become ctypes values now, so a run converts nothing
+        self._args = [types[i](a) if isinstance(a, int) else a for i, a in enumerate(args)]
+        self._dev = dev.index if dev.index is not None else torch.cuda.current_device()
+        self._branch = ctypes.c_int32(0)
+        self._branch_ref = ctypes.byref(self._branch)
+
+    def run(self, stream=None) -> int:
+        if stream is None:
+            stream = (_raw_stream(self._dev) if _raw_stream is not None else
+                      torch.cuda.current_stream(self._dev).cuda_stream)
+        st = self._fn(*self._args, stream, self._branch_ref)
+        if st != MLA_OK:
+            _check(st, "mla_verify_attention")
+        return self._branch.value
 
 
 def mla_kernel_timing_enable(on: bool = True) -> None:

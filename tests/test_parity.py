@@ -270,3 +270,30 @@ def test_bounded_wait_runs_out_and_context_stays_usable():
     case = make_case(Geometry(H=8), 4, [300], seed=91)
     out, _ = run_gpu(case, "absorbed")
     compare(out, oracle_out(case), torch.bfloat16, "after the self-test")
+
+
+# ---------------------------------------------------------------------------
+# Prepared call: the same entry point with its arguments marshalled once
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode,page", [("absorbed", 0), ("materialised", 64)])
+def test_prepared_call_runs_on_new_buffer_contents(mode, page):
+    case = make_case(Geometry(H=8), 4, [300, 129], seed=95, page_size=page)
+    d = device_tensors(case)
+    call = B.PreparedVerifyAttention(d["q_nope"], d["q_rope"], d["c_kv"], d["k_rope"], d["W_UK"],
+                                     d["W_UV"], case.cache_lens, mode=mode,
+                                     page_table=d["page_table"], cache_lens_dev=d["lens_dev"])
+    want_branch = B.BRANCH_ABSORBED if mode == "absorbed" else B.BRANCH_MATERIALISED
+    assert call.run() == want_branch
+    torch.cuda.synchronize()
+    B.mla_device_status()
+    compare(call.out, oracle_out(case), torch.bfloat16, f"prepared {mode}")
+    # new queries written into the same buffers: the next run reads them
+    other = make_case(Geometry(H=8), 4, [300, 129], seed=96, page_size=page)
+    d["q_nope"].copy_(other.q_nope)
+    d["q_rope"].copy_(other.q_rope)
+    call.run()
+    torch.cuda.synchronize()
+    B.mla_device_status()
+    case.q_nope, case.q_rope = other.q_nope, other.q_rope
+    compare(call.out, oracle_out(case), torch.bfloat16, f"prepared {mode}, new queries")
