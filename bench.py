@@ -275,6 +275,73 @@ def _profile_traffic(kernel: str):
     return None
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons of the bench's GPU, read through NVML
+    (the driver's libnvidia-ml, found by the GPU's PCI bus id so that a
+    remapped CUDA_VISIBLE_DEVICES cannot point it at another GPU) every half
+    millisecond from a background thread, so that even a timed region of a
+    few milliseconds gets samples taken while it runs.  Reading only."""
+
+    # clock-event reason bits (nvml.h)
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, dev_index: int):
+        import ctypes
+        import threading
+        self.ctypes, self.threading = ctypes, threading
+        nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if nvml.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        rt = _cudart()
+        bus = ctypes.create_string_buffer(32)
+        rt.cudaDeviceGetPCIBusId.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.c_int]
+        if rt.cudaDeviceGetPCIBusId(bus, 32, dev_index) != 0:
+            raise RuntimeError("cudaDeviceGetPCIBusId failed")
+        self.handle = ctypes.c_void_p()
+        if nvml.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.handle)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByPciBusId failed")
+        self.nvml = nvml
+        self.get_reasons = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))  # 1 = SM clock
+        self.max_mhz = float(mx.value)
+        self.samples, self.reasons, self.run = [], 0, False
+
+    def _loop(self):
+        ctypes = self.ctypes
+        mhz, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while self.run:
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(float(mhz.value))
+            if self.get_reasons(self.handle, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(0.0005)
+
+    def start(self):
+        self.run = True
+        self.thread = self.threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.run = False
+        self.thread.join()
+        if not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for n, bit in self.REASONS.items() if self.reasons & bit),
+                "samples": len(self.samples), "source": "nvml"}
+
+
+def clock_sampler(dev_index: int):
+    """NVML sampling when the driver library is there, else nvidia-smi."""
+    try:
+        return NvmlClockSampler(dev_index)
+    except Exception:
+        return ClockSampler(dev_index)
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons during the timed region."""
 
@@ -487,9 +554,10 @@ def run_ours(args):
             dist.barrier()
 
     # ---- timed region: K graph-replayed steps --------------------------------
-    sampler = ClockSampler(local)
+    sampler = clock_sampler(local)
     sampler.start()
-    time.sleep(0.3)
+    if isinstance(sampler, ClockSampler):
+        time.sleep(0.3)  # nvidia-smi needs a moment before its first line
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
