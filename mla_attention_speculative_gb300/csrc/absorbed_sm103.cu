@@ -2,8 +2,8 @@
 //
 // "One guard, 110x off the verify step", section "The defect": fold the key
 // up-projection into the query, attend against the compressed latent, then
-// apply the value up-projection.  Three kernels, all bf16 operands with fp32
-// accumulation in tensor memory:
+// apply the value up-projection.  Three kernels (the GEMM runs twice), all
+// bf16 operands with fp32 accumulation in tensor memory:
 //
 //  swapab_gemm     fold: q_lat[row, h, :] = q_nope[row, h, :] . W_UK[h] (n -> 512)
 //                  and unembed: out[row, h, :] = o_lat[row, h, :] . W_UV[h]
@@ -17,13 +17,13 @@
 //                  Each latent tile is read once for all 128 rows of a tile
 //                  ("Multi-row attention kernel" on the same page).  A cluster
 //                  of two CTAs shares one 128-row tile: CTA j holds latent
-//                  columns [256j, 256j+256) (CTA 0 also the 64 RoPE columns),
+//                  columns [256j, 256j+256) and RoPE columns [32j, 32j+32),
 //                  computes its partial scores over its columns, swaps them
 //                  with the peer through distributed shared memory, and both
 //                  accumulate their half of o_lat (128 x 256 fp32 in TMEM).
 //  merge_sm103     log-sum-exp merge of the split-KV pieces into bf16 o_lat.
 //
-// The four kernels are chained with programmatic dependent launch: each one
+// The four launches are chained with programmatic dependent launch: each one
 // starts the loads that do not depend on its predecessor (weights, the KV
 // cache) before waiting for it.
 //
