@@ -304,17 +304,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int tile = blockIdx.x >> 1, split = blockIdx.y, b = blockIdx.z;
-  const int T = p.lens[b];
-  const int nsplit = (T + p.chunk - 1) / p.chunk;
-  if (split >= nsplit) return;  // both CTAs of the cluster leave together
-
-  const int row0 = tile * BM;
-  const int l_last = min(p.R - 1, row0 + BM - 1) / p.H;
-  const int vis_end = T - p.L + l_last + 1;
-  const int kv0 = split * p.chunk;
-  const int kv1 = min(min(kv0 + p.chunk, T), vis_end);
-  const int ntiles = kv1 > kv0 ? (kv1 - kv0 + BN - 1) / BN : 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // (the sequence length is first needed after the barrier and TMEM setup
+  // below, which its load overlaps)
+  const int T = p.lens[b];
 
   uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
   uint32_t* slot = (uint32_t*)(bars + B_COUNT + 4);
@@ -345,16 +338,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
     fence_mbar_init();
-    // arm the exchange barrier for tile 0 (the peer's bulk copy counts it down)
-    if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
-    if (ntiles > 1) mbar_arrive_expect_tx(bar(B_XFULL + 1), X_BYTES);
   }
   if (warp == 1) tmem_alloc(smem_u32(slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers exist (and are armed) before any remote access
   const uint32_t tmem = *slot;
+  const int nsplit = (T + p.chunk - 1) / p.chunk;
+  if (split >= nsplit) {  // both CTAs of the cluster leave together, the peer untouched
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
+  const int row0 = tile * BM;
+  const int l_last = min(p.R - 1, row0 + BM - 1) / p.H;
+  const int vis_end = T - p.L + l_last + 1;
+  const int kv0 = split * p.chunk;
+  const int kv1 = min(min(kv0 + p.chunk, T), vis_end);
+  const int ntiles = kv1 > kv0 ? (kv1 - kv0 + BN - 1) / BN : 0;
+  // arm the exchange barriers for tiles 0 and 1 (the peer's bulk copies count
+  // them down), then publish the setup to the peer: each role waits for the
+  // peer's setup only before its first access to the peer, so the KV loads,
+  // the query load and the score MMAs do not wait for the slower CTA
+  if (threadIdx.x == 0) {
+    if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
+    if (ntiles > 1) mbar_arrive_expect_tx(bar(B_XFULL + 1), X_BYTES);
+  }
+  cluster_arrive();
   pdl_launch_dependents();  // the merge may launch; it waits for this grid
 
   if (warp == 0) {
@@ -408,6 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       for (int i = max(issued - STAGES, 0); i < issued; ++i)
         mbar_wait(bar(B_KVFULL + i % STAGES), (i / STAGES) & 1);
     }
+    cluster_wait();  // (this role never touches the peer)
   } else if (warp == 1) {
     // ------------------------------------------------------- score-MMA issuer
     // S(i) = Q . K(i)^T over this CTA's 256 latent (Q from TMEM) + 32 RoPE
@@ -443,6 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0);
     }
+    cluster_wait();
   } else if (warp == 2) {
     // --------------------------------------------------------- P.V issuer
     // O += P(j) . V(j) over this CTA's 256 latent columns of the KV tile; the
@@ -467,11 +478,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mma_commit(bar(B_DRAIN + 1));
       mbar_wait(bar(B_DRAIN + 1), 0);
     }
+    cluster_wait();
   } else if (warp >= XCHG_WARP0) {
     // ------------------------------------------------------- score exchange
     // One warp per TMEM lane quarter ships this CTA's partial scores of each
     // tile to the peer as soon as the score MMAs finish, up to two tiles ahead
     // of the softmax, so the softmax's own steps never wait on a copy.
+    cluster_wait();  // the peer's exchange barriers are set up
     if (ntiles > 0) {
       bool ok = true;
       const int quarter = warp & 3;
@@ -571,6 +584,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_arrive(bar(B_QTMEM));
       load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
     }
+    cluster_wait();  // the peer's barriers are set up before the first remote arrive
     // One tile of the softmax; `s` holds tile i's own (rounded) partial on
     // entry and tile i+1's on exit (read once P(i) is out, so only one tile's
     // scores are ever live in registers).
