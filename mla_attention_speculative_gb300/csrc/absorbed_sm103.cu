@@ -746,7 +746,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         tma_store_3d(&tm_op, sKV + bx * (BM * 128), (int)rank * 256 + 64 * bx, row0,
                      b * p.splits + split);
       bulk_commit();
-      bulk_wait_all();
+      // the staging may be released once the stores have read it; their
+      // writes are complete when the grid is (the merge reads them after its
+      // dependency wait)
+      bulk_wait_read();
     }
     if (live && rank == 0 && wg == 0) {
       float* mlp = p.ml + (((size_t)b * p.splits + split) * p.R + row) * 2;

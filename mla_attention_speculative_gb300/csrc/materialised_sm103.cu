@@ -235,7 +235,9 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
     for (int c = 0; c < (nk + nv) / 64; ++c)
       tma_store_3d(&tm_out, sbase + c * (EX_BM * 128), out0 + 64 * c, t0, plane);
     bulk_commit();
-    bulk_wait_all();
+    // shared memory is free once the stores have read it; their writes are
+    // complete when the grid is (the attention reads them after its wait)
+    bulk_wait_read();
   }
   tc_fence_before();
   __syncthreads();
