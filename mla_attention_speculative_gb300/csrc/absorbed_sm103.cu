@@ -779,6 +779,7 @@ struct MergeParams {
   const int32_t* lens;
   __nv_bfloat16* o_lat;         // [B*R, 512]
   int R, chunk, splits;
+  int rows;                     // B*R
 };
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
@@ -880,6 +881,68 @@ __global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
           make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
                      pack_bf16(y[6], y[7]));
     }
+  }
+}
+
+// Few pieces per row: one warp per row over all its pieces (lane c owns
+// columns 8c..8c+7 and 256+8c..256+8c+7), eight pieces' loads in flight per
+// lane, so no shared memory and no barrier; four rows per CTA.
+constexpr int MR_ROWS = 4;
+__global__ void __launch_bounds__(32 * MR_ROWS) merge_rows_sm103(MergeParams p) {
+  pdl_launch_dependents();  // the unembedding may start loading its weights
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = blockIdx.x * MR_ROWS + w;  // b*R + row
+  const bool live = rg < p.rows;
+  const int b = live ? rg / p.R : 0, row = rg - b * p.R;
+  // (the length is a call input: read it before the wait)
+  const int nsplit = live ? (p.lens[b] + p.chunk - 1) / p.chunk : 0;
+  pdl_wait();
+  if (!live) return;
+  const size_t base = (size_t)b * p.splits * p.R + row;
+  float M = -FLT_MAX, den = 0.f, acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += 8) {
+    float2 mls[8];
+    uint4 x[8][2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const size_t e = base + (size_t)min(s0 + j, nsplit - 1) * p.R;
+      mls[j] = *(const float2*)(p.ml + e * 2);
+      const __nv_bfloat16* o = p.o_part + e * kLat + 8 * lane;
+      x[j][0] = *(const uint4*)(o);
+      x[j][1] = *(const uint4*)(o + 256);
+      if (s0 + j >= nsplit) mls[j].y = 0.f;  // past the last piece: weight 0
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (mls[j].y > 0.f) {
+        if (mls[j].x > M) {  // warp-uniform: every lane reads the same (m, l)
+          const float f = ex2(M - mls[j].x);
+          M = mls[j].x;
+          den *= f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] *= f;
+        }
+        const float wt = ex2(mls[j].x - M) * mls[j].y;
+        den += wt;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float f[8];
+          bf16x8_to_f32(x[j][half], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[8 * half + e] += wt * f[e];
+        }
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const float* a = acc + 8 * half;
+    *(uint4*)(p.o_lat + (size_t)rg * kLat + 256 * half + 8 * lane) =
+        make_uint4(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv),
+                   pack_bf16(a[4] * inv, a[5] * inv), pack_bf16(a[6] * inv, a[7] * inv));
   }
 }
 
@@ -1001,12 +1064,13 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     if (e != cudaSuccess) return e;
   }
   {
-    MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits};
+    MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits, p.B * R};
     KernelTimer kt("merge_sm103", a.stream);
     if (p.splits >= 16)
       e = launch_pdl(merge_sm103<1>, dim3(p.B * R, 2), dim3(128), 0, a.stream, mp);
     else
-      e = launch_pdl(merge_sm103<2>, dim3(p.B * R, 1), dim3(128), 0, a.stream, mp);
+      e = launch_pdl(merge_rows_sm103, dim3((p.B * R + MR_ROWS - 1) / MR_ROWS), dim3(32 * MR_ROWS),
+                     0, a.stream, mp);
     if (e != cudaSuccess) return e;
   }
   {
