@@ -21,7 +21,8 @@
 //                  computes its partial scores over its columns, swaps them
 //                  with the peer through distributed shared memory, and both
 //                  accumulate their half of o_lat (128 x 256 fp32 in TMEM).
-//  merge_sm103     log-sum-exp merge of the split-KV pieces into bf16 o_lat.
+//  merge_sm103     log-sum-exp merge of the split-KV pieces into bf16 o_lat
+//                  (merge_rows_sm103 when a row has few pieces).
 //
 // The four launches are chained with programmatic dependent launch: each one
 // starts the loads that do not depend on its predecessor (weights, the KV
@@ -771,8 +772,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
 // 4th piece, each lane CPL groups of 8 columns, with its own running maximum
 // (raised, and the sums rescaled, when a piece's maximum is larger), so there
 // is no separate max pass and the loads of many pieces are in flight at once;
-// the four warps' sums are combined in shared memory.  CPL = 1 when pieces are
-// many (more CTAs, fewer loads each), 2 when they are few.
+// the four warps' sums are combined in shared memory.  The launcher uses this
+// form (CPL = 1: more CTAs, fewer loads each) for rows of 16 pieces or more;
+// rows with fewer go to merge_rows_sm103 below, one warp per row.
 struct MergeParams {
   const __nv_bfloat16* o_part;  // [B, splits, R, 512]
   const float* ml;              // [B, splits, R, 2]
