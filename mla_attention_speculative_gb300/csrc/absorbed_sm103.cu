@@ -1068,8 +1068,10 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   {
     MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits, p.B * R};
     KernelTimer kt("merge_sm103", a.stream);
-    if (p.splits >= 16)
+    if (p.splits >= 32)
       e = launch_pdl(merge_sm103<1>, dim3(p.B * R, 2), dim3(128), 0, a.stream, mp);
+    else if (p.splits >= 16)
+      e = launch_pdl(merge_sm103<2>, dim3(p.B * R, 1), dim3(128), 0, a.stream, mp);
     else
       e = launch_pdl(merge_rows_sm103, dim3((p.B * R + MR_ROWS - 1) / MR_ROWS), dim3(32 * MR_ROWS),
                      0, a.stream, mp);
