@@ -772,9 +772,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
 // 4th piece, each lane CPL groups of 8 columns, with its own running maximum
 // (raised, and the sums rescaled, when a piece's maximum is larger), so there
 // is no separate max pass and the loads of many pieces are in flight at once;
-// the four warps' sums are combined in shared memory.  The launcher uses this
-// form (CPL = 1: more CTAs, fewer loads each) for rows of 16 pieces or more;
-// rows with fewer go to merge_rows_sm103 below, one warp per row.
+// the four warps' sums are combined in shared memory.  The launcher uses
+// CPL = 1 (two CTAs per row: more CTAs, fewer loads each) for rows of 32
+// pieces or more, CPL = 2 (one CTA per row) for 16 to 31, and sends rows with
+// fewer to merge_rows_sm103 below, one warp per row.
 struct MergeParams {
   const __nv_bfloat16* o_part;  // [B, splits, R, 512]
   const float* ml;              // [B, splits, R, 2]
