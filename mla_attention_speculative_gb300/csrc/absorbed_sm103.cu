@@ -794,11 +794,11 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   }
 }
 
-template <int CPL>
-__global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
-  constexpr int NBATCH = 16 / CPL;  // pieces whose loads are in flight together
-  __shared__ float part[4][CPL * 8][32];
-  __shared__ float mden[4][2];
+template <int CPL, int W>  // W warps take every W-th piece
+__global__ void __launch_bounds__(32 * W) merge_sm103(MergeParams p) {
+  constexpr int NBATCH = 64 / (CPL * W);  // pieces whose loads are in flight together
+  __shared__ float part[W][CPL * 8][32];
+  __shared__ float mden[W][2];
   // the unembedding may start loading its weights now; it waits for this grid
   // before reading o_lat
   pdl_launch_dependents();
@@ -818,12 +818,12 @@ __global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
   for (int c = 0; c < CPL; ++c)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[c][e] = 0.f;
-  for (int s0 = w; s0 < nsplit; s0 += 4 * NBATCH) {
+  for (int s0 = w; s0 < nsplit; s0 += W * NBATCH) {
     float2 mls[NBATCH];
     uint4 x[NBATCH][CPL];
 #pragma unroll
     for (int k = 0; k < NBATCH; ++k) {
-      const int s = s0 + 4 * k;
+      const int s = s0 + W * k;
       const size_t e = base + (size_t)min(s, nsplit - 1) * stride;
       mls[k] = *(const float2*)(p.ml + e * 2);
       const __nv_bfloat16* o = p.o_part + e * kLat + col0 + 8 * lane;
@@ -865,10 +865,12 @@ __global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
   }
   __syncthreads();
   if (w == 0) {
-    const float Mall = fmaxf(fmaxf(mden[0][0], mden[1][0]), fmaxf(mden[2][0], mden[3][0]));
-    float f[4], dsum = 0.f;
+    float Mall = mden[0][0];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 1; g < W; ++g) Mall = fmaxf(Mall, mden[g][0]);
+    float f[W], dsum = 0.f;
+#pragma unroll
+    for (int g = 0; g < W; ++g) {
       f[g] = mden[g][1] > 0.f ? ex2(mden[g][0] - Mall) : 0.f;
       dsum += f[g] * mden[g][1];
     }
@@ -877,9 +879,12 @@ __global__ void __launch_bounds__(128) merge_sm103(MergeParams p) {
     for (int c = 0; c < CPL; ++c) {
       float y[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        y[e] = (f[0] * part[0][8 * c + e][lane] + f[1] * part[1][8 * c + e][lane] +
-                f[2] * part[2][8 * c + e][lane] + f[3] * part[3][8 * c + e][lane]) * inv;
+      for (int e = 0; e < 8; ++e) {
+        float a = 0.f;
+#pragma unroll
+        for (int g = 0; g < W; ++g) a += f[g] * part[g][8 * c + e][lane];
+        y[e] = a * inv;
+      }
       *(uint4*)(p.o_lat + (size_t)rg * kLat + col0 + 256 * c + 8 * lane) =
           make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
                      pack_bf16(y[6], y[7]));
@@ -1069,10 +1074,12 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   {
     MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits, p.B * R};
     KernelTimer kt("merge_sm103", a.stream);
-    if (p.splits >= 32)
-      e = launch_pdl(merge_sm103<1>, dim3(p.B * R, 2), dim3(128), 0, a.stream, mp);
+    if (p.splits >= 48)
+      e = launch_pdl(merge_sm103<1, 8>, dim3(p.B * R, 2), dim3(256), 0, a.stream, mp);
+    else if (p.splits >= 32)
+      e = launch_pdl(merge_sm103<1, 4>, dim3(p.B * R, 2), dim3(128), 0, a.stream, mp);
     else if (p.splits >= 16)
-      e = launch_pdl(merge_sm103<2>, dim3(p.B * R, 1), dim3(128), 0, a.stream, mp);
+      e = launch_pdl(merge_sm103<2, 4>, dim3(p.B * R, 1), dim3(128), 0, a.stream, mp);
     else
       e = launch_pdl(merge_rows_sm103, dim3((p.B * R + MR_ROWS - 1) / MR_ROWS), dim3(32 * MR_ROWS),
                      0, a.stream, mp);
