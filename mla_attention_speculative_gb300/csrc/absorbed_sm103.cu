@@ -769,13 +769,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
 // =========================================================================
 // o_lat[row] = sum_s w_s (O_s / l_s)[row] / sum_s w_s with w_s = 2^(m_s - M) l_s
 // (bf16 out).  One CTA per (query row, 256*CPL-column slice): warp w takes every
-// 4th piece, each lane CPL groups of 8 columns, with its own running maximum
+// W-th piece, each lane CPL groups of 8 columns, with its own running maximum
 // (raised, and the sums rescaled, when a piece's maximum is larger), so there
 // is no separate max pass and the loads of many pieces are in flight at once;
-// the four warps' sums are combined in shared memory.  The launcher uses
-// CPL = 1 (two CTAs per row: more CTAs, fewer loads each) for rows of 32
-// pieces or more, CPL = 2 (one CTA per row) for 16 to 31, and sends rows with
-// fewer to merge_rows_sm103 below, one warp per row.
+// the W warps' sums are combined in shared memory.  The launcher uses CPL = 1
+// (two CTAs per row: more CTAs, fewer loads each) with eight warps for rows of
+// 48 pieces or more and four for 32 to 47, CPL = 2 (one CTA per row) for 16 to
+// 31, and sends rows with fewer to merge_rows_sm103 below, one warp per row.
 struct MergeParams {
   const __nv_bfloat16* o_part;  // [B, splits, R, 512]
   const float* ml;              // [B, splits, R, 2]
