@@ -717,17 +717,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // This CTA's half of O / l (128 rows x 256 columns, bf16) goes through the
     // drained KV stages as four 128-byte-swizzled boxes of 64 columns, then
     // out with TMA stores (rows past R are clipped).
-    for (int c = 0; c < OPT; c += 16) {
-      uint32_t v[16];
+    // (64 columns per round: four TMEM loads in flight, one wait)
+    for (int c = 0; c < OPT; c += 64) {
+      uint32_t v[64];
       if (ntiles > 0) {
-        tmem_ld16(tmem + lane_base + TM_O + OPT * wg + c, v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tmem_ld16(tmem + lane_base + TM_O + OPT * wg + c + 16 * k,
+                    *(uint32_t(*)[16])(v + 16 * k));
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = 0u;
+        for (int e = 0; e < 64; ++e) v[e] = 0u;
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const int col = OPT * wg + c + 8 * u;
         const uint32_t addr = sKV + (col >> 6) * (BM * 128) + q * 128 +
                               ((((col & 63) >> 3) ^ (q & 7)) << 4);
