@@ -159,17 +159,23 @@ mla_status_t mla_verify_attention(
  *
  * Arguments are those of mla_verify_attention without mode, workspace and
  * workspace_bytes; the absorbed branch always runs.  Scratch comes from one
- * 32 MiB static device array inside the library, which every GPU that loads
- * the library keeps reserved until the process exits.  A call whose scratch
+ * 32 MiB static device array inside the library.  A call whose scratch
  * (mla_workspace_bytes with MLA_MODE_ABSORBED) exceeds 32 MiB returns
  * MLA_ERR_WORKSPACE before launching anything.  It never calls cudaMalloc,
  * cudaFree or an allocating library routine.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture starts.  All calls share the array and it keeps
- * the previous call's contents (nothing in it needs to start at zero): calls
- * that overlap on the GPU race on it, so issue them one at a time. */
+ * The array lives in its own CUDA module, which CUDA loads lazily: the FIRST
+ * call of this entry point on a device loads it and so reserves the 32 MiB on
+ * that device (kept until the process exits).  Make that first call as a
+ * warm-up, before a host memory pool claims the device (otherwise the load
+ * fails and the call returns MLA_ERR_WORKSPACE with a message saying so) and
+ * before any stream capture starts.  Every call looks up the array's address
+ * in the current context (cudaGetSymbolAddress); `stream` must belong to the
+ * current device (else MLA_ERR_INVALID_ARG).
+ *
+ * All calls share the one array and it keeps the previous call's contents
+ * (nothing in it needs to start at zero): calls that overlap on the GPU
+ * (concurrent streams or threads) race on it, so issue them one at a time. */
 mla_status_t mla_verify_attention_noalloc(
     const mla_geometry_t* geom,
     const void* q_nope, const void* q_rope,
@@ -181,6 +187,19 @@ mla_status_t mla_verify_attention_noalloc(
     const int32_t* page_table, int32_t page_size, int32_t max_pages_per_seq,
     int32_t num_pages,
     void* out, void* stream, int32_t* branch_taken);
+
+/* Host-side check of a page table before it is used: for every sequence b, the table must hold
+ * ceil(cache_lens_host[b] / page_size) <= max_pages_per_seq pages, and every
+ * entry j < ceil(T_b / page_size) of row b of page_table_host ([batch,
+ * max_pages_per_seq], host memory, row-major) must lie in [0, num_pages).
+ * Entries past a sequence's last page are not read.  Returns MLA_OK, or
+ * MLA_ERR_INVALID_ARG with the first offending entry in mla_last_error().
+ * Pure host code, no CUDA.  The kernels guard the same range on the device:
+ * an out-of-range id met there forms no address, its positions read as
+ * zeros, and mla_device_status reports it (code 300). */
+mla_status_t mla_check_page_table(const int32_t* page_table_host, int32_t batch,
+                                  int32_t max_pages_per_seq, const int32_t* cache_lens_host,
+                                  int32_t page_size, int32_t num_pages);
 
 /* Per-kernel timing, for benchmarks.  While enabled, every kernel launch the
  * library makes is bracketed by a pair of CUDA events recorded on the call's
@@ -200,11 +219,18 @@ mla_status_t mla_kernel_timing_read(char* names, size_t names_len, int32_t* laun
                                     int32_t* n_kernels, int32_t reset);
 
 /* Waits for the device to go idle, then reads the kernels' status word:
- * MLA_OK when no bounded wait inside a kernel ran out since the last clear,
- * MLA_ERR_TIMEOUT otherwise (*code receives the site that gave up, 0 when
- * none).  The kernels never hang on a missing signal: each wait gives up
- * after about a second, records its site here and lets the kernel finish
- * (its outputs are then undefined).  clear != 0 resets the word. */
+ * MLA_OK when nothing was recorded since the last clear; MLA_ERR_TIMEOUT
+ * when a bounded wait inside a kernel ran out (*code receives the site that
+ * gave up, 1..299); MLA_ERR_INVALID_ARG when a kernel met a page id outside
+ * [0, num_pages) (*code = 300; that page's positions were read as zeros).
+ * The kernels never hang on a missing signal: each wait gives up after about
+ * a second, records its site here and lets the kernel finish (its outputs are
+ * then undefined).  clear != 0 resets the word.
+ *
+ * With MLA_DEBUG_CHECKS=1 in the environment, mla_verify_attention also
+ * synchronises the stream, copies cache_lens_dev (and the page table) to the
+ * host and checks them against cache_lens_host and [0, num_pages) before it
+ * launches anything (not while a stream is being captured). */
 mla_status_t mla_device_status(int32_t* code, int32_t clear);
 
 /* Failure-path self-test: launches one CTA on `stream` (cudaStream_t, NULL =

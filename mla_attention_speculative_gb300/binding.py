@@ -61,6 +61,7 @@ _SIGS = {
     "mla_verify_attention_noalloc": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P,
                                             _P, _P, _I32, _I32, _P, _I32, _I32, _I32, _P,
                                             _P, _P]),
+    "mla_check_page_table": (_I32, [_P, _I32, _I32, _P, _I32, _I32]),
     "mla_kernel_timing_enable": (_I32, [_I32]),
     "mla_kernel_timing_read": (_I32, [ctypes.c_char_p, ctypes.c_size_t, _P, _P, _I32, _P,
                                       _I32]),
@@ -161,6 +162,18 @@ def mla_workspace_bytes(geom: Geometry, L: int, cache_lens: Sequence[int], mode=
     return out.value
 
 
+def mla_check_page_table(page_table, cache_lens: Sequence[int], page_size: int,
+                         num_pages: int) -> None:
+    """Host-side range check of a page table (any int array-like [B, max_pages]);
+    raises MlaError (MLA_ERR_INVALID_ARG) naming the first bad entry."""
+    t = torch.as_tensor(page_table, dtype=torch.int32).cpu().contiguous()
+    if t.dim() != 2:
+        raise ValueError("page_table must be [batch, max_pages]")
+    lens = _lens_array(cache_lens)
+    _check(lib().mla_check_page_table(t.data_ptr(), t.shape[0], t.shape[1], lens, int(page_size),
+                                      int(num_pages)), "mla_check_page_table")
+
+
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
@@ -202,10 +215,12 @@ def cache_strides(c_kv: torch.Tensor, k_rope: torch.Tensor, paged: bool):
 
 
 def _verify_args(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, mode, out, workspace,
-                 page_table, cache_lens_dev, scale):
+                 page_table, cache_lens_dev, scale, noalloc=False):
     """Checks, defaults and the C arguments of mla_verify_attention up to (not
     including) the stream and the branch pointer.  Returns (args, out, dev,
-    keep), keep holding every tensor the arguments point into."""
+    keep), keep holding every tensor the arguments point into.  With
+    ``noalloc`` the arguments are those of mla_verify_attention_noalloc (no
+    mode, no workspace)."""
     B, L, H, n = q_nope.shape
     rope = q_rope.shape[-1]
     r = W_UK.shape[-1]
@@ -221,17 +236,20 @@ def _verify_args(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, mode, out
         cache_lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
     if out is None:
         out = torch.empty((B, L, H, v), dtype=q_nope.dtype, device=dev)
-    m = MODES.get(mode, mode)
-    if workspace is None:  # (a given workspace that is too small is rejected by the call)
-        need = mla_workspace_bytes(geom, L, lens, m)
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     page_size = c_kv.shape[1] if paged else 0
     max_pages = page_table.shape[1] if paged else 0
     num_pages = c_kv.shape[0] if paged else 0
     args = [ctypes.byref(geom), _ptr(q_nope), _ptr(q_rope), _ptr(c_kv), _ptr(k_rope), cs, ks, seq,
             _ptr(W_UK), _ptr(W_UV), _ptr(cache_lens_dev), arr, B, L, _ptr(page_table), page_size,
-            max_pages, num_pages, m, _ptr(out), _ptr(workspace),
-            workspace.numel() * workspace.element_size()]
+            max_pages, num_pages]
+    if noalloc:
+        args += [_ptr(out)]
+    else:
+        m = MODES.get(mode, mode)
+        if workspace is None:  # (a given workspace that is too small is rejected by the call)
+            need = mla_workspace_bytes(geom, L, lens, m)
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        args += [m, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size()]
     keep = (q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, page_table, cache_lens_dev, out, workspace)
     return args, out, dev, keep
 
@@ -326,30 +344,13 @@ def mla_verify_attention_noalloc(q_nope: torch.Tensor, q_rope: torch.Tensor,
                                  scale: Optional[float] = None, stream=None):
     """Absorbed-branch verify call that uses the library's static scratch
     instead of a workspace (for callers that cannot allocate device memory).
-    Same tensors as :func:`mla_verify_attention`; returns (out, branch)."""
-    B, L, H, n = q_nope.shape
-    rope = q_rope.shape[-1]
-    r = W_UK.shape[-1]
-    v = W_UV.shape[-1]
-    dev = q_nope.device
-    geom = _geometry(H, r, n, v, rope, q_nope.dtype, scale)
-    lens = [int(t) for t in cache_lens]
-    arr = _lens_array(lens)
-    paged = page_table is not None
-    cs, ks, seq = cache_strides(c_kv, k_rope, paged)
-    if cache_lens_dev is None:
-        cache_lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
-    if out is None:
-        out = torch.empty((B, L, H, v), dtype=q_nope.dtype, device=dev)
+    Same tensors and checks as :func:`mla_verify_attention`; returns (out, branch)."""
+    args, out, dev, _ = _verify_args(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens,
+                                     None, out, None, page_table, cache_lens_dev, scale,
+                                     noalloc=True)
     if stream is None:
         stream = _current_stream(dev)
-    page_size = c_kv.shape[1] if paged else 0
-    max_pages = page_table.shape[1] if paged else 0
-    num_pages = c_kv.shape[0] if paged else 0
     branch = ctypes.c_int32(0)
-    st = lib().mla_verify_attention_noalloc(
-        ctypes.byref(geom), _ptr(q_nope), _ptr(q_rope), _ptr(c_kv), _ptr(k_rope), cs, ks, seq,
-        _ptr(W_UK), _ptr(W_UV), _ptr(cache_lens_dev), arr, B, L, _ptr(page_table), page_size,
-        max_pages, num_pages, _ptr(out), stream, ctypes.byref(branch))
+    st = lib().mla_verify_attention_noalloc(*args, stream, ctypes.byref(branch))
     _check(st, "mla_verify_attention_noalloc")
     return out, branch.value

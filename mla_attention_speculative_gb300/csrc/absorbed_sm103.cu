@@ -37,6 +37,7 @@
 
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 #include <utility>
 
 #include "mla_internal.h"
@@ -230,7 +231,7 @@ struct AttnParams {
   const int32_t* lens;
   const int32_t* page_table;
   const __nv_bfloat16* q_lat;  // Q tiles [B, rtiles, 64 chunks, 128 rows, 8] bf16
-  int page_size, max_pages;
+  int page_size, max_pages, num_pages;
   long long seq_stride;
   int L, H, R;        // R = L*H query rows per sequence
   int rtiles;         // ceil(R / 128)
@@ -376,10 +377,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       auto load_kv = [&](int i) {
         const int s = i % STAGES;
         const int t0 = kv0 + i * BN;
-        const long long y =
-            p.page_table ? (long long)p.page_table[(long long)b * p.max_pages + t0 / p.page_size] *
-                                   p.page_size + (t0 % p.page_size)
-                         : (long long)b * p.seq_stride + t0;
+        long long y;
+        if (p.page_table) {
+          const int page = p.page_table[(long long)b * p.max_pages + t0 / p.page_size];
+          // an id outside [0, num_pages) forms no address: the box is read
+          // from wholly negative rows, which TMA fills with zeros
+          if (page < 0 || page >= p.num_pages) {
+            report_timeout(kBadPageSite);
+            y = -2 * BN;
+          } else {
+            y = (long long)page * p.page_size + (t0 % p.page_size);
+          }
+        } else {
+          y = (long long)b * p.seq_stride + t0;
+        }
         const uint32_t st = sKV + s * KV_STAGE;
         mbar_arrive_expect_tx(bar(B_KVFULL + s), KV_STAGE);
         for (int c = 0; c < 4; ++c)
@@ -1028,9 +1039,12 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
                                (uint64_t)R * kLat * 2, 64, BM);
   if (!ok) return cudaErrorInvalidValue;
 
+  // shared-memory opt-in, once per device (calls may come from several threads)
+  static std::mutex attrs_mu;
   static bool attrs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> attrs_lock(attrs_mu);
   if (dev >= 0 && dev < 64 && !attrs[dev]) {
     cudaError_t e = cudaFuncSetAttribute(swapab_gemm_sm103,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1057,6 +1071,7 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.B = p.B;
     ap.page_size = c.page_size;
     ap.max_pages = c.max_pages;
+    ap.num_pages = c.num_pages;
     ap.seq_stride = c.seq_stride;
     ap.L = p.L;
     ap.H = p.H;

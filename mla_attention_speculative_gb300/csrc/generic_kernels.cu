@@ -20,7 +20,12 @@
 #include "mla_internal.h"
 
 namespace mla {
+
+static __device__ int g_generic_status;
+
 namespace {
+
+__device__ __forceinline__ void report_bad_page() { atomicCAS(&g_generic_status, 0, kBadPageSite); }
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -117,6 +122,10 @@ __global__ void __launch_bounds__(128) attn_rows_kernel(AttnParams p) {
   const T* krp = (const T*)p.cache.k_rope;
   for (int t = t0; t < t1; ++t) {
     const int64_t crow = cache_row(p.cache, b, t);
+    if (crow < 0) {  // page id out of range: the position is left out
+      if (lane == 0) report_bad_page();
+      continue;
+    }
     const T* kmain;
     const T* vrow;
     if (ABSORBED) {
@@ -285,7 +294,11 @@ __global__ void __launch_bounds__(256) expand_kernel(CacheView cache, const T* _
       const int mm = idx / BK, kk = idx - mm * BK;
       const int t = t0 + mm;
       float x = 0.f;
-      if (t < Tb && k0 + kk < r) x = to_f(ckv[cache_row(cache, b, t) * cache.ckv_stride + k0 + kk]);
+      if (t < Tb && k0 + kk < r) {
+        const int64_t crow = cache_row(cache, b, t);
+        if (crow >= 0) x = to_f(ckv[crow * cache.ckv_stride + k0 + kk]);
+        else if (kk == 0) report_bad_page();
+      }
       sa[kk][mm] = x;
     }
     for (int idx = threadIdx.x; idx < BK * BN; idx += 256) {
@@ -409,6 +422,16 @@ cudaError_t launch_generic_absorbed(const Plan& p, const Args& a) {
 cudaError_t launch_generic_materialised(const Plan& p, const Args& a) {
   return p.dtype == MLA_DTYPE_FP32 ? run_materialised<float>(p, a)
                                    : run_materialised<__nv_bfloat16>(p, a);
+}
+
+int generic_device_status(bool clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_generic_status, sizeof(int)) != cudaSuccess) return -1;
+  if (clear && v != 0) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_generic_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
 }
 
 }  // namespace mla

@@ -31,6 +31,7 @@
 
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 #include <utility>
 
 #include "mla_internal.h"
@@ -65,13 +66,18 @@ __device__ __forceinline__ void wait_or_fail(bool& ok, uint32_t bar, uint32_t pa
   }
 }
 
-// Row of cached position t of sequence b in the 2-D cache tensors.
+// Row of cached position t of sequence b in the 2-D cache tensors.  A page id
+// outside [0, num_pages) forms no address: it is reported and the row becomes
+// a wholly negative one, whose boxes TMA fills with zeros.
 __device__ __forceinline__ int cache_y(const int32_t* page_table, int page_size, int max_pages,
-                                       long long seq_stride, int b, int t) {
-  return page_table ? (int)((long long)page_table[(long long)b * max_pages + t / page_size] *
-                                page_size +
-                            (t % page_size))
-                    : (int)((long long)b * seq_stride + t);
+                                       int num_pages, long long seq_stride, int b, int t) {
+  if (page_table == nullptr) return (int)((long long)b * seq_stride + t);
+  const int page = page_table[(long long)b * max_pages + t / page_size];
+  if (page < 0 || page >= num_pages) {
+    report_timeout(kBadPageSite);
+    return -256;
+  }
+  return (int)((long long)page * page_size + (t % page_size));
 }
 
 // =========================================================================
@@ -80,7 +86,7 @@ __device__ __forceinline__ int cache_y(const int32_t* page_table, int page_size,
 struct ExpandParams {
   const int32_t* lens;
   const int32_t* page_table;
-  int page_size, max_pages;
+  int page_size, max_pages, num_pages;
   long long seq_stride;
   int H, n, v, stages;
   uint32_t tmem_cols, v_col;  // TMEM allocation; V accumulator's first column
@@ -144,9 +150,9 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
     // in one page (page sizes are multiples of 64).  Rows at or past T are
     // loaded but never read back.
     bool ok = true;
-    const int y0 = cache_y(p.page_table, p.page_size, p.max_pages, p.seq_stride, b, t0);
+    const int y0 = cache_y(p.page_table, p.page_size, p.max_pages, p.num_pages, p.seq_stride, b, t0);
     const int y1 = t0 + 64 < T
-                       ? cache_y(p.page_table, p.page_size, p.max_pages, p.seq_stride, b, t0 + 64)
+                       ? cache_y(p.page_table, p.page_size, p.max_pages, p.num_pages, p.seq_stride, b, t0 + 64)
                        : y0 + 64;
     int issued = 0;
     for (int kc = 0; kc < kChunks; ++kc) {
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(128, 1) expand_sm103(const __grid_constant__ C
 struct MatAttnParams {
   const int32_t* lens;
   const int32_t* page_table;
-  int page_size, max_pages;
+  int page_size, max_pages, num_pages;
   long long seq_stride;
   __nv_bfloat16* out;  // [B, L, H, v]
   int L, H, n, v;
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
         if (i >= KS) wait_or_fail(ok, k_empty(s), ((i / KS) - 1) & 1, 50);
         if (!ok) break;
         const int t0 = i * MA_BN;
-        const int y = cache_y(p.page_table, p.page_size, p.max_pages, p.seq_stride, b, t0);
+        const int y = cache_y(p.page_table, p.page_size, p.max_pages, p.num_pages, p.seq_stride, b, t0);
         const uint32_t st = sK + s * KB;
         mbar_arrive_expect_tx(k_full(s), KB);
         for (int c = 0; c < n / 64; ++c)
@@ -686,9 +692,12 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
   const ExpandShape es = expand_shape(p.n, p.v);
   const MatRings mr = mat_rings(p.n, p.v);
   const int ma_smem = mr.smem;
+  // shared-memory opt-in, once per device (calls may come from several threads)
+  static std::mutex attrs_mu;
   static bool attrs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> attrs_lock(attrs_mu);
   if (dev >= 0 && dev < 64 && !attrs[dev]) {
     cudaError_t e = cudaFuncSetAttribute(expand_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemPerBlock);
@@ -702,7 +711,7 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
   }
   cudaError_t e;
   {
-    ExpandParams ep{a.lens, c.page_table, c.page_size, c.max_pages, c.seq_stride,
+    ExpandParams ep{a.lens, c.page_table, c.page_size, c.max_pages, c.num_pages, c.seq_stride,
                     p.H,    p.n,          p.v,         es.stages,   es.tmem_cols,
                     es.v_col, es.split};
     KernelTimer kt("expand_sm103", a.stream);
@@ -712,7 +721,7 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
     if (e != cudaSuccess) return e;
   }
   {
-    MatAttnParams mp{a.lens, c.page_table, c.page_size, c.max_pages, c.seq_stride,
+    MatAttnParams mp{a.lens, c.page_table, c.page_size, c.max_pages, c.num_pages, c.seq_stride,
                      (__nv_bfloat16*)a.out, p.L, p.H, p.n, p.v, mr.ks, mr.vs,
                      p.scale * 1.4426950408889634f};
     KernelTimer kt("mat_attn_sm103", a.stream);

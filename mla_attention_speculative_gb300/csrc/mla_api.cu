@@ -9,7 +9,9 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "mla_internal.h"
@@ -122,8 +124,29 @@ static bool lens_ok(const int32_t* lens, int32_t batch, int32_t L) {
   return true;
 }
 
-static constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs
 static constexpr int kGenericRowsPerCTA = 4; // one warp per query row
+
+int device_sm_count() {
+  constexpr int kDefault = 152;  // GB300: 2 dies x 76 SMs
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int cached[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return kDefault;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < kMaxDevices && cached[dev] > 0) return cached[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0) {
+    cudaGetLastError();
+    sms = kDefault;
+  }
+  if (dev < kMaxDevices) cached[dev] = sms;
+  return sms;
+}
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -165,12 +188,13 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
   // the GPU a few times over, pieces a multiple of 64 rows.
   const int64_t rows = (int64_t)L * p->H;
   const size_t eb = p->dtype == MLA_DTYPE_BF16 ? 2 : 4;
+  const int64_t num_sms = device_sm_count();
   const size_t nrow = (size_t)batch * rows;
   {
     SplitPlan& g = p->generic;
     const int64_t row_ctas =
         (int64_t)batch * ((rows + kGenericRowsPerCTA - 1) / kGenericRowsPerCTA);
-    const int64_t want = 4 * kNumSMs;
+    const int64_t want = 4 * num_sms;
     int64_t splits = (want + row_ctas - 1) / row_ctas;
     const int64_t max_splits = (p->Tmax + 63) / 64;
     if (splits > max_splits) splits = max_splits;
@@ -214,7 +238,7 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     constexpr int64_t kClusterOverhead = 4;
     SplitPlan& f = p->fast;
     const int64_t row_tiles = (rows + 127) / 128;
-    const int64_t slots = kNumSMs / 2;
+    const int64_t slots = num_sms / 2;
     const int64_t max_tiles = (p->Tmax + 63) / 64;
     int64_t best_ct = max_tiles, best_cost = -1;
     for (int64_t ct = max_tiles; ct >= 1; --ct) {
@@ -246,7 +270,89 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Every page a position t < T_b needs is in [0, num_pages), and the table is
+// wide enough for the longest sequence.
+static mla_status_t check_page_table(const int32_t* table, int32_t batch, int32_t max_pages,
+                                     const int32_t* lens, int32_t page_size, int32_t num_pages) {
+  if (table == nullptr || lens == nullptr || batch < 1 || max_pages < 1 || page_size < 1 ||
+      num_pages < 1) {
+    set_error("page table check needs a table, lengths, batch, max_pages, page_size and "
+              "num_pages >= 1");
+    return MLA_ERR_INVALID_ARG;
+  }
+  for (int32_t b = 0; b < batch; ++b) {
+    if (lens[b] < 0) {
+      set_error("cache_lens[%d] = %d is negative", b, lens[b]);
+      return MLA_ERR_INVALID_ARG;
+    }
+    const int64_t need = ((int64_t)lens[b] + page_size - 1) / page_size;
+    if (need > max_pages) {
+      set_error("sequence %d needs %lld pages but the table holds %d per sequence", b,
+                (long long)need, max_pages);
+      return MLA_ERR_INVALID_ARG;
+    }
+    for (int64_t j = 0; j < need; ++j) {
+      const int32_t id = table[(int64_t)b * max_pages + j];
+      if (id < 0 || id >= num_pages) {
+        set_error("page_table[%d][%lld] = %d is outside [0, %d)", b, (long long)j, id,
+                  num_pages);
+        return MLA_ERR_INVALID_ARG;
+      }
+    }
+  }
+  return MLA_OK;
+}
+
+// MLA_DEBUG_CHECKS=1 in the environment: each call copies the device cache
+// lengths (and page table) back to the host and checks them before launching.
+static bool debug_checks() {
+  static const bool on = [] {
+    const char* e = std::getenv("MLA_DEBUG_CHECKS");
+    return e != nullptr && e[0] != '\0' && e[0] != '0';
+  }();
+  return on;
+}
+
+static mla_status_t debug_check_device_args(const int32_t* lens_dev, const int32_t* lens_host,
+                                            int32_t batch, const int32_t* page_table,
+                                            int32_t max_pages, int32_t page_size,
+                                            int32_t num_pages, cudaStream_t stream) {
+  std::vector<int32_t> lens(batch);
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(lens.data(), lens_dev, sizeof(int32_t) * batch, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    set_error("debug check could not read cache_lens_dev: %s", cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  for (int32_t b = 0; b < batch; ++b) {
+    if (lens[b] != lens_host[b]) {
+      set_error("cache_lens_dev[%d] = %d but cache_lens_host[%d] = %d", b, lens[b], b,
+                lens_host[b]);
+      return MLA_ERR_INVALID_ARG;
+    }
+  }
+  if (page_table == nullptr) return MLA_OK;
+  std::vector<int32_t> table((size_t)batch * max_pages);
+  e = cudaMemcpy(table.data(), page_table, sizeof(int32_t) * table.size(),
+                 cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    set_error("debug check could not read page_table: %s", cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  return check_page_table(table.data(), batch, max_pages, lens_host, page_size, num_pages);
+}
+
 }  // namespace mla
+
+extern "C" mla_status_t mla_check_page_table(const int32_t* page_table_host, int32_t batch,
+                                             int32_t max_pages_per_seq,
+                                             const int32_t* cache_lens_host, int32_t page_size,
+                                             int32_t num_pages) {
+  return check_page_table(page_table_host, batch, max_pages_per_seq, cache_lens_host, page_size,
+                          num_pages);
+}
+
 
 extern "C" mla_status_t mla_select_branch(const mla_geometry_t* g, int32_t L,
                                           const int32_t* lens, int32_t batch, int32_t mode,
@@ -327,6 +433,12 @@ extern "C" mla_status_t mla_verify_attention(
     return MLA_ERR_INVALID_ARG;
   }
 
+  if (debug_checks()) {
+    st = debug_check_device_args(lens_dev, lens_host, batch, page_table, max_pages_per_seq,
+                                 page_size, num_pages, (cudaStream_t)stream);
+    if (st != MLA_OK) return st;
+  }
+
   Args a;
   a.q_nope = q_nope;
   a.q_rope = q_rope;
@@ -384,14 +496,26 @@ extern "C" const char* mla_status_string(int32_t s) {
 extern "C" const char* mla_last_error(void) { return g_err; }
 
 extern "C" mla_status_t mla_device_status(int32_t* code, int32_t clear) {
-  const int va = absorbed_device_status(clear != 0);
-  const int vm = materialised_device_status(clear != 0);
-  const int vs = selftest_device_status(clear != 0);
-  const int v = va < 0 || vm < 0 || vs < 0 ? -1 : va != 0 ? va : vm != 0 ? vm : vs;
+  const int words[4] = {absorbed_device_status(clear != 0), materialised_device_status(clear != 0),
+                        generic_device_status(clear != 0), selftest_device_status(clear != 0)};
+  int v = 0;
+  for (int w : words) {
+    if (w < 0) {
+      v = -1;
+      break;
+    }
+    if (v == 0) v = w;
+  }
   if (code) *code = v;
   if (v < 0) {
     set_error("could not read the device status word");
     return MLA_ERR_CUDA;
+  }
+  if (v >= kBadPageSite) {
+    set_error("a kernel met a page id outside [0, num_pages) (site %d); the positions of that "
+              "page read as zeros",
+              v);
+    return MLA_ERR_INVALID_ARG;
   }
   if (v != 0) {
     set_error("a bounded device wait ran out (site %d)", v);

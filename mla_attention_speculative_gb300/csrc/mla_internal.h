@@ -65,10 +65,17 @@ struct CacheView {
   int32_t num_pages;
 };
 
-// Global row index of cached position t of sequence b.
+// Status-word code a kernel records when a page-table entry it needs lies
+// outside [0, num_pages): no address is formed from it, and the positions of
+// that page read as zeros.  Codes below it are bounded waits that ran out.
+constexpr int kBadPageSite = 300;
+
+// Global row index of cached position t of sequence b, or -1 when the page
+// id that holds it is outside [0, num_pages) (nothing may be read then).
 __host__ __device__ inline int64_t cache_row(const CacheView& c, int b, int t) {
   if (c.page_table == nullptr) return (int64_t)b * c.seq_stride + t;
   const int32_t page = c.page_table[(int64_t)b * c.max_pages + t / c.page_size];
+  if (page < 0 || page >= c.num_pages) return -1;
   return (int64_t)page * c.page_size + (t % c.page_size);
 }
 
@@ -87,6 +94,12 @@ struct Args {
 // Generic kernels: CUDA-core arithmetic for any geometry, fp32 or bf16.
 cudaError_t launch_generic_absorbed(const Plan& p, const Args& a);
 cudaError_t launch_generic_materialised(const Plan& p, const Args& a);
+// Status word of the generic kernels (kBadPageSite or 0); synchronises.
+int generic_device_status(bool clear);
+
+// Streaming multiprocessors of the current device (152 on GB300; 152 also
+// when no device can be queried, so host-only planning stays defined).
+int device_sm_count();
 
 // Tensor-core kernels for the absorbed branch (bf16, r = 512, rope = 64,
 // n a multiple of 64 up to 256, v a multiple of 128 up to 512).

@@ -7,22 +7,28 @@
 // latency-critical loops where a cudaMalloc (which can synchronise the whole
 // device) is not acceptable.  This entry point runs the same absorbed-branch
 // kernels as mla_verify_attention, but their scratch lives in one
-// file-scope __device__ array of kStaticScratchBytes, which every GPU that
-// loads this library keeps reserved until the process exits.
+// file-scope __device__ array of kStaticScratchBytes.
+//
+// This file is its own CUDA module, and CUDA loads modules lazily: the array
+// is reserved on a device when the module is first loaded there, which is the
+// first call of this entry point on that device (its cudaGetSymbolAddress),
+// not when the library is loaded.  From then on the device keeps the 32 MiB
+// until the process exits.  The first call on each device should therefore
+// come early, as a warm-up: before a host pool claims the device's memory
+// (or the load fails for lack of memory, reported as MLA_ERR_WORKSPACE) and
+// before any stream capture begins.
 //
 // The array's name, used in host code, is only a host-side stand-in for the
-// device symbol: its device address is looked up with cudaGetSymbolAddress
-// once per device, with that device current, the first time this entry point
-// runs on it.  That first call on each device should therefore come before
-// any stream capture begins.
+// device symbol.  Its device address is looked up with cudaGetSymbolAddress
+// on every call, with the call's device current (the stream must belong to
+// it), so a call made in another context or after a device reset gets that
+// context's address, never a stale one.
 //
 // Every call shares the one array and it keeps whatever the previous call
-// left in it.  The absorbed launch path writes every scratch value before it
-// reads it, so nothing has to start at zero; calls that overlap on the GPU
+// left in it.  The absorbed launch path writes every scratch value it later
+// uses, so nothing has to start at zero; calls that overlap on the GPU
 // (concurrent streams, or other threads) race on the array and must not be
 // issued.
-
-#include <mutex>
 
 #include "mla_internal.h"
 
@@ -34,25 +40,37 @@ static __device__ __align__(256) char g_static_scratch[kStaticScratchBytes];
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_static_scratch on the current device (looked up once).
-cudaError_t static_scratch(void** addr) {
-  int dev = -1;
+// Device address of g_static_scratch in the current context, after checking
+// that `stream` belongs to the current device.
+mla_status_t static_scratch(cudaStream_t stream, void** addr) {
+  int dev = -1, sdev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+  if (e == cudaSuccess) e = cudaStreamGetDevice(stream, &sdev);
+  if (e != cudaSuccess) {
+    set_error("could not query the current device or the stream's device: %s",
+              cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
   }
-  *addr = g_scratch_addr[dev];
-  return cudaSuccess;
+  if (sdev != dev) {
+    set_error("the stream belongs to device %d but device %d is current", sdev, dev);
+    return MLA_ERR_INVALID_ARG;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    set_error("device %d has no room left for the %zu-byte static scratch, which is reserved "
+              "by the first mla_verify_attention_noalloc call on a device: make that call "
+              "before the host's memory pool claims the device",
+              dev, kStaticScratchBytes);
+    return MLA_ERR_WORKSPACE;
+  }
+  if (e != cudaSuccess) {
+    set_error("cudaGetSymbolAddress of the static scratch failed: %s", cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  *addr = p;
+  return MLA_OK;
 }
 
 }  // namespace
@@ -78,11 +96,8 @@ extern "C" mla_status_t mla_verify_attention_noalloc(
     return MLA_ERR_WORKSPACE;
   }
   void* scratch = nullptr;
-  const cudaError_t e = static_scratch(&scratch);
-  if (e != cudaSuccess) {
-    set_error("cudaGetSymbolAddress of the static scratch failed: %s", cudaGetErrorString(e));
-    return MLA_ERR_CUDA;
-  }
+  st = static_scratch((cudaStream_t)stream, &scratch);
+  if (st != MLA_OK) return st;
   return mla_verify_attention(g, q_nope, q_rope, c_kv, k_rope, c_kv_row_stride,
                               k_rope_row_stride, seq_stride_rows, W_UK, W_UV, lens_dev,
                               lens_host, batch, L, page_table, page_size, max_pages_per_seq,

@@ -76,8 +76,15 @@ def _normal(gen, shape, std, dtype):
     return x.to(dtype)
 
 
+def dominant_position(T: int, L: int) -> int:
+    """Where ``make_case(dominant=...)`` plants its key: position T - L + 1, the
+    first one that verify row 0 must not see (T // 2 when L == 1)."""
+    return T - L + 1 if L > 1 else T // 2
+
+
 def make_case(geom: Geometry, L: int, cache_lens, dtype=torch.bfloat16, seed: int = 0,
-              page_size: int = 0, tmax: Optional[int] = None) -> Case:
+              page_size: int = 0, tmax: Optional[int] = None, q_std: float = 1.0,
+              dominant: float = 0.0) -> Case:
     """Draw one case.  ``page_size`` > 0 gives a paged cache with a random page table.
 
     Draw order is fixed (q_nope, q_rope, cache, k_rope, W_UK, W_UV, page
@@ -86,13 +93,20 @@ def make_case(geom: Geometry, L: int, cache_lens, dtype=torch.bfloat16, seed: in
     ``tmax`` is given; paged caches hold sum(ceil(T_b/page)) pages, shuffled,
     and the tail rows of each sequence's last page are filled with random
     values too (they must be ignored by the attention).
+
+    Sharper score distributions for edge cases: ``q_std`` scales both query
+    parts (q_std = 12 gives scores with a standard deviation of about 12
+    nats at the configured geometries instead of about 1); ``dominant`` = D > 0
+    sets the first RoPE component of every query to D and that of the key at
+    ``dominant_position(T_b, L)`` to D, so that key wins by about D^2/sqrt(n+rope)
+    nats (contiguous caches only).
     """
     cache_lens = [int(t) for t in cache_lens]
     B = len(cache_lens)
     g = torch.Generator().manual_seed(int(seed))
     wstd = 1.0 / (512 ** 0.5)
-    q_nope = _normal(g, (B, L, geom.H, geom.n), 1.0, dtype)
-    q_rope = _normal(g, (B, L, geom.H, geom.rope), 1.0, dtype)
+    q_nope = _normal(g, (B, L, geom.H, geom.n), q_std, dtype)
+    q_rope = _normal(g, (B, L, geom.H, geom.rope), q_std, dtype)
     page_table = None
     if page_size > 0:
         npages = [(t + page_size - 1) // page_size for t in cache_lens]
@@ -113,6 +127,12 @@ def make_case(geom: Geometry, L: int, cache_lens, dtype=torch.bfloat16, seed: in
         for b in range(B):
             page_table[b, :npages[b]] = perm[k:k + npages[b]]
             k += npages[b]
+    if dominant:
+        if page_size > 0:
+            raise ValueError("dominant keys are planted in contiguous caches only")
+        q_rope[..., 0] = dominant
+        for b, T in enumerate(cache_lens):
+            k_rope[b, dominant_position(T, L), 0] = dominant
     return Case(geom, L, cache_lens, dtype, q_nope, q_rope, c_kv, k_rope, W_UK, W_UV,
                 page_table, page_size)
 

@@ -7,5 +7,5 @@ benchmark's CPU-baseline leg use it.  The GPU library never imports it.
 from .mla_oracle import (  # noqa: F401
     BRANCH_ABSORBED, BRANCH_MATERIALISED, MODE_ABSORBED, MODE_AUTO, MODE_MATERIALISED,
     absorbed, brute_force, default_scale, gather_paged, materialised,
-    max_absorbed_queries, max_absorbed_queries_batch, select_branch, verify_attention,
+    max_absorbed_queries, max_absorbed_queries_batch, select_branch,
 )

@@ -44,8 +44,12 @@ design notes of the repository):
   already applied to q_rope and k_rope.
 
 parity pinned: every function here is checked in tests/test_oracle.py against
-the printed thresholds, brute force on tiny inputs, a library attention
-routine, the absorbed == materialised identity and closed-form special cases.
+something other than itself -- the printed thresholds, brute force on tiny
+inputs, torch's scaled_dot_product_attention (its default scale is the
+query width's inverse square root, which pins default_scale), the absorbed ==
+materialised identity, closed-form special cases, and for gather_paged a
+round trip through an independently written page scatter plus paged ==
+contiguous attention under a random page permutation.
 """
 
 from __future__ import annotations
@@ -235,18 +239,6 @@ def materialised(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=Non
             o = p @ val                                            # [h, rows, v]
             out[b, :, c0:c0 + len(hs)] = np.transpose(o, (1, 0, 2))
     return out
-
-
-def verify_attention(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, L=None,
-                     mode=MODE_AUTO, scale=None, heads=None):
-    """Dispatch on the crossover, then run the chosen branch.  Returns (out, branch)."""
-    B, Lq, H, n = np.shape(q_nope)
-    r = np.shape(c_kv)[-1]
-    v = np.shape(W_UV)[-1]
-    branch = select_branch(r, n, v, Lq, cache_lens, mode)
-    fn = absorbed if branch == BRANCH_ABSORBED else materialised
-    return fn(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=scale,
-              heads=heads), branch
 
 
 def brute_force(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, scale=None):

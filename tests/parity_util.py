@@ -3,21 +3,28 @@ run it through the C ABI, build the oracle's float64 inputs from the same
 (dtype-rounded) values, and compare with the tolerances below.
 
 Tolerances.  bf16 inputs with fp32 accumulation must match the float64
-oracle within max-abs 2e-2 and mean-abs 2e-3 (the stated bar), and, as a
-tighter internal gate that catches real mistakes, max-abs 8e-3 and relative
-L2 1e-2.  The kernels round q_lat, the softmax weights P and o_lat (absorbed)
-or the expanded K_nope/V (materialised) to bf16 for the tensor-core
-contractions, and the output to bf16: each rounding carries a relative error
-of at most 2^-9, which bounds the expected relative L2 error near 3e-3 and
-the max-abs error near two bf16 ULPs (2^-7) of the largest output.
-The configured workloads give outputs below 1 in magnitude, where these
-absolute bounds apply as stated; edge cases with larger outputs (T = 1, where
-the output is c_kv[0] . W_UV, of order 1) scale every absolute bound by the
-largest |output| (S = max(1, max|want|)).
+oracle within max-abs 2e-2 and mean-abs 2e-3 (the stated bar).  A tighter
+internal gate, relative to the size of the outputs so that it bites at their
+real scale, catches real mistakes: max-abs at most 2^-6 * max|want| and
+relative L2 at most 1e-2.  The kernels round q_lat, the softmax weights P
+and o_lat (absorbed) or the expanded K_nope/V (materialised) to bf16 for the
+tensor-core contractions, and the output to bf16: each rounding carries a
+relative error of at most 2^-9, which bounds the expected relative L2 error
+near 3e-3 and the max-abs error near two bf16 ULPs (2 * 2^-7 relative) of the
+largest output.  The configured workloads give outputs below 1 in magnitude,
+where the stated absolute bar applies as written; edge cases with larger
+outputs (T = 1, where the output is c_kv[0] . W_UV, or one dominant key) scale
+the absolute bar by the largest |output| (S = max(1, max|want|)).
 fp32 runs on CUDA cores in fp32 throughout: max-abs 1e-4*S, relative L2 1e-5.
+
+With MLA_PARITY_LOG set to a file name, every comparison appends one JSON
+line with its errors (for calibrating these bounds; the asserts are the same).
 """
 
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
@@ -28,7 +35,7 @@ from mla_attention_speculative_gb300.inputs import Case
 
 BF16_MAX_ABS = 2e-2
 BF16_MEAN_ABS = 2e-3
-BF16_MAX_ABS_GATE = 8e-3
+BF16_MAX_REL_GATE = 2.0 ** -6     # max-abs / max|want|
 BF16_REL_L2 = 1e-2
 FP32_MAX_ABS = 1e-4
 FP32_REL_L2 = 1e-5
@@ -89,12 +96,18 @@ def compare(got: torch.Tensor, want: np.ndarray, dtype, what=""):
     max_abs = float(err.max())
     mean_abs = float(err.mean())
     rel = float(np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-30))
-    S = max(1.0, float(np.abs(want).max()))
+    wmax = float(np.abs(want).max())
+    S = max(1.0, wmax)
     msg = (f"{what}: max_abs={max_abs:.3e} mean_abs={mean_abs:.3e} rel_l2={rel:.3e} "
-           f"scale={S:.2f}")
+           f"max|want|={wmax:.3e}")
+    log = os.environ.get("MLA_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps(dict(what=what, max_abs=max_abs, mean_abs=mean_abs, rel_l2=rel,
+                                    max_want=wmax, dtype=str(dtype))) + "\n")
     if dtype == torch.float32:
         assert max_abs <= FP32_MAX_ABS * S and rel <= FP32_REL_L2, msg
     else:
         assert max_abs <= BF16_MAX_ABS * S and mean_abs <= BF16_MEAN_ABS * S, msg
-        assert max_abs <= BF16_MAX_ABS_GATE * S and rel <= BF16_REL_L2, msg
+        assert max_abs <= BF16_MAX_REL_GATE * wmax and rel <= BF16_REL_L2, msg
     return dict(max_abs=max_abs, mean_abs=mean_abs, rel_l2=rel)

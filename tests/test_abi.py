@@ -167,3 +167,40 @@ def test_status_strings():
     assert B.status_string(0) == "MLA_OK"
     assert B.status_string(-3) == "MLA_ERR_WORKSPACE"
     assert B.status_string(-99) == "MLA_ERR_UNKNOWN"
+
+
+# ---------------------------------------------------------------------------
+# Host-side page-table validation
+# ---------------------------------------------------------------------------
+
+def test_page_table_check_accepts_valid_table():
+    table = [[3, 0, 7], [1, 2, -1]]          # -1 past sequence 1's last page is not read
+    B.mla_check_page_table(table, [130, 100], 64, 8)
+
+
+@pytest.mark.parametrize("table,lens,num_pages,bad", [
+    ([[3, 8, 0]], [130], 8, "page_table[0][1] = 8"),     # one past the pool
+    ([[0, -1]], [65], 4, "page_table[0][1] = -1"),       # negative id inside the sequence
+    ([[0, 1], [2, 99]], [10, 128], 4, "page_table[1][1] = 99"),
+    ([[0, 1]], [129], 4, "needs 3 pages"),               # table too narrow for T
+])
+def test_page_table_check_rejects_out_of_range(table, lens, num_pages, bad):
+    with pytest.raises(B.MlaError) as e:
+        B.mla_check_page_table(table, lens, 64, num_pages)
+    assert e.value.status == B.MLA_ERR_INVALID_ARG
+    assert bad in str(e.value)
+
+
+def test_noalloc_binding_rejects_non_contiguous_views():
+    # the tensor maps assume row-major operands: a transposed view must be
+    # refused before anything reaches the library
+    import torch
+    q = torch.zeros(1, 2, 4, 128, dtype=torch.bfloat16).transpose(1, 2)
+    qr = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
+    ckv = torch.zeros(1, 64, 512, dtype=torch.bfloat16)
+    kr = torch.zeros(1, 64, 64, dtype=torch.bfloat16)
+    wuk = torch.zeros(2, 128, 512, dtype=torch.bfloat16)
+    wuv = torch.zeros(2, 512, 128, dtype=torch.bfloat16)
+    for fn in (B.mla_verify_attention_noalloc, B.mla_verify_attention):
+        with pytest.raises(ValueError, match="q_nope must be contiguous"):
+            fn(q, qr, ckv, kr, wuk, wuv, [64])

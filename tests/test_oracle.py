@@ -151,8 +151,12 @@ def test_brute_force_scale_parameter():
                                    atol=1e-12)
 
 
-def _sdpa_reference(c, scale):
-    """Same attention through torch's scaled_dot_product_attention (float64, CPU)."""
+def _sdpa_reference(c, scale=None):
+    """Same attention through torch's scaled_dot_product_attention (float64, CPU).
+
+    ``scale`` None leaves the scale to the library, whose default is the
+    inverse square root of the query width, here n + rope: an independent
+    statement of the oracle's default_scale."""
     q_nope, q_rope = c["q_nope"], c["q_rope"]
     B, L, H, n = q_nope.shape
     out = np.zeros((B, L, H, c["W_UV"].shape[-1]))
@@ -180,8 +184,7 @@ def test_branches_match_library_attention(geom):
     r, n, v = geom
     rng = np.random.default_rng(r + n + v)
     c = _rand_case(rng, B=2, L=5, H=3, r=r, n=n, v=v, rope=64, lens=[37, 80])
-    s = O.default_scale(n, 64)
-    ref = _sdpa_reference(c, s)
+    ref = _sdpa_reference(c)      # the library's own default scale
     np.testing.assert_allclose(O.absorbed(**c), ref, atol=1e-12, rtol=0)
     np.testing.assert_allclose(O.materialised(**c), ref, atol=1e-12, rtol=0)
 
@@ -273,23 +276,57 @@ def test_causal_mask_boundary_with_dominant_key():
         assert np.max(np.abs(out[0, 0] - val)) > 1e-3
 
 
-def test_gather_paged_walks_page_table():
-    rng = np.random.default_rng(14)
-    page = 4
-    lens = [5, 9, 1]
-    npg = [(t + page - 1) // page for t in lens]
-    pages = rng.standard_normal((sum(npg), page, 3))
-    perm = rng.permutation(sum(npg))
-    table = np.zeros((3, max(npg)), dtype=np.int64)
+def _scatter_to_pages(contig, lens, page, perm):
+    """The inverse of a page walk, written independently of gather_paged:
+    sequence b's logical page j (rows j*page .. j*page+page-1 of its
+    contiguous cache) is copied whole into physical page perm[k], k counting
+    pages in sequence order.  Returns (pages, page table)."""
+    npg = [-(-T // page) for T in lens]
+    pages = np.full((sum(npg), page, contig.shape[-1]), np.nan)
+    table = np.full((len(lens), max(npg)), -1, dtype=np.int64)
     k = 0
-    for b in range(3):
-        table[b, :npg[b]] = perm[k:k + npg[b]]
-        k += npg[b]
-    got = O.gather_paged(pages, table, lens, page)
-    for b in range(3):
-        for t in range(lens[b]):
-            p = table[b][t // page]
-            assert np.array_equal(got[b, t], pages[p, t % page])
+    for b, T in enumerate(lens):
+        for j in range(npg[b]):
+            dst = int(perm[k])
+            k += 1
+            table[b, j] = dst
+            rows = contig[b, j * page:min((j + 1) * page, T)]
+            pages[dst, :rows.shape[0]] = rows
+    return pages, table
+
+
+def test_gather_paged_round_trip():
+    # scatter a contiguous cache into shuffled pages, gather it back: exact
+    rng = np.random.default_rng(14)
+    for page, lens in ((4, [5, 9, 1]), (64, [64, 65, 200, 3]), (16, [16, 1, 47])):
+        contig = rng.standard_normal((len(lens), max(lens), 3))
+        perm = rng.permutation(sum(-(-T // page) for T in lens))
+        pages, table = _scatter_to_pages(contig, lens, page, perm)
+        got = O.gather_paged(pages, table, lens, page)
+        for b, T in enumerate(lens):
+            assert np.array_equal(got[b, :T], contig[b, :T])
+
+
+def test_paged_attention_equals_contiguous():
+    # attention over a paged cache (gathered) equals attention over the
+    # contiguous cache, for a random page permutation
+    rng = np.random.default_rng(17)
+    page = 8
+    c = _rand_case(rng, B=3, L=3, H=2, r=16, n=8, v=4, rope=4, lens=[9, 24, 3])
+    perm = rng.permutation(sum(-(-T // page) for T in c["cache_lens"]))
+    pc, table = _scatter_to_pages(c["c_kv"], c["cache_lens"], page, perm)
+    pk, _ = _scatter_to_pages(c["k_rope"], c["cache_lens"], page, perm)
+    paged = dict(c, c_kv=O.gather_paged(pc, table, c["cache_lens"], page),
+                 k_rope=O.gather_paged(pk, table, c["cache_lens"], page))
+    np.testing.assert_array_equal(O.absorbed(**paged), O.absorbed(**c))
+    np.testing.assert_allclose(O.brute_force(**paged), O.absorbed(**c), atol=1e-12)
+
+
+def test_default_scale_stated_value():
+    # the tiny fp32 workload states its softmax scale as 1/sqrt(192) for
+    # n = 128, rope = 64 (the pages themselves leave the scale open)
+    assert O.default_scale(128, 64) == 1.0 / math.sqrt(192)
+    assert abs(O.default_scale(128, 64) - 0.07216878364870323) < 1e-17
 
 
 # ---------------------------------------------------------------------------
@@ -310,11 +347,15 @@ def test_planted_mask_offset_is_caught(monkeypatch):
 
 
 def test_planted_scale_is_caught(monkeypatch):
+    # 1/sqrt(n) instead of 1/sqrt(n + rope): caught by the stated literal and by
+    # the library attention's default scale
     rng = np.random.default_rng(16)
     c = _rand_case(rng, B=1, L=2, H=2, r=512, n=128, v=128, rope=64, lens=[20])
-    ref = _sdpa_reference(c, O.default_scale(128, 64))
+    ref = _sdpa_reference(c)
     monkeypatch.setattr(O, "default_scale", lambda n, rope: 1.0 / math.sqrt(n))
     assert np.max(np.abs(O.absorbed(**c) - ref)) > 1e-4
+    with pytest.raises(AssertionError):
+        test_default_scale_stated_value()
 
 
 def test_planted_threshold_strictness_is_caught(monkeypatch):
@@ -330,3 +371,21 @@ def test_planted_threshold_strictness_is_caught(monkeypatch):
     monkeypatch.setattr(O, "max_absorbed_queries", strict)
     rows = [g for g in _golden_thresholds() if g[:3] == (512, 256, 256)]
     assert any(O.max_absorbed_queries(r, n, v, t) != want for r, n, v, t, want, _ in rows)
+
+
+def test_planted_page_walk_off_by_one_is_caught(monkeypatch):
+    real = O.gather_paged
+
+    def off_by_one(pages, page_table, cache_lens, page_size):
+        pages = np.asarray(pages)
+        out = np.zeros((len(cache_lens), int(max(cache_lens)), pages.shape[-1]))
+        for b, T in enumerate(cache_lens):
+            t = np.arange(int(T))
+            out[b, :T] = pages[np.asarray(page_table)[b, (t + 1) // page_size], t % page_size]
+        return out
+
+    monkeypatch.setattr(O, "gather_paged", off_by_one)
+    with pytest.raises(AssertionError):
+        test_gather_paged_round_trip()
+    monkeypatch.setattr(O, "gather_paged", real)
+    test_gather_paged_round_trip()

@@ -175,6 +175,48 @@ def test_repeat_call_is_deterministic():
 
 
 # ---------------------------------------------------------------------------
+# Sharp score distributions at full size: the two CTAs of an absorbed pair
+# exchange their partial scores rounded to fp16, whose spacing grows with the
+# score's magnitude; these cases put that rounding where it matters most
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L", [1, 16])
+def test_peaked_logits_dsv3_T8192(L):
+    # queries scaled by 12: scores with a standard deviation of about 12 nats,
+    # the largest about 50 nats above the mean
+    case = make_case(DSV3, L, [8192], seed=200 + L, q_std=12.0)
+    _sampled_check(case, ["absorbed", "materialised"], f"peaked L={L}", nheads=8, nrows=6)
+
+
+@pytest.mark.parametrize("L", [1, 16])
+def test_dominant_key_dsv3_T8192(L):
+    # one key ahead of all others by about 65 nats, at the first position verify
+    # row 0 must not see: rows l >= 1 return (nearly) its value, row 0 does not
+    case = make_case(DSV3, L, [8192], seed=210 + L, dominant=30.0)
+    _sampled_check(case, ["absorbed", "materialised"], f"dominant L={L}", nheads=8, nrows=6)
+
+
+@pytest.mark.parametrize("geom,L,lens", [
+    (Geometry(H=24), 5, [300, 1000]),      # 120 rows: one Q tile, 8 rows padding
+    (GLM47, 3, [2500]),                    # 96 rows
+    (Geometry(H=40), 5, [700]),            # 200 rows: second Q tile mostly padding
+])
+def test_nan_poisoned_workspace(geom, L, lens):
+    # the workspace starts as all-ones bytes (NaN in bf16 and fp32): padded
+    # query rows and any scratch read before it is written must not leak
+    case = make_case(geom, L, lens, seed=220 + L)
+    want = oracle_out(case)
+    d = device_tensors(case)
+    for mode in ("absorbed", "materialised"):
+        g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope)
+        need = B.mla_workspace_bytes(g, L, lens, mode)
+        ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+        out, branch = run_gpu(case, mode, dev_t=d, workspace=ws)
+        _check_branch(case, mode, branch)
+        compare(out, want, torch.bfloat16, f"nan workspace {mode}")
+
+
+# ---------------------------------------------------------------------------
 # The measurement configurations at full size, sampled outputs
 # ---------------------------------------------------------------------------
 
@@ -270,6 +312,33 @@ def test_bounded_wait_runs_out_and_context_stays_usable():
     case = make_case(Geometry(H=8), 4, [300], seed=91)
     out, _ = run_gpu(case, "absorbed")
     compare(out, oracle_out(case), torch.bfloat16, "after the self-test")
+
+
+# ---------------------------------------------------------------------------
+# A page id outside [0, num_pages) in the device page table: the kernels form
+# no address from it, read that page's positions as zeros, and report it
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode,page", [("absorbed", 64), ("materialised", 64),
+                                       ("absorbed", 16)])
+def test_out_of_range_page_id_is_reported(mode, page):
+    case = make_case(Geometry(H=8), 2, [200, 70], seed=97, page_size=page)
+    d = device_tensors(case)
+    bad = d["page_table"].clone()
+    bad[0, 1] = case.c_kv.shape[0] + 5       # one page of sequence 0 past the pool
+    with pytest.raises(B.MlaError) as e:
+        B.mla_check_page_table(bad.cpu(), case.cache_lens, page, case.c_kv.shape[0])
+    assert e.value.status == B.MLA_ERR_INVALID_ARG
+    B.mla_verify_attention(d["q_nope"], d["q_rope"], d["c_kv"], d["k_rope"], d["W_UK"],
+                           d["W_UV"], case.cache_lens, mode=mode, page_table=bad,
+                           cache_lens_dev=d["lens_dev"])
+    torch.cuda.synchronize()
+    with pytest.raises(B.MlaError) as e:
+        B.mla_device_status()
+    assert e.value.status == B.MLA_ERR_INVALID_ARG
+    assert B.mla_device_status() == 0          # the report was cleared
+    out, _ = run_gpu(case, mode, dev_t=d)      # the valid table still works
+    compare(out, oracle_out(case), torch.bfloat16, f"after bad page {mode}")
 
 
 # ---------------------------------------------------------------------------
