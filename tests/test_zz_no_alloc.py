@@ -51,7 +51,7 @@ def _both(case):
 CALLS = [
     (DSV3, 16, [8192], 0),                 # 2048 query rows: most of the scratch in use
     (Geometry(H=32), 1, [3001, 700], 0),   # 32 rows per sequence: 96 padding rows per tile
-    (Geometry(H=8), 3, [70, 200, 1], 64),  # paged cache, 24 rows per sequence
+    (Geometry(H=8), 3, [70, 200, 3], 64),  # paged cache, 24 rows per sequence
     (Geometry(H=40), 5, [700], 0),         # 200 rows: a second, mostly padding, tile
 ]
 
