@@ -93,7 +93,11 @@ def _work(kernel: str, L: int, T: int, H=128, r=512, n=128, v=128, rope=64):
     attend = (cache + rows * (r + rope) * bf + rows * r * bf,
               2 * rows * T * (r + rope) + 2 * rows * T * r)
     unembed = (H * r * v * bf + rows * r * bf + rows * v * bf, 2 * rows * r * v)
+    # attention, merge and unembedding in one kernel: no o_lat hand-off
+    fused = (cache + rows * (r + rope) * bf + H * r * v * bf + rows * v * bf,
+             attend[1] + unembed[1])
     table = {
+        "absorbed_fused_sm103": fused,
         "generic_fold": fold,
         "generic_absorbed_attention": attend,
         "generic_combine_unembed": unembed,
@@ -250,6 +254,7 @@ KERNEL_SOURCES = {
     "generic_combine_unembed": ["generic_kernels.cu"],
     "fold_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "absorbed_attn_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
+    "absorbed_fused_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "merge_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "unembed_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "expand_sm103": ["materialised_sm103.cu", "sm103_ptx.cuh"],

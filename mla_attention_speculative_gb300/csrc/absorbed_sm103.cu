@@ -98,6 +98,10 @@ struct GemmParams {
   // 8 latent columns, each chunk 128 rows x 16 B, so a warp that loads one
   // chunk for its 32 rows reads 512 contiguous bytes.
   int L, ntile;
+  // the fused attention's per-sequence arrival counters, zeroed here once the
+  // preceding grid (which may still be using them) has completed
+  uint32_t* zero;
+  int nzero;
 };
 
 constexpr int GEMM_MAX_K = 512;
@@ -142,6 +146,8 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
                     h * K + 64 * kc);
     }
     pdl_wait();  // the activations may come from the preceding kernel
+    if (p.nzero > 0 && (blockIdx.x | blockIdx.y | blockIdx.z) == 0)
+      for (int i = 0; i < p.nzero; ++i) p.zero[i] = 0u;
     for (int kc = 0; kc < nk; ++kc)
       tma_load_2d(smem_u32(sB + kc * NB * 128), &tm_act, smem_u32(&bars[kc]), h * K + 64 * kc,
                   row0);
@@ -216,7 +222,18 @@ constexpr int OFF_STG = OFF_X + 2 * X_BYTES;        // this CTA's partial scores
 constexpr int OFF_RED = OFF_STG + X_BYTES;          // row maxima of the warpgroups
 constexpr int OFF_LS = OFF_RED + NWG * BM * 4;      // row sums of the warpgroups
 constexpr int OFF_BAR = OFF_LS + NWG * BM * 4;
-constexpr int ATTN_SMEM = OFF_BAR + 256 + 1024;     // + barriers + alignment slack
+constexpr int ATTN_SMEM = OFF_BAR + 512 + 1024;     // + barriers + alignment slack
+// Fused merge + unembedding (after the attention; every buffer above is free
+// by then): the W_UV tile of one (head, 128-column) unit, 512 x 128 bf16 as
+// two 64-column MN-major atoms, over the KV stages; the merged o_lat rows of
+// the unit (the B operand, K-major, at most FUSED_MAX_L rows padded to 16)
+// over the P and exchange tiles, followed by the merge's per-group partials.
+constexpr int FUSED_MAX_L = kFusedMaxL;
+constexpr int FU_W_BYTES = 2 * kLat * 128;
+constexpr int FU_B_BYTES = 8 * FUSED_MAX_L * 128;
+constexpr int FU_SCRATCH = OFF_P + FU_B_BYTES;
+static_assert(OFF_KV + FU_W_BYTES <= OFF_P, "W_UV tile fits over the KV stages");
+static_assert(FU_SCRATCH + ATTN_THREADS * 10 * 4 <= OFF_RED, "merge scratch fits");
 // Tensor memory: O half [0,256) fp32; this CTA's 256 latent query columns as
 // bf16 pairs [256,384) (the A operand of the score MMAs); S buffers [384,512).
 constexpr uint32_t TM_O = 0;
@@ -242,13 +259,18 @@ struct AttnParams {
   float* ml;              // [B, splits, R, 2]: (m, l) of each piece
   const char* pf;     // W_UV, pulled into L2 while the attention runs
   size_t pf_bytes;
+  // fused merge + unembedding only
+  uint32_t* counters;     // [B] CTAs of sequence b that have published their pieces
+  __nv_bfloat16* out;     // [B, L, H, v]
+  int v;                  // value width, a multiple of 128
 };
 
 // Barrier slots.  Every barrier that is waited on by parity alone has enough
 // copies that it cannot complete twice before its waiter looks.
 enum {
   B_QFULL = 0, B_QTMEM = 1, B_KVFULL = 2, B_KVEMPTY = 6, B_SFULL = 10, B_SFREE = 12,
-  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22, B_COUNT = 24
+  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22,
+  B_WFULL = 24, B_UDONE = 25, B_COUNT = 26
 };
 
 // One partial score of this CTA in log2-softmax units, rounded to fp16: the
@@ -296,11 +318,235 @@ __device__ __forceinline__ uint32_t xchg_offset(int wg, int q, int c) {
   return (uint32_t)((q >> 5) * XQUARTER + wg * (32 * XROW) + (q & 31) * XROW + ((c ^ sw) << 4));
 }
 
+// 8 bf16 (one 16-byte load) to fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// =========================================================================
+// fused merge + unembedding (the last phase of the FUSED attention kernel)
+// =========================================================================
+// Once every CTA of sequence b has published its piece (O/l in bf16, (m, l)),
+// the CTAs of the sequence share its (head, 128-column) units: for unit
+// (h, mt) a CTA merges rows (l, h), l < L, over the pieces,
+//   o_lat = sum_s w_s (O_s / l_s) / sum_s w_s,  w_s = 2^(m_s - M) l_s,
+// straight into shared memory as the K-major B operand (bf16, as the separate
+// merge writes it), and multiplies it by the W_UV tile of columns
+// [128 mt, 128 mt + 128) (loaded by TMA while the CTA waits for the others;
+// the attention pulled W_UV into L2): D[128 x L] = W_UV[h][:, tile]^T o_lat^T
+// in TMEM, then out[b, l, h, 128 mt + m].  No o_lat round trip, no launches.
+__device__ __forceinline__ void fused_merge_unembed(const AttnParams& p, const CUtensorMap& tm_wuv,
+                                                    uint8_t* smem, uint32_t tmem, uint64_t* bars,
+                                                    int b, int split, int nsplit) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t sW = smem_u32(smem + OFF_KV), sB = smem_u32(smem + OFF_P);
+  float* scratch = (float*)(smem + FU_SCRATCH);
+  volatile int* stop = (volatile int*)(smem + OFF_RED);  // (the row maxima are done with)
+  const int nmt = p.v / 128;
+  const int units = p.H * nmt;
+  const int ncta = (int)gridDim.x * nsplit;  // the CTAs of this sequence that wrote pieces
+  const int cid = split * (int)gridDim.x + (int)blockIdx.x;
+  const int NBp = (p.L + 15) & ~15;
+  auto load_w = [&](int u) {
+    const int h = u / nmt, mt = u - h * nmt;
+    mbar_arrive_expect_tx(bar(B_WFULL), FU_W_BYTES);
+    for (int kc = 0; kc < kLat / 64; ++kc)
+      for (int j = 0; j < 2; ++j)
+        tma_load_2d(sW + j * kLat * 128 + kc * 8192, &tm_wuv, bar(B_WFULL), mt * 128 + 64 * j,
+                    h * kLat + 64 * kc);
+  };
+  if (threadIdx.x == 0) {
+    *stop = 0;
+    if (cid < units) load_w(cid);
+  }
+  // publish this CTA's pieces (its softmax threads fenced their writes and the
+  // storing thread waited for its TMA stores before the barrier above), then
+  // wait for the other CTAs of the sequence; the grid is resident as a whole,
+  // so they all get here, and the wait is bounded anyway
+  if (threadIdx.x == 96) {
+    __threadfence();
+    red_release_gpu_add(p.counters + b, 1u);
+    const uint32_t target = (uint32_t)ncta;
+    if (ld_acquire_gpu(p.counters + b) < target) {
+      const long long t0 = clock64();
+      while (ld_acquire_gpu(p.counters + b) < target) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+          report_timeout(30);
+          *stop = 1;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+  }
+  __syncthreads();
+  const bool go = *stop == 0;
+  const int P = p.L * 64;  // (row, 16-byte column chunk) pairs of a unit
+  const int G = P >= ATTN_THREADS ? 1 : min(8, ATTN_THREADS / P);  // piece groups per pair
+  const size_t R = (size_t)p.R;
+  int k = 0;
+  for (int u = cid; u < units; u += ncta, ++k) {
+    const int h = u / nmt, mt = u - h * nmt;
+    // ---- merge rows (l, h) into the B operand
+    if (go) {
+      for (int t = threadIdx.x; t < P * G; t += ATTN_THREADS) {
+        const int g = t / P, pr = t - g * P;
+        const int l = pr >> 6, c = pr & 63;
+        const size_t base = (size_t)b * p.splits * R + (size_t)l * p.H + h;
+        float M = -FLT_MAX, den = 0.f, acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int s0 = g; s0 < nsplit; s0 += 4 * G) {
+          float2 mls[4];
+          uint4 x[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int sj = s0 + j * G;
+            const size_t e = base + (size_t)min(sj, nsplit - 1) * R;
+            mls[j] = __ldcg((const float2*)(p.ml + e * 2));
+            x[j] = __ldcg((const uint4*)(p.o_part + e * kLat) + c);
+            if (sj >= nsplit) mls[j].y = 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (mls[j].y > 0.f) {
+              if (mls[j].x > M) {
+                const float f = ex2(M - mls[j].x);
+                M = mls[j].x;
+                den *= f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] *= f;
+              }
+              const float w = ex2(mls[j].x - M) * mls[j].y;
+              den += w;
+              float f[8];
+              bf16x8_to_f32(x[j], f);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[e] += w * f[e];
+            }
+          }
+        }
+        if (G == 1) {
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          const uint32_t addr =
+              sB + (c >> 3) * (NBp * 128) + l * 128 + ((((uint32_t)c & 7u) ^ (l & 7u)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "r"(pack_bf16(acc[0] * inv, acc[1] * inv)),
+                       "r"(pack_bf16(acc[2] * inv, acc[3] * inv)),
+                       "r"(pack_bf16(acc[4] * inv, acc[5] * inv)),
+                       "r"(pack_bf16(acc[6] * inv, acc[7] * inv))
+                       : "memory");
+        } else {
+          float* sc = scratch + (size_t)t * 10;
+          sc[0] = M;
+          sc[1] = den;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sc[2 + e] = acc[e];
+        }
+      }
+      if (G > 1) {
+        __syncthreads();
+        for (int pr = threadIdx.x; pr < P; pr += ATTN_THREADS) {
+          const int l = pr >> 6, c = pr & 63;
+          float Mall = -FLT_MAX;
+          for (int g = 0; g < G; ++g) {
+            const float* sc = scratch + (size_t)(g * P + pr) * 10;
+            if (sc[1] > 0.f) Mall = fmaxf(Mall, sc[0]);
+          }
+          float dsum = 0.f, y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = 0.f;
+          for (int g = 0; g < G; ++g) {
+            const float* sc = scratch + (size_t)(g * P + pr) * 10;
+            const float f = sc[1] > 0.f ? ex2(sc[0] - Mall) : 0.f;
+            dsum += f * sc[1];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] += f * sc[2 + e];
+          }
+          const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
+          const uint32_t addr =
+              sB + (c >> 3) * (NBp * 128) + l * 128 + ((((uint32_t)c & 7u) ^ (l & 7u)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "r"(pack_bf16(y[0] * inv, y[1] * inv)), "r"(pack_bf16(y[2] * inv, y[3] * inv)),
+                       "r"(pack_bf16(y[4] * inv, y[5] * inv)), "r"(pack_bf16(y[6] * inv, y[7] * inv))
+                       : "memory");
+        }
+      }
+      // the padding rows of the B operand are zero
+      for (int idx = threadIdx.x; idx < (NBp - p.L) * 64; idx += ATTN_THREADS) {
+        const int l = p.L + (idx >> 6), c = idx & 63;
+        const uint32_t addr =
+            sB + (c >> 3) * (NBp * 128) + l * 128 + ((((uint32_t)c & 7u) ^ (l & 7u)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+      }
+    }
+    fence_async_shared();
+    tc_fence_before();
+    __syncthreads();
+    // ---- D[128 x NBp] = W_UV tile^T (A, MN-major) x o_lat rows^T (B, K-major)
+    if (threadIdx.x == 32) {
+      tc_fence_after();
+      bool ok = go;
+      wait_or_fail(ok, bar(B_WFULL), k & 1, 31);
+      if (ok) {
+        const uint32_t idesc = idesc_bf16(128, NBp, 1, 0);
+        for (int kc = 0; kc < kLat / 64; ++kc)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + TM_O, sdesc_sw128(sW + (kc * 64 + ks * 16) * 128, kLat * 128, 1024),
+                     sdesc_sw128(sB + kc * NBp * 128 + ks * 32, 16, 1024), idesc,
+                     (kc | ks) != 0);
+      }
+      mma_commit(bar(B_UDONE));  // (arrives even when nothing was issued)
+    }
+    if (warp >= 3 && warp < 7) {
+      // one warpgroup: TMEM lane m is output column 128 mt + m
+      bool ok = go;
+      wait_or_fail(ok, bar(B_UDONE), k & 1, 32);
+      tc_fence_after();
+      if (ok) {
+        const int m = (warp & 3) * 32 + lane;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        __nv_bfloat16* o = p.out + ((size_t)b * p.L * p.H + h) * p.v + mt * 128 + m;
+        for (int c0 = 0; c0 < NBp; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + TM_O + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int l = c0 + i;
+            if (l < p.L) o[(size_t)l * p.H * p.v] = __float2bfloat16_rn(__uint_as_float(v[i]));
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    // the MMA that read the W_UV tile has completed: load the next unit's
+    if (threadIdx.x == 0 && go && u + ncta < units) load_w(u + ncta);
+  }
+  // nothing this CTA loaded may still be landing when it exits: a unit's
+  // tile is only loaded when the loop will consume it, and an early stop
+  // leaves at most the first one pending
+  if (threadIdx.x == 0 && !go && cid < units) mbar_wait(bar(B_WFULL), 0);
+}
+
+// FUSED: the kernel also merges the pieces and applies W_UV (see the fused
+// phase at the end); it is launched only when the whole grid fits on the GPU
+// at once, since each sequence's CTAs wait for one another there.
+template <bool FUSED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     absorbed_attn_sm103(const __grid_constant__ CUtensorMap tm_qr,
                         const __grid_constant__ CUtensorMap tm_ckv,
                         const __grid_constant__ CUtensorMap tm_kr,
-                        const __grid_constant__ CUtensorMap tm_op, AttnParams p) {
+                        const __grid_constant__ CUtensorMap tm_op,
+                        const __grid_constant__ CUtensorMap tm_wuv, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t rank = cluster_ctarank();
@@ -339,6 +585,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     }
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
+    mbar_init(bar(B_WFULL), 1);
+    mbar_init(bar(B_UDONE), 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(slot), 512);
@@ -762,16 +1010,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         tma_store_3d(&tm_op, sKV + bx * (BM * 128), (int)rank * 256 + 64 * bx, row0,
                      b * p.splits + split);
       bulk_commit();
-      // the staging may be released once the stores have read it; their
-      // writes are complete when the grid is (the merge reads them after its
-      // dependency wait)
-      bulk_wait_read();
+      if constexpr (FUSED) {
+        // other CTAs of the sequence read the pieces in this grid: the writes
+        // must be complete, and ordered before the arrival below
+        bulk_wait_all();
+        fence_proxy_async_global();
+      } else {
+        // the staging may be released once the stores have read it; their
+        // writes are complete when the grid is (the merge reads them after
+        // its dependency wait)
+        bulk_wait_read();
+      }
     }
     if (live && rank == 0 && wg == 0) {
       float* mlp = p.ml + (((size_t)b * p.splits + split) * p.R + row) * 2;
       mlp[0] = m_run == -INFINITY ? -FLT_MAX : m_run;
       mlp[1] = l_tot;
     }
+    if constexpr (FUSED) __threadfence();
+  }
+  if constexpr (FUSED) {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    fused_merge_unembed(p, tm_wuv, smem, tmem, bars, b, split, nsplit);
   }
   tc_fence_before();
   __syncthreads();
@@ -799,15 +1061,6 @@ struct MergeParams {
   int R, chunk, splits;
   int rows;                     // B*R
 };
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
 
 template <int CPL, int W>  // W warps take every W-th piece
 __global__ void __launch_bounds__(32 * W) merge_sm103(MergeParams p) {
@@ -1009,6 +1262,59 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Per-device one-time setup: the kernels' shared-memory opt-in and the number
+// of attention clusters that fit on the device at once (the fused kernel is
+// only launched when its whole grid does).  Calls may come from several
+// threads; the first one on a device does the work under a lock.
+struct DeviceSetup {
+  cudaError_t err = cudaSuccess;
+  int slots = 0;
+  bool done = false;
+};
+
+const DeviceSetup& device_setup() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static DeviceSetup setups[kMaxDevices];
+  static DeviceSetup no_device;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    no_device.slots = device_sm_count() / 2;
+    no_device.err = cudaErrorNoDevice;
+    return no_device;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  DeviceSetup& d = setups[dev];
+  if (d.done) return d;
+  cudaError_t e = set_smem(swapab_gemm_sm103, gemm_smem(kLat, 64));
+  if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103<false>, ATTN_SMEM);
+  if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103<true>, ATTN_SMEM);
+  int slots = 0;
+  if (e == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(ATTN_THREADS);
+    cfg.dynamicSmemBytes = ATTN_SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&slots, absorbed_attn_sm103<true>, &cfg);
+  }
+  if (e != cudaSuccess || slots <= 0) {
+    cudaGetLastError();
+    slots = device_sm_count() / 2;
+  }
+  d.err = e;
+  d.slots = slots;
+  d.done = true;
+  return d;
+}
+
 }  // namespace
 
 cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
@@ -1039,25 +1345,12 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
                                (uint64_t)R * kLat * 2, 64, BM);
   if (!ok) return cudaErrorInvalidValue;
 
-  // shared-memory opt-in, once per device (calls may come from several threads)
-  static std::mutex attrs_mu;
-  static bool attrs[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> attrs_lock(attrs_mu);
-  if (dev >= 0 && dev < 64 && !attrs[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(swapab_gemm_sm103,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gemm_smem(kLat, 64));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(absorbed_attn_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               ATTN_SMEM);
-    if (e != cudaSuccess) return e;
-    attrs[dev] = true;
-  }
+  const DeviceSetup& ds = device_setup();
+  if (ds.err != cudaSuccess) return ds.err;
   cudaError_t e;
   {
-    GemmParams gp{q_lat, BL, p.H, p.n, kLat, NBf, p.L, (R + BM - 1) / BM};
+    GemmParams gp{q_lat, BL, p.H, p.n, kLat, NBf, p.L, (R + BM - 1) / BM,
+                  p.fused ? (uint32_t*)(a.ws + p.off_cnt) : nullptr, p.fused ? p.B : 0};
     KernelTimer kt("fold_sm103", a.stream);
     e = launch_pdl(swapab_gemm_sm103, dim3(kLat / 128, p.H, (BL + NBf - 1) / NBf), dim3(128),
                    gemm_smem(p.n, NBf), a.stream, tm_wuk, tm_qn, gp);
@@ -1084,10 +1377,20 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.ml = ml;
     ap.pf = (const char*)a.W_UV;
     ap.pf_bytes = (size_t)p.H * kLat * p.v * 2;
+    ap.counters = (uint32_t*)(a.ws + p.off_cnt);
+    ap.out = (__nv_bfloat16*)a.out;
+    ap.v = p.v;
+    const dim3 grid(2 * ((R + BM - 1) / BM), p.splits, p.B);
+    if (p.fused) {
+      KernelTimer kt("absorbed_fused_sm103", a.stream);
+      e = launch_pdl(absorbed_attn_sm103<true>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
+                     tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, ap);
+      if (e != cudaSuccess) return e;
+      return cudaGetLastError();
+    }
     KernelTimer kt("absorbed_attn_sm103", a.stream);
-    e = launch_pdl(absorbed_attn_sm103, dim3(2 * ((R + BM - 1) / BM), p.splits, p.B),
-                   dim3(ATTN_THREADS),
-                   ATTN_SMEM, a.stream, tm_qr, tm_ckv, tm_kr, tm_op, ap);
+    e = launch_pdl(absorbed_attn_sm103<false>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
+                   tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, ap);
     if (e != cudaSuccess) return e;
   }
   {
@@ -1105,13 +1408,18 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     if (e != cudaSuccess) return e;
   }
   {
-    GemmParams gp{(__nv_bfloat16*)a.out, BL, p.H, kLat, p.v, NBu, 0, 0};
+    GemmParams gp{(__nv_bfloat16*)a.out, BL, p.H, kLat, p.v, NBu, 0, 0, nullptr, 0};
     KernelTimer kt("unembed_sm103", a.stream);
     e = launch_pdl(swapab_gemm_sm103, dim3(p.v / 128, p.H, (BL + NBu - 1) / NBu), dim3(128),
                    gemm_smem(kLat, NBu), a.stream, tm_wuv, tm_ol, gp);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
+}
+
+int absorbed_cluster_slots() {
+  const DeviceSetup& ds = device_setup();
+  return ds.slots;
 }
 
 int absorbed_device_status(bool clear) {

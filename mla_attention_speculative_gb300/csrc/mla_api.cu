@@ -238,7 +238,7 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     constexpr int64_t kClusterOverhead = 4;
     SplitPlan& f = p->fast;
     const int64_t row_tiles = (rows + 127) / 128;
-    const int64_t slots = num_sms / 2;
+    const int64_t slots = absorbed_cluster_slots();
     const int64_t max_tiles = (p->Tmax + 63) / 64;
     int64_t best_ct = max_tiles, best_cost = -1;
     for (int64_t ct = max_tiles; ct >= 1; --ct) {
@@ -261,7 +261,15 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     off = align256(off + nrow * f.splits * 2 * sizeof(float));
     f.off_olat = off;
     off = align256(off + nrow * p->r * 2);
+    f.off_cnt = off;  // per-sequence arrival counters of the fused kernel
+    off = align256(off + (size_t)batch * sizeof(uint32_t));
     f.bytes = off;
+    // One kernel for attention, merge and unembedding when every cluster of
+    // the grid is on the GPU at once (each sequence's CTAs wait for one
+    // another before merging) and the verify block is narrow enough.
+    int64_t clusters = 0;
+    for (int b = 0; b < batch; ++b) clusters += row_tiles * ((lens[b] + f.chunk - 1) / f.chunk);
+    p->fused = clusters <= slots && L <= kFusedMaxL;
   }
   p->ws_bytes = p->fast_ok && p->fast.bytes > p->generic.bytes ? p->fast.bytes : p->generic.bytes;
   p->use(p->generic);

@@ -15,7 +15,7 @@ namespace mla {
 struct SplitPlan {
   int chunk = 0;    // KV rows per piece (multiple of 64)
   int splits = 0;   // largest number of pieces of any sequence
-  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0;
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0, off_cnt = 0;
   size_t bytes = 0;
 };
 
@@ -38,9 +38,12 @@ struct Plan {
   SplitPlan generic;   // CUDA-core kernels, any geometry and paging
   SplitPlan fast;      // tcgen05/TMA kernels of the chosen branch
   bool fast_ok = false;
+  // tensor-core absorbed branch: attention, merge and unembedding in one
+  // kernel (the grid fits on the GPU at once and L <= kFusedMaxL)
+  bool fused = false;
   size_t ws_bytes = 0;
   // the layout of the family that runs (copied from generic or fast)
-  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0;
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0, off_cnt = 0;
   void use(const SplitPlan& sp) {
     chunk = sp.chunk;
     splits = sp.splits;
@@ -49,8 +52,12 @@ struct Plan {
     off_ml = sp.off_ml;
     off_exp = sp.off_exp;
     off_olat = sp.off_olat;
+    off_cnt = sp.off_cnt;
   }
 };
+
+// Widest verify block the fused absorbed kernel merges and unembeds itself.
+constexpr int kFusedMaxL = 32;
 
 // Device-side view of the cache addressing shared by all kernels.
 struct CacheView {
@@ -105,6 +112,9 @@ int device_sm_count();
 // n a multiple of 64 up to 256, v a multiple of 128 up to 512).
 bool fast_absorbed_supported(const Plan& p);
 cudaError_t launch_fast_absorbed(const Plan& p, const Args& a);
+// Two-CTA clusters of the absorbed attention that fit on the current device
+// at once (device_sm_count() / 2 when it cannot be queried).
+int absorbed_cluster_slots();
 // Status word of the tensor-core kernels (0 = no wait ran out); synchronises.
 int absorbed_device_status(bool clear);
 // The status-word site the bounded-wait self-test records.

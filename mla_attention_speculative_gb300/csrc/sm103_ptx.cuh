@@ -220,6 +220,23 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
+// Global counters shared by the CTAs of one grid: a release add publishes this
+// thread's earlier writes (and those ordered before it by a CTA barrier) to a
+// thread whose acquire load then reads the sum.
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Order this thread's async-proxy (TMA) global writes, already complete,
+// before its later generic-proxy operations.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA / tensor core) accesses.
 __device__ __forceinline__ void fence_async_shared() {

@@ -268,14 +268,17 @@ def test_long_context(L, lens):
 # geometries (contiguous and 64-row pages), the CUDA-core kernels otherwise
 # ---------------------------------------------------------------------------
 
+# absorbed: one kernel for attention + merge + unembedding when the grid fits
+# on the GPU at once, else separate merge and unembedding kernels
+TC_ABSORBED_FUSED = {"fold_sm103", "absorbed_fused_sm103"}
 TC_ABSORBED = {"fold_sm103", "absorbed_attn_sm103", "merge_sm103", "unembed_sm103"}
 TC_MATERIALISED = {"expand_sm103", "mat_attn_sm103"}
 
 
 @pytest.mark.parametrize("mode,dtype,page,want", [
-    ("absorbed", torch.bfloat16, 0, TC_ABSORBED),
+    ("absorbed", torch.bfloat16, 0, TC_ABSORBED_FUSED),
     ("materialised", torch.bfloat16, 0, TC_MATERIALISED),
-    ("absorbed", torch.bfloat16, 64, TC_ABSORBED),
+    ("absorbed", torch.bfloat16, 64, TC_ABSORBED_FUSED),
     ("materialised", torch.bfloat16, 64, TC_MATERIALISED),
     ("materialised", torch.bfloat16, 16, {"generic_expand", "generic_materialised_attention",
                                           "generic_combine"}),
@@ -366,3 +369,31 @@ def test_prepared_call_runs_on_new_buffer_contents(mode, page):
     B.mla_device_status()
     case.q_nope, case.q_rope = other.q_nope, other.q_rope
     compare(call.out, oracle_out(case), torch.bfloat16, f"prepared {mode}, new queries")
+
+
+def test_kernel_routing_multi_wave_absorbed_is_unfused():
+    # 32 sequences of 2048 positions, 8 rows x 128 heads each: far more
+    # clusters than fit on the GPU at once, so merge and unembedding run as
+    # their own kernels
+    case = make_case(DSV3, 8, [2048] * 32, seed=72, page_size=64)
+    B.mla_kernel_timing_enable(True)
+    try:
+        B.mla_kernel_timing_read(reset=True)
+        out, _ = run_gpu(case, "absorbed")
+        ran = set(B.mla_kernel_timing_read(reset=True))
+    finally:
+        B.mla_kernel_timing_enable(False)
+    assert ran == TC_ABSORBED, ran
+    heads = [0, 77, 127]
+    compare(out[:, :, heads], oracle_out(case, heads=heads), torch.bfloat16, "multi-wave")
+
+
+@pytest.mark.parametrize("L,lens", [(1, [8192]), (16, [8192]), (32, [4096, 900]), (33, [2048])])
+def test_fused_and_unfused_agree_in_structure(L, lens):
+    # widths on both sides of the fused kernel's limit (32 rows per sequence)
+    case = make_case(Geometry(H=64, n=128, v=256), L, lens, seed=300 + L)
+    heads = [0, 31, 63]
+    rows = sample_indices(L, 4, L)
+    out, _ = run_gpu(case, "absorbed")
+    compare(out[:, rows][:, :, heads], oracle_out(case, heads=heads, rows=rows), torch.bfloat16,
+            f"fused-limit L={L}")
