@@ -361,10 +361,7 @@ __device__ __forceinline__ void fused_merge_unembed(const AttnParams& p, const C
         tma_load_2d(sW + j * kLat * 128 + kc * 8192, &tm_wuv, bar(B_WFULL), mt * 128 + 64 * j,
                     h * kLat + 64 * kc);
   };
-  if (threadIdx.x == 0) {
-    *stop = 0;
-    if (cid < units) load_w(cid);
-  }
+  if (threadIdx.x == 0 && cid < units) load_w(cid);
   // publish this CTA's pieces (its softmax threads fenced their writes and the
   // storing thread waited for its TMA stores before the barrier above), then
   // wait for the other CTAs of the sequence; the grid is resident as a whole,
@@ -373,17 +370,19 @@ __device__ __forceinline__ void fused_merge_unembed(const AttnParams& p, const C
     __threadfence();
     red_release_gpu_add(p.counters + b, 1u);
     const uint32_t target = (uint32_t)ncta;
+    int gave_up = 0;
     if (ld_acquire_gpu(p.counters + b) < target) {
       const long long t0 = clock64();
       while (ld_acquire_gpu(p.counters + b) < target) {
         if (clock64() - t0 > kWaitLimitCycles) {
           report_timeout(30);
-          *stop = 1;
+          gave_up = 1;
           break;
         }
         __nanosleep(32);
       }
     }
+    *stop = gave_up;  // (the only writer)
   }
   __syncthreads();
   const bool go = *stop == 0;
