@@ -201,6 +201,24 @@ mla_status_t mla_check_page_table(const int32_t* page_table_host, int32_t batch,
                                   int32_t max_pages_per_seq, const int32_t* cache_lens_host,
                                   int32_t page_size, int32_t num_pages);
 
+/* Draft cap from a measured verify-cost curve ("Draft caps and calibration",
+ * the cost model "in formula form, for a cap C", and "How mlx-dspark picks
+ * it"): returns the cap C in [0, limit] that maximises
+ *     speedup(C) = accepted(C) * verify(1) / (drafter(C) + verify(C + 1)),
+ *     accepted(C) = 1 + p + p^2 + ... + p^C,
+ * where verify(w) = verify_cost[w - 1] is the measured cost of one verify
+ * pass over w rows (any unit; verify(1) is one plain decode step, so costs
+ * count in single-token steps), drafter(C) = drafter_cost[0] for every C
+ * when n_drafter == 1, else drafter_cost[C].  C = 0 is plain decoding:
+ * speedup(0) = 1.  limit = min(max_cap, n_verify - 1, n_drafter - 1 when
+ * n_drafter > 1).  Ties go to the smaller cap.  speedup_out (host, may be
+ * NULL) receives speedup(0..limit).  Returns -1 on bad arguments (p outside
+ * [0, 1], a non-positive verify cost, a negative drafter cost, NULL arrays);
+ * mla_last_error() says which.  Pure host code, double precision. */
+int32_t mla_select_draft_cap(double p, const double* verify_cost, int32_t n_verify,
+                             const double* drafter_cost, int32_t n_drafter, int32_t max_cap,
+                             double* speedup_out);
+
 /* Per-kernel timing, for benchmarks.  While enabled, every kernel launch the
  * library makes is bracketed by a pair of CUDA events recorded on the call's
  * stream (events come from a library-owned pool; no device memory).  Do not

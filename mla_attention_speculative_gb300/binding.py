@@ -62,6 +62,7 @@ _SIGS = {
                                             _P, _P, _I32, _I32, _P, _I32, _I32, _I32, _P,
                                             _P, _P]),
     "mla_check_page_table": (_I32, [_P, _I32, _I32, _P, _I32, _I32]),
+    "mla_select_draft_cap": (_I32, [ctypes.c_double, _P, _I32, _P, _I32, _I32, _P]),
     "mla_kernel_timing_enable": (_I32, [_I32]),
     "mla_kernel_timing_read": (_I32, [ctypes.c_char_p, ctypes.c_size_t, _P, _P, _I32, _P,
                                       _I32]),
@@ -172,6 +173,24 @@ def mla_check_page_table(page_table, cache_lens: Sequence[int], page_size: int,
     lens = _lens_array(cache_lens)
     _check(lib().mla_check_page_table(t.data_ptr(), t.shape[0], t.shape[1], lens, int(page_size),
                                       int(num_pages)), "mla_check_page_table")
+
+
+def mla_select_draft_cap(p: float, verify_cost: Sequence[float], drafter_cost,
+                         max_cap: int):
+    """(best cap, [speedup(0), ..., speedup(limit)]) from a measured verify-cost
+    curve (verify_cost[w-1] = cost of a pass over w rows) and the drafter's
+    cost (one number, or one per cap)."""
+    dr = [float(drafter_cost)] if isinstance(drafter_cost, (int, float)) else \
+        [float(x) for x in drafter_cost]
+    vc = (ctypes.c_double * len(verify_cost))(*[float(x) for x in verify_cost])
+    dc = (ctypes.c_double * len(dr))(*dr)
+    n_out = max(1, min(int(max_cap), len(verify_cost) - 1) + 1)
+    sp = (ctypes.c_double * n_out)()
+    cap = lib().mla_select_draft_cap(float(p), vc, len(verify_cost), dc, len(dr), int(max_cap), sp)
+    if cap < 0:
+        raise MlaError(MLA_ERR_INVALID_ARG, "mla_select_draft_cap", mla_last_error())
+    limit = min(int(max_cap), len(verify_cost) - 1, len(dr) - 1 if len(dr) > 1 else 1 << 30)
+    return int(cap), [sp[i] for i in range(limit + 1)]
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:

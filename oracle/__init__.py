@@ -9,3 +9,4 @@ from .mla_oracle import (  # noqa: F401
     absorbed, brute_force, default_scale, gather_paged, materialised,
     max_absorbed_queries, max_absorbed_queries_batch, select_branch,
 )
+from .draft_cap import accepted, select_draft_cap  # noqa: F401
