@@ -93,9 +93,10 @@ def _work(kernel: str, L: int, T: int, H=128, r=512, n=128, v=128, rope=64):
     attend = (cache + rows * (r + rope) * bf + rows * r * bf,
               2 * rows * T * (r + rope) + 2 * rows * T * r)
     unembed = (H * r * v * bf + rows * r * bf + rows * v * bf, 2 * rows * r * v)
-    # attention, merge and unembedding in one kernel: no o_lat hand-off
-    fused = (cache + rows * (r + rope) * bf + H * r * v * bf + rows * v * bf,
-             attend[1] + unembed[1])
+    # the whole call in one kernel (fold, attention, merge, unembedding): no
+    # q_lat or o_lat hand-off
+    fused = (H * n * r * bf + rows * n * bf + cache + rows * rope * bf + H * r * v * bf
+             + rows * v * bf, fold[1] + attend[1] + unembed[1])
     table = {
         "absorbed_fused_sm103": fused,
         "generic_fold": fold,
@@ -181,7 +182,7 @@ def _bench_materialised(B, dev, peaks, reps):
         del c
         lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
         g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope, torch.bfloat16)
-        ws = torch.empty(B.mla_workspace_bytes(g, L, lens, mode), dtype=torch.uint8, device=dev)
+        ws = B.new_workspace(B.mla_workspace_bytes(g, L, lens, mode), dev)
         out = torch.empty((len(lens), L, geom.H, geom.v), dtype=torch.bfloat16, device=dev)
         br = {}
 
@@ -525,8 +526,7 @@ def run_ours(args):
         D.append(d)
     lens = [CACHE_LEN]
     lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
-    ws = {L: torch.empty(max(B.mla_workspace_bytes(g, L, lens, "auto"), 256),
-                         dtype=torch.uint8, device=dev) for L in WIDTHS}
+    ws = {L: B.new_workspace(B.mla_workspace_bytes(g, L, lens, "auto"), dev) for L in WIDTHS}
     outs = {L: torch.empty((1, L, geom.H, geom.v), dtype=torch.bfloat16, device=dev)
             for L in WIDTHS}
     q = [{L: (d["q_nope"][:, :L].contiguous(), d["q_rope"][:, :L].contiguous())

@@ -29,6 +29,11 @@
  * Conventions for every entry point:
  *  - Ownership: the caller owns every buffer.  The library allocates no
  *    device memory in these calls; scratch comes from the caller's workspace.
+ *  - Reads may start early: the kernels chain to the preceding kernel in the
+ *    stream by programmatic dependent launch, and they may start reading
+ *    W_UK, W_UV and the latent cache (never the queries, lengths or page
+ *    table) before a preceding kernel that allows it has finished; a kernel
+ *    that writes those buffers right before a call must not trigger early.
  *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
  *    default stream).  Calls are asynchronous on it; inputs must stay alive
  *    and unmodified until the stream reaches the call's kernels.
@@ -108,7 +113,14 @@ mla_status_t mla_select_branch(const mla_geometry_t* geom, int32_t L,
 
 /* Bytes of device workspace mla_verify_attention needs for this call
  * (branch-dependent: split-KV partials for the absorbed branch, the expanded
- * K_nope/V buffer for the materialised branch).  Host only. */
+ * K_nope/V buffer for the materialised branch).  Host only.
+ *
+ * Every workspace begins with a 512-byte header that must be zero before the
+ * first call that uses it; every call leaves it zero (the absorbed branch's
+ * single-kernel path keeps its cross-CTA arrival counters there).  Zero it
+ * once when the workspace is allocated (cudaMemsetAsync of 512 bytes).  The
+ * rest needs no initialisation.  If mla_device_status ever reports
+ * MLA_ERR_TIMEOUT, zero the header again before reusing the workspace. */
 mla_status_t mla_workspace_bytes(const mla_geometry_t* geom, int32_t batch, int32_t L,
                                  const int32_t* cache_lens_host, int32_t mode,
                                  size_t* bytes);
@@ -135,7 +147,8 @@ mla_status_t mla_workspace_bytes(const mla_geometry_t* geom, int32_t batch, int3
  *          [0, num_pages), or NULL for a contiguous cache
  *  out     device [batch, L, H, v] in the geometry's dtype
  *  workspace / workspace_bytes  device scratch of at least
- *          mla_workspace_bytes() bytes (may be NULL when that is 0)
+ *          mla_workspace_bytes() bytes, 256-byte aligned, whose first 512
+ *          bytes are zero (see mla_workspace_bytes)
  *  branch_taken  host, may be NULL; receives the mla_branch_t used
  */
 mla_status_t mla_verify_attention(

@@ -193,6 +193,17 @@ def mla_select_draft_cap(p: float, verify_cost: Sequence[float], drafter_cost,
     return int(cap), [sp[i] for i in range(limit + 1)]
 
 
+WORKSPACE_HEADER = 512
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A workspace of `nbytes` whose 512-byte header is zero, as the library
+    requires before a workspace's first call (the rest is left as allocated)."""
+    ws = torch.empty(max(int(nbytes), WORKSPACE_HEADER), dtype=torch.uint8, device=device)
+    ws[:WORKSPACE_HEADER].zero_()
+    return ws
+
+
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
@@ -266,8 +277,7 @@ def _verify_args(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, mode, out
     else:
         m = MODES.get(mode, mode)
         if workspace is None:  # (a given workspace that is too small is rejected by the call)
-            need = mla_workspace_bytes(geom, L, lens, m)
-            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+            workspace = new_workspace(mla_workspace_bytes(geom, L, lens, m), dev)
         args += [m, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size()]
     keep = (q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, page_table, cache_lens_dev, out, workspace)
     return args, out, dev, keep

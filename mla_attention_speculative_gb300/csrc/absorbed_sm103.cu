@@ -98,10 +98,6 @@ struct GemmParams {
   // 8 latent columns, each chunk 128 rows x 16 B, so a warp that loads one
   // chunk for its 32 rows reads 512 contiguous bytes.
   int L, ntile;
-  // the fused attention's per-sequence arrival counters, zeroed here once the
-  // preceding grid (which may still be using them) has completed
-  uint32_t* zero;
-  int nzero;
 };
 
 constexpr int GEMM_MAX_K = 512;
@@ -146,8 +142,6 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
                     h * K + 64 * kc);
     }
     pdl_wait();  // the activations may come from the preceding kernel
-    if (p.nzero > 0 && (blockIdx.x | blockIdx.y | blockIdx.z) == 0)
-      for (int i = 0; i < p.nzero; ++i) p.zero[i] = 0u;
     for (int kc = 0; kc < nk; ++kc)
       tma_load_2d(smem_u32(sB + kc * NB * 128), &tm_act, smem_u32(&bars[kc]), h * K + 64 * kc,
                   row0);
@@ -259,10 +253,18 @@ struct AttnParams {
   float* ml;              // [B, splits, R, 2]: (m, l) of each piece
   const char* pf;     // W_UV, pulled into L2 while the attention runs
   size_t pf_bytes;
-  // fused merge + unembedding only
-  uint32_t* counters;     // [B] CTAs of sequence b that have published their pieces
+  // fused kernel only: the fold before the attention, the merge and the
+  // unembedding after it
+  uint32_t* counters;     // workspace header: [0] CTAs past the fold, [1] CTAs
+                          // that have left, [2 + b] CTAs of sequence b that
+                          // have published their pieces (all zero between calls)
   __nv_bfloat16* out;     // [B, L, H, v]
+  __nv_bfloat16* q_lat_w; // the Q tiles the fold writes (same buffer as q_lat)
   int v;                  // value width, a multiple of 128
+  int n;                  // nope width (the fold's K), a multiple of 64
+  int BL;                 // B*L batch rows of the fold
+  int NBf, nrb;           // fold rows per unit (multiple of 16, <= 64), row blocks
+  int fstages, fsb;       // fold ring depth and stage bytes
 };
 
 // Barrier slots.  Every barrier that is waited on by parity alone has enough
@@ -270,8 +272,20 @@ struct AttnParams {
 enum {
   B_QFULL = 0, B_QTMEM = 1, B_KVFULL = 2, B_KVEMPTY = 6, B_SFULL = 10, B_SFREE = 12,
   B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22,
-  B_WFULL = 24, B_UDONE = 25, B_COUNT = 26
+  B_WFULL = 24, B_UDONE = 25,
+  // the fused kernel's fold: ring stages full / free, accumulator full / free, done
+  B_FFULL = 26, B_FEMPTY = 29, B_FACC = 32, B_FFREE = 34, B_FDONE = 36, B_COUNT = 37
 };
+
+// The fused kernel's fold ring lives over KV stages 2 and 3 and the P,
+// exchange and staging tiles (KV stages 0 and 1 hold the first two KV tiles,
+// loaded while the fold runs).
+constexpr int FOLD_BASE = OFF_KV + 2 * KV_STAGE;
+constexpr int FOLD_BYTES = OFF_RED - FOLD_BASE;
+constexpr int FOLD_MAX_STAGES = 3;
+static_assert(FOLD_BASE % 1024 == 0, "fold ring stages need 1 KiB alignment");
+// the widest fold stage (n = 256, 64 rows) fits at least once
+static_assert(2 * 256 * 128 + 4 * 64 * 128 <= FOLD_BYTES, "fold ring holds a stage");
 
 // One partial score of this CTA in log2-softmax units, rounded to fp16: the
 // exchange warps send exactly this to the peer and the softmax adds exactly
@@ -316,6 +330,133 @@ constexpr int XQUARTER = 32 * XROW * NWG;       // bytes per lane quarter
 __device__ __forceinline__ uint32_t xchg_offset(int wg, int q, int c) {
   const int sw = XCH == 4 ? ((q >> 1) & 3) : XCH == 2 ? ((q >> 2) & 1) : 0;
   return (uint32_t)((q >> 5) * XQUARTER + wg * (32 * XROW) + (q & 31) * XROW + ((c ^ sw) << 4));
+}
+
+// =========================================================================
+// fused fold (the first phase of the FUSED attention kernel)
+// =========================================================================
+// q_lat[row, h, :] = q_nope[row, h, :] . W_UK[h] for the B*L batch rows, as the
+// swap-AB GEMM above computes it, spread over every CTA of the attention's
+// grid: unit (h, mt, rb) is D[128 x NBf] = W_UK[h][:, 128 mt : 128 mt + 128]^T
+// x q_nope[rows of block rb, h, :]^T, units u = gid, gid + nctas, ...  Its
+// operands stream through a ring of fstages stages, its accumulator
+// alternates between two 64-column TMEM buffers (the S buffers, unused until
+// the attention starts), and the softmax warpgroups write it out in the
+// attention's Q-tile layout (warpgroup u & 1 takes unit u).
+struct FoldUnit {
+  int h, mt, rb;
+};
+__device__ __forceinline__ FoldUnit fold_unit(int u, int nrb) {
+  const int hm = u / nrb;
+  return {hm >> 2, hm & 3, u - hm * nrb};
+}
+__device__ __forceinline__ int fold_units_of(int units, int gid, int nctas) {
+  return units > gid ? (units - gid + nctas - 1) / nctas : 0;
+}
+
+// TMA producer of the fold: W_UK tiles (inputs the preceding kernel does not
+// write) are requested before the dependency wait, q_nope after it.  Returns
+// once every fold MMA has finished, so the ring's memory is free again.
+__device__ __forceinline__ void fold_produce(const AttnParams& p, const CUtensorMap& tm_wuk,
+                                             const CUtensorMap& tm_qn, uint32_t fold_base,
+                                             uint64_t* bars, int gid, int nctas) {
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int nk = p.n / 64;
+  const int nlocal = fold_units_of(p.H * 4 * p.nrb, gid, nctas);
+  const uint32_t a_bytes = 2u * p.n * 128, tx = (uint32_t)nk * (16384u + p.NBf * 128u);
+  auto load_w = [&](int k) {
+    const FoldUnit f = fold_unit(gid + k * nctas, p.nrb);
+    const uint32_t st = fold_base + (k % p.fstages) * p.fsb;
+    const uint32_t fb = bar(B_FFULL + k % p.fstages);
+    mbar_arrive_expect_tx(fb, tx);
+    for (int kc = 0; kc < nk; ++kc)
+      for (int j = 0; j < 2; ++j)
+        tma_load_2d(st + j * p.n * 128 + kc * 8192, &tm_wuk, fb, f.mt * 128 + 64 * j,
+                    f.h * p.n + 64 * kc);
+  };
+  auto load_q = [&](int k) {
+    const FoldUnit f = fold_unit(gid + k * nctas, p.nrb);
+    const uint32_t st = fold_base + (k % p.fstages) * p.fsb + a_bytes;
+    for (int kc = 0; kc < nk; ++kc)
+      tma_load_2d(st + kc * p.NBf * 128, &tm_qn, bar(B_FFULL + k % p.fstages),
+                  f.h * p.n + 64 * kc, f.rb * p.NBf);
+  };
+  prefetch_tmap(&tm_wuk);
+  const int first = min(nlocal, p.fstages);
+  for (int k = 0; k < first; ++k) load_w(k);
+  pdl_wait();  // q_nope may come from the preceding kernel
+  for (int k = 0; k < first; ++k) load_q(k);
+  bool ok = true;
+  for (int k = first; k < nlocal; ++k) {
+    wait_or_fail(ok, bar(B_FEMPTY + k % p.fstages), ((k / p.fstages) - 1) & 1, 40);
+    if (!ok) break;
+    load_w(k);
+    load_q(k);
+  }
+  // every fold MMA is done (and so every load it consumed has landed)
+  mbar_wait(bar(B_FDONE), 0);
+}
+
+// MMA issuer of the fold.
+__device__ __forceinline__ void fold_mma(const AttnParams& p, uint32_t fold_base, uint32_t tmem,
+                                         uint64_t* bars, int gid, int nctas) {
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int nk = p.n / 64;
+  const int nlocal = fold_units_of(p.H * 4 * p.nrb, gid, nctas);
+  const uint32_t idesc = idesc_bf16(128, p.NBf, 1, 0);
+  bool ok = true;
+  for (int k = 0; k < nlocal && ok; ++k) {
+    const int s = k % p.fstages, buf = k & 1;
+    wait_or_fail(ok, bar(B_FFULL + s), (k / p.fstages) & 1, 41);
+    if (k >= 2) wait_or_fail(ok, bar(B_FFREE + buf), ((k - 2) >> 1) & 1, 42);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t sa = fold_base + s * p.fsb, sb = sa + 2 * p.n * 128;
+    for (int kc = 0; kc < nk; ++kc)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + TM_S + buf * 64,
+                 sdesc_sw128(sa + (kc * 64 + ks * 16) * 128, p.n * 128, 1024),
+                 sdesc_sw128(sb + kc * p.NBf * 128 + ks * 32, 16, 1024), idesc, (kc | ks) != 0);
+    mma_commit(bar(B_FEMPTY + s));
+    mma_commit(bar(B_FACC + buf));
+  }
+  mma_commit(bar(B_FDONE));  // (also when no unit was issued)
+}
+
+// Epilogue of the fold, one softmax warpgroup per unit parity: q_lat in bf16,
+// in the attention's Q-tile layout.
+__device__ __forceinline__ void fold_store(const AttnParams& p, uint32_t tmem, uint64_t* bars,
+                                           int gid, int nctas, int wg, int warp, int lane) {
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int nlocal = fold_units_of(p.H * 4 * p.nrb, gid, nctas);
+  const int q = (warp & 3) * 32 + lane;  // TMEM lane = latent column within the unit's 128
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  bool ok = true;
+  for (int k = wg; k < nlocal; k += 2) {
+    const FoldUnit f = fold_unit(gid + k * nctas, p.nrb);
+    wait_or_fail(ok, bar(B_FACC + (k & 1)), (k >> 1) & 1, 43);
+    tc_fence_after();
+    if (ok) {
+      const int m = f.mt * 128 + q;
+      for (int c0 = 0; c0 < p.NBf; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_base + TM_S + (k & 1) * 64 + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int row = f.rb * p.NBf + c0 + i;  // batch row b*L + l
+          if (row >= p.BL) continue;
+          const int b = row / p.L, r = (row - b * p.L) * p.H + f.h;
+          const size_t idx =
+              ((((size_t)b * p.rtiles + (r >> 7)) * 64 + (m >> 3)) * 128 + (r & 127)) * 8 + (m & 7);
+          p.q_lat_w[idx] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(bar(B_FFREE + (k & 1)));
+  }
 }
 
 // 8 bf16 (one 16-byte load) to fp32.
@@ -368,12 +509,12 @@ __device__ __forceinline__ void fused_merge_unembed(const AttnParams& p, const C
   // so they all get here, and the wait is bounded anyway
   if (threadIdx.x == 96) {
     __threadfence();
-    red_release_gpu_add(p.counters + b, 1u);
+    red_release_gpu_add(p.counters + 2 + b, 1u);
     const uint32_t target = (uint32_t)ncta;
     int gave_up = 0;
-    if (ld_acquire_gpu(p.counters + b) < target) {
+    if (ld_acquire_gpu(p.counters + 2 + b) < target) {
       const long long t0 = clock64();
-      while (ld_acquire_gpu(p.counters + b) < target) {
+      while (ld_acquire_gpu(p.counters + 2 + b) < target) {
         if (clock64() - t0 > kWaitLimitCycles) {
           report_timeout(30);
           gave_up = 1;
@@ -545,7 +686,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
                         const __grid_constant__ CUtensorMap tm_ckv,
                         const __grid_constant__ CUtensorMap tm_kr,
                         const __grid_constant__ CUtensorMap tm_op,
-                        const __grid_constant__ CUtensorMap tm_wuv, AttnParams p) {
+                        const __grid_constant__ CUtensorMap tm_wuv,
+                        const __grid_constant__ CUtensorMap tm_wuk,
+                        const __grid_constant__ CUtensorMap tm_qn, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t rank = cluster_ctarank();
@@ -586,6 +729,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     mbar_init(bar(B_DRAIN + 1), 1);
     mbar_init(bar(B_WFULL), 1);
     mbar_init(bar(B_UDONE), 1);
+    if constexpr (FUSED) {
+      for (int k = 0; k < FOLD_MAX_STAGES; ++k) {
+        mbar_init(bar(B_FFULL + k), 1);
+        mbar_init(bar(B_FEMPTY + k), 1);
+      }
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(bar(B_FACC + k), 1);
+        mbar_init(bar(B_FFREE + k), 128);
+      }
+      mbar_init(bar(B_FDONE), 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(slot), 512);
@@ -594,16 +748,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *slot;
   const int nsplit = (T + p.chunk - 1) / p.chunk;
-  if (split >= nsplit) {  // both CTAs of the cluster leave together, the peer untouched
+  // A CTA whose piece lies past its sequence's end has no attention to do.
+  // Both CTAs of a cluster share the piece, so they leave (or, in the fused
+  // kernel, skip the attention) together and never touch the peer.
+  const bool active = split < nsplit;
+  if (!FUSED && !active) {
     if (warp == 1) tmem_dealloc(tmem, 512);
     return;
   }
+  const int gid = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  const int nctas = gridDim.x * gridDim.y * gridDim.z;
+  const uint32_t fold_base = smem_u32(smem + FOLD_BASE);
   const int row0 = tile * BM;
   const int l_last = min(p.R - 1, row0 + BM - 1) / p.H;
   const int vis_end = T - p.L + l_last + 1;
   const int kv0 = split * p.chunk;
   const int kv1 = min(min(kv0 + p.chunk, T), vis_end);
-  const int ntiles = kv1 > kv0 ? (kv1 - kv0 + BN - 1) / BN : 0;
+  const int ntiles = active && kv1 > kv0 ? (kv1 - kv0 + BN - 1) / BN : 0;
   // arm the exchange barriers for tiles 0 and 1 (the peer's bulk copies count
   // them down), then publish the setup to the peer: each role waits for the
   // peer's setup only before its first access to the peer, so the KV loads,
@@ -612,12 +773,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
     if (ntiles > 1) mbar_arrive_expect_tx(bar(B_XFULL + 1), X_BYTES);
   }
-  cluster_arrive();
-  pdl_launch_dependents();  // the merge may launch; it waits for this grid
+  if (active) cluster_arrive();
+  pdl_launch_dependents();  // the next kernel may launch; it waits for this grid
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0) {
       bool ok = true;
       prefetch_tmap(&tm_ckv);
       const int qrow = b * p.R + row0;
@@ -645,38 +806,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
                       (int)y);
         tma_load_2d(st + 4 * KV_CHUNK, &tm_kr, bar(B_KVFULL + s), (int)rank * 32, (int)y);
       };
-      // the cache does not depend on the preceding kernel: start every stage now
+      // the cache does not depend on the preceding kernel: start every stage
+      // now -- in the fused kernel the first two, with the fold's operands in
+      // the other two (they follow once the fold is done)
       const int pre = min(ntiles, STAGES);
-      for (int i = 0; i < pre; ++i) load_kv(i);
-      // q_rope is a call input; it still waits so no read overtakes the predecessor
-      pdl_wait();
-      mbar_arrive_expect_tx(bar(B_QFULL), Q_ROPE);
-      tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
-      // The unembedding weights are read right after this kernel; at verify
-      // widths the attention leaves HBM mostly idle, so each CTA pulls a slice
-      // into L2 -- once its own first KV tiles have landed, so that the two do
-      // not share the HBM bandwidth the first tiles wait for.
-      if (p.pf != nullptr) {
-        mbar_wait(bar(B_KVFULL + (pre - 1) % STAGES), 0);
-        const size_t nct = (size_t)gridDim.x * gridDim.y * gridDim.z;
-        const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-        const size_t slice = ((p.pf_bytes + nct - 1) / nct + 4095) & ~(size_t)4095;
-        for (size_t o = id * slice; o < min(p.pf_bytes, (id + 1) * slice); o += 32768)
-          prefetch_l2(p.pf + o, (uint32_t)min((size_t)32768, p.pf_bytes - o));
+      int started = 0;
+      if constexpr (FUSED) {
+        started = min(ntiles, 2);
+        for (int i = 0; i < started; ++i) load_kv(i);
+        fold_produce(p, tm_wuk, tm_qn, fold_base, bars, gid, nctas);
       }
-      int issued = pre;
-      for (int i = STAGES; i < ntiles; ++i) {
-        wait_or_fail(ok, bar(B_KVEMPTY + i % STAGES), ((i / STAGES) - 1) & 1, 10);
-        if (!ok) break;
-        load_kv(i);
-        issued = i + 1;
+      if (ntiles > 0) {
+        for (int i = started; i < pre; ++i) load_kv(i);
+        // q_rope is a call input; it still waits so no read overtakes the predecessor
+        pdl_wait();
+        mbar_arrive_expect_tx(bar(B_QFULL), Q_ROPE);
+        tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
+        // The unembedding weights are read right after this kernel; at verify
+        // widths the attention leaves HBM mostly idle, so each CTA pulls a slice
+        // into L2 -- once its own first KV tiles have landed, so that the two do
+        // not share the HBM bandwidth the first tiles wait for.
+        if (p.pf != nullptr) {
+          mbar_wait(bar(B_KVFULL + (pre - 1) % STAGES), 0);
+          const size_t nct = (size_t)gridDim.x * gridDim.y * gridDim.z;
+          const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+          const size_t slice = ((p.pf_bytes + nct - 1) / nct + 4095) & ~(size_t)4095;
+          for (size_t o = id * slice; o < min(p.pf_bytes, (id + 1) * slice); o += 32768)
+            prefetch_l2(p.pf + o, (uint32_t)min((size_t)32768, p.pf_bytes - o));
+        }
+        int issued = pre;
+        for (int i = STAGES; i < ntiles; ++i) {
+          wait_or_fail(ok, bar(B_KVEMPTY + i % STAGES), ((i / STAGES) - 1) & 1, 10);
+          if (!ok) break;
+          load_kv(i);
+          issued = i + 1;
+        }
+        // nothing this thread started may still be landing when the CTA exits
+        mbar_wait(bar(B_QFULL), 0);
+        for (int i = max(issued - STAGES, 0); i < issued; ++i)
+          mbar_wait(bar(B_KVFULL + i % STAGES), (i / STAGES) & 1);
       }
-      // nothing this thread started may still be landing when the CTA exits
-      mbar_wait(bar(B_QFULL), 0);
-      for (int i = max(issued - STAGES, 0); i < issued; ++i)
-        mbar_wait(bar(B_KVFULL + i % STAGES), (i / STAGES) & 1);
     }
-    cluster_wait();  // (this role never touches the peer)
+    if (active) cluster_wait();  // (this role never touches the peer)
   } else if (warp == 1) {
     // ------------------------------------------------------- score-MMA issuer
     // S(i) = Q . K(i)^T over this CTA's 256 latent (Q from TMEM) + 32 RoPE
@@ -684,6 +855,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // The scores run ahead of the softmax on their own; P.V comes from another
     // warp (MMA issue is nearly synchronous, so a wait in one issuer leaves
     // the tensor pipe to the other).
+    if constexpr (FUSED) {
+      if (lane == 0) fold_mma(p, fold_base, tmem, bars, gid, nctas);
+    }
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
       const uint64_t dqr = sdesc_sw64(sQR, 512);
@@ -712,7 +886,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0);
     }
-    cluster_wait();
+    if (active) cluster_wait();
   } else if (warp == 2) {
     // --------------------------------------------------------- P.V issuer
     // O += P(j) . V(j) over this CTA's 256 latent columns of the KV tile; the
@@ -737,13 +911,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mma_commit(bar(B_DRAIN + 1));
       mbar_wait(bar(B_DRAIN + 1), 0);
     }
-    cluster_wait();
+    if (active) cluster_wait();
   } else if (warp >= XCHG_WARP0) {
     // ------------------------------------------------------- score exchange
     // One warp per TMEM lane quarter ships this CTA's partial scores of each
     // tile to the peer as soon as the score MMAs finish, up to two tiles ahead
     // of the softmax, so the softmax's own steps never wait on a copy.
-    cluster_wait();  // the peer's exchange barriers are set up
+    if (active) cluster_wait();  // the peer's exchange barriers are set up
     if (ntiles > 0) {
       bool ok = true;
       const int quarter = warp & 3;
@@ -817,6 +991,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     int armed = min(ntiles, 2), received = 0;  // exchange phases armed / completed
     float m_run = -INFINITY, l_part = 0.f;
     float s[CPT];
+    if constexpr (FUSED) {
+      // the fold's epilogue (after the dependency wait: the previous call may
+      // still read its Q tiles), then every CTA of the grid must be past it
+      // before any reads the Q tiles
+      pdl_wait();
+      fold_store(p, tmem, bars, gid, nctas, wg, warp, lane);
+      __threadfence();
+      named_bar_sync(1, SOFTMAX_THREADS);
+      if (sm_tid == 0) {
+        red_release_gpu_add(p.counters, 1u);
+        if (active && ld_acquire_gpu(p.counters) < (uint32_t)nctas) {
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(p.counters) < (uint32_t)nctas) {
+            if (clock64() - t0 > kWaitLimitCycles) {
+              report_timeout(44);
+              break;
+            }
+            __nanosleep(32);
+          }
+        }
+      }
+      named_bar_sync(1, SOFTMAX_THREADS);
+    }
     if (ntiles > 0) {
       // this CTA's latent query columns into TMEM as bf16 pairs (the fold wrote them)
       pdl_wait();
@@ -830,7 +1027,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         uint32_t v[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint4 x = src[(size_t)(8 * k + u) * 128];
+          // (L2 reads: in the fused kernel other CTAs wrote these in this grid)
+          const uint4 x = __ldcg(src + (size_t)(8 * k + u) * 128);
           v[4 * u] = x.x;
           v[4 * u + 1] = x.y;
           v[4 * u + 2] = x.z;
@@ -843,7 +1041,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_arrive(bar(B_QTMEM));
       load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
     }
-    cluster_wait();  // the peer's barriers are set up before the first remote arrive
+    if (active) cluster_wait();  // the peer's barriers are set up before the first remote arrive
     // One tile of the softmax; `s` holds tile i's own (rounded) partial on
     // entry and tile i+1's on exit (read once P(i) is out, so only one tile's
     // scores are ever live in registers).
@@ -960,6 +1158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       for (int j = received; j < armed; ++j)
         mbar_wait_cluster(bar(B_XFULL + (j & 1)), (j >> 1) & 1);
     // ---------------------------------------------------------------- epilogue
+    if (active) {
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
     pdl_wait();  // the partials may still be read by the previous call's merge
     tc_fence_after();
@@ -1027,17 +1226,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mlp[1] = l_tot;
     }
     if constexpr (FUSED) __threadfence();
+    }
   }
   if constexpr (FUSED) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    fused_merge_unembed(p, tm_wuv, smem, tmem, bars, b, split, nsplit);
+    if (active) fused_merge_unembed(p, tm_wuv, smem, tmem, bars, b, split, nsplit);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 512);
-  cluster_sync();  // no peer access may outlive this CTA
+  if (active) cluster_sync();  // no peer access may outlive this CTA
+  if constexpr (FUSED) {
+    // The last CTA of the grid to leave puts the counters back to zero for
+    // the next call (every other CTA is past every wait by then).
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(p.counters + 1, 1u) == (uint32_t)nctas - 1) {
+        p.counters[0] = 0u;
+        p.counters[1] = 0u;
+        for (int i = 0; i < p.B; ++i) p.counters[2 + i] = 0u;
+        __threadfence();
+      }
+    }
+  }
 }
 
 // =========================================================================
@@ -1347,10 +1560,17 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   const DeviceSetup& ds = device_setup();
   if (ds.err != cudaSuccess) return ds.err;
   cudaError_t e;
-  {
-    GemmParams gp{q_lat, BL, p.H, p.n, kLat, NBf, p.L, (R + BM - 1) / BM,
-                  p.fused ? (uint32_t*)(a.ws + p.off_cnt) : nullptr, p.fused ? p.B : 0};
+  // the fused kernel folds the queries itself, in units of at most 64 rows
+  const int NBq = ((BL + 15) / 16) * 16 > 64 ? 64 : ((BL + 15) / 16) * 16;
+  const int fsb = (2 * p.n * 128 + (p.n / 64) * NBq * 128 + 1023) & ~1023;
+  CUtensorMap tm_qn_fused;
+  if (p.fused) {
+    if (!make_tmap_bf16_2d(&tm_qn_fused, a.q_nope, (uint64_t)p.H * p.n, BL,
+                           (uint64_t)p.H * p.n * 2, 64, NBq, 128))
+      return cudaErrorInvalidValue;
+  } else {
     KernelTimer kt("fold_sm103", a.stream);
+    GemmParams gp{q_lat, BL, p.H, p.n, kLat, NBf, p.L, (R + BM - 1) / BM};
     e = launch_pdl(swapab_gemm_sm103, dim3(kLat / 128, p.H, (BL + NBf - 1) / NBf), dim3(128),
                    gemm_smem(p.n, NBf), a.stream, tm_wuk, tm_qn, gp);
     if (e != cudaSuccess) return e;
@@ -1378,18 +1598,25 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.pf_bytes = (size_t)p.H * kLat * p.v * 2;
     ap.counters = (uint32_t*)(a.ws + p.off_cnt);
     ap.out = (__nv_bfloat16*)a.out;
+    ap.q_lat_w = q_lat;
     ap.v = p.v;
+    ap.n = p.n;
+    ap.BL = BL;
+    ap.NBf = NBq;
+    ap.nrb = (BL + NBq - 1) / NBq;
+    ap.fsb = fsb;
+    ap.fstages = FOLD_BYTES / fsb < FOLD_MAX_STAGES ? FOLD_BYTES / fsb : FOLD_MAX_STAGES;
     const dim3 grid(2 * ((R + BM - 1) / BM), p.splits, p.B);
     if (p.fused) {
       KernelTimer kt("absorbed_fused_sm103", a.stream);
       e = launch_pdl(absorbed_attn_sm103<true>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
-                     tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, ap);
+                     tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, tm_wuk, tm_qn_fused, ap);
       if (e != cudaSuccess) return e;
       return cudaGetLastError();
     }
     KernelTimer kt("absorbed_attn_sm103", a.stream);
     e = launch_pdl(absorbed_attn_sm103<false>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
-                   tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, ap);
+                   tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, tm_wuk, tm_qn, ap);
     if (e != cudaSuccess) return e;
   }
   {
@@ -1407,7 +1634,7 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     if (e != cudaSuccess) return e;
   }
   {
-    GemmParams gp{(__nv_bfloat16*)a.out, BL, p.H, kLat, p.v, NBu, 0, 0, nullptr, 0};
+    GemmParams gp{(__nv_bfloat16*)a.out, BL, p.H, kLat, p.v, NBu, 0, 0};
     KernelTimer kt("unembed_sm103", a.stream);
     e = launch_pdl(swapab_gemm_sm103, dim3(p.v / 128, p.H, (BL + NBu - 1) / NBu), dim3(128),
                    gemm_smem(kLat, NBu), a.stream, tm_wuv, tm_ol, gp);

@@ -204,7 +204,7 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     g.chunk = (int)chunk;
     g.splits = (int)((p->Tmax + chunk - 1) / chunk);
     const int dv = p->branch == MLA_BRANCH_ABSORBED ? p->r : p->v;
-    size_t off = 0;
+    size_t off = kWorkspaceHeader;
     if (p->branch == MLA_BRANCH_ABSORBED) {
       g.off_qlat = off;
       off = align256(off + nrow * p->r * sizeof(float));
@@ -226,8 +226,8 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     SplitPlan& f = p->fast;
     f.chunk = p->Tmax;
     f.splits = 1;
-    f.off_exp = 0;
-    f.bytes = align256(fast_materialised_workspace(*p));
+    f.off_exp = kWorkspaceHeader;
+    f.bytes = align256(kWorkspaceHeader + fast_materialised_workspace(*p));
   } else if (p->fast_ok) {
     // Tensor-core split-KV: clusters of 2 CTAs, one per (128-row tile, piece).
     // Pick the piece length ct (in 64-row KV tiles) that minimises
@@ -252,7 +252,8 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     }
     f.chunk = (int)(best_ct * 64);
     f.splits = (int)((p->Tmax + f.chunk - 1) / f.chunk);
-    size_t off = 0;
+    f.off_cnt = 0;  // the fused kernel's counters, in the zeroed header
+    size_t off = kWorkspaceHeader;
     f.off_qlat = off;  // Q tiles: every sequence's rows padded to 128-row tiles
     off = align256(off + (size_t)batch * row_tiles * 128 * p->r * 2);
     f.off_opart = off;  // bf16 O / l of every piece
@@ -261,15 +262,14 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     off = align256(off + nrow * f.splits * 2 * sizeof(float));
     f.off_olat = off;
     off = align256(off + nrow * p->r * 2);
-    f.off_cnt = off;  // per-sequence arrival counters of the fused kernel
-    off = align256(off + (size_t)batch * sizeof(uint32_t));
     f.bytes = off;
-    // One kernel for attention, merge and unembedding when every cluster of
-    // the grid is on the GPU at once (each sequence's CTAs wait for one
-    // another before merging) and the verify block is narrow enough.
-    int64_t clusters = 0;
-    for (int b = 0; b < batch; ++b) clusters += row_tiles * ((lens[b] + f.chunk - 1) / f.chunk);
-    p->fused = clusters <= slots && L <= kFusedMaxL;
+    // One kernel for the whole call (fold, attention, merge, unembedding)
+    // when every cluster of its grid is on the GPU at once -- its CTAs wait
+    // for one another after the fold and before the merge -- the verify block
+    // is narrow enough, and the header holds the counters.
+    const int64_t clusters = row_tiles * f.splits * batch;
+    p->fused = clusters <= slots && L <= kFusedMaxL &&
+               (size_t)(2 + batch) * sizeof(uint32_t) <= kWorkspaceHeader;
   }
   p->ws_bytes = p->fast_ok && p->fast.bytes > p->generic.bytes ? p->fast.bytes : p->generic.bytes;
   p->use(p->generic);

@@ -56,8 +56,12 @@ struct Plan {
   }
 };
 
-// Widest verify block the fused absorbed kernel merges and unembeds itself.
+// Widest verify block the fused absorbed kernel handles.
 constexpr int kFusedMaxL = 32;
+// Every workspace starts with this many bytes that must be zero before its
+// first call and that every call leaves zero (the fused absorbed kernel's
+// arrival counters live there).
+constexpr size_t kWorkspaceHeader = 512;
 
 // Device-side view of the cache addressing shared by all kernels.
 struct CacheView {

@@ -202,8 +202,9 @@ def test_dominant_key_dsv3_T8192(L):
     (Geometry(H=40), 5, [700]),            # 200 rows: second Q tile mostly padding
 ])
 def test_nan_poisoned_workspace(geom, L, lens):
-    # the workspace starts as all-ones bytes (NaN in bf16 and fp32): padded
-    # query rows and any scratch read before it is written must not leak
+    # the workspace starts as all-ones bytes (NaN in bf16 and fp32) past its
+    # zeroed header: padded query rows and any scratch read before it is
+    # written must not leak
     case = make_case(geom, L, lens, seed=220 + L)
     want = oracle_out(case)
     d = device_tensors(case)
@@ -211,6 +212,7 @@ def test_nan_poisoned_workspace(geom, L, lens):
         g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope)
         need = B.mla_workspace_bytes(g, L, lens, mode)
         ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+        ws[:B.WORKSPACE_HEADER].zero_()
         out, branch = run_gpu(case, mode, dev_t=d, workspace=ws)
         _check_branch(case, mode, branch)
         compare(out, want, torch.bfloat16, f"nan workspace {mode}")
@@ -268,9 +270,9 @@ def test_long_context(L, lens):
 # geometries (contiguous and 64-row pages), the CUDA-core kernels otherwise
 # ---------------------------------------------------------------------------
 
-# absorbed: one kernel for attention + merge + unembedding when the grid fits
-# on the GPU at once, else separate merge and unembedding kernels
-TC_ABSORBED_FUSED = {"fold_sm103", "absorbed_fused_sm103"}
+# absorbed: one kernel for fold + attention + merge + unembedding when the
+# grid fits on the GPU at once, else separate fold, merge and unembedding
+TC_ABSORBED_FUSED = {"absorbed_fused_sm103"}
 TC_ABSORBED = {"fold_sm103", "absorbed_attn_sm103", "merge_sm103", "unembed_sm103"}
 TC_MATERIALISED = {"expand_sm103", "mat_attn_sm103"}
 
@@ -397,3 +399,32 @@ def test_fused_and_unfused_agree_in_structure(L, lens):
     out, _ = run_gpu(case, "absorbed")
     compare(out[:, rows][:, :, heads], oracle_out(case, heads=heads, rows=rows), torch.bfloat16,
             f"fused-limit L={L}")
+
+
+def test_repeated_fused_calls_leave_the_header_zero():
+    # the fused kernel's arrival counters are back at zero after every call,
+    # so one workspace serves call after call (graph replays included)
+    case = make_case(Geometry(H=32), 4, [3000], seed=310)
+    d = device_tensors(case)
+    g = B.make_geometry(32, 512, 128, 128, 64)
+    ws = B.new_workspace(B.mla_workspace_bytes(g, 4, [3000], "absorbed"), "cuda")
+    want = oracle_out(case)
+    for _ in range(3):
+        out, _ = run_gpu(case, "absorbed", dev_t=d, workspace=ws)
+        assert int(ws[:B.WORKSPACE_HEADER].count_nonzero()) == 0
+        compare(out, want, torch.bfloat16, "repeated fused")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        run_gpu(case, "absorbed", dev_t=d, workspace=ws)     # warm-up on the capture stream
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            out2, _ = B.mla_verify_attention(d["q_nope"], d["q_rope"], d["c_kv"], d["k_rope"],
+                                             d["W_UK"], d["W_UV"], case.cache_lens,
+                                             mode="absorbed", workspace=ws,
+                                             cache_lens_dev=d["lens_dev"])
+    for _ in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        B.mla_device_status()
+        assert int(ws[:B.WORKSPACE_HEADER].count_nonzero()) == 0
+        compare(out2, want, torch.bfloat16, "fused graph replay")
