@@ -232,6 +232,56 @@ int32_t mla_select_draft_cap(double p, const double* verify_cost, int32_t n_veri
                              const double* drafter_cost, int32_t n_drafter, int32_t max_cap,
                              double* speedup_out);
 
+/* ------------------------------------------------------------------------
+ * Speculative-rollback state maintenance ("Over 107tok/s Qwen3.8-Flash-Next
+ * on M3 Ultra").  Element i of row (h, q) of a strided buffer sits at word
+ * i*strides[0] + h*strides[1] + q*strides[2] (non-negative strides, in
+ * 32-bit words); words are copied as bit patterns.
+ * ------------------------------------------------------------------------ */
+
+/* One snapshot window: the s words of the concatenated row starting at
+ * window_start go to cache[cache_offset + q*sequence_stride + h*s + i]. */
+typedef struct {
+  int32_t window_start;
+  int64_t cache_offset;
+  int64_t sequence_stride;
+} mla_snapshot_window_t;
+
+/* Section "A later extension: load snapshot history once", Algorithms 4 and
+ * 5: X = S || T row by row (S: s state words, T: n new words per row; H
+ * channels, Q sequences; 1 <= s <= 8, 1 <= n, s + n <= 16) and the k <= 8
+ * snapshot windows of X into `cache` (cache_words words long).  All buffers
+ * are device memory.  When 2 <= k <= 8 and the windows' destinations are
+ * pairwise disjoint and lie outside S, T and X, one kernel loads each row
+ * once and writes X and every window from that load (*fused_out = 1);
+ * otherwise the ordinary path runs: X, then one copy per window that reads X
+ * back (*fused_out = 0; the windows are written in order).  A window outside
+ * the row or a destination outside the cache is MLA_ERR_INVALID_ARG.
+ * Asynchronous on `stream`.  fused_out is host memory and may be NULL. */
+mla_status_t mla_concat_snapshots(const uint32_t* S, const int64_t* s_strides, const uint32_t* T,
+                                  const int64_t* t_strides, uint32_t* X,
+                                  const int64_t* x_strides, int32_t s, int32_t n, int32_t H,
+                                  int32_t Q, uint32_t* cache, int64_t cache_words,
+                                  const mla_snapshot_window_t* windows, int32_t k, void* stream,
+                                  int32_t* fused_out);
+
+/* Section "Keep the pooled keys; score them again", ValidBlock and Algorithm
+ * 1: how many leading pooled blocks of ratio r survive a rollback that
+ * removes positions from p0 on.  blocks: device [n_blocks, 8 + r] int32 rows
+ * {stream, start, n_src, key_cell, pos[0..3], src_cell[0..r)}; cell_pos:
+ * device [n_cells] logical positions (negative: empty cell); cell_seq:
+ * device [n_cells] owner bit masks (bit q: sequence q).  A block is valid
+ * when n_src == r, stream == 0, start >= 0, start + r <= p0, key_cell is one
+ * of its source cells, all four pos[] equal start, and source cell i is in
+ * [0, n_cells), live, owned by sequence 0 alone and at position start + i.
+ * *prefix_out (device int32) receives the index of the first invalid block
+ * (n_blocks when all are valid), or 0 when a global guard fails: n_streams
+ * != 1, seq != 0, p0 < 0, or a bounded removal (p1 >= 0).  Asynchronous. */
+mla_status_t mla_rollback_valid_prefix(const int32_t* blocks, int32_t n_blocks, int32_t r,
+                                       const int32_t* cell_pos, const uint64_t* cell_seq,
+                                       int32_t n_cells, int32_t p0, int32_t p1, int32_t seq,
+                                       int32_t n_streams, int32_t* prefix_out, void* stream);
+
 /* Per-kernel timing, for benchmarks.  While enabled, every kernel launch the
  * library makes is bracketed by a pair of CUDA events recorded on the call's
  * stream (events come from a library-owned pool; no device memory).  Do not

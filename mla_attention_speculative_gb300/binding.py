@@ -63,6 +63,10 @@ _SIGS = {
                                             _P, _P]),
     "mla_check_page_table": (_I32, [_P, _I32, _I32, _P, _I32, _I32]),
     "mla_select_draft_cap": (_I32, [ctypes.c_double, _P, _I32, _P, _I32, _I32, _P]),
+    "mla_concat_snapshots": (_I32, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64, _P,
+                                    _I32, _P, _P]),
+    "mla_rollback_valid_prefix": (_I32, [_P, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                                         _P, _P]),
     "mla_kernel_timing_enable": (_I32, [_I32]),
     "mla_kernel_timing_read": (_I32, [ctypes.c_char_p, ctypes.c_size_t, _P, _P, _I32, _P,
                                       _I32]),
@@ -202,6 +206,55 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
     ws = torch.empty(max(int(nbytes), WORKSPACE_HEADER), dtype=torch.uint8, device=device)
     ws[:WORKSPACE_HEADER].zero_()
     return ws
+
+
+class SnapshotWindow(ctypes.Structure):
+    _fields_ = [("window_start", ctypes.c_int32), ("cache_offset", ctypes.c_int64),
+                ("sequence_stride", ctypes.c_int64)]
+
+
+def _words(t: torch.Tensor) -> torch.Tensor:
+    """A 32-bit tensor seen as uint32 words (no copy)."""
+    if t.element_size() != 4:
+        raise ValueError("snapshot buffers hold 32-bit words")
+    return t
+
+
+def mla_concat_snapshots(S, s_strides, T, t_strides, X, x_strides, s: int, n: int, H: int,
+                         Q: int, cache, windows, stream=None) -> bool:
+    """Concatenate S || T into X and write the snapshot windows into `cache`
+    (flat 32-bit device tensors; strides in words).  windows: list of
+    (window_start, cache_offset, sequence_stride).  Returns True when the
+    fused single-load kernel ran, False for the ordinary path."""
+    for t in (S, T, X, cache):
+        _words(t)
+    arr = (SnapshotWindow * max(1, len(windows)))(*[SnapshotWindow(*w) for w in windows])
+    st = lambda v: (ctypes.c_int64 * 3)(*[int(x) for x in v])
+    if stream is None:
+        stream = _current_stream(X.device)
+    fused = ctypes.c_int32(0)
+    _check(lib().mla_concat_snapshots(_ptr(S), st(s_strides), _ptr(T), st(t_strides), _ptr(X),
+                                      st(x_strides), s, n, H, Q, _ptr(cache), cache.numel(),
+                                      arr, len(windows), stream, ctypes.byref(fused)),
+           "mla_concat_snapshots")
+    return bool(fused.value)
+
+
+def mla_rollback_valid_prefix(blocks, r: int, cell_pos, cell_seq, p0: int, p1: int = -1,
+                              seq: int = 0, n_streams: int = 1, stream=None) -> torch.Tensor:
+    """Leading valid pooled blocks after a rollback from p0 (device int32
+    tensor of one element).  blocks: int32 [n_blocks, 8 + r]; cell_pos: int32
+    [n_cells]; cell_seq: int64 [n_cells] owner bit masks."""
+    dev = cell_pos.device
+    out = torch.empty(1, dtype=torch.int32, device=dev)
+    _dense(blocks=blocks, cell_pos=cell_pos, cell_seq=cell_seq)
+    if stream is None:
+        stream = _current_stream(dev)
+    _check(lib().mla_rollback_valid_prefix(_ptr(blocks), blocks.shape[0], r, _ptr(cell_pos),
+                                           _ptr(cell_seq), cell_pos.numel(), p0, p1, seq,
+                                           n_streams, _ptr(out), stream),
+           "mla_rollback_valid_prefix")
+    return out
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:

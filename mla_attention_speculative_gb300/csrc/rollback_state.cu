@@ -1,0 +1,276 @@
+// Speculative-rollback state maintenance on the GPU.
+//
+// "Over 107tok/s Qwen3.8-Flash-Next on M3 Ultra":
+//  * section "A later extension: load snapshot history once", Algorithm 4
+//    (recognise a safe snapshot group) and Algorithm 5 (one load per row,
+//    then the concatenation and every snapshot window written from it):
+//    mla_concat_snapshots.  A thread owns one (channel, sequence) row, loads
+//    its s state words and n new words once into registers, writes the
+//    concatenated row and then each window's s words.  When the group is not
+//    safe to fuse, the ordinary path runs: the concatenation, then one copy
+//    per window that reads it back.  Words are moved as uint32 bit patterns.
+//  * section "Keep the pooled keys; score them again", ValidBlock and
+//    Algorithm 1 (retain a rollback-valid prefix): mla_rollback_valid_prefix.
+//    The predicate is checked for every block in parallel and the prefix ends
+//    at the first block that fails it (a minimum over the failing indices).
+
+#include <algorithm>
+#include <utility>
+#include <vector>
+
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kMaxWindows = 8;
+constexpr int kMaxRow = 16;
+
+struct Strides {
+  long long i, h, q;
+};
+struct Window {
+  int a;
+  long long offset, stride;
+};
+struct ConcatParams {
+  const uint32_t* S;
+  const uint32_t* T;
+  uint32_t* X;
+  uint32_t* cache;
+  Strides ss, ts, xs;
+  int s, n, H, Q, k;
+  Window w[kMaxWindows];
+};
+
+// Algorithm 5: one thread per row, 128 threads per CTA.
+__global__ void __launch_bounds__(128) concat_snapshots_kernel(ConcatParams p) {
+  const long long g = (long long)blockIdx.x * 128 + threadIdx.x;
+  if (g >= (long long)p.H * p.Q) return;
+  const int h = (int)(g % p.H), q = (int)(g / p.H);
+  uint32_t v[kMaxRow];
+#pragma unroll
+  for (int i = 0; i < kMaxRow; ++i) {
+    v[i] = 0u;
+    if (i < p.s) v[i] = p.S[i * p.ss.i + h * p.ss.h + q * p.ss.q];
+    else if (i < p.s + p.n) v[i] = p.T[(i - p.s) * p.ts.i + h * p.ts.h + q * p.ts.q];
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxRow; ++i)
+    if (i < p.s + p.n) p.X[i * p.xs.i + h * p.xs.h + q * p.xs.q] = v[i];
+  for (int j = 0; j < p.k; ++j) {
+    uint32_t* d = p.cache + p.w[j].offset + q * p.w[j].stride + (long long)h * p.s;
+    const int a = p.w[j].a;
+#pragma unroll
+    for (int i = 0; i < kMaxRow / 2; ++i) {
+      if (i >= p.s) break;
+      // V[a + i] with a register-resident array: select, never index
+      uint32_t x = 0u;
+#pragma unroll
+      for (int t = 0; t < kMaxRow; ++t) x = (t == a + i) ? v[t] : x;
+      d[i] = x;
+    }
+  }
+}
+
+// Ordinary path, one snapshot copy: reads the window back from X.
+__global__ void __launch_bounds__(128) snapshot_copy_kernel(const uint32_t* X, Strides xs,
+                                                            uint32_t* cache, Window w, int s,
+                                                            int H, int Q) {
+  const long long g = (long long)blockIdx.x * 128 + threadIdx.x;
+  if (g >= (long long)H * Q) return;
+  const int h = (int)(g % H), q = (int)(g / H);
+  uint32_t* d = cache + w.offset + q * w.stride + (long long)h * s;
+  for (int i = 0; i < s; ++i) d[i] = X[(w.a + i) * xs.i + h * xs.h + q * xs.q];
+}
+
+// Word range [lo, hi) a strided buffer covers, in bytes from address 0.
+std::pair<uintptr_t, uintptr_t> span(const void* base, int ni, int H, int Q, const Strides& st) {
+  const long long last = (ni - 1) * st.i + (long long)(H - 1) * st.h + (long long)(Q - 1) * st.q;
+  const uintptr_t lo = (uintptr_t)base;
+  return {lo, lo + (uintptr_t)(last + 1) * 4};
+}
+
+bool overlap_any(std::vector<std::pair<uintptr_t, uintptr_t>> r) {
+  std::sort(r.begin(), r.end());
+  for (size_t i = 1; i < r.size(); ++i)
+    if (r[i].first < r[i - 1].second) return true;
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// Rollback-valid prefix
+// ---------------------------------------------------------------------------
+// Block row layout (int32): stream, start, n_src, key, pos[0..3], src[0..r).
+constexpr int kBlockHead = 8;
+
+__device__ __forceinline__ bool valid_block(const int32_t* blk, int r, int p0,
+                                            const int32_t* cell_pos, const uint64_t* cell_seq,
+                                            int n_cells) {
+  const int stream = blk[0], start = blk[1], n_src = blk[2], key = blk[3];
+  if (n_src != r || stream != 0 || start < 0 || (long long)start + r > p0) return false;
+  for (int c = 0; c < 4; ++c)
+    if (blk[4 + c] != start) return false;
+  bool key_found = false;
+  for (int i = 0; i < r; ++i) {
+    const int c = blk[kBlockHead + i];
+    if (c == key) key_found = true;
+    if (c < 0 || c >= n_cells) return false;
+    if (cell_pos[c] < 0 || cell_seq[c] != 1ull || cell_pos[c] != start + i) return false;
+  }
+  return key_found;
+}
+
+constexpr int kPrefixThreads = 1024;
+
+__global__ void __launch_bounds__(kPrefixThreads)
+    rollback_prefix_kernel(const int32_t* blocks, int n_blocks, int r, const int32_t* cell_pos,
+                           const uint64_t* cell_seq, int n_cells, int p0, int32_t* out) {
+  __shared__ int warp_min[kPrefixThreads / 32];
+  int first_bad = n_blocks;
+  for (int b = threadIdx.x; b < n_blocks; b += kPrefixThreads) {
+    if (b >= first_bad) break;
+    if (!valid_block(blocks + (long long)b * (kBlockHead + r), r, p0, cell_pos, cell_seq,
+                     n_cells)) {
+      first_bad = b;
+      break;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) first_bad = min(first_bad, __shfl_xor_sync(~0u, first_bad, o));
+  if ((threadIdx.x & 31) == 0) warp_min[threadIdx.x >> 5] = first_bad;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int m = warp_min[threadIdx.x];
+    for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(~0u, m, o));
+    if (threadIdx.x == 0) *out = m;
+  }
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" mla_status_t mla_concat_snapshots(
+    const uint32_t* S, const int64_t* s_strides, const uint32_t* T, const int64_t* t_strides,
+    uint32_t* X, const int64_t* x_strides, int32_t s, int32_t n, int32_t H, int32_t Q,
+    uint32_t* cache, int64_t cache_words, const mla_snapshot_window_t* windows, int32_t k,
+    void* stream, int32_t* fused_out) {
+  if (!S || !T || !X || !s_strides || !t_strides || !x_strides || (k > 0 && (!cache || !windows))) {
+    set_error("concat/snapshot: a pointer is NULL");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (s < 1 || n < 1 || s + n > kMaxRow || s > kMaxRow / 2 || H < 1 || Q < 1 || k < 0 ||
+      k > kMaxWindows) {
+    set_error("concat/snapshot: need 1 <= s <= 8, 1 <= n, s + n <= 16, H, Q >= 1, 0 <= k <= 8 "
+              "(s=%d n=%d H=%d Q=%d k=%d)", s, n, H, Q, k);
+    return MLA_ERR_INVALID_ARG;
+  }
+  ConcatParams p;
+  p.S = S;
+  p.T = T;
+  p.X = X;
+  p.cache = cache;
+  p.ss = {s_strides[0], s_strides[1], s_strides[2]};
+  p.ts = {t_strides[0], t_strides[1], t_strides[2]};
+  p.xs = {x_strides[0], x_strides[1], x_strides[2]};
+  for (const Strides* st : {&p.ss, &p.ts, &p.xs}) {
+    if (st->i < 0 || st->h < 0 || st->q < 0) {
+      set_error("concat/snapshot: strides must not be negative");
+      return MLA_ERR_INVALID_ARG;
+    }
+  }
+  p.s = s;
+  p.n = n;
+  p.H = H;
+  p.Q = Q;
+  p.k = k;
+  std::vector<std::pair<uintptr_t, uintptr_t>> dest;
+  bool rows_overlap = false;
+  for (int j = 0; j < k; ++j) {
+    const mla_snapshot_window_t& w = windows[j];
+    if (w.window_start < 0 || w.window_start + s > s + n || w.cache_offset < 0 ||
+        w.sequence_stride < 0 ||
+        w.cache_offset + (int64_t)(Q - 1) * w.sequence_stride + (int64_t)H * s > cache_words) {
+      set_error("concat/snapshot: window %d (start %d, offset %lld, stride %lld) is outside the "
+                "row or the cache of %lld words", j, w.window_start, (long long)w.cache_offset,
+                (long long)w.sequence_stride, (long long)cache_words);
+      return MLA_ERR_INVALID_ARG;
+    }
+    p.w[j] = {w.window_start, w.cache_offset, w.sequence_stride};
+    std::vector<std::pair<uintptr_t, uintptr_t>> rows;
+    for (int q = 0; q < Q; ++q) {
+      const uintptr_t lo = (uintptr_t)(cache + w.cache_offset + (int64_t)q * w.sequence_stride);
+      rows.push_back({lo, lo + (uintptr_t)H * s * 4});
+    }
+    rows_overlap = rows_overlap || overlap_any(rows);
+    dest.insert(dest.end(), rows.begin(), rows.end());
+  }
+  // Algorithm 4: fuse only a group of 2..8 windows whose destinations are
+  // pairwise disjoint and lie outside S, T and X
+  bool fuse = k >= 2 && !rows_overlap && !overlap_any(dest);
+  if (fuse) {
+    const std::pair<uintptr_t, uintptr_t> others[3] = {span(S, s, H, Q, p.ss), span(T, n, H, Q, p.ts),
+                                                       span(X, s + n, H, Q, p.xs)};
+    for (const auto& o : others)
+      for (const auto& d : dest)
+        if (d.first < o.second && o.first < d.second) fuse = false;
+  }
+  const cudaStream_t st = (cudaStream_t)stream;
+  const unsigned grid = (unsigned)(((long long)H * Q + 127) / 128);
+  cudaError_t e;
+  if (fuse) {
+    KernelTimer kt("concat_snapshots", st);
+    concat_snapshots_kernel<<<grid, 128, 0, st>>>(p);
+    e = cudaGetLastError();
+  } else {
+    ConcatParams c = p;
+    c.k = 0;  // the concatenation alone
+    {
+      KernelTimer kt("concat", st);
+      concat_snapshots_kernel<<<grid, 128, 0, st>>>(c);
+    }
+    e = cudaGetLastError();
+    for (int j = 0; j < k && e == cudaSuccess; ++j) {
+      KernelTimer kt("snapshot_copy", st);
+      snapshot_copy_kernel<<<grid, 128, 0, st>>>(X, p.xs, cache, p.w[j], s, H, Q);
+      e = cudaGetLastError();
+    }
+  }
+  if (e != cudaSuccess) {
+    set_error("CUDA error %d (%s)", (int)e, cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  if (fused_out) *fused_out = fuse ? 1 : 0;
+  return MLA_OK;
+}
+
+extern "C" mla_status_t mla_rollback_valid_prefix(const int32_t* blocks, int32_t n_blocks,
+                                                  int32_t r, const int32_t* cell_pos,
+                                                  const uint64_t* cell_seq, int32_t n_cells,
+                                                  int32_t p0, int32_t p1, int32_t seq,
+                                                  int32_t n_streams, int32_t* prefix_out,
+                                                  void* stream) {
+  if (prefix_out == nullptr || n_blocks < 0 || r < 1 || n_cells < 0 ||
+      (n_blocks > 0 && blocks == nullptr) || (n_cells > 0 && (!cell_pos || !cell_seq))) {
+    set_error("rollback prefix: bad arguments (n_blocks=%d r=%d n_cells=%d)", n_blocks, r,
+              n_cells);
+    return MLA_ERR_INVALID_ARG;
+  }
+  // Algorithm 1's global guards: one stream, sequence 0, a removal from a
+  // non-negative position to the end; otherwise nothing is retained
+  const bool keep = n_streams == 1 && seq == 0 && p0 >= 0 && p1 < 0;
+  const cudaStream_t st = (cudaStream_t)stream;
+  {
+    KernelTimer kt("rollback_prefix", st);
+    rollback_prefix_kernel<<<1, kPrefixThreads, 0, st>>>(blocks, keep ? n_blocks : 0, r,
+                                                          cell_pos, cell_seq, n_cells, p0,
+                                                          prefix_out);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("CUDA error %d (%s)", (int)e, cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}

@@ -10,3 +10,4 @@ from .mla_oracle import (  # noqa: F401
     max_absorbed_queries, max_absorbed_queries_batch, select_branch,
 )
 from .draft_cap import accepted, select_draft_cap  # noqa: F401
+from . import rollback_state  # noqa: F401
