@@ -217,17 +217,15 @@ constexpr int OFF_RED = OFF_STG + X_BYTES;          // row maxima of the warpgro
 constexpr int OFF_LS = OFF_RED + NWG * BM * 4;      // row sums of the warpgroups
 constexpr int OFF_BAR = OFF_LS + NWG * BM * 4;
 constexpr int ATTN_SMEM = OFF_BAR + 512 + 1024;     // + barriers + alignment slack
-// Fused merge + unembedding (after the attention; every buffer above is free
+// Fused unembedding + merge (after the attention; every buffer above is free
 // by then): the W_UV tile of one (head, 128-column) unit, 512 x 128 bf16 as
-// two 64-column MN-major atoms, over the KV stages; the merged o_lat rows of
-// the unit (the B operand, K-major, at most FUSED_MAX_L rows padded to 16)
-// over the P and exchange tiles, followed by the merge's per-group partials.
-constexpr int FUSED_MAX_L = kFusedMaxL;
+// two 64-column MN-major atoms, over the KV stages; one chunk of at most 64
+// piece rows (the B operand, K-major, eight 64-column slabs) over the P,
+// exchange and staging tiles; the combine weights over the RoPE query tile.
 constexpr int FU_W_BYTES = 2 * kLat * 128;
-constexpr int FU_B_BYTES = 8 * FUSED_MAX_L * 128;
-constexpr int FU_SCRATCH = OFF_P + FU_B_BYTES;
 static_assert(OFF_KV + FU_W_BYTES <= OFF_P, "W_UV tile fits over the KV stages");
-static_assert(FU_SCRATCH + ATTN_THREADS * 10 * 4 <= OFF_RED, "merge scratch fits");
+static_assert(OFF_P + 8 * 64 * 128 <= OFF_RED, "a chunk of 64 piece rows fits");
+static_assert(kFusedMaxL * kFusedMaxSplits * 4 <= Q_ROPE, "combine weights fit");
 // Tensor memory: O half [0,256) fp32; this CTA's 256 latent query columns as
 // bf16 pairs [256,384) (the A operand of the score MMAs); S buffers [384,512).
 constexpr uint32_t TM_O = 0;
@@ -265,6 +263,7 @@ struct AttnParams {
   int BL;                 // B*L batch rows of the fold
   int NBf, nrb;           // fold rows per unit (multiple of 16, <= 64), row blocks
   int fstages, fsb;       // fold ring depth and stage bytes
+  int Lc;                 // verify rows per unembedding chunk (Lc * splits <= 64)
 };
 
 // Barrier slots.  Every barrier that is waited on by parity alone has enough
@@ -274,7 +273,9 @@ enum {
   B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22,
   B_WFULL = 24, B_UDONE = 25,
   // the fused kernel's fold: ring stages full / free, accumulator full / free, done
-  B_FFULL = 26, B_FEMPTY = 29, B_FACC = 32, B_FFREE = 34, B_FDONE = 36, B_COUNT = 37
+  B_FFULL = 26, B_FEMPTY = 29, B_FACC = 32, B_FFREE = 34, B_FDONE = 36,
+  // the fused kernel's unembedding: piece rows landed, all of a unit's MMAs done
+  B_OFULL = 37, B_DDONE = 38, B_COUNT = 39
 };
 
 // The fused kernel's fold ring lives over KV stages 2 and 3 and the P,
@@ -384,6 +385,12 @@ __device__ __forceinline__ void fold_produce(const AttnParams& p, const CUtensor
   prefetch_tmap(&tm_wuk);
   const int first = min(nlocal, p.fstages);
   for (int k = 0; k < first; ++k) load_w(k);
+  // the units past the ring's depth: their W_UK tiles start towards L2 now
+  for (int k = first; k < nlocal; ++k) {
+    const FoldUnit f = fold_unit(gid + k * nctas, p.nrb);
+    for (int kc = 0; kc < nk; ++kc)
+      for (int j = 0; j < 2; ++j) tma_prefetch_2d(&tm_wuk, f.mt * 128 + 64 * j, f.h * p.n + 64 * kc);
+  }
   pdl_wait();  // q_nope may come from the preceding kernel
   for (int k = 0; k < first; ++k) load_q(k);
   bool ok = true;
@@ -470,30 +477,38 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
 }
 
 // =========================================================================
-// fused merge + unembedding (the last phase of the FUSED attention kernel)
+// fused unembedding + merge (the last phase of the FUSED attention kernel)
 // =========================================================================
-// Once every CTA of sequence b has published its piece (O/l in bf16, (m, l)),
-// the CTAs of the sequence share its (head, 128-column) units: for unit
-// (h, mt) a CTA merges rows (l, h), l < L, over the pieces,
-//   o_lat = sum_s w_s (O_s / l_s) / sum_s w_s,  w_s = 2^(m_s - M) l_s,
-// straight into shared memory as the K-major B operand (bf16, as the separate
-// merge writes it), and multiplies it by the W_UV tile of columns
-// [128 mt, 128 mt + 128) (loaded by TMA while the CTA waits for the others;
-// the attention pulled W_UV into L2): D[128 x L] = W_UV[h][:, tile]^T o_lat^T
-// in TMEM, then out[b, l, h, 128 mt + m].  No o_lat round trip, no launches.
-__device__ __forceinline__ void fused_merge_unembed(const AttnParams& p, const CUtensorMap& tm_wuv,
-                                                    uint8_t* smem, uint32_t tmem, uint64_t* bars,
-                                                    int b, int split, int nsplit) {
+// The split-KV merge and the unembedding commute.  With the combine weights
+// of row (l, h) of sequence b, w_{l,s} = 2^(m_s - M_l) l_s / sum_s' 2^(m_s' - M_l) l_s'
+// over its pieces s,
+//   out[b, l, h, :] = (sum_s w_{l,s} (O_s / l_s)[l, h, :]) . W_UV[h]
+//                   = sum_s w_{l,s} ((O_s / l_s)[l, h, :] . W_UV[h]).
+// Once every CTA of sequence b has published its piece, the sequence's CTAs
+// share its (head, 128-column) units.  For unit (h, mt) a CTA loads the bf16
+// rows (O_s / l_s)[l, h, :] of every piece s and verify row l straight into
+// shared memory with TMA -- one 4-D box per 64-column slab, rows ordered by l
+// and then s, in chunks of Lc verify rows (Lc * splits <= 64 rows) -- and
+// multiplies each chunk by the W_UV tile of columns [128 mt, 128 mt + 128),
+// D[128 x rows] = W_UV tile^T x rows^T, into its own 64 TMEM columns.  The
+// epilogue then sums each verify row's columns of D with its weights.  All
+// the partial rows are in flight at once (no per-thread loads), and o_lat is
+// never formed.
+__device__ __forceinline__ void fused_unembed_merge(const AttnParams& p, const CUtensorMap& tm_wuv,
+                                                    const CUtensorMap& tm_pieces, uint8_t* smem,
+                                                    uint32_t tmem, uint64_t* bars, int b,
+                                                    int split, int nsplit) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t sW = smem_u32(smem + OFF_KV), sB = smem_u32(smem + OFF_P);
-  float* scratch = (float*)(smem + FU_SCRATCH);
+  float* wts = (float*)(smem + OFF_QR);                  // [L][splits] combine weights
   volatile int* stop = (volatile int*)(smem + OFF_RED);  // (the row maxima are done with)
   const int nmt = p.v / 128;
   const int units = p.H * nmt;
   const int ncta = (int)gridDim.x * nsplit;  // the CTAs of this sequence that wrote pieces
   const int cid = split * (int)gridDim.x + (int)blockIdx.x;
-  const int NBp = (p.L + 15) & ~15;
+  const int S = p.splits, Lc = p.Lc;
+  const int nch = (p.L + Lc - 1) / Lc;
   auto load_w = [&](int u) {
     const int h = u / nmt, mt = u - h * nmt;
     mbar_arrive_expect_tx(bar(B_WFULL), FU_W_BYTES);
@@ -527,148 +542,103 @@ __device__ __forceinline__ void fused_merge_unembed(const AttnParams& p, const C
   }
   __syncthreads();
   const bool go = *stop == 0;
-  const int P = p.L * 64;  // (row, 16-byte column chunk) pairs of a unit
-  const int G = P >= ATTN_THREADS ? 1 : min(8, ATTN_THREADS / P);  // piece groups per pair
   const size_t R = (size_t)p.R;
+  int n_o = 0, n_u = 0;  // (MMA thread) chunk loads and chunk MMAs so far
   int k = 0;
   for (int u = cid; u < units; u += ncta, ++k) {
     const int h = u / nmt, mt = u - h * nmt;
-    // ---- merge rows (l, h) into the B operand
-    if (go) {
-      for (int t = threadIdx.x; t < P * G; t += ATTN_THREADS) {
-        const int g = t / P, pr = t - g * P;
-        const int l = pr >> 6, c = pr & 63;
-        const size_t base = (size_t)b * p.splits * R + (size_t)l * p.H + h;
-        float M = -FLT_MAX, den = 0.f, acc[8];
+    if (warp == 1) {
+      // ---- every chunk: TMA the piece rows, then D[:, 64c ..] = W_UV tile^T x rows^T
+      if (lane == 0 && go) {
+        bool ok = true;
+        wait_or_fail(ok, bar(B_WFULL), k & 1, 31);
+        const uint32_t slab = 128u * S * Lc;  // bytes of one 64-column slab of a chunk
+        for (int c = 0; c < nch && ok; ++c) {
+          mbar_arrive_expect_tx(bar(B_OFULL), 8 * slab);
+          for (int kc = 0; kc < kLat / 64; ++kc)
+            tma_load_4d(sB + kc * 8192, &tm_pieces, bar(B_OFULL), 64 * kc, h, b * S, c * Lc);
+          wait_or_fail(ok, bar(B_OFULL), n_o & 1, 33);
+          ++n_o;
+          if (!ok) break;
+          tc_fence_after();
+          const int N = (S * Lc + 15) & ~15;
+          const uint32_t idesc = idesc_bf16(128, N, 1, 0);
+          for (int kc = 0; kc < kLat / 64; ++kc)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int s0 = g; s0 < nsplit; s0 += 4 * G) {
-          float2 mls[4];
-          uint4 x[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int sj = s0 + j * G;
-            const size_t e = base + (size_t)min(sj, nsplit - 1) * R;
-            mls[j] = __ldcg((const float2*)(p.ml + e * 2));
-            x[j] = __ldcg((const uint4*)(p.o_part + e * kLat) + c);
-            if (sj >= nsplit) mls[j].y = 0.f;
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (mls[j].y > 0.f) {
-              if (mls[j].x > M) {
-                const float f = ex2(M - mls[j].x);
-                M = mls[j].x;
-                den *= f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] *= f;
-              }
-              const float w = ex2(mls[j].x - M) * mls[j].y;
-              den += w;
-              float f[8];
-              bf16x8_to_f32(x[j], f);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[e] += w * f[e];
-            }
-          }
-        }
-        if (G == 1) {
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          const uint32_t addr =
-              sB + (c >> 3) * (NBp * 128) + l * 128 + ((((uint32_t)c & 7u) ^ (l & 7u)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                       "r"(pack_bf16(acc[0] * inv, acc[1] * inv)),
-                       "r"(pack_bf16(acc[2] * inv, acc[3] * inv)),
-                       "r"(pack_bf16(acc[4] * inv, acc[5] * inv)),
-                       "r"(pack_bf16(acc[6] * inv, acc[7] * inv))
-                       : "memory");
-        } else {
-          float* sc = scratch + (size_t)t * 10;
-          sc[0] = M;
-          sc[1] = den;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) sc[2 + e] = acc[e];
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16(tmem + 64 * c, sdesc_sw128(sW + (kc * 64 + ks * 16) * 128, kLat * 128, 1024),
+                       sdesc_sw128(sB + kc * 8192 + ks * 32, 16, 1024), idesc, (kc | ks) != 0);
+          mma_commit(bar(B_UDONE));
+          // the slab buffer is free for the next chunk once these MMAs are done
+          wait_or_fail(ok, bar(B_UDONE), n_u & 1, 34);
+          ++n_u;
         }
       }
-      if (G > 1) {
-        __syncthreads();
-        for (int pr = threadIdx.x; pr < P; pr += ATTN_THREADS) {
-          const int l = pr >> 6, c = pr & 63;
-          float Mall = -FLT_MAX;
-          for (int g = 0; g < G; ++g) {
-            const float* sc = scratch + (size_t)(g * P + pr) * 10;
-            if (sc[1] > 0.f) Mall = fmaxf(Mall, sc[0]);
-          }
-          float dsum = 0.f, y[8];
+      if (lane == 0) mma_commit(bar(B_DDONE));  // (arrives even when nothing was issued)
+    } else if (go) {
+      // ---- the combine weights of rows (l, h), one warp per verify row
+      for (int l = warp == 0 ? 0 : warp - 1; l < p.L; l += 14) {
+        const size_t base = (size_t)b * S * R + (size_t)l * p.H + h;
+        float2 ml[2];
+        float M = -FLT_MAX;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = 0.f;
-          for (int g = 0; g < G; ++g) {
-            const float* sc = scratch + (size_t)(g * P + pr) * 10;
-            const float f = sc[1] > 0.f ? ex2(sc[0] - Mall) : 0.f;
-            dsum += f * sc[1];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] += f * sc[2 + e];
-          }
-          const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
-          const uint32_t addr =
-              sB + (c >> 3) * (NBp * 128) + l * 128 + ((((uint32_t)c & 7u) ^ (l & 7u)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                       "r"(pack_bf16(y[0] * inv, y[1] * inv)), "r"(pack_bf16(y[2] * inv, y[3] * inv)),
-                       "r"(pack_bf16(y[4] * inv, y[5] * inv)), "r"(pack_bf16(y[6] * inv, y[7] * inv))
-                       : "memory");
+        for (int j = 0; j < 2; ++j) {
+          const int sj = lane + 32 * j;
+          ml[j] = sj < nsplit ? __ldcg((const float2*)(p.ml + (base + (size_t)sj * R) * 2))
+                              : make_float2(-FLT_MAX, 0.f);
+          if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
         }
-      }
-      // the padding rows of the B operand are zero
-      for (int idx = threadIdx.x; idx < (NBp - p.L) * 64; idx += ATTN_THREADS) {
-        const int l = p.L + (idx >> 6), c = idx & 63;
-        const uint32_t addr =
-            sB + (c >> 3) * (NBp * 128) + l * 128 + ((((uint32_t)c & 7u) ^ (l & 7u)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, o));
+        float w[2], sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          w[j] = ml[j].y > 0.f ? ex2(ml[j].x - M) * ml[j].y : 0.f;
+          sum += w[j];
+        }
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          if (lane + 32 * j < S) wts[l * S + lane + 32 * j] = w[j] * inv;
       }
     }
-    fence_async_shared();
-    tc_fence_before();
-    __syncthreads();
-    // ---- D[128 x NBp] = W_UV tile^T (A, MN-major) x o_lat rows^T (B, K-major)
-    if (threadIdx.x == 32) {
-      tc_fence_after();
-      bool ok = go;
-      wait_or_fail(ok, bar(B_WFULL), k & 1, 31);
-      if (ok) {
-        const uint32_t idesc = idesc_bf16(128, NBp, 1, 0);
-        for (int kc = 0; kc < kLat / 64; ++kc)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + TM_O, sdesc_sw128(sW + (kc * 64 + ks * 16) * 128, kLat * 128, 1024),
-                     sdesc_sw128(sB + kc * NBp * 128 + ks * 32, 16, 1024), idesc,
-                     (kc | ks) != 0);
-      }
-      mma_commit(bar(B_UDONE));  // (arrives even when nothing was issued)
-    }
+    __syncthreads();  // weights in shared memory
     if (warp >= 3 && warp < 7) {
-      // one warpgroup: TMEM lane m is output column 128 mt + m
+      // ---- one warpgroup: TMEM lane m is output column 128 mt + m
       bool ok = go;
-      wait_or_fail(ok, bar(B_UDONE), k & 1, 32);
+      wait_or_fail(ok, bar(B_DDONE), k & 1, 32);
       tc_fence_after();
       if (ok) {
         const int m = (warp & 3) * 32 + lane;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         __nv_bfloat16* o = p.out + ((size_t)b * p.L * p.H + h) * p.v + mt * 128 + m;
-        for (int c0 = 0; c0 < NBp; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_base + TM_O + c0, v);
-          tmem_wait_ld();
+        for (int c = 0; c < nch; ++c) {
+          const int rows = min(Lc, p.L - c * Lc) * S;  // columns of this chunk that are rows
+          int l = c * Lc, s = 0;
+          float acc = 0.f;
+          for (int j0 = 0; j0 < rows; j0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_base + 64 * c + j0, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int l = c0 + i;
-            if (l < p.L) o[(size_t)l * p.H * p.v] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            for (int e = 0; e < 16; ++e) {
+              if (j0 + e < rows) {
+                if (s < nsplit) acc += wts[l * S + s] * __uint_as_float(v[e]);
+                if (++s == S) {  // row l complete
+                  o[(size_t)l * p.H * p.v] = __float2bfloat16_rn(acc);
+                  acc = 0.f;
+                  s = 0;
+                  ++l;
+                }
+              }
+            }
           }
         }
       }
     }
     tc_fence_before();
     __syncthreads();
-    // the MMA that read the W_UV tile has completed: load the next unit's
+    // the MMAs that read the W_UV tile are complete: load the next unit's
     if (threadIdx.x == 0 && go && u + ncta < units) load_w(u + ncta);
   }
   // nothing this CTA loaded may still be landing when it exits: a unit's
@@ -688,7 +658,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
                         const __grid_constant__ CUtensorMap tm_op,
                         const __grid_constant__ CUtensorMap tm_wuv,
                         const __grid_constant__ CUtensorMap tm_wuk,
-                        const __grid_constant__ CUtensorMap tm_qn, AttnParams p) {
+                        const __grid_constant__ CUtensorMap tm_qn,
+                        const __grid_constant__ CUtensorMap tm_pieces, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t rank = cluster_ctarank();
@@ -739,6 +710,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         mbar_init(bar(B_FFREE + k), 128);
       }
       mbar_init(bar(B_FDONE), 1);
+      mbar_init(bar(B_OFULL), 1);
+      mbar_init(bar(B_DDONE), 1);
     }
     fence_mbar_init();
   }
@@ -1232,7 +1205,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (active) fused_merge_unembed(p, tm_wuv, smem, tmem, bars, b, split, nsplit);
+    if (active) fused_unembed_merge(p, tm_wuv, tm_pieces, smem, tmem, bars, b, split, nsplit);
   }
   tc_fence_before();
   __syncthreads();
@@ -1606,17 +1579,27 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.nrb = (BL + NBq - 1) / NBq;
     ap.fsb = fsb;
     ap.fstages = FOLD_BYTES / fsb < FOLD_MAX_STAGES ? FOLD_BYTES / fsb : FOLD_MAX_STAGES;
+    ap.Lc = 64 / p.splits > 0 ? 64 / p.splits : 1;
     const dim3 grid(2 * ((R + BM - 1) / BM), p.splits, p.B);
     if (p.fused) {
+      // the piece rows of one head as [l][piece][h][col]: row (b, s, l, h) of
+      // o_part sits at ((b * splits + s) * R + l * H + h) * 512 elements
+      CUtensorMap tm_pieces;
+      const uint64_t dims[4] = {(uint64_t)kLat, (uint64_t)p.H, (uint64_t)p.B * p.splits,
+                                (uint64_t)p.L};
+      const uint64_t strides[3] = {(uint64_t)kLat * 2, (uint64_t)R * kLat * 2,
+                                   (uint64_t)p.H * kLat * 2};
+      const uint32_t box[4] = {64, 1, (uint32_t)p.splits, (uint32_t)ap.Lc};
+      if (!make_tmap_bf16_4d(&tm_pieces, o_part, dims, strides, box)) return cudaErrorInvalidValue;
       KernelTimer kt("absorbed_fused_sm103", a.stream);
       e = launch_pdl(absorbed_attn_sm103<true>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
-                     tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, tm_wuk, tm_qn_fused, ap);
+                     tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, tm_wuk, tm_qn_fused, tm_pieces, ap);
       if (e != cudaSuccess) return e;
       return cudaGetLastError();
     }
     KernelTimer kt("absorbed_attn_sm103", a.stream);
     e = launch_pdl(absorbed_attn_sm103<false>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
-                   tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, tm_wuk, tm_qn, ap);
+                   tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, tm_wuk, tm_qn, tm_op, ap);
     if (e != cudaSuccess) return e;
   }
   {

@@ -240,17 +240,43 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     const int64_t row_tiles = (rows + 127) / 128;
     const int64_t slots = absorbed_cluster_slots();
     const int64_t max_tiles = (p->Tmax + 63) / 64;
-    int64_t best_ct = max_tiles, best_cost = -1;
-    for (int64_t ct = max_tiles; ct >= 1; --ct) {
-      int64_t clusters = 0;
-      for (int b = 0; b < batch; ++b) clusters += row_tiles * (((lens[b] + 63) / 64 + ct - 1) / ct);
-      const int64_t cost = ((clusters + slots - 1) / slots) * (ct + kClusterOverhead);
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best_ct = ct;
+    // the best piece length among those of at least ct_min tiles
+    auto best_piece = [&](int64_t ct_min) {
+      int64_t best_ct = max_tiles, best_cost = -1;
+      for (int64_t ct = max_tiles; ct >= ct_min; --ct) {
+        int64_t clusters = 0;
+        for (int b = 0; b < batch; ++b)
+          clusters += row_tiles * (((lens[b] + 63) / 64 + ct - 1) / ct);
+        const int64_t cost = ((clusters + slots - 1) / slots) * (ct + kClusterOverhead);
+        if (best_cost < 0 || cost < best_cost) {
+          best_cost = cost;
+          best_ct = ct;
+        }
+      }
+      return best_ct;
+    };
+    // The single-kernel path (fold, attention, unembedding, merge) needs its
+    // whole grid on the GPU at once -- its CTAs wait for one another after the
+    // fold and before the merge -- a verify block of at most kFusedMaxL rows,
+    // at most kFusedMaxSplits pieces per sequence, and its counters in the
+    // workspace header; it is taken whenever some piece length allows it.
+    auto fits_fused = [&](int64_t ct) {
+      const int64_t splits = (p->Tmax + ct * 64 - 1) / (ct * 64);
+      const int64_t lc = kFusedMaxSplits / splits;
+      return splits <= kFusedMaxSplits && row_tiles * splits * batch <= slots &&
+             L <= kFusedMaxL && (L + lc - 1) / lc <= 8 &&
+             (size_t)(2 + batch) * sizeof(uint32_t) <= kWorkspaceHeader;
+    };
+    int64_t ct = best_piece(1);
+    p->fused = fits_fused(ct);
+    if (!p->fused) {
+      const int64_t ct64 = best_piece((max_tiles + kFusedMaxSplits - 1) / kFusedMaxSplits);
+      if (fits_fused(ct64)) {
+        ct = ct64;
+        p->fused = true;
       }
     }
-    f.chunk = (int)(best_ct * 64);
+    f.chunk = (int)(ct * 64);
     f.splits = (int)((p->Tmax + f.chunk - 1) / f.chunk);
     f.off_cnt = 0;  // the fused kernel's counters, in the zeroed header
     size_t off = kWorkspaceHeader;
@@ -263,13 +289,6 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     f.off_olat = off;
     off = align256(off + nrow * p->r * 2);
     f.bytes = off;
-    // One kernel for the whole call (fold, attention, merge, unembedding)
-    // when every cluster of its grid is on the GPU at once -- its CTAs wait
-    // for one another after the fold and before the merge -- the verify block
-    // is narrow enough, and the header holds the counters.
-    const int64_t clusters = row_tiles * f.splits * batch;
-    p->fused = clusters <= slots && L <= kFusedMaxL &&
-               (size_t)(2 + batch) * sizeof(uint32_t) <= kWorkspaceHeader;
   }
   p->ws_bytes = p->fast_ok && p->fast.bytes > p->generic.bytes ? p->fast.bytes : p->generic.bytes;
   p->use(p->generic);

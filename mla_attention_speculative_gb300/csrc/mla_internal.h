@@ -56,8 +56,10 @@ struct Plan {
   }
 };
 
-// Widest verify block the fused absorbed kernel handles.
+// Widest verify block, and most split-KV pieces per sequence, the fused
+// absorbed kernel handles.
 constexpr int kFusedMaxL = 32;
+constexpr int kFusedMaxSplits = 64;
 // Every workspace starts with this many bytes that must be zero before its
 // first call and that every call leaves zero (the fused absorbed kernel's
 // arrival counters live there).

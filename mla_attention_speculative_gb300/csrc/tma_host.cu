@@ -31,8 +31,8 @@ namespace {
 struct MapKey {
   int type, rank, swizzle;
   const void* base;
-  uint64_t dims[3], strides[2];
-  uint32_t box[3];
+  uint64_t dims[4], strides[3];
+  uint32_t box[4];
 };
 struct MapEntry {
   MapKey key;
@@ -71,7 +71,7 @@ bool encode_cached(CUtensorMap* map, CUtensorMapDataType type, int rank, const v
   }
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint32_t es[3] = {1, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, type, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
                         es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -116,6 +116,15 @@ bool make_tmap_f32_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64
                       uint32_t box_inner, uint32_t box_rows) {
   return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, inner, rows, planes,
                    row_stride_bytes, plane_stride_bytes, box_inner, box_rows);
+}
+
+bool make_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                       const uint64_t strides_bytes[3], const uint32_t box[4]) {
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+  const cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  return encode_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, d, st, b,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace mla

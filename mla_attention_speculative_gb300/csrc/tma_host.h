@@ -27,4 +27,10 @@ bool make_tmap_f32_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64
                       uint64_t planes, uint64_t row_stride_bytes, uint64_t plane_stride_bytes,
                       uint32_t box_inner, uint32_t box_rows);
 
+// A 4-D bf16 tensor (dims[0] innermost, 64 elements per box row, 128-byte
+// swizzle) with byte strides for dims 1..3 in any order; boxes land in shared
+// memory with box[3] outermost.
+bool make_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                       const uint64_t strides_bytes[3], const uint32_t box[4]);
+
 }  // namespace mla
