@@ -304,3 +304,46 @@ def gather_paged(pages, page_table, cache_lens, page_size):
         t = np.arange(T)
         out[b, :T] = pages[np.asarray(page_table)[b, t // page_size], t % page_size]
     return out
+
+
+def sparse_absorbed(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, topk, scale=None,
+                    heads=None, rows=None):
+    """Absorbed attention over a selected set of cached positions.
+
+    "One guard, 110x off the verify step", section "The sparse model is
+    different": an indexer selects the top 2048 cached positions and attention
+    runs over those only.  ``topk`` [B, L, k] lists, for verify row l of
+    sequence b, the positions its attention reads; an entry is used when
+    0 <= t <= T_b - L + l (the causal verify limit), so -1 pads a short list.
+    Readings: every head of a verify row shares its list (the indexer picks
+    positions, the heads share the latent); a row whose list holds no usable
+    position returns zeros.  Otherwise the steps are those of ``absorbed``,
+    with the scores taken over the listed positions only.
+    """
+    q_nope, q_rope = _as64(q_nope), _as64(q_rope)
+    W_UK, W_UV = _as64(W_UK), _as64(W_UV)
+    topk = np.asarray(topk)
+    B, L, H, n = q_nope.shape
+    rope = q_rope.shape[-1]
+    v = W_UV.shape[-1]
+    if scale is None:
+        scale = default_scale(n, rope)
+    heads = list(range(H)) if heads is None else list(heads)
+    rows = list(range(L)) if rows is None else list(rows)
+    out = np.zeros((B, len(rows), len(heads), v), dtype=np.float64)
+    for b in range(B):
+        T = int(cache_lens[b])
+        for ri, l in enumerate(rows):
+            idx = [int(t) for t in topk[b, l] if 0 <= int(t) <= T - L + l]
+            if not idx:
+                continue
+            ckv = _as64(c_kv[b, idx])          # [k', r]
+            kr = _as64(k_rope[b, idx])         # [k', rope]
+            qn = q_nope[b, l, heads]           # [h, n]
+            qr = q_rope[b, l, heads]           # [h, rope]
+            q_lat = np.einsum('hn,hnr->hr', qn, W_UK[heads])
+            s_ = (q_lat @ ckv.T + qr @ kr.T) * scale
+            p_ = _softmax_rows(s_)
+            o_lat = p_ @ ckv
+            out[b, ri] = np.einsum('hr,hrv->hv', o_lat, W_UV[heads])
+    return out
