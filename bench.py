@@ -93,12 +93,8 @@ def _work(kernel: str, L: int, T: int, H=128, r=512, n=128, v=128, rope=64):
     attend = (cache + rows * (r + rope) * bf + rows * r * bf,
               2 * rows * T * (r + rope) + 2 * rows * T * r)
     unembed = (H * r * v * bf + rows * r * bf + rows * v * bf, 2 * rows * r * v)
-    # the whole call in one kernel (fold, attention, merge, unembedding): no
-    # q_lat or o_lat hand-off
-    fused = (H * n * r * bf + rows * n * bf + cache + rows * rope * bf + H * r * v * bf
-             + rows * v * bf, fold[1] + attend[1] + unembed[1])
     table = {
-        "absorbed_fused_sm103": fused,
+        "unembed_merge_sm103": unembed,
         "generic_fold": fold,
         "generic_absorbed_attention": attend,
         "generic_combine_unembed": unembed,
@@ -255,7 +251,7 @@ KERNEL_SOURCES = {
     "generic_combine_unembed": ["generic_kernels.cu"],
     "fold_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "absorbed_attn_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
-    "absorbed_fused_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
+    "unembed_merge_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "merge_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "unembed_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
     "expand_sm103": ["materialised_sm103.cu", "sm103_ptx.cuh"],

@@ -113,14 +113,8 @@ mla_status_t mla_select_branch(const mla_geometry_t* geom, int32_t L,
 
 /* Bytes of device workspace mla_verify_attention needs for this call
  * (branch-dependent: split-KV partials for the absorbed branch, the expanded
- * K_nope/V buffer for the materialised branch).  Host only.
- *
- * Every workspace begins with a 512-byte header that must be zero before the
- * first call that uses it; every call leaves it zero (the absorbed branch's
- * single-kernel path keeps its cross-CTA arrival counters there).  Zero it
- * once when the workspace is allocated (cudaMemsetAsync of 512 bytes).  The
- * rest needs no initialisation.  If mla_device_status ever reports
- * MLA_ERR_TIMEOUT, zero the header again before reusing the workspace. */
+ * K_nope/V buffer for the materialised branch).  The workspace needs no
+ * initialisation.  Host only. */
 mla_status_t mla_workspace_bytes(const mla_geometry_t* geom, int32_t batch, int32_t L,
                                  const int32_t* cache_lens_host, int32_t mode,
                                  size_t* bytes);
@@ -147,8 +141,8 @@ mla_status_t mla_workspace_bytes(const mla_geometry_t* geom, int32_t batch, int3
  *          [0, num_pages), or NULL for a contiguous cache
  *  out     device [batch, L, H, v] in the geometry's dtype
  *  workspace / workspace_bytes  device scratch of at least
- *          mla_workspace_bytes() bytes, 256-byte aligned, whose first 512
- *          bytes are zero (see mla_workspace_bytes)
+ *          mla_workspace_bytes() bytes, 256-byte aligned (may be NULL when
+ *          that is 0)
  *  branch_taken  host, may be NULL; receives the mla_branch_t used
  */
 mla_status_t mla_verify_attention(

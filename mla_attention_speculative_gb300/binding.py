@@ -197,15 +197,9 @@ def mla_select_draft_cap(p: float, verify_cost: Sequence[float], drafter_cost,
     return int(cap), [sp[i] for i in range(limit + 1)]
 
 
-WORKSPACE_HEADER = 512
-
-
 def new_workspace(nbytes: int, device) -> torch.Tensor:
-    """A workspace of `nbytes` whose 512-byte header is zero, as the library
-    requires before a workspace's first call (the rest is left as allocated)."""
-    ws = torch.empty(max(int(nbytes), WORKSPACE_HEADER), dtype=torch.uint8, device=device)
-    ws[:WORKSPACE_HEADER].zero_()
-    return ws
+    """An (uninitialised) workspace of at least `nbytes` bytes."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 class SnapshotWindow(ctypes.Structure):

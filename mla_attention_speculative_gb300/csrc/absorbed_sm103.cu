@@ -21,10 +21,15 @@
 //                  computes its partial scores over its columns, swaps them
 //                  with the peer through distributed shared memory, and both
 //                  accumulate their half of o_lat (128 x 256 fp32 in TMEM).
-//  merge_sm103     log-sum-exp merge of the split-KV pieces into bf16 o_lat
-//                  (merge_rows_sm103 when a row has few pieces).
+//  unembed_merge   the split-KV merge and the unembedding in one kernel: they
+//                  commute, so every piece's rows are multiplied by W_UV in one
+//                  TMA-fed tensor-core GEMM and the products are combined with
+//                  the pieces' log-sum-exp weights (see the kernel).  When a
+//                  sequence has more than 64 pieces, merge_sm103 /
+//                  merge_rows_sm103 (log-sum-exp merge into bf16 o_lat) and the
+//                  swap-AB unembedding run instead.
 //
-// The four launches are chained with programmatic dependent launch: each one
+// The launches are chained with programmatic dependent launch: each one
 // starts the loads that do not depend on its predecessor (weights, the KV
 // cache) before waiting for it.
 //
@@ -216,16 +221,7 @@ constexpr int OFF_STG = OFF_X + 2 * X_BYTES;        // this CTA's partial scores
 constexpr int OFF_RED = OFF_STG + X_BYTES;          // row maxima of the warpgroups
 constexpr int OFF_LS = OFF_RED + NWG * BM * 4;      // row sums of the warpgroups
 constexpr int OFF_BAR = OFF_LS + NWG * BM * 4;
-constexpr int ATTN_SMEM = OFF_BAR + 512 + 1024;     // + barriers + alignment slack
-// Fused unembedding + merge (after the attention; every buffer above is free
-// by then): the W_UV tile of one (head, 128-column) unit, 512 x 128 bf16 as
-// two 64-column MN-major atoms, over the KV stages; one chunk of at most 64
-// piece rows (the B operand, K-major, eight 64-column slabs) over the P,
-// exchange and staging tiles; the combine weights over the RoPE query tile.
-constexpr int FU_W_BYTES = 2 * kLat * 128;
-static_assert(OFF_KV + FU_W_BYTES <= OFF_P, "W_UV tile fits over the KV stages");
-static_assert(OFF_P + 8 * 64 * 128 <= OFF_RED, "a chunk of 64 piece rows fits");
-static_assert(kFusedMaxL * kFusedMaxSplits * 4 <= Q_ROPE, "combine weights fit");
+constexpr int ATTN_SMEM = OFF_BAR + 256 + 1024;     // + barriers + alignment slack
 // Tensor memory: O half [0,256) fp32; this CTA's 256 latent query columns as
 // bf16 pairs [256,384) (the A operand of the score MMAs); S buffers [384,512).
 constexpr uint32_t TM_O = 0;
@@ -251,42 +247,14 @@ struct AttnParams {
   float* ml;              // [B, splits, R, 2]: (m, l) of each piece
   const char* pf;     // W_UV, pulled into L2 while the attention runs
   size_t pf_bytes;
-  // fused kernel only: the fold before the attention, the merge and the
-  // unembedding after it
-  uint32_t* counters;     // workspace header: [0] CTAs past the fold, [1] CTAs
-                          // that have left, [2 + b] CTAs of sequence b that
-                          // have published their pieces (all zero between calls)
-  __nv_bfloat16* out;     // [B, L, H, v]
-  __nv_bfloat16* q_lat_w; // the Q tiles the fold writes (same buffer as q_lat)
-  int v;                  // value width, a multiple of 128
-  int n;                  // nope width (the fold's K), a multiple of 64
-  int BL;                 // B*L batch rows of the fold
-  int NBf, nrb;           // fold rows per unit (multiple of 16, <= 64), row blocks
-  int fstages, fsb;       // fold ring depth and stage bytes
-  int Lc;                 // verify rows per unembedding chunk (Lc * splits <= 64)
 };
 
 // Barrier slots.  Every barrier that is waited on by parity alone has enough
 // copies that it cannot complete twice before its waiter looks.
 enum {
   B_QFULL = 0, B_QTMEM = 1, B_KVFULL = 2, B_KVEMPTY = 6, B_SFULL = 10, B_SFREE = 12,
-  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22,
-  B_WFULL = 24, B_UDONE = 25,
-  // the fused kernel's fold: ring stages full / free, accumulator full / free, done
-  B_FFULL = 26, B_FEMPTY = 29, B_FACC = 32, B_FFREE = 34, B_FDONE = 36,
-  // the fused kernel's unembedding: piece rows landed, all of a unit's MMAs done
-  B_OFULL = 37, B_DDONE = 38, B_COUNT = 39
+  B_PFULL = 14, B_ODONE = 16, B_XFULL = 18, B_XFREE = 20, B_DRAIN = 22, B_COUNT = 24
 };
-
-// The fused kernel's fold ring lives over KV stages 2 and 3 and the P,
-// exchange and staging tiles (KV stages 0 and 1 hold the first two KV tiles,
-// loaded while the fold runs).
-constexpr int FOLD_BASE = OFF_KV + 2 * KV_STAGE;
-constexpr int FOLD_BYTES = OFF_RED - FOLD_BASE;
-constexpr int FOLD_MAX_STAGES = 3;
-static_assert(FOLD_BASE % 1024 == 0, "fold ring stages need 1 KiB alignment");
-// the widest fold stage (n = 256, 64 rows) fits at least once
-static_assert(2 * 256 * 128 + 4 * 64 * 128 <= FOLD_BYTES, "fold ring holds a stage");
 
 // One partial score of this CTA in log2-softmax units, rounded to fp16: the
 // exchange warps send exactly this to the peer and the softmax adds exactly
@@ -333,333 +301,11 @@ __device__ __forceinline__ uint32_t xchg_offset(int wg, int q, int c) {
   return (uint32_t)((q >> 5) * XQUARTER + wg * (32 * XROW) + (q & 31) * XROW + ((c ^ sw) << 4));
 }
 
-// =========================================================================
-// fused fold (the first phase of the FUSED attention kernel)
-// =========================================================================
-// q_lat[row, h, :] = q_nope[row, h, :] . W_UK[h] for the B*L batch rows, as the
-// swap-AB GEMM above computes it, spread over every CTA of the attention's
-// grid: unit (h, mt, rb) is D[128 x NBf] = W_UK[h][:, 128 mt : 128 mt + 128]^T
-// x q_nope[rows of block rb, h, :]^T, units u = gid, gid + nctas, ...  Its
-// operands stream through a ring of fstages stages, its accumulator
-// alternates between two 64-column TMEM buffers (the S buffers, unused until
-// the attention starts), and the softmax warpgroups write it out in the
-// attention's Q-tile layout (warpgroup u & 1 takes unit u).
-struct FoldUnit {
-  int h, mt, rb;
-};
-__device__ __forceinline__ FoldUnit fold_unit(int u, int nrb) {
-  const int hm = u / nrb;
-  return {hm >> 2, hm & 3, u - hm * nrb};
-}
-__device__ __forceinline__ int fold_units_of(int units, int gid, int nctas) {
-  return units > gid ? (units - gid + nctas - 1) / nctas : 0;
-}
-
-// TMA producer of the fold: W_UK tiles (inputs the preceding kernel does not
-// write) are requested before the dependency wait, q_nope after it.  Returns
-// once every fold MMA has finished, so the ring's memory is free again.
-__device__ __forceinline__ void fold_produce(const AttnParams& p, const CUtensorMap& tm_wuk,
-                                             const CUtensorMap& tm_qn, uint32_t fold_base,
-                                             uint64_t* bars, int gid, int nctas) {
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const int nk = p.n / 64;
-  const int nlocal = fold_units_of(p.H * 4 * p.nrb, gid, nctas);
-  const uint32_t a_bytes = 2u * p.n * 128, tx = (uint32_t)nk * (16384u + p.NBf * 128u);
-  auto load_w = [&](int k) {
-    const FoldUnit f = fold_unit(gid + k * nctas, p.nrb);
-    const uint32_t st = fold_base + (k % p.fstages) * p.fsb;
-    const uint32_t fb = bar(B_FFULL + k % p.fstages);
-    mbar_arrive_expect_tx(fb, tx);
-    for (int kc = 0; kc < nk; ++kc)
-      for (int j = 0; j < 2; ++j)
-        tma_load_2d(st + j * p.n * 128 + kc * 8192, &tm_wuk, fb, f.mt * 128 + 64 * j,
-                    f.h * p.n + 64 * kc);
-  };
-  auto load_q = [&](int k) {
-    const FoldUnit f = fold_unit(gid + k * nctas, p.nrb);
-    const uint32_t st = fold_base + (k % p.fstages) * p.fsb + a_bytes;
-    for (int kc = 0; kc < nk; ++kc)
-      tma_load_2d(st + kc * p.NBf * 128, &tm_qn, bar(B_FFULL + k % p.fstages),
-                  f.h * p.n + 64 * kc, f.rb * p.NBf);
-  };
-  prefetch_tmap(&tm_wuk);
-  const int first = min(nlocal, p.fstages);
-  for (int k = 0; k < first; ++k) load_w(k);
-  // the units past the ring's depth: their W_UK tiles start towards L2 now
-  for (int k = first; k < nlocal; ++k) {
-    const FoldUnit f = fold_unit(gid + k * nctas, p.nrb);
-    for (int kc = 0; kc < nk; ++kc)
-      for (int j = 0; j < 2; ++j) tma_prefetch_2d(&tm_wuk, f.mt * 128 + 64 * j, f.h * p.n + 64 * kc);
-  }
-  pdl_wait();  // q_nope may come from the preceding kernel
-  for (int k = 0; k < first; ++k) load_q(k);
-  bool ok = true;
-  for (int k = first; k < nlocal; ++k) {
-    wait_or_fail(ok, bar(B_FEMPTY + k % p.fstages), ((k / p.fstages) - 1) & 1, 40);
-    if (!ok) break;
-    load_w(k);
-    load_q(k);
-  }
-  // every fold MMA is done (and so every load it consumed has landed)
-  mbar_wait(bar(B_FDONE), 0);
-}
-
-// MMA issuer of the fold.
-__device__ __forceinline__ void fold_mma(const AttnParams& p, uint32_t fold_base, uint32_t tmem,
-                                         uint64_t* bars, int gid, int nctas) {
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const int nk = p.n / 64;
-  const int nlocal = fold_units_of(p.H * 4 * p.nrb, gid, nctas);
-  const uint32_t idesc = idesc_bf16(128, p.NBf, 1, 0);
-  bool ok = true;
-  for (int k = 0; k < nlocal && ok; ++k) {
-    const int s = k % p.fstages, buf = k & 1;
-    wait_or_fail(ok, bar(B_FFULL + s), (k / p.fstages) & 1, 41);
-    if (k >= 2) wait_or_fail(ok, bar(B_FFREE + buf), ((k - 2) >> 1) & 1, 42);
-    if (!ok) break;
-    tc_fence_after();
-    const uint32_t sa = fold_base + s * p.fsb, sb = sa + 2 * p.n * 128;
-    for (int kc = 0; kc < nk; ++kc)
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + TM_S + buf * 64,
-                 sdesc_sw128(sa + (kc * 64 + ks * 16) * 128, p.n * 128, 1024),
-                 sdesc_sw128(sb + kc * p.NBf * 128 + ks * 32, 16, 1024), idesc, (kc | ks) != 0);
-    mma_commit(bar(B_FEMPTY + s));
-    mma_commit(bar(B_FACC + buf));
-  }
-  mma_commit(bar(B_FDONE));  // (also when no unit was issued)
-}
-
-// Epilogue of the fold, one softmax warpgroup per unit parity: q_lat in bf16,
-// in the attention's Q-tile layout.
-__device__ __forceinline__ void fold_store(const AttnParams& p, uint32_t tmem, uint64_t* bars,
-                                           int gid, int nctas, int wg, int warp, int lane) {
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const int nlocal = fold_units_of(p.H * 4 * p.nrb, gid, nctas);
-  const int q = (warp & 3) * 32 + lane;  // TMEM lane = latent column within the unit's 128
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  bool ok = true;
-  for (int k = wg; k < nlocal; k += 2) {
-    const FoldUnit f = fold_unit(gid + k * nctas, p.nrb);
-    wait_or_fail(ok, bar(B_FACC + (k & 1)), (k >> 1) & 1, 43);
-    tc_fence_after();
-    if (ok) {
-      const int m = f.mt * 128 + q;
-      for (int c0 = 0; c0 < p.NBf; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_base + TM_S + (k & 1) * 64 + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int row = f.rb * p.NBf + c0 + i;  // batch row b*L + l
-          if (row >= p.BL) continue;
-          const int b = row / p.L, r = (row - b * p.L) * p.H + f.h;
-          const size_t idx =
-              ((((size_t)b * p.rtiles + (r >> 7)) * 64 + (m >> 3)) * 128 + (r & 127)) * 8 + (m & 7);
-          p.q_lat_w[idx] = __float2bfloat16_rn(__uint_as_float(v[i]));
-        }
-      }
-    }
-    tc_fence_before();
-    mbar_arrive(bar(B_FFREE + (k & 1)));
-  }
-}
-
-// 8 bf16 (one 16-byte load) to fp32.
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-// =========================================================================
-// fused unembedding + merge (the last phase of the FUSED attention kernel)
-// =========================================================================
-// The split-KV merge and the unembedding commute.  With the combine weights
-// of row (l, h) of sequence b, w_{l,s} = 2^(m_s - M_l) l_s / sum_s' 2^(m_s' - M_l) l_s'
-// over its pieces s,
-//   out[b, l, h, :] = (sum_s w_{l,s} (O_s / l_s)[l, h, :]) . W_UV[h]
-//                   = sum_s w_{l,s} ((O_s / l_s)[l, h, :] . W_UV[h]).
-// Once every CTA of sequence b has published its piece, the sequence's CTAs
-// share its (head, 128-column) units.  For unit (h, mt) a CTA loads the bf16
-// rows (O_s / l_s)[l, h, :] of every piece s and verify row l straight into
-// shared memory with TMA -- one 4-D box per 64-column slab, rows ordered by l
-// and then s, in chunks of Lc verify rows (Lc * splits <= 64 rows) -- and
-// multiplies each chunk by the W_UV tile of columns [128 mt, 128 mt + 128),
-// D[128 x rows] = W_UV tile^T x rows^T, into its own 64 TMEM columns.  The
-// epilogue then sums each verify row's columns of D with its weights.  All
-// the partial rows are in flight at once (no per-thread loads), and o_lat is
-// never formed.
-__device__ __forceinline__ void fused_unembed_merge(const AttnParams& p, const CUtensorMap& tm_wuv,
-                                                    const CUtensorMap& tm_pieces, uint8_t* smem,
-                                                    uint32_t tmem, uint64_t* bars, int b,
-                                                    int split, int nsplit) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const uint32_t sW = smem_u32(smem + OFF_KV), sB = smem_u32(smem + OFF_P);
-  float* wts = (float*)(smem + OFF_QR);                  // [L][splits] combine weights
-  volatile int* stop = (volatile int*)(smem + OFF_RED);  // (the row maxima are done with)
-  const int nmt = p.v / 128;
-  const int units = p.H * nmt;
-  const int ncta = (int)gridDim.x * nsplit;  // the CTAs of this sequence that wrote pieces
-  const int cid = split * (int)gridDim.x + (int)blockIdx.x;
-  const int S = p.splits, Lc = p.Lc;
-  const int nch = (p.L + Lc - 1) / Lc;
-  auto load_w = [&](int u) {
-    const int h = u / nmt, mt = u - h * nmt;
-    mbar_arrive_expect_tx(bar(B_WFULL), FU_W_BYTES);
-    for (int kc = 0; kc < kLat / 64; ++kc)
-      for (int j = 0; j < 2; ++j)
-        tma_load_2d(sW + j * kLat * 128 + kc * 8192, &tm_wuv, bar(B_WFULL), mt * 128 + 64 * j,
-                    h * kLat + 64 * kc);
-  };
-  if (threadIdx.x == 0 && cid < units) load_w(cid);
-  // publish this CTA's pieces (its softmax threads fenced their writes and the
-  // storing thread waited for its TMA stores before the barrier above), then
-  // wait for the other CTAs of the sequence; the grid is resident as a whole,
-  // so they all get here, and the wait is bounded anyway
-  if (threadIdx.x == 96) {
-    __threadfence();
-    red_release_gpu_add(p.counters + 2 + b, 1u);
-    const uint32_t target = (uint32_t)ncta;
-    int gave_up = 0;
-    if (ld_acquire_gpu(p.counters + 2 + b) < target) {
-      const long long t0 = clock64();
-      while (ld_acquire_gpu(p.counters + 2 + b) < target) {
-        if (clock64() - t0 > kWaitLimitCycles) {
-          report_timeout(30);
-          gave_up = 1;
-          break;
-        }
-        __nanosleep(32);
-      }
-    }
-    *stop = gave_up;  // (the only writer)
-  }
-  __syncthreads();
-  const bool go = *stop == 0;
-  const size_t R = (size_t)p.R;
-  int n_o = 0, n_u = 0;  // (MMA thread) chunk loads and chunk MMAs so far
-  int k = 0;
-  for (int u = cid; u < units; u += ncta, ++k) {
-    const int h = u / nmt, mt = u - h * nmt;
-    if (warp == 1) {
-      // ---- every chunk: TMA the piece rows, then D[:, 64c ..] = W_UV tile^T x rows^T
-      if (lane == 0 && go) {
-        bool ok = true;
-        wait_or_fail(ok, bar(B_WFULL), k & 1, 31);
-        const uint32_t slab = 128u * S * Lc;  // bytes of one 64-column slab of a chunk
-        for (int c = 0; c < nch && ok; ++c) {
-          mbar_arrive_expect_tx(bar(B_OFULL), 8 * slab);
-          for (int kc = 0; kc < kLat / 64; ++kc)
-            tma_load_4d(sB + kc * 8192, &tm_pieces, bar(B_OFULL), 64 * kc, h, b * S, c * Lc);
-          wait_or_fail(ok, bar(B_OFULL), n_o & 1, 33);
-          ++n_o;
-          if (!ok) break;
-          tc_fence_after();
-          const int N = (S * Lc + 15) & ~15;
-          const uint32_t idesc = idesc_bf16(128, N, 1, 0);
-          for (int kc = 0; kc < kLat / 64; ++kc)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_bf16(tmem + 64 * c, sdesc_sw128(sW + (kc * 64 + ks * 16) * 128, kLat * 128, 1024),
-                       sdesc_sw128(sB + kc * 8192 + ks * 32, 16, 1024), idesc, (kc | ks) != 0);
-          mma_commit(bar(B_UDONE));
-          // the slab buffer is free for the next chunk once these MMAs are done
-          wait_or_fail(ok, bar(B_UDONE), n_u & 1, 34);
-          ++n_u;
-        }
-      }
-      if (lane == 0) mma_commit(bar(B_DDONE));  // (arrives even when nothing was issued)
-    } else if (go) {
-      // ---- the combine weights of rows (l, h), one warp per verify row
-      for (int l = warp == 0 ? 0 : warp - 1; l < p.L; l += 14) {
-        const size_t base = (size_t)b * S * R + (size_t)l * p.H + h;
-        float2 ml[2];
-        float M = -FLT_MAX;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int sj = lane + 32 * j;
-          ml[j] = sj < nsplit ? __ldcg((const float2*)(p.ml + (base + (size_t)sj * R) * 2))
-                              : make_float2(-FLT_MAX, 0.f);
-          if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
-        }
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, o));
-        float w[2], sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          w[j] = ml[j].y > 0.f ? ex2(ml[j].x - M) * ml[j].y : 0.f;
-          sum += w[j];
-        }
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
-        const float inv = sum > 0.f ? 1.f / sum : 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          if (lane + 32 * j < S) wts[l * S + lane + 32 * j] = w[j] * inv;
-      }
-    }
-    __syncthreads();  // weights in shared memory
-    if (warp >= 3 && warp < 7) {
-      // ---- one warpgroup: TMEM lane m is output column 128 mt + m
-      bool ok = go;
-      wait_or_fail(ok, bar(B_DDONE), k & 1, 32);
-      tc_fence_after();
-      if (ok) {
-        const int m = (warp & 3) * 32 + lane;
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        __nv_bfloat16* o = p.out + ((size_t)b * p.L * p.H + h) * p.v + mt * 128 + m;
-        for (int c = 0; c < nch; ++c) {
-          const int rows = min(Lc, p.L - c * Lc) * S;  // columns of this chunk that are rows
-          int l = c * Lc, s = 0;
-          float acc = 0.f;
-          for (int j0 = 0; j0 < rows; j0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + lane_base + 64 * c + j0, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              if (j0 + e < rows) {
-                if (s < nsplit) acc += wts[l * S + s] * __uint_as_float(v[e]);
-                if (++s == S) {  // row l complete
-                  o[(size_t)l * p.H * p.v] = __float2bfloat16_rn(acc);
-                  acc = 0.f;
-                  s = 0;
-                  ++l;
-                }
-              }
-            }
-          }
-        }
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-    // the MMAs that read the W_UV tile are complete: load the next unit's
-    if (threadIdx.x == 0 && go && u + ncta < units) load_w(u + ncta);
-  }
-  // nothing this CTA loaded may still be landing when it exits: a unit's
-  // tile is only loaded when the loop will consume it, and an early stop
-  // leaves at most the first one pending
-  if (threadIdx.x == 0 && !go && cid < units) mbar_wait(bar(B_WFULL), 0);
-}
-
-// FUSED: the kernel also merges the pieces and applies W_UV (see the fused
-// phase at the end); it is launched only when the whole grid fits on the GPU
-// at once, since each sequence's CTAs wait for one another there.
-template <bool FUSED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     absorbed_attn_sm103(const __grid_constant__ CUtensorMap tm_qr,
                         const __grid_constant__ CUtensorMap tm_ckv,
                         const __grid_constant__ CUtensorMap tm_kr,
-                        const __grid_constant__ CUtensorMap tm_op,
-                        const __grid_constant__ CUtensorMap tm_wuv,
-                        const __grid_constant__ CUtensorMap tm_wuk,
-                        const __grid_constant__ CUtensorMap tm_qn,
-                        const __grid_constant__ CUtensorMap tm_pieces, AttnParams p) {
+                        const __grid_constant__ CUtensorMap tm_op, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t rank = cluster_ctarank();
@@ -698,21 +344,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     }
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
-    mbar_init(bar(B_WFULL), 1);
-    mbar_init(bar(B_UDONE), 1);
-    if constexpr (FUSED) {
-      for (int k = 0; k < FOLD_MAX_STAGES; ++k) {
-        mbar_init(bar(B_FFULL + k), 1);
-        mbar_init(bar(B_FEMPTY + k), 1);
-      }
-      for (int k = 0; k < 2; ++k) {
-        mbar_init(bar(B_FACC + k), 1);
-        mbar_init(bar(B_FFREE + k), 128);
-      }
-      mbar_init(bar(B_FDONE), 1);
-      mbar_init(bar(B_OFULL), 1);
-      mbar_init(bar(B_DDONE), 1);
-    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(slot), 512);
@@ -721,23 +352,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *slot;
   const int nsplit = (T + p.chunk - 1) / p.chunk;
-  // A CTA whose piece lies past its sequence's end has no attention to do.
-  // Both CTAs of a cluster share the piece, so they leave (or, in the fused
-  // kernel, skip the attention) together and never touch the peer.
-  const bool active = split < nsplit;
-  if (!FUSED && !active) {
+  if (split >= nsplit) {  // both CTAs of the cluster leave together, the peer untouched
     if (warp == 1) tmem_dealloc(tmem, 512);
     return;
   }
-  const int gid = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-  const int nctas = gridDim.x * gridDim.y * gridDim.z;
-  const uint32_t fold_base = smem_u32(smem + FOLD_BASE);
   const int row0 = tile * BM;
   const int l_last = min(p.R - 1, row0 + BM - 1) / p.H;
   const int vis_end = T - p.L + l_last + 1;
   const int kv0 = split * p.chunk;
   const int kv1 = min(min(kv0 + p.chunk, T), vis_end);
-  const int ntiles = active && kv1 > kv0 ? (kv1 - kv0 + BN - 1) / BN : 0;
+  const int ntiles = kv1 > kv0 ? (kv1 - kv0 + BN - 1) / BN : 0;
   // arm the exchange barriers for tiles 0 and 1 (the peer's bulk copies count
   // them down), then publish the setup to the peer: each role waits for the
   // peer's setup only before its first access to the peer, so the KV loads,
@@ -746,12 +370,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     if (ntiles > 0) mbar_arrive_expect_tx(bar(B_XFULL), X_BYTES);
     if (ntiles > 1) mbar_arrive_expect_tx(bar(B_XFULL + 1), X_BYTES);
   }
-  if (active) cluster_arrive();
-  pdl_launch_dependents();  // the next kernel may launch; it waits for this grid
+  cluster_arrive();
+  pdl_launch_dependents();  // the merge may launch; it waits for this grid
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && ntiles > 0) {
       bool ok = true;
       prefetch_tmap(&tm_ckv);
       const int qrow = b * p.R + row0;
@@ -779,48 +403,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
                       (int)y);
         tma_load_2d(st + 4 * KV_CHUNK, &tm_kr, bar(B_KVFULL + s), (int)rank * 32, (int)y);
       };
-      // the cache does not depend on the preceding kernel: start every stage
-      // now -- in the fused kernel the first two, with the fold's operands in
-      // the other two (they follow once the fold is done)
+      // the cache does not depend on the preceding kernel: start every stage now
       const int pre = min(ntiles, STAGES);
-      int started = 0;
-      if constexpr (FUSED) {
-        started = min(ntiles, 2);
-        for (int i = 0; i < started; ++i) load_kv(i);
-        fold_produce(p, tm_wuk, tm_qn, fold_base, bars, gid, nctas);
+      for (int i = 0; i < pre; ++i) load_kv(i);
+      // q_rope is a call input; it still waits so no read overtakes the predecessor
+      pdl_wait();
+      mbar_arrive_expect_tx(bar(B_QFULL), Q_ROPE);
+      tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
+      // The unembedding weights are read right after this kernel; at verify
+      // widths the attention leaves HBM mostly idle, so each CTA pulls a slice
+      // into L2 -- once its own first KV tiles have landed, so that the two do
+      // not share the HBM bandwidth the first tiles wait for.
+      if (p.pf != nullptr) {
+        mbar_wait(bar(B_KVFULL + (pre - 1) % STAGES), 0);
+        const size_t nct = (size_t)gridDim.x * gridDim.y * gridDim.z;
+        const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const size_t slice = ((p.pf_bytes + nct - 1) / nct + 4095) & ~(size_t)4095;
+        for (size_t o = id * slice; o < min(p.pf_bytes, (id + 1) * slice); o += 32768)
+          prefetch_l2(p.pf + o, (uint32_t)min((size_t)32768, p.pf_bytes - o));
       }
-      if (ntiles > 0) {
-        for (int i = started; i < pre; ++i) load_kv(i);
-        // q_rope is a call input; it still waits so no read overtakes the predecessor
-        pdl_wait();
-        mbar_arrive_expect_tx(bar(B_QFULL), Q_ROPE);
-        tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, qrow);
-        // The unembedding weights are read right after this kernel; at verify
-        // widths the attention leaves HBM mostly idle, so each CTA pulls a slice
-        // into L2 -- once its own first KV tiles have landed, so that the two do
-        // not share the HBM bandwidth the first tiles wait for.
-        if (p.pf != nullptr) {
-          mbar_wait(bar(B_KVFULL + (pre - 1) % STAGES), 0);
-          const size_t nct = (size_t)gridDim.x * gridDim.y * gridDim.z;
-          const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-          const size_t slice = ((p.pf_bytes + nct - 1) / nct + 4095) & ~(size_t)4095;
-          for (size_t o = id * slice; o < min(p.pf_bytes, (id + 1) * slice); o += 32768)
-            prefetch_l2(p.pf + o, (uint32_t)min((size_t)32768, p.pf_bytes - o));
-        }
-        int issued = pre;
-        for (int i = STAGES; i < ntiles; ++i) {
-          wait_or_fail(ok, bar(B_KVEMPTY + i % STAGES), ((i / STAGES) - 1) & 1, 10);
-          if (!ok) break;
-          load_kv(i);
-          issued = i + 1;
-        }
-        // nothing this thread started may still be landing when the CTA exits
-        mbar_wait(bar(B_QFULL), 0);
-        for (int i = max(issued - STAGES, 0); i < issued; ++i)
-          mbar_wait(bar(B_KVFULL + i % STAGES), (i / STAGES) & 1);
+      int issued = pre;
+      for (int i = STAGES; i < ntiles; ++i) {
+        wait_or_fail(ok, bar(B_KVEMPTY + i % STAGES), ((i / STAGES) - 1) & 1, 10);
+        if (!ok) break;
+        load_kv(i);
+        issued = i + 1;
       }
+      // nothing this thread started may still be landing when the CTA exits
+      mbar_wait(bar(B_QFULL), 0);
+      for (int i = max(issued - STAGES, 0); i < issued; ++i)
+        mbar_wait(bar(B_KVFULL + i % STAGES), (i / STAGES) & 1);
     }
-    if (active) cluster_wait();  // (this role never touches the peer)
+    cluster_wait();  // (this role never touches the peer)
   } else if (warp == 1) {
     // ------------------------------------------------------- score-MMA issuer
     // S(i) = Q . K(i)^T over this CTA's 256 latent (Q from TMEM) + 32 RoPE
@@ -828,9 +442,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     // The scores run ahead of the softmax on their own; P.V comes from another
     // warp (MMA issue is nearly synchronous, so a wait in one issuer leaves
     // the tensor pipe to the other).
-    if constexpr (FUSED) {
-      if (lane == 0) fold_mma(p, fold_base, tmem, bars, gid, nctas);
-    }
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
       const uint64_t dqr = sdesc_sw64(sQR, 512);
@@ -859,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0);
     }
-    if (active) cluster_wait();
+    cluster_wait();
   } else if (warp == 2) {
     // --------------------------------------------------------- P.V issuer
     // O += P(j) . V(j) over this CTA's 256 latent columns of the KV tile; the
@@ -884,13 +495,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mma_commit(bar(B_DRAIN + 1));
       mbar_wait(bar(B_DRAIN + 1), 0);
     }
-    if (active) cluster_wait();
+    cluster_wait();
   } else if (warp >= XCHG_WARP0) {
     // ------------------------------------------------------- score exchange
     // One warp per TMEM lane quarter ships this CTA's partial scores of each
     // tile to the peer as soon as the score MMAs finish, up to two tiles ahead
     // of the softmax, so the softmax's own steps never wait on a copy.
-    if (active) cluster_wait();  // the peer's exchange barriers are set up
+    cluster_wait();  // the peer's exchange barriers are set up
     if (ntiles > 0) {
       bool ok = true;
       const int quarter = warp & 3;
@@ -964,29 +575,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     int armed = min(ntiles, 2), received = 0;  // exchange phases armed / completed
     float m_run = -INFINITY, l_part = 0.f;
     float s[CPT];
-    if constexpr (FUSED) {
-      // the fold's epilogue (after the dependency wait: the previous call may
-      // still read its Q tiles), then every CTA of the grid must be past it
-      // before any reads the Q tiles
-      pdl_wait();
-      fold_store(p, tmem, bars, gid, nctas, wg, warp, lane);
-      __threadfence();
-      named_bar_sync(1, SOFTMAX_THREADS);
-      if (sm_tid == 0) {
-        red_release_gpu_add(p.counters, 1u);
-        if (active && ld_acquire_gpu(p.counters) < (uint32_t)nctas) {
-          const long long t0 = clock64();
-          while (ld_acquire_gpu(p.counters) < (uint32_t)nctas) {
-            if (clock64() - t0 > kWaitLimitCycles) {
-              report_timeout(44);
-              break;
-            }
-            __nanosleep(32);
-          }
-        }
-      }
-      named_bar_sync(1, SOFTMAX_THREADS);
-    }
     if (ntiles > 0) {
       // this CTA's latent query columns into TMEM as bf16 pairs (the fold wrote them)
       pdl_wait();
@@ -1000,8 +588,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         uint32_t v[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          // (L2 reads: in the fused kernel other CTAs wrote these in this grid)
-          const uint4 x = __ldcg(src + (size_t)(8 * k + u) * 128);
+          const uint4 x = src[(size_t)(8 * k + u) * 128];
           v[4 * u] = x.x;
           v[4 * u + 1] = x.y;
           v[4 * u + 2] = x.z;
@@ -1014,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_arrive(bar(B_QTMEM));
       load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
     }
-    if (active) cluster_wait();  // the peer's barriers are set up before the first remote arrive
+    cluster_wait();  // the peer's barriers are set up before the first remote arrive
     // One tile of the softmax; `s` holds tile i's own (rounded) partial on
     // entry and tile i+1's on exit (read once P(i) is out, so only one tile's
     // scores are ever live in registers).
@@ -1131,7 +718,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       for (int j = received; j < armed; ++j)
         mbar_wait_cluster(bar(B_XFULL + (j & 1)), (j >> 1) & 1);
     // ---------------------------------------------------------------- epilogue
-    if (active) {
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
     pdl_wait();  // the partials may still be read by the previous call's merge
     tc_fence_after();
@@ -1181,49 +767,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         tma_store_3d(&tm_op, sKV + bx * (BM * 128), (int)rank * 256 + 64 * bx, row0,
                      b * p.splits + split);
       bulk_commit();
-      if constexpr (FUSED) {
-        // other CTAs of the sequence read the pieces in this grid: the writes
-        // must be complete, and ordered before the arrival below
-        bulk_wait_all();
-        fence_proxy_async_global();
-      } else {
-        // the staging may be released once the stores have read it; their
-        // writes are complete when the grid is (the merge reads them after
-        // its dependency wait)
-        bulk_wait_read();
-      }
+      // the staging may be released once the stores have read it; their
+      // writes are complete when the grid is (the merge reads them after its
+      // dependency wait)
+      bulk_wait_read();
     }
     if (live && rank == 0 && wg == 0) {
       float* mlp = p.ml + (((size_t)b * p.splits + split) * p.R + row) * 2;
       mlp[0] = m_run == -INFINITY ? -FLT_MAX : m_run;
       mlp[1] = l_tot;
     }
-    if constexpr (FUSED) __threadfence();
-    }
-  }
-  if constexpr (FUSED) {
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (active) fused_unembed_merge(p, tm_wuv, tm_pieces, smem, tmem, bars, b, split, nsplit);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 512);
-  if (active) cluster_sync();  // no peer access may outlive this CTA
-  if constexpr (FUSED) {
-    // The last CTA of the grid to leave puts the counters back to zero for
-    // the next call (every other CTA is past every wait by then).
-    if (threadIdx.x == 0) {
-      __threadfence();
-      if (atomicAdd(p.counters + 1, 1u) == (uint32_t)nctas - 1) {
-        p.counters[0] = 0u;
-        p.counters[1] = 0u;
-        for (int i = 0; i < p.B; ++i) p.counters[2 + i] = 0u;
-        __threadfence();
-      }
-    }
-  }
+  cluster_sync();  // no peer access may outlive this CTA
 }
 
 // =========================================================================
@@ -1246,6 +804,15 @@ struct MergeParams {
   int R, chunk, splits;
   int rows;                     // B*R
 };
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
 
 template <int CPL, int W>  // W warps take every W-th piece
 __global__ void __launch_bounds__(32 * W) merge_sm103(MergeParams p) {
@@ -1407,6 +974,220 @@ __global__ void __launch_bounds__(32 * MR_ROWS) merge_rows_sm103(MergeParams p) 
   }
 }
 
+// =========================================================================
+// unembedding + merge of the split-KV pieces
+// =========================================================================
+// The merge and the unembedding commute.  With the combine weights of row
+// (l, h) of sequence b over its pieces s,
+//   w_{l,s} = 2^(m_s - M_l) l_s / sum_s' 2^(m_s' - M_l) l_s',
+//   out[b, l, h, :] = (sum_s w_{l,s} (O_s / l_s)[l, h, :]) . W_UV[h]
+//                   = sum_s w_{l,s} ((O_s / l_s)[l, h, :] . W_UV[h]).
+// One CTA per (head h, 128-column tile mt, block of sequences).  Its W_UV
+// tile (K = 512 rows, MN-major) is loaded with TMA before the dependency
+// wait (W_UV does not depend on the attention, which also pulled it into
+// L2).  After the wait, chunk after chunk: one 4-D TMA box brings the bf16
+// rows (O_s / l_s)[l, h, :] of every piece s of Lc verify rows of one
+// sequence (rows ordered by l, then s; Lc * splits <= 64) into shared memory
+// as the K-major B operand, and one GEMM D[128 x rows] = W_UV tile^T x rows^T
+// lands in one of two 64-column TMEM slabs.  Meanwhile three warps compute
+// every chunk's combine weights from (m, l), in the chunk's column order; the
+// epilogue warpgroup sums each verify row's columns with them and writes the
+// row.  All the piece rows of a chunk are in flight at once, and o_lat is
+// never formed.
+struct UnembedMergeParams {
+  const float* ml;        // [B, splits, R, 2]
+  const int32_t* lens;
+  __nv_bfloat16* out;     // [B, L, H, v]
+  int B, L, H, R, v, splits, chunk;
+  int Lc;                 // verify rows per chunk (Lc * splits <= 64)
+  int seq_per_cta;
+};
+constexpr int UM_THREADS = 256;            // warp 0 issues, 1..3 weights, 4..7 epilogue
+constexpr int UM_W = 2 * kLat * 128;       // W_UV tile
+constexpr int UM_B = 8 * 64 * 128;         // one chunk of at most 64 piece rows
+constexpr int UM_MAX_CHUNKS = 64;          // chunks per CTA (weights table of 16 KB)
+constexpr int UM_OFF_B = UM_W;
+constexpr int UM_OFF_WT = UM_OFF_B + UM_B;
+constexpr int UM_OFF_BAR = UM_OFF_WT + UM_MAX_CHUNKS * 64 * 4;
+constexpr int UM_SMEM = UM_OFF_BAR + 128 + 1024;
+static_assert(UM_SMEM <= 232448, "shared memory per CTA");
+enum { UB_WFULL = 0, UB_OFULL = 1, UB_DONE = 2, UB_FREE = 4, UB_COUNT = 6 };
+
+__global__ void __launch_bounds__(UM_THREADS, 1)
+    unembed_merge_sm103(const __grid_constant__ CUtensorMap tm_wuv,
+                        const __grid_constant__ CUtensorMap tm_pieces, UnembedMergeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const uint32_t sW = smem_u32(smem), sB = smem_u32(smem + UM_OFF_B);
+  float* wts = (float*)(smem + UM_OFF_WT);  // [chunk][64] weights in column order
+  uint64_t* bars = (uint64_t*)(smem + UM_OFF_BAR);
+  uint32_t* slot = (uint32_t*)(bars + UB_COUNT);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nmt = p.v / 128;
+  const int h = blockIdx.x / nmt, mt = blockIdx.x - h * nmt;
+  const int b0 = blockIdx.y * p.seq_per_cta;
+  const int nb = min(p.seq_per_cta, p.B - b0);
+  const int S = p.splits, Lc = p.Lc;
+  const int cps = (p.L + Lc - 1) / Lc;  // chunks per sequence
+  const int nch = nb * cps;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(UB_WFULL), 1);
+    mbar_init(bar(UB_OFULL), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(UB_DONE + k), 1);
+      mbar_init(bar(UB_FREE + k), 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(slot), 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  pdl_launch_dependents();  // the next kernel may start its own independent loads
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA + MMA issue (one thread)
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(UB_WFULL), UM_W);
+      for (int kc = 0; kc < kLat / 64; ++kc)
+        for (int j = 0; j < 2; ++j)
+          tma_load_2d(sW + j * kLat * 128 + kc * 8192, &tm_wuv, bar(UB_WFULL), mt * 128 + 64 * j,
+                      h * kLat + 64 * kc);
+      pdl_wait();  // the pieces come from the attention
+      const uint32_t slab = 128u * S * Lc;
+      const int N = (S * Lc + 15) & ~15;
+      const uint32_t idesc = idesc_bf16(128, N, 1, 0);
+      for (int c = 0; c < nch && ok; ++c) {
+        const int b = b0 + c / cps, l0 = (c % cps) * Lc;
+        mbar_arrive_expect_tx(bar(UB_OFULL), 8 * slab);
+        for (int kc = 0; kc < kLat / 64; ++kc)
+          tma_load_4d(sB + kc * 8192, &tm_pieces, bar(UB_OFULL), 64 * kc, h, b * S, l0);
+        wait_or_fail(ok, bar(UB_OFULL), c & 1, 50);
+        if (c == 0) wait_or_fail(ok, bar(UB_WFULL), 0, 51);
+        if (c >= 2) wait_or_fail(ok, bar(UB_FREE + (c & 1)), ((c - 2) >> 1) & 1, 52);
+        if (!ok) break;
+        tc_fence_after();
+        for (int kc = 0; kc < kLat / 64; ++kc)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + 64 * (c & 1),
+                     sdesc_sw128(sW + (kc * 64 + ks * 16) * 128, kLat * 128, 1024),
+                     sdesc_sw128(sB + kc * 8192 + ks * 32, 16, 1024), idesc, (kc | ks) != 0);
+        mma_commit(bar(UB_DONE + (c & 1)));
+        // the chunk buffer is free for the next box once these MMAs are done
+        wait_or_fail(ok, bar(UB_DONE + (c & 1)), (c >> 1) & 1, 53);
+        if (!ok) break;
+      }
+      // nothing this thread started may still be landing when the CTA exits
+      mbar_wait(bar(UB_WFULL), 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------ combine weights (3 warps)
+    pdl_wait();
+    for (int row = warp - 1; row < nch * Lc; row += 3) {  // (chunk, verify row in it)
+      const int c = row / Lc, li = row - c * Lc;
+      const int b = b0 + c / cps, l = (c % cps) * Lc + li;
+      float* wt = wts + c * 64 + li * S;
+      if (l >= p.L) {
+        for (int s = lane; s < S; s += 32) wt[s] = 0.f;
+        continue;
+      }
+      const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
+      const size_t base = (size_t)b * S * p.R + (size_t)l * p.H + h;
+      float2 ml[2];
+      float M = -FLT_MAX;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int sj = lane + 32 * j;
+        ml[j] = sj < nsplit ? *(const float2*)(p.ml + (base + (size_t)sj * p.R) * 2)
+                            : make_float2(-FLT_MAX, 0.f);
+        if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
+      }
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, o));
+      float w[2], sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        w[j] = ml[j].y > 0.f ? ex2(ml[j].x - M) * ml[j].y : 0.f;
+        sum += w[j];
+      }
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
+      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (lane + 32 * j < S) wt[lane + 32 * j] = w[j] * inv;
+    }
+    named_bar_sync(1, 224);  // weights -> epilogue
+  } else {
+    // ------------------------------------------------ epilogue (one warpgroup)
+    // TMEM lane m is output column 128 mt + m; a chunk's column j is piece
+    // j % S of its verify row j / S.  Pieces past a sequence's last have
+    // weight 0 and rows that were never written: they are skipped, not
+    // multiplied (the rows may hold anything).
+    named_bar_sync(1, 224);
+    const int m = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int c = 0; c < nch; ++c) {
+      const int b = b0 + c / cps, l0 = (c % cps) * Lc;
+      const int rows = min(Lc, p.L - l0) * S;
+      wait_or_fail(ok, bar(UB_DONE + (c & 1)), (c >> 1) & 1, 54);
+      tc_fence_after();
+      if (ok) {
+        __nv_bfloat16* o = p.out + (((size_t)b * p.L + l0) * p.H + h) * p.v + mt * 128 + m;
+        const float* wt = wts + c * 64;
+        float acc = 0.f;
+        int row_end = S - 1, l = 0;
+        for (int j0 = 0; j0 < rows; j0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + 64 * (c & 1) + j0, v);
+          float wv[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 w4 = *(const float4*)(wt + j0 + 4 * q);
+            wv[4 * q] = w4.x;
+            wv[4 * q + 1] = w4.y;
+            wv[4 * q + 2] = w4.z;
+            wv[4 * q + 3] = w4.w;
+          }
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = j0 + e;
+            if (j < rows) {
+              if (wv[e] != 0.f) acc = fmaf(wv[e], __uint_as_float(v[e]), acc);
+              if (j == row_end) {  // verify row l0 + l complete
+                o[(size_t)l * p.H * p.v] = __float2bfloat16_rn(acc);
+                acc = 0.f;
+                row_end += S;
+                ++l;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(UB_FREE + (c & 1)));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// Per-device one-time setup: the kernels' shared-memory opt-in and the number
+// of attention clusters that fit on the device at once (the piece planner
+// sizes its grid with it).  Calls may come from several threads; the first
+// one on a device does the work under a lock.
+struct DeviceSetup {
+  cudaError_t err = cudaSuccess;
+  int slots = 0;
+  bool done = false;
+};
+
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1447,16 +1228,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Per-device one-time setup: the kernels' shared-memory opt-in and the number
-// of attention clusters that fit on the device at once (the fused kernel is
-// only launched when its whole grid does).  Calls may come from several
-// threads; the first one on a device does the work under a lock.
-struct DeviceSetup {
-  cudaError_t err = cudaSuccess;
-  int slots = 0;
-  bool done = false;
-};
-
 const DeviceSetup& device_setup() {
   constexpr int kMaxDevices = 64;
   static std::mutex mu;
@@ -1473,8 +1244,8 @@ const DeviceSetup& device_setup() {
   DeviceSetup& d = setups[dev];
   if (d.done) return d;
   cudaError_t e = set_smem(swapab_gemm_sm103, gemm_smem(kLat, 64));
-  if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103<false>, ATTN_SMEM);
-  if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103<true>, ATTN_SMEM);
+  if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103, ATTN_SMEM);
+  if (e == cudaSuccess) e = set_smem(unembed_merge_sm103, UM_SMEM);
   int slots = 0;
   if (e == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
@@ -1488,9 +1259,10 @@ const DeviceSetup& device_setup() {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaOccupancyMaxActiveClusters(&slots, absorbed_attn_sm103<true>, &cfg);
+    if (cudaOccupancyMaxActiveClusters(&slots, absorbed_attn_sm103, &cfg) != cudaSuccess)
+      slots = 0;
   }
-  if (e != cudaSuccess || slots <= 0) {
+  if (slots <= 0) {
     cudaGetLastError();
     slots = device_sm_count() / 2;
   }
@@ -1501,6 +1273,8 @@ const DeviceSetup& device_setup() {
 }
 
 }  // namespace
+
+int absorbed_cluster_slots() { return device_setup().slots; }
 
 cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   const int BL = p.B * p.L;
@@ -1533,17 +1307,9 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
   const DeviceSetup& ds = device_setup();
   if (ds.err != cudaSuccess) return ds.err;
   cudaError_t e;
-  // the fused kernel folds the queries itself, in units of at most 64 rows
-  const int NBq = ((BL + 15) / 16) * 16 > 64 ? 64 : ((BL + 15) / 16) * 16;
-  const int fsb = (2 * p.n * 128 + (p.n / 64) * NBq * 128 + 1023) & ~1023;
-  CUtensorMap tm_qn_fused;
-  if (p.fused) {
-    if (!make_tmap_bf16_2d(&tm_qn_fused, a.q_nope, (uint64_t)p.H * p.n, BL,
-                           (uint64_t)p.H * p.n * 2, 64, NBq, 128))
-      return cudaErrorInvalidValue;
-  } else {
-    KernelTimer kt("fold_sm103", a.stream);
+  {
     GemmParams gp{q_lat, BL, p.H, p.n, kLat, NBf, p.L, (R + BM - 1) / BM};
+    KernelTimer kt("fold_sm103", a.stream);
     e = launch_pdl(swapab_gemm_sm103, dim3(kLat / 128, p.H, (BL + NBf - 1) / NBf), dim3(128),
                    gemm_smem(p.n, NBf), a.stream, tm_wuk, tm_qn, gp);
     if (e != cudaSuccess) return e;
@@ -1569,38 +1335,50 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.ml = ml;
     ap.pf = (const char*)a.W_UV;
     ap.pf_bytes = (size_t)p.H * kLat * p.v * 2;
-    ap.counters = (uint32_t*)(a.ws + p.off_cnt);
-    ap.out = (__nv_bfloat16*)a.out;
-    ap.q_lat_w = q_lat;
-    ap.v = p.v;
-    ap.n = p.n;
-    ap.BL = BL;
-    ap.NBf = NBq;
-    ap.nrb = (BL + NBq - 1) / NBq;
-    ap.fsb = fsb;
-    ap.fstages = FOLD_BYTES / fsb < FOLD_MAX_STAGES ? FOLD_BYTES / fsb : FOLD_MAX_STAGES;
-    ap.Lc = 64 / p.splits > 0 ? 64 / p.splits : 1;
-    const dim3 grid(2 * ((R + BM - 1) / BM), p.splits, p.B);
-    if (p.fused) {
-      // the piece rows of one head as [l][piece][h][col]: row (b, s, l, h) of
+    KernelTimer kt("absorbed_attn_sm103", a.stream);
+    e = launch_pdl(absorbed_attn_sm103, dim3(2 * ((R + BM - 1) / BM), p.splits, p.B),
+                   dim3(ATTN_THREADS),
+                   ATTN_SMEM, a.stream, tm_qr, tm_ckv, tm_kr, tm_op, ap);
+    if (e != cudaSuccess) return e;
+  }
+  if (p.splits <= 64) {
+    // unembedding + merge in one kernel
+    UnembedMergeParams up;
+    up.ml = ml;
+    up.lens = a.lens;
+    up.out = (__nv_bfloat16*)a.out;
+    up.B = p.B;
+    up.L = p.L;
+    up.H = p.H;
+    up.R = R;
+    up.v = p.v;
+    up.splits = p.splits;
+    up.chunk = p.chunk;
+    up.Lc = 64 / p.splits < p.L ? 64 / p.splits : p.L;
+    // sequences per CTA: about two CTAs per SM at most, and at most
+    // UM_MAX_CHUNKS chunks per CTA
+    const int units = p.H * (p.v / 128);
+    const int cps = (p.L + up.Lc - 1) / up.Lc;
+    int spc = (p.B * units + 2 * device_sm_count() - 1) / (2 * device_sm_count());
+    if (spc < 1) spc = 1;
+    if (spc * cps > UM_MAX_CHUNKS) spc = UM_MAX_CHUNKS / cps > 0 ? UM_MAX_CHUNKS / cps : 1;
+    up.seq_per_cta = spc;
+    if (cps <= UM_MAX_CHUNKS) {
+      // the pieces of one head as [l][piece][h][col]: row (b, s, l, h) of
       // o_part sits at ((b * splits + s) * R + l * H + h) * 512 elements
       CUtensorMap tm_pieces;
       const uint64_t dims[4] = {(uint64_t)kLat, (uint64_t)p.H, (uint64_t)p.B * p.splits,
                                 (uint64_t)p.L};
       const uint64_t strides[3] = {(uint64_t)kLat * 2, (uint64_t)R * kLat * 2,
                                    (uint64_t)p.H * kLat * 2};
-      const uint32_t box[4] = {64, 1, (uint32_t)p.splits, (uint32_t)ap.Lc};
+      const uint32_t box[4] = {64, 1, (uint32_t)p.splits, (uint32_t)up.Lc};
       if (!make_tmap_bf16_4d(&tm_pieces, o_part, dims, strides, box)) return cudaErrorInvalidValue;
-      KernelTimer kt("absorbed_fused_sm103", a.stream);
-      e = launch_pdl(absorbed_attn_sm103<true>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
-                     tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, tm_wuk, tm_qn_fused, tm_pieces, ap);
+      KernelTimer kt("unembed_merge_sm103", a.stream);
+      e = launch_pdl(unembed_merge_sm103, dim3(units, (p.B + spc - 1) / spc), dim3(UM_THREADS),
+                     UM_SMEM, a.stream, tm_wuv, tm_pieces, up);
       if (e != cudaSuccess) return e;
       return cudaGetLastError();
     }
-    KernelTimer kt("absorbed_attn_sm103", a.stream);
-    e = launch_pdl(absorbed_attn_sm103<false>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
-                   tm_qr, tm_ckv, tm_kr, tm_op, tm_wuv, tm_wuk, tm_qn, tm_op, ap);
-    if (e != cudaSuccess) return e;
   }
   {
     MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits, p.B * R};
@@ -1624,11 +1402,6 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
-}
-
-int absorbed_cluster_slots() {
-  const DeviceSetup& ds = device_setup();
-  return ds.slots;
 }
 
 int absorbed_device_status(bool clear) {

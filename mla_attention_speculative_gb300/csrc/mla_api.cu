@@ -204,7 +204,7 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     g.chunk = (int)chunk;
     g.splits = (int)((p->Tmax + chunk - 1) / chunk);
     const int dv = p->branch == MLA_BRANCH_ABSORBED ? p->r : p->v;
-    size_t off = kWorkspaceHeader;
+    size_t off = 0;
     if (p->branch == MLA_BRANCH_ABSORBED) {
       g.off_qlat = off;
       off = align256(off + nrow * p->r * sizeof(float));
@@ -226,8 +226,8 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     SplitPlan& f = p->fast;
     f.chunk = p->Tmax;
     f.splits = 1;
-    f.off_exp = kWorkspaceHeader;
-    f.bytes = align256(kWorkspaceHeader + fast_materialised_workspace(*p));
+    f.off_exp = 0;
+    f.bytes = align256(fast_materialised_workspace(*p));
   } else if (p->fast_ok) {
     // Tensor-core split-KV: clusters of 2 CTAs, one per (128-row tile, piece).
     // Pick the piece length ct (in 64-row KV tiles) that minimises
@@ -240,46 +240,19 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
     const int64_t row_tiles = (rows + 127) / 128;
     const int64_t slots = absorbed_cluster_slots();
     const int64_t max_tiles = (p->Tmax + 63) / 64;
-    // the best piece length among those of at least ct_min tiles
-    auto best_piece = [&](int64_t ct_min) {
-      int64_t best_ct = max_tiles, best_cost = -1;
-      for (int64_t ct = max_tiles; ct >= ct_min; --ct) {
-        int64_t clusters = 0;
-        for (int b = 0; b < batch; ++b)
-          clusters += row_tiles * (((lens[b] + 63) / 64 + ct - 1) / ct);
-        const int64_t cost = ((clusters + slots - 1) / slots) * (ct + kClusterOverhead);
-        if (best_cost < 0 || cost < best_cost) {
-          best_cost = cost;
-          best_ct = ct;
-        }
-      }
-      return best_ct;
-    };
-    // The single-kernel path (fold, attention, unembedding, merge) needs its
-    // whole grid on the GPU at once -- its CTAs wait for one another after the
-    // fold and before the merge -- a verify block of at most kFusedMaxL rows,
-    // at most kFusedMaxSplits pieces per sequence, and its counters in the
-    // workspace header; it is taken whenever some piece length allows it.
-    auto fits_fused = [&](int64_t ct) {
-      const int64_t splits = (p->Tmax + ct * 64 - 1) / (ct * 64);
-      const int64_t lc = kFusedMaxSplits / splits;
-      return splits <= kFusedMaxSplits && row_tiles * splits * batch <= slots &&
-             L <= kFusedMaxL && (L + lc - 1) / lc <= 8 &&
-             (size_t)(2 + batch) * sizeof(uint32_t) <= kWorkspaceHeader;
-    };
-    int64_t ct = best_piece(1);
-    p->fused = fits_fused(ct);
-    if (!p->fused) {
-      const int64_t ct64 = best_piece((max_tiles + kFusedMaxSplits - 1) / kFusedMaxSplits);
-      if (fits_fused(ct64)) {
-        ct = ct64;
-        p->fused = true;
+    int64_t ct = max_tiles, best_cost = -1;
+    for (int64_t c = max_tiles; c >= 1; --c) {
+      int64_t clusters = 0;
+      for (int b = 0; b < batch; ++b) clusters += row_tiles * (((lens[b] + 63) / 64 + c - 1) / c);
+      const int64_t cost = ((clusters + slots - 1) / slots) * (c + kClusterOverhead);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        ct = c;
       }
     }
     f.chunk = (int)(ct * 64);
     f.splits = (int)((p->Tmax + f.chunk - 1) / f.chunk);
-    f.off_cnt = 0;  // the fused kernel's counters, in the zeroed header
-    size_t off = kWorkspaceHeader;
+    size_t off = 0;
     f.off_qlat = off;  // Q tiles: every sequence's rows padded to 128-row tiles
     off = align256(off + (size_t)batch * row_tiles * 128 * p->r * 2);
     f.off_opart = off;  // bf16 O / l of every piece

@@ -15,7 +15,7 @@ namespace mla {
 struct SplitPlan {
   int chunk = 0;    // KV rows per piece (multiple of 64)
   int splits = 0;   // largest number of pieces of any sequence
-  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0, off_cnt = 0;
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0;
   size_t bytes = 0;
 };
 
@@ -38,12 +38,9 @@ struct Plan {
   SplitPlan generic;   // CUDA-core kernels, any geometry and paging
   SplitPlan fast;      // tcgen05/TMA kernels of the chosen branch
   bool fast_ok = false;
-  // tensor-core absorbed branch: attention, merge and unembedding in one
-  // kernel (the grid fits on the GPU at once and L <= kFusedMaxL)
-  bool fused = false;
   size_t ws_bytes = 0;
   // the layout of the family that runs (copied from generic or fast)
-  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0, off_cnt = 0;
+  size_t off_qlat = 0, off_opart = 0, off_ml = 0, off_exp = 0, off_olat = 0;
   void use(const SplitPlan& sp) {
     chunk = sp.chunk;
     splits = sp.splits;
@@ -52,18 +49,10 @@ struct Plan {
     off_ml = sp.off_ml;
     off_exp = sp.off_exp;
     off_olat = sp.off_olat;
-    off_cnt = sp.off_cnt;
   }
 };
 
-// Widest verify block, and most split-KV pieces per sequence, the fused
-// absorbed kernel handles.
-constexpr int kFusedMaxL = 32;
-constexpr int kFusedMaxSplits = 64;
-// Every workspace starts with this many bytes that must be zero before its
-// first call and that every call leaves zero (the fused absorbed kernel's
-// arrival counters live there).
-constexpr size_t kWorkspaceHeader = 512;
+
 
 // Device-side view of the cache addressing shared by all kernels.
 struct CacheView {

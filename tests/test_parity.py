@@ -202,9 +202,8 @@ def test_dominant_key_dsv3_T8192(L):
     (Geometry(H=40), 5, [700]),            # 200 rows: second Q tile mostly padding
 ])
 def test_nan_poisoned_workspace(geom, L, lens):
-    # the workspace starts as all-ones bytes (NaN in bf16 and fp32) past its
-    # zeroed header: padded query rows and any scratch read before it is
-    # written must not leak
+    # the workspace starts as all-ones bytes (NaN in bf16 and fp32): padded
+    # query rows and any scratch read before it is written must not leak
     case = make_case(geom, L, lens, seed=220 + L)
     want = oracle_out(case)
     d = device_tensors(case)
@@ -212,7 +211,6 @@ def test_nan_poisoned_workspace(geom, L, lens):
         g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope)
         need = B.mla_workspace_bytes(g, L, lens, mode)
         ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
-        ws[:B.WORKSPACE_HEADER].zero_()
         out, branch = run_gpu(case, mode, dev_t=d, workspace=ws)
         _check_branch(case, mode, branch)
         compare(out, want, torch.bfloat16, f"nan workspace {mode}")
@@ -270,17 +268,17 @@ def test_long_context(L, lens):
 # geometries (contiguous and 64-row pages), the CUDA-core kernels otherwise
 # ---------------------------------------------------------------------------
 
-# absorbed: one kernel for fold + attention + merge + unembedding when the
-# grid fits on the GPU at once, else separate fold, merge and unembedding
-TC_ABSORBED_FUSED = {"absorbed_fused_sm103"}
-TC_ABSORBED = {"fold_sm103", "absorbed_attn_sm103", "merge_sm103", "unembed_sm103"}
+# absorbed: fold, attention, then the unembedding and the merge in one kernel
+# (at most 64 pieces per sequence), else a merge kernel and the unembedding
+TC_ABSORBED = {"fold_sm103", "absorbed_attn_sm103", "unembed_merge_sm103"}
+TC_ABSORBED_MANY_PIECES = {"fold_sm103", "absorbed_attn_sm103", "merge_sm103", "unembed_sm103"}
 TC_MATERIALISED = {"expand_sm103", "mat_attn_sm103"}
 
 
 @pytest.mark.parametrize("mode,dtype,page,want", [
-    ("absorbed", torch.bfloat16, 0, TC_ABSORBED_FUSED),
+    ("absorbed", torch.bfloat16, 0, TC_ABSORBED),
     ("materialised", torch.bfloat16, 0, TC_MATERIALISED),
-    ("absorbed", torch.bfloat16, 64, TC_ABSORBED_FUSED),
+    ("absorbed", torch.bfloat16, 64, TC_ABSORBED),
     ("materialised", torch.bfloat16, 64, TC_MATERIALISED),
     ("materialised", torch.bfloat16, 16, {"generic_expand", "generic_materialised_attention",
                                           "generic_combine"}),
@@ -373,11 +371,14 @@ def test_prepared_call_runs_on_new_buffer_contents(mode, page):
     compare(call.out, oracle_out(case), torch.bfloat16, f"prepared {mode}, new queries")
 
 
-def test_kernel_routing_multi_wave_absorbed_is_unfused():
-    # 32 sequences of 2048 positions, 8 rows x 128 heads each: far more
-    # clusters than fit on the GPU at once, so merge and unembedding run as
-    # their own kernels
-    case = make_case(DSV3, 8, [2048] * 32, seed=72, page_size=64)
+@pytest.mark.parametrize("geom,L,lens,want", [
+    # 76 pieces of one 64-position tile: more than the combined kernel takes
+    (Geometry(H=8), 1, [76 * 64], TC_ABSORBED_MANY_PIECES),
+    # 32 sequences, several sequences per unembedding CTA
+    (DSV3, 8, [2048] * 32, TC_ABSORBED),
+])
+def test_kernel_routing_absorbed_merge_forms(geom, L, lens, want):
+    case = make_case(geom, L, lens, seed=72, page_size=64)
     B.mla_kernel_timing_enable(True)
     try:
         B.mla_kernel_timing_read(reset=True)
@@ -385,46 +386,18 @@ def test_kernel_routing_multi_wave_absorbed_is_unfused():
         ran = set(B.mla_kernel_timing_read(reset=True))
     finally:
         B.mla_kernel_timing_enable(False)
-    assert ran == TC_ABSORBED, ran
-    heads = [0, 77, 127]
-    compare(out[:, :, heads], oracle_out(case, heads=heads), torch.bfloat16, "multi-wave")
+    assert ran == want, ran
+    heads = [0, geom.H // 2, geom.H - 1]
+    compare(out[:, :, heads], oracle_out(case, heads=heads), torch.bfloat16, f"merge forms L={L}")
 
 
-@pytest.mark.parametrize("L,lens", [(1, [8192]), (16, [8192]), (32, [4096, 900]), (33, [2048])])
-def test_fused_and_unfused_agree_in_structure(L, lens):
-    # widths on both sides of the fused kernel's limit (32 rows per sequence)
+@pytest.mark.parametrize("L,lens", [(1, [8192]), (16, [8192]), (32, [4096, 900]), (40, [2048])])
+def test_unembed_merge_chunks(L, lens):
+    # v = 256 (two column tiles per head), chunks of several verify rows, two
+    # sequences of different piece counts
     case = make_case(Geometry(H=64, n=128, v=256), L, lens, seed=300 + L)
     heads = [0, 31, 63]
     rows = sample_indices(L, 4, L)
     out, _ = run_gpu(case, "absorbed")
     compare(out[:, rows][:, :, heads], oracle_out(case, heads=heads, rows=rows), torch.bfloat16,
-            f"fused-limit L={L}")
-
-
-def test_repeated_fused_calls_leave_the_header_zero():
-    # the fused kernel's arrival counters are back at zero after every call,
-    # so one workspace serves call after call (graph replays included)
-    case = make_case(Geometry(H=32), 4, [3000], seed=310)
-    d = device_tensors(case)
-    g = B.make_geometry(32, 512, 128, 128, 64)
-    ws = B.new_workspace(B.mla_workspace_bytes(g, 4, [3000], "absorbed"), "cuda")
-    want = oracle_out(case)
-    for _ in range(3):
-        out, _ = run_gpu(case, "absorbed", dev_t=d, workspace=ws)
-        assert int(ws[:B.WORKSPACE_HEADER].count_nonzero()) == 0
-        compare(out, want, torch.bfloat16, "repeated fused")
-    stream = torch.cuda.Stream()
-    with torch.cuda.stream(stream):
-        run_gpu(case, "absorbed", dev_t=d, workspace=ws)     # warm-up on the capture stream
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            out2, _ = B.mla_verify_attention(d["q_nope"], d["q_rope"], d["c_kv"], d["k_rope"],
-                                             d["W_UK"], d["W_UV"], case.cache_lens,
-                                             mode="absorbed", workspace=ws,
-                                             cache_lens_dev=d["lens_dev"])
-    for _ in range(3):
-        graph.replay()
-        torch.cuda.synchronize()
-        B.mla_device_status()
-        assert int(ws[:B.WORKSPACE_HEADER].count_nonzero()) == 0
-        compare(out2, want, torch.bfloat16, "fused graph replay")
+            f"unembed-merge L={L}")
