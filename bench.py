@@ -47,8 +47,9 @@ def _args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-materialised", action="store_true",
-                    help="skip the materialised-branch shapes")
+    ap.add_argument("--no-shapes", "--no-materialised", dest="no_shapes", action="store_true",
+                    help="skip the secondary shapes (crossover sweep, batched paged, long "
+                         "context, materialised)")
     ap.add_argument("--widths", default=None,
                     help="comma-separated verify widths instead of 1,2,4,8,16 (for profiling "
                          "one width; the line then describes that workload, not the headline)")
@@ -79,38 +80,58 @@ def _peaks():
 # the method must do), for the roofline of the dominant kernel.
 # ---------------------------------------------------------------------------
 
-def _work(kernel: str, L: int, T: int, H=128, r=512, n=128, v=128, rope=64):
-    """(bytes, flops) one launch of `kernel` must move / do for one call at (L, T).
+def visible(L: int, T: int) -> int:
+    """Positions the L verify rows of one sequence see together: row l sees
+    t <= T - L + l, so L (T - L) + L (L + 1) / 2 in all (causal work only)."""
+    return L * (T - L) + L * (L + 1) // 2
+
+
+def kernel_work(kernel: str, geom, L: int, lens):
+    """(bytes, flops) one launch of `kernel` must move / do for one call.
 
     Bytes count what the kernel's role needs to cross HBM once, with bf16
-    intermediates (q_lat, o_lat) as the minimal hand-off between kernels; the
-    split-KV partials of an implementation are not counted.  Flops count the
-    contraction the kernel performs (2 per multiply-add)."""
+    intermediates (q_lat, o_lat, the expanded K/V) as the minimal hand-off
+    between kernels; split-KV partials are an implementation cost and are not
+    counted.  Flops count the contraction the kernel performs over the
+    positions each row may see (2 per multiply-add; masked work not counted)."""
     bf = 2
-    rows = L * H
-    cache = T * (r + rope) * bf
-    fold = (H * n * r * bf + rows * n * bf + rows * r * bf, 2 * rows * n * r)
-    attend = (cache + rows * (r + rope) * bf + rows * r * bf,
-              2 * rows * T * (r + rope) + 2 * rows * T * r)
-    unembed = (H * r * v * bf + rows * r * bf + rows * v * bf, 2 * rows * r * v)
+    H, r, n, v, rope = geom.H, geom.r, geom.n, geom.v, geom.rope
+    d = n + v
+    B = len(lens)
+    rows = B * L * H
+    sT = sum(lens)
+    vis = sum(visible(L, T) for T in lens)
+    cache = sT * (r + rope) * bf
+    fold = (H * n * r * bf + rows * (n + r) * bf, 2 * rows * n * r)
+    attend = (cache + rows * (r + rope) * bf + rows * r * bf, 2 * H * vis * (2 * r + rope))
+    unembed = (H * r * v * bf + rows * (r + v) * bf, 2 * rows * r * v)
+    expand = (sT * r * bf + H * r * d * bf + sT * H * d * bf, 2 * sT * r * H * d)
+    mat_attn = (sT * H * d * bf + sT * rope * bf + rows * (n + rope + v) * bf,
+                2 * H * (n + rope + v) * vis)
     table = {
-        "unembed_merge_sm103": unembed,
-        "generic_fold": fold,
-        "generic_absorbed_attention": attend,
+        "fold_sm103": fold, "generic_fold": fold,
+        "absorbed_attn_sm103": attend, "generic_absorbed_attention": attend,
+        "unembed_merge_sm103": unembed, "unembed_sm103": unembed,
         "generic_combine_unembed": unembed,
-        "fold_sm103": fold,
-        "absorbed_attn_sm103": attend,
-        "unembed_sm103": unembed,
+        "expand_sm103": expand, "generic_expand": expand,
+        "mat_attn_sm103": mat_attn, "generic_materialised_attention": mat_attn,
     }
     return table.get(kernel)
 
 
+def _work(kernel: str, L: int, T: int):
+    """kernel_work for the headline workload (DSV3-like, one sequence)."""
+    from mla_attention_speculative_gb300.inputs import DSV3
+    return kernel_work(kernel, DSV3, L, [T])
+
+
 def call_work(branch: str, geom, L: int, lens):
     """Algorithmic (bytes, flops, cache_bytes) of one verify call, as the
-    method must do it (causal triangle and softmax ignored):
-      absorbed:     flops = sum_b 2 H L (n r + T_b (r + rope) + T_b r + r v)
+    method must do it (masked positions and the softmax not counted;
+    vis_b = visible(L, T_b)):
+      absorbed:     flops = sum_b 2 H (L n r + vis_b (r + rope) + vis_b r + L r v)
                     bytes = sum_b T_b (r + rope) 2 + H (n r + r v) 2 + B L H (n + rope + v) 2
-      materialised: flops = sum_b 2 H (T_b r d + L T_b (n + rope) + L T_b v)
+      materialised: flops = sum_b 2 H (T_b r d + vis_b (n + rope) + vis_b v)
                     bytes = the absorbed bytes + 2 sum_b T_b H d 2 (the expanded
                     keys and values written once and read once)."""
     H, r, n, v, rope = geom.H, geom.r, geom.n, geom.v, geom.rope
@@ -119,9 +140,10 @@ def call_work(branch: str, geom, L: int, lens):
     cache = sum(T * (r + rope) * 2 for T in lens)
     byts = cache + H * (n * r + r * v) * 2 + B * L * H * (n + rope + v) * 2
     if branch == "absorbed":
-        flops = sum(2 * H * L * (n * r + T * (r + rope) + T * r + r * v) for T in lens)
+        flops = sum(2 * H * (L * n * r + visible(L, T) * (2 * r + rope) + L * r * v)
+                    for T in lens)
     else:
-        flops = sum(2 * H * (T * r * d + L * T * (n + rope) + L * T * v) for T in lens)
+        flops = sum(2 * H * (T * r * d + visible(L, T) * (n + rope + v)) for T in lens)
         byts += 2 * sum(T * H * d * 2 for T in lens)
     return byts, flops, cache
 
@@ -136,63 +158,85 @@ def call_roofline(branch: str, geom, L: int, lens, us: float, peaks) -> dict:
             "frac": max(t_b, t_f) / us, "cache_only_frac": max(t_c, t_f) / us}
 
 
-def _mat_work(kernel: str, geom, L: int, lens):
-    """(bytes, flops) of one materialised-branch launch: the expansion GEMM
-    (sum(T) x H*(n+v) x r) and causal attention over the expanded cache (row l
-    of a sequence sees T - L + l + 1 positions; masked work is not counted)."""
-    bf = 2
-    H, r, n, v, rope = geom.H, geom.r, geom.n, geom.v, geom.rope
-    d = n + v
-    sT = sum(lens)
-    if kernel in ("expand_sm103", "generic_expand"):
-        return (sT * r * bf + H * r * d * bf + sT * H * d * bf, 2 * sT * r * H * d)
-    if kernel in ("mat_attn_sm103", "generic_materialised_attention"):
-        vis = sum(L * (T - L) + L * (L + 1) // 2 for T in lens)
-        byts = sT * H * d * bf + sT * rope * bf + len(lens) * L * H * (n + rope + v) * bf
-        return (byts, 2 * H * (n + rope + v) * vis)
-    return None
+def kernel_rates(kernel: str, geom, L: int, lens, us: float, peaks) -> dict:
+    """A launch's achieved HBM and tensor rates and the fraction of the bound
+    that its algorithmic work puts it under."""
+    w = kernel_work(kernel, geom, L, lens)
+    ent = {"us": us}
+    if w is None:
+        return ent
+    gbs = w[0] / (us * 1e-6) / 1e9
+    tfs = w[1] / (us * 1e-6) / 1e12
+    t_b, t_f = w[0] / (peaks["hbm_gbs"] * 1e9), w[1] / (peaks["bf16_tflops"] * 1e12)
+    ent.update(gbs=gbs, hbm_frac=gbs / peaks["hbm_gbs"], tflops=tfs,
+               tensor_frac=tfs / peaks["bf16_tflops"], bound="hbm" if t_b >= t_f else "tensor")
+    ent["frac"] = ent["hbm_frac"] if t_b >= t_f else ent["tensor_frac"]
+    return ent
 
 
-# The materialised branch's measurement shapes: the GLM-4.7-Flash-like
-# crossover sweep past its threshold, the long-context cold prefill (T = L),
-# and the DeepSeek-V3-like width-16 call forced onto this branch.
-MAT_SHAPES = (
-    ("glm47-like T=8192 L=512", "GLM47", 512, [8192], "auto"),
-    ("glm47-like T=8192 L=2048", "GLM47", 2048, [8192], "auto"),
-    ("512/256/256 H=64 B=4 T=L=2048 cold prefill", "GLM53", 2048, [2048] * 4, "auto"),
-    ("dsv3-like T=8192 L=16 forced", "DSV3", 16, [8192], "materialised"),
-)
+# Secondary measurements beside the headline (each its own workload, its own
+# line in the "shapes" object):
+# - the GLM-4.7-Flash-like crossover sweep at cache 8192 with each branch
+#   forced (the pages time both branches across L to validate the formula);
+# - the batched paged serving verify (32 sequences, T ~ U{1024..32768}, L = 8,
+#   page 64, shuffled page table, absorbed);
+# - long-context verify (512/256/256, H = 64, B = 4, T = 131072, L = 1, 5, 8,
+#   16, auto) and its cold prefill (T = L = 2048, auto -> materialised);
+# - the DeepSeek-V3-like width-16 call forced onto the materialised branch.
+CROSSOVER_L = (1, 16, 64, 128, 256, 379, 398, 512, 1024, 2048)
+L2_ROTATE_BYTES = 256 << 20   # rotate input copies until a graph touches this much
 
 
-def _bench_materialised(B, dev, peaks, reps):
-    """Per shape: us per call (graph replay, CUDA events) and each kernel's
-    achieved rate against its roofline (events around each launch)."""
+def _shape_list():
+    from mla_attention_speculative_gb300 import inputs as I
+    out = []
+    for L in CROSSOVER_L:
+        for mode in ("absorbed", "materialised"):
+            out.append(dict(group="crossover_glm47_T8192", geom=I.GLM47, L=L, lens=[8192],
+                            mode=mode, page=0))
+    out.append(dict(group="batched_paged", geom=I.DSV3, L=8,
+                    lens=I.workload_shapes("batched_paged")[0][1], mode="absorbed", page=64))
+    for L, lens in I.workload_shapes("long_context"):
+        out.append(dict(group="long_context", geom=I.GLM53, L=L, lens=lens, mode="auto", page=0))
+    out.append(dict(group="dsv3_forced_materialised", geom=I.DSV3, L=16, lens=[8192],
+                    mode="materialised", page=0))
+    return out
+
+
+def _bench_shapes(B, dev, peaks, reps):
+    """Per shape: us per call (CUDA graph of calls over rotating input copies so
+    the working set exceeds L2, CUDA events), the call roofline, and each
+    kernel's achieved rates (events around each launch, eager calls)."""
     import torch
     from mla_attention_speculative_gb300 import inputs as I
-    res = []
-    for name, gname, L, lens, mode in MAT_SHAPES:
-        geom = getattr(I, gname)
-        c = I.make_case(geom, L, lens, dtype=torch.bfloat16, seed=2000 + L)
-        d = {k: getattr(c, k).to(dev) for k in
-             ("q_nope", "q_rope", "c_kv", "k_rope", "W_UK", "W_UV")}
-        del c
+    groups = {}
+    for k, sh in enumerate(_shape_list()):
+        geom, L, lens, mode, page = sh["geom"], sh["L"], sh["lens"], sh["mode"], sh["page"]
+        layer_bytes = (sum(lens) * (geom.r + geom.rope)
+                       + geom.H * geom.r * (geom.n + geom.v)) * 2
+        copies = max(1, min(8, -(-L2_ROTATE_BYTES // layer_bytes)))
+        cases = [I.make_case(geom, L, lens, seed=3000 + 17 * k + i, page_size=page, device=dev)
+                 for i in range(copies)]
         lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
         g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope, torch.bfloat16)
         ws = B.new_workspace(B.mla_workspace_bytes(g, L, lens, mode), dev)
         out = torch.empty((len(lens), L, geom.H, geom.v), dtype=torch.bfloat16, device=dev)
         br = {}
 
-        def call():
-            _, br["b"] = B.mla_verify_attention(d["q_nope"], d["q_rope"], d["c_kv"], d["k_rope"],
-                                                d["W_UK"], d["W_UV"], lens, mode=mode, out=out,
-                                                workspace=ws, cache_lens_dev=lens_dev)
-        for _ in range(3):
-            call()
+        def call(c):
+            _, br["b"] = B.mla_verify_attention(
+                c.q_nope, c.q_rope, c.c_kv, c.k_rope, c.W_UK, c.W_UV, lens, mode=mode,
+                out=out, workspace=ws, cache_lens_dev=lens_dev,
+                page_table=c.page_table if page else None)
+
+        for c in cases:
+            call(c)
         torch.cuda.synchronize()
         st = torch.cuda.Stream(dev)
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=st):
-            call()
+            for c in cases:
+                call(c)
         gr.replay()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -201,39 +245,49 @@ def _bench_materialised(B, dev, peaks, reps):
             gr.replay()
         b.record()
         torch.cuda.synchronize()
-        us_call = a.elapsed_time(b) * 1e3 / reps
+        us_call = a.elapsed_time(b) * 1e3 / (reps * copies)
         B.mla_kernel_timing_read(reset=True)
         B.mla_kernel_timing_enable(True)
-        for _ in range(reps):
-            call()
+        for _ in range(max(1, reps // 2)):
+            for c in cases:
+                call(c)
         torch.cuda.synchronize()
         B.mla_kernel_timing_enable(False)
         kt = B.mla_kernel_timing_read(reset=True)
-        kern = {}
-        for k, (nl, ms) in kt.items():
-            w = _mat_work(k, geom, L, lens)
-            us = ms * 1e3 / max(nl, 1)
-            ent = {"us": us}
-            if w is not None:
-                tb, tf = w[0] / (peaks["hbm_gbs"] * 1e9), w[1] / (peaks["bf16_tflops"] * 1e12)
-                if tf >= tb:
-                    ach = w[1] / (us * 1e-6) / 1e12
-                    ent.update(bound="tensor", achieved=ach, unit="TFLOP/s",
-                               frac=ach / peaks["bf16_tflops"])
-                else:
-                    ach = w[0] / (us * 1e-6) / 1e9
-                    ent.update(bound="hbm", achieved=ach, unit="GB/s", frac=ach / peaks["hbm_gbs"])
-            kern[k] = ent
-        res.append({"workload": name, "branch": B.BRANCH_NAMES[br["b"]],
-                    "us_per_call": us_call,
-                    "call_roofline": call_roofline(B.BRANCH_NAMES[br["b"]], geom, L, lens,
-                                                   us_call, peaks),
-                    "kernels": kern})
-        del d, ws, out, gr
+        branch = B.BRANCH_NAMES[br["b"]]
+        ent = {"L": L, "mode": mode, "branch": branch, "us_per_call": us_call,
+               "call_roofline": call_roofline(branch, geom, L, lens, us_call, peaks),
+               "kernels": {kn: kernel_rates(kn, geom, L, lens, ms * 1e3 / max(nl, 1), peaks)
+                           for kn, (nl, ms) in kt.items()}}
+        if len(lens) > 1:
+            ent["B"] = len(lens)
+            ent["sum_T"] = sum(lens)
+        else:
+            ent["T"] = lens[0]
+        if page:
+            ent["page_size"] = page
+        gd = groups.setdefault(sh["group"], {
+            "geometry": f"H={geom.H} r={geom.r} n={geom.n} v={geom.v} rope={geom.rope}",
+            "calls": []})
+        gd["calls"].append(ent)
+        del cases, ws, out, gr
         torch.cuda.empty_cache()
-    return {"shapes": res, "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
+    cx = groups.get("crossover_glm47_T8192")
+    if cx:
+        from mla_attention_speculative_gb300.inputs import GLM47
+        t = {}
+        for e in cx["calls"]:
+            t.setdefault(e["L"], {})[e["mode"]] = e["us_per_call"]
+        first = next((L for L in sorted(t) if t[L]["materialised"] < t[L]["absorbed"]), None)
+        cx["formula_threshold"] = B.mla_max_absorbed_queries(GLM47.r, GLM47.n, GLM47.v, 8192)
+        cx["measured_crossover"] = {
+            "first_L_materialised_faster": first,
+            "us": {str(L): {"absorbed": v["absorbed"], "materialised": v["materialised"]}
+                   for L, v in sorted(t.items())}}
+    return {"groups": groups, "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
             "peak_source": f"of {peaks['source']}",
-            "note": "workspace (the expanded cache) is larger than L2 and is rewritten each call"}
+            "timing": "CUDA graph of one call per input copy, copies rotated until the "
+                      "working set exceeds 256 MB (> L2); work counts causal positions only"}
 
 
 def _source_sha(names):
@@ -645,9 +699,9 @@ def run_ours(args):
     # ---- end to end: host inputs -> device -> host result, per step ----------
     e2e = _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world)
 
-    mat = None
-    if not args.no_materialised:
-        mat = _bench_materialised(B, dev, peaks, reps=max(3, min(args.steps, 20)))
+    shapes = None
+    if not args.no_shapes:
+        shapes = _bench_shapes(B, dev, peaks, reps=max(3, min(args.steps, 10)))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -673,7 +727,7 @@ def run_ours(args):
                                  us, peaks) for L, us in per_L.items()},
             "roofline": roof,
             "kernel_ms_per_step": {k: v[1] / args.steps for k, v in ktimes.items()},
-            "materialised": mat,
+            "shapes": shapes,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": e2e,

@@ -169,24 +169,50 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   if (!*fail) {
-    const int m = mt * 128 + warp * 32 + lane;
-    for (int c0 = 0; c0 < NB; c0 += 16) {
-      uint32_t v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-      tmem_wait_ld();
+    // D[m][row] leaves through the drained weight buffer, 64 rows at a time:
+    // staged as bf16 [row][128 columns] (16-byte chunks XOR-swizzled by row),
+    // then written as 16-byte chunks of 8 consecutive output columns.
+    uint8_t* stg = sA;  // 64 rows x 256 B (the weight buffer holds at least 16 KB)
+    const int ml = warp * 32 + lane;  // this thread's TMEM lane = column of the tile
+    for (int g0 = 0; g0 < NB; g0 += 64) {
+      const int gn = min(64, NB - g0);
+      for (int c0 = 0; c0 < gn; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + g0 + c0, v);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int row = row0 + c0 + i;
+        for (int i = 0; i < 16; ++i) {
+          const int rl = c0 + i;
+          *(__nv_bfloat16*)(stg + rl * 256 + ((((ml >> 3) ^ (rl & 15))) << 4) + (ml & 7) * 2) =
+              __float2bfloat16_rn(__uint_as_float(v[i]));
+        }
+      }
+      __syncthreads();
+      for (int k = threadIdx.x; k < gn * 16; k += 128) {
+        // q_lat tiles: a column chunk's rows are contiguous, so consecutive
+        // threads take consecutive rows; row-major output: consecutive chunks
+        int rl, mc;
+        if (p.L > 0) {
+          mc = k / gn;
+          rl = k - mc * gn;
+        } else {
+          rl = k >> 4;
+          mc = k & 15;
+        }
+        const int row = row0 + g0 + rl;
         if (row >= p.rows) continue;
+        const uint4 val = *(const uint4*)(stg + rl * 256 + ((mc ^ (rl & 15)) << 4));
+        const int m = mt * 128 + mc * 8;
         size_t idx;
         if (p.L > 0) {
           const int b = row / p.L, r = (row - b * p.L) * p.H + h;
-          idx = ((((size_t)b * p.ntile + (r >> 7)) * 64 + (m >> 3)) * 128 + (r & 127)) * 8 + (m & 7);
+          idx = ((((size_t)b * p.ntile + (r >> 7)) * 64 + (m >> 3)) * 128 + (r & 127)) * 8;
         } else {
           idx = ((size_t)row * p.H + h) * p.M + m;
         }
-        p.out[idx] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        *(uint4*)(p.out + idx) = val;
       }
+      __syncthreads();
     }
   }
   tc_fence_before();
@@ -1000,7 +1026,7 @@ struct UnembedMergeParams {
   __nv_bfloat16* out;     // [B, L, H, v]
   int B, L, H, R, v, splits, chunk;
   int Lc;                 // verify rows per chunk (Lc * splits <= 64)
-  int seq_per_cta;
+  int chunks_per_cta;     // consecutive chunks of the (sequence, verify-row block) list
 };
 constexpr int UM_THREADS = 256;            // warp 0 issues, 1..3 weights, 4..7 epilogue
 constexpr int UM_W = 2 * kLat * 128;       // W_UV tile
@@ -1026,11 +1052,12 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nmt = p.v / 128;
   const int h = blockIdx.x / nmt, mt = blockIdx.x - h * nmt;
-  const int b0 = blockIdx.y * p.seq_per_cta;
-  const int nb = min(p.seq_per_cta, p.B - b0);
   const int S = p.splits, Lc = p.Lc;
   const int cps = (p.L + Lc - 1) / Lc;  // chunks per sequence
-  const int nch = nb * cps;
+  // this CTA's chunks: g0 .. g0 + nch - 1 of the B * cps chunks, sequence by
+  // sequence; chunk g is verify rows (g % cps) * Lc .. of sequence g / cps
+  const int g0 = blockIdx.y * p.chunks_per_cta;
+  const int nch = min(p.chunks_per_cta, p.B * cps - g0);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(UB_WFULL), 1);
@@ -1062,7 +1089,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
       const int N = (S * Lc + 15) & ~15;
       const uint32_t idesc = idesc_bf16(128, N, 1, 0);
       for (int c = 0; c < nch && ok; ++c) {
-        const int b = b0 + c / cps, l0 = (c % cps) * Lc;
+        const int b = (g0 + c) / cps, l0 = ((g0 + c) % cps) * Lc;
         mbar_arrive_expect_tx(bar(UB_OFULL), 8 * slab);
         for (int kc = 0; kc < kLat / 64; ++kc)
           tma_load_4d(sB + kc * 8192, &tm_pieces, bar(UB_OFULL), 64 * kc, h, b * S, l0);
@@ -1088,37 +1115,67 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
   } else if (warp < 4) {
     // ------------------------------------------------ combine weights (3 warps)
     pdl_wait();
-    for (int row = warp - 1; row < nch * Lc; row += 3) {  // (chunk, verify row in it)
-      const int c = row / Lc, li = row - c * Lc;
-      const int b = b0 + c / cps, l = (c % cps) * Lc + li;
-      float* wt = wts + c * 64 + li * S;
-      if (l >= p.L) {
-        for (int s = lane; s < S; s += 32) wt[s] = 0.f;
-        continue;
-      }
-      const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
-      const size_t base = (size_t)b * S * p.R + (size_t)l * p.H + h;
-      float2 ml[2];
-      float M = -FLT_MAX;
+    if (S <= 8) {
+      // few pieces per row (wide verify widths): one thread per row, its
+      // pieces' (m, l) loads all in flight at once
+      for (int row = threadIdx.x - 32; row < nch * Lc; row += 96) {
+        const int c = row / Lc, li = row - c * Lc;
+        const int b = (g0 + c) / cps, l = ((g0 + c) % cps) * Lc + li;
+        float* wt = wts + c * 64 + li * S;
+        const int nsplit = l < p.L ? (p.lens[b] + p.chunk - 1) / p.chunk : 0;
+        const size_t base = (size_t)b * S * p.R + (size_t)min(l, p.L - 1) * p.H + h;
+        float2 ml[8];
+        float M = -FLT_MAX;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int sj = lane + 32 * j;
-        ml[j] = sj < nsplit ? *(const float2*)(p.ml + (base + (size_t)sj * p.R) * 2)
-                            : make_float2(-FLT_MAX, 0.f);
-        if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
-      }
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, o));
-      float w[2], sum = 0.f;
+        for (int j = 0; j < 8; ++j) {
+          ml[j] = j < nsplit && j < S ? *(const float2*)(p.ml + (base + (size_t)j * p.R) * 2)
+                                      : make_float2(-FLT_MAX, 0.f);
+          if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
+        }
+        float w[8], sum = 0.f;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        w[j] = ml[j].y > 0.f ? ex2(ml[j].x - M) * ml[j].y : 0.f;
-        sum += w[j];
-      }
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
-      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+        for (int j = 0; j < 8; ++j) {
+          w[j] = ml[j].y > 0.f ? ex2(ml[j].x - M) * ml[j].y : 0.f;
+          sum += w[j];
+        }
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-        if (lane + 32 * j < S) wt[lane + 32 * j] = w[j] * inv;
+        for (int j = 0; j < 8; ++j)
+          if (j < S) wt[j] = w[j] * inv;
+      }
+    } else {
+      for (int row = warp - 1; row < nch * Lc; row += 3) {  // (chunk, verify row in it)
+        const int c = row / Lc, li = row - c * Lc;
+        const int b = (g0 + c) / cps, l = ((g0 + c) % cps) * Lc + li;
+        float* wt = wts + c * 64 + li * S;
+        if (l >= p.L) {
+          for (int s = lane; s < S; s += 32) wt[s] = 0.f;
+          continue;
+        }
+        const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
+        const size_t base = (size_t)b * S * p.R + (size_t)l * p.H + h;
+        float2 ml[2];
+        float M = -FLT_MAX;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int sj = lane + 32 * j;
+          ml[j] = sj < nsplit ? *(const float2*)(p.ml + (base + (size_t)sj * p.R) * 2)
+                              : make_float2(-FLT_MAX, 0.f);
+          if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
+        }
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, o));
+        float w[2], sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          w[j] = ml[j].y > 0.f ? ex2(ml[j].x - M) * ml[j].y : 0.f;
+          sum += w[j];
+        }
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(~0u, sum, o);
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          if (lane + 32 * j < S) wt[lane + 32 * j] = w[j] * inv;
+      }
     }
     named_bar_sync(1, 224);  // weights -> epilogue
   } else {
@@ -1132,7 +1189,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
-      const int b = b0 + c / cps, l0 = (c % cps) * Lc;
+      const int b = (g0 + c) / cps, l0 = ((g0 + c) % cps) * Lc;
       const int rows = min(Lc, p.L - l0) * S;
       wait_or_fail(ok, bar(UB_DONE + (c & 1)), (c >> 1) & 1, 54);
       tc_fence_after();
@@ -1355,15 +1412,17 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     up.splits = p.splits;
     up.chunk = p.chunk;
     up.Lc = 64 / p.splits < p.L ? 64 / p.splits : p.L;
-    // sequences per CTA: about two CTAs per SM at most, and at most
-    // UM_MAX_CHUNKS chunks per CTA
+    // chunks per CTA: one wave of CTAs (each loads its 128 KB W_UV tile
+    // once for all of its chunks), at most UM_MAX_CHUNKS
     const int units = p.H * (p.v / 128);
     const int cps = (p.L + up.Lc - 1) / up.Lc;
-    int spc = (p.B * units + 2 * device_sm_count() - 1) / (2 * device_sm_count());
-    if (spc < 1) spc = 1;
-    if (spc * cps > UM_MAX_CHUNKS) spc = UM_MAX_CHUNKS / cps > 0 ? UM_MAX_CHUNKS / cps : 1;
-    up.seq_per_cta = spc;
-    if (cps <= UM_MAX_CHUNKS) {
+    const long long total = (long long)p.B * cps;
+    const long long want_ctas = device_sm_count();  // one CTA fits an SM
+    long long cpc = (total * units + want_ctas - 1) / want_ctas;
+    if (cpc < 1) cpc = 1;
+    if (cpc > UM_MAX_CHUNKS) cpc = UM_MAX_CHUNKS;
+    up.chunks_per_cta = (int)cpc;
+    {
       // the pieces of one head as [l][piece][h][col]: row (b, s, l, h) of
       // o_part sits at ((b * splits + s) * R + l * H + h) * 512 elements
       CUtensorMap tm_pieces;
@@ -1374,7 +1433,8 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
       const uint32_t box[4] = {64, 1, (uint32_t)p.splits, (uint32_t)up.Lc};
       if (!make_tmap_bf16_4d(&tm_pieces, o_part, dims, strides, box)) return cudaErrorInvalidValue;
       KernelTimer kt("unembed_merge_sm103", a.stream);
-      e = launch_pdl(unembed_merge_sm103, dim3(units, (p.B + spc - 1) / spc), dim3(UM_THREADS),
+      e = launch_pdl(unembed_merge_sm103, dim3(units, (unsigned)((total + cpc - 1) / cpc)),
+                     dim3(UM_THREADS),
                      UM_SMEM, a.stream, tm_wuv, tm_pieces, up);
       if (e != cudaSuccess) return e;
       return cudaGetLastError();

@@ -8,8 +8,9 @@ for them with the same geometry:
 
 * activations q_nope, q_rope, c_kv, k_rope ~ N(0, 1);
 * weights W_UK, W_UV ~ N(0, 1/512) (standard deviation 1/sqrt(512));
-* all draws are float32 from a CPU ``torch.Generator`` seeded per case, then
-  rounded to the case's dtype (bf16 rounds to nearest even).
+* all draws are float32 from a ``torch.Generator`` seeded per case (on the
+  CPU, or on the GPU for the benchmark's large shapes), then rounded to the
+  case's dtype (bf16 rounds to nearest even).
 
 Layouts (row-major): q_nope [B,L,H,n], q_rope [B,L,H,rope],
 c_kv [B,Tmax,r], k_rope [B,Tmax,rope], W_UK [H,n,r], W_UV [H,r,v].
@@ -70,7 +71,7 @@ class Case:
 
 
 def _normal(gen, shape, std, dtype):
-    x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32, device=gen.device)
     if std != 1.0:
         x = x * std
     return x.to(dtype)
@@ -84,7 +85,7 @@ def dominant_position(T: int, L: int) -> int:
 
 def make_case(geom: Geometry, L: int, cache_lens, dtype=torch.bfloat16, seed: int = 0,
               page_size: int = 0, tmax: Optional[int] = None, q_std: float = 1.0,
-              dominant: float = 0.0) -> Case:
+              dominant: float = 0.0, device="cpu") -> Case:
     """Draw one case.  ``page_size`` > 0 gives a paged cache with a random page table.
 
     Draw order is fixed (q_nope, q_rope, cache, k_rope, W_UK, W_UV, page
@@ -100,10 +101,14 @@ def make_case(geom: Geometry, L: int, cache_lens, dtype=torch.bfloat16, seed: in
     sets the first RoPE component of every query to D and that of the key at
     ``dominant_position(T_b, L)`` to D, so that key wins by about D^2/sqrt(n+rope)
     nats (contiguous caches only).
+
+    ``device`` draws on that device with its own seeded generator (a CUDA
+    generator gives other values than the CPU one for the same seed; the
+    benchmark draws its large inputs this way, the tests on the CPU).
     """
     cache_lens = [int(t) for t in cache_lens]
     B = len(cache_lens)
-    g = torch.Generator().manual_seed(int(seed))
+    g = torch.Generator(device=device).manual_seed(int(seed))
     wstd = 1.0 / (512 ** 0.5)
     q_nope = _normal(g, (B, L, geom.H, geom.n), q_std, dtype)
     q_rope = _normal(g, (B, L, geom.H, geom.rope), q_std, dtype)
@@ -120,9 +125,9 @@ def make_case(geom: Geometry, L: int, cache_lens, dtype=torch.bfloat16, seed: in
     W_UK = _normal(g, (geom.H, geom.n, geom.r), wstd, dtype)
     W_UV = _normal(g, (geom.H, geom.r, geom.v), wstd, dtype)
     if page_size > 0:
-        perm = torch.randperm(total, generator=g).to(torch.int32)
+        perm = torch.randperm(total, generator=g, device=g.device).to(torch.int32)
         maxp = max(npages)
-        page_table = torch.zeros((B, maxp), dtype=torch.int32)
+        page_table = torch.zeros((B, maxp), dtype=torch.int32, device=g.device)
         k = 0
         for b in range(B):
             page_table[b, :npages[b]] = perm[k:k + npages[b]]
