@@ -158,6 +158,47 @@ mla_status_t mla_verify_attention(
     int32_t mode, void* out, void* workspace, size_t workspace_bytes,
     void* stream, int32_t* branch_taken);
 
+/* Bytes of device workspace mla_verify_attention_sparse needs for `batch`
+ * sequences of L verify rows with index lists of topk_len entries (the
+ * pieces of the split follow the lists, not the cache lengths).  Host only. */
+mla_status_t mla_sparse_workspace_bytes(const mla_geometry_t* geom, int32_t batch, int32_t L,
+                                        const int32_t* cache_lens_host, int32_t topk_len,
+                                        size_t* bytes);
+
+/* Verify attention over selected cached positions: the sparse model's top-k
+ * attention ("One guard, 110x off the verify step", section "The sparse
+ * model is different": an indexer picks the top 2048 cached positions and
+ * attention runs over those only; mlx-lm pull request 1817, opening section,
+ * on deepseek_v32's top-k gather).  Always the absorbed branch.
+ *
+ *  topk      device [batch, L, topk_len] int32: verify row l of sequence b
+ *            attends to the positions topk[b, l, j] with
+ *            0 <= topk[b, l, j] <= T_b - L + l; other entries (-1 padding,
+ *            positions past the row's causal limit) are skipped.  A row whose
+ *            list holds no usable position gets zeros.  The list is read as
+ *            given: a position listed twice counts twice.
+ *  topk_len  entries per list, >= 1
+ *
+ * Every other argument is that of mla_verify_attention (no mode: the
+ * absorbed branch runs; no branch output).  The workspace must hold
+ * mla_sparse_workspace_bytes() bytes.  bf16 calls with r = 512, rope = 64
+ * and H a multiple of 128 (every 128-row tile is one verify row) run the
+ * tensor-core kernels, which gather the listed cache rows tile by tile; other
+ * calls run the CUDA-core kernels.  The index lists may be written by the
+ * kernel right before the call: they are read only after it has finished. */
+mla_status_t mla_verify_attention_sparse(
+    const mla_geometry_t* geom,
+    const void* q_nope, const void* q_rope,
+    const void* c_kv, const void* k_rope,
+    int64_t c_kv_row_stride, int64_t k_rope_row_stride, int64_t seq_stride_rows,
+    const void* W_UK, const void* W_UV,
+    const int32_t* cache_lens_dev, const int32_t* cache_lens_host,
+    int32_t batch, int32_t L,
+    const int32_t* topk, int32_t topk_len,
+    const int32_t* page_table, int32_t page_size, int32_t max_pages_per_seq,
+    int32_t num_pages,
+    void* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* The absorbed-branch verify call without a workspace, for callers that cannot
  * allocate device memory (a plugin host or serving engine that owns every
  * device allocation and gives its attention back-end no allocator, or a

@@ -62,6 +62,10 @@ _SIGS = {
                                             _P, _P, _I32, _I32, _P, _I32, _I32, _I32, _P,
                                             _P, _P]),
     "mla_check_page_table": (_I32, [_P, _I32, _I32, _P, _I32, _I32]),
+    "mla_sparse_workspace_bytes": (_I32, [_P, _I32, _I32, _P, _I32, _P]),
+    "mla_verify_attention_sparse": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P,
+                                           _I32, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _P,
+                                           ctypes.c_size_t, _P]),
     "mla_select_draft_cap": (_I32, [ctypes.c_double, _P, _I32, _P, _I32, _I32, _P]),
     "mla_concat_snapshots": (_I32, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64, _P,
                                     _I32, _P, _P]),
@@ -164,6 +168,16 @@ def mla_workspace_bytes(geom: Geometry, L: int, cache_lens: Sequence[int], mode=
     _check(lib().mla_workspace_bytes(ctypes.byref(geom), len(cache_lens), L, arr,
                                      MODES.get(mode, mode), ctypes.byref(out)),
            "mla_workspace_bytes")
+    return out.value
+
+
+def mla_sparse_workspace_bytes(geom: Geometry, L: int, cache_lens: Sequence[int],
+                               topk_len: int) -> int:
+    arr = _lens_array(cache_lens)
+    out = ctypes.c_size_t(0)
+    _check(lib().mla_sparse_workspace_bytes(ctypes.byref(geom), len(cache_lens), L, arr,
+                                            int(topk_len), ctypes.byref(out)),
+           "mla_sparse_workspace_bytes")
     return out.value
 
 
@@ -430,3 +444,39 @@ def mla_verify_attention_noalloc(q_nope: torch.Tensor, q_rope: torch.Tensor,
     st = lib().mla_verify_attention_noalloc(*args, stream, ctypes.byref(branch))
     _check(st, "mla_verify_attention_noalloc")
     return out, branch.value
+
+
+def mla_verify_attention_sparse(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv: torch.Tensor,
+                                k_rope: torch.Tensor, W_UK: torch.Tensor, W_UV: torch.Tensor,
+                                cache_lens: Sequence[int], topk: torch.Tensor,
+                                out: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None,
+                                page_table: Optional[torch.Tensor] = None,
+                                cache_lens_dev: Optional[torch.Tensor] = None,
+                                scale: Optional[float] = None, stream=None) -> torch.Tensor:
+    """Absorbed verify call over selected cached positions (the sparse model's
+    top-k attention).  ``topk`` is an int32 device tensor [B, L, k]: verify row
+    l of sequence b attends to the positions topk[b, l, :] that lie in
+    [0, T_b - L + l] (others, e.g. -1 padding, are skipped).  The other
+    tensors are those of :func:`mla_verify_attention`.  Returns out."""
+    _dense(topk=topk)
+    if topk.dtype != torch.int32 or topk.dim() != 3 or tuple(topk.shape[:2]) != \
+            tuple(q_nope.shape[:2]):
+        raise ValueError("topk must be int32 [B, L, k] matching q_nope's B and L")
+    k = topk.shape[2]
+    args, out, dev, _ = _verify_args(q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, cache_lens, None,
+                                     out, None, page_table, cache_lens_dev, scale, noalloc=True)
+    geom_ref, L, arr = args[0], args[13], args[11]
+    if workspace is None:
+        nbytes = ctypes.c_size_t(0)
+        _check(lib().mla_sparse_workspace_bytes(geom_ref, len(cache_lens), L, arr, int(k),
+                                                ctypes.byref(nbytes)),
+               "mla_sparse_workspace_bytes")
+        workspace = new_workspace(nbytes.value, dev)
+    if stream is None:
+        stream = _current_stream(dev)
+    # (geometry .. B, L) + (topk, k) + (page table .. num_pages) + (out, workspace, bytes)
+    cargs = args[:14] + [_ptr(topk), int(k)] + args[14:18] + \
+        [_ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), stream]
+    _check(lib().mla_verify_attention_sparse(*cargs), "mla_verify_attention_sparse")
+    return out

@@ -132,9 +132,6 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
-  // The next kernel may launch now and start its own independent loads; it
-  // waits for this grid before reading what it writes.
-  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     bool ok = true;
@@ -147,6 +144,12 @@ __global__ void __launch_bounds__(128) swapab_gemm_sm103(const __grid_constant__
                     h * K + 64 * kc);
     }
     pdl_wait();  // the activations may come from the preceding kernel
+    // The next kernel may launch now and start its own independent loads (it
+    // waits for this grid before reading what this one writes).  Triggering
+    // only after this grid's own wait means a kernel that follows starts
+    // after the kernel before this one has finished, so what that kernel
+    // wrote (lengths, page table, index lists) is complete for it.
+    pdl_launch_dependents();
     for (int kc = 0; kc < nk; ++kc)
       tma_load_2d(smem_u32(sB + kc * NB * 128), &tm_act, smem_u32(&bars[kc]), h * K + 64 * kc,
                   row0);
@@ -273,6 +276,13 @@ struct AttnParams {
   float* ml;              // [B, splits, R, 2]: (m, l) of each piece
   const char* pf;     // W_UV, pulled into L2 while the attention runs
   size_t pf_bytes;
+  // index-list (top-k) mode: [B, L, topk_k] positions per verify row, and the
+  // cache as plain pointers (rows are gathered one by one)
+  const int32_t* topk;
+  int topk_k;
+  const char* ckv;
+  const char* kr;
+  long long ckv_stride, kr_stride;  // elements between rows
 };
 
 // Barrier slots.  Every barrier that is waited on by parity alone has enough
@@ -327,6 +337,15 @@ __device__ __forceinline__ uint32_t xchg_offset(int wg, int q, int c) {
   return (uint32_t)((q >> 5) * XQUARTER + wg * (32 * XROW) + (q & 31) * XROW + ((c ^ sw) << 4));
 }
 
+// SPARSE: the index-list mode ("One guard, 110x off the verify step", section
+// "The sparse model is different": attention runs over the cached positions
+// an indexer selected).  A tile's 64 columns are list entries j of its verify
+// row (all rows of a 128-row tile belong to one verify row: H is a multiple
+// of 128); the producer warp gathers their cache rows with 16-byte cp.async
+// copies into the layout the TMA boxes would give, zero-filling entries that
+// are padding (< 0), past the row's causal limit or on a bad page, and the
+// softmax masks those columns.  Pieces split the list instead of [0, T).
+template <bool SPARSE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     absorbed_attn_sm103(const __grid_constant__ CUtensorMap tm_qr,
                         const __grid_constant__ CUtensorMap tm_ckv,
@@ -355,7 +374,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QTMEM), SOFTMAX_THREADS);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(B_KVFULL + s), 1);
+      // index-list mode: each producer lane's copies arrive on their own
+      mbar_init(bar(B_KVFULL + s), SPARSE ? 32 : 1);
       mbar_init(bar(B_KVEMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -377,7 +397,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
-  const int nsplit = (T + p.chunk - 1) / p.chunk;
+  const int klen = SPARSE ? p.topk_k : T;  // list entries, or positions
+  const int nsplit = (klen + p.chunk - 1) / p.chunk;
   if (split >= nsplit) {  // both CTAs of the cluster leave together, the peer untouched
     if (warp == 1) tmem_dealloc(tmem, 512);
     return;
@@ -386,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   const int l_last = min(p.R - 1, row0 + BM - 1) / p.H;
   const int vis_end = T - p.L + l_last + 1;
   const int kv0 = split * p.chunk;
-  const int kv1 = min(min(kv0 + p.chunk, T), vis_end);
+  const int kv1 = SPARSE ? min(kv0 + p.chunk, klen) : min(min(kv0 + p.chunk, T), vis_end);
   const int ntiles = kv1 > kv0 ? (kv1 - kv0 + BN - 1) / BN : 0;
   // arm the exchange barriers for tiles 0 and 1 (the peer's bulk copies count
   // them down), then publish the setup to the peer: each role waits for the
@@ -399,7 +420,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   cluster_arrive();
   pdl_launch_dependents();  // the merge may launch; it waits for this grid
 
-  if (warp == 0) {
+  if (warp == 0 && SPARSE) {
+    // ------------------------------------------- gathering producer (32 lanes)
+    if (ntiles > 0) {
+      bool ok = true;
+      pdl_wait();  // the index list may come from the preceding kernel
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(B_QFULL), Q_ROPE);
+        tma_load_2d(sQR, &tm_qr, bar(B_QFULL), (int)rank * 32, b * p.R + row0);
+      }
+      const int l = row0 / p.H;
+      const int last_t = T - p.L + l;
+      const int32_t* list = p.topk + ((size_t)b * p.L + l) * p.topk_k;
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES) {
+          if (lane == 0) wait_or_fail(ok, bar(B_KVEMPTY + s), ((i / STAGES) - 1) & 1, 10);
+          ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+          if (!ok) break;
+        }
+        // this lane resolves tile rows lane and lane + 32: the cache row of
+        // the listed position, or -1 (zero-filled, masked)
+        long long crow[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = kv0 + i * BN + lane + 32 * u;
+          const int t = j < kv1 ? list[j] : -1;
+          crow[u] = -1;
+          if (t >= 0 && t <= last_t) {
+            if (p.page_table) {
+              const int page = p.page_table[(long long)b * p.max_pages + t / p.page_size];
+              if (page < 0 || page >= p.num_pages) report_timeout(kBadPageSite);
+              else crow[u] = (long long)page * p.page_size + (t % p.page_size);
+            } else {
+              crow[u] = (long long)b * p.seq_stride + t;
+            }
+          }
+        }
+        const uint32_t st = sKV + s * KV_STAGE;
+        // latent: this CTA's 256 columns of a row are 512 bytes, one 16-byte
+        // chunk per lane; chunk c of row jr lands where the 128-byte-swizzled
+        // box of its 64 columns puts it
+        for (int jr = 0; jr < BN; ++jr) {
+          const long long cr = __shfl_sync(0xffffffffu, crow[jr >> 5], jr & 31);
+          const uint32_t dst =
+              st + (lane >> 3) * KV_CHUNK + jr * 128 + ((((lane & 7) ^ (jr & 7))) << 4);
+          const char* src = cr >= 0 ? p.ckv + (cr * p.ckv_stride + 256 * rank) * 2 + lane * 16
+                                    : p.ckv;
+          cp_async16(dst, src, cr >= 0 ? 16u : 0u);
+        }
+        // RoPE: 32 columns (64 bytes, 64-byte swizzle) per row, 8 rows per round
+        for (int jr0 = 0; jr0 < BN; jr0 += 8) {
+          const int jr = jr0 + (lane >> 2), c = lane & 3;
+          const long long cr = __shfl_sync(0xffffffffu, crow[jr0 >> 5], jr & 31);
+          const uint32_t dst = st + 4 * KV_CHUNK + jr * 64 + ((c ^ ((jr >> 1) & 3)) << 4);
+          const char* src =
+              cr >= 0 ? p.kr + (cr * p.kr_stride + 32 * rank) * 2 + c * 16 : p.kr;
+          cp_async16(dst, src, cr >= 0 ? 16u : 0u);
+        }
+        cp_async_mbar_arrive(bar(B_KVFULL + s));
+      }
+      // nothing this warp started may still be landing when the CTA exits
+      cp_async_wait_all();
+      if (lane == 0) mbar_wait(bar(B_QFULL), 0);
+    }
+    cluster_wait();  // (this role never touches the peer)
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
@@ -481,6 +567,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         wait_or_fail(ok, bar(B_KVFULL + s), (i / STAGES) & 1, 12);
         if (i >= SBUF) wait_or_fail(ok, bar(B_SFREE + sb), ((i - SBUF) / SBUF) & 1, 13);
         if (!ok) break;
+        // gathered tiles were written by cp.async (generic proxy): order them
+        // before the tensor core's reads
+        if (SPARSE) fence_async_shared();
         tc_fence_after();
         const uint64_t soff = (uint64_t)(s * (KV_STAGE >> 4));
         const uint32_t d = tmem + TM_S + sb * BN;
@@ -510,6 +599,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         const int sj = j % STAGES, pb = j & 1;
         wait_or_fail(ok, bar(B_PFULL + pb), (j >> 1) & 1, 14);
         if (!ok) break;
+        if (SPARSE) fence_async_shared();
         tc_fence_after();
         const uint64_t soff = (uint64_t)(sj * (KV_STAGE >> 4));
 #pragma unroll
@@ -601,6 +691,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     int armed = min(ntiles, 2), received = 0;  // exchange phases armed / completed
     float m_run = -INFINITY, l_part = 0.f;
     float s[CPT];
+    // index-list mode: this warp's lane holds list entry c0 + lane of a tile
+    const int32_t* list = SPARSE ? p.topk + ((size_t)b * p.L + l) * p.topk_k : nullptr;
+    auto list_entry = [&](int i) {
+      const int j = kv0 + i * BN + c0 + lane;
+      return j < kv1 ? list[j] : -1;
+    };
+    int pos_next = -1;
     if (ntiles > 0) {
       // this CTA's latent query columns into TMEM as bf16 pairs (the fold wrote them)
       pdl_wait();
@@ -625,6 +722,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_QTMEM));
+      if (SPARSE) pos_next = list_entry(0);
       load_partial(ok, tmem, lane_base, c0, 0, bar(B_SFULL), bar(B_SFREE), p.sl2, s);
     }
     cluster_wait();  // the peer's barriers are set up before the first remote arrive
@@ -654,7 +752,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
           s[j + 1] += f.y;
         }
       }
-      if (edge) {
+      if (SPARSE) {
+        // every row of the tile is one verify row: one mask per warp
+        const uint32_t vm = __ballot_sync(0xffffffffu, pos_next >= 0 && pos_next <= last_t);
+        if (i + 1 < ntiles) pos_next = list_entry(i + 1);
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) s[j] = ((vm >> j) & 1u) ? s[j] : -INFINITY;
+      } else if (edge) {
 #pragma unroll
         for (int j = 0; j < CPT; ++j) s[j] = (t0 + c0 + j <= last_t) ? s[j] : -INFINITY;
       }
@@ -720,7 +824,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       l_part += rs[0] + rs[1];
       // positions at or past T in the last tile: zero their value rows (they may hold
       // anything, and 0 * NaN would poison the accumulator)
-      if (t0 + BN > T) {
+      if (!SPARSE && t0 + BN > T) {
         const int z0 = max(T - t0, 0);
         const uint32_t st = sKV + (i % STAGES) * KV_STAGE;
         const int units = (BN - z0) * 8;  // 16-byte units per 128-byte row
@@ -829,6 +933,7 @@ struct MergeParams {
   __nv_bfloat16* o_lat;         // [B*R, 512]
   int R, chunk, splits;
   int rows;                     // B*R
+  int fixed_len;                // > 0: every sequence's pieces split this many list entries
 };
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
@@ -854,7 +959,7 @@ __global__ void __launch_bounds__(32 * W) merge_sm103(MergeParams p) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the length is a call input: read it while the attention finishes, so the
   // pieces' loads are the only round trip after the wait
-  const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
+  const int nsplit = ((p.fixed_len > 0 ? p.fixed_len : p.lens[b]) + p.chunk - 1) / p.chunk;
   pdl_wait();
   const size_t base = (size_t)b * p.splits * p.R + row;
   const size_t stride = (size_t)p.R;
@@ -949,7 +1054,8 @@ __global__ void __launch_bounds__(32 * MR_ROWS) merge_rows_sm103(MergeParams p) 
   const bool live = rg < p.rows;
   const int b = live ? rg / p.R : 0, row = rg - b * p.R;
   // (the length is a call input: read it before the wait)
-  const int nsplit = live ? (p.lens[b] + p.chunk - 1) / p.chunk : 0;
+  const int nsplit =
+      live ? ((p.fixed_len > 0 ? p.fixed_len : p.lens[b]) + p.chunk - 1) / p.chunk : 0;
   pdl_wait();
   if (!live) return;
   const size_t base = (size_t)b * p.splits * p.R + row;
@@ -1027,6 +1133,7 @@ struct UnembedMergeParams {
   int B, L, H, R, v, splits, chunk;
   int Lc;                 // verify rows per chunk (Lc * splits <= 64)
   int chunks_per_cta;     // consecutive chunks of the (sequence, verify-row block) list
+  int fixed_len;          // > 0: every sequence's pieces split this many list entries
 };
 constexpr int UM_THREADS = 256;            // warp 0 issues, 1..3 weights, 4..7 epilogue
 constexpr int UM_W = 2 * kLat * 128;       // W_UV tile
@@ -1122,7 +1229,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
         const int c = row / Lc, li = row - c * Lc;
         const int b = (g0 + c) / cps, l = ((g0 + c) % cps) * Lc + li;
         float* wt = wts + c * 64 + li * S;
-        const int nsplit = l < p.L ? (p.lens[b] + p.chunk - 1) / p.chunk : 0;
+        const int len = p.fixed_len > 0 ? p.fixed_len : p.lens[b];
+        const int nsplit = l < p.L ? (len + p.chunk - 1) / p.chunk : 0;
         const size_t base = (size_t)b * S * p.R + (size_t)min(l, p.L - 1) * p.H + h;
         float2 ml[8];
         float M = -FLT_MAX;
@@ -1152,7 +1260,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
           for (int s = lane; s < S; s += 32) wt[s] = 0.f;
           continue;
         }
-        const int nsplit = (p.lens[b] + p.chunk - 1) / p.chunk;
+        const int nsplit = ((p.fixed_len > 0 ? p.fixed_len : p.lens[b]) + p.chunk - 1) / p.chunk;
         const size_t base = (size_t)b * S * p.R + (size_t)l * p.H + h;
         float2 ml[2];
         float M = -FLT_MAX;
@@ -1301,7 +1409,8 @@ const DeviceSetup& device_setup() {
   DeviceSetup& d = setups[dev];
   if (d.done) return d;
   cudaError_t e = set_smem(swapab_gemm_sm103, gemm_smem(kLat, 64));
-  if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103, ATTN_SMEM);
+  if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103<false>, ATTN_SMEM);
+  if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103<true>, ATTN_SMEM);
   if (e == cudaSuccess) e = set_smem(unembed_merge_sm103, UM_SMEM);
   int slots = 0;
   if (e == cudaSuccess) {
@@ -1316,7 +1425,7 @@ const DeviceSetup& device_setup() {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&slots, absorbed_attn_sm103, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&slots, absorbed_attn_sm103<false>, &cfg) != cudaSuccess)
       slots = 0;
   }
   if (slots <= 0) {
@@ -1392,10 +1501,22 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     ap.ml = ml;
     ap.pf = (const char*)a.W_UV;
     ap.pf_bytes = (size_t)p.H * kLat * p.v * 2;
-    KernelTimer kt("absorbed_attn_sm103", a.stream);
-    e = launch_pdl(absorbed_attn_sm103, dim3(2 * ((R + BM - 1) / BM), p.splits, p.B),
-                   dim3(ATTN_THREADS),
-                   ATTN_SMEM, a.stream, tm_qr, tm_ckv, tm_kr, tm_op, ap);
+    ap.topk = a.topk;
+    ap.topk_k = a.topk_k;
+    ap.ckv = (const char*)c.c_kv;
+    ap.kr = (const char*)c.k_rope;
+    ap.ckv_stride = c.ckv_stride;
+    ap.kr_stride = c.kr_stride;
+    const dim3 grid(2 * ((R + BM - 1) / BM), p.splits, p.B);
+    if (a.topk) {
+      KernelTimer kt("absorbed_attn_sparse_sm103", a.stream);
+      e = launch_pdl(absorbed_attn_sm103<true>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
+                     tm_qr, tm_ckv, tm_kr, tm_op, ap);
+    } else {
+      KernelTimer kt("absorbed_attn_sm103", a.stream);
+      e = launch_pdl(absorbed_attn_sm103<false>, grid, dim3(ATTN_THREADS), ATTN_SMEM, a.stream,
+                     tm_qr, tm_ckv, tm_kr, tm_op, ap);
+    }
     if (e != cudaSuccess) return e;
   }
   if (p.splits <= 64) {
@@ -1422,6 +1543,7 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     if (cpc < 1) cpc = 1;
     if (cpc > UM_MAX_CHUNKS) cpc = UM_MAX_CHUNKS;
     up.chunks_per_cta = (int)cpc;
+    up.fixed_len = a.topk ? a.topk_k : 0;
     {
       // the pieces of one head as [l][piece][h][col]: row (b, s, l, h) of
       // o_part sits at ((b * splits + s) * R + l * H + h) * 512 elements
@@ -1441,7 +1563,8 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
     }
   }
   {
-    MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits, p.B * R};
+    MergeParams mp{o_part, ml, a.lens, o_lat, R, p.chunk, p.splits, p.B * R,
+                   a.topk ? a.topk_k : 0};
     KernelTimer kt("merge_sm103", a.stream);
     if (p.splits >= 48)
       e = launch_pdl(merge_sm103<1, 8>, dim3(p.B * R, 2), dim3(256), 0, a.stream, mp);

@@ -12,6 +12,12 @@
 //   O_part [B, splits, L*H, Dv]   un-normalised sum of exp(s - m) * value
 //   ml     [B, splits, L*H, 2]    (m, l): running max and sum of exp(s - m)
 // Sequence b uses ceil(T_b / chunk) pieces; pieces past that are never read.
+//
+// Sparse (top-k) calls ("One guard, 110x off the verify step", section "The
+// sparse model is different": attention runs over the positions an indexer
+// selected) replace the position range of a row by its index list: verify
+// row l of sequence b reads topk[b, l, 0..k), an entry used when
+// 0 <= t <= T_b - L + l; pieces split the list, ceil(k / chunk) of them.
 
 #include <cuda_bf16.h>
 
@@ -75,6 +81,8 @@ struct AttnParams {
   CacheView cache;
   const void* kexp;         // materialised: T [B, Tmax, H, n+v]
   const int32_t* lens;
+  const int32_t* topk;      // sparse: [B, L, topk_k] positions, else NULL
+  int topk_k;
   int L, H, Dm, rope, Dv, n_plus_v, Tmax;
   float scale;
   int chunk, splits;
@@ -89,12 +97,14 @@ __global__ void __launch_bounds__(128) attn_rows_kernel(AttnParams p) {
   const int LH = p.L * p.H;
   const int row = blockIdx.x * 4 + warp;
   const int Tb = p.lens[b];
-  const int nsplit = (Tb + p.chunk - 1) / p.chunk;
+  const int klen = p.topk ? p.topk_k : Tb;  // positions (or list entries) to split
+  const int nsplit = (klen + p.chunk - 1) / p.chunk;
   if (s >= nsplit || row >= LH) return;
   const int l = row / p.H, h = row - l * p.H;
   const int last = Tb - p.L + l;  // last visible position of this row
   const int t0 = s * p.chunk;
-  const int t1 = min(min(t0 + p.chunk, Tb), last + 1);
+  const int t1 = p.topk ? min(t0 + p.chunk, klen) : min(min(t0 + p.chunk, Tb), last + 1);
+  const int32_t* list = p.topk ? p.topk + ((size_t)b * p.L + l) * p.topk_k : nullptr;
 
   const int km = p.Dm / 32, kr = p.rope / 32, kv = p.Dv / 32;
   const int rm = p.Dm - km * 32, rr = p.rope - kr * 32, rvv = p.Dv - kv * 32;  // ragged tails
@@ -120,7 +130,14 @@ __global__ void __launch_bounds__(128) attn_rows_kernel(AttnParams p) {
   float m = -FLT_MAX, lsum = 0.f;
   const T* ckv = (const T*)p.cache.c_kv;
   const T* krp = (const T*)p.cache.k_rope;
-  for (int t = t0; t < t1; ++t) {
+  bool any = false;
+  for (int j = t0; j < t1; ++j) {
+    int t = j;
+    if (list) {
+      t = list[j];
+      if (t < 0 || t > last) continue;  // padding, or past the row's causal limit
+    }
+    any = true;
     const int64_t crow = cache_row(p.cache, b, t);
     if (crow < 0) {  // page id out of range: the position is left out
       if (lane == 0) report_bad_page();
@@ -169,7 +186,7 @@ __global__ void __launch_bounds__(128) attn_rows_kernel(AttnParams p) {
     if (k < kv || (k == kv && lane < rvv)) op[d] = o[k];
   }
   if (lane == 0) {
-    p.ml[prow * 2 + 0] = t1 > t0 ? m : -FLT_MAX;
+    p.ml[prow * 2 + 0] = any ? m : -FLT_MAX;
     p.ml[prow * 2 + 1] = lsum;
   }
 }
@@ -198,7 +215,7 @@ __global__ void combine_unembed_kernel(const float* __restrict__ o_part,
                                        const float* __restrict__ ml, const T* __restrict__ W_UV,
                                        const int32_t* __restrict__ lens, T* __restrict__ out,
                                        int B, int L, int H, int r, int v, int chunk,
-                                       int splits) {
+                                       int splits, int fixed_len) {
   extern __shared__ float so[];  // [ROWS][r]
   const int h = blockIdx.y;
   const int g0 = blockIdx.x * ROWS;  // first (b*L + l)
@@ -207,7 +224,8 @@ __global__ void combine_unembed_kernel(const float* __restrict__ o_part,
   for (int rr = 0; rr < nrows; ++rr) {
     const int bl = g0 + rr;
     const int b = bl / L, l = bl - b * L;
-    const int nsplit = (lens[b] + chunk - 1) / chunk;
+    // pieces of this sequence: its cache length, or the index-list length
+    const int nsplit = ((fixed_len > 0 ? fixed_len : lens[b]) + chunk - 1) / chunk;
     const size_t row = (size_t)l * H + h;
     const float* mlr = ml + (((size_t)b * splits) * LH + row) * 2;
     float M;
@@ -359,6 +377,8 @@ cudaError_t run_absorbed(const Plan& p, const Args& a) {
     ap.cache = a.cache;
     ap.kexp = nullptr;
     ap.lens = a.lens;
+    ap.topk = a.topk;
+    ap.topk_k = a.topk_k;
     ap.L = p.L; ap.H = p.H; ap.Dm = p.r; ap.rope = p.rope; ap.Dv = p.r; ap.n_plus_v = 0;
     ap.Tmax = p.Tmax; ap.scale = p.scale; ap.chunk = p.chunk; ap.splits = p.splits;
     ap.o_part = o_part; ap.ml = ml;
@@ -373,7 +393,7 @@ cudaError_t run_absorbed(const Plan& p, const Args& a) {
     combine_unembed_kernel<T, ROWS_UNEMBED>
         <<<grid, threads, ROWS_UNEMBED * p.r * sizeof(float), a.stream>>>(
             o_part, ml, (const T*)a.W_UV, a.lens, (T*)a.out, p.B, p.L, p.H, p.r, p.v, p.chunk,
-            p.splits);
+            p.splits, a.topk ? a.topk_k : 0);
   }
   return cudaGetLastError();
 }
@@ -396,6 +416,8 @@ cudaError_t run_materialised(const Plan& p, const Args& a) {
     ap.cache = a.cache;
     ap.kexp = kexp;
     ap.lens = a.lens;
+    ap.topk = nullptr;
+    ap.topk_k = 0;
     ap.L = p.L; ap.H = p.H; ap.Dm = p.n; ap.rope = p.rope; ap.Dv = p.v;
     ap.n_plus_v = p.n + p.v;
     ap.Tmax = p.Tmax; ap.scale = p.scale; ap.chunk = p.chunk; ap.splits = p.splits;

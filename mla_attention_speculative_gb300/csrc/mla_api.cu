@@ -375,16 +375,52 @@ extern "C" mla_status_t mla_workspace_bytes(const mla_geometry_t* g, int32_t bat
   return MLA_OK;
 }
 
-extern "C" mla_status_t mla_verify_attention(
+namespace mla {
+
+// The plan of a sparse (top-k) call: the absorbed branch, with the pieces
+// cut along each row's index list of topk_len entries instead of [0, T_b).
+static mla_status_t make_sparse_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
+                                     const int32_t* lens_host, int32_t topk_len, Plan* p) {
+  if (!geometry_ok(g) || !lens_ok(lens_host, batch, L)) return MLA_ERR_INVALID_ARG;
+  if (topk_len < 1) {
+    set_error("topk_len %d < 1", topk_len);
+    return MLA_ERR_INVALID_ARG;
+  }
+  // the planner sizes pieces from these lengths (at least L, which it requires)
+  std::vector<int32_t> plan_lens(batch, topk_len > L ? topk_len : L);
+  const mla_status_t st = make_plan(g, batch, L, plan_lens.data(), MLA_MODE_ABSORBED, p);
+  if (st != MLA_OK) return st;
+  // the tensor-core kernel takes one verify row per 128-row tile
+  if (p->fast_ok && p->H % 128 != 0) {
+    p->fast_ok = false;
+    p->ws_bytes = p->generic.bytes;
+  }
+  return MLA_OK;
+}
+
+// Validation and launch shared by the dense and the sparse entry points
+// (topk == NULL: dense).
+static mla_status_t verify_impl(
     const mla_geometry_t* g, const void* q_nope, const void* q_rope, const void* c_kv,
     const void* k_rope, int64_t c_kv_row_stride, int64_t k_rope_row_stride,
     int64_t seq_stride_rows, const void* W_UK, const void* W_UV, const int32_t* lens_dev,
-    const int32_t* lens_host, int32_t batch, int32_t L, const int32_t* page_table,
-    int32_t page_size, int32_t max_pages_per_seq, int32_t num_pages, int32_t mode, void* out,
-    void* workspace, size_t workspace_bytes, void* stream, int32_t* branch_taken) {
+    const int32_t* lens_host, int32_t batch, int32_t L, const int32_t* topk, int32_t topk_len,
+    const int32_t* page_table, int32_t page_size, int32_t max_pages_per_seq, int32_t num_pages,
+    int32_t mode, void* out, void* workspace, size_t workspace_bytes, void* stream,
+    int32_t* branch_taken) {
   Plan p;
-  mla_status_t st = make_plan(g, batch, L, lens_host, mode, &p);
+  mla_status_t st = topk ? make_sparse_plan(g, batch, L, lens_host, topk_len, &p)
+                         : make_plan(g, batch, L, lens_host, mode, &p);
   if (st != MLA_OK) return st;
+  if (topk) {
+    // the real cache lengths bound the addresses the list may name
+    p.Tmax = 0;
+    for (int b = 0; b < batch; ++b) p.Tmax = lens_host[b] > p.Tmax ? lens_host[b] : p.Tmax;
+    if (!aligned16(topk)) {
+      set_error("topk is not 16-byte aligned");
+      return MLA_ERR_INVALID_ARG;
+    }
+  }
 
   const void* ptrs[] = {q_nope, q_rope, c_kv, k_rope, W_UK, W_UV, lens_dev, out};
   const char* names[] = {"q_nope", "q_rope", "c_kv", "k_rope", "W_UK", "W_UV",
@@ -454,6 +490,8 @@ extern "C" mla_status_t mla_verify_attention(
   a.W_UK = W_UK;
   a.W_UV = W_UV;
   a.lens = lens_dev;
+  a.topk = topk;
+  a.topk_k = topk ? topk_len : 0;
   a.out = out;
   a.ws = (char*)workspace;
   a.stream = (cudaStream_t)stream;
@@ -464,6 +502,7 @@ extern "C" mla_status_t mla_verify_attention(
                                         : (int64_t)(batch - 1) * seq_stride_rows + p.Tmax;
   const bool fast = p.fast_ok && (page_table == nullptr || page_size % 64 == 0) &&
                     cache_rows < ((int64_t)1 << 31);
+  // (the generic kernels' split plan was made with the list length as T too)
   cudaError_t e;
   if (fast) {
     p.use(p.fast);
@@ -479,6 +518,49 @@ extern "C" mla_status_t mla_verify_attention(
   }
   if (branch_taken) *branch_taken = p.branch;
   return MLA_OK;
+}
+
+}  // namespace mla
+
+extern "C" mla_status_t mla_verify_attention(
+    const mla_geometry_t* g, const void* q_nope, const void* q_rope, const void* c_kv,
+    const void* k_rope, int64_t c_kv_row_stride, int64_t k_rope_row_stride,
+    int64_t seq_stride_rows, const void* W_UK, const void* W_UV, const int32_t* lens_dev,
+    const int32_t* lens_host, int32_t batch, int32_t L, const int32_t* page_table,
+    int32_t page_size, int32_t max_pages_per_seq, int32_t num_pages, int32_t mode, void* out,
+    void* workspace, size_t workspace_bytes, void* stream, int32_t* branch_taken) {
+  return verify_impl(g, q_nope, q_rope, c_kv, k_rope, c_kv_row_stride, k_rope_row_stride,
+                     seq_stride_rows, W_UK, W_UV, lens_dev, lens_host, batch, L, nullptr, 0,
+                     page_table, page_size, max_pages_per_seq, num_pages, mode, out, workspace,
+                     workspace_bytes, stream, branch_taken);
+}
+
+extern "C" mla_status_t mla_sparse_workspace_bytes(const mla_geometry_t* g, int32_t batch,
+                                                   int32_t L, const int32_t* lens_host,
+                                                   int32_t topk_len, size_t* bytes) {
+  if (bytes == nullptr) { set_error("bytes output is NULL"); return MLA_ERR_INVALID_ARG; }
+  Plan p;
+  const mla_status_t st = make_sparse_plan(g, batch, L, lens_host, topk_len, &p);
+  if (st != MLA_OK) return st;
+  *bytes = p.ws_bytes;
+  return MLA_OK;
+}
+
+extern "C" mla_status_t mla_verify_attention_sparse(
+    const mla_geometry_t* g, const void* q_nope, const void* q_rope, const void* c_kv,
+    const void* k_rope, int64_t c_kv_row_stride, int64_t k_rope_row_stride,
+    int64_t seq_stride_rows, const void* W_UK, const void* W_UV, const int32_t* lens_dev,
+    const int32_t* lens_host, int32_t batch, int32_t L, const int32_t* topk, int32_t topk_len,
+    const int32_t* page_table, int32_t page_size, int32_t max_pages_per_seq, int32_t num_pages,
+    void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (topk == nullptr) {
+    set_error("topk is NULL");
+    return MLA_ERR_INVALID_ARG;
+  }
+  return verify_impl(g, q_nope, q_rope, c_kv, k_rope, c_kv_row_stride, k_rope_row_stride,
+                     seq_stride_rows, W_UK, W_UV, lens_dev, lens_host, batch, L, topk, topk_len,
+                     page_table, page_size, max_pages_per_seq, num_pages, MLA_MODE_ABSORBED, out,
+                     workspace, workspace_bytes, stream, nullptr);
 }
 
 extern "C" const char* mla_status_string(int32_t s) {

@@ -88,6 +88,10 @@ struct Args {
   const void* W_UK;
   const void* W_UV;
   const int32_t* lens;      // device
+  // sparse (top-k) calls: [B, L, topk_k] device positions per verify row;
+  // NULL for the dense call
+  const int32_t* topk = nullptr;
+  int topk_k = 0;
   void* out;
   char* ws;                 // device workspace base
   cudaStream_t stream;

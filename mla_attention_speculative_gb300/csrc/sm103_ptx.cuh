@@ -235,27 +235,27 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
-// Global counters shared by the CTAs of one grid: a release add publishes this
-// thread's earlier writes (and those ordered before it by a CTA barrier) to a
-// thread whose acquire load then reads the sum.
-__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// Order this thread's async-proxy (TMA) global writes, already complete,
-// before its later generic-proxy operations.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA / tensor core) accesses.
 __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------ per-thread async copies
+// 16 bytes from global to shared memory; src_bytes < 16 fills the rest of
+// the 16 bytes with zeros (src_bytes == 0 reads nothing).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed (the barrier's count includes these arrivals).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ----------------------------------------------------------------- tcgen05

@@ -180,3 +180,29 @@ def workload_shapes(name: str):
             lens = uniform_cache_lens(int(B), int(lo), int(hi), w["seed"])
         out.append((L, list(lens)))
     return out
+
+
+def make_topk(cache_lens, L: int, k: int, seed: int, pad: int = 0, past_limit: int = 0,
+              device="cpu") -> torch.Tensor:
+    """Seeded synthetic index lists for the sparse (top-k) call: int32
+    [B, L, k].  Row l of sequence b lists k distinct positions drawn uniformly
+    from [0, T_b) (all of them, in random order, padded with -1 when k > T_b),
+    a stand-in for an indexer's selection; then the last ``pad`` entries of
+    every list become -1 and ``past_limit`` entries (when there are that many
+    positions past the row's causal limit T_b - L + l) are swapped for such
+    positions, which the attention must skip."""
+    B = len(cache_lens)
+    g = torch.Generator().manual_seed(int(seed) + 104729)
+    out = torch.full((B, L, k), -1, dtype=torch.int32)
+    for b, T in enumerate(cache_lens):
+        for l in range(L):
+            perm = torch.randperm(int(T), generator=g)[:k].to(torch.int32)
+            out[b, l, :perm.numel()] = perm
+            last = int(T) - L + l
+            beyond = torch.arange(last + 1, int(T), dtype=torch.int32)
+            m = min(int(past_limit), beyond.numel(), k)
+            if m:
+                out[b, l, :m] = beyond[:m]
+            if pad:
+                out[b, l, k - min(pad, k):] = -1
+    return out.to(device)

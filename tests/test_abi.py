@@ -204,3 +204,39 @@ def test_noalloc_binding_rejects_non_contiguous_views():
     for fn in (B.mla_verify_attention_noalloc, B.mla_verify_attention):
         with pytest.raises(ValueError, match="q_nope must be contiguous"):
             fn(q, qr, ckv, kr, wuk, wuv, [64])
+
+
+# ---------------------------------------------------------------------------
+# Sparse (top-k) entry points: host-side checks, no GPU
+# ---------------------------------------------------------------------------
+
+def _sparse_call(topk=0x40000, k=8, **over):
+    lib = B.lib()
+    geom = _geom()
+    lens = (ctypes.c_int32 * 1)(64)
+    fake = 0x10000
+    a = dict(q_nope=fake, L=4, ws=None, ws_bytes=0)
+    a.update(over)
+    return lib.mla_verify_attention_sparse(
+        ctypes.byref(geom), a["q_nope"], fake, fake, fake, 512, 64, 64, fake, fake, fake, lens,
+        1, a["L"], topk, k, None, 0, 0, 0, fake, a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(topk=None), B.MLA_ERR_INVALID_ARG),
+    (dict(k=0), B.MLA_ERR_INVALID_ARG),
+    (dict(topk=0x40004), B.MLA_ERR_INVALID_ARG),   # misaligned list
+    (dict(L=65), B.MLA_ERR_INVALID_ARG),           # L > T
+    (dict(), B.MLA_ERR_WORKSPACE),                 # no workspace given
+])
+def test_sparse_call_rejects_before_launch(over, status):
+    assert _sparse_call(**over) == status
+    assert B.mla_last_error() != ""
+
+
+def test_sparse_workspace_follows_the_list_length():
+    g = _geom(H=128)
+    small = B.mla_sparse_workspace_bytes(g, 1, [32768], 64)
+    large = B.mla_sparse_workspace_bytes(g, 1, [32768], 2048)
+    dense = B.mla_workspace_bytes(g, 1, [32768], "absorbed")
+    assert 0 < small <= large <= dense
