@@ -10,4 +10,4 @@ from .mla_oracle import (  # noqa: F401
     max_absorbed_queries, max_absorbed_queries_batch, select_branch, sparse_absorbed,
 )
 from .draft_cap import accepted, select_draft_cap  # noqa: F401
-from . import rollback_state  # noqa: F401
+from . import indexer_pool, rollback_state  # noqa: F401
