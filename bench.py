@@ -86,14 +86,15 @@ def visible(L: int, T: int) -> int:
     return L * (T - L) + L * (L + 1) // 2
 
 
-def kernel_work(kernel: str, geom, L: int, lens):
+def kernel_work(kernel: str, geom, L: int, lens, topk_k: int = 0):
     """(bytes, flops) one launch of `kernel` must move / do for one call.
 
     Bytes count what the kernel's role needs to cross HBM once, with bf16
     intermediates (q_lat, o_lat, the expanded K/V) as the minimal hand-off
     between kernels; split-KV partials are an implementation cost and are not
     counted.  Flops count the contraction the kernel performs over the
-    positions each row may see (2 per multiply-add; masked work not counted)."""
+    positions each row may see (2 per multiply-add; masked work not counted).
+    A sparse call (topk_k > 0) reads topk_k listed rows per verify row."""
     bf = 2
     H, r, n, v, rope = geom.H, geom.r, geom.n, geom.v, geom.rope
     d = n + v
@@ -102,6 +103,9 @@ def kernel_work(kernel: str, geom, L: int, lens):
     sT = sum(lens)
     vis = sum(visible(L, T) for T in lens)
     cache = sT * (r + rope) * bf
+    if topk_k:
+        vis = B * L * topk_k
+        cache = vis * (r + rope) * bf
     fold = (H * n * r * bf + rows * (n + r) * bf, 2 * rows * n * r)
     attend = (cache + rows * (r + rope) * bf + rows * r * bf, 2 * H * vis * (2 * r + rope))
     unembed = (H * r * v * bf + rows * (r + v) * bf, 2 * rows * r * v)
@@ -111,6 +115,7 @@ def kernel_work(kernel: str, geom, L: int, lens):
     table = {
         "fold_sm103": fold, "generic_fold": fold,
         "absorbed_attn_sm103": attend, "generic_absorbed_attention": attend,
+        "absorbed_attn_sparse_sm103": attend,
         "unembed_merge_sm103": unembed, "unembed_sm103": unembed,
         "generic_combine_unembed": unembed,
         "expand_sm103": expand, "generic_expand": expand,
@@ -125,7 +130,7 @@ def _work(kernel: str, L: int, T: int):
     return kernel_work(kernel, DSV3, L, [T])
 
 
-def call_work(branch: str, geom, L: int, lens):
+def call_work(branch: str, geom, L: int, lens, topk_k: int = 0):
     """Algorithmic (bytes, flops, cache_bytes) of one verify call, as the
     method must do it (masked positions and the softmax not counted;
     vis_b = visible(L, T_b)):
@@ -138,8 +143,12 @@ def call_work(branch: str, geom, L: int, lens):
     d = n + v
     B = len(lens)
     cache = sum(T * (r + rope) * 2 for T in lens)
+    if topk_k:  # sparse: every verify row reads its topk_k listed rows
+        cache = B * L * topk_k * (r + rope) * 2
     byts = cache + H * (n * r + r * v) * 2 + B * L * H * (n + rope + v) * 2
-    if branch == "absorbed":
+    if topk_k:
+        flops = B * 2 * H * L * (n * r + topk_k * (2 * r + rope) + r * v)
+    elif branch == "absorbed":
         flops = sum(2 * H * (L * n * r + visible(L, T) * (2 * r + rope) + L * r * v)
                     for T in lens)
     else:
@@ -148,9 +157,9 @@ def call_work(branch: str, geom, L: int, lens):
     return byts, flops, cache
 
 
-def call_roofline(branch: str, geom, L: int, lens, us: float, peaks) -> dict:
+def call_roofline(branch: str, geom, L: int, lens, us: float, peaks, topk_k: int = 0) -> dict:
     """Fraction of the call roofline max(bytes / BW, flops / peak) reached in `us`."""
-    byts, flops, cache = call_work(branch, geom, L, lens)
+    byts, flops, cache = call_work(branch, geom, L, lens, topk_k)
     t_b = byts / (peaks["hbm_gbs"] * 1e3)      # us
     t_f = flops / (peaks["bf16_tflops"] * 1e6)  # us
     t_c = cache / (peaks["hbm_gbs"] * 1e3)
@@ -158,10 +167,10 @@ def call_roofline(branch: str, geom, L: int, lens, us: float, peaks) -> dict:
             "frac": max(t_b, t_f) / us, "cache_only_frac": max(t_c, t_f) / us}
 
 
-def kernel_rates(kernel: str, geom, L: int, lens, us: float, peaks) -> dict:
+def kernel_rates(kernel: str, geom, L: int, lens, us: float, peaks, topk_k: int = 0) -> dict:
     """A launch's achieved HBM and tensor rates and the fraction of the bound
     that its algorithmic work puts it under."""
-    w = kernel_work(kernel, geom, L, lens)
+    w = kernel_work(kernel, geom, L, lens, topk_k)
     ent = {"us": us}
     if w is None:
         return ent
@@ -182,7 +191,9 @@ def kernel_rates(kernel: str, geom, L: int, lens, us: float, peaks) -> dict:
 #   page 64, shuffled page table, absorbed);
 # - long-context verify (512/256/256, H = 64, B = 4, T = 131072, L = 1, 5, 8,
 #   16, auto) and its cold prefill (T = L = 2048, auto -> materialised);
-# - the DeepSeek-V3-like width-16 call forced onto the materialised branch.
+# - the DeepSeek-V3-like width-16 call forced onto the materialised branch;
+# - the sparse (top-k) call at the sparse model's budget of 2048 positions
+#   (DeepSeek-V3-like geometry, seeded random lists) at caches of 8K and 32K.
 CROSSOVER_L = (1, 16, 64, 128, 256, 379, 398, 512, 1024, 2048)
 L2_ROTATE_BYTES = 256 << 20   # rotate input copies until a graph touches this much
 
@@ -200,6 +211,9 @@ def _shape_list():
         out.append(dict(group="long_context", geom=I.GLM53, L=L, lens=lens, mode="auto", page=0))
     out.append(dict(group="dsv3_forced_materialised", geom=I.DSV3, L=16, lens=[8192],
                     mode="materialised", page=0))
+    for T, L in ((8192, 1), (32768, 1), (32768, 4), (32768, 8)):
+        out.append(dict(group="sparse_dsv3_k2048", geom=I.DSV3, L=L, lens=[T], mode="sparse",
+                        page=0, topk=2048))
     return out
 
 
@@ -212,6 +226,7 @@ def _bench_shapes(B, dev, peaks, reps):
     groups = {}
     for k, sh in enumerate(_shape_list()):
         geom, L, lens, mode, page = sh["geom"], sh["L"], sh["lens"], sh["mode"], sh["page"]
+        kk = sh.get("topk", 0)
         layer_bytes = (sum(lens) * (geom.r + geom.rope)
                        + geom.H * geom.r * (geom.n + geom.v)) * 2
         copies = max(1, min(8, -(-L2_ROTATE_BYTES // layer_bytes)))
@@ -219,24 +234,35 @@ def _bench_shapes(B, dev, peaks, reps):
                  for i in range(copies)]
         lens_dev = torch.tensor(lens, dtype=torch.int32, device=dev)
         g = B.make_geometry(geom.H, geom.r, geom.n, geom.v, geom.rope, torch.bfloat16)
-        ws = B.new_workspace(B.mla_workspace_bytes(g, L, lens, mode), dev)
+        if kk:
+            ws = B.new_workspace(B.mla_sparse_workspace_bytes(g, L, lens, kk), dev)
+            lists = [I.make_topk(lens, L, kk, seed=4000 + i, device=dev) for i in range(copies)]
+        else:
+            ws = B.new_workspace(B.mla_workspace_bytes(g, L, lens, mode), dev)
         out = torch.empty((len(lens), L, geom.H, geom.v), dtype=torch.bfloat16, device=dev)
         br = {}
 
-        def call(c):
+        def call(i):
+            c = cases[i]
+            if kk:
+                B.mla_verify_attention_sparse(
+                    c.q_nope, c.q_rope, c.c_kv, c.k_rope, c.W_UK, c.W_UV, lens,
+                    lists[i], out=out, workspace=ws, cache_lens_dev=lens_dev)
+                br["b"] = B.BRANCH_ABSORBED
+                return
             _, br["b"] = B.mla_verify_attention(
                 c.q_nope, c.q_rope, c.c_kv, c.k_rope, c.W_UK, c.W_UV, lens, mode=mode,
                 out=out, workspace=ws, cache_lens_dev=lens_dev,
                 page_table=c.page_table if page else None)
 
-        for c in cases:
-            call(c)
+        for i in range(copies):
+            call(i)
         torch.cuda.synchronize()
         st = torch.cuda.Stream(dev)
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=st):
-            for c in cases:
-                call(c)
+            for i in range(copies):
+                call(i)
         gr.replay()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -249,16 +275,18 @@ def _bench_shapes(B, dev, peaks, reps):
         B.mla_kernel_timing_read(reset=True)
         B.mla_kernel_timing_enable(True)
         for _ in range(max(1, reps // 2)):
-            for c in cases:
-                call(c)
+            for i in range(copies):
+                call(i)
         torch.cuda.synchronize()
         B.mla_kernel_timing_enable(False)
         kt = B.mla_kernel_timing_read(reset=True)
         branch = B.BRANCH_NAMES[br["b"]]
         ent = {"L": L, "mode": mode, "branch": branch, "us_per_call": us_call,
-               "call_roofline": call_roofline(branch, geom, L, lens, us_call, peaks),
-               "kernels": {kn: kernel_rates(kn, geom, L, lens, ms * 1e3 / max(nl, 1), peaks)
+               "call_roofline": call_roofline(branch, geom, L, lens, us_call, peaks, kk),
+               "kernels": {kn: kernel_rates(kn, geom, L, lens, ms * 1e3 / max(nl, 1), peaks, kk)
                            for kn, (nl, ms) in kt.items()}}
+        if kk:
+            ent["topk"] = kk
         if len(lens) > 1:
             ent["B"] = len(lens)
             ent["sum_T"] = sum(lens)

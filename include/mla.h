@@ -317,6 +317,68 @@ mla_status_t mla_rollback_valid_prefix(const int32_t* blocks, int32_t n_blocks, 
                                        int32_t n_cells, int32_t p0, int32_t p1, int32_t seq,
                                        int32_t n_streams, int32_t* prefix_out, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Indexer key pooling for the sparse model ("One guard, 110x off the verify
+ * step", sections "The same bug, one layer over" and "The sparse model is
+ * different").  Window w of a sequence covers cache positions 4w..4w+3; its
+ * pooled key is the mean of the keys it holds (the last window of a cache
+ * whose length is not a multiple of four holds fewer).
+ * ------------------------------------------------------------------------ */
+
+/* What a pool describes: the cache length it was computed for (-1: no pool
+ * yet; a caller starts from {-1, 0, 0}), the batch and the key width. */
+typedef struct {
+  int64_t length;
+  int32_t batch;
+  int32_t dim;
+} mla_indexer_pool_state_t;
+
+/* One indexer step: the cache now holds cache_len tokens per sequence,
+ * new_tokens of them appended since the last step.  keys: device, dtype
+ * bf16 or fp32 (an mla_dtype_t), key (b, t) at
+ * keys + (b*seq_stride_rows + t)*key_row_stride; dim a multiple of 32 up to
+ * 512.  pooled: device fp32 [batch, pooled_windows_cap, dim] with
+ * pooled_windows_cap >= ceil(cache_len/4); *state (host) says what it holds.
+ *
+ * When every guard of the page holds -- the pool exists (state->length >= 0),
+ * there is no padding (padded == 0), the batch shape matches (state->batch ==
+ * batch, state->dim == dim) and the cache is exactly as long as the pool
+ * remembers (state->length == cache_len - new_tokens) -- only windows
+ * floor(state->length/4) .. ceil(cache_len/4)-1 are recomputed, for any
+ * new_tokens >= 1 (*incremental_out = 1).  Otherwise (for instance after a
+ * speculative rejection trimmed the cache) every window is recomputed
+ * (*incremental_out = 0).  Either way each window is computed by the same
+ * code, so a wide step pools bit for bit as the same tokens fed one at a
+ * time.  *state is updated on return.  Asynchronous on `stream`;
+ * incremental_out is host memory and may be NULL. */
+mla_status_t mla_indexer_pool_update(const void* keys, int32_t dtype, int64_t key_row_stride,
+                                     int64_t seq_stride_rows, int32_t batch, int32_t dim,
+                                     int64_t cache_len, int32_t new_tokens, int32_t padded,
+                                     float* pooled, int64_t pooled_windows_cap,
+                                     mla_indexer_pool_state_t* state, int32_t* incremental_out,
+                                     void* stream);
+
+/* Workspace bytes of mla_indexer_select (the scores of every window). */
+mla_status_t mla_indexer_select_workspace_bytes(int32_t batch, int32_t new_tokens,
+                                                int64_t cache_len, size_t* bytes);
+
+/* Top-k windows for each new token.  q: device fp32 [batch, new_tokens,
+ * dim] (one indexer query per new token, 1 <= new_tokens <= 32,
+ * new_tokens*dim*4 <= 48 KB).  Token s of a step sits at position
+ * p = cache_len - new_tokens + s and may pick window w when 4w <= p; score
+ * = q . pooled key (fp32).  It keeps the k_windows highest scores (ties to
+ * the lower window) and writes them in ascending window order to
+ * windows_out (device [batch, new_tokens, k_windows] int32, may be NULL)
+ * and their positions 4w+i (only those <= p) to positions_out (device
+ * [batch, new_tokens, 4*k_windows] int32), -1 padded: positions_out is the
+ * index list mla_verify_attention_sparse takes with L = new_tokens and
+ * topk_len = 4*k_windows (512 windows make the page's 2048 positions). */
+mla_status_t mla_indexer_select(const float* q, const float* pooled, int64_t pooled_windows_cap,
+                                int32_t batch, int32_t dim, int64_t cache_len,
+                                int32_t new_tokens, int32_t k_windows, int32_t* windows_out,
+                                int32_t* positions_out, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
 /* Per-kernel timing, for benchmarks.  While enabled, every kernel launch the
  * library makes is bracketed by a pair of CUDA events recorded on the call's
  * stream (events come from a library-owned pool; no device memory).  Do not

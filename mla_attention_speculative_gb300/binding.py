@@ -63,6 +63,11 @@ _SIGS = {
                                             _P, _P]),
     "mla_check_page_table": (_I32, [_P, _I32, _I32, _P, _I32, _I32]),
     "mla_sparse_workspace_bytes": (_I32, [_P, _I32, _I32, _P, _I32, _P]),
+    "mla_indexer_pool_update": (_I32, [_P, _I32, _I64, _I64, _I32, _I32, _I64, _I32, _I32, _P,
+                                       _I64, _P, _P, _P]),
+    "mla_indexer_select_workspace_bytes": (_I32, [_I32, _I32, _I64, _P]),
+    "mla_indexer_select": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _I32, _I32, _P, _P, _P,
+                                  ctypes.c_size_t, _P]),
     "mla_verify_attention_sparse": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P,
                                            _I32, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _P,
                                            ctypes.c_size_t, _P]),
@@ -480,3 +485,53 @@ def mla_verify_attention_sparse(q_nope: torch.Tensor, q_rope: torch.Tensor, c_kv
         [_ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), stream]
     _check(lib().mla_verify_attention_sparse(*cargs), "mla_verify_attention_sparse")
     return out
+
+
+class IndexerPoolState(ctypes.Structure):
+    """What a pool of indexer keys describes (mla_indexer_pool_state_t)."""
+    _fields_ = [("length", ctypes.c_int64), ("batch", ctypes.c_int32), ("dim", ctypes.c_int32)]
+
+    def __init__(self):
+        super().__init__(-1, 0, 0)
+
+
+def mla_indexer_pool_update(keys: torch.Tensor, cache_len: int, new_tokens: int,
+                            pooled: torch.Tensor, state: IndexerPoolState, padded: bool = False,
+                            stream=None) -> bool:
+    """Pool the indexer keys of one step.  keys [batch, Tmax, dim] (bf16 or
+    fp32, rows contiguous), pooled fp32 [batch, cap, dim]; ``state`` is
+    updated.  Returns True when the incremental (tail-only) path ran."""
+    if keys.dim() != 3 or keys.stride(-1) != 1 or not pooled.is_contiguous() or \
+            pooled.dtype != torch.float32:
+        raise ValueError("keys must be [batch, T, dim] with contiguous rows, pooled fp32 "
+                         "[batch, cap, dim] contiguous")
+    Bn, _, d = keys.shape
+    inc = ctypes.c_int32(0)
+    if stream is None:
+        stream = _current_stream(keys.device)
+    _check(lib().mla_indexer_pool_update(
+        _ptr(keys), DTYPES[keys.dtype], keys.stride(1), keys.stride(0) // keys.stride(1), Bn, d,
+        int(cache_len), int(new_tokens), 1 if padded else 0, _ptr(pooled), pooled.shape[1],
+        ctypes.byref(state), ctypes.byref(inc), stream), "mla_indexer_pool_update")
+    return bool(inc.value)
+
+
+def mla_indexer_select(q: torch.Tensor, pooled: torch.Tensor, cache_len: int, k_windows: int,
+                       stream=None):
+    """(windows [batch, S, k], positions [batch, S, 4k]) int32: each new
+    token's k best visible windows, ascending, and their positions."""
+    _dense(q=q, pooled=pooled)
+    Bn, S, d = q.shape
+    dev = q.device
+    wins = torch.empty((Bn, S, k_windows), dtype=torch.int32, device=dev)
+    pos = torch.empty((Bn, S, 4 * k_windows), dtype=torch.int32, device=dev)
+    nbytes = ctypes.c_size_t(0)
+    _check(lib().mla_indexer_select_workspace_bytes(Bn, S, int(cache_len), ctypes.byref(nbytes)),
+           "mla_indexer_select_workspace_bytes")
+    ws = new_workspace(nbytes.value, dev)
+    if stream is None:
+        stream = _current_stream(dev)
+    _check(lib().mla_indexer_select(_ptr(q), _ptr(pooled), pooled.shape[1], Bn, d, int(cache_len),
+                                    S, int(k_windows), _ptr(wins), _ptr(pos), _ptr(ws),
+                                    ws.numel(), stream), "mla_indexer_select")
+    return wins, pos
