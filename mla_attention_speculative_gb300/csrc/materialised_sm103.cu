@@ -265,6 +265,13 @@ struct MatAttnParams {
   int L, H, n, v;
   int ks, vs;          // K ring and V ring depths
   float sl2;           // softmax scale x log2(e)
+  int B;
+  // split-KV when the query tiles alone leave SMs idle: piece sp of a query
+  // tile covers KV tiles [sp * chunk_tiles, (sp + 1) * chunk_tiles) and
+  // leaves O / l (bf16) and (m, l) for mat_combine_sm103
+  int splits, chunk_tiles;
+  __nv_bfloat16* o_part;  // [B, splits, L, H, v]
+  float* ml;              // [B, splits, L, H, 2]
 };
 
 constexpr int MA_BM = 128;
@@ -305,13 +312,35 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
                                                          MatAttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // One CTA per (128-row query tile, KV piece, head, sequence), the query
+  // tiles and pieces of one head next to each other so that they share its
+  // expanded keys and values in L2.  (Handing out the longest query tiles
+  // first instead made the causal prefill 8 % slower: every wave then read
+  // 152 heads' keys and values.)
+  const int nqt = (p.L + MA_BM - 1) / MA_BM;
+  const int qt = (int)(blockIdx.x % nqt);
+  const int rest = (int)(blockIdx.x / nqt);
+  const int sp = rest % p.splits, h = (rest / p.splits) % p.H, b = rest / (p.splits * p.H);
   const int T = p.lens[b];
   const int n = p.n, v = p.v, L = p.L;
   const int l0 = qt * MA_BM;
   const int l_last = min(L - 1, l0 + MA_BM - 1);
   const int kv_end = T - L + l_last + 1;  // no row of the tile sees t >= kv_end
-  const int ntiles = (kv_end + MA_BN - 1) / MA_BN;
+  // this CTA's KV tiles: [i0, i0 + ntiles) of the tile's visible ones; the
+  // loops below count from 0, positions add tbase
+  const int i0 = sp * p.chunk_tiles;
+  const int ntiles = min((kv_end + MA_BN - 1) / MA_BN - i0, p.chunk_tiles);
+  const int tbase = i0 * MA_BN;
+  if (ntiles <= 0) {
+    // a piece past what the tile sees: an empty part for the combine
+    for (int q = threadIdx.x; q < MA_BM; q += blockDim.x) {
+      if (l0 + q >= L) continue;
+      const size_t prow = (((size_t)b * p.splits + sp) * L + l0 + q) * p.H + h;
+      p.ml[prow * 2] = -FLT_MAX;
+      p.ml[prow * 2 + 1] = 0.f;
+    }
+    return;
+  }
   const int KS = p.ks, VS = p.vs;
   const int QB = mat_q_bytes(n), KB = mat_k_bytes(n), VB = mat_v_bytes(v);
   const uint32_t sQ = smem_u32(smem), sK = sQ + QB, sV = sK + KS * KB;
@@ -371,7 +400,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
         const int s = i % KS;
         if (i >= KS) wait_or_fail(ok, k_empty(s), ((i / KS) - 1) & 1, 50);
         if (!ok) break;
-        const int t0 = i * MA_BN;
+        const int t0 = tbase + i * MA_BN;
         const int y = cache_y(p.page_table, p.page_size, p.max_pages, p.num_pages, p.seq_stride, b, t0);
         const uint32_t st = sK + s * KB;
         mbar_arrive_expect_tx(k_full(s), KB);
@@ -396,7 +425,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
         const uint32_t st = sV + s * VB;
         mbar_arrive_expect_tx(v_full(s), VB);
         for (int j = 0; j < v / 64; ++j)
-          tma_load_3d(st + j * 8192, &tm_kx, v_full(s), n + 64 * j, i * MA_BN, plane);
+          tma_load_3d(st + j * 8192, &tm_kx, v_full(s), n + 64 * j, tbase + i * MA_BN, plane);
         issued = i + 1;
       }
       for (int i = max(issued - VS, 0); i < issued; ++i) mbar_wait(v_full(i % VS), (i / VS) & 1);
@@ -474,7 +503,7 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
     float m_run = -INFINITY, l_run = 0.f;
     for (int i = 0; i < ntiles; ++i) {
       const int sb = i % MA_SBUF;
-      const int t0 = i * MA_BN;
+      const int t0 = tbase + i * MA_BN;
       wait_or_fail(ok, bar(M_SFULL + sb), (i / MA_SBUF) & 1, 54);
       tc_fence_after();
       uint32_t u[MA_CPT];
@@ -568,8 +597,15 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
     for (int g = 0; g < MA_NWG; ++g) l_tot += xrow[g * MA_BM + q];
     const bool live = l0 + q < L;
     const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-    __nv_bfloat16* dst =
-        p.out + (((size_t)b * L + (live ? l0 + q : 0)) * p.H + h) * (size_t)v + opt * wg;
+    // one piece: the output row; several: this piece's O / l and (m, l)
+    const size_t orow = p.splits > 1
+                            ? (((size_t)b * p.splits + sp) * L + (live ? l0 + q : 0)) * p.H + h
+                            : ((size_t)b * L + (live ? l0 + q : 0)) * p.H + h;
+    __nv_bfloat16* dst = (p.splits > 1 ? p.o_part : p.out) + orow * (size_t)v + opt * wg;
+    if (p.splits > 1 && live && wg == 0) {
+      p.ml[orow * 2] = m_run == -INFINITY ? -FLT_MAX : m_run;
+      p.ml[orow * 2 + 1] = l_tot;
+    }
     for (int c = 0; c < opt; c += 32) {
       uint32_t r[32];
       tmem_ld16(tmem + lane_base + opt * wg + c, *(uint32_t(*)[16])(r));
@@ -593,6 +629,47 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// out[b, l, h, :] = sum_s w_s (O_s / l_s)[b, l, h, :] / sum_s w_s with
+// w_s = 2^(m_s - M) l_s over the KV pieces of the materialised attention (M
+// the largest m_s; empty pieces have l_s = 0).  One warp per output row; a
+// lane holds one piece's (m, l) and 8 columns of the sums.
+constexpr int MC_ROWS = 4;  // rows (warps) per CTA
+__global__ void __launch_bounds__(32 * MC_ROWS)
+    mat_combine_sm103(const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ ml,
+                      __nv_bfloat16* __restrict__ out, int rows, int LH, int v, int splits) {
+  pdl_wait();  // the pieces come from the attention
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * MC_ROWS + warp;
+  if (row >= rows) return;
+  const int b = row / LH, r = row - b * LH;
+  float2 e = make_float2(-FLT_MAX, 0.f);
+  if (lane < splits) e = *(const float2*)(ml + (((size_t)b * splits + lane) * LH + r) * 2);
+  float M = e.y > 0.f ? e.x : -FLT_MAX;
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w = e.y > 0.f ? ex2(e.x - M) * e.y : 0.f;
+  float den = w;
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  for (int c = lane * 8; c < v; c += 256) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < splits; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      if (ws == 0.f) continue;  // an empty piece: its row was never written
+      const uint4 x = *(const uint4*)(o_part + (((size_t)b * splits + s) * LH + r) * v + c);
+      const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[2 * k] = fmaf(ws, __uint_as_float(u[k] << 16), acc[2 * k]);
+        acc[2 * k + 1] = fmaf(ws, __uint_as_float(u[k] & 0xffff0000u), acc[2 * k + 1]);
+      }
+    }
+    *(uint4*)(out + (size_t)row * v + c) =
+        make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                   pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
   }
 }
 
@@ -662,8 +739,52 @@ bool fast_materialised_supported(const Plan& p) {
   return e.stages >= 2 && e.smem - kSmemExtra >= EX_BM * cols * 2 && mat_rings(p.n, p.v).ks >= 2;
 }
 
+namespace {
+
+// KV pieces per query tile of the materialised attention: when the (query
+// tile, head, sequence) CTAs leave SMs idle, each is cut into pieces of
+// chunk_tiles KV tiles, choosing the cut that minimises waves x (tiles per
+// piece + the fixed cost of a CTA, about four tiles) with one CTA per SM.
+struct MatSplit {
+  int splits = 1, chunk_tiles = 1;
+};
+MatSplit mat_split(const Plan& p) {
+  const long long units = (long long)((p.L + MA_BM - 1) / MA_BM) * p.H * p.B;
+  const int tiles = (p.Tmax + MA_BN - 1) / MA_BN;
+  const long long slots = device_sm_count();
+  MatSplit best;
+  best.chunk_tiles = tiles;
+  const long long whole = ((units + slots - 1) / slots) * (tiles + 4);
+  long long best_cost = whole;
+  for (int s = 2; s <= 16; ++s) {
+    const int ct = (tiles + s - 1) / s;
+    if (ct < 8) break;
+    const long long cost = ((units * s + slots - 1) / slots) * (ct + 4);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best.chunk_tiles = ct;
+    }
+  }
+  // the pieces' round trip and the combine kernel cost more than the model's
+  // four tiles: cut only for a clear gain (measured: four pieces of the
+  // 512/192/256 L = 1024 call at T = 8192 by the model's 5 % were 8 % slower)
+  if (best_cost * 4 > whole * 3) best.chunk_tiles = tiles;
+  best.splits = (tiles + best.chunk_tiles - 1) / best.chunk_tiles;
+  return best;
+}
+
+size_t align256_bytes(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
 size_t fast_materialised_workspace(const Plan& p) {
-  return (size_t)p.B * p.H * p.Tmax * (p.n + p.v) * 2;
+  size_t bytes = align256_bytes((size_t)p.B * p.H * p.Tmax * (p.n + p.v) * 2);
+  const MatSplit ms = mat_split(p);
+  if (ms.splits > 1) {
+    const size_t rows = (size_t)p.B * ms.splits * p.L * p.H;
+    bytes += align256_bytes(rows * p.v * 2) + align256_bytes(rows * 2 * sizeof(float));
+  }
+  return bytes;
 }
 
 cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
@@ -721,11 +842,17 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
     if (e != cudaSuccess) return e;
   }
   {
+    const MatSplit ms = mat_split(p);
+    char* ws_pieces = a.ws + p.off_exp +
+                      align256_bytes((size_t)p.B * p.H * p.Tmax * (p.n + p.v) * 2);
+    const size_t prow = (size_t)p.B * ms.splits * p.L * p.H;
     MatAttnParams mp{a.lens, c.page_table, c.page_size, c.max_pages, c.num_pages, c.seq_stride,
                      (__nv_bfloat16*)a.out, p.L, p.H, p.n, p.v, mr.ks, mr.vs,
-                     p.scale * 1.4426950408889634f};
+                     p.scale * 1.4426950408889634f, p.B, ms.splits, ms.chunk_tiles,
+                     (__nv_bfloat16*)ws_pieces,
+                     (float*)(ws_pieces + align256_bytes(prow * p.v * 2))};
     KernelTimer kt("mat_attn_sm103", a.stream);
-    const dim3 grid((p.L + MA_BM - 1) / MA_BM, p.H, p.B);
+    const dim3 grid((unsigned)(((p.L + MA_BM - 1) / MA_BM) * p.H * p.B * ms.splits));
     auto go = [&](auto kernel) {
       return launch_pdl(kernel, grid, dim3(MA_THREADS), ma_smem, a.stream, tm_qn, tm_qr, tm_kx,
                         tm_kr, mp);
@@ -737,6 +864,14 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
       default: e = go(mat_attn_sm103<5>); break;
     }
     if (e != cudaSuccess) return e;
+    if (ms.splits > 1) {
+      const int rows = p.B * p.L * p.H;
+      KernelTimer kc("mat_combine_sm103", a.stream);
+      e = launch_pdl(mat_combine_sm103, dim3((rows + MC_ROWS - 1) / MC_ROWS), dim3(32 * MC_ROWS),
+                     0, a.stream, (const __nv_bfloat16*)mp.o_part, (const float*)mp.ml,
+                     (__nv_bfloat16*)a.out, rows, p.L * p.H, p.v, ms.splits);
+      if (e != cudaSuccess) return e;
+    }
   }
   return cudaGetLastError();
 }

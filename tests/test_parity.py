@@ -401,3 +401,27 @@ def test_unembed_merge_chunks(L, lens):
     out, _ = run_gpu(case, "absorbed")
     compare(out[:, rows][:, :, heads], oracle_out(case, heads=heads, rows=rows), torch.bfloat16,
             f"unembed-merge L={L}")
+
+
+# ---------------------------------------------------------------------------
+# Materialised split-KV: when the query tiles leave SMs idle the attention is
+# cut into KV pieces and a combine kernel merges them
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("geom,L,lens", [
+    (Geometry(H=4), 1024, [1024]),              # cold cache: the first query tiles' later pieces see nothing
+    (Geometry(H=8, n=192, v=256), 1, [8192]),   # a single query row per head
+    (Geometry(H=8), 130, [5000, 777]),          # two sequences, ragged
+])
+def test_materialised_split_kv(geom, L, lens):
+    case = make_case(geom, L, lens, seed=L + len(lens))
+    B.mla_kernel_timing_enable(True)
+    try:
+        B.mla_kernel_timing_read(reset=True)
+        out, branch = run_gpu(case, "materialised")
+        ran = set(B.mla_kernel_timing_read(reset=True))
+    finally:
+        B.mla_kernel_timing_enable(False)
+    assert branch == B.BRANCH_MATERIALISED
+    assert ran == TC_MATERIALISED | {"mat_combine_sm103"}, ran
+    compare(out, oracle_out(case), torch.bfloat16, f"split materialised L={L} lens={lens}")
