@@ -50,6 +50,10 @@ def _args():
     ap.add_argument("--no-shapes", "--no-materialised", dest="no_shapes", action="store_true",
                     help="skip the secondary shapes (crossover sweep, batched paged, long "
                          "context, materialised)")
+    ap.add_argument("--shape-groups", default=None,
+                    help="comma-separated names of the secondary shape groups to run (default "
+                         "all: crossover_glm47_T8192, batched_paged, long_context, "
+                         "dsv3_forced_materialised, sparse_dsv3_k2048, indexer_pool_T131072)")
     ap.add_argument("--widths", default=None,
                     help="comma-separated verify widths instead of 1,2,4,8,16 (for profiling "
                          "one width; the line then describes that workload, not the headline)")
@@ -217,7 +221,7 @@ def _shape_list():
     return out
 
 
-def _bench_shapes(B, dev, peaks, reps):
+def _bench_shapes(B, dev, peaks, reps, only=None):
     """Per shape: us per call (CUDA graph of calls over rotating input copies so
     the working set exceeds L2, CUDA events), the call roofline, and each
     kernel's achieved rates (events around each launch, eager calls)."""
@@ -225,6 +229,8 @@ def _bench_shapes(B, dev, peaks, reps):
     from mla_attention_speculative_gb300 import inputs as I
     groups = {}
     for k, sh in enumerate(_shape_list()):
+        if only is not None and sh["group"] not in only:
+            continue
         geom, L, lens, mode, page = sh["geom"], sh["L"], sh["lens"], sh["mode"], sh["page"]
         kk = sh.get("topk", 0)
         layer_bytes = (sum(lens) * (geom.r + geom.rope)
@@ -312,10 +318,68 @@ def _bench_shapes(B, dev, peaks, reps):
             "first_L_materialised_faster": first,
             "us": {str(L): {"absorbed": v["absorbed"], "materialised": v["materialised"]}
                    for L, v in sorted(t.items())}}
+    if only is None or "indexer_pool_T131072" in only:
+        groups["indexer_pool_T131072"] = _bench_indexer(B, dev, peaks, reps)
     return {"groups": groups, "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
             "peak_source": f"of {peaks['source']}",
             "timing": "CUDA graph of one call per input copy, copies rotated until the "
                       "working set exceeds 256 MB (> L2); work counts causal positions only"}
+
+
+def _bench_indexer(B, dev, peaks, reps):
+    """The sparse model's indexer step at a 128K cache: a full pool of the
+    windows of four, the incremental (tail-only) step for S = 1, 4, 8 new
+    tokens, and the top-512-window selection for 8 new tokens.  Device time
+    per launch from events around each launch; six key buffers rotate so a
+    full pool reads its keys from HBM."""
+    import torch
+    T, d, k = 131072, 128, 512
+    W = T // 4
+    copies = 6
+    g = torch.Generator(device=dev).manual_seed(5000)
+    keys = [torch.randn(1, T, d, generator=g, device=dev).to(torch.bfloat16) for _ in range(copies)]
+    pooled = [torch.zeros((1, W, d), device=dev) for _ in range(copies)]
+    q = torch.randn(1, 8, d, generator=g, device=dev)
+    out = {"geometry": f"keys bf16 [1, {T}, {d}], windows of four, k = {k} windows", "calls": []}
+
+    def timed(fn, n):
+        B.mla_kernel_timing_read(reset=True)
+        B.mla_kernel_timing_enable(True)
+        for i in range(n):
+            fn(i)
+        torch.cuda.synchronize()
+        B.mla_kernel_timing_enable(False)
+        return B.mla_kernel_timing_read(reset=True)
+
+    n = max(6, reps)
+    for S in (T, 1, 4, 8):
+        def step(i, S=S):
+            st = B.IndexerPoolState()
+            if S != T:   # a pool that remembers the cache before this step
+                st.length, st.batch, st.dim = T - S, 1, d
+            B.mla_indexer_pool_update(keys[i % copies], T, S, pooled[i % copies], st)
+        step(0)
+        kt = timed(step, n)
+        nl, ms = kt["indexer_pool_windows"]
+        us = ms * 1e3 / nl
+        ent = {"step": "full pool" if S == T else f"incremental, S = {S}", "us": us}
+        if S == T:
+            byts = T * d * 2 + W * d * 4
+            ent.update(gbs=byts / (us * 1e-6) / 1e9, hbm_frac=byts / (us * 1e-6) / 1e9 /
+                       peaks["hbm_gbs"], bound="hbm")
+        out["calls"].append(ent)
+    B.mla_indexer_select(q, pooled[0], T, k)
+    kt = timed(lambda i: B.mla_indexer_select(q, pooled[i % copies], T, k), n)
+    sel = {"step": "select top-512 windows, S = 8"}
+    for name, (nl, ms) in kt.items():
+        sel[name + "_us"] = ms * 1e3 / nl
+    byts = W * d * 4 + 8 * W * 4
+    sel["score_gbs"] = byts / (sel["indexer_score_windows_us"] * 1e-6) / 1e9
+    sel["score_hbm_frac"] = sel["score_gbs"] / peaks["hbm_gbs"]
+    out["calls"].append(sel)
+    del keys, pooled
+    torch.cuda.empty_cache()
+    return out
 
 
 def _source_sha(names):
@@ -729,7 +793,8 @@ def run_ours(args):
 
     shapes = None
     if not args.no_shapes:
-        shapes = _bench_shapes(B, dev, peaks, reps=max(3, min(args.steps, 10)))
+        shapes = _bench_shapes(B, dev, peaks, reps=max(3, min(args.steps, 10)),
+                               only=args.shape_groups.split(",") if args.shape_groups else None)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -16,17 +16,19 @@
 // bit for bit as the same tokens fed one at a time.
 //
 // Three kernels, all bound by memory or latency:
-//   pool_windows   one warp per window: four key rows read once, summed in
-//                  a fixed order, scaled by 1/count, stored as fp32
-//   score_windows  one warp per window: the window's pooled key read once and
-//                  dotted with every new token's query (kept in shared memory)
+//   pool_windows   one warp per window: four key rows read once (as vectors),
+//                  summed in a fixed order, scaled by 1/count, stored as fp32
+//   score_windows  one thread per window: the window's pooled key read once
+//                  and dotted with every new token's query (in shared memory)
 //   select_topk    one CTA per new token: an 8-bit radix select of the k-th
 //                  largest score over the windows the token may see, then the
 //                  chosen windows in ascending order and their positions
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cfloat>
+#include <mutex>
 
 #include "mla_internal.h"
 
@@ -40,8 +42,25 @@ constexpr int kMaxNewTokens = 32;
 __device__ __forceinline__ float ld_f(const float* p) { return *p; }
 __device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
-// pooled[b, w, :] for w in [w0, w1): one warp per window, each lane dim/32
-// columns (strided by 32 so a row is read coalesced).
+// pooled[b, w, :] for w in [w0, w1): one warp per window; lane j owns
+// columns [j * dim/32, (j + 1) * dim/32), read as whole vectors when that run
+// is a multiple of four elements.
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float (&f)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&f)[4]) {
+  const float4 v = *(const float4*)p;
+  f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[4]) {
+  const uint2 v = *(const uint2*)p;
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xffff0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) pool_windows(const T* __restrict__ keys, long long row_stride,
                                                     long long seq_stride, int dim, long long len,
@@ -53,16 +72,42 @@ __global__ void __launch_bounds__(256) pool_windows(const T* __restrict__ keys, 
   if (w >= w1) return;
   const long long t0 = kWindow * w;
   const int cnt = (int)min((long long)kWindow, len - t0);
-  const T* base = keys + (long long)b * seq_stride * row_stride;
+  const T* base = keys + (long long)b * seq_stride * row_stride + t0 * row_stride;
   float* out = pooled + ((long long)b * cap + w) * dim;
-  for (int c = lane; c < dim; c += 32) {
-    float s = ld_f(base + t0 * row_stride + c);
-    for (int i = 1; i < cnt; ++i) s += ld_f(base + (t0 + i) * row_stride + c);
-    out[c] = cnt == kWindow ? s * 0.25f : s / (float)cnt;
+  const int cpl = dim / 32;
+  if (cpl % 4 == 0) {
+    for (int c = lane * cpl; c < (lane + 1) * cpl; c += 4) {
+      float rows[kWindow][4];
+#pragma unroll
+      for (int i = 0; i < kWindow; ++i) {
+        if (i < cnt) load4(base + i * row_stride + c, rows[i]);
+        else rows[i][0] = rows[i][1] = rows[i][2] = rows[i][3] = 0.f;
+      }
+      float ov[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float s = rows[0][e];
+#pragma unroll
+        for (int i = 1; i < kWindow; ++i)
+          if (i < cnt) s += rows[i][e];
+        ov[e] = cnt == kWindow ? s * 0.25f : s / (float)cnt;
+      }
+      *(float4*)(out + c) = make_float4(ov[0], ov[1], ov[2], ov[3]);
+    }
+  } else {
+    for (int c = lane; c < dim; c += 32) {
+      float s = ld_f(base + c);
+      for (int i = 1; i < cnt; ++i) s += ld_f(base + i * row_stride + c);
+      out[c] = cnt == kWindow ? s * 0.25f : s / (float)cnt;
+    }
   }
 }
 
-// scores[b, s, w] = q[b, s, :] . pooled[b, w, :] for w < nwin.
+// scores[b, s, w] = q[b, s, :] . pooled[b, w, :] for w < nwin.  One thread
+// per window: it reads the window's pooled key once, 16 bytes at a time, and
+// dots it with up to eight queries per pass; the queries sit in shared memory
+// and every thread of a warp reads the same query element at once.
+constexpr int kScoreGroup = 8;
 __global__ void __launch_bounds__(256) score_windows(const float* __restrict__ q,
                                                      const float* __restrict__ pooled,
                                                      long long cap, int dim, int S,
@@ -71,22 +116,29 @@ __global__ void __launch_bounds__(256) score_windows(const float* __restrict__ q
   const int b = blockIdx.y;
   for (int i = threadIdx.x; i < S * dim; i += blockDim.x) sq[i] = q[(long long)b * S * dim + i];
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long w = (long long)blockIdx.x * 8 + warp;
+  const long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (w >= nwin) return;
-  const float* pk = pooled + ((long long)b * cap + w) * dim;
-  float kv[kMaxDim / 32];
-  const int per = dim / 32;
+  const float4* pk = (const float4*)(pooled + ((long long)b * cap + w) * dim);
+  for (int s0 = 0; s0 < S; s0 += kScoreGroup) {
+    float acc[kScoreGroup];
 #pragma unroll
-  for (int j = 0; j < kMaxDim / 32; ++j) kv[j] = j < per ? pk[lane + 32 * j] : 0.f;
-  for (int s = 0; s < S; ++s) {
-    float acc = 0.f;
+    for (int j = 0; j < kScoreGroup; ++j) acc[j] = 0.f;
+    for (int c = 0; c < dim / 4; ++c) {
+      const float4 kv = pk[c];
 #pragma unroll
-    for (int j = 0; j < kMaxDim / 32; ++j)
-      if (j < per) acc = fmaf(sq[s * dim + lane + 32 * j], kv[j], acc);
+      for (int j = 0; j < kScoreGroup; ++j) {
+        if (s0 + j < S) {
+          const float4 qv = *(const float4*)(sq + (s0 + j) * dim + 4 * c);
+          acc[j] = fmaf(qv.x, kv.x, acc[j]);
+          acc[j] = fmaf(qv.y, kv.y, acc[j]);
+          acc[j] = fmaf(qv.z, kv.z, acc[j]);
+          acc[j] = fmaf(qv.w, kv.w, acc[j]);
+        }
+      }
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) scores[((long long)b * S + s) * nwin + w] = acc;
+    for (int j = 0; j < kScoreGroup; ++j)
+      if (s0 + j < S) scores[((long long)b * S + s0 + j) * nwin + w] = acc[j];
   }
 }
 
@@ -97,6 +149,9 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kSelThreads = 1024;
+constexpr int kSelPerThread = 4;                       // consecutive windows per thread and round
+constexpr int kSelRound = kSelThreads * kSelPerThread;
+constexpr int kSelSmemWindows = 48 * 1024;            // scores staged in shared memory up to this
 
 // Exclusive prefix sum of one value per thread over the CTA; *total receives the sum.
 __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
@@ -127,10 +182,14 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 
 // Row (b, s): the k best of the windows w <= p/4 (p = len - S + s), ties to
 // the lower window; windows listed ascending, then their positions <= p.
+// The row's scores are staged in shared memory when they fit; the k-th
+// largest is found by an 8-bit radix select over order-preserving keys, and
+// the chosen windows are written in order, 4096 windows per round.
 __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restrict__ scores,
                                                           long long nwin, int S, long long len,
                                                           int k, int32_t* __restrict__ win_out,
                                                           int32_t* __restrict__ pos_out) {
+  extern __shared__ float ssc[];
   __shared__ int hist[256];
   __shared__ int warp_sums[32];
   __shared__ int sel[2];  // chosen digit, remaining count
@@ -138,11 +197,13 @@ __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restri
   const long long p = len - S + s;
   const long long vis = p / kWindow + 1;
   const int keff = (int)min((long long)k, vis);
-  const float* sc = scores + ((long long)b * S + s) * nwin;
   const long long row = (long long)b * S + s;
-  // this thread's contiguous segment of windows
-  const long long seg = (vis + kSelThreads - 1) / kSelThreads;
-  const long long lo = min(vis, (long long)threadIdx.x * seg), hi = min(vis, lo + seg);
+  const float* src = scores + row * nwin;
+  if (vis <= kSelSmemWindows) {
+    for (long long w = threadIdx.x; w < vis; w += kSelThreads) ssc[w] = src[w];
+    __syncthreads();
+    src = ssc;
+  }
 
   uint32_t prefix = 0, mask = 0;
   int remaining = keff;
@@ -150,8 +211,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restri
     const int shift = 24 - 8 * pass;
     for (int i = threadIdx.x; i < 256; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (long long w = lo; w < hi; ++w) {
-      const uint32_t key = order_key(sc[w]);
+    for (long long w = threadIdx.x; w < vis; w += kSelThreads) {
+      const uint32_t key = order_key(src[w]);
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
     }
     __syncthreads();
@@ -171,37 +232,45 @@ __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restri
     __syncthreads();
   }
   // prefix is now the k-th largest key; `remaining` of the windows equal to
-  // it are taken, lowest windows first
-  int gt = 0, eq = 0;
-  for (long long w = lo; w < hi; ++w) {
-    const uint32_t key = order_key(sc[w]);
-    gt += key > prefix;
-    eq += key == prefix;
-  }
-  int total;
-  const int eq_before = block_exclusive_scan(eq, warp_sums, &total);
-  const int eq_take = max(0, min(eq, remaining - eq_before));
-  const int taken = keff > 0 ? gt + eq_take : 0;
-  const int out0 = block_exclusive_scan(taken, warp_sums, &total);
-  int o = out0, eq_seen = 0;
-  if (taken > 0) {
-    for (long long w = lo; w < hi; ++w) {
-      const uint32_t key = order_key(sc[w]);
-      bool take = key > prefix;
-      if (key == prefix) take = eq_seen++ < eq_take;
-      if (!take) continue;
+  // it are taken, lowest windows first.  Rounds of 4096 windows in order.
+  int taken_before = 0, eq_before_round = 0;
+  for (long long r0 = 0; r0 < vis; r0 += kSelRound) {
+    const long long w0 = r0 + (long long)threadIdx.x * kSelPerThread;
+    uint32_t keys[kSelPerThread];
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int e = 0; e < kSelPerThread; ++e) {
+      keys[e] = w0 + e < vis ? order_key(src[w0 + e]) : 0u;
+      gt += w0 + e < vis && keys[e] > prefix;
+      eq += w0 + e < vis && keys[e] == prefix;
+    }
+    int eq_total, take_total;
+    const int eq_rank = eq_before_round + block_exclusive_scan(eq, warp_sums, &eq_total);
+    const int eq_take = max(0, min(eq, remaining - eq_rank));
+    const int take = keff > 0 ? gt + eq_take : 0;
+    int o = taken_before + block_exclusive_scan(take, warp_sums, &take_total);
+    int eq_seen = 0;
+#pragma unroll
+    for (int e = 0; e < kSelPerThread; ++e) {
+      if (w0 + e >= vis || take == 0) continue;
+      bool t = keys[e] > prefix;
+      if (keys[e] == prefix) t = eq_seen++ < eq_take;
+      if (!t) continue;
+      const long long w = w0 + e;
       if (win_out) win_out[row * k + o] = (int32_t)w;
 #pragma unroll
       for (int i = 0; i < kWindow; ++i) {
-        const long long t = kWindow * w + i;
+        const long long tpos = kWindow * w + i;
         pos_out[row * (long long)kWindow * k + (long long)kWindow * o + i] =
-            t <= p ? (int32_t)t : -1;
+            tpos <= p ? (int32_t)tpos : -1;
       }
       ++o;
     }
+    taken_before += take_total;
+    eq_before_round += eq_total;
   }
   // padding past the chosen windows
-  for (int j = total + threadIdx.x; j < k; j += kSelThreads) {
+  for (int j = taken_before + threadIdx.x; j < k; j += kSelThreads) {
     if (win_out) win_out[row * k + j] = -1;
 #pragma unroll
     for (int i = 0; i < kWindow; ++i) pos_out[row * (long long)kWindow * k + kWindow * j + i] = -1;
@@ -329,13 +398,27 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
   float* scores = (float*)workspace;
   {
     KernelTimer kt("indexer_score_windows", st);
-    score_windows<<<dim3((unsigned)((nwin + 7) / 8), batch), 256,
+    score_windows<<<dim3((unsigned)((nwin + 255) / 256), batch), 256,
                     (size_t)new_tokens * dim * sizeof(float), st>>>(
         q, pooled, pooled_windows_cap, dim, new_tokens, nwin, scores);
   }
   {
     KernelTimer kt("indexer_select_topk", st);
-    select_topk<<<dim3(new_tokens, batch), kSelThreads, 0, st>>>(
+    const long long vis_max = (cache_len - 1) / kWindow + 1;
+    const size_t sel_smem = vis_max <= kSelSmemWindows ? (size_t)vis_max * sizeof(float) : 0;
+    if (sel_smem > 48 * 1024) {
+      static std::once_flag once;
+      static cudaError_t attr_err = cudaSuccess;
+      std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kSelSmemWindows * (int)sizeof(float));
+      });
+      if (attr_err != cudaSuccess) {
+        set_error("CUDA error %d (%s)", (int)attr_err, cudaGetErrorString(attr_err));
+        return MLA_ERR_CUDA;
+      }
+    }
+    select_topk<<<dim3(new_tokens, batch), kSelThreads, sel_smem, st>>>(
         scores, nwin, new_tokens, cache_len, k_windows, windows_out, positions_out);
   }
   const cudaError_t e = cudaGetLastError();
