@@ -1146,6 +1146,50 @@ constexpr int UM_SMEM = UM_OFF_BAR + 128 + 1024;
 static_assert(UM_SMEM <= 232448, "shared memory per CTA");
 enum { UB_WFULL = 0, UB_OFULL = 1, UB_DONE = 2, UB_FREE = 4, UB_COUNT = 6 };
 
+// Combine weights of every (chunk, verify row) of a CTA, one thread of warps
+// 1..3 per row, for rows of up to 32 pieces.
+__device__ __forceinline__ void um_weights_many_rows(const UnembedMergeParams& p, float* wts, int h,
+                                                  int g0, int nch, int cps, int Lc, int S) {
+  for (int row = threadIdx.x - 32; row < nch * Lc; row += 96) {
+    const int c = row / Lc, li = row - c * Lc;
+    const int b = (g0 + c) / cps, l = ((g0 + c) % cps) * Lc + li;
+    float* wt = wts + c * 64 + li * S;
+    const int len = p.fixed_len > 0 ? p.fixed_len : p.lens[b];
+    const int nsplit = l < p.L ? min((len + p.chunk - 1) / p.chunk, S) : 0;
+    const float2* mlr = (const float2*)p.ml + (size_t)b * S * p.R +
+                        (size_t)min(l, p.L - 1) * p.H + h;
+    float M = -FLT_MAX;
+    for (int j0 = 0; j0 < nsplit; j0 += 8) {
+      float2 e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        e[j] = j0 + j < nsplit ? mlr[(size_t)(j0 + j) * p.R] : make_float2(-FLT_MAX, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (e[j].y > 0.f) M = fmaxf(M, e[j].x);
+    }
+    float sum = 0.f;
+    for (int j0 = 0; j0 < S; j0 += 8) {
+      float2 e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        e[j] = j0 + j < nsplit ? mlr[(size_t)(j0 + j) * p.R] : make_float2(-FLT_MAX, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = e[j].y > 0.f ? ex2(e[j].x - M) * e[j].y : 0.f;
+        sum += w;
+        if (j0 + j < S) wt[j0 + j] = w;
+      }
+    }
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    for (int j = 0; j < S; ++j) wt[j] *= inv;
+  }
+}
+
+// MANY_ROWS: the instantiation for CTAs with many rows of 9 to 32 pieces
+// (batches of long caches), which computes their weights one thread per row;
+// the other instantiation, without that code, serves everything else.
+template <bool MANY_ROWS>
 __global__ void __launch_bounds__(UM_THREADS, 1)
     unembed_merge_sm103(const __grid_constant__ CUtensorMap tm_wuv,
                         const __grid_constant__ CUtensorMap tm_pieces, UnembedMergeParams p) {
@@ -1251,6 +1295,15 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
         for (int j = 0; j < 8; ++j)
           if (j < S) wt[j] = w[j] * inv;
       }
+    } else if (MANY_ROWS && S <= 32) {
+      // many rows of up to 32 pieces (two passes of S/8 round trips to memory
+      // per row beat the warp-per-row form's rows/3 round trips):
+      // one thread per row, eight pieces' (m, l) loads in flight per batch:
+      // the row maximum first, then the weights (the second read hits L1),
+      // normalised in shared memory.  (The warp-per-row form below walked a
+      // CTA's rows three at a time, one round trip to memory each: 237 us
+      // against 173 for the batched serving call's unembedding.)
+      um_weights_many_rows(p, wts, h, g0, nch, cps, Lc, S);
     } else {
       for (int row = warp - 1; row < nch * Lc; row += 3) {  // (chunk, verify row in it)
         const int c = row / Lc, li = row - c * Lc;
@@ -1411,7 +1464,8 @@ const DeviceSetup& device_setup() {
   cudaError_t e = set_smem(swapab_gemm_sm103, gemm_smem(kLat, 64));
   if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103<false>, ATTN_SMEM);
   if (e == cudaSuccess) e = set_smem(absorbed_attn_sm103<true>, ATTN_SMEM);
-  if (e == cudaSuccess) e = set_smem(unembed_merge_sm103, UM_SMEM);
+  if (e == cudaSuccess) e = set_smem(unembed_merge_sm103<false>, UM_SMEM);
+  if (e == cudaSuccess) e = set_smem(unembed_merge_sm103<true>, UM_SMEM);
   int slots = 0;
   if (e == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
@@ -1554,10 +1608,15 @@ cudaError_t launch_fast_absorbed(const Plan& p, const Args& a) {
                                    (uint64_t)p.H * kLat * 2};
       const uint32_t box[4] = {64, 1, (uint32_t)p.splits, (uint32_t)up.Lc};
       if (!make_tmap_bf16_4d(&tm_pieces, o_part, dims, strides, box)) return cudaErrorInvalidValue;
+      // rows of 9 to 32 pieces, many per CTA: two passes of S/8 round trips to
+      // memory per row (one thread each) beat one round trip per three rows
+      const long long rows_per_cta = cpc * up.Lc;
+      const bool many_rows = p.splits > 8 && p.splits <= 32 &&
+                             2 * ((p.splits + 7) / 8) < (rows_per_cta + 2) / 3;
       KernelTimer kt("unembed_merge_sm103", a.stream);
-      e = launch_pdl(unembed_merge_sm103, dim3(units, (unsigned)((total + cpc - 1) / cpc)),
-                     dim3(UM_THREADS),
-                     UM_SMEM, a.stream, tm_wuv, tm_pieces, up);
+      e = launch_pdl(many_rows ? unembed_merge_sm103<true> : unembed_merge_sm103<false>,
+                     dim3(units, (unsigned)((total + cpc - 1) / cpc)), dim3(UM_THREADS), UM_SMEM,
+                     a.stream, tm_wuv, tm_pieces, up);
       if (e != cudaSuccess) return e;
       return cudaGetLastError();
     }
