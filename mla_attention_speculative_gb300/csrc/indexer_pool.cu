@@ -297,9 +297,9 @@ extern "C" mla_status_t mla_indexer_pool_update(const void* keys, int32_t dtype,
     set_error("unknown dtype %d", dtype);
     return MLA_ERR_INVALID_ARG;
   }
-  if (batch < 1 || dim < 32 || dim > kMaxDim || dim % 32 != 0) {
-    set_error("batch %d must be >= 1 and dim %d a multiple of 32 in [32, %d]", batch, dim,
-              kMaxDim);
+  if (batch < 1 || batch > 65535 || dim < 32 || dim > kMaxDim || dim % 32 != 0) {
+    set_error("batch %d must be in [1, 65535] and dim %d a multiple of 32 in [32, %d]", batch,
+              dim, kMaxDim);
     return MLA_ERR_INVALID_ARG;
   }
   if (new_tokens < 1 || cache_len < new_tokens) {
@@ -370,7 +370,8 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
     set_error("q, pooled and positions_out must not be NULL");
     return MLA_ERR_INVALID_ARG;
   }
-  if (batch < 1 || dim < 32 || dim > kMaxDim || dim % 32 != 0 || new_tokens < 1 ||
+  if (batch < 1 || batch > 65535 || dim < 32 || dim > kMaxDim || dim % 32 != 0 ||
+      new_tokens < 1 ||
       new_tokens > kMaxNewTokens || cache_len < new_tokens || k_windows < 1) {
     set_error("bad arguments (batch %d, dim %d, new_tokens %d (<= %d), cache_len %lld, k %d)",
               batch, dim, new_tokens, kMaxNewTokens, (long long)cache_len, k_windows);

@@ -111,7 +111,10 @@ static bool geometry_ok(const mla_geometry_t* g) {
 }
 
 static bool lens_ok(const int32_t* lens, int32_t batch, int32_t L) {
-  if (batch < 1) { set_error("batch %d < 1", batch); return false; }
+  if (batch < 1 || batch > 65535) {
+    set_error("batch %d outside [1, 65535]", batch);  // (a grid dimension)
+    return false;
+  }
   if (L < 1) { set_error("L %d < 1", L); return false; }
   if (lens == nullptr) { set_error("cache_lens_host is NULL"); return false; }
   for (int32_t b = 0; b < batch; ++b) {

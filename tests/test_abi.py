@@ -240,3 +240,25 @@ def test_sparse_workspace_follows_the_list_length():
     large = B.mla_sparse_workspace_bytes(g, 1, [32768], 2048)
     dense = B.mla_workspace_bytes(g, 1, [32768], "absorbed")
     assert 0 < small <= large <= dense
+
+
+def test_batch_beyond_grid_limit_is_rejected():
+    lens = [64] * 65536
+    with pytest.raises(B.MlaError) as e:
+        B.mla_workspace_bytes(_geom(), 1, lens)
+    assert e.value.status == B.MLA_ERR_INVALID_ARG
+    assert "65535" in str(e.value)
+
+
+@pytest.mark.parametrize("kw", [dict(dim=48), dict(dim=1024), dict(new_tokens=0),
+                                dict(cache_len=3, new_tokens=4), dict(cap=10)])
+def test_indexer_pool_update_rejects_bad_arguments(kw):
+    args = dict(dim=128, cache_len=100, new_tokens=4, cap=25)
+    args.update(kw)
+    st = B.IndexerPoolState()
+    lib = B.lib()
+    status = lib.mla_indexer_pool_update(0x10000, 0, args["dim"], 1 << 20, 1, args["dim"],
+                                         args["cache_len"], args["new_tokens"], 0, 0x20000,
+                                         args["cap"], ctypes.byref(st), None, None)
+    assert status == B.MLA_ERR_INVALID_ARG
+    assert st.length == -1          # the state is untouched by a rejected call
