@@ -485,6 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       if (lane == 0) mbar_wait(bar(B_QFULL), 0);
     }
     cluster_wait();  // (this role never touches the peer)
+    cluster_arrive();  // done with the peer: the exit barrier's arrival
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
@@ -547,6 +548,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         mbar_wait(bar(B_KVFULL + i % STAGES), (i / STAGES) & 1);
     }
     cluster_wait();  // (this role never touches the peer)
+    cluster_arrive();  // done with the peer: the exit barrier's arrival
   } else if (warp == 1) {
     // ------------------------------------------------------- score-MMA issuer
     // S(i) = Q . K(i)^T over this CTA's 256 latent (Q from TMEM) + 32 RoPE
@@ -586,6 +588,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_wait(bar(B_DRAIN), 0);
     }
     cluster_wait();
+    cluster_arrive();
   } else if (warp == 2) {
     // --------------------------------------------------------- P.V issuer
     // O += P(j) . V(j) over this CTA's 256 latent columns of the KV tile; the
@@ -612,6 +615,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       mbar_wait(bar(B_DRAIN + 1), 0);
     }
     cluster_wait();
+    cluster_arrive();
   } else if (warp >= XCHG_WARP0) {
     // ------------------------------------------------------- score exchange
     // One warp per TMEM lane quarter ships this CTA's partial scores of each
@@ -672,6 +676,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       }
       if (lane == 0) bulk_wait_read();
     }
+    // every copy this warp sent has been read out of its staging block; the
+    // peer waits for their landing itself
+    __syncwarp();
+    cluster_arrive();
   } else {
     // ------------------------------------------------- softmax warpgroups
     // NWG warpgroups: thread (wg, q) owns row q, score columns CPT*wg.. and O
@@ -847,6 +855,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
     if (sm_tid == 0)
       for (int j = received; j < armed; ++j)
         mbar_wait_cluster(bar(B_XFULL + (j & 1)), (j >> 1) & 1);
+    // the last remote arrive of this warpgroup is done: the exit barrier's
+    // arrival (the epilogue below touches only this CTA)
+    __syncwarp();
+    cluster_arrive();
     // ---------------------------------------------------------------- epilogue
     if (ntiles > 0) wait_or_fail(ok, bar(B_ODONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 25);
     pdl_wait();  // the partials may still be read by the previous call's merge
@@ -911,7 +923,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 512);
-  cluster_sync();  // no peer access may outlive this CTA
+  // no peer access may outlive this CTA: every thread of both CTAs arrived
+  // once its accesses to the peer were done
+  cluster_wait();
 }
 
 // =========================================================================
