@@ -53,7 +53,8 @@ def _args():
     ap.add_argument("--shape-groups", default=None,
                     help="comma-separated names of the secondary shape groups to run (default "
                          "all: crossover_glm47_T8192, batched_paged, long_context, "
-                         "dsv3_forced_materialised, sparse_dsv3_k2048, indexer_pool_T131072)")
+                         "dsv3_forced_materialised, sparse_dsv3_k2048, indexer_pool_T131072, "
+                         "conv_snapshots_H8192)")
     ap.add_argument("--widths", default=None,
                     help="comma-separated verify widths instead of 1,2,4,8,16 (for profiling "
                          "one width; the line then describes that workload, not the headline)")
@@ -320,6 +321,8 @@ def _bench_shapes(B, dev, peaks, reps, only=None):
                    for L, v in sorted(t.items())}}
     if only is None or "indexer_pool_T131072" in only:
         groups["indexer_pool_T131072"] = _bench_indexer(B, dev, peaks, reps)
+    if only is None or "conv_snapshots_H8192" in only:
+        groups["conv_snapshots_H8192"] = _bench_snapshots(B, dev, peaks, reps)
     return {"groups": groups, "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
             "peak_source": f"of {peaks['source']}",
             "timing": "CUDA graph of one call per input copy, copies rotated until the "
@@ -378,6 +381,68 @@ def _bench_indexer(B, dev, peaks, reps):
     sel["score_hbm_frac"] = sel["score_gbs"] / peaks["hbm_gbs"]
     out["calls"].append(sel)
     del keys, pooled
+    torch.cuda.empty_cache()
+    return out
+
+
+def _bench_snapshots(B, dev, peaks, reps):
+    """The rollback state's convolution snapshots: S (s = 3 state words per
+    channel) concatenated with T (n = 5 new activations, channel-fastest) into
+    X, and k = 3 snapshot windows of s words written from the row, for
+    H = 8192 channels and Q = 1 or 64 sequences.  The fused kernel (one load
+    per row) against the ordinary path (the concatenation, then one copy per
+    window that reads X back), forced by giving the three windows one
+    destination.  Device time per call from a CUDA graph of back-to-back
+    calls (launch gaps inside the call included, host time not); four input
+    copies rotate so Q = 64 reads from HBM."""
+    import torch
+    s_, n_, k_, H = 3, 5, 3, 8192
+    out = {"geometry": f"s = {s_}, n = {n_}, k = {k_} windows of s, H = {H}, 32-bit words, "
+                       "S and X [Q][H][s(+n)], T [Q][n][H]", "calls": []}
+    g = torch.Generator(device=dev).manual_seed(5100)
+    for Q in (1, 64):
+        copies = 4 if Q > 1 else 1
+        rows = H * Q
+        ss, ts, xs = (1, s_, H * s_), (H, 1, H * n_), (1, s_ + n_, H * (s_ + n_))
+
+        def words(nw):
+            return torch.randint(-2**31, 2**31 - 1, (nw,), generator=g, device=dev,
+                                 dtype=torch.int32)
+        bufs = [dict(S=words(rows * s_), T=words(rows * n_), X=words(rows * (s_ + n_)),
+                     C=words(k_ * rows * s_)) for _ in range(copies)]
+        fused_w = [(n_ - k_ + 1 + j, j * rows * s_, H * s_) for j in range(k_)]
+        same_w = [(n_ - k_ + 1 + j, 0, H * s_) for j in range(k_)]
+        ent = {"Q": Q}
+        for name, wins in (("fused", fused_w), ("separate", same_w)):
+            def call(i, wins=wins):
+                b = bufs[i % copies]
+                return B.mla_concat_snapshots(b["S"], ss, b["T"], ts, b["X"], xs, s_, n_, H, Q,
+                                              b["C"], wins)
+            ran_fused = call(0)
+            assert ran_fused == (name == "fused")
+            n = 4 * copies if Q > 1 else 16
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(n):
+                    call(i)
+            graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            per = []
+            for _ in range(max(5, reps)):
+                e0.record()
+                graph.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                per.append(e0.elapsed_time(e1) * 1e3 / n)
+            us = sorted(per)[len(per) // 2]
+            words_moved = rows * ((s_ + n_) * 2 + k_ * s_ * (2 if name == "separate" else 1))
+            ent[name] = {"us_per_call": us, "dispatches": 1 if name == "fused" else 1 + k_,
+                         "bytes": 4 * words_moved,
+                         "hbm_frac": 4 * words_moved / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+            del graph
+        out["calls"].append(ent)
+        del bufs
     torch.cuda.empty_cache()
     return out
 

@@ -18,11 +18,13 @@
 // Three kernels, all bound by memory or latency:
 //   pool_windows   one warp per window: four key rows read once (as vectors),
 //                  summed in a fixed order, scaled by 1/count, stored as fp32
-//   score_windows  one thread per window: the window's pooled key read once
-//                  and dotted with every new token's query (in shared memory)
-//   select_topk    one CTA per new token: an 8-bit radix select of the k-th
-//                  largest score over the windows the token may see, then the
-//                  chosen windows in ascending order and their positions
+//   score_windows  each window's pooled key read once, whole 512-byte rows
+//                  per warp load at dim 128, and dotted with every new
+//                  token's query; partial sums folded by a reduce-scatter
+//   select_topk    one CTA per new token: a radix select (12, 10, 10-bit
+//                  digits) of the k-th largest score over the windows the
+//                  token may see, then the chosen windows in ascending order
+//                  and their positions
 
 #include <cuda_bf16.h>
 
@@ -31,8 +33,10 @@
 #include <mutex>
 
 #include "mla_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace mla {
+using namespace sm103;
 namespace {
 
 constexpr int kWindow = 4;
@@ -43,8 +47,8 @@ __device__ __forceinline__ float ld_f(const float* p) { return *p; }
 __device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
 // pooled[b, w, :] for w in [w0, w1): one warp per window; lane j owns
-// columns [j * dim/32, (j + 1) * dim/32), read as whole vectors when that run
-// is a multiple of four elements.
+// columns [j * dim/32, (j + 1) * dim/32), read as whole vectors (vec) when
+// that run is a multiple of four elements and the rows are aligned for it.
 template <typename T>
 __device__ __forceinline__ void load4(const T* p, float (&f)[4]);
 template <>
@@ -65,7 +69,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) pool_windows(const T* __restrict__ keys, long long row_stride,
                                                     long long seq_stride, int dim, long long len,
                                                     long long w0, long long w1,
-                                                    float* __restrict__ pooled, long long cap) {
+                                                    float* __restrict__ pooled, long long cap,
+                                                    bool vec) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long w = w0 + (long long)blockIdx.x * 8 + warp;
   const int b = blockIdx.y;
@@ -75,7 +80,7 @@ __global__ void __launch_bounds__(256) pool_windows(const T* __restrict__ keys, 
   const T* base = keys + (long long)b * seq_stride * row_stride + t0 * row_stride;
   float* out = pooled + ((long long)b * cap + w) * dim;
   const int cpl = dim / 32;
-  if (cpl % 4 == 0) {
+  if (vec) {
     for (int c = lane * cpl; c < (lane + 1) * cpl; c += 4) {
       float rows[kWindow][4];
 #pragma unroll
@@ -103,42 +108,163 @@ __global__ void __launch_bounds__(256) pool_windows(const T* __restrict__ keys, 
   }
 }
 
-// scores[b, s, w] = q[b, s, :] . pooled[b, w, :] for w < nwin.  One thread
-// per window: it reads the window's pooled key once, 16 bytes at a time, and
-// dots it with up to eight queries per pass; the queries sit in shared memory
-// and every thread of a warp reads the same query element at once.
-constexpr int kScoreGroup = 8;
-__global__ void __launch_bounds__(256) score_windows(const float* __restrict__ q,
-                                                     const float* __restrict__ pooled,
-                                                     long long cap, int dim, int S,
-                                                     long long nwin, float* __restrict__ scores) {
-  extern __shared__ float sq[];  // [S][dim]
+// scores[b, s, w] = q[b, s, :] . pooled[b, w, :] for w < nwin.
+//
+// dim = 128 (score_windows_d128): a CTA per 64 windows.  One bulk copy (TMA,
+// completing on an mbarrier) brings the 64 pooled keys (32 KB, contiguous)
+// into shared memory, so every CTA's whole tile is requested at once; the
+// queries are read meanwhile, lane l holding the 16-byte piece l of each of
+// eight queries in registers.  Each warp then takes 16 windows, four at a
+// time: lane l reads piece l of each window (a warp reads a window's 512 bytes
+// in one instruction), which gives it 4 x 8 partial sums; a reduce-scatter
+// over the 32 lanes (exchanges at distance 16, 8, 4, 2, 1, each halving the
+// values a lane carries) leaves lane l with the whole score of window
+// (l >> 3) & 3 of the four and query l & 7 of the group.
+//
+// Other dims (score_windows): eight lanes per window, lane g holding the
+// 16-byte pieces g, g + 8, ... of the key; the queries are staged in shared
+// memory, and the eight partial sums are folded the same way over eight lanes.
+constexpr int kD128WarpWindows = 16;
+constexpr int kD128Threads = 128;
+constexpr int kD128CtaWindows = (kD128Threads / 32) * kD128WarpWindows;
+constexpr int kScoreThreads = 256;
+constexpr int kIndexerWaitSite = 70;
+
+__device__ int g_indexer_status = 0;
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kD128Threads) score_windows_d128(
+    const float* __restrict__ q, const float* __restrict__ pooled, long long cap, int S,
+    long long nwin, float* __restrict__ scores) {
+  extern __shared__ float4 tile[];  // [kD128CtaWindows][32]
+  __shared__ __align__(8) uint64_t full;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
-  for (int i = threadIdx.x; i < S * dim; i += blockDim.x) sq[i] = q[(long long)b * S * dim + i];
+  const long long c0 = (long long)blockIdx.x * kD128CtaWindows;
+  const int nw = (int)min((long long)kD128CtaWindows, nwin - c0);
+  const uint32_t bar = smem_u32(&full);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, (uint32_t)nw * 512u);
+    bulk_load(smem_u32(tile), pooled + ((long long)b * cap + c0) * 128, (uint32_t)nw * 512u, bar);
+  }
+  __syncthreads();  // the barrier is initialised before anyone waits on it
+  const float4* qb = (const float4*)(q + (long long)b * S * 128) + lane;
+  float4 qv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) qv[j] = j < S ? __ldg(qb + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!mbar_wait(bar, 0)) {
+    // the copy is still owed: record it, give it one more bounded wait, leave
+    if (threadIdx.x == 0) atomicCAS(&g_indexer_status, 0, kIndexerWaitSite);
+    mbar_wait(bar, 0);
+    return;
+  }
+  const int wl0 = warp * kD128WarpWindows;  // this warp's first window in the tile
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        qv[j] = s0 + j < S ? __ldg(qb + 32 * (s0 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int c = 0; c < kD128WarpWindows; c += 4) {
+      if (wl0 + c >= nw) break;  // warp-uniform
+      float a[32];  // a[i * 8 + j]: window wl0 + c + i, query s0 + j
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 kv = tile[(wl0 + c + i) * 32 + lane];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float t = kv.x * qv[j].x;
+          t = fmaf(kv.y, qv[j].y, t);
+          t = fmaf(kv.z, qv[j].z, t);
+          t = fmaf(kv.w, qv[j].w, t);
+          a[i * 8 + j] = t;
+        }
+      }
+#pragma unroll
+      for (int d = 16, n = 32; d >= 1; d >>= 1, n >>= 1) {
+        const bool hi = lane & d;
+#pragma unroll
+        for (int t = 0; t < n / 2; ++t) {
+          const float send = hi ? a[t] : a[t + n / 2];
+          a[t] = (hi ? a[t + n / 2] : a[t]) + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+      }
+      const int wl = wl0 + c + ((lane >> 3) & 3);
+      const int j = lane & 7;
+      if (wl < nw && s0 + j < S) scores[((long long)b * S + s0 + j) * nwin + c0 + wl] = a[0];
+    }
+  }
+}
+
+constexpr int kScoreLanes = 8;
+constexpr int kScoreWinPerCta = kScoreThreads / kScoreLanes;
+constexpr int kScoreMaxVec = kMaxDim / (4 * kScoreLanes);
+
+__global__ void __launch_bounds__(kScoreThreads) score_windows(const float* __restrict__ q,
+                                                               const float* __restrict__ pooled,
+                                                               long long cap, int dim, int S,
+                                                               long long nwin,
+                                                               float* __restrict__ scores) {
+  extern __shared__ float4 sq4[];  // [S][dim / 4]
+  const int b = blockIdx.y;
+  const int g = threadIdx.x & (kScoreLanes - 1);
+  const long long w = (long long)blockIdx.x * kScoreWinPerCta + (threadIdx.x / kScoreLanes);
+  const int nv = dim / (4 * kScoreLanes);
+  const bool live = w < nwin;
+  // the key first: its loads are in flight while the queries are staged
+  const float4* pk = (const float4*)(pooled + ((long long)b * cap + (live ? w : 0)) * dim) + g;
+  float4 kv[kScoreMaxVec];
+#pragma unroll
+  for (int i = 0; i < kScoreMaxVec; ++i)
+    kv[i] = (live && i < nv) ? __ldg(pk + kScoreLanes * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int d4 = dim / 4;
+  const float4* qb = (const float4*)(q + (long long)b * S * dim);
+  for (int i = threadIdx.x; i < S * d4; i += kScoreThreads) sq4[i] = qb[i];
   __syncthreads();
-  const long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (w >= nwin) return;
-  const float4* pk = (const float4*)(pooled + ((long long)b * cap + w) * dim);
-  for (int s0 = 0; s0 < S; s0 += kScoreGroup) {
-    float acc[kScoreGroup];
+  const bool h4 = g & 4, h2 = g & 2, h1 = g & 1;
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float acc[8];
 #pragma unroll
-    for (int j = 0; j < kScoreGroup; ++j) acc[j] = 0.f;
-    for (int c = 0; c < dim / 4; ++c) {
-      const float4 kv = pk[c];
+    for (int j = 0; j < 8; ++j) {
+      acc[j] = 0.f;
+      if (s0 + j < S) {
+        const float4* qs = sq4 + (s0 + j) * d4 + g;
 #pragma unroll
-      for (int j = 0; j < kScoreGroup; ++j) {
-        if (s0 + j < S) {
-          const float4 qv = *(const float4*)(sq + (s0 + j) * dim + 4 * c);
-          acc[j] = fmaf(qv.x, kv.x, acc[j]);
-          acc[j] = fmaf(qv.y, kv.y, acc[j]);
-          acc[j] = fmaf(qv.z, kv.z, acc[j]);
-          acc[j] = fmaf(qv.w, kv.w, acc[j]);
+        for (int i = 0; i < kScoreMaxVec; ++i) {
+          if (i < nv) {
+            const float4 qv = qs[kScoreLanes * i];
+            acc[j] = fmaf(qv.x, kv[i].x, acc[j]);
+            acc[j] = fmaf(qv.y, kv[i].y, acc[j]);
+            acc[j] = fmaf(qv.z, kv[i].z, acc[j]);
+            acc[j] = fmaf(qv.w, kv[i].w, acc[j]);
+          }
         }
       }
     }
+    float r4[4], r2[2];
 #pragma unroll
-    for (int j = 0; j < kScoreGroup; ++j)
-      if (s0 + j < S) scores[((long long)b * S + s0 + j) * nwin + w] = acc[j];
+    for (int t = 0; t < 4; ++t) {
+      const float send = h4 ? acc[t] : acc[t + 4];
+      r4[t] = (h4 ? acc[t + 4] : acc[t]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const float send = h2 ? r4[t] : r4[t + 2];
+      r2[t] = (h2 ? r4[t + 2] : r4[t]) + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const float send = h1 ? r2[0] : r2[1];
+    const float sc = (h1 ? r2[1] : r2[0]) + __shfl_xor_sync(0xffffffffu, send, 1);
+    if (live && s0 + g < S) scores[((long long)b * S + s0 + g) * nwin + w] = sc;
   }
 }
 
@@ -149,125 +275,309 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kSelThreads = 1024;
-constexpr int kSelPerThread = 4;                       // consecutive windows per thread and round
-constexpr int kSelRound = kSelThreads * kSelPerThread;
-constexpr int kSelSmemWindows = 48 * 1024;            // scores staged in shared memory up to this
+constexpr int kSelRun = 32;                        // consecutive windows per thread and round
+constexpr int kSelRound = kSelThreads * kSelRun;
+constexpr int kSelSmemWindows = 48 * 1024;        // scores staged in shared memory up to this
+constexpr int kSelTopBits = 12;                    // first digit: sign, exponent, 3 mantissa bits
+constexpr int kSelLowBits = 10;                    // second and third digits
+constexpr int kSelCand = 2048;                     // first-digit bucket kept as a list up to this
 
 // Exclusive prefix sum of one value per thread over the CTA; *total receives the sum.
-__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+__device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int t = warp_sums[lane];
+    uint32_t t = warp_sums[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      const uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
       if (lane >= o) t += y;
     }
     warp_sums[lane] = t;  // inclusive over warps
   }
   __syncthreads();
-  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  const uint32_t before = (warp > 0 ? warp_sums[warp - 1] : 0u) + x - v;
   *total = warp_sums[31];
   __syncthreads();
   return before;
 }
 
+// The bin holding the `remaining`-th largest key of an nbins-bin histogram,
+// counting from the top bin down.  Thread t brings the counts c[0..per) of
+// the per = nbins/1024 bins top - 0, ..., top - (per - 1), top = nbins - 1 -
+// t * per; one CTA-wide scan of their sums finds the thread whose run crosses
+// `remaining`.  Every thread then reads out[0] = that bin, out[1] = how many
+// of its keys are still to take, out[1] <= out[2] = its count.
+__device__ void find_bucket_counts(const int (&c)[4], int per, int nbins, int remaining,
+                                   uint32_t* warp_sums, int* out) {
+  const int top = nbins - 1 - (int)threadIdx.x * per;
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sum += i < per ? c[i] : 0;
+  uint32_t total;
+  const int excl = (int)block_exclusive_scan((uint32_t)sum, warp_sums, &total);
+  if (excl < remaining && excl + sum >= remaining) {
+    int cum = excl, pick = 0, cnt = 0;
+    bool found = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // constant indices keep c[] in registers
+      if (!found && i < per && cum + c[i] >= remaining) {
+        found = true;
+        pick = i;
+        cnt = c[i];
+      } else if (!found) {
+        cum += i < per ? c[i] : 0;
+      }
+    }
+    out[0] = top - pick;
+    out[1] = remaining - cum;
+    out[2] = cnt;
+  }
+  __syncthreads();
+}
+
+// The same over a histogram in this CTA's shared memory.
+__device__ void find_bucket(const int* hist, int nbins, int remaining, uint32_t* warp_sums,
+                            int* out) {
+  const int per = nbins / kSelThreads;  // 1 or 4
+  const int top = nbins - 1 - (int)threadIdx.x * per;
+  int c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = i < per ? hist[top - i] : 0;
+  find_bucket_counts(c, per, nbins, remaining, warp_sums, out);
+}
+
+// Appends up to four keys per lane to the candidate list: one shared atomic
+// per warp, each lane's keys placed after those of the lanes below it.
+__device__ __forceinline__ void append_keys(const uint32_t (&key)[4], const bool (&in)[4],
+                                            uint32_t* cand, int* ncand) {
+  const int lane = threadIdx.x & 31;
+  const int c = (int)in[0] + (int)in[1] + (int)in[2] + (int)in[3];
+  if (!__any_sync(0xffffffffu, c > 0)) return;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int base = 0;
+  if (lane == 31) base = atomicAdd(ncand, incl);
+  base = __shfl_sync(0xffffffffu, base, 31) + incl - c;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (in[e]) cand[base++] = key[e];
+}
+
 // Row (b, s): the k best of the windows w <= p/4 (p = len - S + s), ties to
 // the lower window; windows listed ascending, then their positions <= p.
-// The row's scores are staged in shared memory when they fit; the k-th
-// largest is found by an 8-bit radix select over order-preserving keys, and
-// the chosen windows are written in order, 4096 windows per round.
+// The row's scores are staged in shared memory when they fit (and then read
+// four at a time).  The k-th largest is found by a radix select over
+// order-preserving keys with digits of 12, 10 and 10 bits.  The first digit
+// (sign, exponent and three mantissa bits) spreads the keys over enough bins
+// that the shared atomics of one warp seldom collide.  The second pass
+// histograms only the keys of the chosen first-digit bucket and, when that
+// bucket holds at most 2048 keys, keeps them as a list, so the third pass
+// reads the list instead of the row.  Once a chosen bucket is taken whole the
+// later digits do not matter and the passes stop.  The output pass gives each
+// thread 32 consecutive windows: it marks the keys above and at the
+// threshold in two bit masks, one CTA-wide scan of both counts places its
+// windows, and it writes them in ascending order.
 __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restrict__ scores,
                                                           long long nwin, int S, long long len,
                                                           int k, int32_t* __restrict__ win_out,
                                                           int32_t* __restrict__ pos_out) {
-  extern __shared__ float ssc[];
-  __shared__ int hist[256];
-  __shared__ int warp_sums[32];
-  __shared__ int sel[2];  // chosen digit, remaining count
+  extern __shared__ float4 ssc4[];
+  __shared__ int hist[1 << kSelTopBits];
+  __shared__ uint32_t cand[kSelCand];
+  __shared__ uint32_t warp_sums[32];
+  __shared__ int sel[3];
+  __shared__ int ncand;
+  const int lane = threadIdx.x & 31;
   const int b = blockIdx.y, s = blockIdx.x;
   const long long p = len - S + s;
-  const long long vis = p / kWindow + 1;
-  const int keff = (int)min((long long)k, vis);
+  const int vis = (int)(p / kWindow + 1);  // the host keeps windows below 2^31
+  const int keff = min(k, vis);
   const long long row = (long long)b * S + s;
   const float* src = scores + row * nwin;
-  if (vis <= kSelSmemWindows) {
-    for (long long w = threadIdx.x; w < vis; w += kSelThreads) ssc[w] = src[w];
+  const bool staged = vis <= kSelSmemWindows;
+  if (staged) {
+    float* ssc = (float*)ssc4;
+    int w = threadIdx.x;
+    if (((uintptr_t)src & 15) == 0) {
+      const float4* s4 = (const float4*)src;
+#pragma unroll 4
+      for (int i = threadIdx.x; i < vis / 4; i += kSelThreads) ssc4[i] = s4[i];
+      w = (vis / 4) * 4 + threadIdx.x;
+    }
+#pragma unroll 8
+    for (; w < vis; w += kSelThreads) ssc[w] = src[w];
     __syncthreads();
     src = ssc;
   }
+  // staged rows are read as float4 up to n4, the rest one key at a time
+  const int n4 = staged ? vis / 4 : 0;
+  const int tail = 4 * n4;
 
-  uint32_t prefix = 0, mask = 0;
-  int remaining = keff;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < 256; i += kSelThreads) hist[i] = 0;
-    __syncthreads();
-    for (long long w = threadIdx.x; w < vis; w += kSelThreads) {
-      const uint32_t key = order_key(src[w]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int cum = 0, d = 255;
-      for (; d > 0; --d) {
-        if (cum + hist[d] >= remaining) break;
-        cum += hist[d];
-      }
-      sel[0] = d;
-      sel[1] = remaining - cum;
-    }
-    __syncthreads();
-    prefix |= (uint32_t)sel[0] << shift;
-    mask |= 255u << shift;
-    remaining = sel[1];
-    __syncthreads();
+  // first digit: bits 31..20 of every key
+  for (int i = threadIdx.x; i < (1 << kSelTopBits); i += kSelThreads) hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n4; i += kSelThreads) {
+    const float4 v = ssc4[i];
+    atomicAdd(&hist[order_key(v.x) >> (32 - kSelTopBits)], 1);
+    atomicAdd(&hist[order_key(v.y) >> (32 - kSelTopBits)], 1);
+    atomicAdd(&hist[order_key(v.z) >> (32 - kSelTopBits)], 1);
+    atomicAdd(&hist[order_key(v.w) >> (32 - kSelTopBits)], 1);
   }
-  // prefix is now the k-th largest key; `remaining` of the windows equal to
-  // it are taken, lowest windows first.  Rounds of 4096 windows in order.
-  int taken_before = 0, eq_before_round = 0;
-  for (long long r0 = 0; r0 < vis; r0 += kSelRound) {
-    const long long w0 = r0 + (long long)threadIdx.x * kSelPerThread;
-    uint32_t keys[kSelPerThread];
-    int gt = 0, eq = 0;
+  for (int w = tail + threadIdx.x; w < vis; w += kSelThreads)
+    atomicAdd(&hist[order_key(src[w]) >> (32 - kSelTopBits)], 1);
+  __syncthreads();
+  find_bucket(hist, 1 << kSelTopBits, keff, warp_sums, sel);
+  constexpr int kShift2 = 32 - kSelTopBits - kSelLowBits;
+  constexpr uint32_t kLowMask = (1u << kSelLowBits) - 1;
+  uint32_t prefix = (uint32_t)sel[0] << (32 - kSelTopBits);
+  uint32_t mask = ~0u << (32 - kSelTopBits);
+  int remaining = sel[1];
+  bool whole = sel[2] == remaining;
+  const bool use_list = sel[2] <= kSelCand;
+
+  // second digit: bits 19..10 of the keys in the chosen bucket
+  if (!whole) {
+    hist[threadIdx.x] = 0;  // 1024 bins, one per thread
+    if (threadIdx.x == 0) ncand = 0;
+    __syncthreads();
+    // warp-uniform loops, so that a warp appends its keys together
+    for (int i0 = threadIdx.x - lane; i0 < n4; i0 += kSelThreads) {
+      const int i = i0 + lane;
+      uint32_t key[4] = {0u, 0u, 0u, 0u};
+      bool in[4] = {false, false, false, false};
+      if (i < n4) {
+        const float4 v = ssc4[i];
+        key[0] = order_key(v.x);
+        key[1] = order_key(v.y);
+        key[2] = order_key(v.z);
+        key[3] = order_key(v.w);
 #pragma unroll
-    for (int e = 0; e < kSelPerThread; ++e) {
-      keys[e] = w0 + e < vis ? order_key(src[w0 + e]) : 0u;
-      gt += w0 + e < vis && keys[e] > prefix;
-      eq += w0 + e < vis && keys[e] == prefix;
+        for (int e = 0; e < 4; ++e) {
+          in[e] = (key[e] & mask) == prefix;
+          if (in[e]) atomicAdd(&hist[(key[e] >> kShift2) & kLowMask], 1);
+        }
+      }
+      if (use_list) append_keys(key, in, cand, &ncand);
     }
-    int eq_total, take_total;
-    const int eq_rank = eq_before_round + block_exclusive_scan(eq, warp_sums, &eq_total);
-    const int eq_take = max(0, min(eq, remaining - eq_rank));
-    const int take = keff > 0 ? gt + eq_take : 0;
-    int o = taken_before + block_exclusive_scan(take, warp_sums, &take_total);
-    int eq_seen = 0;
+    for (int w0 = tail + threadIdx.x - lane; w0 < vis; w0 += kSelThreads) {
+      const int w = w0 + lane;
+      uint32_t key[4] = {0u, 0u, 0u, 0u};
+      bool in[4] = {false, false, false, false};
+      if (w < vis) {
+        key[0] = order_key(src[w]);
+        in[0] = (key[0] & mask) == prefix;
+        if (in[0]) atomicAdd(&hist[(key[0] >> kShift2) & kLowMask], 1);
+      }
+      if (use_list) append_keys(key, in, cand, &ncand);
+    }
+    __syncthreads();
+    find_bucket(hist, 1 << kSelLowBits, remaining, warp_sums, sel);
+    prefix |= (uint32_t)sel[0] << kShift2;
+    mask |= kLowMask << kShift2;
+    remaining = sel[1];
+    whole = sel[2] == remaining;
+  }
+
+  // third digit: bits 9..0
+  if (!whole) {
+    hist[threadIdx.x] = 0;
+    __syncthreads();
+    if (use_list) {
+      const int nc = ncand;
+      for (int i = threadIdx.x; i < nc; i += kSelThreads) {
+        const uint32_t key = cand[i];
+        if ((key & mask) == prefix) atomicAdd(&hist[key & kLowMask], 1);
+      }
+    } else {
+      for (int w = threadIdx.x; w < vis; w += kSelThreads) {
+        const uint32_t key = order_key(src[w]);
+        if ((key & mask) == prefix) atomicAdd(&hist[key & kLowMask], 1);
+      }
+    }
+    __syncthreads();
+    find_bucket(hist, 1 << kSelLowBits, remaining, warp_sums, sel);
+    prefix |= (uint32_t)sel[0];
+    mask = ~0u;
+    remaining = sel[1];
+  }
+
+  // Keys whose digits under `mask` exceed `prefix` are taken; of those equal to
+  // it, the first `remaining` (lowest windows first).
+  const bool vec_pos = ((uintptr_t)pos_out & 15) == 0;
+  int taken_before = 0, eq_before = 0;
+  for (int r0 = 0; r0 < vis; r0 += kSelRound) {
+    const int w0 = r0 + (int)threadIdx.x * kSelRun;
+    uint32_t gtm = 0, eqm = 0;
+    if (staged && w0 + kSelRun <= vis) {
 #pragma unroll
-    for (int e = 0; e < kSelPerThread; ++e) {
-      if (w0 + e >= vis || take == 0) continue;
-      bool t = keys[e] > prefix;
-      if (keys[e] == prefix) t = eq_seen++ < eq_take;
-      if (!t) continue;
-      const long long w = w0 + e;
+      for (int e = 0; e < kSelRun / 4; ++e) {
+        const int j = (e + lane) & (kSelRun / 4 - 1);  // rotated: eight lanes hit 32 banks
+        const float4 v = ssc4[w0 / 4 + j];
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t key = order_key(f[c]) & mask;
+          gtm |= (uint32_t)(key > prefix) << (4 * j + c);
+          eqm |= (uint32_t)(key == prefix) << (4 * j + c);
+        }
+      }
+    } else {
+#pragma unroll 8
+      for (int e = 0; e < kSelRun; ++e) {
+        const int j = (e + lane) & (kSelRun - 1);  // rotated, so a warp's reads hit 32 banks
+        if (w0 + j < vis) {
+          const uint32_t key = order_key(src[w0 + j]) & mask;
+          gtm |= (uint32_t)(key > prefix) << j;
+          eqm |= (uint32_t)(key == prefix) << j;
+        }
+      }
+    }
+    const int gt = __popc(gtm), eq = __popc(eqm);
+    uint32_t tot;
+    const uint32_t pre = block_exclusive_scan(((uint32_t)gt << 16) | (uint32_t)eq, warp_sums, &tot);
+    const int gt_pre = (int)(pre >> 16), eq_pre = (int)(pre & 0xffffu);
+    const int rem_eq = max(0, remaining - eq_before);
+    const int eq_take = max(0, min(eq, rem_eq - eq_pre));
+    int o = taken_before + gt_pre + min(eq_pre, rem_eq);
+    uint32_t takem = gtm;
+    for (uint32_t m = eqm, n = 0; n < (uint32_t)eq_take; ++n) {
+      takem |= m & (0u - m);  // lowest remaining equal key
+      m &= m - 1;
+    }
+    while (takem) {
+      const int j = __ffs(takem) - 1;
+      takem &= takem - 1;
+      const long long w = w0 + j;
       if (win_out) win_out[row * k + o] = (int32_t)w;
+      int32_t pv[kWindow];
 #pragma unroll
       for (int i = 0; i < kWindow; ++i) {
         const long long tpos = kWindow * w + i;
-        pos_out[row * (long long)kWindow * k + (long long)kWindow * o + i] =
-            tpos <= p ? (int32_t)tpos : -1;
+        pv[i] = tpos <= p ? (int32_t)tpos : -1;
+      }
+      int32_t* dst = pos_out + row * (long long)kWindow * k + (long long)kWindow * o;
+      if (vec_pos) {
+        *(int4*)dst = make_int4(pv[0], pv[1], pv[2], pv[3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kWindow; ++i) dst[i] = pv[i];
       }
       ++o;
     }
-    taken_before += take_total;
-    eq_before_round += eq_total;
+    taken_before += (int)(tot >> 16) + min((int)(tot & 0xffffu), rem_eq);
+    eq_before += (int)(tot & 0xffffu);
   }
   // padding past the chosen windows
   for (int j = taken_before + threadIdx.x; j < k; j += kSelThreads) {
@@ -277,7 +587,276 @@ __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restri
   }
 }
 
+// The same selection with a row spread over a cluster of eight CTAs: CTA r
+// stages and scans windows [r * slice, (r + 1) * slice) of the row.  Each
+// digit's histogram is built in every CTA's shared memory for its own slice;
+// after a cluster barrier every CTA sums the eight histograms bin by bin
+// through distributed shared memory, so all eight take the same decision.
+// In the output pass a CTA's windows are placed after those its lower-ranked
+// peers take, from the peers' totals (one more exchange).
+constexpr int kSelCluster = 8;
+constexpr int kSelClusterSlice = kSelThreads * 32;  // windows a CTA stages, at most
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// This thread's top-down bin counts (as find_bucket_counts takes them),
+// summed over the histograms at the same address in every CTA of the cluster.
+__device__ __forceinline__ void cluster_counts(const int* hist, int nbins, int (&c)[4]) {
+  const int per = nbins / kSelThreads;
+  const int top = nbins - 1 - (int)threadIdx.x * per;
+  c[0] = c[1] = c[2] = c[3] = 0;
+  // every load is issued before the first sum, so the eight remote reads overlap
+  if (per == 4) {
+    const uint32_t a = smem_u32(hist + top - 3);  // bins top-3 .. top, 16-byte aligned
+    uint4 v[kSelCluster];
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) v[r] = ld_cluster_v4(mapa(a, r));
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) {
+      c[0] += (int)v[r].w;
+      c[1] += (int)v[r].z;
+      c[2] += (int)v[r].y;
+      c[3] += (int)v[r].x;
+    }
+  } else {
+    const uint32_t a = smem_u32(hist + top);
+    uint32_t v[kSelCluster];
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) v[r] = ld_cluster_u32(mapa(a, r));
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) c[0] += (int)v[r];
+  }
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
+    const float* __restrict__ scores, long long nwin, int S, long long len, int k,
+    int32_t* __restrict__ win_out, int32_t* __restrict__ pos_out) {
+  extern __shared__ float4 ssc4[];  // this CTA's slice of the row
+  __shared__ __align__(16) int hist_a[1 << kSelTopBits];
+  __shared__ __align__(16) int hist_b[1 << kSelLowBits];
+  __shared__ uint32_t cand[kSelCand];
+  __shared__ uint32_t warp_sums[32];
+  __shared__ int sel[3];
+  __shared__ int ncand;
+  __shared__ int cta_tot[2];
+  const int lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();
+  const int s = blockIdx.y, b = blockIdx.z;
+  const long long p = len - S + s;
+  const int vis = (int)(p / kWindow + 1);
+  const int keff = min(k, vis);
+  const long long row = (long long)b * S + s;
+  const int slice = ((vis + kSelCluster - 1) / kSelCluster + 3) & ~3;
+  const int lo = min(vis, rank * slice);
+  const int nloc = min(vis, lo + slice) - lo;
+  float* ssc = (float*)ssc4;
+  const float* src = scores + row * nwin + lo;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < nloc; i += kSelThreads) ssc[i] = src[i];
+  for (int i = threadIdx.x; i < (1 << kSelTopBits); i += kSelThreads) hist_a[i] = 0;
+  __syncthreads();
+  const int n4 = nloc / 4, tail = 4 * n4;
+
+  // first digit: bits 31..20
+  for (int i = threadIdx.x; i < n4; i += kSelThreads) {
+    const float4 v = ssc4[i];
+    atomicAdd(&hist_a[order_key(v.x) >> (32 - kSelTopBits)], 1);
+    atomicAdd(&hist_a[order_key(v.y) >> (32 - kSelTopBits)], 1);
+    atomicAdd(&hist_a[order_key(v.z) >> (32 - kSelTopBits)], 1);
+    atomicAdd(&hist_a[order_key(v.w) >> (32 - kSelTopBits)], 1);
+  }
+  for (int w = tail + threadIdx.x; w < nloc; w += kSelThreads)
+    atomicAdd(&hist_a[order_key(ssc[w]) >> (32 - kSelTopBits)], 1);
+  cluster_sync();  // every slice's histogram is complete
+  int c[4];
+  cluster_counts(hist_a, 1 << kSelTopBits, c);
+  find_bucket_counts(c, (1 << kSelTopBits) / kSelThreads, 1 << kSelTopBits, keff, warp_sums,
+                     sel);
+  constexpr int kShift2 = 32 - kSelTopBits - kSelLowBits;
+  constexpr uint32_t kLowMask = (1u << kSelLowBits) - 1;
+  uint32_t prefix = (uint32_t)sel[0] << (32 - kSelTopBits);
+  uint32_t mask = ~0u << (32 - kSelTopBits);
+  int remaining = sel[1];
+  bool whole = sel[2] == remaining;
+  const bool use_list = sel[2] <= kSelCand;  // then no slice holds more than the list
+
+  // second digit: bits 19..10 of the keys in the chosen bucket
+  if (!whole) {
+    hist_b[threadIdx.x] = 0;
+    if (threadIdx.x == 0) ncand = 0;
+    __syncthreads();
+    for (int i0 = threadIdx.x - lane; i0 < n4; i0 += kSelThreads) {
+      const int i = i0 + lane;
+      uint32_t key[4] = {0u, 0u, 0u, 0u};
+      bool in[4] = {false, false, false, false};
+      if (i < n4) {
+        const float4 v = ssc4[i];
+        key[0] = order_key(v.x);
+        key[1] = order_key(v.y);
+        key[2] = order_key(v.z);
+        key[3] = order_key(v.w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          in[e] = (key[e] & mask) == prefix;
+          if (in[e]) atomicAdd(&hist_b[(key[e] >> kShift2) & kLowMask], 1);
+        }
+      }
+      if (use_list) append_keys(key, in, cand, &ncand);
+    }
+    for (int w0 = tail + threadIdx.x - lane; w0 < nloc; w0 += kSelThreads) {
+      const int w = w0 + lane;
+      uint32_t key[4] = {0u, 0u, 0u, 0u};
+      bool in[4] = {false, false, false, false};
+      if (w < nloc) {
+        key[0] = order_key(ssc[w]);
+        in[0] = (key[0] & mask) == prefix;
+        if (in[0]) atomicAdd(&hist_b[(key[0] >> kShift2) & kLowMask], 1);
+      }
+      if (use_list) append_keys(key, in, cand, &ncand);
+    }
+    cluster_sync();
+    cluster_counts(hist_b, 1 << kSelLowBits, c);
+    find_bucket_counts(c, 1, 1 << kSelLowBits, remaining, warp_sums, sel);
+    prefix |= (uint32_t)sel[0] << kShift2;
+    mask |= kLowMask << kShift2;
+    remaining = sel[1];
+    whole = sel[2] == remaining;
+  }
+
+  // third digit: bits 9..0, in the bins of hist_a (every peer read hist_a
+  // before it arrived on the barrier that ended the second digit)
+  if (!whole) {
+    hist_a[threadIdx.x] = 0;
+    __syncthreads();
+    if (use_list) {
+      const int nc = ncand;
+      for (int i = threadIdx.x; i < nc; i += kSelThreads) {
+        const uint32_t key = cand[i];
+        if ((key & mask) == prefix) atomicAdd(&hist_a[key & kLowMask], 1);
+      }
+    } else {
+      for (int w = threadIdx.x; w < nloc; w += kSelThreads) {
+        const uint32_t key = order_key(ssc[w]);
+        if ((key & mask) == prefix) atomicAdd(&hist_a[key & kLowMask], 1);
+      }
+    }
+    cluster_sync();
+    cluster_counts(hist_a, 1 << kSelLowBits, c);
+    find_bucket_counts(c, 1, 1 << kSelLowBits, remaining, warp_sums, sel);
+    prefix |= (uint32_t)sel[0];
+    mask = ~0u;
+    remaining = sel[1];
+  }
+
+  // output: thread t marks windows [t * run, (t + 1) * run) of the slice
+  const int run = 4 * ((nloc + 4 * kSelThreads - 1) / (4 * kSelThreads));  // <= 32
+  const int t0 = (int)threadIdx.x * run;
+  uint32_t gtm = 0, eqm = 0;
+  if (run > 0 && t0 + run <= nloc) {
+    const int q4 = run / 4;
+    for (int e = 0; e < q4; ++e) {
+      const int j = (e + lane) % q4;  // rotated across the lanes
+      const float4 v = ssc4[t0 / 4 + j];
+      const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint32_t key = order_key(f[cc]) & mask;
+        gtm |= (uint32_t)(key > prefix) << (4 * j + cc);
+        eqm |= (uint32_t)(key == prefix) << (4 * j + cc);
+      }
+    }
+  } else {
+    for (int j = 0; j < run && t0 + j < nloc; ++j) {
+      const uint32_t key = order_key(ssc[t0 + j]) & mask;
+      gtm |= (uint32_t)(key > prefix) << j;
+      eqm |= (uint32_t)(key == prefix) << j;
+    }
+  }
+  const int gt = __popc(gtm), eq = __popc(eqm);
+  uint32_t tot;
+  const uint32_t pre = block_exclusive_scan(((uint32_t)gt << 16) | (uint32_t)eq, warp_sums, &tot);
+  if (threadIdx.x == 0) {
+    cta_tot[0] = (int)(tot >> 16);
+    cta_tot[1] = (int)(tot & 0xffffu);
+  }
+  cluster_sync();  // every CTA's totals are published
+  // lane r < rank reads peer r's totals; a warp sum gives every lane the lot
+  int gt_before = 0, eq_before = 0;
+  if (lane < rank) {
+    gt_before = (int)ld_cluster_u32(mapa(smem_u32(&cta_tot[0]), lane));
+    eq_before = (int)ld_cluster_u32(mapa(smem_u32(&cta_tot[1]), lane));
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    gt_before += __shfl_xor_sync(0xffffffffu, gt_before, o);
+    eq_before += __shfl_xor_sync(0xffffffffu, eq_before, o);
+  }
+  cluster_arrive();  // done with the peers' shared memory; wait for theirs at the end
+  const int gt_pre = (int)(pre >> 16), eq_pre = (int)(pre & 0xffffu);
+  const int rem_eq = max(0, remaining - eq_before);
+  const int eq_take = max(0, min(eq, rem_eq - eq_pre));
+  int o = gt_before + min(eq_before, remaining) + gt_pre + min(eq_pre, rem_eq);
+  uint32_t takem = gtm;
+  for (uint32_t m = eqm, n = 0; n < (uint32_t)eq_take; ++n) {
+    takem |= m & (0u - m);
+    m &= m - 1;
+  }
+  const bool vec_pos = ((uintptr_t)pos_out & 15) == 0;
+  while (takem) {
+    const int j = __ffs(takem) - 1;
+    takem &= takem - 1;
+    const long long w = (long long)lo + t0 + j;
+    if (win_out) win_out[row * k + o] = (int32_t)w;
+    int32_t pv[kWindow];
+#pragma unroll
+    for (int i = 0; i < kWindow; ++i) {
+      const long long tpos = kWindow * w + i;
+      pv[i] = tpos <= p ? (int32_t)tpos : -1;
+    }
+    int32_t* dst = pos_out + row * (long long)kWindow * k + (long long)kWindow * o;
+    if (vec_pos) {
+      *(int4*)dst = make_int4(pv[0], pv[1], pv[2], pv[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kWindow; ++i) dst[i] = pv[i];
+    }
+    ++o;
+  }
+  // padding past the keff chosen windows
+  if (rank == kSelCluster - 1) {
+    for (int j = keff + threadIdx.x; j < k; j += kSelThreads) {
+      if (win_out) win_out[row * k + j] = -1;
+#pragma unroll
+      for (int i = 0; i < kWindow; ++i) pos_out[row * (long long)kWindow * k + kWindow * j + i] = -1;
+    }
+  }
+  cluster_wait();
+}
+
 }  // namespace
+
+int indexer_device_status(bool clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_indexer_status, sizeof(int)) != cudaSuccess) return -1;
+  if (clear && v != 0) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_indexer_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
+}
+
 }  // namespace mla
 
 using namespace mla;
@@ -326,15 +905,18 @@ extern "C" mla_status_t mla_indexer_pool_update(const void* keys, int32_t dtype,
   if (nw > 0) {
     const dim3 grid((unsigned)((nw + 7) / 8), batch);
     cudaStream_t st = (cudaStream_t)stream;
+    const size_t esz = dtype == MLA_DTYPE_BF16 ? 2 : 4;
+    const bool vec = (dim / 32) % 4 == 0 && key_row_stride % 4 == 0 &&
+                     (uintptr_t)keys % (4 * esz) == 0 && (uintptr_t)pooled % 16 == 0;
     KernelTimer kt("indexer_pool_windows", st);
     if (dtype == MLA_DTYPE_BF16)
       pool_windows<__nv_bfloat16><<<grid, 256, 0, st>>>(
           (const __nv_bfloat16*)keys, key_row_stride, seq_stride_rows, dim, cache_len, w0, nwin,
-          pooled, pooled_windows_cap);
+          pooled, pooled_windows_cap, vec);
     else
       pool_windows<float><<<grid, 256, 0, st>>>((const float*)keys, key_row_stride,
                                                  seq_stride_rows, dim, cache_len, w0, nwin,
-                                                 pooled, pooled_windows_cap);
+                                                 pooled, pooled_windows_cap, vec);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {
@@ -378,9 +960,17 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
     return MLA_ERR_INVALID_ARG;
   }
   const long long nwin = (cache_len + kWindow - 1) / kWindow;
+  if (nwin > (1LL << 30)) {
+    set_error("a cache of %lld tokens has more than 2^30 windows", (long long)cache_len);
+    return MLA_ERR_INVALID_ARG;
+  }
   if (pooled_windows_cap < nwin) {
     set_error("the pool holds %lld windows; a cache of %lld tokens fills %lld",
               (long long)pooled_windows_cap, (long long)cache_len, nwin);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (((uintptr_t)q | (uintptr_t)pooled) & 15) {
+    set_error("q and pooled must be 16-byte aligned (the scoring kernel reads them as float4)");
     return MLA_ERR_INVALID_ARG;
   }
   if ((size_t)new_tokens * dim * sizeof(float) > 48 * 1024) {
@@ -399,15 +989,21 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
   float* scores = (float*)workspace;
   {
     KernelTimer kt("indexer_score_windows", st);
-    score_windows<<<dim3((unsigned)((nwin + 255) / 256), batch), 256,
-                    (size_t)new_tokens * dim * sizeof(float), st>>>(
-        q, pooled, pooled_windows_cap, dim, new_tokens, nwin, scores);
+    if (dim == 128) {
+      const dim3 grid((unsigned)((nwin + kD128CtaWindows - 1) / kD128CtaWindows), batch);
+      score_windows_d128<<<grid, kD128Threads, kD128CtaWindows * 512, st>>>(
+          q, pooled, pooled_windows_cap, new_tokens, nwin, scores);
+    } else {
+      const dim3 grid((unsigned)((nwin + kScoreWinPerCta - 1) / kScoreWinPerCta), batch);
+      score_windows<<<grid, kScoreThreads, (size_t)new_tokens * dim * sizeof(float), st>>>(
+          q, pooled, pooled_windows_cap, dim, new_tokens, nwin, scores);
+    }
   }
   {
     KernelTimer kt("indexer_select_topk", st);
     const long long vis_max = (cache_len - 1) / kWindow + 1;
     const size_t sel_smem = vis_max <= kSelSmemWindows ? (size_t)vis_max * sizeof(float) : 0;
-    if (sel_smem > 48 * 1024) {
+    {  // the static arrays and the staged scores together pass 48 KB
       static std::once_flag once;
       static cudaError_t attr_err = cudaSuccess;
       std::call_once(once, [] {
@@ -419,8 +1015,53 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
         return MLA_ERR_CUDA;
       }
     }
-    select_topk<<<dim3(new_tokens, batch), kSelThreads, sel_smem, st>>>(
-        scores, nwin, new_tokens, cache_len, k_windows, windows_out, positions_out);
+    // a cluster of eight CTAs per row when its slices fit and the device
+    // can hold such a cluster; otherwise one CTA per row
+    const long long slice_max = ((vis_max + kSelCluster - 1) / kSelCluster + 3) & ~3LL;
+    static std::once_flag once_c;
+    static bool cluster_ok = false;
+    std::call_once(once_c, [] {
+      if (cudaFuncSetAttribute(select_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSelClusterSlice * (int)sizeof(float)) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+      }
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kSelCluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(kSelCluster, 1, 1);
+      cfg.blockDim = dim3(kSelThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSelClusterSlice * sizeof(float);
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      cluster_ok = cudaOccupancyMaxActiveClusters(&n, select_topk_cluster, &cfg) == cudaSuccess &&
+                   n > 0;
+      cudaGetLastError();
+    });
+    if (cluster_ok && slice_max <= kSelClusterSlice) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kSelCluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(kSelCluster, new_tokens, batch);
+      cfg.blockDim = dim3(kSelThreads, 1, 1);
+      cfg.dynamicSmemBytes = (size_t)slice_max * sizeof(float);
+      cfg.stream = st;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cudaLaunchKernelEx(&cfg, select_topk_cluster, (const float*)scores, (long long)nwin,
+                         (int)new_tokens, (long long)cache_len, (int)k_windows, windows_out,
+                         positions_out);
+    } else {
+      select_topk<<<dim3(new_tokens, batch), kSelThreads, sel_smem, st>>>(
+          scores, nwin, new_tokens, cache_len, k_windows, windows_out, positions_out);
+    }
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

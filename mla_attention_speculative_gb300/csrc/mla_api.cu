@@ -581,8 +581,9 @@ extern "C" const char* mla_status_string(int32_t s) {
 extern "C" const char* mla_last_error(void) { return g_err; }
 
 extern "C" mla_status_t mla_device_status(int32_t* code, int32_t clear) {
-  const int words[4] = {absorbed_device_status(clear != 0), materialised_device_status(clear != 0),
-                        generic_device_status(clear != 0), selftest_device_status(clear != 0)};
+  const int words[5] = {absorbed_device_status(clear != 0), materialised_device_status(clear != 0),
+                        generic_device_status(clear != 0), selftest_device_status(clear != 0),
+                        indexer_device_status(clear != 0)};
   int v = 0;
   for (int w : words) {
     if (w < 0) {

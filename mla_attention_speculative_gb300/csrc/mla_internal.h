@@ -131,6 +131,9 @@ size_t fast_materialised_workspace(const Plan& p);
 cudaError_t launch_fast_materialised(const Plan& p, const Args& a);
 int materialised_device_status(bool clear);
 
+// Status word of the indexer kernels (0 = no wait ran out); synchronises.
+int indexer_device_status(bool clear);
+
 // Records a one-line failure description for mla_last_error().
 void set_error(const char* fmt, ...);
 

@@ -262,3 +262,21 @@ def test_indexer_pool_update_rejects_bad_arguments(kw):
                                          args["cap"], ctypes.byref(st), None, None)
     assert status == B.MLA_ERR_INVALID_ARG
     assert st.length == -1          # the state is untouched by a rejected call
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), B.MLA_ERR_WORKSPACE),                      # valid, but no workspace given
+    (dict(q=0x10004), B.MLA_ERR_INVALID_ARG),           # q not 16-byte aligned
+    (dict(pooled=0x20008), B.MLA_ERR_INVALID_ARG),      # pooled not 16-byte aligned
+    (dict(new_tokens=33), B.MLA_ERR_INVALID_ARG),
+    (dict(dim=512, new_tokens=32), B.MLA_ERR_INVALID_ARG),   # 64 KB of queries > 48 KB
+    (dict(cap=10), B.MLA_ERR_INVALID_ARG),
+    (dict(k=0), B.MLA_ERR_INVALID_ARG),
+])
+def test_indexer_select_rejects_before_launch(kw, status):
+    a = dict(q=0x10000, pooled=0x20000, cap=25, dim=128, cache_len=100, new_tokens=4, k=8)
+    a.update(kw)
+    st = B.lib().mla_indexer_select(a["q"], a["pooled"], a["cap"], 1, a["dim"], a["cache_len"],
+                                    a["new_tokens"], a["k"], None, 0x30000, None, 0, None)
+    assert st == status
+    assert B.mla_last_error() != ""

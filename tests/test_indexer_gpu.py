@@ -144,7 +144,8 @@ def _check_selection(q, pooled, T, S, k, wins, pos):
                 assert np.array_equal(pos[b, s], opos[s])
 
 
-@pytest.mark.parametrize("T,S,k", [(4099, 4, 64), (131072, 8, 512), (37, 3, 20), (9, 2, 512)])
+@pytest.mark.parametrize("T,S,k", [(4099, 4, 64), (131072, 8, 512), (37, 3, 20), (9, 2, 512),
+                                   (200003, 2, 1000)])
 def test_select_is_a_valid_topk(T, S, k):
     keys = _keys(2, T, 128, torch.bfloat16, T + S).cuda()
     pooled = torch.zeros((2, -(-T // 4), 128), device="cuda")
@@ -154,6 +155,27 @@ def test_select_is_a_valid_topk(T, S, k):
     wins, pos = B.mla_indexer_select(q, pooled, T, k)
     torch.cuda.synchronize()
     _check_selection(q, pooled, T, S, k, wins, pos)
+
+
+@pytest.mark.parametrize("T,S,k,dim", [(5003, 3, 200, 64), (9001, 20, 300, 96),
+                                       (131075, 4, 512, 128), (200003, 2, 3000, 64),
+                                       (1048803, 2, 700, 32)])
+def test_select_with_many_ties_is_exactly_the_oracles(T, S, k, dim):
+    # small-integer keys and queries: every score is an exact fp32 integer
+    # whatever the summation order, so many windows tie at the k-th score and
+    # the choice (ties to the lower window) is unique.  A row of windows is
+    # spread over a cluster of CTAs up to 262120 windows; 1048803 tokens make
+    # 262201, which one CTA per row selects over several output rounds, from
+    # global memory.  dim 96 and 32 take the scoring kernel's generic form
+    g = torch.Generator().manual_seed(T + k)
+    W = -(-T // 4)
+    pooled = torch.randint(-3, 4, (1, W, dim), generator=g).float()
+    q = torch.randint(-2, 3, (1, S, dim), generator=g).float()
+    wins, pos = B.mla_indexer_select(q.cuda(), pooled.cuda(), T, k)
+    torch.cuda.synchronize()
+    ow, opos = P.select_topk(q[0].double().numpy(), pooled[0].double().numpy(), T, S, k)
+    assert np.array_equal(wins[0].cpu().numpy(), ow)
+    assert np.array_equal(pos[0].cpu().numpy(), opos)
 
 
 def test_selection_ties_go_to_the_lower_window():
