@@ -284,14 +284,17 @@ typedef struct {
 
 /* Section "A later extension: load snapshot history once", Algorithms 4 and
  * 5: X = S || T row by row (S: s state words, T: n new words per row; H
- * channels, Q sequences; 1 <= s <= 8, 1 <= n, s + n <= 16) and the k <= 8
+ * channels, Q sequences; 1 <= s <= 8, 1 <= n, s + n <= 16, Q <= 65535,
+ * H*(s + n) <= 2^30) and the k <= 8
  * snapshot windows of X into `cache` (cache_words words long).  All buffers
  * are device memory.  When 2 <= k <= 8 and the windows' destinations are
  * pairwise disjoint and lie outside S, T and X, one kernel loads each row
  * once and writes X and every window from that load (*fused_out = 1);
  * otherwise the ordinary path runs: X, then one copy per window that reads X
- * back (*fused_out = 0; the windows are written in order).  A window outside
- * the row or a destination outside the cache is MLA_ERR_INVALID_ARG.
+ * back (*fused_out = 0; the windows are written in order).  X may share
+ * words with S or T only row for row (then each row is read before it is
+ * written).  A window outside the row or a destination outside the cache is
+ * MLA_ERR_INVALID_ARG.
  * Asynchronous on `stream`.  fused_out is host memory and may be NULL. */
 mla_status_t mla_concat_snapshots(const uint32_t* S, const int64_t* s_strides, const uint32_t* T,
                                   const int64_t* t_strides, uint32_t* X,

@@ -4,11 +4,14 @@
 //  * section "A later extension: load snapshot history once", Algorithm 4
 //    (recognise a safe snapshot group) and Algorithm 5 (one load per row,
 //    then the concatenation and every snapshot window written from it):
-//    mla_concat_snapshots.  A thread owns one (channel, sequence) row, loads
-//    its s state words and n new words once into registers, writes the
-//    concatenated row and then each window's s words.  When the group is not
-//    safe to fuse, the ordinary path runs: the concatenation, then one copy
-//    per window that reads it back.  Words are moved as uint32 bit patterns.
+//    mla_concat_snapshots.  Every source word is loaded once and the
+//    concatenated row and each window's s words are written from that load.
+//    For the contiguous row layouts a CTA stages 256 channels' words in
+//    shared memory and writes X and the windows as contiguous runs; other
+//    layouts give a thread one (channel, sequence) row in registers, as the
+//    page does.  When the group is not safe to fuse, the ordinary path runs:
+//    the concatenation, then one copy per window that reads it back.  Words
+//    are moved as uint32 bit patterns.
 //  * section "Keep the pooled keys; score them again", ValidBlock and
 //    Algorithm 1 (retain a rollback-valid prefix): mla_rollback_valid_prefix.
 //    The predicate is checked for every block in parallel and the prefix ends
@@ -40,10 +43,11 @@ struct ConcatParams {
   uint32_t* cache;
   Strides ss, ts, xs;
   int s, n, H, Q, k;
+  int magic_w, magic_s;  // div_magic(s + n), div_magic(s)
   Window w[kMaxWindows];
 };
 
-// Algorithm 5: one thread per row, 128 threads per CTA.
+// Algorithm 5 for any strides: one thread per row, 128 threads per CTA.
 __global__ void __launch_bounds__(128) concat_snapshots_kernel(ConcatParams p) {
   const long long g = (long long)blockIdx.x * 128 + threadIdx.x;
   if (g >= (long long)p.H * p.Q) return;
@@ -73,15 +77,98 @@ __global__ void __launch_bounds__(128) concat_snapshots_kernel(ConcatParams p) {
   }
 }
 
-// Ordinary path, one snapshot copy: reads the window back from X.
-__global__ void __launch_bounds__(128) snapshot_copy_kernel(const uint32_t* X, Strides xs,
+// The same for the contiguous row layouts: S rows of s words and X rows of
+// s + n words per channel, T rows of n words or channel-fastest planes.  A CTA
+// takes 256 channels of one sequence: it loads their S and T words into
+// shared memory in coalesced runs (each source word once), then writes their
+// X rows and every window's s words per channel as contiguous runs, so no
+// warp store is scattered over rows.
+constexpr int kRowsPerCta = 256;
+
+// Element e of a run of rows `w` words wide, walked 256 at a time: row and
+// column advance by 256 / w and 256 % w with a carry, no division per word.
+// The start uses e / w = (e * m) >> 16 with m = ceil(2^16 / w), exact for
+// e < 4096 and w <= 16 (the error e (m - 2^16/w) / 2^16 < 1/16 <= 1/w).
+__host__ __device__ constexpr int div_magic(int w) { return (65536 + w - 1) / w; }
+struct RowWalk {
+  int h, i, dq, dr, w;
+  __device__ RowWalk(int e, int w_, int magic)
+      : h((e * magic) >> 16), i(e - ((e * magic) >> 16) * w_), dq((kRowsPerCta * magic) >> 16),
+        dr(kRowsPerCta - ((kRowsPerCta * magic) >> 16) * w_), w(w_) {}
+  __device__ void next() {
+    h += dq;
+    i += dr;
+    if (i >= w) {
+      i -= w;
+      ++h;
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kRowsPerCta) concat_rows_kernel(ConcatParams p, int t_rows) {
+  __shared__ uint32_t sS[kRowsPerCta * (kMaxRow / 2)];
+  __shared__ uint32_t sT[kRowsPerCta * kMaxRow];
+  const int q = blockIdx.y;
+  const int h0 = blockIdx.x * kRowsPerCta;
+  const int R = min(kRowsPerCta, p.H - h0);
+  const int s = p.s, n = p.n, w = s + n;
+  // every load of the thread is issued before the first store to shared memory
+  const uint32_t* Sb = p.S + q * p.ss.q + (long long)h0 * s;
+  uint32_t vs[kMaxRow / 2], vt[kMaxRow];
+#pragma unroll
+  for (int m = 0; m < kMaxRow / 2; ++m) {
+    const int e = threadIdx.x + m * kRowsPerCta;
+    vs[m] = e < R * s ? Sb[e] : 0u;
+  }
+  const uint32_t* Tb = p.T + q * p.ts.q + (t_rows ? (long long)h0 * n : (long long)h0);
+#pragma unroll
+  for (int m = 0; m < kMaxRow; ++m) {
+    // row layout: word threadIdx + 256 m of the block; planes: plane m, channel threadIdx
+    const bool live = t_rows ? threadIdx.x + m * kRowsPerCta < R * n
+                             : m < n && (int)threadIdx.x < R;
+    vt[m] = live ? Tb[t_rows ? threadIdx.x + m * kRowsPerCta : m * p.ts.i + threadIdx.x] : 0u;
+  }
+#pragma unroll
+  for (int m = 0; m < kMaxRow / 2; ++m) {
+    const int e = threadIdx.x + m * kRowsPerCta;
+    if (e < R * s) sS[e] = vs[m];
+  }
+#pragma unroll
+  for (int m = 0; m < kMaxRow; ++m) {
+    if (t_rows) {
+      const int e = threadIdx.x + m * kRowsPerCta;
+      if (e < R * n) sT[e] = vt[m];
+    } else if (m < n && (int)threadIdx.x < R) {
+      sT[threadIdx.x * n + m] = vt[m];
+    }
+  }
+  __syncthreads();
+  uint32_t* Xb = p.X + q * p.xs.q + (long long)h0 * w;
+  RowWalk x(threadIdx.x, w, p.magic_w);
+  for (int e = threadIdx.x; e < R * w; e += kRowsPerCta, x.next())
+    Xb[e] = x.i < s ? sS[x.h * s + x.i] : sT[x.h * n + x.i - s];
+  for (int j = 0; j < p.k; ++j) {
+    const int a = p.w[j].a;
+    uint32_t* d = p.cache + p.w[j].offset + q * p.w[j].stride + (long long)h0 * s;
+    RowWalk c(threadIdx.x, s, p.magic_s);
+    for (int e = threadIdx.x; e < R * s; e += kRowsPerCta, c.next()) {
+      const int i = a + c.i;
+      d[e] = i < s ? sS[c.h * s + i] : sT[c.h * n + i - s];
+    }
+  }
+}
+
+// Ordinary path, one snapshot copy: reads the window back from X.  One thread
+// per cache word (channel e / s, element a + e % s of its row), so the writes
+// are contiguous.
+__global__ void __launch_bounds__(256) snapshot_copy_kernel(const uint32_t* X, Strides xs,
                                                             uint32_t* cache, Window w, int s,
-                                                            int H, int Q) {
-  const long long g = (long long)blockIdx.x * 128 + threadIdx.x;
-  if (g >= (long long)H * Q) return;
-  const int h = (int)(g % H), q = (int)(g / H);
-  uint32_t* d = cache + w.offset + q * w.stride + (long long)h * s;
-  for (int i = 0; i < s; ++i) d[i] = X[(w.a + i) * xs.i + h * xs.h + q * xs.q];
+                                                            int H) {
+  const int q = blockIdx.y;
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  if (e >= H * s) return;
+  const int h = e / s, i = e - h * s;
+  cache[w.offset + q * w.stride + e] = X[(w.a + i) * xs.i + h * xs.h + q * xs.q];
 }
 
 // Word range [lo, hi) a strided buffer covers, in bytes from address 0.
@@ -161,9 +248,10 @@ extern "C" mla_status_t mla_concat_snapshots(
     return MLA_ERR_INVALID_ARG;
   }
   if (s < 1 || n < 1 || s + n > kMaxRow || s > kMaxRow / 2 || H < 1 || Q < 1 || k < 0 ||
-      k > kMaxWindows) {
-    set_error("concat/snapshot: need 1 <= s <= 8, 1 <= n, s + n <= 16, H, Q >= 1, 0 <= k <= 8 "
-              "(s=%d n=%d H=%d Q=%d k=%d)", s, n, H, Q, k);
+      k > kMaxWindows || Q > 65535 || (long long)H * (s + n) > (1LL << 30)) {
+    set_error("concat/snapshot: need 1 <= s <= 8, 1 <= n, s + n <= 16, 1 <= Q <= 65535, "
+              "1 <= H with H (s + n) <= 2^30, 0 <= k <= 8 (s=%d n=%d H=%d Q=%d k=%d)", s, n, H, Q,
+              k);
     return MLA_ERR_INVALID_ARG;
   }
   ConcatParams p;
@@ -182,6 +270,8 @@ extern "C" mla_status_t mla_concat_snapshots(
   }
   p.s = s;
   p.n = n;
+  p.magic_w = div_magic(s + n);
+  p.magic_s = div_magic(s);
   p.H = H;
   p.Q = Q;
   p.k = k;
@@ -216,24 +306,45 @@ extern "C" mla_status_t mla_concat_snapshots(
       for (const auto& d : dest)
         if (d.first < o.second && o.first < d.second) fuse = false;
   }
+  // The staged kernel serves the contiguous row layouts when X shares no word
+  // with S or T (a CTA reads its rows before it writes, not before other CTAs
+  // write); other layouts take one thread per row.
+  const bool t_rows = p.ts.i == 1 && p.ts.h == n;
+  const bool t_planes = p.ts.h == 1 && p.ts.i >= H;
+  bool staged = p.ss.i == 1 && p.ss.h == s && p.xs.i == 1 && p.xs.h == s + n &&
+                (t_rows || t_planes);
+  if (staged) {
+    const auto x = span(X, s + n, H, Q, p.xs), a = span(S, s, H, Q, p.ss),
+               b = span(T, n, H, Q, p.ts);
+    staged = !(x.first < a.second && a.first < x.second) &&
+             !(x.first < b.second && b.first < x.second);
+  }
   const cudaStream_t st = (cudaStream_t)stream;
   const unsigned grid = (unsigned)(((long long)H * Q + 127) / 128);
+  const dim3 grid_rows((unsigned)((H + kRowsPerCta - 1) / kRowsPerCta), (unsigned)Q);
+  auto concat = [&](const ConcatParams& c) {
+    if (staged)
+      concat_rows_kernel<<<grid_rows, kRowsPerCta, 0, st>>>(c, t_rows ? 1 : 0);
+    else
+      concat_snapshots_kernel<<<grid, 128, 0, st>>>(c);
+  };
   cudaError_t e;
   if (fuse) {
     KernelTimer kt("concat_snapshots", st);
-    concat_snapshots_kernel<<<grid, 128, 0, st>>>(p);
+    concat(p);
     e = cudaGetLastError();
   } else {
     ConcatParams c = p;
     c.k = 0;  // the concatenation alone
     {
       KernelTimer kt("concat", st);
-      concat_snapshots_kernel<<<grid, 128, 0, st>>>(c);
+      concat(c);
     }
     e = cudaGetLastError();
+    const dim3 grid_copy((unsigned)(((long long)H * s + 255) / 256), (unsigned)Q);
     for (int j = 0; j < k && e == cudaSuccess; ++j) {
       KernelTimer kt("snapshot_copy", st);
-      snapshot_copy_kernel<<<grid, 128, 0, st>>>(X, p.xs, cache, p.w[j], s, H, Q);
+      snapshot_copy_kernel<<<grid_copy, 256, 0, st>>>(X, p.xs, cache, p.w[j], s, H);
       e = cudaGetLastError();
     }
   }

@@ -39,8 +39,10 @@ def _row_loop(S, T, X, cache, s, n, H, Q, ss, ts, xs, windows):
 def _case(rng, s, n, H, Q, layout="row"):
     if layout == "row":           # [Q][H][i]
         ss, ts, xs = (1, s, H * s), (1, n, H * n), (1, s + n, H * (s + n))
-    else:                         # channel-fastest new activations [Q][i][H]
+    elif layout == "channels":    # channel-fastest new activations [Q][i][H]
         ss, ts, xs = (1, s, H * s), (H, 1, H * n), (1, s + n, H * (s + n))
+    else:                         # channel-fastest state too: one thread per row
+        ss, ts, xs = (H, 1, H * s), (H, 1, H * n), (1, s + n, H * (s + n))
     S = rng.integers(0, 2**32, size=H * Q * s, dtype=np.uint64).astype(np.uint32)
     T = rng.integers(0, 2**32, size=H * Q * n, dtype=np.uint64).astype(np.uint32)
     return S, T, ss, ts, xs
@@ -172,7 +174,8 @@ def _gpu_concat(rng, s, n, H, Q, windows, cache_words, layout="row"):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("s,n,k,layout", [(3, 5, 3, "row"), (8, 8, 8, "row"), (1, 1, 2, "row"),
-                                          (3, 6, 4, "channels")])
+                                          (3, 6, 4, "channels"), (3, 5, 3, "planes"),
+                                          (2, 7, 5, "planes")])
 def test_gpu_fused_group_is_bit_exact(s, n, k, layout):
     rng = np.random.default_rng(s * 100 + n * 10 + k)
     H, Q = 300, 5
