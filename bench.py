@@ -68,6 +68,23 @@ def _dist():
     return rank, world, local
 
 
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest of every rank's x (a host float), through one all-reduce on
+    `device` (the GPU for NCCL, the CPU for gloo); x itself on one rank."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, seconds_slowest):
+    """Whole-job throughput of independent replicas: the units every rank
+    processed over the slowest rank's time."""
+    return world * units_per_rank / seconds_slowest
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -789,13 +806,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    total_calls = world * args.steps * len(WIDTHS)
-    value = total_calls / (ms / 1e3)
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    value = job_rate(args.steps * len(WIDTHS), world, ms / 1e3)
     ms_per_step = ms / args.steps
 
     # ---- per-kernel device time (events around each launch, eager steps) -----
@@ -1005,10 +1017,8 @@ def _e2e(args, B, D, q, lens, lens_dev, ws, outs, geom, dev, barrier, world):
     barrier()
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([el], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = float(t.item())
-    return {"value": world * args.steps * len(WIDTHS) / el, "unit": UNIT,
+        el = max_over_ranks(el, dist, dev)
+    return {"value": job_rate(args.steps * len(WIDTHS), world, el), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
