@@ -15,21 +15,23 @@
 // computed by the same code whichever path asks for it, so a wide step pools
 // bit for bit as the same tokens fed one at a time.
 //
-// Three kernels, all bound by memory or latency:
-//   pool_windows   one warp per window: four key rows read once (as vectors),
-//                  summed in a fixed order, scaled by 1/count, stored as fp32
-//   score_windows  each window's pooled key read once, whole 512-byte rows
-//                  per warp load at dim 128, and dotted with every new
-//                  token's query; partial sums folded by a reduce-scatter
-//   select_topk    one CTA per new token: a radix select (12, 10, 10-bit
-//                  digits) of the k-th largest score over the windows the
-//                  token may see, then the chosen windows in ascending order
-//                  and their positions
+// Three steps, all bound by memory or latency:
+//   pool_windows        one warp per window: four key rows read once (as
+//                       vectors), summed in a fixed order, scaled by 1/count,
+//                       stored as fp32
+//   score_windows_d128  each window's pooled key read once (a bulk copy per 64
+//                       windows) and dotted with every new token's query;
+//                       partial sums folded by a reduce-scatter over the lanes
+//                       (score_windows: the same for dims other than 128)
+//   select_topk_cluster a row (one new token) spread over a cluster of eight
+//                       CTAs: a radix select (12, 10, 10-bit digits) of the
+//                       k-th largest score over the windows the token may see,
+//                       then the chosen windows in ascending order and their
+//                       positions (select_topk: one CTA per row, for rows too
+//                       long for the cluster's shared memory)
 
 #include <cuda_bf16.h>
 
-#include <algorithm>
-#include <cfloat>
 #include <mutex>
 
 #include "mla_internal.h"
