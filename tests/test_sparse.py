@@ -141,3 +141,32 @@ def test_repeat_call_is_deterministic():
     a = run_sparse(case, topk)
     b = run_sparse(case, topk)
     assert torch.equal(a, b)
+
+
+def _sparse_draw(i):
+    rng = np.random.default_rng(7000 + i)
+    H = int(rng.choice([128, 128, 128, 8, 40]))
+    n = int(rng.choice([64, 128, 192, 256]))
+    v = int(rng.choice([128, 256]))
+    L = int(rng.integers(1, 17))
+    lens = [int(rng.integers(L, 4001)) for _ in range(int(rng.integers(1, 4)))]
+    k = int(rng.integers(1, 1501))
+    pad = int(rng.integers(0, 6))
+    past = int(rng.integers(0, 4))
+    page = int(rng.choice([0, 64]))
+    dtype = torch.float32 if rng.random() < 0.2 else torch.bfloat16
+    return Geometry(H=H, n=n, v=v), L, lens, k, pad, past, page, dtype
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_sparse_shape(i):
+    # seeded random shapes: list length (one partial tile to many), padding,
+    # entries past the causal limit, ragged caches, paging, both kernel forms;
+    # every element of 8 sampled heads against the oracle
+    geom, L, lens, k, pad, past, page, dtype = _sparse_draw(i)
+    case = make_case(geom, L, lens, dtype=dtype, seed=7100 + i, page_size=page)
+    topk = make_topk(lens, L, k, seed=7200 + i, pad=pad, past_limit=past)
+    got = run_sparse(case, topk)
+    heads = sorted({0, geom.H - 1} | set(range(1, geom.H, max(1, geom.H // 6))))[:8]
+    compare(got[:, :, heads], want_sparse(case, topk, heads=heads), dtype,
+            f"sparse sweep{i} H={geom.H} n={geom.n} v={geom.v} L={L} lens={lens} k={k}")
