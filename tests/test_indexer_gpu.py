@@ -204,3 +204,32 @@ def test_selected_positions_feed_the_sparse_verify():
     heads = [0, 5, 127]
     want = oracle.sparse_absorbed(**oracle_inputs(case), topk=pos.cpu().numpy(), heads=heads)
     compare(out[:, :, heads], want, torch.bfloat16, "indexer -> sparse verify")
+
+
+def _select_draw(i):
+    rng = np.random.default_rng(8000 + i)
+    T = int(np.exp(rng.uniform(np.log(1), np.log(300000))))
+    dim = int(rng.choice([32, 64, 96, 128, 128, 256]))
+    S = int(rng.integers(1, min(32, 48 * 1024 // (4 * dim)) + 1))
+    S = min(S, T)
+    k = int(rng.integers(1, 4001))
+    batch = int(rng.integers(1, 4))
+    return T, S, k, dim, batch
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_select_is_exactly_the_oracles(i):
+    # seeded random shapes with small-integer keys and queries (every score an
+    # exact fp32 integer, many ties): the chosen windows and positions equal
+    # the oracle's bit for bit, through either form of the selection
+    T, S, k, dim, batch = _select_draw(i)
+    g = torch.Generator().manual_seed(8100 + i)
+    W = -(-T // 4)
+    pooled = torch.randint(-3, 4, (batch, W, dim), generator=g).float()
+    q = torch.randint(-2, 3, (batch, S, dim), generator=g).float()
+    wins, pos = B.mla_indexer_select(q.cuda(), pooled.cuda(), T, k)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        ow, opos = P.select_topk(q[b].double().numpy(), pooled[b].double().numpy(), T, S, k)
+        assert np.array_equal(wins[b].cpu().numpy(), ow), (i, T, S, k, dim, b)
+        assert np.array_equal(pos[b].cpu().numpy(), opos), (i, T, S, k, dim, b)
