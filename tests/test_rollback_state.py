@@ -227,3 +227,25 @@ def test_gpu_rollback_prefix_matches_oracle(seed):
                                            torch.from_numpy(cp).cuda(),
                                            torch.from_numpy(cs.view(np.int64)).cuda(), p0,
                                            seq=1).item()) == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", range(12))
+def test_gpu_random_groups_are_bit_exact(i):
+    # seeded random row widths, window counts and starts, channel and sequence
+    # counts, all three layouts; one group in four gives two windows the same
+    # destination, which must take the ordinary path with the same result
+    rng = np.random.default_rng(300 + i)
+    s = int(rng.integers(1, 9))
+    n = int(rng.integers(1, 17 - s))
+    k = int(rng.integers(1, 9))
+    H = int(rng.integers(1, 700))
+    Q = int(rng.integers(1, 7))
+    layout = str(rng.choice(["row", "channels", "planes"]))
+    block = k * H * s
+    windows = [(int(rng.integers(0, n + 1)), j * H * s, block) for j in range(k)]
+    unsafe = k >= 2 and rng.random() < 0.25
+    if unsafe:
+        windows[1] = (windows[1][0], windows[0][1], block)
+    fused = _gpu_concat(rng, s, n, H, Q, windows, block * Q, layout)
+    assert fused == (k >= 2 and not unsafe)
