@@ -29,6 +29,7 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 #include <mutex>
@@ -266,10 +267,14 @@ struct MatAttnParams {
   int ks, vs;          // K ring and V ring depths
   float sl2;           // softmax scale x log2(e)
   int B;
-  // split-KV when the query tiles alone leave SMs idle: piece sp of a query
-  // tile covers KV tiles [sp * chunk_tiles, (sp + 1) * chunk_tiles) and
-  // leaves O / l (bf16) and (m, l) for mat_combine_sm103
+  // split-KV when the query tiles alone leave SMs idle: each piece of a
+  // query tile leaves O / l (bf16) and (m, l) for mat_combine_sm103
   int splits, chunk_tiles;
+  // piece 0 covers KV tiles [0, first_tiles), piece sp >= 1 covers
+  // [first_tiles + (sp - 1) * chunk_tiles, + chunk_tiles); first_tiles =
+  // chunk_tiles unless one long and one short piece fill a partial wave
+  int first_tiles;
+  int sp_outer;  // 1: pieces slowest in the launch order (every long piece first)
   __nv_bfloat16* o_part;  // [B, splits, L, H, v]
   float* ml;              // [B, splits, L, H, 2]
 };
@@ -320,7 +325,16 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
   const int nqt = (p.L + MA_BM - 1) / MA_BM;
   const int qt = (int)(blockIdx.x % nqt);
   const int rest = (int)(blockIdx.x / nqt);
-  const int sp = rest % p.splits, h = (rest / p.splits) % p.H, b = rest / (p.splits * p.H);
+  int sp, h, b;
+  if (p.sp_outer) {
+    h = rest % p.H;
+    b = (rest / p.H) % p.B;
+    sp = rest / (p.H * p.B);
+  } else {
+    sp = rest % p.splits;
+    h = (rest / p.splits) % p.H;
+    b = rest / (p.splits * p.H);
+  }
   const int T = p.lens[b];
   const int n = p.n, v = p.v, L = p.L;
   const int l0 = qt * MA_BM;
@@ -328,8 +342,8 @@ __global__ void __launch_bounds__(MA_THREADS, 1) mat_attn_sm103(const __grid_con
   const int kv_end = T - L + l_last + 1;  // no row of the tile sees t >= kv_end
   // this CTA's KV tiles: [i0, i0 + ntiles) of the tile's visible ones; the
   // loops below count from 0, positions add tbase
-  const int i0 = sp * p.chunk_tiles;
-  const int ntiles = min((kv_end + MA_BN - 1) / MA_BN - i0, p.chunk_tiles);
+  const int i0 = sp == 0 ? 0 : p.first_tiles + (sp - 1) * p.chunk_tiles;
+  const int ntiles = min((kv_end + MA_BN - 1) / MA_BN - i0, sp == 0 ? p.first_tiles : p.chunk_tiles);
   const int tbase = i0 * MA_BN;
   if (ntiles <= 0) {
     // a piece past what the tile sees: an empty part for the combine
@@ -746,7 +760,7 @@ namespace {
 // chunk_tiles KV tiles, choosing the cut that minimises waves x (tiles per
 // piece + the fixed cost of a CTA, about four tiles) with one CTA per SM.
 struct MatSplit {
-  int splits = 1, chunk_tiles = 1;
+  int splits = 1, chunk_tiles = 1, first_tiles = 1, sp_outer = 0;
 };
 MatSplit mat_split(const Plan& p) {
   const long long units = (long long)((p.L + MA_BM - 1) / MA_BM) * p.H * p.B;
@@ -768,8 +782,36 @@ MatSplit mat_split(const Plan& p) {
   // the pieces' round trip and the combine kernel cost more than the model's
   // four tiles: cut only for a clear gain (measured: four pieces of the
   // 512/192/256 L = 1024 call at T = 8192 by the model's 5 % were 8 % slower)
-  if (best_cost * 4 > whole * 3) best.chunk_tiles = tiles;
+  if (best_cost * 4 > whole * 3) {
+    best.chunk_tiles = tiles;
+    best_cost = whole;
+  }
   best.splits = (tiles + best.chunk_tiles - 1) / best.chunk_tiles;
+  best.first_tiles = best.chunk_tiles;
+  // One partial wave (units < slots) leaves slots - units SMs idle.  Cut each
+  // unit into one long piece of a >= tiles / 2 tiles and one short piece of
+  // the rest, long pieces first: the short ones run in waves on the idle SMs
+  // while the long ones run, so the whole takes about
+  // max(a + o, ceil(units / (slots - units)) (tiles - a + o)).  Kept for a
+  // clear gain (10 % by the model; the combine kernel is one more launch).
+  if (units < slots && tiles >= 16) {
+    constexpr long long o = 4;
+    const long long short_waves = (units + (slots - units) - 1) / (slots - units);
+    long long best_a = 0, best_span = best_cost;
+    for (long long a = (tiles + 1) / 2; a < tiles; ++a) {
+      const long long span = std::max(a + o, short_waves * (tiles - a + o));
+      if (span < best_span) {
+        best_span = span;
+        best_a = a;
+      }
+    }
+    if (best_a > 0 && best_span * 10 <= best_cost * 9) {
+      best.splits = 2;
+      best.first_tiles = (int)best_a;
+      best.chunk_tiles = tiles - (int)best_a;
+      best.sp_outer = 1;
+    }
+  }
   return best;
 }
 
@@ -849,6 +891,7 @@ cudaError_t launch_fast_materialised(const Plan& p, const Args& a) {
     MatAttnParams mp{a.lens, c.page_table, c.page_size, c.max_pages, c.num_pages, c.seq_stride,
                      (__nv_bfloat16*)a.out, p.L, p.H, p.n, p.v, mr.ks, mr.vs,
                      p.scale * 1.4426950408889634f, p.B, ms.splits, ms.chunk_tiles,
+                     ms.first_tiles, ms.sp_outer,
                      (__nv_bfloat16*)ws_pieces,
                      (float*)(ws_pieces + align256_bytes(prow * p.v * 2))};
     KernelTimer kt("mat_attn_sm103", a.stream);
