@@ -847,6 +847,54 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
   cluster_wait();
 }
 
+// Per-device launch setup of the selection kernels (the opt-ins to more
+// than 48 KB of shared memory, and whether a cluster of eight 1024-thread
+// CTAs fits the device), made once per device; calls may come from several
+// threads.
+struct SelectSetup {
+  cudaError_t err = cudaSuccess;
+  bool cluster_ok = false;
+};
+SelectSetup select_setup() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  static SelectSetup setups[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    SelectSetup bad;
+    bad.err = cudaErrorInvalidDevice;
+    return bad;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    SelectSetup su;
+    su.err = cudaFuncSetAttribute(select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSelSmemWindows * (int)sizeof(float));
+    if (su.err == cudaSuccess &&
+        cudaFuncSetAttribute(select_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSelClusterSlice * (int)sizeof(float)) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kSelCluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(kSelCluster, 1, 1);
+      cfg.blockDim = dim3(kSelThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSelClusterSlice * sizeof(float);
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      su.cluster_ok =
+          cudaOccupancyMaxActiveClusters(&n, select_topk_cluster, &cfg) == cudaSuccess && n > 0;
+    }
+    cudaGetLastError();  // a device without room for the cluster is not an error
+    setups[dev] = su;
+    done[dev] = true;
+  }
+  return setups[dev];
+}
+
 }  // namespace
 
 int indexer_device_status(bool clear) {
@@ -1005,45 +1053,15 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
     KernelTimer kt("indexer_select_topk", st);
     const long long vis_max = (cache_len - 1) / kWindow + 1;
     const size_t sel_smem = vis_max <= kSelSmemWindows ? (size_t)vis_max * sizeof(float) : 0;
-    {  // the static arrays and the staged scores together pass 48 KB
-      static std::once_flag once;
-      static cudaError_t attr_err = cudaSuccess;
-      std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSelSmemWindows * (int)sizeof(float));
-      });
-      if (attr_err != cudaSuccess) {
-        set_error("CUDA error %d (%s)", (int)attr_err, cudaGetErrorString(attr_err));
-        return MLA_ERR_CUDA;
-      }
-    }
     // a cluster of eight CTAs per row when its slices fit and the device
     // can hold such a cluster; otherwise one CTA per row
+    const SelectSetup setup = select_setup();
+    if (setup.err != cudaSuccess) {
+      set_error("CUDA error %d (%s)", (int)setup.err, cudaGetErrorString(setup.err));
+      return MLA_ERR_CUDA;
+    }
+    const bool cluster_ok = setup.cluster_ok;
     const long long slice_max = ((vis_max + kSelCluster - 1) / kSelCluster + 3) & ~3LL;
-    static std::once_flag once_c;
-    static bool cluster_ok = false;
-    std::call_once(once_c, [] {
-      if (cudaFuncSetAttribute(select_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSelClusterSlice * (int)sizeof(float)) != cudaSuccess) {
-        cudaGetLastError();
-        return;
-      }
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = kSelCluster;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(kSelCluster, 1, 1);
-      cfg.blockDim = dim3(kSelThreads, 1, 1);
-      cfg.dynamicSmemBytes = kSelClusterSlice * sizeof(float);
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      cluster_ok = cudaOccupancyMaxActiveClusters(&n, select_topk_cluster, &cfg) == cudaSuccess &&
-                   n > 0;
-      cudaGetLastError();
-    });
     if (cluster_ok && slice_max <= kSelClusterSlice) {
       cudaLaunchConfig_t cfg = {};
       cudaLaunchAttribute attr[1];
