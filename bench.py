@@ -53,8 +53,8 @@ def _args():
     ap.add_argument("--shape-groups", default=None,
                     help="comma-separated names of the secondary shape groups to run (default "
                          "all: crossover_glm47_T8192, batched_paged, long_context, "
-                         "dsv3_forced_materialised, sparse_dsv3_k2048, indexer_pool_T131072, "
-                         "conv_snapshots_H8192)")
+                         "dsv3_forced_materialised, sparse_dsv3_k2048, draft_cap_dsv3_T8192, "
+                         "indexer_pool_T131072, conv_snapshots_H8192)")
     ap.add_argument("--widths", default=None,
                     help="comma-separated verify widths instead of 1,2,4,8,16 (for profiling "
                          "one width; the line then describes that workload, not the headline)")
@@ -236,7 +236,30 @@ def _shape_list():
     for T, L in ((8192, 1), (32768, 1), (32768, 4), (32768, 8)):
         out.append(dict(group="sparse_dsv3_k2048", geom=I.DSV3, L=L, lens=[T], mode="sparse",
                         page=0, topk=2048))
+    for L in range(1, DRAFT_CAP_MAX + 2):
+        out.append(dict(group="draft_cap_dsv3_T8192", geom=I.DSV3, L=L, lens=[8192],
+                        mode="auto", page=0))
     return out
+
+
+DRAFT_CAP_MAX = 16
+DRAFT_P = (0.5, 0.7, 0.8, 0.9)
+
+
+def _draft_caps(B, group):
+    """The draft cap that "Draft caps and calibration" picks from a measured
+    verify curve: verify(w) is this build's µs per layer call over w rows
+    (w = 1 .. DRAFT_CAP_MAX + 1, a cap C verifying C + 1 rows), for a few
+    acceptance rates p, with the drafter free and at a tenth of one verify."""
+    us = {e["L"]: e["us_per_call"] for e in group["calls"]}
+    curve = [us[w] for w in range(1, DRAFT_CAP_MAX + 2)]
+    caps = []
+    for p in DRAFT_P:
+        for drafter in (0.0, 0.1 * curve[0]):
+            cap, speedup = B.mla_select_draft_cap(p, curve, drafter, DRAFT_CAP_MAX)
+            caps.append({"p": p, "drafter_us": drafter, "cap": cap,
+                         "speedup": speedup[cap]})
+    return {"verify_us": curve, "caps": caps}
 
 
 def _bench_shapes(B, dev, peaks, reps, only=None):
@@ -336,6 +359,9 @@ def _bench_shapes(B, dev, peaks, reps, only=None):
             "first_L_materialised_faster": first,
             "us": {str(L): {"absorbed": v["absorbed"], "materialised": v["materialised"]}
                    for L, v in sorted(t.items())}}
+    dc = groups.get("draft_cap_dsv3_T8192")
+    if dc:
+        dc["draft_cap"] = _draft_caps(B, dc)
     if only is None or "indexer_pool_T131072" in only:
         groups["indexer_pool_T131072"] = _bench_indexer(B, dev, peaks, reps)
     if only is None or "conv_snapshots_H8192" in only:
