@@ -38,8 +38,8 @@ when a global guard fails (streams != 1, sequence != 0, p0 < 0, or a bounded
 removal p1 >= 0) nothing is kept.
 
 parity pinned: tests/test_rollback_state.py checks the ordinary path
-against a one-row-at-a-time loop written from Algorithm 5's listing of what
-each thread stores, the page's worked count (an eight-word row and three
+against a one-row-at-a-time loop of what Algorithm 5 says each thread
+stores, the page's worked count (an eight-word row and three
 three-word snapshots: 17 logical reads separately, 8 fused), every
 ValidBlock condition broken one at a time, and the stated invariant that
 every retained block is complete, exclusively owned and before the suffix.
