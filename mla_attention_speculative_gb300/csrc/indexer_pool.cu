@@ -590,18 +590,31 @@ __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restri
 }
 
 // The same selection with a row spread over a cluster of eight CTAs: CTA r
-// stages and scans windows [r * slice, (r + 1) * slice) of the row.  Each
-// digit's histogram is built in every CTA's shared memory for its own slice;
-// after a cluster barrier every CTA sums the eight histograms bin by bin
-// through distributed shared memory, so all eight take the same decision.
+// stages and scans windows [r * slice, (r + 1) * slice) of the row.  The
+// first digit (10 bits) is histogrammed in every CTA's shared memory for its
+// own slice; after a cluster barrier every CTA sums the eight histograms bin
+// by bin through distributed shared memory, so all eight take the same
+// decision.  Each CTA then compacts its slice's keys of the chosen bucket,
+// and after one more barrier every CTA gathers all eight lists (at most 2048
+// keys) and takes the last two digits (11 bits each) locally.  A bucket too
+// large to gather has those digits summed over the cluster like the first.
 // In the output pass a CTA's windows are placed after those its lower-ranked
 // peers take, from the peers' totals (one more exchange).
 constexpr int kSelCluster = 8;
 constexpr int kSelClusterSlice = kSelThreads * 32;  // windows a CTA stages, at most
+constexpr int kClD1 = 10;                           // digits of the cluster form: 10, 11, 11 bits
+constexpr int kClD2 = 11;
+constexpr int kClCand = 2048;                       // a chosen bucket gathered whole up to this
 
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_cluster_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr)
+               : "memory");
   return v;
 }
 __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
@@ -632,6 +645,16 @@ __device__ __forceinline__ void cluster_counts(const int* hist, int nbins, int (
       c[2] += (int)v[r].y;
       c[3] += (int)v[r].x;
     }
+  } else if (per == 2) {
+    const uint32_t a = smem_u32(hist + top - 1);  // bins top-1, top, 8-byte aligned
+    uint2 v[kSelCluster];
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) v[r] = ld_cluster_v2(mapa(a, r));
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) {
+      c[0] += (int)v[r].y;
+      c[1] += (int)v[r].x;
+    }
   } else {
     const uint32_t a = smem_u32(hist + top);
     uint32_t v[kSelCluster];
@@ -646,9 +669,10 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
     const float* __restrict__ scores, long long nwin, int S, long long len, int k,
     int32_t* __restrict__ win_out, int32_t* __restrict__ pos_out) {
   extern __shared__ float4 ssc4[];  // this CTA's slice of the row
-  __shared__ __align__(16) int hist_a[1 << kSelTopBits];
-  __shared__ __align__(16) int hist_b[1 << kSelLowBits];
-  __shared__ uint32_t cand[kSelCand];
+  __shared__ __align__(16) int hist_a[1 << kClD2];
+  __shared__ __align__(16) int hist_b[1 << kClD2];
+  __shared__ uint32_t cand[kClCand];      // this slice's keys of the chosen bucket
+  __shared__ uint32_t all_cand[kClCand];  // every slice's, gathered
   __shared__ uint32_t warp_sums[32];
   __shared__ int sel[3];
   __shared__ int ncand;
@@ -667,36 +691,38 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
   const float* src = scores + row * nwin + lo;
 #pragma unroll 4
   for (int i = threadIdx.x; i < nloc; i += kSelThreads) ssc[i] = src[i];
-  for (int i = threadIdx.x; i < (1 << kSelTopBits); i += kSelThreads) hist_a[i] = 0;
+  for (int i = threadIdx.x; i < (1 << kClD1); i += kSelThreads) hist_a[i] = 0;
   __syncthreads();
   const int n4 = nloc / 4, tail = 4 * n4;
 
-  // first digit: bits 31..20
+  // first digit: bits 31..22 (sign, exponent, one mantissa bit), summed over
+  // the cluster: 1024 bins, so each CTA reads 32 KB of its peers' counts
   for (int i = threadIdx.x; i < n4; i += kSelThreads) {
     const float4 v = ssc4[i];
-    atomicAdd(&hist_a[order_key(v.x) >> (32 - kSelTopBits)], 1);
-    atomicAdd(&hist_a[order_key(v.y) >> (32 - kSelTopBits)], 1);
-    atomicAdd(&hist_a[order_key(v.z) >> (32 - kSelTopBits)], 1);
-    atomicAdd(&hist_a[order_key(v.w) >> (32 - kSelTopBits)], 1);
+    atomicAdd(&hist_a[order_key(v.x) >> (32 - kClD1)], 1);
+    atomicAdd(&hist_a[order_key(v.y) >> (32 - kClD1)], 1);
+    atomicAdd(&hist_a[order_key(v.z) >> (32 - kClD1)], 1);
+    atomicAdd(&hist_a[order_key(v.w) >> (32 - kClD1)], 1);
   }
   for (int w = tail + threadIdx.x; w < nloc; w += kSelThreads)
-    atomicAdd(&hist_a[order_key(ssc[w]) >> (32 - kSelTopBits)], 1);
+    atomicAdd(&hist_a[order_key(ssc[w]) >> (32 - kClD1)], 1);
   cluster_sync();  // every slice's histogram is complete
   int c[4];
-  cluster_counts(hist_a, 1 << kSelTopBits, c);
-  find_bucket_counts(c, (1 << kSelTopBits) / kSelThreads, 1 << kSelTopBits, keff, warp_sums,
-                     sel);
-  constexpr int kShift2 = 32 - kSelTopBits - kSelLowBits;
-  constexpr uint32_t kLowMask = (1u << kSelLowBits) - 1;
-  uint32_t prefix = (uint32_t)sel[0] << (32 - kSelTopBits);
-  uint32_t mask = ~0u << (32 - kSelTopBits);
+  cluster_counts(hist_a, 1 << kClD1, c);
+  find_bucket_counts(c, 1, 1 << kClD1, keff, warp_sums, sel);
+  constexpr int kShift2 = 32 - kClD1 - kClD2;
+  constexpr uint32_t kLowMask = (1u << kClD2) - 1;
+  uint32_t prefix = (uint32_t)sel[0] << (32 - kClD1);
+  uint32_t mask = ~0u << (32 - kClD1);
   int remaining = sel[1];
   bool whole = sel[2] == remaining;
-  const bool use_list = sel[2] <= kSelCand;  // then no slice holds more than the list
+  const bool gather = sel[2] <= kClCand;  // the same decision in every CTA
 
-  // second digit: bits 19..10 of the keys in the chosen bucket
-  if (!whole) {
+  if (!whole && gather) {
+    // The bucket's keys of every slice, gathered into each CTA: the last two
+    // digits are then taken locally, with no more cluster barriers.
     hist_b[threadIdx.x] = 0;
+    hist_b[threadIdx.x + kSelThreads] = 0;
     if (threadIdx.x == 0) ncand = 0;
     __syncthreads();
     for (int i0 = threadIdx.x - lane; i0 < n4; i0 += kSelThreads) {
@@ -710,12 +736,9 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
         key[2] = order_key(v.z);
         key[3] = order_key(v.w);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          in[e] = (key[e] & mask) == prefix;
-          if (in[e]) atomicAdd(&hist_b[(key[e] >> kShift2) & kLowMask], 1);
-        }
+        for (int e = 0; e < 4; ++e) in[e] = (key[e] & mask) == prefix;
       }
-      if (use_list) append_keys(key, in, cand, &ncand);
+      append_keys(key, in, cand, &ncand);
     }
     for (int w0 = tail + threadIdx.x - lane; w0 < nloc; w0 += kSelThreads) {
       const int w = w0 + lane;
@@ -724,42 +747,105 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
       if (w < nloc) {
         key[0] = order_key(ssc[w]);
         in[0] = (key[0] & mask) == prefix;
-        if (in[0]) atomicAdd(&hist_b[(key[0] >> kShift2) & kLowMask], 1);
       }
-      if (use_list) append_keys(key, in, cand, &ncand);
+      append_keys(key, in, cand, &ncand);
     }
-    cluster_sync();
-    cluster_counts(hist_b, 1 << kSelLowBits, c);
-    find_bucket_counts(c, 1, 1 << kSelLowBits, remaining, warp_sums, sel);
+    cluster_sync();  // every slice's list is complete
+    // lane r of each warp reads slice r's count; its list starts at the
+    // exclusive prefix of the counts
+    const int cnt = lane < kSelCluster ? (int)ld_cluster_u32(mapa(smem_u32(&ncand), lane)) : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < kSelCluster; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int n_all = __shfl_sync(0xffffffffu, incl, kSelCluster - 1);
+    int offs[kSelCluster];
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) offs[r] = __shfl_sync(0xffffffffu, incl - cnt, r);
+    // at most two keys per thread; both loads are issued before either store
+    uint32_t got[kClCand / kSelThreads];
+#pragma unroll
+    for (int u = 0; u < kClCand / kSelThreads; ++u) {
+      const int j = threadIdx.x + u * kSelThreads;
+      got[u] = 0u;
+      if (j < n_all) {
+        int rr = 0, base = 0;  // the last list starting at or before j
+#pragma unroll
+        for (int r = 1; r < kSelCluster; ++r) {
+          if (j >= offs[r]) {
+            rr = r;
+            base = offs[r];
+          }
+        }
+        got[u] = ld_cluster_u32(mapa(smem_u32(cand + (j - base)), rr));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kClCand / kSelThreads; ++u) {
+      const int j = threadIdx.x + u * kSelThreads;
+      if (j < n_all) all_cand[j] = got[u];
+    }
+    __syncthreads();
+    // second digit: bits 21..11 of the gathered keys
+    for (int i = threadIdx.x; i < n_all; i += kSelThreads)
+      atomicAdd(&hist_b[(all_cand[i] >> kShift2) & kLowMask], 1);
+    __syncthreads();
+    find_bucket(hist_b, 1 << kClD2, remaining, warp_sums, sel);
     prefix |= (uint32_t)sel[0] << kShift2;
     mask |= kLowMask << kShift2;
     remaining = sel[1];
     whole = sel[2] == remaining;
-  }
-
-  // third digit: bits 9..0, in the bins of hist_a (every peer read hist_a
-  // before it arrived on the barrier that ended the second digit)
-  if (!whole) {
-    hist_a[threadIdx.x] = 0;
-    __syncthreads();
-    if (use_list) {
-      const int nc = ncand;
-      for (int i = threadIdx.x; i < nc; i += kSelThreads) {
-        const uint32_t key = cand[i];
+    if (!whole) {
+      // third digit: bits 10..0
+      hist_a[threadIdx.x] = 0;
+      hist_a[threadIdx.x + kSelThreads] = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < n_all; i += kSelThreads) {
+        const uint32_t key = all_cand[i];
         if ((key & mask) == prefix) atomicAdd(&hist_a[key & kLowMask], 1);
       }
-    } else {
+      __syncthreads();
+      find_bucket(hist_a, 1 << kClD2, remaining, warp_sums, sel);
+      prefix |= (uint32_t)sel[0];
+      mask = ~0u;
+      remaining = sel[1];
+    }
+  } else if (!whole) {
+    // A bucket too large to gather: the last two digits are summed over the
+    // cluster like the first (2048 bins each).
+    hist_b[threadIdx.x] = 0;
+    hist_b[threadIdx.x + kSelThreads] = 0;
+    __syncthreads();
+    for (int w = threadIdx.x; w < nloc; w += kSelThreads) {
+      const uint32_t key = order_key(ssc[w]);
+      if ((key & mask) == prefix) atomicAdd(&hist_b[(key >> kShift2) & kLowMask], 1);
+    }
+    cluster_sync();
+    cluster_counts(hist_b, 1 << kClD2, c);
+    find_bucket_counts(c, 2, 1 << kClD2, remaining, warp_sums, sel);
+    prefix |= (uint32_t)sel[0] << kShift2;
+    mask |= kLowMask << kShift2;
+    remaining = sel[1];
+    whole = sel[2] == remaining;
+    if (!whole) {
+      // in the bins of hist_a: every peer read them before it arrived on
+      // the barrier that ended the second digit
+      hist_a[threadIdx.x] = 0;
+      hist_a[threadIdx.x + kSelThreads] = 0;
+      __syncthreads();
       for (int w = threadIdx.x; w < nloc; w += kSelThreads) {
         const uint32_t key = order_key(ssc[w]);
         if ((key & mask) == prefix) atomicAdd(&hist_a[key & kLowMask], 1);
       }
+      cluster_sync();
+      cluster_counts(hist_a, 1 << kClD2, c);
+      find_bucket_counts(c, 2, 1 << kClD2, remaining, warp_sums, sel);
+      prefix |= (uint32_t)sel[0];
+      mask = ~0u;
+      remaining = sel[1];
     }
-    cluster_sync();
-    cluster_counts(hist_a, 1 << kSelLowBits, c);
-    find_bucket_counts(c, 1, 1 << kSelLowBits, remaining, warp_sums, sel);
-    prefix |= (uint32_t)sel[0];
-    mask = ~0u;
-    remaining = sel[1];
   }
 
   // output: thread t marks windows [t * run, (t + 1) * run) of the slice
