@@ -422,6 +422,25 @@ def _bench_indexer(B, dev, peaks, reps):
     byts = W * d * 4 + 8 * W * 4
     sel["score_gbs"] = byts / (sel["indexer_score_windows_us"] * 1e-6) / 1e9
     sel["score_hbm_frac"] = sel["score_gbs"] / peaks["hbm_gbs"]
+    # the whole call (scoring, then the selection chained to it): a CUDA graph
+    # of calls over the rotating pools, events around its replays
+    ncall = 2 * copies
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(ncall):
+            B.mla_indexer_select(q, pooled[i % copies], T, k)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per = []
+    for _ in range(5):
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1) * 1e3 / ncall)
+    sel["call_us"] = sorted(per)[len(per) // 2]
+    del graph
     out["calls"].append(sel)
     del keys, pooled
     torch.cuda.empty_cache()

@@ -159,6 +159,8 @@ __global__ void __launch_bounds__(kD128Threads) score_windows_d128(
     bulk_load(smem_u32(tile), pooled + ((long long)b * cap + c0) * 128, (uint32_t)nw * 512u, bar);
   }
   __syncthreads();  // the barrier is initialised before anyone waits on it
+  // the selection may be placed now; it waits for this grid before it reads
+  pdl_launch_dependents();
   const float4* qb = (const float4*)(q + (long long)b * S * 128) + lane;
   float4 qv[8];
 #pragma unroll
@@ -233,6 +235,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_windows(const float* __re
   const float4* qb = (const float4*)(q + (long long)b * S * dim);
   for (int i = threadIdx.x; i < S * d4; i += kScoreThreads) sq4[i] = qb[i];
   __syncthreads();
+  pdl_launch_dependents();
   const bool h4 = g & 4, h2 = g & 2, h1 = g & 1;
   for (int s0 = 0; s0 < S; s0 += 8) {
     float acc[8];
@@ -409,6 +412,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restri
   const long long row = (long long)b * S + s;
   const float* src = scores + row * nwin;
   const bool staged = vis <= kSelSmemWindows;
+  pdl_wait();  // the scores come from the preceding kernel
   if (staged) {
     float* ssc = (float*)ssc4;
     int w = threadIdx.x;
@@ -689,6 +693,7 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
   const int nloc = min(vis, lo + slice) - lo;
   float* ssc = (float*)ssc4;
   const float* src = scores + row * nwin + lo;
+  pdl_wait();  // the scores come from the preceding kernel
 #pragma unroll 4
   for (int i = threadIdx.x; i < nloc; i += kSelThreads) ssc[i] = src[i];
   for (int i = threadIdx.x; i < (1 << kClD1); i += kSelThreads) hist_a[i] = 0;
@@ -1149,24 +1154,38 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
     const bool cluster_ok = setup.cluster_ok;
     const long long slice_max = ((vis_max + kSelCluster - 1) / kSelCluster + 3) & ~3LL;
     if (cluster_ok && slice_max <= kSelClusterSlice) {
+      // chained to the scoring kernel (programmatic dependent launch)
       cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
+      cudaLaunchAttribute attr[2];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = kSelCluster;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
       cfg.gridDim = dim3(kSelCluster, new_tokens, batch);
       cfg.blockDim = dim3(kSelThreads, 1, 1);
       cfg.dynamicSmemBytes = (size_t)slice_max * sizeof(float);
       cfg.stream = st;
       cfg.attrs = attr;
-      cfg.numAttrs = 1;
+      cfg.numAttrs = 2;
       cudaLaunchKernelEx(&cfg, select_topk_cluster, (const float*)scores, (long long)nwin,
                          (int)new_tokens, (long long)cache_len, (int)k_windows, windows_out,
                          positions_out);
     } else {
-      select_topk<<<dim3(new_tokens, batch), kSelThreads, sel_smem, st>>>(
-          scores, nwin, new_tokens, cache_len, k_windows, windows_out, positions_out);
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.gridDim = dim3(new_tokens, batch, 1);
+      cfg.blockDim = dim3(kSelThreads, 1, 1);
+      cfg.dynamicSmemBytes = sel_smem;
+      cfg.stream = st;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cudaLaunchKernelEx(&cfg, select_topk, (const float*)scores, (long long)nwin,
+                         (int)new_tokens, (long long)cache_len, (int)k_windows, windows_out,
+                         positions_out);
     }
   }
   const cudaError_t e = cudaGetLastError();
