@@ -54,7 +54,7 @@ def _args():
                     help="comma-separated names of the secondary shape groups to run (default "
                          "all: crossover_glm47_T8192, batched_paged, long_context, "
                          "dsv3_forced_materialised, sparse_dsv3_k2048, draft_cap_dsv3_T8192, "
-                         "indexer_pool_T131072, conv_snapshots_H8192)")
+                         "indexer_pool_T131072, sparse_step_dsv3_T32768, conv_snapshots_H8192)")
     ap.add_argument("--widths", default=None,
                     help="comma-separated verify widths instead of 1,2,4,8,16 (for profiling "
                          "one width; the line then describes that workload, not the headline)")
@@ -364,6 +364,8 @@ def _bench_shapes(B, dev, peaks, reps, only=None):
         dc["draft_cap"] = _draft_caps(B, dc)
     if only is None or "indexer_pool_T131072" in only:
         groups["indexer_pool_T131072"] = _bench_indexer(B, dev, peaks, reps)
+    if only is None or "sparse_step_dsv3_T32768" in only:
+        groups["sparse_step_dsv3_T32768"] = _bench_sparse_step(B, dev, reps)
     if only is None or "conv_snapshots_H8192" in only:
         groups["conv_snapshots_H8192"] = _bench_snapshots(B, dev, peaks, reps)
     return {"groups": groups, "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
@@ -444,6 +446,62 @@ def _bench_indexer(B, dev, peaks, reps):
     out["calls"].append(sel)
     del keys, pooled
     torch.cuda.empty_cache()
+    return out
+
+
+def _bench_sparse_step(B, dev, reps):
+    """The sparse model's verify step for one DSV3-like layer at a 32K cache:
+    the indexer's incremental pool update for the L new tokens, the top-512
+    window selection (2048 positions per verify row), and the sparse verify
+    over those positions, as one CUDA graph of steps over rotating layers;
+    events around its replays.  L = 1 and 4."""
+    import torch
+    from mla_attention_speculative_gb300.inputs import DSV3, make_case
+    T, d, kw = 32768, 128, 512
+    out = {"geometry": f"DSV3-like H=128 512/128/128, T = {T}; indexer keys bf16 [1, T, {d}], "
+                       f"top {kw} windows = {4 * kw} positions", "calls": []}
+    g = torch.Generator(device=dev).manual_seed(5200)
+    layers = 4
+    for L in (1, 4):
+        cases = [make_case(DSV3, L, [T], seed=5300 + L * 10 + i, device=dev)
+                 for i in range(layers)]
+        keys = [torch.randn(1, T, d, generator=g, device=dev).to(torch.bfloat16)
+                for _ in range(layers)]
+        pooled = [torch.zeros((1, T // 4, d), device=dev) for _ in range(layers)]
+        for i in range(layers):
+            B.mla_indexer_pool_update(keys[i], T, T, pooled[i], B.IndexerPoolState())
+        qi = torch.randn(1, L, d, generator=g, device=dev)
+        lens_dev = torch.tensor([T], dtype=torch.int32, device=dev)
+
+        def step(i):
+            c = cases[i % layers]
+            st = B.IndexerPoolState()
+            st.length, st.batch, st.dim = T - L, 1, d   # the pool before this step
+            B.mla_indexer_pool_update(keys[i % layers], T, L, pooled[i % layers], st)
+            _, pos = B.mla_indexer_select(qi, pooled[i % layers], T, kw)
+            B.mla_verify_attention_sparse(c.q_nope, c.q_rope, c.c_kv, c.k_rope, c.W_UK, c.W_UV,
+                                          [T], pos, cache_lens_dev=lens_dev)
+        for i in range(layers):
+            step(i)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(2 * layers):
+                step(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        per = []
+        for _ in range(max(5, reps)):
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) * 1e3 / (2 * layers))
+        out["calls"].append({"L": L, "us_per_step": sorted(per)[len(per) // 2],
+                             "launches_per_step": 6})
+        del graph, cases, keys, pooled
+        torch.cuda.empty_cache()
     return out
 
 

@@ -427,6 +427,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk(const float* __restri
     __syncthreads();
     src = ssc;
   }
+  // a following call may start its independent loads; it waits for this grid
+  pdl_launch_dependents();
   // staged rows are read as float4 up to n4, the rest one key at a time
   const int n4 = staged ? vis / 4 : 0;
   const int tail = 4 * n4;
@@ -698,6 +700,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
   for (int i = threadIdx.x; i < nloc; i += kSelThreads) ssc[i] = src[i];
   for (int i = threadIdx.x; i < (1 << kClD1); i += kSelThreads) hist_a[i] = 0;
   __syncthreads();
+  // a following call may start its independent loads; it waits for this grid
+  pdl_launch_dependents();
   const int n4 = nloc / 4, tail = 4 * n4;
 
   // first digit: bits 31..22 (sign, exponent, one mantissa bit), summed over
