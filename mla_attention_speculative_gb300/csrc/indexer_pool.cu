@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(256) pool_windows(const T* __restrict__ keys, 
                                                     long long w0, long long w1,
                                                     float* __restrict__ pooled, long long cap,
                                                     bool vec) {
+  // the scoring may be placed at once; it waits for this grid before it reads
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long w = w0 + (long long)blockIdx.x * 8 + warp;
   const int b = blockIdx.y;
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(kD128Threads) score_windows_d128(
   const long long c0 = (long long)blockIdx.x * kD128CtaWindows;
   const int nw = (int)min((long long)kD128CtaWindows, nwin - c0);
   const uint32_t bar = smem_u32(&full);
+  pdl_wait();  // the pooled keys and the queries may come from the preceding kernel
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
@@ -225,6 +228,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_windows(const float* __re
   const long long w = (long long)blockIdx.x * kScoreWinPerCta + (threadIdx.x / kScoreLanes);
   const int nv = dim / (4 * kScoreLanes);
   const bool live = w < nwin;
+  pdl_wait();  // the pooled keys and the queries may come from the preceding kernel
   // the key first: its loads are in flight while the queries are staged
   const float4* pk = (const float4*)(pooled + ((long long)b * cap + (live ? w : 0)) * dim) + g;
   float4 kv[kScoreMaxVec];
@@ -1134,14 +1138,26 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
   float* scores = (float*)workspace;
   {
     KernelTimer kt("indexer_score_windows", st);
+    // chained to the preceding kernel (programmatic dependent launch)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (dim == 128) {
-      const dim3 grid((unsigned)((nwin + kD128CtaWindows - 1) / kD128CtaWindows), batch);
-      score_windows_d128<<<grid, kD128Threads, kD128CtaWindows * 512, st>>>(
-          q, pooled, pooled_windows_cap, new_tokens, nwin, scores);
+      cfg.gridDim = dim3((unsigned)((nwin + kD128CtaWindows - 1) / kD128CtaWindows), batch);
+      cfg.blockDim = dim3(kD128Threads);
+      cfg.dynamicSmemBytes = kD128CtaWindows * 512;
+      cudaLaunchKernelEx(&cfg, score_windows_d128, q, pooled, (long long)pooled_windows_cap,
+                         (int)new_tokens, (long long)nwin, scores);
     } else {
-      const dim3 grid((unsigned)((nwin + kScoreWinPerCta - 1) / kScoreWinPerCta), batch);
-      score_windows<<<grid, kScoreThreads, (size_t)new_tokens * dim * sizeof(float), st>>>(
-          q, pooled, pooled_windows_cap, dim, new_tokens, nwin, scores);
+      cfg.gridDim = dim3((unsigned)((nwin + kScoreWinPerCta - 1) / kScoreWinPerCta), batch);
+      cfg.blockDim = dim3(kScoreThreads);
+      cfg.dynamicSmemBytes = (size_t)new_tokens * dim * sizeof(float);
+      cudaLaunchKernelEx(&cfg, score_windows, q, pooled, (long long)pooled_windows_cap,
+                         (int)dim, (int)new_tokens, (long long)nwin, scores);
     }
   }
   {
