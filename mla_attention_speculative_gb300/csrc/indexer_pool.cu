@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(256) pool_windows(const T* __restrict__ keys, 
                                                     bool vec) {
   // the scoring may be placed at once; it waits for this grid before it reads
   pdl_launch_dependents();
+  pdl_wait();  // the keys may come from the preceding kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long w = w0 + (long long)blockIdx.x * 8 + warp;
   const int b = blockIdx.y;
@@ -1058,15 +1059,26 @@ extern "C" mla_status_t mla_indexer_pool_update(const void* keys, int32_t dtype,
     const bool vec = (dim / 32) % 4 == 0 && key_row_stride % 4 == 0 &&
                      (uintptr_t)keys % (4 * esz) == 0 && (uintptr_t)pooled % 16 == 0;
     KernelTimer kt("indexer_pool_windows", st);
+    // chained to the preceding kernel (programmatic dependent launch)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const long long len = cache_len, first = w0, last = nwin, cap = pooled_windows_cap;
     if (dtype == MLA_DTYPE_BF16)
-      pool_windows<__nv_bfloat16><<<grid, 256, 0, st>>>(
-          (const __nv_bfloat16*)keys, key_row_stride, seq_stride_rows, dim, cache_len, w0, nwin,
-          pooled, pooled_windows_cap, vec);
+      e = cudaLaunchKernelEx(&cfg, pool_windows<__nv_bfloat16>, (const __nv_bfloat16*)keys,
+                             (long long)key_row_stride, (long long)seq_stride_rows, (int)dim, len,
+                             first, last, pooled, cap, vec);
     else
-      pool_windows<float><<<grid, 256, 0, st>>>((const float*)keys, key_row_stride,
-                                                 seq_stride_rows, dim, cache_len, w0, nwin,
-                                                 pooled, pooled_windows_cap, vec);
-    e = cudaGetLastError();
+      e = cudaLaunchKernelEx(&cfg, pool_windows<float>, (const float*)keys,
+                             (long long)key_row_stride, (long long)seq_stride_rows, (int)dim, len,
+                             first, last, pooled, cap, vec);
+    if (e == cudaSuccess) e = cudaGetLastError();
   }
   if (e != cudaSuccess) {
     set_error("CUDA error %d (%s)", (int)e, cudaGetErrorString(e));
