@@ -788,18 +788,25 @@ MatSplit mat_split(const Plan& p) {
   }
   best.splits = (tiles + best.chunk_tiles - 1) / best.chunk_tiles;
   best.first_tiles = best.chunk_tiles;
-  // One partial wave (units < slots) leaves slots - units SMs idle.  Cut each
-  // unit into one long piece of a >= tiles / 2 tiles and one short piece of
-  // the rest, long pieces first: the short ones run in waves on the idle SMs
-  // while the long ones run, so the whole takes about
-  // max(a + o, ceil(units / (slots - units)) (tiles - a + o)).  Kept for a
-  // clear gain (10 % by the model; the combine kernel is one more launch).
-  if (units < slots && tiles >= 16) {
+  // A partial last wave leaves SMs idle.  Cut each unit into one long piece
+  // of a >= tiles / 2 tiles and one short piece of the rest, long pieces
+  // launched first: the long ones take W = ceil(units / slots) waves of
+  // a + o, and the short ones (tiles - a + o each) run on the SMs the last
+  // long wave leaves idle, any that do not fit there in further waves after.
+  // Kept for a clear gain (10 % by the model; the combine kernel is one more
+  // launch).
+  const long long idle = (slots - units % slots) % slots;
+  if (idle > 0 && tiles >= 16) {
     constexpr long long o = 4;
-    const long long short_waves = (units + (slots - units) - 1) / (slots - units);
+    const long long W = (units + slots - 1) / slots;
     long long best_a = 0, best_span = best_cost;
     for (long long a = (tiles + 1) / 2; a < tiles; ++a) {
-      const long long span = std::max(a + o, short_waves * (tiles - a + o));
+      const long long piece = tiles - a + o;
+      // short pieces that fit beside the last long wave: idle SMs, each
+      // running a + o worth of them
+      const long long fit = idle * ((a + o) / piece);
+      const long long rest = units > fit ? units - fit : 0;
+      const long long span = W * (a + o) + ((rest + slots - 1) / slots) * piece;
       if (span < best_span) {
         best_span = span;
         best_a = a;
