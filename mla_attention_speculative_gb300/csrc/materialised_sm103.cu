@@ -660,6 +660,14 @@ __global__ void __launch_bounds__(32 * MC_ROWS)
   const int row = blockIdx.x * MC_ROWS + warp;
   if (row >= rows) return;
   const int b = row / LH, r = row - b * LH;
+  // the first columns' piece loads go out before the weights are known: they
+  // do not depend on them (an empty piece is read, never added)
+  const int c0 = lane * 8;
+  uint4 x[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j < splits && c0 < v)
+      x[j] = *(const uint4*)(o_part + (((size_t)b * splits + j) * LH + r) * v + c0);
   float2 e = make_float2(-FLT_MAX, 0.f);
   if (lane < splits) e = *(const float2*)(ml + (((size_t)b * splits + lane) * LH + r) * 2);
   float M = e.y > 0.f ? e.x : -FLT_MAX;
@@ -668,17 +676,27 @@ __global__ void __launch_bounds__(32 * MC_ROWS)
   float den = w;
   for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  for (int c = lane * 8; c < v; c += 256) {
+  for (int c = c0; c < v; c += 256) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < splits; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
-      if (ws == 0.f) continue;  // an empty piece: its row was never written
-      const uint4 x = *(const uint4*)(o_part + (((size_t)b * splits + s) * LH + r) * v + c);
-      const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+    for (int s0 = 0; s0 < splits; s0 += 4) {
+      // up to four pieces' loads in flight before any of them is used
+      if (c != c0 || s0 != 0) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc[2 * k] = fmaf(ws, __uint_as_float(u[k] << 16), acc[2 * k]);
-        acc[2 * k + 1] = fmaf(ws, __uint_as_float(u[k] & 0xffff0000u), acc[2 * k + 1]);
+        for (int j = 0; j < 4; ++j)
+          if (s0 + j < splits)
+            x[j] = *(const uint4*)(o_part + (((size_t)b * splits + s0 + j) * LH + r) * v + c);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (s0 + j >= splits) break;
+        const float ws = __shfl_sync(0xffffffffu, w, s0 + j);
+        if (ws == 0.f) continue;
+        const uint32_t u[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] = fmaf(ws, __uint_as_float(u[k] << 16), acc[2 * k]);
+          acc[2 * k + 1] = fmaf(ws, __uint_as_float(u[k] & 0xffff0000u), acc[2 * k + 1]);
+        }
       }
     }
     *(uint4*)(out + (size_t)row * v + c) =
