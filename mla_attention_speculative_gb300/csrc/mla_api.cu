@@ -129,6 +129,30 @@ static bool lens_ok(const int32_t* lens, int32_t batch, int32_t L) {
 
 static constexpr int kGenericRowsPerCTA = 4; // one warp per query row
 
+// Finish time of one sequence's split-KV clusters on `slots` cluster slots,
+// each cluster starting on the slot that frees first, in launch order (piece
+// index outermost): (S - 1) x R pieces of c KV tiles, then R pieces of the
+// tail, each costing its tiles plus o.  After the full pieces, P - r slots
+// are free at q A and r at (q + 1) A (F = q P + r full pieces of cost A); the
+// tail pieces go to whichever group frees first, a group's worth at a time.
+int64_t pieces_makespan(int64_t R, int64_t klen, int64_t c, int64_t slots, int64_t o) {
+  const int64_t S = (klen + c - 1) / c;
+  const int64_t A = c + o, Bt = klen - (S - 1) * c + o;
+  const int64_t F = (S - 1) * R, q = F / slots, r = F % slots;
+  int64_t t1 = q * A, n1 = slots - r, t2 = (q + 1) * A, n2 = r;
+  int64_t span = r > 0 ? t2 : t1, left = R;
+  while (left > 0) {
+    const bool first = n2 == 0 || t1 <= t2;
+    int64_t& t = first ? t1 : t2;
+    const int64_t n = first ? n1 : n2;
+    const int64_t take = left < n ? left : n;
+    left -= take;
+    span = span > t + Bt ? span : t + Bt;
+    t += Bt;
+  }
+  return span;
+}
+
 int device_sm_count() {
   constexpr int kDefault = 152;  // GB300: 2 dies x 76 SMs
   constexpr int kMaxDevices = 64;
@@ -252,6 +276,24 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
         best_cost = cost;
         ct = c;
       }
+    }
+    // One sequence: the clusters launch piece index outermost, so every row
+    // tile's short last piece comes last and can run in the gaps the full
+    // pieces leave.  Score a few shorter pieces by that list schedule; keep
+    // at most 64 pieces, which the fused merge takes.
+    if (batch == 1) {
+      const int64_t klen = (lens[0] + 63) / 64;
+      int64_t best_c = ct;
+      int64_t best_span = pieces_makespan(row_tiles, klen, ct, slots, kClusterOverhead);
+      for (int64_t c = ct - 1; c >= 1 && c >= ct - 8; --c) {
+        if ((klen + c - 1) / c > 64) break;
+        const int64_t span = pieces_makespan(row_tiles, klen, c, slots, kClusterOverhead);
+        if (span < best_span) {
+          best_span = span;
+          best_c = c;
+        }
+      }
+      ct = best_c;
     }
     f.chunk = (int)(ct * 64);
     f.splits = (int)((p->Tmax + f.chunk - 1) / f.chunk);
