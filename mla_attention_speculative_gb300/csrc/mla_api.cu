@@ -277,12 +277,15 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
         ct = c;
       }
     }
-    // One sequence: the clusters launch piece index outermost, so every row
-    // tile's short last piece comes last and can run in the gaps the full
-    // pieces leave.  Score a few shorter pieces by that list schedule; keep
-    // at most 64 pieces, which the fused merge takes.
-    if (batch == 1) {
-      const int64_t klen = (lens[0] + 63) / 64;
+    // One sequence whose pieces fit one wave: the clusters launch piece index
+    // outermost, so every row tile's short last piece comes last and can run
+    // in the gaps the full pieces leave.  Score a few shorter pieces by that
+    // list schedule; keep at most 64 pieces, which the fused merge takes.
+    // (Plans of several waves keep the wave model: the schedule below is too
+    // coarse for them.)
+    const int64_t klen0 = (lens[0] + 63) / 64;
+    if (batch == 1 && row_tiles * ((klen0 + ct - 1) / ct) <= slots) {
+      const int64_t klen = klen0;
       int64_t best_c = ct;
       int64_t best_span = pieces_makespan(row_tiles, klen, ct, slots, kClusterOverhead);
       for (int64_t c = ct - 1; c >= 1 && c >= ct - 8; --c) {
