@@ -432,8 +432,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
       const int l = row0 / p.H;
       const int last_t = T - p.L + l;
       const int32_t* list = p.topk + ((size_t)b * p.L + l) * p.topk_k;
+      // list entry of row lane + 32 u of tile i, or -1 past the piece
+      auto entry = [&](int i, int u) -> int {
+        const int j = kv0 + i * BN + lane + 32 * u;
+        return (i < ntiles && j < kv1) ? list[j] : -1;
+      };
+      // the entries of the next four tiles are loaded ahead of their copies
+      // (in rotating registers), so a tile's rows are known when its turn comes
+      int e0a = entry(0, 0), e0b = entry(0, 1), e1a = entry(1, 0), e1b = entry(1, 1);
+      int e2a = entry(2, 0), e2b = entry(2, 1), e3a = entry(3, 0), e3b = entry(3, 1);
       for (int i = 0; i < ntiles; ++i) {
         const int s = i % STAGES;
+        const int ta = e0a, tb = e0b;
+        e0a = e1a;
+        e0b = e1b;
+        e1a = e2a;
+        e1b = e2b;
+        e2a = e3a;
+        e2b = e3b;
+        e3a = entry(i + 4, 0);
+        e3b = entry(i + 4, 1);
         if (i >= STAGES) {
           if (lane == 0) wait_or_fail(ok, bar(B_KVEMPTY + s), ((i / STAGES) - 1) & 1, 10);
           ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
@@ -444,8 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ATTN_THREADS, 1)
         long long crow[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int j = kv0 + i * BN + lane + 32 * u;
-          const int t = j < kv1 ? list[j] : -1;
+          const int t = u == 0 ? ta : tb;
           crow[u] = -1;
           if (t >= 0 && t <= last_t) {
             if (p.page_table) {
