@@ -580,11 +580,11 @@ KERNEL_SOURCES = {
     "generic_absorbed_attention": ["generic_kernels.cu"],
     "generic_fold": ["generic_kernels.cu"],
     "generic_combine_unembed": ["generic_kernels.cu"],
-    "fold_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
-    "absorbed_attn_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
-    "unembed_merge_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
-    "merge_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
-    "unembed_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh"],
+    "fold_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh", "mla_api.cu"],
+    "absorbed_attn_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh", "mla_api.cu"],
+    "unembed_merge_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh", "mla_api.cu"],
+    "merge_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh", "mla_api.cu"],
+    "unembed_sm103": ["absorbed_sm103.cu", "sm103_ptx.cuh", "mla_api.cu"],
     "expand_sm103": ["materialised_sm103.cu", "sm103_ptx.cuh"],
     "mat_attn_sm103": ["materialised_sm103.cu", "sm103_ptx.cuh"],
 }

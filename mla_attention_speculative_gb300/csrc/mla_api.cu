@@ -296,7 +296,21 @@ static mla_status_t make_plan(const mla_geometry_t* g, int32_t batch, int32_t L,
           best_c = c;
         }
       }
-      ct = best_c;
+      // A length that divides the cache evenly leaves no short last piece:
+      // every cluster ends together, which the schedule above (a flat
+      // overhead per piece) under-rates by about a tile or two.  Take the
+      // best such length at or above the choice when it scores within two
+      // (no more pieces than the choice, so still one wave).
+      int64_t even_c = 0, even_span = 0;
+      for (int64_t c = best_c; c <= klen; ++c) {
+        if (klen % c != 0) continue;
+        const int64_t span = pieces_makespan(row_tiles, klen, c, slots, kClusterOverhead);
+        if (span <= best_span + 2 && (even_c == 0 || span < even_span)) {
+          even_span = span;
+          even_c = c;
+        }
+      }
+      ct = even_c > 0 ? even_c : best_c;
     }
     f.chunk = (int)(ct * 64);
     f.splits = (int)((p->Tmax + f.chunk - 1) / f.chunk);
