@@ -19,10 +19,11 @@
 //   pool_windows        one warp per window: four key rows read once (as
 //                       vectors), summed in a fixed order, scaled by 1/count,
 //                       stored as fp32
-//   score_windows_d128  each window's pooled key read once (a bulk copy per 64
-//                       windows) and dotted with every new token's query;
-//                       partial sums folded by a reduce-scatter over the lanes
-//                       (score_windows: the same for dims other than 128)
+//   score_windows_d128  each window's pooled key read once (TMA tensor copies
+//                       of 64 windows, 128-byte swizzle) and dotted with every
+//                       new token's query, one lane per window
+//                       (score_windows: eight lanes per window, for dims
+//                       other than 128)
 //   select_topk_cluster a row (one new token) spread over a cluster of eight
 //                       CTAs: a radix select (12, 10, 10-bit digits) of the
 //                       k-th largest score over the windows the token may see,
@@ -36,6 +37,7 @@
 
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
+#include "tma_host.h"
 
 namespace mla {
 using namespace sm103;
@@ -115,102 +117,122 @@ __global__ void __launch_bounds__(256) pool_windows(const T* __restrict__ keys, 
 
 // scores[b, s, w] = q[b, s, :] . pooled[b, w, :] for w < nwin.
 //
-// dim = 128 (score_windows_d128): a CTA per 64 windows.  One bulk copy (TMA,
-// completing on an mbarrier) brings the 64 pooled keys (32 KB, contiguous)
-// into shared memory, so every CTA's whole tile is requested at once; the
-// queries are read meanwhile, lane l holding the 16-byte piece l of each of
-// eight queries in registers.  Each warp then takes 16 windows, four at a
-// time: lane l reads piece l of each window (a warp reads a window's 512 bytes
-// in one instruction), which gives it 4 x 8 partial sums; a reduce-scatter
-// over the 32 lanes (exchanges at distance 16, 8, 4, 2, 1, each halving the
-// values a lane carries) leaves lane l with the whole score of window
-// (l >> 3) & 3 of the four and query l & 7 of the group.
+// dim = 128 (score_windows_d128): a CTA of eight warps per 64 windows.  Four
+// TMA tensor copies, one per 32 dims (128 bytes of each window), bring the 64
+// pooled keys into shared memory with the 128-byte swizzle, each completing
+// on its own mbarrier.  Warp (x, half) takes box x of windows
+// [32 half, 32 half + 32), one lane per window, and starts as soon as its box
+// lands: each lane accumulates its window's partial dot products over those
+// 32 dims with eight queries at a time in registers, dims in order, with no
+// exchange between lanes.  The queries sit in shared memory (padded with zeros
+// to a multiple of eight) and are read as broadcasts; boxes 1..3 leave their
+// partial sums in shared memory and the box-0 warps add them, in box order,
+// and write each query's 32 scores as one coalesced row.  The swizzle puts
+// 16-byte piece c of window row r at piece c ^ (r & 7) of its 128-byte row,
+// so the eight lanes of each shared-memory phase read eight different bank
+// groups.
 //
 // Other dims (score_windows): eight lanes per window, lane g holding the
 // 16-byte pieces g, g + 8, ... of the key; the queries are staged in shared
-// memory, and the eight partial sums are folded the same way over eight lanes.
-constexpr int kD128WarpWindows = 16;
-constexpr int kD128Threads = 128;
-constexpr int kD128CtaWindows = (kD128Threads / 32) * kD128WarpWindows;
+// memory, and the eight partial sums are folded over the eight lanes by a
+// reduce-scatter (exchanges at distance 4, 2, 1).
+constexpr int kD128CtaWindows = 64;
+constexpr int kD128Boxes = 4;  // 32 dims (128 bytes) each
+constexpr int kD128Threads = kD128Boxes * kD128CtaWindows;  // one warp per (box, 32 windows)
+constexpr int kD128BoxBytes = kD128CtaWindows * 128;
+constexpr int kD128RedBytes = (kD128Boxes - 1) * 8 * kD128CtaWindows * 4;
 constexpr int kScoreThreads = 256;
 constexpr int kIndexerWaitSite = 70;
 
 __device__ int g_indexer_status = 0;
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst), "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
+// Shared memory of score_windows_d128 for S new tokens: the key boxes
+// (1024-byte aligned for the swizzle), the partial sums of boxes 1..3, then
+// the queries padded to eight.
+__host__ __device__ constexpr int d128_smem_bytes(int S) {
+  return 1024 + kD128Boxes * kD128BoxBytes + kD128RedBytes + ((S + 7) / 8) * 8 * 512;
 }
 
 __global__ void __launch_bounds__(kD128Threads) score_windows_d128(
-    const float* __restrict__ q, const float* __restrict__ pooled, long long cap, int S,
+    const __grid_constant__ CUtensorMap tm_keys, const float* __restrict__ q, int S,
     long long nwin, float* __restrict__ scores) {
-  extern __shared__ float4 tile[];  // [kD128CtaWindows][32]
-  __shared__ __align__(8) uint64_t full;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // offsets from the shared array itself keep every access a shared-memory one
+  uint8_t* keys = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  float* red = (float*)(keys + kD128Boxes * kD128BoxBytes);      // [box - 1][8][64]
+  float4* sq = (float4*)(keys + kD128Boxes * kD128BoxBytes + kD128RedBytes);  // [S8][32]
+  __shared__ __align__(8) uint64_t full[kD128Boxes];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int x = warp >> 1;                   // this warp's box (dims 32x .. 32x + 31)
+  const int r = (warp & 1) * 32 + lane;      // this lane's window row in the tile
   const int b = blockIdx.y;
   const long long c0 = (long long)blockIdx.x * kD128CtaWindows;
-  const int nw = (int)min((long long)kD128CtaWindows, nwin - c0);
-  const uint32_t bar = smem_u32(&full);
+  const long long w = c0 + r;
+  const int S8 = (S + 7) & ~7;
   pdl_wait();  // the pooled keys and the queries may come from the preceding kernel
   if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+    for (int i = 0; i < kD128Boxes; ++i) mbar_init(smem_u32(&full[i]), 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar, (uint32_t)nw * 512u);
-    bulk_load(smem_u32(tile), pooled + ((long long)b * cap + c0) * 128, (uint32_t)nw * 512u, bar);
+    for (int i = 0; i < kD128Boxes; ++i) {
+      const uint32_t bar = smem_u32(&full[i]);
+      mbar_arrive_expect_tx(bar, kD128BoxBytes);
+      // rows past the pool's capacity come back as zeros; rows past nwin are
+      // scored but not stored
+      tma_load_3d(smem_u32(keys + i * kD128BoxBytes), &tm_keys, bar, 32 * i, (int)c0, b);
+    }
   }
-  __syncthreads();  // the barrier is initialised before anyone waits on it
+  // the queries of this sequence, staged while the keys arrive
+  const float4* qb = (const float4*)(q + (long long)b * S * 128);
+  for (int i = threadIdx.x; i < S8 * 32; i += kD128Threads)
+    sq[i] = i < S * 32 ? __ldg(qb + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();  // the barriers are initialised and the queries staged
   // the selection may be placed now; it waits for this grid before it reads
   pdl_launch_dependents();
-  const float4* qb = (const float4*)(q + (long long)b * S * 128) + lane;
-  float4 qv[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) qv[j] = j < S ? __ldg(qb + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
-  if (!mbar_wait(bar, 0)) {
-    // the copy is still owed: record it, give it one more bounded wait, leave
-    if (threadIdx.x == 0) atomicCAS(&g_indexer_status, 0, kIndexerWaitSite);
-    mbar_wait(bar, 0);
-    return;
+  if (!mbar_wait(smem_u32(&full[x]), 0)) {
+    // the copy is still owed: record it (the call's scores are then not to be
+    // used, and the status word says so) and give it one more bounded wait, as
+    // the tile must outlive it; the warp still takes part in the barriers below
+    if (lane == 0) atomicCAS(&g_indexer_status, 0, kIndexerWaitSite);
+    mbar_wait(smem_u32(&full[x]), 0);
   }
-  const int wl0 = warp * kD128WarpWindows;  // this warp's first window in the tile
+  const uint8_t* row = keys + x * kD128BoxBytes + r * 128;
   for (int s0 = 0; s0 < S; s0 += 8) {
-    if (s0 > 0) {
+    float acc[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        qv[j] = s0 + j < S ? __ldg(qb + 32 * (s0 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    const float4* qx = sq + s0 * 32 + x * 8;
 #pragma unroll
-    for (int c = 0; c < kD128WarpWindows; c += 4) {
-      if (wl0 + c >= nw) break;  // warp-uniform
-      float a[32];  // a[i * 8 + j]: window wl0 + c + i, query s0 + j
+    for (int c = 0; c < 8; ++c) {
+      const float4 kv = *(const float4*)(row + ((c ^ (r & 7)) << 4));
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 kv = tile[(wl0 + c + i) * 32 + lane];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float t = kv.x * qv[j].x;
-          t = fmaf(kv.y, qv[j].y, t);
-          t = fmaf(kv.z, qv[j].z, t);
-          t = fmaf(kv.w, qv[j].w, t);
-          a[i * 8 + j] = t;
-        }
+      for (int j = 0; j < 8; ++j) {
+        const float4 qv = qx[j * 32 + c];
+        acc[j] = fmaf(kv.x, qv.x, acc[j]);
+        acc[j] = fmaf(kv.y, qv.y, acc[j]);
+        acc[j] = fmaf(kv.z, qv.z, acc[j]);
+        acc[j] = fmaf(kv.w, qv.w, acc[j]);
       }
-#pragma unroll
-      for (int d = 16, n = 32; d >= 1; d >>= 1, n >>= 1) {
-        const bool hi = lane & d;
-#pragma unroll
-        for (int t = 0; t < n / 2; ++t) {
-          const float send = hi ? a[t] : a[t + n / 2];
-          a[t] = (hi ? a[t + n / 2] : a[t]) + __shfl_xor_sync(0xffffffffu, send, d);
-        }
-      }
-      const int wl = wl0 + c + ((lane >> 3) & 3);
-      const int j = lane & 7;
-      if (wl < nw && s0 + j < S) scores[((long long)b * S + s0 + j) * nwin + c0 + wl] = a[0];
     }
+    if (x > 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) red[((x - 1) * 8 + j) * kD128CtaWindows + r] = acc[j];
+    }
+    __syncthreads();  // the partial sums of boxes 1..3 are in shared memory
+    if (x == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float t = acc[j];
+#pragma unroll
+        for (int xx = 0; xx < kD128Boxes - 1; ++xx) t += red[(xx * 8 + j) * kD128CtaWindows + r];
+        acc[j] = t;
+      }
+      if (w < nwin) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (s0 + j < S) scores[((long long)b * S + s0 + j) * nwin + w] = acc[j];
+      }
+    }
+    __syncthreads();  // the partial sums are read before the next group writes them
   }
 }
 
@@ -947,8 +969,8 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_cluster(
   cluster_wait();
 }
 
-// Per-device launch setup of the selection kernels (the opt-ins to more
-// than 48 KB of shared memory, and whether a cluster of eight 1024-thread
+// Per-device launch setup of the scoring and selection kernels (the opt-ins
+// to more than 48 KB of shared memory, and whether a cluster of eight 1024-thread
 // CTAs fits the device), made once per device; calls may come from several
 // threads.
 struct SelectSetup {
@@ -970,6 +992,9 @@ SelectSetup select_setup() {
     SelectSetup su;
     su.err = cudaFuncSetAttribute(select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kSelSmemWindows * (int)sizeof(float));
+    if (su.err == cudaSuccess)
+      su.err = cudaFuncSetAttribute(score_windows_d128, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    d128_smem_bytes(kMaxNewTokens));
     if (su.err == cudaSuccess &&
         cudaFuncSetAttribute(select_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSelClusterSlice * (int)sizeof(float)) == cudaSuccess) {
@@ -1148,6 +1173,18 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
   }
   cudaStream_t st = (cudaStream_t)stream;
   float* scores = (float*)workspace;
+  const SelectSetup setup = select_setup();
+  if (setup.err != cudaSuccess) {
+    set_error("CUDA error %d (%s)", (int)setup.err, cudaGetErrorString(setup.err));
+    return MLA_ERR_CUDA;
+  }
+  CUtensorMap tm_keys;
+  if (dim == 128 &&
+      !make_tmap_f32_3d(&tm_keys, pooled, 128, (uint64_t)pooled_windows_cap, (uint64_t)batch, 512,
+                        (uint64_t)pooled_windows_cap * 512, 32, kD128CtaWindows)) {
+    set_error("the pooled keys' tensor map could not be encoded");
+    return MLA_ERR_CUDA;
+  }
   {
     KernelTimer kt("indexer_score_windows", st);
     // chained to the preceding kernel (programmatic dependent launch)
@@ -1161,9 +1198,9 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
     if (dim == 128) {
       cfg.gridDim = dim3((unsigned)((nwin + kD128CtaWindows - 1) / kD128CtaWindows), batch);
       cfg.blockDim = dim3(kD128Threads);
-      cfg.dynamicSmemBytes = kD128CtaWindows * 512;
-      cudaLaunchKernelEx(&cfg, score_windows_d128, q, pooled, (long long)pooled_windows_cap,
-                         (int)new_tokens, (long long)nwin, scores);
+      cfg.dynamicSmemBytes = d128_smem_bytes(new_tokens);
+      cudaLaunchKernelEx(&cfg, score_windows_d128, tm_keys, q, (int)new_tokens, (long long)nwin,
+                         scores);
     } else {
       cfg.gridDim = dim3((unsigned)((nwin + kScoreWinPerCta - 1) / kScoreWinPerCta), batch);
       cfg.blockDim = dim3(kScoreThreads);
@@ -1178,11 +1215,6 @@ extern "C" mla_status_t mla_indexer_select(const float* q, const float* pooled,
     const size_t sel_smem = vis_max <= kSelSmemWindows ? (size_t)vis_max * sizeof(float) : 0;
     // a cluster of eight CTAs per row when its slices fit and the device
     // can hold such a cluster; otherwise one CTA per row
-    const SelectSetup setup = select_setup();
-    if (setup.err != cudaSuccess) {
-      set_error("CUDA error %d (%s)", (int)setup.err, cudaGetErrorString(setup.err));
-      return MLA_ERR_CUDA;
-    }
     const bool cluster_ok = setup.cluster_ok;
     const long long slice_max = ((vis_max + kSelCluster - 1) / kSelCluster + 3) & ~3LL;
     if (cluster_ok && slice_max <= kSelClusterSlice) {
