@@ -58,8 +58,11 @@ namespace {
 
 constexpr int kLat = 512;
 
+// The first 1024-byte boundary at or after the dynamic shared array, as an
+// offset from the array itself (no integer round trip), so that the compiler
+// still knows every pointer derived from it is a shared-memory one.
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+  return p + ((1024u - (sm103::smem_u32(p) & 1023u)) & 1023u);
 }
 
 __device__ __forceinline__ void report_timeout(int code) { atomicCAS(&g_absorbed_status, 0, code); }
