@@ -158,6 +158,116 @@ __global__ void __launch_bounds__(kRowsPerCta) concat_rows_kernel(ConcatParams p
   }
 }
 
+// The same layouts when every run starts on a 16-byte boundary (the bases,
+// the per-sequence strides, the plane stride and the windows' offsets and
+// strides multiples of four words): the S and T words of the CTA's channels
+// come in as 16-byte loads and are kept in shared memory as they lie (S
+// [channel][s], T [channel][n] or [plane][channel]), so staging is a plain
+// copy: a thread issues all of its (at most four, as s + n <= 16) 16-byte
+// loads before its first store.  Then X and every window are written as
+// 16-byte stores, each gathering its four words from shared memory (word c of
+// channel h's row is S's word c for c < s, else T's word c - s).  A run's
+// last words past a multiple of four go one at a time.
+constexpr int kStagePieces = kRowsPerCta * kMaxRow / 4 / kRowsPerCta;  // 16-byte loads a thread
+
+template <bool T_ROWS>
+struct StagedRow {
+  const uint32_t* sS;
+  const uint32_t* sT;
+  int s, n;
+  __device__ uint32_t operator()(int h, int c) const {
+    return c < s ? sS[h * s + c] : (T_ROWS ? sT[h * n + c - s] : sT[(c - s) * kRowsPerCta + h]);
+  }
+};
+
+// dst[e] = row(e / rw, col0 + e % rw) for e < len (a run of rows rw words wide)
+template <typename Row>
+__device__ __forceinline__ void write_run(uint32_t* __restrict__ dst, int len, int rw, int magic,
+                                          int col0, const Row& row) {
+  const int n4 = len >> 2;
+  for (int f = threadIdx.x; f < n4; f += kRowsPerCta) {
+    const int e = 4 * f;
+    int h = (e * magic) >> 16, i = e - h * rw;
+    uint32_t v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      v[u] = row(h, col0 + i);
+      if (++i == rw) {
+        i = 0;
+        ++h;
+      }
+    }
+    reinterpret_cast<uint4*>(dst)[f] = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+  for (int e = 4 * n4 + (int)threadIdx.x; e < len; e += kRowsPerCta) {
+    const int h = (e * magic) >> 16;
+    dst[e] = row(h, col0 + e - h * rw);
+  }
+}
+
+template <bool T_ROWS>
+__global__ void __launch_bounds__(kRowsPerCta) concat_rows_vec_kernel(ConcatParams p) {
+  __shared__ __align__(16) uint32_t sS[kRowsPerCta * (kMaxRow / 2)];
+  __shared__ __align__(16) uint32_t sT[kRowsPerCta * kMaxRow];
+  const int q = blockIdx.y;
+  const int h0 = blockIdx.x * kRowsPerCta;
+  const int R = min(kRowsPerCta, p.H - h0);
+  const int s = p.s, n = p.n, w = s + n;
+  const uint32_t* Sb = p.S + q * p.ss.q + (long long)h0 * s;
+  const uint32_t* Tb = p.T + q * p.ts.q + (T_ROWS ? (long long)h0 * n : (long long)h0);
+  // 16-byte pieces: S's run, then T's run (rows) or each plane's run (planes)
+  const int nS4 = (R * s) >> 2, r4 = R >> 2;
+  const int nT4 = T_ROWS ? (R * n) >> 2 : n * r4;
+  uint4 v[kStagePieces];
+#pragma unroll
+  for (int m = 0; m < kStagePieces; ++m) {
+    const int t = threadIdx.x + m * kRowsPerCta;
+    const int g = t - nS4;
+    if (t < nS4) {
+      v[m] = __ldg(reinterpret_cast<const uint4*>(Sb) + t);
+    } else if (g < nT4) {
+      if (T_ROWS) {
+        v[m] = __ldg(reinterpret_cast<const uint4*>(Tb) + g);
+      } else {
+        const int j = g / r4;
+        v[m] = __ldg(reinterpret_cast<const uint4*>(Tb + j * p.ts.i) + (g - j * r4));
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kStagePieces; ++m) {
+    const int t = threadIdx.x + m * kRowsPerCta;
+    const int g = t - nS4;
+    if (t < nS4) {
+      reinterpret_cast<uint4*>(sS)[t] = v[m];
+    } else if (g < nT4) {
+      if (T_ROWS) {
+        reinterpret_cast<uint4*>(sT)[g] = v[m];
+      } else {
+        const int j = g / r4;
+        reinterpret_cast<uint4*>(sT + j * kRowsPerCta)[g - j * r4] = v[m];
+      }
+    }
+  }
+  // the words past the last whole piece of each run
+  for (int e = 4 * nS4 + (int)threadIdx.x; e < R * s; e += kRowsPerCta) sS[e] = __ldg(Sb + e);
+  if (T_ROWS) {
+    for (int e = 4 * nT4 + (int)threadIdx.x; e < R * n; e += kRowsPerCta) sT[e] = __ldg(Tb + e);
+  } else if (R > 4 * r4) {
+    const int rt = R - 4 * r4;
+    for (int e = threadIdx.x; e < n * rt; e += kRowsPerCta) {
+      const int j = e / rt, h = 4 * r4 + e - j * rt;
+      sT[j * kRowsPerCta + h] = __ldg(Tb + j * p.ts.i + h);
+    }
+  }
+  __syncthreads();
+  const StagedRow<T_ROWS> row{sS, sT, s, n};
+  write_run(p.X + q * p.xs.q + (long long)h0 * w, R * w, w, p.magic_w, 0, row);
+  for (int j = 0; j < p.k; ++j)
+    write_run(p.cache + p.w[j].offset + q * p.w[j].stride + (long long)h0 * s, R * s, s,
+              p.magic_s, p.w[j].a, row);
+}
+
 // Ordinary path, one snapshot copy: reads the window back from X.  One thread
 // per cache word (channel e / s, element a + e % s of its row), so the writes
 // are contiguous.
@@ -322,8 +432,18 @@ extern "C" mla_status_t mla_concat_snapshots(
   const cudaStream_t st = (cudaStream_t)stream;
   const unsigned grid = (unsigned)(((long long)H * Q + 127) / 128);
   const dim3 grid_rows((unsigned)((H + kRowsPerCta - 1) / kRowsPerCta), (unsigned)Q);
+  // 16-byte runs: every base, per-sequence stride and window offset and
+  // stride (and the plane stride of T) a multiple of four words
+  auto a16 = [](const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; };
+  bool vec = staged && a16(S) && a16(T) && a16(X) && p.ss.q % 4 == 0 && p.ts.q % 4 == 0 &&
+             p.xs.q % 4 == 0 && (t_rows || p.ts.i % 4 == 0) && (k == 0 || a16(cache));
+  for (int j = 0; j < k; ++j) vec = vec && p.w[j].offset % 4 == 0 && p.w[j].stride % 4 == 0;
   auto concat = [&](const ConcatParams& c) {
-    if (staged)
+    if (vec && t_rows)
+      concat_rows_vec_kernel<true><<<grid_rows, kRowsPerCta, 0, st>>>(c);
+    else if (vec)
+      concat_rows_vec_kernel<false><<<grid_rows, kRowsPerCta, 0, st>>>(c);
+    else if (staged)
       concat_rows_kernel<<<grid_rows, kRowsPerCta, 0, st>>>(c, t_rows ? 1 : 0);
     else
       concat_snapshots_kernel<<<grid, 128, 0, st>>>(c);

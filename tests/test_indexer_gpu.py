@@ -178,6 +178,26 @@ def test_select_with_many_ties_is_exactly_the_oracles(T, S, k, dim):
     assert np.array_equal(pos[0].cpu().numpy(), opos)
 
 
+@pytest.mark.parametrize("T,S,dim", [(4099, 9, 128), (150, 17, 128), (4099, 9, 64)])
+def test_pool_rows_past_the_cache_are_never_read_into_the_choice(T, S, dim):
+    # a pool with room for more windows than the cache fills, the rest NaN:
+    # the scoring reads whole tiles of rows (those past the last window are
+    # scored and dropped), and the choice must equal the oracle's on the
+    # filled rows exactly (small-integer data, exact scores)
+    g = torch.Generator().manual_seed(T + S)
+    W = -(-T // 4)
+    filled = torch.randint(-3, 4, (2, W, dim), generator=g).float()
+    pooled = torch.full((2, W + 100, dim), float("nan"))
+    pooled[:, :W] = filled
+    q = torch.randint(-2, 3, (2, S, dim), generator=g).float()
+    wins, pos = B.mla_indexer_select(q.cuda(), pooled.cuda(), T, 300)
+    torch.cuda.synchronize()
+    for b in range(2):
+        ow, opos = P.select_topk(q[b].double().numpy(), filled[b].double().numpy(), T, S, 300)
+        assert np.array_equal(wins[b].cpu().numpy(), ow)
+        assert np.array_equal(pos[b].cpu().numpy(), opos)
+
+
 def test_selection_ties_go_to_the_lower_window():
     pooled = torch.ones((1, 10, 32), device="cuda")
     q = torch.ones((1, 1, 32), device="cuda")

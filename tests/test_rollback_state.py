@@ -185,6 +185,36 @@ def test_gpu_fused_group_is_bit_exact(s, n, k, layout):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("layout", ["row", "channels"])
+@pytest.mark.parametrize("H", [3, 257, 515])
+def test_gpu_padded_strides_and_ragged_runs_are_bit_exact(layout, H):
+    # sequence strides padded to multiples of four words, so every run starts
+    # on a 16-byte boundary and takes the 16-byte copies, while the channel
+    # count leaves the last CTA's runs a few words past a multiple of four
+    rng = np.random.default_rng(H + len(layout))
+    s, n, k, Q = 3, 5, 3, 3
+    pad = lambda x: (x + 7) // 4 * 4
+    ss = (1, s, pad(H * s))
+    ts = (1, n, pad(H * n)) if layout == "row" else (pad(H), 1, pad(H) * n + 4)
+    xs = (1, s + n, pad(H * (s + n)))
+    S = rng.integers(0, 2**32, size=ss[2] * Q, dtype=np.uint64).astype(np.uint32)
+    T = rng.integers(0, 2**32, size=ts[2] * Q, dtype=np.uint64).astype(np.uint32)
+    row = pad(H * s)
+    block = k * row
+    windows = [(int(rng.integers(0, n + 1)), j * row, block) for j in range(k)]
+    want_X, want_c = O.concat_separate(S, T, np.zeros(xs[2] * Q, np.uint32),
+                                       np.zeros(block * Q, np.uint32), s, n, H, Q, ss, ts, xs,
+                                       windows)
+    i32 = lambda a: torch.from_numpy(a.view(np.int32)).cuda()
+    dX = torch.zeros(xs[2] * Q, dtype=torch.int32, device="cuda")
+    dc = torch.zeros(block * Q, dtype=torch.int32, device="cuda")
+    assert B.mla_concat_snapshots(i32(S), ss, i32(T), ts, dX, xs, s, n, H, Q, dc, windows)
+    torch.cuda.synchronize()
+    assert np.array_equal(dX.cpu().numpy().view(np.uint32), want_X)
+    assert np.array_equal(dc.cpu().numpy().view(np.uint32), want_c)
+
+
+@pytest.mark.gpu
 def test_gpu_unsafe_group_takes_the_ordinary_path():
     rng = np.random.default_rng(3)
     s, n, H, Q = 3, 5, 64, 3
