@@ -263,9 +263,34 @@ __global__ void __launch_bounds__(kRowsPerCta) concat_rows_vec_kernel(ConcatPara
   __syncthreads();
   const StagedRow<T_ROWS> row{sS, sT, s, n};
   write_run(p.X + q * p.xs.q + (long long)h0 * w, R * w, w, p.magic_w, 0, row);
-  for (int j = 0; j < p.k; ++j)
-    write_run(p.cache + p.w[j].offset + q * p.w[j].stride + (long long)h0 * s, R * s, s,
-              p.magic_s, p.w[j].a, row);
+  // windows: all k share their runs' shape, so a thread walks the rows and
+  // columns of its four words once and reads them at every window's start
+  const int nW4 = (R * s) >> 2;
+  for (int f = threadIdx.x; f < nW4; f += kRowsPerCta) {
+    int hh[4], ii[4];
+    const int e = 4 * f;
+    int h = (e * p.magic_s) >> 16, i = e - h * s;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      hh[u] = h;
+      ii[u] = i;
+      if (++i == s) {
+        i = 0;
+        ++h;
+      }
+    }
+    for (int j = 0; j < p.k; ++j) {
+      const int a = p.w[j].a;
+      uint32_t* d = p.cache + p.w[j].offset + q * p.w[j].stride + (long long)h0 * s;
+      reinterpret_cast<uint4*>(d)[f] = make_uint4(row(hh[0], a + ii[0]), row(hh[1], a + ii[1]),
+                                                  row(hh[2], a + ii[2]), row(hh[3], a + ii[3]));
+    }
+  }
+  for (int e = 4 * nW4 + (int)threadIdx.x; e < R * s; e += kRowsPerCta) {
+    const int h = (e * p.magic_s) >> 16, i = e - h * s;
+    for (int j = 0; j < p.k; ++j)
+      p.cache[p.w[j].offset + q * p.w[j].stride + (long long)h0 * s + e] = row(h, p.w[j].a + i);
+  }
 }
 
 // Ordinary path, one snapshot copy: reads the window back from X.  One thread
