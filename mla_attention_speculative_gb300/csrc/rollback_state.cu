@@ -180,31 +180,6 @@ struct StagedRow {
   }
 };
 
-// dst[e] = row(e / rw, col0 + e % rw) for e < len (a run of rows rw words wide)
-template <typename Row>
-__device__ __forceinline__ void write_run(uint32_t* __restrict__ dst, int len, int rw, int magic,
-                                          int col0, const Row& row) {
-  const int n4 = len >> 2;
-  for (int f = threadIdx.x; f < n4; f += kRowsPerCta) {
-    const int e = 4 * f;
-    int h = (e * magic) >> 16, i = e - h * rw;
-    uint32_t v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      v[u] = row(h, col0 + i);
-      if (++i == rw) {
-        i = 0;
-        ++h;
-      }
-    }
-    reinterpret_cast<uint4*>(dst)[f] = make_uint4(v[0], v[1], v[2], v[3]);
-  }
-  for (int e = 4 * n4 + (int)threadIdx.x; e < len; e += kRowsPerCta) {
-    const int h = (e * magic) >> 16;
-    dst[e] = row(h, col0 + e - h * rw);
-  }
-}
-
 template <bool T_ROWS>
 __global__ void __launch_bounds__(kRowsPerCta) concat_rows_vec_kernel(ConcatParams p) {
   __shared__ __align__(16) uint32_t sS[kRowsPerCta * (kMaxRow / 2)];
@@ -262,7 +237,29 @@ __global__ void __launch_bounds__(kRowsPerCta) concat_rows_vec_kernel(ConcatPara
   }
   __syncthreads();
   const StagedRow<T_ROWS> row{sS, sT, s, n};
-  write_run(p.X + q * p.xs.q + (long long)h0 * w, R * w, w, p.magic_w, 0, row);
+  // X: word e of the run is column e % w of row e / w
+  uint32_t* Xb = p.X + q * p.xs.q + (long long)h0 * w;
+  const int nX4 = (R * w) >> 2;
+  for (int f = threadIdx.x; f < nX4; f += kRowsPerCta) {
+    int hh[4], ii[4];
+    const int e = 4 * f;
+    int h = (e * p.magic_w) >> 16, i = e - h * w;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      hh[u] = h;
+      ii[u] = i;
+      if (++i == w) {
+        i = 0;
+        ++h;
+      }
+    }
+    reinterpret_cast<uint4*>(Xb)[f] =
+        make_uint4(row(hh[0], ii[0]), row(hh[1], ii[1]), row(hh[2], ii[2]), row(hh[3], ii[3]));
+  }
+  for (int e = 4 * nX4 + (int)threadIdx.x; e < R * w; e += kRowsPerCta) {
+    const int h = (e * p.magic_w) >> 16;
+    Xb[e] = row(h, e - h * w);
+  }
   // windows: all k share their runs' shape, so a thread walks the rows and
   // columns of its four words once and reads them at every window's start
   const int nW4 = (R * s) >> 2;
