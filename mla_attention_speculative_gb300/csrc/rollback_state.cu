@@ -193,6 +193,9 @@ __global__ void __launch_bounds__(kRowsPerCta) concat_rows_vec_kernel(ConcatPara
   // 16-byte pieces: S's run, then T's run (rows) or each plane's run (planes)
   const int nS4 = (R * s) >> 2, r4 = R >> 2;
   const int nT4 = T_ROWS ? (R * n) >> 2 : n * r4;
+  // plane of T piece g: g / r4 as (g * m4) >> 16, exact since g < 15 r4 and
+  // r4 <= 64 (the error g (m4 - 2^16 / r4) / 2^16 < g / 2^16 < 1 / r4)
+  const int m4 = r4 > 0 ? (65536 + r4 - 1) / r4 : 0;
   uint4 v[kStagePieces];
 #pragma unroll
   for (int m = 0; m < kStagePieces; ++m) {
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kRowsPerCta) concat_rows_vec_kernel(ConcatPara
       if (T_ROWS) {
         v[m] = __ldg(reinterpret_cast<const uint4*>(Tb) + g);
       } else {
-        const int j = g / r4;
+        const int j = (g * m4) >> 16;
         v[m] = __ldg(reinterpret_cast<const uint4*>(Tb + j * p.ts.i) + (g - j * r4));
       }
     }
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kRowsPerCta) concat_rows_vec_kernel(ConcatPara
       if (T_ROWS) {
         reinterpret_cast<uint4*>(sT)[g] = v[m];
       } else {
-        const int j = g / r4;
+        const int j = (g * m4) >> 16;
         reinterpret_cast<uint4*>(sT + j * kRowsPerCta)[g - j * r4] = v[m];
       }
     }
