@@ -25,11 +25,14 @@
 //                       (score_windows: eight lanes per window, for dims
 //                       other than 128)
 //   select_topk_cluster a row (one new token) spread over a cluster of eight
-//                       CTAs: a radix select (12, 10, 10-bit digits) of the
-//                       k-th largest score over the windows the token may see,
-//                       then the chosen windows in ascending order and their
-//                       positions (select_topk: one CTA per row, for rows too
-//                       long for the cluster's shared memory)
+//                       CTAs: a radix select (a 10-bit digit summed over the
+//                       cluster, then the chosen bucket's keys gathered into
+//                       every CTA for two 11-bit digits) of the k-th largest
+//                       score over the windows the token may see, then the
+//                       chosen windows in ascending order and their positions
+//                       (select_topk: one CTA per row and 12, 10, 10-bit
+//                       digits, for rows too long for the cluster's shared
+//                       memory)
 
 #include <cuda_bf16.h>
 
